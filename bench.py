@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the fused low-rank-adapted linear layer on GB300.
+
+Headline step: one forward + backward of the bf16 LoRA linear layer at the LLM attention
+projection size (M = 8192 tokens = batch 4 x seq 2048, d_in = d_out = 4096, rank 16, alpha 32),
+through the C ABI, inputs resident in HBM.  value = algorithmic TFLOP/s of the whole job.
+
+Also measured in the same run (the "workloads" object): the DoRA-rows layer
+(8192 x 4096 -> 11008, r 32), the LoRA SwiGLU MLP (16384 tokens, 4096 -> 14336 -> 4096, r 16)
+and the W8A8 + LoRA forward (16384 x 3072 x 3072, r 32), each with its own roofline line.
+
+One JSON line on stdout (rank 0).  Multi-GPU (torchrun): independent replicas, weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused LoRA/DoRA linear fwd+bwd TFLOP/s and % bf16 tensor peak (1 GB300)"
+HEADLINE = "lora_4096_bf16"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------- flop counts
+def lora_flops(M, d_in, d_out, r):
+    """Algorithmic flops of one forward + backward (no dW0; W0 frozen)."""
+    fwd = 2 * M * d_in * d_out + 2 * M * r * (d_in + d_out)
+    bwd = 2 * M * d_in * d_out + 4 * M * r * (d_in + d_out)
+    return fwd, bwd
+
+
+def dora_flops(M, d_in, d_out, r):
+    fwd, bwd = lora_flops(M, d_in, d_out, r)
+    return fwd + 2 * d_out * d_in * r, bwd + 2 * d_out * d_in * r   # W0 A^T prepass, W0^T (g o B) norm term
+
+
+def mlp_flops(M, H, I, r):
+    proj = 2 * M * H * I
+    fwd = 3 * proj + 3 * 2 * M * r * (H + I)
+    bwd = 3 * proj + 3 * 4 * M * r * (H + I)
+    return fwd, bwd
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if len(win) < 3:
+            win = [s for _, s in self.samples]
+            window = "whole run (timed region shorter than the sampling period)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in win if num(s[0]) is not None]
+        mx = [num(s[1]) for s in win if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i in range(4) if len(s) > 4 + i and s[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win), "window": window,
+                "power_w_max": max((num(s[2]) or 0.0) for s in win)}
+
+
+# ----------------------------------------------------------------------------- peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_lora_sample(M_s, seed=7):
+    """One fwd+bwd of the fp64 oracle on an M_s-row sample of the headline workload."""
+    import numpy as np
+
+    import datagen as D
+    import oracle as O
+    case = D.scaled(D.WORKLOADS[HEADLINE], M=M_s)
+    t = D.make_linear(case)
+    f = {k: (None if v is None else v.double().numpy()) for k, v in t.items()}
+    t0 = time.perf_counter()
+    O.lora_linear_fwd(f["X"], f["W0"], f["A"], f["B"], case.s)
+    O.lora_linear_bwd(f["X"], f["W0"], f["A"], f["B"], case.s, f["dY"])
+    dt = time.perf_counter() - t0
+    fwd, bwd = lora_flops(M_s, case.d_in, case.d_out, case.r)
+    np.asarray(0)
+    return dt, fwd + bwd
+
+
+def cpu_baseline(budget_s=12.0):
+    M_s, dt, fl = 64, 0.0, 0
+    while True:
+        dt, fl = oracle_lora_sample(M_s)
+        if dt * 2 > budget_s or M_s >= 8192:
+            break
+        M_s *= 2
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{M_s} of the 8192 token rows of the {HEADLINE} workload, forward + backward, fp64 "
+                      f"materialised W' = W0 + sBA, {dt:.2f} s"}
+
+
+def run_reference(args, rank):
+    """Reference arm: the fp64 CPU oracle as it stands, timed on the host cores."""
+    if rank != 0:
+        return
+    # calibrate a per-step sample so that (warmup + steps) samples take about two minutes
+    dt1, _ = oracle_lora_sample(64)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    M_s = 64
+    while M_s < 8192 and dt1 * (M_s * 2 / 64) <= per_step:
+        M_s *= 2
+    for _ in range(args.warmup):
+        oracle_lora_sample(M_s)
+    tot_t, tot_f = 0.0, 0
+    for _ in range(args.steps):
+        dt, fl = oracle_lora_sample(M_s)
+        tot_t += dt
+        tot_f += fl
+    v = tot_f / tot_t / 1e12
+    sample = f"each step {M_s} of the 8192 token rows of {HEADLINE}, forward + backward, fp64 oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{HEADLINE}: M=8192 d_in=4096 d_out=4096 r=16 alpha=32, fwd+bwd (row sample)"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ----------------------------------------------------------------------------- multi-rank
+def reduce_max(vals, dist, device):
+    """Max over ranks of each timing (the slowest replica sets the job's time)."""
+    if dist is None:
+        return list(vals)
+    import torch
+    t = torch.tensor(list(vals), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(flops_per_rank_step, world, ms_max):
+    """Whole-job TFLOP/s: the work of all replicas over the slowest replica's step time."""
+    return flops_per_rank_step * world / (ms_max * 1e-3) / 1e12
+
+
+# ----------------------------------------------------------------------------- GPU workloads
+def timed(fn, steps, warmup, dist=None):
+    import torch
+    for _ in range(warmup):
+        fn()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    t0 = time.time()
+    for _ in range(steps):
+        fn()
+    e1.record(st)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1) / steps, t0, t1
+
+
+def gemm_roofline(L, peaks, ms_step, sustained):
+    """Roofline of the dominant kernel (tcgen05 GEMM) from the library's own event timing."""
+    ms, n, fl = L.lora_prof_gemm(reset=True)
+    if n == 0 or ms <= 0:
+        return None
+    ach = fl / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    return {"kernel": "tc_gemm_kernel (tcgen05 GEMM with fused rank-r tail)", "bound": "tensor",
+            "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+            "peak_kind": ("sustained" if sustained else "burst") + " bf16, " + peaks["source"],
+            "launches": n, "avg_launch_ms": round(ms / n, 4), "share_of_step": round(ms / n * (n and 1) / 1, 4),
+            "traffic": None}
+
+
+def headline(args, L, ops, dist, world, peaks):
+    import torch
+
+    import datagen as D
+    case = D.WORKLOADS[HEADLINE]
+    t = D.make_linear(case)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    X, W0, A, B, dY = (t[k].to(dev) for k in ("X", "W0", "A", "B", "dY"))
+    M, d_in, d_out, r, s = case.M, case.d_in, case.d_out, case.r, case.s
+    sh = L.shape(M, d_in, d_out, r, L.LORA_BF16)
+    Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=dev)
+    Z = torch.empty(M, r, dtype=torch.bfloat16, device=dev)
+    dX = torch.empty_like(X)
+    dA = torch.empty_like(A)
+    dB = torch.empty_like(B)
+    wsf = torch.zeros(L.lora_workspace_bytes(L.OP_LINEAR_FWD, sh), dtype=torch.uint8, device=dev)
+    wsb = torch.zeros(L.lora_workspace_bytes(L.OP_LINEAR_BWD, sh), dtype=torch.uint8, device=dev)
+
+    def step():
+        L.lora_linear_fwd(sh, X, W0, A, B, None, s, Y, Z, wsf)
+        L.lora_linear_bwd(sh, X, W0, A, B, Z, dY, s, dX, dA, dB, None, wsb)
+
+    fwd_fl, bwd_fl = lora_flops(M, d_in, d_out, r)
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    time.sleep(0.3)
+    L.lora_prof_gemm(reset=True)
+    n0 = L.lora_launch_count()
+    L.lora_prof_enable(True)
+    ms, t0, t1 = timed(step, args.steps, args.warmup, dist)
+    L.lora_prof_enable(False)
+    launches = L.lora_launch_count() - n0
+    # launches of the warm-up steps are in the count too: scale to the timed steps
+    gpu_launches = launches * args.steps // (args.steps + args.warmup)
+    roof = gemm_roofline(L, peaks, ms, sustained=False)
+    if roof is not None:
+        roof["share_of_step"] = round(roof["avg_launch_ms"] * 2 / ms, 3)
+    clocks = clk.summary(t0, t1)
+    clk.stop()
+    for ws in (wsf, wsb):
+        if L.lora_check_device_error(ws) != 0:
+            raise RuntimeError("a kernel recorded a timed-out wait during the benchmark")
+
+    # end to end: host (pinned) inputs copied in and adapter gradients read back every step
+    Xh = t["X"].pin_memory()
+    dYh = t["dY"].pin_memory()
+    dAh = torch.empty_like(dA, device="cpu").pin_memory()
+    dBh = torch.empty_like(dB, device="cpu").pin_memory()
+
+    def e2e_step():
+        X.copy_(Xh, non_blocking=True)
+        dY.copy_(dYh, non_blocking=True)
+        step()
+        dAh.copy_(dA, non_blocking=True)
+        dBh.copy_(dB, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    ms_e2e, _, _ = timed(e2e_step, e2e_steps, 2, dist)
+    ms_all, ms_e2e = reduce_max([ms, ms_e2e], dist, dev)
+    return {
+        "value": job_throughput(fwd_fl + bwd_fl, world, ms_all), "ms_per_step": ms_all, "clocks": clocks,
+        "roofline": roof, "gpu_launches": gpu_launches,
+        "e2e": {"value": job_throughput(fwd_fl + bwd_fl, world, ms_e2e), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": X.numel() * 2 + dY.numel() * 2,
+                "d2h_bytes_per_step": dA.numel() * 2 + dB.numel() * 2, "ms_per_step": ms_e2e},
+        "tokens_per_s": M * world / (ms_all * 1e-3),
+        "frac_of_bf16_peak_step": (fwd_fl + bwd_fl) / (ms_all * 1e-3) / 1e12 / peaks["bf16_tflops"],
+    }
+
+
+def extra_workloads(args, L, ops, peaks):
+    """DoRA, SwiGLU MLP and W8A8 workloads, each a fwd+bwd (fwd only for W8A8) step."""
+    import torch
+
+    import datagen as D
+    import oracle as O
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = {}
+    steps, warm = max(3, min(args.steps, 20)), 3
+
+    # DoRA rows
+    case = D.WORKLOADS["dora_4096x11008_bf16"]
+    t = D.make_linear(case)
+    g = {k: v.to(dev) for k, v in t.items() if v is not None}
+    r0 = ops.dora_rownorm2(g["W0"])
+
+    def dora_step():
+        Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps, g["bias"])
+        ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V, g["dY"], case.s,
+                            case.eps)
+    L.lora_prof_gemm(reset=True)
+    L.lora_prof_enable(True)
+    ms, _, _ = timed(dora_step, steps, warm)
+    L.lora_prof_enable(False)
+    f, b = dora_flops(case.M, case.d_in, case.d_out, case.r)
+    out["dora_4096x11008_bf16"] = {"ms_per_step": ms, "tflops": (f + b) / (ms * 1e-3) / 1e12,
+                                   "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                   "roofline": gemm_roofline(L, peaks, ms, False)}
+    del g, t
+
+    # SwiGLU MLP
+    case = D.WORKLOADS["mlp_swiglu_4096x14336_bf16"]
+    t = D.make_mlp(case)
+    g = {k: v.to(dev) for k, v in t.items()}
+    P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
+
+    def mlp_step():
+        Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
+        ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
+    L.lora_prof_gemm(reset=True)
+    L.lora_prof_enable(True)
+    ms, _, _ = timed(mlp_step, max(3, steps // 2), 2)
+    L.lora_prof_enable(False)
+    f, b = mlp_flops(case.M, case.H, case.I, case.r)
+    out["mlp_swiglu_4096x14336_bf16"] = {"ms_per_step": ms, "tflops": (f + b) / (ms * 1e-3) / 1e12,
+                                         "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                         "roofline": gemm_roofline(L, peaks, ms, True)}
+    del g, t, P
+    torch.cuda.empty_cache()
+
+    # W8A8 + LoRA forward (quantise X, int8 GEMM with LoRA epilogue)
+    case = D.WORKLOADS["w8a8_lora_3072"]
+    t = D.make_w8a8(case)
+    Wq, sw = O.quantize_rows(t["W0"].numpy())
+    X = t["X"].to(dev)
+    A = t["A"].to(dev)
+    B = t["B"].to(dev)
+    Wq = torch.from_numpy(Wq).to(dev)
+    sw = torch.from_numpy(sw).to(dev)
+
+    def w8_step():
+        Xq, sx, Z = ops.w8a8_quantize_rows(X, A)
+        ops.w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, case.s)
+    ms, _, _ = timed(w8_step, steps, warm)
+    ops_int8 = 2 * case.M * case.d_in * case.d_out
+    lora_fl = 2 * case.M * case.r * (case.d_in + case.d_out)
+    out["w8a8_lora_3072"] = {"ms_per_step": ms, "int8_tops": ops_int8 / (ms * 1e-3) / 1e12,
+                             "lora_tflops": lora_fl / (ms * 1e-3) / 1e12,
+                             "note": "int8 product on the warp-level integer MMA (sm_103a has no tcgen05 int8 kind)"}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workloads", default="all", choices=["all", "headline"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+
+    from dora_adapter_linear_gb300.build import build
+    if rank == 0:
+        build()
+    if dist is not None:
+        dist.barrier()
+    from dora_adapter_linear_gb300 import _lib as L
+    from dora_adapter_linear_gb300 import ops
+
+    peaks = measured_peaks()
+    h = headline(args, L, ops, dist, world, peaks)
+    extra = extra_workloads(args, L, ops, peaks) if args.workloads == "all" and rank == 0 else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(h["value"], 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(h["ms_per_step"], 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded Gaussian inputs of the workload's shapes; random-init weights)",
+            "config": {"workload": f"{HEADLINE}: LoRA linear fwd+bwd, M=8192 (batch 4 x seq 2048), "
+                                   "d_in=d_out=4096, rank 16, alpha 32, no bias",
+                       "global_batch": 4 * world, "seq_len": 2048, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: X, dY 64 MiB each + W0 32 MiB + outputs per step (no flush)",
+                       "flops_per_step": sum(lora_flops(8192, 4096, 4096, 16))},
+            "tokens_per_s": round(h["tokens_per_s"]), "frac_of_bf16_peak": round(h["frac_of_bf16_peak_step"], 4),
+            "peaks": peaks, "roofline": h["roofline"], "cpu_baseline": cpu, "e2e": h["e2e"],
+            "gpu_launches": h["gpu_launches"], "clocks": h["clocks"], "workloads": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

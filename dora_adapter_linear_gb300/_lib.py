@@ -1,0 +1,228 @@
+"""ctypes binding of liblora_gb300.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls, takes torch tensors (or
+None) in the same order, passes their device pointers and the current CUDA stream, and
+raises LoraError on a non-OK status.  No arithmetic of the layer happens in Python.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int, c_int8, c_int32, c_int64, c_size_t, c_uint32, c_void_p
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblora_gb300.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "lora_gb300.h")
+
+LORA_F32, LORA_BF16 = 0, 1
+OP_LINEAR_FWD, OP_LINEAR_BWD, OP_DORA_FWD, OP_DORA_BWD, OP_MLP_FWD, OP_MLP_BWD = range(6)
+STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_UNSUPPORTED", 3: "LORA_ERR_MISALIGNED",
+          4: "LORA_ERR_WORKSPACE", 5: "LORA_ERR_CUDA", 6: "LORA_ERR_DEVICE_TIMEOUT"}
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({_lib().lora_status_string(status).decode()})")
+
+
+class LoraShape(ctypes.Structure):
+    _fields_ = [("M", c_int64), ("d_in", c_int64), ("d_out", c_int64), ("r", c_int64), ("dtype", c_int32)]
+
+
+class LoraMlpShape(ctypes.Structure):
+    _fields_ = [("M", c_int64), ("H", c_int64), ("I", c_int64), ("r", c_int64), ("dtype", c_int32)]
+
+
+class LoraProj(ctypes.Structure):
+    _fields_ = [("W", c_void_p), ("A", c_void_p), ("B", c_void_p), ("s", c_float)]
+
+
+P = c_void_p
+_SIGS = {
+    "lora_status_string": (c_char_p, [c_int]),
+    "lora_abi_version": (c_int, []),
+    "lora_workspace_bytes": (c_size_t, [c_int, POINTER(LoraShape)]),
+    "lora_mlp_workspace_bytes": (c_size_t, [c_int, POINTER(LoraMlpShape)]),
+    "lora_clear_device_error": (c_int, [P, P]),
+    "lora_check_device_error": (c_int, [P, P]),
+    "lora_linear_fwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, c_float, P, P, P, c_size_t, P]),
+    "lora_linear_bwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, P, c_float, P, P, P, P, P, c_size_t, P]),
+    "dora_rownorm2": (c_int, [POINTER(LoraShape), P, P, P]),
+    "dora_linear_fwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, P, P, c_float, c_float, P, P, P, P, P,
+                                c_size_t, P]),
+    "dora_linear_bwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, P, P, P, P, P, P, c_float, c_float,
+                                P, P, P, P, P, P, c_size_t, P]),
+    "lora_mlp_swiglu_fwd": (c_int, [POINTER(LoraMlpShape), P, POINTER(LoraProj), POINTER(LoraProj),
+                                    POINTER(LoraProj), P, P, P, P, P, P, P, c_size_t, P]),
+    "lora_mlp_swiglu_bwd": (c_int, [POINTER(LoraMlpShape), P, POINTER(LoraProj), POINTER(LoraProj),
+                                    POINTER(LoraProj), P, P, P, P, P, P, P, P, P, P, P, P, P, P, c_size_t, P]),
+    "w8a8_quantize_rows": (c_int, [c_int64, c_int64, P, P, P, P, c_int64, P, P]),
+    "w8a8_lora_fwd": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, c_float, P, P, P, P]),
+    "lora_debug_wait_timeout": (c_int, [P, c_uint32, P]),
+    "lora_launch_count": (ctypes.c_uint64, []),
+    "lora_prof_enable": (c_int, [c_int]),
+    "lora_prof_gemm": (c_int, [POINTER(ctypes.c_double), POINTER(c_int64), POINTER(ctypes.c_double), c_int]),
+}
+
+_LIB = None
+
+
+def _lib():
+    """Load the library (fails loudly if it has not been built: there is no fallback)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing; build it with dora_adapter_linear_gb300.build.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def ptr(t):
+    """Device pointer of a tensor (None -> NULL)."""
+    if t is None:
+        return None
+    return c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is not None:
+        return c_void_p(stream if isinstance(stream, int) else stream.cuda_stream)
+    import torch
+    return c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ck(status, where):
+    if status != 0:
+        raise LoraError(status, where)
+
+
+def dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return LORA_BF16
+    if t.dtype == torch.float32:
+        return LORA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def shape(M, d_in, d_out, r, dtype) -> LoraShape:
+    return LoraShape(M, d_in, d_out, r, dtype)
+
+
+def mlp_shape(M, H, I, r, dtype=LORA_BF16) -> LoraMlpShape:
+    return LoraMlpShape(M, H, I, r, dtype)
+
+
+def proj(W, A, B, s) -> LoraProj:
+    return LoraProj(W.data_ptr(), A.data_ptr(), B.data_ptr(), float(s))
+
+
+# ------------------------------------------------------------------ entry points
+def lora_status_string(status: int) -> str:
+    return _lib().lora_status_string(status).decode()
+
+
+def lora_abi_version() -> int:
+    return _lib().lora_abi_version()
+
+
+def lora_workspace_bytes(op: int, sh: LoraShape) -> int:
+    return _lib().lora_workspace_bytes(op, ctypes.byref(sh))
+
+
+def lora_mlp_workspace_bytes(op: int, sh: LoraMlpShape) -> int:
+    return _lib().lora_mlp_workspace_bytes(op, ctypes.byref(sh))
+
+
+def lora_clear_device_error(ws, stream=None):
+    _ck(_lib().lora_clear_device_error(ptr(ws), _stream(stream)), "lora_clear_device_error")
+
+
+def lora_check_device_error(ws, stream=None) -> int:
+    """Returns the status (0 = clear, 6 = a bounded wait ran out); synchronises the stream."""
+    return _lib().lora_check_device_error(ptr(ws), _stream(stream))
+
+
+def lora_debug_wait_timeout(ws, timeout_us: int, stream=None):
+    _ck(_lib().lora_debug_wait_timeout(ptr(ws), timeout_us, _stream(stream)), "lora_debug_wait_timeout")
+
+
+def lora_launch_count() -> int:
+    return int(_lib().lora_launch_count())
+
+
+def lora_prof_enable(on: bool):
+    _ck(_lib().lora_prof_enable(1 if on else 0), "lora_prof_enable")
+
+
+def lora_prof_gemm(reset: bool = True):
+    """(device ms, launches, algorithmic flops) of the GEMM launches recorded since the last reset."""
+    ms, n, fl = ctypes.c_double(), c_int64(), ctypes.c_double()
+    _ck(_lib().lora_prof_gemm(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl), 1 if reset else 0),
+        "lora_prof_gemm")
+    return ms.value, n.value, fl.value
+
+
+def lora_linear_fwd(sh, X, W0, A, B, bias, s, Y, Z_save, ws, stream=None):
+    _ck(_lib().lora_linear_fwd(ctypes.byref(sh), ptr(X), ptr(W0), ptr(A), ptr(B), ptr(bias), float(s), ptr(Y),
+                               ptr(Z_save), ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                               _stream(stream)), "lora_linear_fwd")
+
+
+def lora_linear_bwd(sh, X, W0, A, B, Z_saved, dY, s, dX, dA, dB, dbias, ws, stream=None):
+    _ck(_lib().lora_linear_bwd(ctypes.byref(sh), ptr(X), ptr(W0), ptr(A), ptr(B), ptr(Z_saved), ptr(dY), float(s),
+                               ptr(dX), ptr(dA), ptr(dB), ptr(dbias), ptr(ws),
+                               0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+        "lora_linear_bwd")
+
+
+def dora_rownorm2(sh, W0, r0, stream=None):
+    _ck(_lib().dora_rownorm2(ctypes.byref(sh), ptr(W0), ptr(r0), _stream(stream)), "dora_rownorm2")
+
+
+def dora_linear_fwd(sh, X, W0, A, B, m, bias, r0, s, eps, Y, Z_save, n_save, V_save, ws, stream=None):
+    _ck(_lib().dora_linear_fwd(ctypes.byref(sh), ptr(X), ptr(W0), ptr(A), ptr(B), ptr(m), ptr(bias), ptr(r0),
+                               float(s), float(eps), ptr(Y), ptr(Z_save), ptr(n_save), ptr(V_save), ptr(ws),
+                               0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+        "dora_linear_fwd")
+
+
+def dora_linear_bwd(sh, X, W0, A, B, m, bias, Y, Z_saved, n_saved, V_saved, dY, s, eps, dX, dA, dB, dm, dbias, ws,
+                    stream=None):
+    _ck(_lib().dora_linear_bwd(ctypes.byref(sh), ptr(X), ptr(W0), ptr(A), ptr(B), ptr(m), ptr(bias), ptr(Y),
+                               ptr(Z_saved), ptr(n_saved), ptr(V_saved), ptr(dY), float(s), float(eps), ptr(dX),
+                               ptr(dA), ptr(dB), ptr(dm), ptr(dbias), ptr(ws),
+                               0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+        "dora_linear_bwd")
+
+
+def lora_mlp_swiglu_fwd(sh, X, gate, up, down, Y, e_save, u_save, h_save, Zgu_save, Zd_save, ws, stream=None):
+    _ck(_lib().lora_mlp_swiglu_fwd(ctypes.byref(sh), ptr(X), ctypes.byref(gate), ctypes.byref(up),
+                                   ctypes.byref(down), ptr(Y), ptr(e_save), ptr(u_save), ptr(h_save), ptr(Zgu_save),
+                                   ptr(Zd_save), ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                   _stream(stream)), "lora_mlp_swiglu_fwd")
+
+
+def lora_mlp_swiglu_bwd(sh, X, gate, up, down, e_saved, u_saved, h_saved, Zgu_saved, Zd_saved, dY, dX, dAg, dBg,
+                        dAu, dBu, dAd, dBd, ws, stream=None):
+    _ck(_lib().lora_mlp_swiglu_bwd(ctypes.byref(sh), ptr(X), ctypes.byref(gate), ctypes.byref(up),
+                                   ctypes.byref(down), ptr(e_saved), ptr(u_saved), ptr(h_saved), ptr(Zgu_saved),
+                                   ptr(Zd_saved), ptr(dY), ptr(dX), ptr(dAg), ptr(dBg), ptr(dAu), ptr(dBu), ptr(dAd),
+                                   ptr(dBd), ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                   _stream(stream)), "lora_mlp_swiglu_bwd")
+
+
+def w8a8_quantize_rows(rows, cols, X, Xq, sx, A=None, r=0, Z=None, stream=None):
+    _ck(_lib().w8a8_quantize_rows(rows, cols, ptr(X), ptr(Xq), ptr(sx), ptr(A), r, ptr(Z), _stream(stream)),
+        "w8a8_quantize_rows")
+
+
+def w8a8_lora_fwd(M, d_in, d_out, r, Xq, sx, Wq, sw, Z, B, s, bias, Y, acc_out=None, stream=None):
+    _ck(_lib().w8a8_lora_fwd(M, d_in, d_out, r, ptr(Xq), ptr(sx), ptr(Wq), ptr(sw), ptr(Z), ptr(B), float(s),
+                             ptr(bias), ptr(Y), ptr(acc_out), _stream(stream)), "w8a8_lora_fwd")

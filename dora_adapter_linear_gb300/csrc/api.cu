@@ -1,0 +1,965 @@
+// C-ABI entry points: argument validation, workspace carving and the launch sequence of each
+// operation.  Nothing here computes; every step runs in the kernels of this library.
+#include <math.h>
+#include <stdlib.h>
+
+#include "../../include/lora_gb300.h"
+#include "internal.h"
+
+using namespace lg;
+
+namespace {
+
+constexpr size_t kErrBytes = 256;
+inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Dry-run-able bump allocator over the caller's workspace: with base == nullptr it only sums sizes.
+struct Carve {
+  char* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t count) {
+    char* p = base ? base + off : nullptr;
+    off += al256(count * sizeof(T));
+    return reinterpret_cast<T*>(p);
+  }
+};
+
+uint64_t wait_timeout_ns() {
+  static uint64_t v = 0;
+  if (v == 0) {
+    const char* e = getenv("LORA_GB300_WAIT_TIMEOUT_MS");
+    double ms = e ? atof(e) : 2000.0;
+    if (!(ms > 0)) ms = 2000.0;
+    v = (uint64_t)(ms * 1e6);
+  }
+  return v;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+#define CK(x)                                  \
+  do {                                         \
+    if ((x) != cudaSuccess) return LORA_ERR_CUDA; \
+  } while (0)
+#define REQ(p)                                   \
+  do {                                           \
+    if ((p) == nullptr) return LORA_ERR_INVALID_ARG; \
+  } while (0)
+#define ALN(p)                                   \
+  do {                                           \
+    if ((p) != nullptr && !al16(p)) return LORA_ERR_MISALIGNED; \
+  } while (0)
+
+lora_status check_shape(const lora_shape* sh) {
+  if (!sh) return LORA_ERR_INVALID_ARG;
+  if (sh->M < 0 || sh->d_in <= 0 || sh->d_out <= 0 || sh->r <= 0) return LORA_ERR_INVALID_ARG;
+  if (sh->dtype != LORA_F32 && sh->dtype != LORA_BF16) return LORA_ERR_INVALID_ARG;
+  if (sh->d_in % 8 || sh->d_out % 8) return LORA_ERR_UNSUPPORTED;
+  if (sh->r > 64) return LORA_ERR_UNSUPPORTED;
+  if (sh->dtype == LORA_BF16 && sh->r % 8) return LORA_ERR_UNSUPPORTED;
+  if (sh->M > (1LL << 31) - 1 || sh->d_in > (1LL << 31) - 1 || sh->d_out > (1LL << 31) - 1)
+    return LORA_ERR_UNSUPPORTED;
+  return LORA_OK;
+}
+
+lora_status check_ws(void* ws, size_t have, size_t need) {
+  if (ws == nullptr || have < need) return LORA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255) return LORA_ERR_MISALIGNED;
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------------ workspace plans
+struct LinFwdWs {
+  uint32_t* err;
+  void* Zs;   // bf16: s*Z ; f32: Z when no Z_save
+};
+size_t plan_lin_fwd(const lora_shape& sh, char* base, LinFwdWs* w) {
+  Carve c{base};
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  const size_t es = sh.dtype == LORA_BF16 ? 2 : 4;
+  w->Zs = c.take<char>((size_t)sh.M * sh.r * es);
+  return c.off;
+}
+
+struct LinBwdWs {
+  uint32_t* err;
+  void* Gs;      // [M, r] bf16 s*G (f32: G)
+  void* Zrec;    // [M, r] recomputed Z
+  float* PB;     // [splitsB, out, r]
+  float* PA;     // [splitsA, in, r]
+  float* csum;   // [splitsB, out]
+  int splitsB, splitsA;
+};
+size_t plan_lin_bwd(const lora_shape& sh, char* base, LinBwdWs* w) {
+  Carve c{base};
+  const size_t es = sh.dtype == LORA_BF16 ? 2 : 4;
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  w->Gs = c.take<char>((size_t)sh.M * sh.r * es);
+  w->Zrec = c.take<char>((size_t)sh.M * sh.r * es);
+  if (sh.dtype == LORA_BF16) {
+    w->splitsB = colreduce_splits(sh.M, sh.d_out);
+    w->splitsA = colreduce_splits(sh.M, sh.d_in);
+    w->PB = c.take<float>((size_t)w->splitsB * sh.d_out * sh.r);
+    w->PA = c.take<float>((size_t)w->splitsA * sh.d_in * sh.r);
+    w->csum = c.take<float>((size_t)w->splitsB * sh.d_out);
+  } else {
+    w->splitsB = w->splitsA = 1;
+    w->PB = w->PA = nullptr;
+    w->csum = c.take<float>((size_t)sh.d_out);
+  }
+  return c.off;
+}
+
+struct DoraFwdWs {
+  uint32_t* err;
+  void* Zs;
+  float* Kr;   // [r, r]
+  float* c;    // [out]
+};
+size_t plan_dora_fwd(const lora_shape& sh, char* base, DoraFwdWs* w) {
+  Carve c{base};
+  const size_t es = sh.dtype == LORA_BF16 ? 2 : 4;
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  w->Zs = c.take<char>((size_t)sh.M * sh.r * es);
+  w->Kr = c.take<float>((size_t)sh.r * sh.r);
+  w->c = c.take<float>((size_t)sh.d_out);
+  return c.off;
+}
+
+struct DoraBwdWs {
+  uint32_t* err;
+  float *c, *g, *dot, *csum, *dotp, *csump, *Kr, *Kg;
+  void *Bc, *gB, *Gs, *Zrec;
+  float *PB, *PA, *PW;
+  int splitsB, splitsA, splitsW;
+};
+size_t plan_dora_bwd(const lora_shape& sh, char* base, DoraBwdWs* w) {
+  Carve c{base};
+  const size_t es = sh.dtype == LORA_BF16 ? 2 : 4;
+  const int64_t out = sh.d_out, in = sh.d_in, r = sh.r, M = sh.M;
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  w->c = c.take<float>(out);
+  w->g = c.take<float>(out);
+  w->dot = c.take<float>(out);
+  w->csum = c.take<float>(out);
+  w->Kr = c.take<float>(r * r);
+  w->Kg = c.take<float>(r * r);
+  w->Bc = c.take<char>(out * r * es);
+  w->gB = c.take<char>(out * r * es);
+  w->Gs = c.take<char>(M * r * es);
+  w->Zrec = c.take<char>(M * r * es);
+  if (sh.dtype == LORA_BF16) {
+    w->splitsB = colreduce_splits(M, out);
+    w->splitsA = colreduce_splits(M, in);
+    w->splitsW = colreduce_splits(out, in);
+    w->PB = c.take<float>(w->splitsB * out * r);
+    w->PA = c.take<float>(w->splitsA * in * r);
+    w->PW = c.take<float>(w->splitsW * in * r);
+    w->dotp = c.take<float>(w->splitsB * out);
+    w->csump = c.take<float>(w->splitsB * out);
+  } else {
+    w->splitsB = w->splitsA = w->splitsW = 1;
+    w->PB = w->PA = w->PW = nullptr;
+    w->dotp = w->csump = nullptr;
+  }
+  return c.off;
+}
+
+struct MlpFwdWs {
+  uint32_t* err;
+  bf16 *Agu, *Zgus, *Zds;
+};
+size_t plan_mlp_fwd(const lora_mlp_shape& sh, char* base, MlpFwdWs* w) {
+  Carve c{base};
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  w->Agu = c.take<bf16>(2 * sh.r * sh.H);
+  w->Zgus = c.take<bf16>(sh.M * 2 * sh.r);
+  w->Zds = c.take<bf16>(sh.M * sh.r);
+  return c.off;
+}
+
+inline int64_t mlp_ipad(const lora_mlp_shape& sh) { return (sh.I + 63) / 64 * 64; }
+
+struct MlpBwdWs {
+  uint32_t* err;
+  bf16 *dedu, *Gds, *Ggus, *Agu;
+  float *PBd, *PAd, *PBg, *PBu, *PAgu;
+  int sBd, sAd, sBg, sAgu;
+};
+size_t plan_mlp_bwd(const lora_mlp_shape& sh, char* base, MlpBwdWs* w) {
+  Carve c{base};
+  const int64_t M = sh.M, H = sh.H, I = sh.I, r = sh.r, Ip = mlp_ipad(sh);
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  w->dedu = c.take<bf16>(M * 2 * Ip);
+  w->Gds = c.take<bf16>(M * r);
+  w->Ggus = c.take<bf16>(M * 2 * r);
+  w->Agu = c.take<bf16>(2 * r * H);
+  w->sBd = colreduce_splits(M, H);
+  w->sAd = colreduce_splits(M, I);
+  w->sBg = w->sAd;
+  w->sAgu = colreduce_splits(M, H);
+  w->PBd = c.take<float>(w->sBd * H * r);
+  w->PAd = c.take<float>(w->sAd * I * r);
+  w->PBg = c.take<float>(w->sBg * I * r);
+  w->PBu = c.take<float>(w->sBg * I * r);
+  w->PAgu = c.take<float>(w->sAgu * H * 2 * r);
+  return c.off;
+}
+
+// ------------------------------------------------------------------ bf16 helpers
+TcGemmDesc fwd_desc(int64_t M, int64_t N, int64_t K, const void* X, const void* W, const void* Zs, const void* B,
+                    int r, void* Y, const bf16* bias, const float* cs, uint32_t* err) {
+  TcGemmDesc d;
+  d.mode = TC_FWD;
+  d.M = (int)M;
+  d.N = (int)N;
+  d.K0 = (int)K;
+  d.A0 = X;
+  d.lda0 = K;
+  d.B0 = W;
+  d.ldb0 = K;
+  d.has_tail = Zs != nullptr;
+  d.A1 = Zs;
+  d.lda1 = r;
+  d.K1 = r;
+  d.K1_a = r;
+  d.B1 = B;
+  d.ldb1 = r;
+  d.K1_b = r;
+  d.out[0] = Y;
+  d.ldo = N;
+  d.bias = bias;
+  d.col_scale = cs;
+  d.err = err;
+  d.timeout_ns = wait_timeout_ns();
+  return d;
+}
+
+TcGemmDesc dx_desc(int64_t M, int64_t N /*in*/, int64_t K /*out*/, const void* dY, const void* W0, const void* Gs,
+                   const void* A, int r, void* dX, const float* kscale, uint32_t* err) {
+  TcGemmDesc d;
+  d.mode = TC_BWD_DX;
+  d.M = (int)M;
+  d.N = (int)N;
+  d.K0 = (int)K;
+  d.A0 = dY;
+  d.lda0 = K;
+  d.B0 = W0;
+  d.ldb0 = N;
+  d.b0_mn = true;
+  d.b0_rows = (int)K;
+  d.has_tail = Gs != nullptr;
+  d.b1_mn = true;
+  d.A1 = Gs;
+  d.lda1 = r;
+  d.K1 = r;
+  d.K1_a = r;
+  d.B1 = A;
+  d.ldb1 = N;
+  d.out[0] = dX;
+  d.ldo = N;
+  d.a_kscale = kscale;
+  d.err = err;
+  d.timeout_ns = wait_timeout_ns();
+  return d;
+}
+
+RowProjDesc rp_desc(int64_t rows, int64_t K, int R, const void* S, const void* U, bool kr) {
+  RowProjDesc d;
+  d.rows = rows;
+  d.K = K;
+  d.R = R;
+  d.S = static_cast<const bf16*>(S);
+  d.lds = K;
+  d.U = static_cast<const bf16*>(U);
+  d.u_kr = kr;
+  d.ldu = kr ? R : K;
+  return d;
+}
+
+ColReduceDesc cr_desc(int64_t rows, int64_t K, int R, const void* S, const void* T, int64_t ldt, float* part,
+                      int splits) {
+  ColReduceDesc d;
+  d.rows = rows;
+  d.K = K;
+  d.R = R;
+  d.S = static_cast<const bf16*>(S);
+  d.lds = K;
+  d.T = static_cast<const bf16*>(T);
+  d.ldt = ldt;
+  d.part = part;
+  d.splits = splits;
+  return d;
+}
+
+SgemmDesc sg(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, bool ta, const void* B, int64_t ldb, bool tb,
+             void* C, int64_t ldc, float alpha = 1.f, float beta = 0.f) {
+  SgemmDesc d;
+  d.M = M;
+  d.N = N;
+  d.K = K;
+  d.A = static_cast<const float*>(A);
+  d.lda = lda;
+  d.ta = ta;
+  d.B = static_cast<const float*>(B);
+  d.ldb = ldb;
+  d.tb = tb;
+  d.C = static_cast<float*>(C);
+  d.ldc = ldc;
+  d.alpha = alpha;
+  d.beta = beta;
+  return d;
+}
+
+}  // namespace
+
+// ============================================================================ ABI
+extern "C" {
+
+const char* lora_status_string(int status) {
+  switch (status) {
+    case LORA_OK: return "ok";
+    case LORA_ERR_INVALID_ARG: return "invalid argument";
+    case LORA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case LORA_ERR_MISALIGNED: return "misaligned pointer";
+    case LORA_ERR_WORKSPACE: return "workspace missing or too small";
+    case LORA_ERR_CUDA: return "CUDA error";
+    case LORA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int lora_abi_version(void) { return 1; }
+
+size_t lora_workspace_bytes(int op, const lora_shape* sh) {
+  if (check_shape(sh) != LORA_OK) return 0;
+  switch (op) {
+    case LORA_OP_LINEAR_FWD: { LinFwdWs w; return plan_lin_fwd(*sh, nullptr, &w); }
+    case LORA_OP_LINEAR_BWD: { LinBwdWs w; return plan_lin_bwd(*sh, nullptr, &w); }
+    case LORA_OP_DORA_FWD: { DoraFwdWs w; return plan_dora_fwd(*sh, nullptr, &w); }
+    case LORA_OP_DORA_BWD: { DoraBwdWs w; return plan_dora_bwd(*sh, nullptr, &w); }
+  }
+  return 0;
+}
+
+static lora_status check_mlp_shape(const lora_mlp_shape* sh) {
+  if (!sh) return LORA_ERR_INVALID_ARG;
+  if (sh->M < 0 || sh->H <= 0 || sh->I <= 0 || sh->r <= 0) return LORA_ERR_INVALID_ARG;
+  if (sh->dtype != LORA_BF16) return sh->dtype == LORA_F32 ? LORA_ERR_UNSUPPORTED : LORA_ERR_INVALID_ARG;
+  if (sh->H % 8 || sh->I % 8 || sh->r % 8 || sh->r > 32) return LORA_ERR_UNSUPPORTED;
+  if (sh->M > (1LL << 31) - 1 || 2 * mlp_ipad(*sh) > (1LL << 31) - 1) return LORA_ERR_UNSUPPORTED;
+  return LORA_OK;
+}
+
+size_t lora_mlp_workspace_bytes(int op, const lora_mlp_shape* sh) {
+  if (check_mlp_shape(sh) != LORA_OK) return 0;
+  if (op == LORA_OP_MLP_FWD) { MlpFwdWs w; return plan_mlp_fwd(*sh, nullptr, &w); }
+  if (op == LORA_OP_MLP_BWD) { MlpBwdWs w; return plan_mlp_bwd(*sh, nullptr, &w); }
+  return 0;
+}
+
+lora_status lora_clear_device_error(void* ws, void* stream) {
+  REQ(ws);
+  if (reinterpret_cast<uintptr_t>(ws) & 255) return LORA_ERR_MISALIGNED;
+  CK(cudaMemsetAsync(ws, 0, kErrBytes, (cudaStream_t)stream));
+  return LORA_OK;
+}
+
+lora_status lora_check_device_error(const void* ws, void* stream) {
+  REQ(ws);
+  CK(cudaStreamSynchronize((cudaStream_t)stream));
+  uint32_t h[2] = {0, 0};
+  CK(cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost));
+  return (h[0] & 1u) ? LORA_ERR_DEVICE_TIMEOUT : LORA_OK;  // bit 0: a bounded wait ran out
+}
+
+uint64_t lora_launch_count(void) { return launch_count(); }
+
+lora_status lora_prof_enable(int on) {
+  prof_set(on != 0);
+  return LORA_OK;
+}
+
+lora_status lora_prof_gemm(double* ms, int64_t* launches, double* flops, int reset) {
+  CK(prof_collect(ms, launches, flops, reset != 0));
+  return LORA_OK;
+}
+
+lora_status lora_debug_wait_timeout(void* ws, uint32_t timeout_us, void* stream) {
+  REQ(ws);
+  if (reinterpret_cast<uintptr_t>(ws) & 255) return LORA_ERR_MISALIGNED;
+  CK(debug_wait_timeout(static_cast<uint32_t*>(ws), (uint64_t)timeout_us * 1000ull, (cudaStream_t)stream));
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------------ LoRA linear
+lora_status lora_linear_fwd(const lora_shape* sh, const void* X, const void* W0, const void* A, const void* B,
+                            const void* bias, float s, void* Y, void* Z_save, void* ws, size_t ws_bytes,
+                            void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  REQ(X); REQ(W0); REQ(A); REQ(B); REQ(Y);
+  ALN(X); ALN(W0); ALN(A); ALN(B); ALN(bias); ALN(Y); ALN(Z_save);
+  if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
+  LinFwdWs w;
+  const size_t need = plan_lin_fwd(*sh, nullptr, &w);
+  if ((e = check_ws(ws, ws_bytes, need)) != LORA_OK) return e;
+  plan_lin_fwd(*sh, static_cast<char*>(ws), &w);
+  if (sh->M == 0) return LORA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
+  const int r = (int)sh->r;
+  if (sh->dtype == LORA_BF16) {
+    if (s != 0.f || Z_save) {
+      RowProjDesc d = rp_desc(M, in, r, X, A, false);
+      d.out_a = static_cast<bf16*>(Z_save);
+      d.out_b = s != 0.f ? static_cast<bf16*>(w.Zs) : nullptr;
+      d.scale_b = s;
+      CK(rowproj(d, st));
+    }
+    // strength 0: the frozen base alone (no tail term at all)
+    CK(tc_gemm(fwd_desc(M, out, in, X, W0, s != 0.f ? w.Zs : nullptr, B, r, Y, static_cast<const bf16*>(bias),
+                        nullptr, w.err),
+               st));
+  } else {
+    void* Z = Z_save ? Z_save : w.Zs;
+    if (s != 0.f || Z_save) CK(sgemm_f32(sg(M, r, in, X, in, false, A, in, true, Z, r), st));
+    SgemmDesc d = sg(M, out, in, X, in, false, W0, in, true, Y, out);
+    d.bias = static_cast<const float*>(bias);
+    CK(sgemm_f32(d, st));
+    if (s != 0.f) CK(sgemm_f32(sg(M, out, r, Z, r, false, B, r, true, Y, out, s, 1.f), st));
+  }
+  return LORA_OK;
+}
+
+lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0, const void* A, const void* B,
+                            const void* Z_saved, const void* dY, float s, void* dX, void* dA, void* dB, void* dbias,
+                            void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  REQ(X); REQ(W0); REQ(A); REQ(B); REQ(dY); REQ(dA); REQ(dB);
+  ALN(X); ALN(W0); ALN(A); ALN(B); ALN(Z_saved); ALN(dY); ALN(dX); ALN(dA); ALN(dB); ALN(dbias);
+  if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
+  LinBwdWs w;
+  const size_t need = plan_lin_bwd(*sh, nullptr, &w);
+  if ((e = check_ws(ws, ws_bytes, need)) != LORA_OK) return e;
+  plan_lin_bwd(*sh, static_cast<char*>(ws), &w);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
+  const int r = (int)sh->r;
+  const size_t es = sh->dtype == LORA_BF16 ? 2 : 4;
+  if (M == 0 || s == 0.f) {
+    // no tokens, or strength 0: adapter gradients vanish; dX is the frozen base's
+    CK(cudaMemsetAsync(dA, 0, (size_t)r * in * es, st));
+    CK(cudaMemsetAsync(dB, 0, (size_t)out * r * es, st));
+    if (dbias && M == 0) CK(cudaMemsetAsync(dbias, 0, (size_t)out * es, st));
+    if (M == 0) return LORA_OK;
+  }
+  if (sh->dtype == LORA_BF16) {
+    if (s == 0.f) {
+      if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, nullptr, A, r, dX, nullptr, w.err), st));
+      if (dbias) {
+        ColReduceDesc d = cr_desc(M, out, 8, dY, dY, out, w.PB, w.splitsB);  // T unused beyond 8 cols
+        d.colsum = w.csum;
+        CK(colreduce(d, st));
+        CK(sum_splits<bf16>(w.csum, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
+      }
+      return LORA_OK;
+    }
+    const void* Z = Z_saved;
+    if (!Z) {
+      RowProjDesc d = rp_desc(M, in, r, X, A, false);
+      d.out_a = static_cast<bf16*>(w.Zrec);
+      CK(rowproj(d, st));
+      Z = w.Zrec;
+    }
+    {  // dB partials (dY^T Z) and column sums of dY, one pass over dY
+      ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB);
+      d.colsum = dbias ? w.csum : nullptr;
+      CK(colreduce(d, st));
+    }
+    {  // s*G = s * dY B
+      RowProjDesc d = rp_desc(M, out, r, dY, B, true);
+      d.out_b = static_cast<bf16*>(w.Gs);
+      d.scale_b = s;
+      CK(rowproj(d, st));
+    }
+    if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, nullptr, w.err), st));
+    CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA), st));
+    Partial pa{w.PA, w.splitsA, r, 0}, none{};
+    CK(finalize_dA<bf16>(r, in, pa, 1.f, none, 0.f, nullptr, 0.f, static_cast<const bf16*>(A), static_cast<bf16*>(dA),
+                         st));
+    Partial pb{w.PB, w.splitsB, r, 0};
+    CK(finalize_dB<bf16>(out, r, pb, s, nullptr, nullptr, nullptr, static_cast<const bf16*>(B), nullptr, s, false,
+                         static_cast<bf16*>(dB), st));
+    if (dbias) CK(sum_splits<bf16>(w.csum, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
+  } else {
+    if (dX) CK(sgemm_f32(sg(M, in, out, dY, out, false, W0, in, false, dX, in), st));
+    if (dbias) {
+      CK(coldot_f32(static_cast<const float*>(dY), nullptr, M, out, w.csum, nullptr, st));
+      CK(sum_splits<float>(w.csum, 1, out, static_cast<float*>(dbias), nullptr, st));
+    }
+    if (s == 0.f) return LORA_OK;
+    const void* Z = Z_saved;
+    if (!Z) {
+      CK(sgemm_f32(sg(M, r, in, X, in, false, A, in, true, w.Zrec, r), st));
+      Z = w.Zrec;
+    }
+    CK(sgemm_f32(sg(M, r, out, dY, out, false, B, r, false, w.Gs, r), st));            // G = dY B
+    if (dX) CK(sgemm_f32(sg(M, in, r, w.Gs, r, false, A, in, false, dX, in, s, 1.f), st));  // dX += s G A
+    CK(sgemm_f32(sg(r, in, M, w.Gs, r, true, X, in, false, dA, in, s), st));            // dA = s G^T X
+    CK(sgemm_f32(sg(out, r, M, dY, out, true, Z, r, false, dB, r, s), st));             // dB = s dY^T Z
+  }
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------------ DoRA
+lora_status dora_rownorm2(const lora_shape* sh, const void* W0, float* r0, void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  REQ(W0); REQ(r0);
+  ALN(W0); ALN(r0);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (sh->dtype == LORA_BF16) CK(rownorm2<bf16>(static_cast<const bf16*>(W0), sh->d_out, sh->d_in, r0, st));
+  else CK(rownorm2<float>(static_cast<const float*>(W0), sh->d_out, sh->d_in, r0, st));
+  return LORA_OK;
+}
+
+lora_status dora_linear_fwd(const lora_shape* sh, const void* X, const void* W0, const void* A, const void* B,
+                            const void* m, const void* bias, const float* r0, float s, float eps, void* Y,
+                            void* Z_save, float* n_save, float* V_save, void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  REQ(X); REQ(W0); REQ(A); REQ(B); REQ(m); REQ(r0); REQ(Y); REQ(n_save); REQ(V_save);
+  ALN(X); ALN(W0); ALN(A); ALN(B); ALN(m); ALN(bias); ALN(r0); ALN(Y); ALN(Z_save); ALN(n_save); ALN(V_save);
+  if (!isfinite(s) || !isfinite(eps) || eps < 0.f) return LORA_ERR_INVALID_ARG;
+  DoraFwdWs w;
+  const size_t need = plan_dora_fwd(*sh, nullptr, &w);
+  if ((e = check_ws(ws, ws_bytes, need)) != LORA_OK) return e;
+  plan_dora_fwd(*sh, static_cast<char*>(ws), &w);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
+  const int r = (int)sh->r;
+  if (sh->dtype == LORA_BF16) {
+    {  // V = W0 A^T (fp32), one pass over W0
+      RowProjDesc d = rp_desc(out, in, r, W0, A, false);
+      d.out_f = V_save;
+      CK(rowproj(d, st));
+    }
+    CK(gram_rows<bf16>(static_cast<const bf16*>(A), r, in, w.Kr, st));
+    CK(dora_norm<bf16>(out, r, r0, V_save, static_cast<const bf16*>(B), w.Kr, static_cast<const bf16*>(m), s, eps,
+                       n_save, w.c, st));
+    if (M == 0) return LORA_OK;
+    if (s != 0.f || Z_save) {
+      RowProjDesc d = rp_desc(M, in, r, X, A, false);
+      d.out_a = static_cast<bf16*>(Z_save);
+      d.out_b = s != 0.f ? static_cast<bf16*>(w.Zs) : nullptr;
+      d.scale_b = s;
+      CK(rowproj(d, st));
+    }
+    if (s == 0.f)  // strength 0: frozen base X W0^T + bias
+      CK(tc_gemm(fwd_desc(M, out, in, X, W0, nullptr, B, r, Y, static_cast<const bf16*>(bias), nullptr, w.err), st));
+    else
+      CK(tc_gemm(fwd_desc(M, out, in, X, W0, w.Zs, B, r, Y, static_cast<const bf16*>(bias), w.c, w.err), st));
+  } else {
+    CK(sgemm_f32(sg(out, r, in, W0, in, false, A, in, true, V_save, r), st));
+    CK(gram_rows<float>(static_cast<const float*>(A), r, in, w.Kr, st));
+    CK(dora_norm<float>(out, r, r0, V_save, static_cast<const float*>(B), w.Kr, static_cast<const float*>(m), s, eps,
+                        n_save, w.c, st));
+    if (M == 0) return LORA_OK;
+    void* Z = Z_save ? Z_save : w.Zs;
+    if (s != 0.f || Z_save) CK(sgemm_f32(sg(M, r, in, X, in, false, A, in, true, Z, r), st));
+    SgemmDesc d = sg(M, out, in, X, in, false, W0, in, true, Y, out);
+    if (s == 0.f) {
+      d.bias = static_cast<const float*>(bias);
+      CK(sgemm_f32(d, st));
+    } else {
+      d.cs = w.c;
+      CK(sgemm_f32(d, st));
+      SgemmDesc d2 = sg(M, out, r, Z, r, false, B, r, true, Y, out, s, 1.f);
+      d2.cs = w.c;
+      d2.bias = static_cast<const float*>(bias);
+      CK(sgemm_f32(d2, st));
+    }
+  }
+  return LORA_OK;
+}
+
+lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0, const void* A, const void* B,
+                            const void* m, const void* bias, const void* Y, const void* Z_saved, const float* n_saved,
+                            const float* V_saved, const void* dY, float s, float eps, void* dX, void* dA, void* dB,
+                            void* dm, void* dbias, void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  REQ(X); REQ(W0); REQ(A); REQ(B); REQ(m); REQ(Y); REQ(n_saved); REQ(V_saved); REQ(dY); REQ(dA); REQ(dB); REQ(dm);
+  ALN(X); ALN(W0); ALN(A); ALN(B); ALN(m); ALN(bias); ALN(Y); ALN(Z_saved); ALN(n_saved); ALN(V_saved); ALN(dY);
+  ALN(dX); ALN(dA); ALN(dB); ALN(dm); ALN(dbias);
+  if (!isfinite(s) || !isfinite(eps) || eps < 0.f) return LORA_ERR_INVALID_ARG;
+  DoraBwdWs w;
+  const size_t need = plan_dora_bwd(*sh, nullptr, &w);
+  if ((e = check_ws(ws, ws_bytes, need)) != LORA_OK) return e;
+  plan_dora_bwd(*sh, static_cast<char*>(ws), &w);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
+  const int r = (int)sh->r;
+  const size_t es = sh->dtype == LORA_BF16 ? 2 : 4;
+  const bool bf = sh->dtype == LORA_BF16;
+  if (M == 0 || s == 0.f) {
+    CK(cudaMemsetAsync(dA, 0, (size_t)r * in * es, st));
+    CK(cudaMemsetAsync(dB, 0, (size_t)out * r * es, st));
+    CK(cudaMemsetAsync(dm, 0, (size_t)out * es, st));
+    if (M == 0) {
+      if (dbias) CK(cudaMemsetAsync(dbias, 0, (size_t)out * es, st));
+      return LORA_OK;
+    }
+    // strength 0: frozen base, dX = dY W0, dbias = colsum(dY)
+    if (bf) {
+      if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, nullptr, A, r, dX, nullptr, w.err), st));
+      if (dbias) {
+        ColReduceDesc d = cr_desc(M, out, 8, dY, dY, out, w.PB, w.splitsB);
+        d.colsum = w.csump;
+        CK(colreduce(d, st));
+        CK(sum_splits<bf16>(w.csump, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
+      }
+    } else {
+      if (dX) CK(sgemm_f32(sg(M, in, out, dY, out, false, W0, in, false, dX, in), st));
+      if (dbias) {
+        CK(coldot_f32(static_cast<const float*>(dY), nullptr, M, out, w.csum, nullptr, st));
+        CK(sum_splits<float>(w.csum, 1, out, static_cast<float*>(dbias), nullptr, st));
+      }
+    }
+    return LORA_OK;
+  }
+  if (bf) {
+    const bf16* mb = static_cast<const bf16*>(m);
+    CK(dora_c<bf16>(out, mb, n_saved, w.c, st));
+    const void* Z = Z_saved;
+    if (!Z) {
+      RowProjDesc d = rp_desc(M, in, r, X, A, false);
+      d.out_a = static_cast<bf16*>(w.Zrec);
+      CK(rowproj(d, st));
+      Z = w.Zrec;
+    }
+    {  // one pass over dY and Y: dY^T Z partials, colsum(dY), colsum(dY o Y)
+      ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB);
+      d.Y = static_cast<const bf16*>(Y);
+      d.ldy = out;
+      d.colsum = w.csump;
+      d.coldot = w.dotp;
+      CK(colreduce(d, st));
+    }
+    CK(sum_splits<float>(w.dotp, w.splitsB, out, w.dot, nullptr, st));
+    CK(sum_splits<float>(w.csump, w.splitsB, out, w.csum, nullptr, st));
+    CK(dora_dc<bf16>(out, w.dot, w.csum, static_cast<const bf16*>(bias), w.c, n_saved, mb, eps, w.g,
+                     static_cast<bf16*>(dm), static_cast<bf16*>(dbias), st));
+    CK(scale_rows<bf16>(static_cast<const bf16*>(B), out, r, w.c, 1.f, static_cast<bf16*>(w.Bc), st));
+    CK(scale_rows<bf16>(static_cast<const bf16*>(B), out, r, w.g, 1.f, static_cast<bf16*>(w.gB), st));
+    {  // s * G = s (dY o c) B  =  s dY (c o B)
+      RowProjDesc d = rp_desc(M, out, r, dY, w.Bc, true);
+      d.out_b = static_cast<bf16*>(w.Gs);
+      d.scale_b = s;
+      CK(rowproj(d, st));
+    }
+    if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, w.c, w.err), st));
+    CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA), st));        // X^T (s G)
+    CK(colreduce(cr_desc(out, in, r, W0, w.gB, r, w.PW, w.splitsW), st));     // W0^T (g o B)
+    CK(gram_rows<bf16>(static_cast<const bf16*>(A), r, in, w.Kr, st));
+    CK(gram_weighted<bf16>(static_cast<const bf16*>(B), out, r, w.g, w.Kg, st));
+    Partial pa{w.PA, w.splitsA, r, 0}, pw{w.PW, w.splitsW, r, 0}, pb{w.PB, w.splitsB, r, 0};
+    CK(finalize_dA<bf16>(r, in, pa, 1.f, pw, 2.f * s, w.Kg, 2.f * s * s, static_cast<const bf16*>(A),
+                         static_cast<bf16*>(dA), st));
+    CK(finalize_dB<bf16>(out, r, pb, s, w.c, w.g, V_saved, static_cast<const bf16*>(B), w.Kr, s, false,
+                         static_cast<bf16*>(dB), st));
+  } else {
+    const float* mf = static_cast<const float*>(m);
+    CK(dora_c<float>(out, mf, n_saved, w.c, st));
+    const void* Z = Z_saved;
+    if (!Z) {
+      CK(sgemm_f32(sg(M, r, in, X, in, false, A, in, true, w.Zrec, r), st));
+      Z = w.Zrec;
+    }
+    CK(coldot_f32(static_cast<const float*>(dY), static_cast<const float*>(Y), M, out, w.csum, w.dot, st));
+    CK(dora_dc<float>(out, w.dot, w.csum, static_cast<const float*>(bias), w.c, n_saved, mf, eps, w.g,
+                      static_cast<float*>(dm), static_cast<float*>(dbias), st));
+    {  // G = (dY o c) B
+      SgemmDesc d = sg(M, r, out, dY, out, false, B, r, false, w.Gs, r);
+      d.kscale = w.c;
+      CK(sgemm_f32(d, st));
+    }
+    if (dX) {
+      SgemmDesc d = sg(M, in, out, dY, out, false, W0, in, false, dX, in);
+      d.kscale = w.c;
+      CK(sgemm_f32(d, st));
+      CK(sgemm_f32(sg(M, in, r, w.Gs, r, false, A, in, false, dX, in, s, 1.f), st));
+    }
+    CK(gram_rows<float>(static_cast<const float*>(A), r, in, w.Kr, st));
+    CK(gram_weighted<float>(static_cast<const float*>(B), out, r, w.g, w.Kg, st));
+    CK(scale_rows<float>(static_cast<const float*>(B), out, r, w.g, 1.f, static_cast<float*>(w.gB), st));
+    CK(sgemm_f32(sg(r, in, M, w.Gs, r, true, X, in, false, dA, in, s), st));                 // s G^T X
+    CK(sgemm_f32(sg(r, in, out, w.gB, r, true, W0, in, false, dA, in, 2.f * s, 1.f), st));  // + 2s (gB)^T W0
+    CK(sgemm_f32(sg(r, in, r, w.Kg, r, false, A, in, false, dA, in, 2.f * s * s, 1.f), st)); // + 2s^2 Kg A
+    {
+      SgemmDesc d = sg(out, r, M, dY, out, true, Z, r, false, dB, r, s);  // s c o (dY^T Z)
+      d.rscale = w.c;
+      CK(sgemm_f32(d, st));
+    }
+    Partial none{};
+    CK(finalize_dB<float>(out, r, none, 0.f, nullptr, w.g, V_saved, static_cast<const float*>(B), w.Kr, s, true,
+                          static_cast<float*>(dB), st));
+  }
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------------ SwiGLU MLP
+static lora_status check_proj(const lora_proj* p) {
+  if (!p || !p->W || !p->A || !p->B) return LORA_ERR_INVALID_ARG;
+  if (!al16(p->W) || !al16(p->A) || !al16(p->B)) return LORA_ERR_MISALIGNED;
+  if (!isfinite(p->s)) return LORA_ERR_INVALID_ARG;
+  return LORA_OK;
+}
+
+lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const lora_proj* gate, const lora_proj* up,
+                                const lora_proj* down, void* Y, void* e_save, void* u_save, void* h_save,
+                                void* Zgu_save, void* Zd_save, void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_mlp_shape(sh);
+  if (e != LORA_OK) return e;
+  if ((e = check_proj(gate)) != LORA_OK || (e = check_proj(up)) != LORA_OK || (e = check_proj(down)) != LORA_OK)
+    return e;
+  REQ(X); REQ(Y); REQ(e_save); REQ(u_save); REQ(h_save); REQ(Zgu_save); REQ(Zd_save);
+  ALN(X); ALN(Y); ALN(e_save); ALN(u_save); ALN(h_save); ALN(Zgu_save); ALN(Zd_save);
+  MlpFwdWs w;
+  const size_t need = plan_mlp_fwd(*sh, nullptr, &w);
+  if ((e = check_ws(ws, ws_bytes, need)) != LORA_OK) return e;
+  plan_mlp_fwd(*sh, static_cast<char*>(ws), &w);
+  if (sh->M == 0) return LORA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, H = sh->H, I = sh->I;
+  const int r = (int)sh->r;
+  CK(concat_rows_bf16(static_cast<const bf16*>(gate->A), r, static_cast<const bf16*>(up->A), r, H, w.Agu, st));
+  {  // [Zg | Zu] = X [Ag ; Au]^T, saved unscaled and scaled per half
+    RowProjDesc d = rp_desc(M, H, 2 * r, X, w.Agu, false);
+    d.out_a = static_cast<bf16*>(Zgu_save);
+    d.out_b = w.Zgus;
+    d.scale_b = gate->s;
+    d.split_col = r;
+    d.scale_b_hi = up->s;
+    CK(rowproj(d, st));
+  }
+  {  // e, u, h = gate/up GEMM with both adapters, SwiGLU epilogue
+    TcGemmDesc d;
+    d.mode = TC_SWIGLU_FWD;
+    d.M = (int)M;
+    d.N = (int)I;
+    d.K0 = (int)H;
+    d.A0 = X;
+    d.lda0 = H;
+    d.B0 = gate->W;
+    d.B0b = up->W;
+    d.ldb0 = H;
+    d.has_tail = true;
+    d.A1 = w.Zgus;
+    d.lda1 = 2 * r;
+    d.K1 = 2 * r;
+    d.K1_a = 2 * r;
+    d.B1 = gate->B;
+    d.B1b = up->B;
+    d.ldb1 = r;
+    d.K1_b = r;
+    d.b1b_x = -r;
+    d.out[0] = e_save;
+    d.out[1] = u_save;
+    d.out[2] = h_save;
+    d.ldo = I;
+    d.err = w.err;
+    d.timeout_ns = wait_timeout_ns();
+    CK(tc_gemm(d, st));
+  }
+  {  // Zd = h Ad^T
+    RowProjDesc d = rp_desc(M, I, r, h_save, down->A, false);
+    d.out_a = static_cast<bf16*>(Zd_save);
+    d.out_b = w.Zds;
+    d.scale_b = down->s;
+    CK(rowproj(d, st));
+  }
+  CK(tc_gemm(fwd_desc(M, H, I, h_save, down->W, w.Zds, down->B, r, Y, nullptr, nullptr, w.err), st));
+  return LORA_OK;
+}
+
+lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const lora_proj* gate, const lora_proj* up,
+                                const lora_proj* down, const void* e_saved, const void* u_saved, const void* h_saved,
+                                const void* Zgu_saved, const void* Zd_saved, const void* dY, void* dX, void* dAg,
+                                void* dBg, void* dAu, void* dBu, void* dAd, void* dBd, void* ws, size_t ws_bytes,
+                                void* stream) {
+  lora_status e = check_mlp_shape(sh);
+  if (e != LORA_OK) return e;
+  if ((e = check_proj(gate)) != LORA_OK || (e = check_proj(up)) != LORA_OK || (e = check_proj(down)) != LORA_OK)
+    return e;
+  REQ(X); REQ(e_saved); REQ(u_saved); REQ(h_saved); REQ(Zgu_saved); REQ(Zd_saved); REQ(dY);
+  REQ(dAg); REQ(dBg); REQ(dAu); REQ(dBu); REQ(dAd); REQ(dBd);
+  ALN(X); ALN(e_saved); ALN(u_saved); ALN(h_saved); ALN(Zgu_saved); ALN(Zd_saved); ALN(dY); ALN(dX);
+  ALN(dAg); ALN(dBg); ALN(dAu); ALN(dBu); ALN(dAd); ALN(dBd);
+  MlpBwdWs w;
+  const size_t need = plan_mlp_bwd(*sh, nullptr, &w);
+  if ((e = check_ws(ws, ws_bytes, need)) != LORA_OK) return e;
+  plan_mlp_bwd(*sh, static_cast<char*>(ws), &w);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, H = sh->H, I = sh->I, Ip = mlp_ipad(*sh);
+  const int r = (int)sh->r;
+  if (M == 0) {
+    CK(cudaMemsetAsync(dAg, 0, (size_t)r * H * 2, st));
+    CK(cudaMemsetAsync(dAu, 0, (size_t)r * H * 2, st));
+    CK(cudaMemsetAsync(dBg, 0, (size_t)I * r * 2, st));
+    CK(cudaMemsetAsync(dBu, 0, (size_t)I * r * 2, st));
+    CK(cudaMemsetAsync(dAd, 0, (size_t)r * I * 2, st));
+    CK(cudaMemsetAsync(dBd, 0, (size_t)H * r * 2, st));
+    return LORA_OK;
+  }
+  const bf16* Zgu = static_cast<const bf16*>(Zgu_saved);
+  // down projection: dBd partials (dY^T Zd), sd*Gd = sd dY Bd
+  CK(colreduce(cr_desc(M, H, r, dY, Zd_saved, r, w.PBd, w.sBd), st));
+  {
+    RowProjDesc d = rp_desc(M, H, r, dY, down->B, true);
+    d.out_b = w.Gds;
+    d.scale_b = down->s;
+    CK(rowproj(d, st));
+  }
+  if (Ip != I) CK(cudaMemsetAsync(w.dedu, 0, (size_t)M * 2 * Ip * 2, st));
+  {  // dh = dY Wd + (sd Gd) Ad, SwiGLU backward in the epilogue -> de, du
+    TcGemmDesc d;
+    d.mode = TC_SWIGLU_BWD;
+    d.M = (int)M;
+    d.N = (int)I;
+    d.K0 = (int)H;
+    d.A0 = dY;
+    d.lda0 = H;
+    d.B0 = down->W;
+    d.ldb0 = I;
+    d.b0_mn = true;
+    d.b0_rows = (int)H;
+    d.has_tail = true;
+    d.b1_mn = true;
+    d.A1 = w.Gds;
+    d.lda1 = r;
+    d.K1 = r;
+    d.K1_a = r;
+    d.B1 = down->A;
+    d.ldb1 = I;
+    d.out[0] = w.dedu;
+    d.out[1] = w.dedu + Ip;
+    d.ldo = 2 * Ip;
+    d.e_in = static_cast<const bf16*>(e_saved);
+    d.u_in = static_cast<const bf16*>(u_saved);
+    d.ld_eu = I;
+    d.err = w.err;
+    d.timeout_ns = wait_timeout_ns();
+    CK(tc_gemm(d, st));
+  }
+  CK(colreduce(cr_desc(M, I, r, h_saved, w.Gds, r, w.PAd, w.sAd), st));     // h^T (sd Gd)
+  {  // de^T Zg and du^T Zu
+    ColReduceDesc d = cr_desc(M, I, r, w.dedu, Zgu, 2 * r, w.PBg, w.sBg);
+    d.lds = 2 * Ip;
+    CK(colreduce(d, st));
+    ColReduceDesc d2 = cr_desc(M, I, r, w.dedu + Ip, Zgu + r, 2 * r, w.PBu, w.sBg);
+    d2.lds = 2 * Ip;
+    CK(colreduce(d2, st));
+  }
+  {  // [sg Gg | su Gu] = [sg de Bg | su du Bu]
+    RowProjDesc d = rp_desc(M, I, r, w.dedu, gate->B, true);
+    d.lds = 2 * Ip;
+    d.out_b = w.Ggus;
+    d.scale_b = gate->s;
+    d.ldo = 2 * r;
+    CK(rowproj(d, st));
+    RowProjDesc d2 = rp_desc(M, I, r, w.dedu + Ip, up->B, true);
+    d2.lds = 2 * Ip;
+    d2.out_b = w.Ggus + r;
+    d2.scale_b = up->s;
+    d2.ldo = 2 * r;
+    CK(rowproj(d2, st));
+  }
+  CK(concat_rows_bf16(static_cast<const bf16*>(gate->A), r, static_cast<const bf16*>(up->A), r, H, w.Agu, st));
+  if (dX) {  // dX = [de | du] [Wg ; Wu] + [sg Gg | su Gu] [Ag ; Au]
+    TcGemmDesc d;
+    d.mode = TC_BWD_DX;
+    d.M = (int)M;
+    d.N = (int)H;
+    d.K0 = (int)(2 * Ip);
+    d.A0 = w.dedu;
+    d.lda0 = 2 * Ip;
+    d.B0 = gate->W;
+    d.B0b = up->W;
+    d.ldb0 = H;
+    d.b0_mn = true;
+    d.b0_rows = (int)I;
+    d.b0b_rows = (int)I;
+    d.k0_split = (int)Ip;
+    d.has_tail = true;
+    d.b1_mn = true;
+    d.A1 = w.Ggus;
+    d.lda1 = 2 * r;
+    d.K1 = 2 * r;
+    d.K1_a = 2 * r;
+    d.B1 = w.Agu;
+    d.ldb1 = H;
+    d.out[0] = dX;
+    d.ldo = H;
+    d.err = w.err;
+    d.timeout_ns = wait_timeout_ns();
+    CK(tc_gemm(d, st));
+  }
+  CK(colreduce(cr_desc(M, H, 2 * r, X, w.Ggus, 2 * r, w.PAgu, w.sAgu), st));  // X^T [sg Gg | su Gu]
+  Partial none{};
+  Partial pag{w.PAgu, w.sAgu, 2 * r, 0}, pau{w.PAgu, w.sAgu, 2 * r, r};
+  CK(finalize_dA<bf16>(r, H, pag, 1.f, none, 0.f, nullptr, 0.f, nullptr, static_cast<bf16*>(dAg), st));
+  CK(finalize_dA<bf16>(r, H, pau, 1.f, none, 0.f, nullptr, 0.f, nullptr, static_cast<bf16*>(dAu), st));
+  Partial pad{w.PAd, w.sAd, r, 0};
+  CK(finalize_dA<bf16>(r, I, pad, 1.f, none, 0.f, nullptr, 0.f, nullptr, static_cast<bf16*>(dAd), st));
+  Partial pbd{w.PBd, w.sBd, r, 0}, pbg{w.PBg, w.sBg, r, 0}, pbu{w.PBu, w.sBg, r, 0};
+  CK(finalize_dB<bf16>(H, r, pbd, down->s, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, false,
+                       static_cast<bf16*>(dBd), st));
+  CK(finalize_dB<bf16>(I, r, pbg, gate->s, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, false,
+                       static_cast<bf16*>(dBg), st));
+  CK(finalize_dB<bf16>(I, r, pbu, up->s, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, false,
+                       static_cast<bf16*>(dBu), st));
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------------ W8A8
+lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t* Xq, float* sx, const void* A,
+                               int64_t r, void* Z, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 8) return rows < 0 || cols <= 0 ? LORA_ERR_INVALID_ARG : LORA_ERR_UNSUPPORTED;
+  REQ(X); REQ(Xq); REQ(sx);
+  ALN(X); ALN(Xq); ALN(A); ALN(Z);
+  if ((A == nullptr) != (Z == nullptr)) return LORA_ERR_INVALID_ARG;
+  if (A && (r < 8 || r > 64 || r % 8)) return LORA_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (rows == 0) return LORA_OK;
+  CK(quantize_rows_bf16(static_cast<const bf16*>(X), rows, cols, Xq, sx, st));
+  if (A) {
+    RowProjDesc d = rp_desc(rows, cols, (int)r, X, A, false);
+    d.out_a = static_cast<bf16*>(Z);
+    CK(rowproj(d, st));
+  }
+  return LORA_OK;
+}
+
+lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq, const float* sx,
+                          const int8_t* Wq, const float* sw, const void* Z, const void* B, float s, const void* bias,
+                          void* Y, int32_t* acc_out, void* stream) {
+  if (M < 0 || d_in <= 0 || d_out <= 0) return LORA_ERR_INVALID_ARG;
+  if (d_in % 32 || d_out % 8) return LORA_ERR_UNSUPPORTED;
+  REQ(Xq); REQ(Wq);
+  if (Y == nullptr && acc_out == nullptr) return LORA_ERR_INVALID_ARG;
+  if (Y && (!sx || !sw)) return LORA_ERR_INVALID_ARG;
+  if ((Z == nullptr) != (B == nullptr)) return LORA_ERR_INVALID_ARG;
+  if (Z && (r < 8 || r > 64 || r % 8)) return LORA_ERR_UNSUPPORTED;
+  if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
+  ALN(Xq); ALN(sx); ALN(Wq); ALN(sw); ALN(Z); ALN(B); ALN(bias); ALN(Y); ALN(acc_out);
+  if (M == 0) return LORA_OK;
+  CK(w8a8_gemm(M, d_in, d_out, Z ? (int)r : 0, Xq, sx, Wq, sw, static_cast<const bf16*>(Z),
+               static_cast<const bf16*>(B), s, static_cast<const bf16*>(bias), static_cast<bf16*>(Y), acc_out,
+               (cudaStream_t)stream));
+  return LORA_OK;
+}
+
+}  // extern "C"

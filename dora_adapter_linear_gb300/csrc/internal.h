@@ -1,0 +1,188 @@
+// Host-side declarations shared by the translation units of the library (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+namespace lg {
+
+typedef __nv_bfloat16 bf16;
+
+int num_sms_current();
+
+// tracing (prof.cu)
+void count_launch(int n = 1);
+uint64_t launch_count();
+bool prof_enabled();
+void prof_set(bool on);
+void prof_mark(cudaStream_t st, bool start, double flops);
+cudaError_t prof_collect(double* ms, int64_t* launches, double* flops, bool reset);
+
+// ------------------------------------------------------------------ tcgen05 GEMM engine
+enum EpiKind { EPI_SCALE_BIAS = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2 };
+enum TcMode {
+  TC_FWD = 0,          // A0 [M,K0] x B0 [N,K0]^T (+ A1 [M,K1] x B1 [N,K1]^T), epilogue scale/bias
+  TC_BWD_DX = 1,       // A0 [M,K0] x B0 [K0,N] (MN-major) (+ A1 x B1 [K1,N]), optional A-scale along K
+  TC_SWIGLU_FWD = 2,   // stacked gate/up weights, SwiGLU epilogue writing e, u, h
+  TC_SWIGLU_BWD = 3    // MN-major B, epilogue forms de, du from saved e, u
+};
+
+struct TcGemmDesc {
+  int mode = TC_FWD;
+  int M = 0, N = 0, K0 = 0, K1 = 0;
+  bool b0_mn = false, b1_mn = false, has_tail = false;
+  const void* A0 = nullptr;
+  int64_t lda0 = 0;
+  const void* B0 = nullptr;
+  const void* B0b = nullptr;  // K-major: second stacked half; MN-major: rows of K past k0_split
+  int64_t ldb0 = 0;
+  int b0_rows = 0, b0b_rows = 0, k0_split = 0;
+  const void* A1 = nullptr;
+  int64_t lda1 = 0;
+  int K1_a = 0;                // columns of the A1 tensor
+  const void* B1 = nullptr;
+  const void* B1b = nullptr;
+  int64_t ldb1 = 0;
+  int K1_b = 0;                // columns of a K-major B1 tensor
+  int b1b_x = 0;
+  void* out[3] = {nullptr, nullptr, nullptr};
+  int64_t ldo = 0;
+  const float* col_scale = nullptr;
+  const bf16* bias = nullptr;
+  const float* a_kscale = nullptr;
+  const bf16* e_in = nullptr;
+  const bf16* u_in = nullptr;
+  int64_t ld_eu = 0;
+  uint32_t* err = nullptr;
+  uint64_t timeout_ns = 2000000000ull;
+  int max_ctas = 0;
+};
+cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st);
+
+// ------------------------------------------------------------------ skinny (rank-r) kernels, bf16
+// T = S U^T : S [rows, K] (ld lds), U either [R, K] (u_kr = false) or [K, R] (u_kr = true).
+// Outputs (each optional): out_a = bf16(scale_a * T), out_b = bf16(scale_b * T), out_f = T (fp32),
+// all with leading dimension R.  R multiple of 8, 8 <= R <= 64.
+struct RowProjDesc {
+  int64_t rows = 0, K = 0;
+  int R = 0;
+  const bf16* S = nullptr;
+  int64_t lds = 0;
+  const bf16* U = nullptr;
+  bool u_kr = false;
+  int64_t ldu = 0;
+  bf16* out_a = nullptr;
+  float scale_a = 1.f;
+  bf16* out_b = nullptr;
+  float scale_b = 1.f;
+  float* out_f = nullptr;
+  int64_t ldo = 0;              // leading dimension of the outputs (0 -> R)
+  int split_col = 1 << 30;      // columns >= split_col of out_b use scale_b_hi
+  float scale_b_hi = 1.f;
+};
+cudaError_t rowproj(const RowProjDesc& d, cudaStream_t st);
+
+// Column reduction over rows: part[split][k][j] = sum_{rows of split} S[row, k] * T[row, j]
+// (S [rows, K] ld lds, T [rows, R] ld ldt), plus optional per-column sums
+// colsum[split][k] = sum S[row,k] and coldot[split][k] = sum S[row,k] * Y[row,k].
+struct ColReduceDesc {
+  int64_t rows = 0, K = 0;
+  int R = 0;
+  const bf16* S = nullptr;
+  int64_t lds = 0;
+  const bf16* T = nullptr;
+  int64_t ldt = 0;
+  const bf16* Y = nullptr;     // optional second [rows, K] input for coldot
+  int64_t ldy = 0;
+  float* part = nullptr;       // [splits, K, R]
+  float* colsum = nullptr;     // [splits, K] or null
+  float* coldot = nullptr;     // [splits, K] or null
+  int splits = 1;
+};
+int colreduce_splits(int64_t rows, int64_t K);
+cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st);
+
+// ------------------------------------------------------------------ small kernels (templated on T)
+template <typename T>
+cudaError_t rownorm2(const T* W, int64_t rows, int64_t cols, float* r0, cudaStream_t st);
+// K = A A^T (fp32 [r, r]) for A [r, cols]
+template <typename T>
+cudaError_t gram_rows(const T* A, int r, int64_t cols, float* K, cudaStream_t st);
+// DoRA norm: q = r0 + 2s sum_j V[o,j] B[o,j] + s^2 sum_j (B Kr)[o,j] B[o,j]; n = max(sqrt(max(q,0)), eps);
+// c = m / n.  Writes n (n_out) and c.
+template <typename T>
+cudaError_t dora_norm(int64_t out, int r, const float* r0, const float* V, const T* B, const float* Kr,
+                      const T* m, float s, float eps, float* n_out, float* c, cudaStream_t st);
+// sum over splits of column partials: dst[k] = sum_s src[s][k]  (fp32 and, optionally, as T)
+template <typename T>
+cudaError_t sum_splits(const float* src, int splits, int64_t n, float* dst_f, T* dst_t, cudaStream_t st);
+// c = m / n
+template <typename T>
+cudaError_t dora_c(int64_t out, const T* m, const float* n, float* c, cudaStream_t st);
+// DoRA backward small step: dc = (dot - bias*colsum)/c ; dm = dc/n ; g = -m dc/(2 n^3) (0 if n<=eps)
+template <typename T>
+cudaError_t dora_dc(int64_t out, const float* dot, const float* csum, const T* bias, const float* c,
+                    const float* n, const T* m, float eps, float* g, T* dm, T* dbias, cudaStream_t st);
+// out[o, j] = scale[o] * B[o, j] (bf16 / T out), scale may be null (=1), with extra factor f.
+template <typename T>
+cudaError_t scale_rows(const T* B, int64_t rows, int r, const float* scale, float f, T* out, cudaStream_t st);
+// Final LoRA/DoRA gradient assembly from fp32 partials:
+//   dA[j, k] = sA * sum_s PA[s][k][j] + sW * sum_s PW[s][k][j] + s2 * sum_l Kg[j,l] A[l,k]
+//   dB[o, j] = sB * rs[o] * sum_s PB[s][o][j] + 2 s g[o] V[o,j] + 2 s^2 g[o] (B Kr)[o,j]
+// Partials are laid out [splits][n][ldp] and read at columns j0 .. j0 + r - 1.
+struct Partial {
+  const float* p = nullptr;
+  int splits = 0;
+  int ldp = 0;
+  int j0 = 0;
+};
+template <typename T>
+cudaError_t finalize_dA(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg, float s2,
+                        const T* A, T* dA, cudaStream_t st);
+template <typename T>
+cudaError_t finalize_dB(int64_t out, int r, Partial PB, float sB, const float* rs, const float* g, const float* V,
+                        const T* B, const float* Kr, float s, bool accumulate, T* dB, cudaStream_t st);
+// Kg = B^T diag(g) B  (fp32 [r, r])
+template <typename T>
+cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float* Kg, cudaStream_t st);
+// rows of two matrices stacked: dst = [X1 ; X2] (rows1 + rows2, cols), same dtype
+cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int64_t rows2, int64_t cols, bf16* dst,
+                             cudaStream_t st);
+cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st);
+
+// ------------------------------------------------------------------ fp32 SIMT path
+// C[M,N] = alpha * op(A) op(B) (op(A) [M,K], op(B) [K,N]) + beta * C, with optional per-K scale of
+// op(A) columns (kscale[K]), per-row output scale (rscale[M]), per-column bias[N] and column scale cs[N]
+// applied as C = cs*acc*alpha + bias (+ beta C).
+struct SgemmDesc {
+  int64_t M = 0, N = 0, K = 0;
+  bool ta = false, tb = false;
+  const float* A = nullptr;
+  int64_t lda = 0;
+  const float* B = nullptr;
+  int64_t ldb = 0;
+  float* C = nullptr;
+  int64_t ldc = 0;
+  float alpha = 1.f, beta = 0.f;
+  const float* kscale = nullptr;
+  const float* rscale = nullptr;
+  const float* cs = nullptr;
+  const float* bias = nullptr;
+};
+cudaError_t sgemm_f32(const SgemmDesc& d, cudaStream_t st);
+// per-column partial sums for fp32 path: colsum[k] = sum_i S[i,k], coldot[k] = sum_i S[i,k]*Y[i,k]
+cudaError_t coldot_f32(const float* S, const float* Y, int64_t rows, int64_t K, float* colsum, float* coldot,
+                       cudaStream_t st);
+
+// ------------------------------------------------------------------ W8A8
+cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t* Xq, float* sx, cudaStream_t st);
+cudaError_t w8a8_gemm(int64_t M, int64_t K, int64_t N, int r, const int8_t* Xq, const float* sx, const int8_t* Wq,
+                      const float* sw, const bf16* Z, const bf16* B, float s, const bf16* bias, bf16* Y,
+                      int32_t* acc_out, cudaStream_t st);
+
+// ------------------------------------------------------------------ debug
+cudaError_t debug_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace lg

@@ -1,0 +1,340 @@
+// Small per-row / per-column kernels of the DoRA norm and the gradient assembly.  They
+// touch vectors of length d_out or [d_out, r] / [r, d_in] matrices (kilobytes to a few MB),
+// so they are latency-bound one-pass kernels; templated on the storage type (fp32 / bf16).
+#include "common.cuh"
+#include "internal.h"
+
+namespace lg {
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T* p, int64_t i) {
+  return to_f<T>(p[i]);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int NT>
+__device__ __forceinline__ float block_sum(float v) {
+  __shared__ float red[NT / 32];
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x < 32) {
+    t = l < NT / 32 ? red[l] : 0.f;
+    t = warp_sum(t);
+  }
+  return t;  // valid in thread 0
+}
+
+// ------------------------------------------------------------------ rowsum(W^2), one warp per row
+template <typename T>
+__global__ void rownorm2_kernel(const T* W, int64_t rows, int64_t cols, float* r0) {
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const T* w = W + row * cols;
+  float acc = 0.f;
+  constexpr int V = 16 / sizeof(T);
+  for (int64_t k = (int64_t)lane * V; k < cols; k += 32 * V) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(w + k);
+    const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const float f = to_f<T>(e[i]);
+      acc = fmaf(f, f, acc);
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) r0[row] = acc;
+}
+
+template <typename T>
+cudaError_t rownorm2(const T* W, int64_t rows, int64_t cols, float* r0, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  rownorm2_kernel<T><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(W, rows, cols, r0);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ K = A A^T, one block per (i, j)
+template <typename T>
+__global__ void gram_rows_kernel(const T* A, int r, int64_t cols, float* K) {
+  const int i = blockIdx.x / r, j = blockIdx.x % r;
+  if (j < i) return;
+  float acc = 0.f;
+  for (int64_t k = threadIdx.x; k < cols; k += blockDim.x) acc = fmaf(ldf(A, i * cols + k), ldf(A, j * cols + k), acc);
+  acc = block_sum<256>(acc);
+  if (threadIdx.x == 0) {
+    K[i * r + j] = acc;
+    K[j * r + i] = acc;
+  }
+}
+template <typename T>
+cudaError_t gram_rows(const T* A, int r, int64_t cols, float* K, cudaStream_t st) {
+  gram_rows_kernel<T><<<r * r, 256, 0, st>>>(A, r, cols, K);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ Kg = B^T diag(g) B
+template <typename T>
+__global__ void gram_weighted_kernel(const T* B, int64_t out, int r, const float* g, float* Kg) {
+  const int i = blockIdx.x / r, j = blockIdx.x % r;
+  if (j < i) return;
+  float acc = 0.f;
+  for (int64_t o = threadIdx.x; o < out; o += blockDim.x) acc = fmaf(g[o] * ldf(B, o * r + i), ldf(B, o * r + j), acc);
+  acc = block_sum<256>(acc);
+  if (threadIdx.x == 0) {
+    Kg[i * r + j] = acc;
+    Kg[j * r + i] = acc;
+  }
+}
+template <typename T>
+cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float* Kg, cudaStream_t st) {
+  gram_weighted_kernel<T><<<r * r, 256, 0, st>>>(B, out, r, g, Kg);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ closed-form DoRA norm, one thread per row
+template <typename T>
+__global__ void dora_norm_kernel(int64_t out, int r, const float* r0, const float* V, const T* B, const float* Kr,
+                                 const T* m, float s, float eps, float* n_out, float* c) {
+  extern __shared__ float sKr[];
+  for (int i = threadIdx.x; i < r * r; i += blockDim.x) sKr[i] = Kr[i];
+  __syncthreads();
+  const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= out) return;
+  float b[64];
+  for (int j = 0; j < r; ++j) b[j] = ldf(B, o * r + j);
+  float t1 = 0.f, t2 = 0.f;
+  for (int j = 0; j < r; ++j) {
+    t1 = fmaf(V[o * r + j], b[j], t1);
+    float bk = 0.f;
+    for (int l = 0; l < r; ++l) bk = fmaf(b[l], sKr[l * r + j], bk);
+    t2 = fmaf(bk, b[j], t2);
+  }
+  const float q = r0[o] + 2.f * s * t1 + s * s * t2;
+  const float n = fmaxf(sqrtf(fmaxf(q, 0.f)), eps);
+  n_out[o] = n;
+  if (c) c[o] = ldf(m, o) / n;
+}
+template <typename T>
+cudaError_t dora_norm(int64_t out, int r, const float* r0, const float* V, const T* B, const float* Kr, const T* m,
+                      float s, float eps, float* n_out, float* c, cudaStream_t st) {
+  if (out <= 0) return cudaSuccess;
+  dora_norm_kernel<T><<<(unsigned)((out + 127) / 128), 128, r * r * sizeof(float), st>>>(out, r, r0, V, B, Kr, m, s,
+                                                                                         eps, n_out, c);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ c = m / n
+template <typename T>
+__global__ void dora_c_kernel(int64_t out, const T* m, const float* n, float* c) {
+  const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (o < out) c[o] = ldf(m, o) / n[o];
+}
+template <typename T>
+cudaError_t dora_c(int64_t out, const T* m, const float* n, float* c, cudaStream_t st) {
+  if (out <= 0) return cudaSuccess;
+  dora_c_kernel<T><<<(unsigned)((out + 255) / 256), 256, 0, st>>>(out, m, n, c);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ sum of split partials
+template <typename T>
+__global__ void sum_splits_kernel(const float* src, int splits, int64_t n, float* dst_f, T* dst_t) {
+  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= n) return;
+  float a = 0.f;
+  for (int s = 0; s < splits; ++s) a += src[(int64_t)s * n + k];
+  if (dst_f) dst_f[k] = a;
+  if (dst_t) dst_t[k] = from_f<T>(a);
+}
+template <typename T>
+cudaError_t sum_splits(const float* src, int splits, int64_t n, float* dst_f, T* dst_t, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  sum_splits_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, splits, n, dst_f, dst_t);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ DoRA dc -> dm, g, dbias
+template <typename T>
+__global__ void dora_dc_kernel(int64_t out, const float* dot, const float* csum, const T* bias, const float* c,
+                               const float* n, const T* m, float eps, float* g, T* dm, T* dbias) {
+  const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= out) return;
+  const float b = bias ? ldf(bias, o) : 0.f;
+  // P = (Y - bias) / c  =>  sum dY * P = (sum dY*Y - bias * sum dY) / c
+  const float dc = (dot[o] - b * csum[o]) / c[o];
+  const float nn = n[o];
+  dm[o] = from_f<T>(dc / nn);
+  g[o] = nn > eps ? -ldf(m, o) * dc / (2.f * nn * nn * nn) : 0.f;
+  if (dbias) dbias[o] = from_f<T>(csum[o]);
+}
+template <typename T>
+cudaError_t dora_dc(int64_t out, const float* dot, const float* csum, const T* bias, const float* c, const float* n,
+                    const T* m, float eps, float* g, T* dm, T* dbias, cudaStream_t st) {
+  if (out <= 0) return cudaSuccess;
+  dora_dc_kernel<T><<<(unsigned)((out + 255) / 256), 256, 0, st>>>(out, dot, csum, bias, c, n, m, eps, g, dm, dbias);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ out = f * scale[o] * B[o, :]
+template <typename T>
+__global__ void scale_rows_kernel(const T* B, int64_t rows, int r, const float* scale, float f, T* out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= rows * r) return;
+  const int64_t o = i / r;
+  const float sc = scale ? scale[o] : 1.f;
+  out[i] = from_f<T>(f * sc * ldf(B, i));
+}
+template <typename T>
+cudaError_t scale_rows(const T* B, int64_t rows, int r, const float* scale, float f, T* out, cudaStream_t st) {
+  const int64_t n = rows * r;
+  if (n <= 0) return cudaSuccess;
+  scale_rows_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(B, rows, r, scale, f, out);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ gradient assembly
+template <typename T>
+__global__ void finalize_dA_kernel(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg,
+                                   float s2, const T* A, T* dA) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // index into dA [r, in]
+  if (i >= (int64_t)r * in) return;
+  const int j = (int)(i / in);
+  const int64_t k = i - (int64_t)j * in;
+  float a = 0.f;
+  if (PA.p) {
+    float t = 0.f;
+    for (int s = 0; s < PA.splits; ++s) t += PA.p[((int64_t)s * in + k) * PA.ldp + PA.j0 + j];
+    a += sA * t;
+  }
+  if (PW.p) {
+    float t = 0.f;
+    for (int s = 0; s < PW.splits; ++s) t += PW.p[((int64_t)s * in + k) * PW.ldp + PW.j0 + j];
+    a += sW * t;
+  }
+  if (Kg) {
+    float t = 0.f;
+    for (int l = 0; l < r; ++l) t = fmaf(Kg[j * r + l], ldf(A, (int64_t)l * in + k), t);
+    a += s2 * t;
+  }
+  dA[i] = from_f<T>(a);
+}
+template <typename T>
+cudaError_t finalize_dA(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg, float s2,
+                        const T* A, T* dA, cudaStream_t st) {
+  const int64_t n = (int64_t)r * in;
+  if (n <= 0) return cudaSuccess;
+  finalize_dA_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(r, in, PA, sA, PW, sW, Kg, s2, A, dA);
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <typename T>
+__global__ void finalize_dB_kernel(int64_t out, int r, Partial PB, float sB, const float* rs, const float* g,
+                                   const float* V, const T* B, const float* Kr, float s, bool accumulate, T* dB) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // index into dB [out, r]
+  if (i >= out * r) return;
+  const int64_t o = i / r;
+  const int j = (int)(i - o * r);
+  float t = 0.f;
+  if (PB.p)
+    for (int sp = 0; sp < PB.splits; ++sp) t += PB.p[((int64_t)sp * out + o) * PB.ldp + PB.j0 + j];
+  float a = sB * (rs ? rs[o] : 1.f) * t;
+  if (accumulate) a += ldf(dB, i);
+  if (g) {
+    float bk = 0.f;
+    for (int l = 0; l < r; ++l) bk = fmaf(ldf(B, o * r + l), Kr[l * r + j], bk);
+    a += 2.f * s * g[o] * V[o * r + j] + 2.f * s * s * g[o] * bk;
+  }
+  dB[i] = from_f<T>(a);
+}
+template <typename T>
+cudaError_t finalize_dB(int64_t out, int r, Partial PB, float sB, const float* rs, const float* g, const float* V,
+                        const T* B, const float* Kr, float s, bool accumulate, T* dB, cudaStream_t st) {
+  const int64_t n = out * r;
+  if (n <= 0) return cudaSuccess;
+  finalize_dB_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(out, r, PB, sB, rs, g, V, B, Kr, s, accumulate,
+                                                                      dB);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ concat / zero
+__global__ void concat_rows_kernel(const uint4* X1, int64_t n1, const uint4* X2, int64_t n2, uint4* dst) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n1) dst[i] = X1[i];
+  else if (i < n1 + n2) dst[i] = X2[i - n1];
+}
+cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int64_t rows2, int64_t cols, bf16* dst,
+                             cudaStream_t st) {
+  const int64_t n1 = rows1 * cols / 8, n2 = rows2 * cols / 8;
+  if (n1 + n2 <= 0) return cudaSuccess;
+  concat_rows_kernel<<<(unsigned)((n1 + n2 + 255) / 256), 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(X1), n1, reinterpret_cast<const uint4*>(X2), n2, reinterpret_cast<uint4*>(dst));
+  count_launch();
+  return cudaGetLastError();
+}
+cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st) {
+  if (bytes == 0) return cudaSuccess;
+  return cudaMemsetAsync(p, 0, bytes, st);
+}
+
+// ------------------------------------------------------------------ bounded-wait test hook
+__global__ void debug_wait_kernel(uint32_t* err, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing ever arrives on `bar`: the wait must run out and record the error
+    (void)mbar_wait(&bar, 0, timeout_ns, &abort_flag, err, 0x7001);
+  }
+  __syncthreads();
+}
+cudaError_t debug_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t st) {
+  debug_wait_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ explicit instantiations
+#define INST(T)                                                                                                    \
+  template cudaError_t rownorm2<T>(const T*, int64_t, int64_t, float*, cudaStream_t);                               \
+  template cudaError_t gram_rows<T>(const T*, int, int64_t, float*, cudaStream_t);                                  \
+  template cudaError_t gram_weighted<T>(const T*, int64_t, int, const float*, float*, cudaStream_t);                \
+  template cudaError_t dora_norm<T>(int64_t, int, const float*, const float*, const T*, const float*, const T*,     \
+                                    float, float, float*, float*, cudaStream_t);                                    \
+  template cudaError_t dora_c<T>(int64_t, const T*, const float*, float*, cudaStream_t);                            \
+  template cudaError_t sum_splits<T>(const float*, int, int64_t, float*, T*, cudaStream_t);                         \
+  template cudaError_t dora_dc<T>(int64_t, const float*, const float*, const T*, const float*, const float*,        \
+                                  const T*, float, float*, T*, T*, cudaStream_t);                                   \
+  template cudaError_t scale_rows<T>(const T*, int64_t, int, const float*, float, T*, cudaStream_t);                \
+  template cudaError_t finalize_dA<T>(int, int64_t, Partial, float, Partial, float, const float*, float, const T*,  \
+                                      T*, cudaStream_t);                                                            \
+  template cudaError_t finalize_dB<T>(int64_t, int, Partial, float, const float*, const float*, const float*,       \
+                                      const T*, const float*, float, bool, T*, cudaStream_t);
+INST(float)
+INST(bf16)
+#undef INST
+
+}  // namespace lg

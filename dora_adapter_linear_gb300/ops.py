@@ -1,0 +1,126 @@
+"""Convenience layer over the C ABI: allocates outputs and workspaces with PyTorch, then calls
+the entry point of the same name.  PyTorch is used only for device memory and the stream."""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+_WS = {}
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A cached, zero-initialised scratch buffer of at least nbytes (error word cleared)."""
+    key = (str(device), torch.cuda.current_stream(device).cuda_stream)
+    buf = _WS.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _WS[key] = buf
+    return buf
+
+
+def _shape_of(X, W0, A):
+    return L.shape(X.shape[0], X.shape[1], W0.shape[0], A.shape[0], L.dtype_code(X))
+
+
+def lora_linear_fwd(X, W0, A, B, s, bias=None, save_z=True):
+    sh = _shape_of(X, W0, A)
+    Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=X.device)
+    Z = torch.empty(X.shape[0], A.shape[0], dtype=X.dtype, device=X.device) if save_z else None
+    ws = workspace(L.lora_workspace_bytes(L.OP_LINEAR_FWD, sh), X.device)
+    L.lora_linear_fwd(sh, X, W0, A, B, bias, s, Y, Z, ws)
+    return Y, Z
+
+
+def lora_linear_bwd(X, W0, A, B, Z, dY, s, need_dx=True, need_dbias=False):
+    sh = _shape_of(X, W0, A)
+    dX = torch.empty_like(X) if need_dx else None
+    dA = torch.empty_like(A)
+    dB = torch.empty_like(B)
+    dbias = torch.empty(W0.shape[0], dtype=X.dtype, device=X.device) if need_dbias else None
+    ws = workspace(L.lora_workspace_bytes(L.OP_LINEAR_BWD, sh), X.device)
+    L.lora_linear_bwd(sh, X, W0, A, B, Z, dY, s, dX, dA, dB, dbias, ws)
+    return dX, dA, dB, dbias
+
+
+def dora_rownorm2(W0):
+    sh = L.shape(0, W0.shape[1], W0.shape[0], 8, L.dtype_code(W0))
+    r0 = torch.empty(W0.shape[0], dtype=torch.float32, device=W0.device)
+    L.dora_rownorm2(sh, W0, r0)
+    return r0
+
+
+def dora_linear_fwd(X, W0, A, B, m, r0, s, eps=1e-12, bias=None, save_z=True):
+    sh = _shape_of(X, W0, A)
+    dev = X.device
+    Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=dev)
+    Z = torch.empty(X.shape[0], A.shape[0], dtype=X.dtype, device=dev) if save_z else None
+    n = torch.empty(W0.shape[0], dtype=torch.float32, device=dev)
+    V = torch.empty(W0.shape[0], A.shape[0], dtype=torch.float32, device=dev)
+    ws = workspace(L.lora_workspace_bytes(L.OP_DORA_FWD, sh), dev)
+    L.dora_linear_fwd(sh, X, W0, A, B, m, bias, r0, s, eps, Y, Z, n, V, ws)
+    return Y, Z, n, V
+
+
+def dora_linear_bwd(X, W0, A, B, m, bias, Y, Z, n, V, dY, s, eps=1e-12, need_dx=True, need_dbias=False):
+    sh = _shape_of(X, W0, A)
+    dX = torch.empty_like(X) if need_dx else None
+    dA = torch.empty_like(A)
+    dB = torch.empty_like(B)
+    dm = torch.empty_like(m)
+    dbias = torch.empty(W0.shape[0], dtype=X.dtype, device=X.device) if need_dbias else None
+    ws = workspace(L.lora_workspace_bytes(L.OP_DORA_BWD, sh), X.device)
+    L.dora_linear_bwd(sh, X, W0, A, B, m, bias, Y, Z, n, V, dY, s, eps, dX, dA, dB, dm, dbias, ws)
+    return dX, dA, dB, dm, dbias
+
+
+def lora_mlp_swiglu_fwd(X, g, u, d):
+    """g, u, d: dicts with W, A, B, s.  Returns (Y, saved) where saved holds e, u, h, Zgu, Zd."""
+    M, H = X.shape
+    I, r = g["W"].shape[0], g["A"].shape[0]
+    sh = L.mlp_shape(M, H, I, r)
+    dev = X.device
+    e_ = torch.empty(M, I, dtype=X.dtype, device=dev)
+    u_ = torch.empty_like(e_)
+    h_ = torch.empty_like(e_)
+    Zgu = torch.empty(M, 2 * r, dtype=X.dtype, device=dev)
+    Zd = torch.empty(M, r, dtype=X.dtype, device=dev)
+    Y = torch.empty(M, H, dtype=X.dtype, device=dev)
+    ws = workspace(L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, sh), dev)
+    pg, pu, pd = (L.proj(p["W"], p["A"], p["B"], p["s"]) for p in (g, u, d))
+    L.lora_mlp_swiglu_fwd(sh, X, pg, pu, pd, Y, e_, u_, h_, Zgu, Zd, ws)
+    return Y, {"e": e_, "u": u_, "h": h_, "Zgu": Zgu, "Zd": Zd}
+
+
+def lora_mlp_swiglu_bwd(X, g, u, d, saved, dY, need_dx=True):
+    M, H = X.shape
+    I, r = g["W"].shape[0], g["A"].shape[0]
+    sh = L.mlp_shape(M, H, I, r)
+    dX = torch.empty_like(X) if need_dx else None
+    grads = {k: torch.empty_like(v) for k, v in
+             (("dAg", g["A"]), ("dBg", g["B"]), ("dAu", u["A"]), ("dBu", u["B"]), ("dAd", d["A"]), ("dBd", d["B"]))}
+    ws = workspace(L.lora_mlp_workspace_bytes(L.OP_MLP_BWD, sh), X.device)
+    pg, pu, pd = (L.proj(p["W"], p["A"], p["B"], p["s"]) for p in (g, u, d))
+    L.lora_mlp_swiglu_bwd(sh, X, pg, pu, pd, saved["e"], saved["u"], saved["h"], saved["Zgu"], saved["Zd"], dY, dX,
+                          grads["dAg"], grads["dBg"], grads["dAu"], grads["dBu"], grads["dAd"], grads["dBd"], ws)
+    grads["dX"] = dX
+    return grads
+
+
+def w8a8_quantize_rows(X, A=None):
+    rows, cols = X.shape
+    Xq = torch.empty(rows, cols, dtype=torch.int8, device=X.device)
+    sx = torch.empty(rows, dtype=torch.float32, device=X.device)
+    Z = torch.empty(rows, A.shape[0], dtype=X.dtype, device=X.device) if A is not None else None
+    L.w8a8_quantize_rows(rows, cols, X, Xq, sx, A, 0 if A is None else A.shape[0], Z)
+    return Xq, sx, Z
+
+
+def w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, s, bias=None, want_acc=False, want_y=True):
+    M, d_in = Xq.shape
+    d_out = Wq.shape[0]
+    r = 0 if Z is None else Z.shape[1]
+    Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=Xq.device) if want_y else None
+    acc = torch.empty(M, d_out, dtype=torch.int32, device=Xq.device) if want_acc else None
+    L.w8a8_lora_fwd(M, d_in, d_out, r, Xq, sx, Wq, sw, Z, B, s, bias, Y, acc)
+    return Y, acc

@@ -1,0 +1,251 @@
+/*
+ * lora_gb300.h -- C ABI of the fused low-rank-adapted linear layer for GB300 (sm_103a).
+ *
+ * The layer:  y = X W0^T + s (X A^T) B^T (+ bias)   forward and backward, computed
+ * without ever forming the dense update dW = B A or its gradient; the DoRA row-scale
+ * variant with its closed-form norm; a SwiGLU MLP built from three such projections;
+ * and an int8 (W8A8) base weight with a per-row dequant scale and a LoRA epilogue.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or retains them.  Tensors are row-major and contiguous:
+ *      X [M, d_in], W0 [d_out, d_in], A [r, d_in] (down), B [d_out, r] (up),
+ *      bias [d_out], m [d_out], Y / dY [M, d_out], Z = X A^T [M, r].
+ *  - dtype LORA_BF16: bf16 storage, fp32 accumulation, bf16 outputs/gradients.
+ *    dtype LORA_F32: fp32 storage, fp32 FMA accumulation (no TF32), fp32 outputs.
+ *  - s is the complete scale strength * alpha / r (the caller folds strength in).
+ *  - Every pointer must be 16-byte aligned; d_in, d_out must be multiples of 8,
+ *    r a multiple of 8 with 8 <= r <= 64 (LORA_BF16) or 1 <= r <= 64 (LORA_F32).
+ *    M >= 0 (M == 0 is a no-op).  Violations return an error before anything is
+ *    launched and leave every output untouched.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  A returned LORA_OK means "validated and launched", not "finished".
+ *  - `ws` is caller-allocated device scratch of at least *_workspace_bytes() bytes,
+ *    256-byte aligned.  Its first 256 bytes hold a device error word that kernels set
+ *    (never clear) when a bounded wait runs out; clear it once with
+ *    lora_clear_device_error() before first use and read it with
+ *    lora_check_device_error().  Two calls that share one workspace must not overlap
+ *    on the GPU (same stream, or ordered by events).
+ *  - Where the pages leave a step open, the plain reading is taken: eps is a floor on
+ *    the DoRA row norm, n = max(sqrt(max(q, 0)), eps); strength 0 returns the frozen
+ *    base layer X W0^T + bias (also for DoRA).
+ *
+ * Citations name the source page by its title and the section of it that defines the
+ * operation.
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_ERR_INVALID_ARG = 1,     /* null required pointer, bad shape, bad dtype, non-finite s */
+    LORA_ERR_UNSUPPORTED = 2,     /* valid request this library does not implement (e.g. r > 64) */
+    LORA_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned (ws: 256-byte) */
+    LORA_ERR_WORKSPACE = 4,       /* ws is NULL or ws_bytes is below the required size */
+    LORA_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed (launch, tensor map) */
+    LORA_ERR_DEVICE_TIMEOUT = 6   /* a kernel's bounded wait ran out (read from the error word) */
+} lora_status;
+
+typedef enum { LORA_F32 = 0, LORA_BF16 = 1 } lora_dtype;
+
+/* Operation ids for lora_workspace_bytes(). */
+typedef enum {
+    LORA_OP_LINEAR_FWD = 0, LORA_OP_LINEAR_BWD = 1,
+    LORA_OP_DORA_FWD = 2, LORA_OP_DORA_BWD = 3,
+    LORA_OP_MLP_FWD = 4, LORA_OP_MLP_BWD = 5
+} lora_op;
+
+typedef struct {
+    int64_t M, d_in, d_out, r;
+    int32_t dtype;                /* lora_dtype */
+} lora_shape;
+
+/* SwiGLU MLP: X [M, H]; gate/up project H -> I, down projects I -> H; one rank r. */
+typedef struct {
+    int64_t M, H, I, r;
+    int32_t dtype;                /* LORA_BF16 only */
+} lora_mlp_shape;
+
+/* One adapted projection of the MLP: W [n_out, n_in], A [r, n_in], B [n_out, r], scale s. */
+typedef struct {
+    const void* W;
+    const void* A;
+    const void* B;
+    float s;
+} lora_proj;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* lora_status_string(int status);
+
+/* Library ABI version (increments on any signature change). */
+int lora_abi_version(void);
+
+/* Bytes of workspace `op` needs for `sh` (LORA_OP_LINEAR_* and LORA_OP_DORA_*). 0 on bad input. */
+size_t lora_workspace_bytes(int op, const lora_shape* sh);
+
+/* Bytes of workspace the MLP entry points need (op = LORA_OP_MLP_FWD / LORA_OP_MLP_BWD). */
+size_t lora_mlp_workspace_bytes(int op, const lora_mlp_shape* sh);
+
+/* Zero the device error word at the head of `ws` (asynchronous on `stream`). */
+lora_status lora_clear_device_error(void* ws, void* stream);
+
+/* Synchronise `stream`, then read the device error word of `ws`:
+ * LORA_OK if clear, LORA_ERR_DEVICE_TIMEOUT if a kernel recorded a timed-out wait. */
+lora_status lora_check_device_error(const void* ws, void* stream);
+
+/* ---------------------------------------------------------------- LoRA linear
+ * Forward:  Y = X W0^T + s (X A^T) B^T (+ bias).
+ * "LoRA/DoRA fast forward: no weight materialization" (stable-audio-3 #69), What
+ * section: the low-rank update is folded into the data GEMMs; "How Unsloth's FastLoRA
+ * Kernel Differs from Standard LoRA Implementations", Fused Forward Pass Architecture.
+ *   bias:   [d_out] or NULL.
+ *   Y:      [M, d_out] output.
+ *   Z_save: [M, r] output or NULL; receives X A^T (unscaled) for the backward.
+ */
+lora_status lora_linear_fwd(const lora_shape* sh, const void* X, const void* W0, const void* A,
+                            const void* B, const void* bias, float s, void* Y, void* Z_save,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of lora_linear_fwd with W0 frozen:
+ *   dX = dY W0 + s (dY B) A,  dA = s (dY B)^T X,  dB = s dY^T Z,  dbias = colsum(dY).
+ * "How Unsloth's FastLoRA Kernel Differs ...", Custom Backward Pass Implementation (the
+ * scale is folded into the gradient products); "nunchaku-style kernel fusion" (OneTrainer
+ * #1680), commit reworking the 8-bit matmuls: the LoRA dgrad folds into the backward and
+ * neither direction builds an (M, d_out) intermediate.
+ *   Z_saved: [M, r] (X A^T from the forward) or NULL to recompute it.
+ *   dX [M, d_in] or NULL (skipped); dA [r, d_in]; dB [d_out, r]; dbias [d_out] or NULL.
+ */
+lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0, const void* A,
+                            const void* B, const void* Z_saved, const void* dY, float s,
+                            void* dX, void* dA, void* dB, void* dbias,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- DoRA (rows)
+ * r0[o] = sum_k W0[o,k]^2 in fp32: the cached per-layer constant of the closed-form norm.
+ * "LoRA/DoRA fast forward ...", commit message (cached rowsum(W0^2) constant) and What
+ * section (the cached norm constant is a per-layer vector).  r0: [d_out] fp32 output.
+ */
+lora_status dora_rownorm2(const lora_shape* sh, const void* W0, float* r0, void* stream);
+
+/* Forward:  n = max(sqrt(q), eps) with the closed form
+ *   q = r0 + 2s rowsum((W0 A^T) o B) + s^2 rowsum((B (A A^T)) o B),
+ *   Y = (m / n)[o] * (X W0^T + s (X A^T) B^T) + bias   (bias added after the row scale).
+ * "LoRA/DoRA fast forward ...", What section (dora-rows is a row scale of the base +
+ * low-rank output; norm in closed form) and Fidelity section (1e-12 eps, un-scaled bias).
+ *   m [d_out], bias [d_out] or NULL, r0 [d_out] fp32 from dora_rownorm2.
+ *   Y [M, d_out]; Z_save [M, r] or NULL; n_save [d_out] fp32 (required, for the backward);
+ *   V_save [d_out, r] fp32 (required): W0 A^T, reused by the backward's norm gradient.
+ */
+lora_status dora_linear_fwd(const lora_shape* sh, const void* X, const void* W0, const void* A,
+                            const void* B, const void* m, const void* bias, const float* r0,
+                            float s, float eps, void* Y, void* Z_save, float* n_save, float* V_save,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of dora_linear_fwd, the norm kept in the graph (no detach):
+ *   dc = colsum(dY o P) with P = (Y - bias) / c recovered from the saved output, c = m/n;
+ *   dm = dc / n;  g = -m dc / (2 n^3) (0 where n was clamped at eps);
+ *   dX = (dY o c) W0 + s ((dY o c) B) A;
+ *   dA = s ((dY o c) B)^T X + 2s (g o B)^T W0 + 2s^2 (B^T diag(g) B) A;
+ *   dB = s c o (dY^T Z) + 2s g o V + 2s^2 g o (B (A A^T)).
+ * "LoRA/DoRA fast forward ...", Fidelity section (norm stays in the autograd graph;
+ * gradients for A, B and the magnitude).
+ *   Y, Z_saved (or NULL to recompute), n_saved and V_saved from the forward.
+ *   dX [M, d_in] or NULL; dA [r, d_in]; dB [d_out, r]; dm [d_out]; dbias [d_out] or NULL.
+ */
+lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0, const void* A,
+                            const void* B, const void* m, const void* bias, const void* Y,
+                            const void* Z_saved, const float* n_saved, const float* V_saved,
+                            const void* dY, float s, float eps,
+                            void* dX, void* dA, void* dB, void* dm, void* dbias,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- LoRA SwiGLU MLP
+ * e = X Wg^T + sg (X Ag^T) Bg^T,  u = X Wu^T + su (X Au^T) Bu^T,  h = silu(e) * u,
+ * Y = h Wd^T + sd (h Ad^T) Bd^T.
+ * "How Unsloth's FastLoRA Kernel Differs ...", Fused Forward Pass Architecture (LoRA_MLP)
+ * and Activation Function Fusion (SwiGLU computed with the LoRA outputs).
+ *   gate, up: W [I, H], A [r, H], B [I, r];  down: W [H, I], A [r, I], B [H, r].
+ *   Y [M, H]; e_save, u_save, h_save [M, I] (required: the backward reads them);
+ *   Zgu_save [M, 2r] = [X Ag^T | X Au^T] and Zd_save [M, r] = h Ad^T (required).
+ */
+lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const lora_proj* gate,
+                                const lora_proj* up, const lora_proj* down, void* Y,
+                                void* e_save, void* u_save, void* h_save, void* Zgu_save,
+                                void* Zd_save, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of lora_mlp_swiglu_fwd (base weights frozen):
+ *   dh = dY Wd + sd (dY Bd) Ad,  de = dh u silu'(e),  du = dh silu(e),
+ *   dX = de Wg + du Wu + sg (de Bg) Ag + su (du Bu) Au,
+ *   dA* = s* (d* B*)^T (input),  dB* = s* (d*)^T Z*.
+ * "How Unsloth's FastLoRA Kernel Differs ...", Custom Backward Pass Implementation.
+ *   dX [M, H] or NULL; dAg, dAu [r, H]; dBg, dBu [I, r]; dAd [r, I]; dBd [H, r].
+ */
+lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const lora_proj* gate,
+                                const lora_proj* up, const lora_proj* down,
+                                const void* e_saved, const void* u_saved, const void* h_saved,
+                                const void* Zgu_saved, const void* Zd_saved, const void* dY,
+                                void* dX, void* dAg, void* dBg, void* dAu, void* dBu,
+                                void* dAd, void* dBd, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- W8A8 + LoRA epilogue
+ * Per-row symmetric int8 quantisation of a bf16 matrix, decided in fp32:
+ *   scale[i] = absmax(X[i, :]) / 127,  Xq = clamp(rint_half_even(X / scale), -127, 127),
+ *   an all-zero row gives scale 0 and codes 0.  Optionally also Z = X A^T (bf16) from the
+ *   unquantised X in the same call.
+ * "nunchaku-style kernel fusion" (OneTrainer #1680), commit reworking the 8-bit matmuls
+ * (axis-wise quantisation for the 8-bit matmul; the autograd Function owns the
+ * down-projection).
+ *   X [rows, cols] bf16; Xq [rows, cols] int8; sx [rows] fp32;
+ *   A [r, cols] bf16 and Z [rows, r] bf16, both NULL or both non-NULL (then r in 8..64).
+ */
+lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t* Xq, float* sx,
+                               const void* A, int64_t r, void* Z, void* stream);
+
+/* Y = float(acc) * sx[i] * sw[o] + s * (Z B^T)[i, o] (+ bias), acc = Xq Wq^T exact in int32.
+ * "nunchaku-style kernel fusion" (OneTrainer #1680): commit reworking the 8-bit matmuls
+ * (epilogues: raw product, per-row dequant, dequant plus rank-tiled low-rank update; no
+ * int32 (M, d_out) materialisation) and commit unifying the five entry points
+ * (mm_8bit(a, b, out_dtype, scale_m, scale_n, lora_xd, lora_up)).
+ *   Xq [M, d_in] int8, sx [M] fp32, Wq [d_out, d_in] int8, sw [d_out] fp32,
+ *   Z [M, r] bf16 ("lora_xd") and B [d_out, r] bf16 ("lora_up"): both NULL (no LoRA) or both set,
+ *   bias [d_out] bf16 or NULL, Y [M, d_out] bf16 (or NULL when only acc_out is wanted),
+ *   acc_out [M, d_out] int32 or NULL: the raw-product epilogue.  d_in multiple of 32.
+ */
+lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq,
+                          const float* sx, const int8_t* Wq, const float* sw, const void* Z,
+                          const void* B, float s, const void* bias, void* Y, int32_t* acc_out,
+                          void* stream);
+
+/* ---------------------------------------------------------------- tracing
+ * Number of kernels this library has launched since it was loaded (host-side count of
+ * launch calls; memsets issued through the CUDA runtime are not counted). */
+uint64_t lora_launch_count(void);
+
+/* Enable (on != 0) or disable CUDA-event timing of the tcgen05 GEMM launches.  While enabled,
+ * each GEMM launch is bracketed by two events recorded on its stream (a few microseconds of
+ * host overhead per launch; the device work is unchanged). */
+lora_status lora_prof_enable(int on);
+
+/* Summed device time (ms), number of launches and algorithmic flops (base contraction plus
+ * rank-r tail, 2*M*N*K) of the GEMM launches recorded since the last reset; waits for the
+ * recorded events.  Any output pointer may be NULL.  reset != 0 clears the record. */
+lora_status lora_prof_gemm(double* ms, int64_t* launches, double* flops, int reset);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on an mbarrier
+ * that nothing ever arrives on, with a limit of `timeout_us` microseconds; the kernel then
+ * records LORA_ERR_DEVICE_TIMEOUT in the error word of `ws` and returns.  It faults and
+ * hangs nothing.  Read the result with lora_check_device_error(). */
+lora_status lora_debug_wait_timeout(void* ws, uint32_t timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LORA_GB300_H */

@@ -1,0 +1,89 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every symbol the header
+declares, and rejects bad arguments before launching anything."""
+import ctypes
+import re
+
+import pytest
+
+from dora_adapter_linear_gb300 import _lib as L
+from dora_adapter_linear_gb300.build import build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return L._lib()
+
+
+def header_functions():
+    text = open(L.HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for must in ("lora_linear_fwd", "lora_linear_bwd", "dora_linear_fwd", "dora_linear_bwd", "dora_rownorm2",
+                 "lora_mlp_swiglu_fwd", "lora_mlp_swiglu_bwd", "w8a8_lora_fwd", "w8a8_quantize_rows"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in header_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(header_functions()) == set(L._SIGS), "binding signatures must cover the header exactly"
+
+
+def test_status_strings(lib):
+    assert L.lora_status_string(0) == "ok"
+    assert "workspace" in L.lora_status_string(4)
+    assert L.lora_status_string(99) == "unknown status"
+    assert L.lora_abi_version() == 1
+
+
+def test_workspace_bytes_rejects_bad_shapes(lib):
+    assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 8, L.LORA_F32)) > 0
+    assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 250, 256, 8, L.LORA_F32)) == 0   # in % 8
+    assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 65, L.LORA_BF16)) == 0  # r > 64
+    assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 12, L.LORA_BF16)) == 0  # r % 8 (bf16)
+    assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 8, 7)) == 0             # dtype
+    assert L.lora_workspace_bytes(99, L.shape(64, 256, 256, 8, L.LORA_F32)) == 0
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16)) > 0
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 40)) == 0          # r > 32
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, L.LORA_F32)) == 0
+
+
+def test_entry_points_validate_before_launch(lib):
+    """Null / misaligned pointers and bad scalars return an error code; nothing is launched."""
+    sh = L.shape(64, 256, 256, 8, L.LORA_F32)
+    fake = ctypes.c_void_p(1 << 20)            # never dereferenced: validation fails first
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    r = lib.lora_linear_fwd(ctypes.byref(sh), None, fake, fake, fake, None, 1.0, fake, None, fake, 1 << 20, None)
+    assert r == 1  # INVALID_ARG (X is NULL)
+    r = lib.lora_linear_fwd(ctypes.byref(sh), odd, fake, fake, fake, None, 1.0, fake, None, fake, 1 << 20, None)
+    assert r == 3  # MISALIGNED
+    r = lib.lora_linear_fwd(ctypes.byref(sh), fake, fake, fake, fake, None, float("nan"), fake, None, fake, 1 << 20,
+                            None)
+    assert r == 1  # non-finite s
+    r = lib.lora_linear_fwd(ctypes.byref(sh), fake, fake, fake, fake, None, 1.0, fake, None, fake, 16, None)
+    assert r == 4  # workspace too small
+    r = lib.lora_linear_fwd(ctypes.byref(sh), fake, fake, fake, fake, None, 1.0, fake, None, None, 1 << 30, None)
+    assert r == 4  # workspace missing
+    bad = L.shape(64, 256, 256, 0, L.LORA_F32)
+    r = lib.lora_linear_bwd(ctypes.byref(bad), fake, fake, fake, fake, None, fake, 1.0, None, fake, fake, None,
+                            fake, 1 << 20, None)
+    assert r == 1
+    r = lib.dora_linear_fwd(ctypes.byref(sh), fake, fake, fake, fake, None, None, fake, 1.0, 1e-12, fake, None, fake,
+                            fake, fake, 1 << 20, None)
+    assert r == 1  # m is NULL
+    r = lib.w8a8_lora_fwd(64, 100, 64, 16, fake, fake, fake, fake, None, None, 1.0, None, fake, None, None)
+    assert r == 2  # d_in not a multiple of 32
+    r = lib.w8a8_lora_fwd(64, 128, 64, 16, fake, fake, fake, fake, fake, None, 1.0, None, fake, None, None)
+    assert r == 1  # Z without B
+    r = lib.w8a8_quantize_rows(4, 12, fake, fake, fake, None, 0, None, None)
+    assert r == 2  # cols % 8
+    mlp = L.mlp_shape(64, 128, 256, 16)
+    pr = L.LoraProj(1 << 20, 1 << 20, 1 << 20, 1.0)
+    r = lib.lora_mlp_swiglu_fwd(ctypes.byref(mlp), fake, ctypes.byref(pr), None, ctypes.byref(pr), fake, fake, fake,
+                                fake, fake, fake, fake, 1 << 30, None)
+    assert r == 1  # up projection missing

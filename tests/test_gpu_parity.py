@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the fp64 CPU oracle on the
+same seeded inputs.  Small cases span several tiles and ragged tails in M, N and K; the
+full-size workloads are checked on sampled rows/columns that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import datagen as D
+import oracle as O
+from parity import assert_close, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from dora_adapter_linear_gb300.build import build
+    build()
+    from dora_adapter_linear_gb300 import ops as _ops
+    return _ops
+
+
+def gpu(t):
+    return None if t is None else t.to(DEV).contiguous()
+
+
+def f64(t):
+    return None if t is None else to64(t)
+
+
+def lin_inputs(name, **kw):
+    case = D.scaled(D.WORKLOADS[name], **kw)
+    t = D.make_linear(case)
+    return case, t, {k: gpu(v) for k, v in t.items()}
+
+
+# ---------------------------------------------------------------------------- infrastructure
+def test_bounded_wait_reports_timeout(ops):
+    from dora_adapter_linear_gb300 import _lib as L
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    assert L.lora_check_device_error(ws) == 0
+    L.lora_debug_wait_timeout(ws, 2000)  # 2 ms limit on a barrier nothing arrives on
+    assert L.lora_check_device_error(ws) == 6
+    L.lora_clear_device_error(ws)
+    assert L.lora_check_device_error(ws) == 0
+
+
+# ---------------------------------------------------------------------------- LoRA, bf16
+SMALL = dict(M=300, d_in=328, d_out=264)
+
+
+def test_base_gemm_kmajor_strength0(ops):
+    case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=16)
+    Y, _ = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], 0.0, save_z=False)
+    ref = O.lora_linear_fwd(f64(t["X"]), f64(t["W0"]), f64(t["A"]), f64(t["B"]), 0.0)
+    assert_close(Y, ref, "bf16", "X W0^T")
+
+
+def test_base_gemm_mnmajor_strength0(ops):
+    case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=16)
+    dX, dA, dB, _ = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], None, g["dY"], 0.0)
+    assert_close(dX, f64(t["dY"]) @ f64(t["W0"]), "bf16", "dY W0")
+    assert not dA.any() and not dB.any()
+
+
+@pytest.mark.parametrize("r", [8, 16, 32, 64])
+@pytest.mark.parametrize("bias", [False, True])
+def test_lora_fwd_bf16(ops, r, bias):
+    case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=r, bias=bias)
+    Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s, g["bias"])
+    X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
+    assert_close(Y, O.lora_linear_fwd(X, W0, A, B, case.s, f64(t["bias"])), "bf16", "Y")
+    assert_close(Z, X @ A.T, "bf16", "Z")
+
+
+@pytest.mark.parametrize("r", [8, 16, 32, 64])
+def test_lora_bwd_bf16(ops, r):
+    case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=r)
+    _, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s)
+    dX, dA, dB, dbias = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s, need_dbias=True)
+    rX, rA, rB, rb = O.lora_linear_bwd(*(f64(t[k]) for k in ("X", "W0", "A", "B")), case.s, f64(t["dY"]))
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dB, rB, "bf16", "dB")
+    assert_close(dbias, rb[None, :], "bf16", "dbias")
+
+
+def test_lora_bwd_recomputes_z(ops):
+    case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=16)
+    dX, dA, dB, _ = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], None, g["dY"], case.s)
+    rX, rA, rB, _ = O.lora_linear_bwd(*(f64(t[k]) for k in ("X", "W0", "A", "B")), case.s, f64(t["dY"]))
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dB, rB, "bf16", "dB")
+
+
+def test_lora_strength0_bit_exact_vs_zero_adapter(ops):
+    """Strength 0 takes the base-only path; a zero up-projection takes the fused path: same bits."""
+    case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=16)
+    Y0, _ = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], 0.0)
+    Yb, _ = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], torch.zeros_like(g["B"]), case.s)
+    assert torch.equal(Y0, Yb)
+
+
+@pytest.mark.parametrize("M", [1, 127, 129])
+def test_lora_ragged_m(ops, M):
+    case, t, g = lin_inputs("lora_4096_bf16", M=M, d_in=136, d_out=520, r=16, bias=True)
+    Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s, g["bias"])
+    X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
+    assert_close(Y, O.lora_linear_fwd(X, W0, A, B, case.s, f64(t["bias"])), "bf16", "Y")
+    dX, dA, dB, _ = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
+    rX, rA, rB, _ = O.lora_linear_bwd(X, W0, A, B, case.s, f64(t["dY"]))
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dB, rB, "bf16", "dB")
+
+
+def test_m_zero_is_noop(ops):
+    case, t, g = lin_inputs("lora_4096_bf16", M=0, d_in=64, d_out=64, r=8)
+    Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s)
+    assert Y.shape == (0, 64)
+    dX, dA, dB, _ = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
+    assert not dA.any() and not dB.any()
+
+
+# ---------------------------------------------------------------------------- LoRA, fp32 (tiny workload)
+def test_lora_tiny_f32(ops):
+    case, t, g = lin_inputs("lora_tiny_f32")
+    Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s, g["bias"])
+    X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
+    assert_close(Y, O.lora_linear_fwd(X, W0, A, B, case.s, f64(t["bias"])), "f32", "Y")
+    dX, dA, dB, dbias = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s, need_dbias=True)
+    rX, rA, rB, rb = O.lora_linear_bwd(X, W0, A, B, case.s, f64(t["dY"]))
+    for got, ref, nm in ((dX, rX, "dX"), (dA, rA, "dA"), (dB, rB, "dB"), (dbias, rb, "dbias")):
+        assert_close(got, ref, "f32", nm)
+
+
+# ---------------------------------------------------------------------------- DoRA
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_dora_fwd_bwd(ops, dtype):
+    case, t, g = lin_inputs("dora_4096x11008_bf16", M=300, d_in=328, d_out=520, r=32, dtype=dtype)
+    r0 = ops.dora_rownorm2(g["W0"])
+    np.testing.assert_allclose(to64(r0), O.dora_rownorm2(f64(t["W0"])), rtol=1e-5)
+    Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps, g["bias"])
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    rY, rn = O.dora_linear_fwd(X, W0, A, B, m, case.s, case.eps, bias)
+    assert_close(Y, rY, dtype, "Y")
+    np.testing.assert_allclose(to64(n), rn, rtol=1e-4)
+    dX, dA, dB, dm, dbias = ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V,
+                                                g["dY"], case.s, case.eps, need_dbias=True)
+    rX, rA, rB, rm, rb = O.dora_linear_bwd(X, W0, A, B, m, case.s, dY, case.eps)
+    for got, ref, nm in ((dX, rX, "dX"), (dA, rA, "dA"), (dB, rB, "dB"), (dm, rm[None], "dm"),
+                         (dbias, rb[None], "dbias")):
+        assert_close(got, ref, dtype, nm)
+
+
+def test_dora_init_is_plain_linear(ops):
+    case, t, g = lin_inputs("dora_4096x11008_bf16", M=256, d_in=256, d_out=264, r=16)
+    g["B"].zero_()
+    m = torch.linalg.vector_norm(g["W0"].float(), dim=1).to(torch.bfloat16)
+    r0 = ops.dora_rownorm2(g["W0"])
+    Y, *_ = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], m, r0, case.s, case.eps, g["bias"])
+    assert_close(Y, f64(t["X"]) @ f64(t["W0"]).T + f64(t["bias"]), "bf16", "Y")
+
+
+def test_dora_strength0_is_frozen_base_bits(ops):
+    case, t, g = lin_inputs("dora_4096x11008_bf16", M=200, d_in=136, d_out=264, r=16)
+    r0 = ops.dora_rownorm2(g["W0"])
+    Yd, *_ = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, 0.0, case.eps, g["bias"])
+    Yl, _ = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], 0.0, g["bias"])
+    assert torch.equal(Yd, Yl)
+
+
+# ---------------------------------------------------------------------------- SwiGLU MLP
+def mlp_inputs(**kw):
+    case = D.scaled(D.WORKLOADS["mlp_swiglu_4096x14336_bf16"], **kw)
+    t = D.make_mlp(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
+    return case, t, g, P
+
+
+def _mlp_args64(t, s):
+    return (f64(t["X"]), f64(t["Wg"]), f64(t["Ag"]), f64(t["Bg"]), s, f64(t["Wu"]), f64(t["Au"]), f64(t["Bu"]), s,
+            f64(t["Wd"]), f64(t["Ad"]), f64(t["Bd"]), s)
+
+
+@pytest.mark.parametrize("I", [200, 256])
+def test_mlp_fwd_bwd(ops, I):
+    case, t, g, P = mlp_inputs(M=300, H=136, I=I, r=16, alpha=24.0)
+    Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
+    args = _mlp_args64(t, case.s)
+    ry, re, ru, rh = O.mlp_swiglu_fwd(*args)
+    assert_close(saved["e"], re, "bf16", "e")
+    assert_close(saved["u"], ru, "bf16", "u")
+    assert_close(saved["h"], rh, "bf16", "h")
+    assert_close(Y, ry, "bf16", "y")
+    gr = ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
+    ref = O.mlp_swiglu_bwd(*args, f64(t["dY"]))
+    for k in ("dX", "dAg", "dBg", "dAu", "dBu", "dAd", "dBd"):
+        assert_close(gr[k], ref[k], "bf16", k)
+
+
+# ---------------------------------------------------------------------------- W8A8
+def w8_inputs(**kw):
+    case = D.scaled(D.WORKLOADS["w8a8_lora_3072"], **kw)
+    t = D.make_w8a8(case)
+    Wq, sw = O.quantize_rows(t["W0"].numpy())      # offline weight quantisation (shared bytes)
+    Xq, sx = O.quantize_rows(t["X"].float().numpy())
+    return case, t, Wq, sw, Xq, sx
+
+
+def test_w8a8_quantize_bit_exact(ops):
+    case, t, *_ = w8_inputs(M=300, d_in=352, d_out=264)
+    X = gpu(t["X"])
+    X[7].zero_()                                   # an all-zero row
+    Xq, sx, Z = ops.w8a8_quantize_rows(X, gpu(t["A"]))
+    rq, rs = O.quantize_rows(X.float().cpu().numpy())
+    np.testing.assert_array_equal(Xq.cpu().numpy(), rq)
+    np.testing.assert_array_equal(sx.cpu().numpy(), rs)
+    assert_close(Z, f64(X.cpu()) @ f64(t["A"]).T, "bf16", "Z")
+
+
+@pytest.mark.parametrize("bias", [False, True])
+def test_w8a8_acc_bit_exact_and_epilogue(ops, bias):
+    case, t, Wq, sw, Xq, sx = w8_inputs(M=300, d_in=352, d_out=264, bias=bias)
+    Z = (t["X"].double() @ t["A"].double().T).to(torch.bfloat16)
+    Y, acc = ops.w8a8_lora_fwd(gpu(torch.from_numpy(Xq)), gpu(torch.from_numpy(sx)), gpu(torch.from_numpy(Wq)),
+                               gpu(torch.from_numpy(sw)), gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]), want_acc=True)
+    ry, racc = O.w8a8_lora_fwd(Xq, sx, Wq, sw, f64(Z), f64(t["B"]), case.s, f64(t["bias"]))
+    np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), racc)
+    assert_close(Y, ry, "bf16", "Y")
+
+
+def test_w8a8_extreme_codes_exact(ops):
+    """All-(+-127) operands: the worst-case |acc| = d_in * 127^2 stays exact in int32."""
+    M, K, N = 130, 3072, 136
+    Xq = np.full((M, K), 127, np.int8)
+    Xq[1::2] = -127
+    Wq = np.full((N, K), -127, np.int8)
+    Y, acc = ops.w8a8_lora_fwd(gpu(torch.from_numpy(Xq)), None, gpu(torch.from_numpy(Wq)), None, None, None, 0.0,
+                               want_acc=True, want_y=False)
+    np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), O.int8_accumulate(Xq, Wq))
