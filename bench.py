@@ -54,6 +54,57 @@ def mlp_flops(M, H, I, r):
 
 
 # ----------------------------------------------------------------------------- clocks
+class NvmlSampler:
+    """Reads SM clock, max clock, power and clock-event reasons through NVML every ~2 ms.
+    Read-only: nothing on the GPU is changed."""
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.samples, self.ok, self._stop = [], False, False
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            import torch
+            pr = torch.cuda.get_device_properties(cuda_index)
+            self.h = ctypes.c_void_p()
+            bus = f"{getattr(pr, 'pci_domain_id', 0):08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+            if self.nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h)) != 0:
+                if self.nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h)) != 0:
+                    return
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def start(self):
+        if self.ok:
+            threading.Thread(target=self._run, daemon=True).start()
+
+    def _run(self):
+        import ctypes
+        mhz, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop:
+            self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz))
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw))
+            self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs))
+            self.samples.append((time.time(), mhz.value, mx.value, mw.value / 1e3, rs.value))
+            time.sleep(0.002)
+
+    def stop(self):
+        self._stop = True
+
+    def summary(self, t0, t1):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not win:
+            return None
+        reasons = sorted({nm for s in win for b, nm in self.BITS.items() if s[4] & b})
+        return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": max(s[2] for s in win),
+                "reasons": reasons, "samples": len(win), "window": "timed (NVML, 2 ms period)",
+                "power_w_max": max(s[3] for s in win)}
+
+
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -257,6 +308,8 @@ def headline(args, L, ops, dist, world, peaks):
     fwd_fl, bwd_fl = lora_flops(M, d_in, d_out, r)
     clk = ClockSampler(torch.cuda.current_device())
     clk.start()
+    nv = NvmlSampler(torch.cuda.current_device())
+    nv.start()
     time.sleep(0.3)
     L.lora_prof_gemm(reset=True)
     n0 = L.lora_launch_count()
@@ -269,7 +322,8 @@ def headline(args, L, ops, dist, world, peaks):
     roof = gemm_roofline(L, peaks, ms, sustained=False)
     if roof is not None:
         roof["share_of_step"] = round(roof["avg_launch_ms"] * 2 / ms, 3)
-    clocks = clk.summary(t0, t1)
+    nv.stop()
+    clocks = nv.summary(t0, t1) or clk.summary(t0, t1)
     clk.stop()
     for ws in (wsf, wsb):
         if L.lora_check_device_error(ws) != 0:
@@ -366,6 +420,9 @@ def extra_workloads(args, L, ops, peaks):
         Xq, sx, Z = ops.w8a8_quantize_rows(X, A)
         ops.w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, case.s)
     ms, _, _ = timed(w8_step, steps, warm)
+    for buf in ops._WS.values():
+        if L.lora_check_device_error(buf) != 0:
+            raise RuntimeError("a kernel recorded a timed-out wait in the workload breakdown")
     ops_int8 = 2 * case.M * case.d_in * case.d_out
     lora_fl = 2 * case.M * case.r * (case.d_in + case.d_out)
     out["w8a8_lora_3072"] = {"ms_per_step": ms, "int8_tops": ops_int8 / (ms * 1e-3) / 1e12,

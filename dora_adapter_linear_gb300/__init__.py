@@ -6,13 +6,7 @@ workspaces with PyTorch before calling it.  There is no CPU or library fallback:
 library is missing, every call raises.
 """
 from . import _lib  # noqa: F401
+from . import ops  # noqa: F401
 from ._lib import LoraError, lora_abi_version, lora_status_string  # noqa: F401
 
 __all__ = ["_lib", "ops", "LoraError", "lora_abi_version", "lora_status_string"]
-
-
-def __getattr__(name):
-    if name == "ops":
-        from . import ops
-        return ops
-    raise AttributeError(name)

@@ -45,6 +45,11 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
   do {                                           \
     if ((p) == nullptr) return LORA_ERR_INVALID_ARG; \
   } while (0)
+// tensors whose leading extent is the token count may be NULL when there are no tokens
+#define REQM(M, p)                                                \
+  do {                                                            \
+    if ((M) > 0 && (p) == nullptr) return LORA_ERR_INVALID_ARG;   \
+  } while (0)
 #define ALN(p)                                   \
   do {                                           \
     if ((p) != nullptr && !al16(p)) return LORA_ERR_MISALIGNED; \
@@ -398,7 +403,7 @@ lora_status lora_linear_fwd(const lora_shape* sh, const void* X, const void* W0,
                             void* stream) {
   lora_status e = check_shape(sh);
   if (e != LORA_OK) return e;
-  REQ(X); REQ(W0); REQ(A); REQ(B); REQ(Y);
+  REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQM(sh->M, Y);
   ALN(X); ALN(W0); ALN(A); ALN(B); ALN(bias); ALN(Y); ALN(Z_save);
   if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
   LinFwdWs w;
@@ -437,7 +442,7 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
                             void* ws, size_t ws_bytes, void* stream) {
   lora_status e = check_shape(sh);
   if (e != LORA_OK) return e;
-  REQ(X); REQ(W0); REQ(A); REQ(B); REQ(dY); REQ(dA); REQ(dB);
+  REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQM(sh->M, dY); REQ(dA); REQ(dB);
   ALN(X); ALN(W0); ALN(A); ALN(B); ALN(Z_saved); ALN(dY); ALN(dX); ALN(dA); ALN(dB); ALN(dbias);
   if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
   LinBwdWs w;
@@ -530,7 +535,7 @@ lora_status dora_linear_fwd(const lora_shape* sh, const void* X, const void* W0,
                             void* Z_save, float* n_save, float* V_save, void* ws, size_t ws_bytes, void* stream) {
   lora_status e = check_shape(sh);
   if (e != LORA_OK) return e;
-  REQ(X); REQ(W0); REQ(A); REQ(B); REQ(m); REQ(r0); REQ(Y); REQ(n_save); REQ(V_save);
+  REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQ(m); REQ(r0); REQM(sh->M, Y); REQ(n_save); REQ(V_save);
   ALN(X); ALN(W0); ALN(A); ALN(B); ALN(m); ALN(bias); ALN(r0); ALN(Y); ALN(Z_save); ALN(n_save); ALN(V_save);
   if (!isfinite(s) || !isfinite(eps) || eps < 0.f) return LORA_ERR_INVALID_ARG;
   DoraFwdWs w;
@@ -591,7 +596,8 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
                             void* dm, void* dbias, void* ws, size_t ws_bytes, void* stream) {
   lora_status e = check_shape(sh);
   if (e != LORA_OK) return e;
-  REQ(X); REQ(W0); REQ(A); REQ(B); REQ(m); REQ(Y); REQ(n_saved); REQ(V_saved); REQ(dY); REQ(dA); REQ(dB); REQ(dm);
+  REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQ(m); REQM(sh->M, Y); REQ(n_saved); REQ(V_saved); REQM(sh->M, dY);
+  REQ(dA); REQ(dB); REQ(dm);
   ALN(X); ALN(W0); ALN(A); ALN(B); ALN(m); ALN(bias); ALN(Y); ALN(Z_saved); ALN(n_saved); ALN(V_saved); ALN(dY);
   ALN(dX); ALN(dA); ALN(dB); ALN(dm); ALN(dbias);
   if (!isfinite(s) || !isfinite(eps) || eps < 0.f) return LORA_ERR_INVALID_ARG;
@@ -725,7 +731,8 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
   if (e != LORA_OK) return e;
   if ((e = check_proj(gate)) != LORA_OK || (e = check_proj(up)) != LORA_OK || (e = check_proj(down)) != LORA_OK)
     return e;
-  REQ(X); REQ(Y); REQ(e_save); REQ(u_save); REQ(h_save); REQ(Zgu_save); REQ(Zd_save);
+  REQM(sh->M, X); REQM(sh->M, Y); REQM(sh->M, e_save); REQM(sh->M, u_save); REQM(sh->M, h_save);
+  REQM(sh->M, Zgu_save); REQM(sh->M, Zd_save);
   ALN(X); ALN(Y); ALN(e_save); ALN(u_save); ALN(h_save); ALN(Zgu_save); ALN(Zd_save);
   MlpFwdWs w;
   const size_t need = plan_mlp_fwd(*sh, nullptr, &w);
@@ -794,7 +801,8 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
   if (e != LORA_OK) return e;
   if ((e = check_proj(gate)) != LORA_OK || (e = check_proj(up)) != LORA_OK || (e = check_proj(down)) != LORA_OK)
     return e;
-  REQ(X); REQ(e_saved); REQ(u_saved); REQ(h_saved); REQ(Zgu_saved); REQ(Zd_saved); REQ(dY);
+  REQM(sh->M, X); REQM(sh->M, e_saved); REQM(sh->M, u_saved); REQM(sh->M, h_saved); REQM(sh->M, Zgu_saved);
+  REQM(sh->M, Zd_saved); REQM(sh->M, dY);
   REQ(dAg); REQ(dBg); REQ(dAu); REQ(dBu); REQ(dAd); REQ(dBd);
   ALN(X); ALN(e_saved); ALN(u_saved); ALN(h_saved); ALN(Zgu_saved); ALN(Zd_saved); ALN(dY); ALN(dX);
   ALN(dAg); ALN(dBg); ALN(dAu); ALN(dBu); ALN(dAd); ALN(dBd);
@@ -928,7 +936,7 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
 lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t* Xq, float* sx, const void* A,
                                int64_t r, void* Z, void* stream) {
   if (rows < 0 || cols <= 0 || cols % 8) return rows < 0 || cols <= 0 ? LORA_ERR_INVALID_ARG : LORA_ERR_UNSUPPORTED;
-  REQ(X); REQ(Xq); REQ(sx);
+  REQM(rows, X); REQM(rows, Xq); REQM(rows, sx);
   ALN(X); ALN(Xq); ALN(A); ALN(Z);
   if ((A == nullptr) != (Z == nullptr)) return LORA_ERR_INVALID_ARG;
   if (A && (r < 8 || r > 64 || r % 8)) return LORA_ERR_UNSUPPORTED;
@@ -948,7 +956,7 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
                           void* Y, int32_t* acc_out, void* stream) {
   if (M < 0 || d_in <= 0 || d_out <= 0) return LORA_ERR_INVALID_ARG;
   if (d_in % 32 || d_out % 8) return LORA_ERR_UNSUPPORTED;
-  REQ(Xq); REQ(Wq);
+  REQM(M, Xq); REQ(Wq);
   if (Y == nullptr && acc_out == nullptr) return LORA_ERR_INVALID_ARG;
   if (Y && (!sx || !sw)) return LORA_ERR_INVALID_ARG;
   if ((Z == nullptr) != (B == nullptr)) return LORA_ERR_INVALID_ARG;

@@ -20,6 +20,7 @@
 #include "internal.h"
 
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 
 namespace lg {
 
@@ -234,7 +235,9 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
         const uint32_t d_tmem = tmem_base + buf * BN;
         for (int ks = 0; ks < nk; ++ks) {
           const bool tail = HAS_TAIL && ks >= nk0;
-          uint64_t* wb = (KSCALE && !tail) ? &ready[stage] : &full[stage];
+          // with K-scaling every stage (tail included) is handed over through `ready`, so that
+          // barrier completes exactly one phase per use of the stage, in step with `full`
+          uint64_t* wb = KSCALE ? &ready[stage] : &full[stage];
           if (!mbar_wait(wb, phase, p.timeout_ns, abort_flag, p.err, 0x103)) {
             ok = false;
             break;
@@ -433,11 +436,14 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       for (int ks = 0; ks < nk; ++ks) {
         const bool tail = HAS_TAIL && ks >= nk0;
-        if (!tail) {
-          if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.err, 0x105)) {
-            ok = false;
-            break;
-          }
+        if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.err, 0x105)) {
+          ok = false;
+          break;
+        }
+        if (tail) {
+          // the rank-r tail is not scaled: hand the stage straight on
+          mbar_arrive(&ready[stage]);
+        } else {
           uint8_t* a = sA + stage * A_STAGE_BYTES;
           const int k0 = ks * BK;
 #pragma unroll
@@ -584,6 +590,11 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   const int tiles = p.num_m_tiles * p.num_n_tiles;
   int grid = num_sms_current();
   if (d.max_ctas > 0 && d.max_ctas < grid) grid = d.max_ctas;
+  // test knob: cap the persistent grid so that small problems still run several tiles per CTA
+  if (const char* env = getenv("LORA_GB300_MAX_CTAS")) {
+    const int v = atoi(env);
+    if (v > 0 && v < grid) grid = v;
+  }
   if (grid > tiles) grid = tiles;
 
   // algorithmic flops of this launch: the base contraction plus the rank-r tail

@@ -27,7 +27,7 @@ __all__ = [
     "f64", "adapted_weight", "lora_linear_fwd", "lora_linear_bwd", "dora_rownorm2",
     "dora_linear_fwd", "dora_linear_bwd", "silu", "dsilu", "mlp_swiglu_fwd", "mlp_swiglu_bwd",
     "quantize_rows", "int8_accumulate", "w8a8_lora_fwd",
-    "lora_fwd_rows", "lora_bwd_sampled", "dora_fwd_rows", "dora_bwd_sampled",
+    "lora_fwd_rows", "lora_bwd_sampled", "dora_fwd_rows", "dora_bwd_sampled", "dora_bwd_rows_sampled",
     "mlp_fwd_rows", "mlp_bwd_rows",
 ]
 
@@ -311,6 +311,26 @@ def dora_bwd_sampled(X, W0, A, B, m, s, dY, rows, in_cols, out_rows, eps=1e-12):
     dWp_rows = c[out_rows, None] * dWd_rows + coef[out_rows, None] * Wp[out_rows]
     dB = s * (dWp_rows @ A.T)
     return dX, dA, dB, dm, dY.sum(axis=0)
+
+
+def dora_bwd_rows_sampled(X, W0, A, B, m, s, dY, rows, out_rows, eps=1e-12):
+    """DoRA gradients that need only some output rows: dX[rows], dB[out_rows], dm[out_rows].
+
+    t_o = <dWd_o, W'_o> is evaluated for the sampled o only, as colsum(dY[:, o] * (X W'_o^T)).
+    """
+    Wp = adapted_weight(W0, A, B, s)
+    n, nraw = _dora_norm(Wp, eps)
+    c = m / n
+    dX = dY[rows] @ (c[:, None] * Wp)
+    Wo = Wp[out_rows]
+    t = (dY[:, out_rows] * (X @ Wo.T)).sum(axis=0)
+    dm = t / n[out_rows]
+    live = nraw[out_rows] > eps
+    coef = np.where(live, (-t * m[out_rows] / (n[out_rows] ** 2)) / np.where(live, nraw[out_rows], 1.0), 0.0)
+    dWd_rows = dY[:, out_rows].T @ X
+    dWp_rows = c[out_rows, None] * dWd_rows + coef[:, None] * Wo
+    dB = s * (dWp_rows @ A.T)
+    return dX, dB, dm
 
 
 def mlp_fwd_rows(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, rows):

@@ -1,0 +1,179 @@
+"""GPU parity at the workloads' full sizes (sampled outputs the oracle computes one by one),
+and small problems run with a capped persistent grid so that every CTA of the tcgen05 GEMM
+processes several tiles (ring wrap-around, both accumulator buffers, barrier phases)."""
+import numpy as np
+import pytest
+import torch
+
+import datagen as D
+import oracle as O
+from parity import assert_close, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from dora_adapter_linear_gb300.build import build
+    build()
+    from dora_adapter_linear_gb300 import ops as _ops
+    return _ops
+
+
+def f64(t):
+    return None if t is None else to64(t)
+
+
+def gpu(t):
+    return None if t is None else t.to(DEV).contiguous()
+
+
+def ws_clear(ops):
+    from dora_adapter_linear_gb300 import _lib as L
+    for buf in ops._WS.values():
+        assert L.lora_check_device_error(buf) == 0, "a kernel recorded a timed-out wait"
+
+
+# ---------------------------------------------------------------------------- capped grid (persistence)
+@pytest.fixture
+def two_ctas(monkeypatch):
+    monkeypatch.setenv("LORA_GB300_MAX_CTAS", "2")
+    yield
+
+
+def test_persistent_lora(ops, two_ctas):
+    case = D.scaled(D.WORKLOADS["lora_4096_bf16"], M=520, d_in=392, d_out=776, r=16, bias=True)
+    t = D.make_linear(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s, g["bias"])
+    X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
+    assert_close(Y, O.lora_linear_fwd(X, W0, A, B, case.s, f64(t["bias"])), "bf16", "Y")
+    dX, dA, dB, _ = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
+    rX, rA, rB, _ = O.lora_linear_bwd(X, W0, A, B, case.s, f64(t["dY"]))
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dB, rB, "bf16", "dB")
+    ws_clear(ops)
+
+
+def test_persistent_dora(ops, two_ctas):
+    case = D.scaled(D.WORKLOADS["dora_4096x11008_bf16"], M=520, d_in=392, d_out=776, r=32)
+    t = D.make_linear(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    r0 = ops.dora_rownorm2(g["W0"])
+    Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps, g["bias"])
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    rY, _ = O.dora_linear_fwd(X, W0, A, B, m, case.s, case.eps, bias)
+    assert_close(Y, rY, "bf16", "Y")
+    dX, dA, dB, dm, _ = ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V, g["dY"],
+                                            case.s, case.eps)
+    rX, rA, rB, rm, _ = O.dora_linear_bwd(X, W0, A, B, m, case.s, dY, case.eps)
+    for got, ref, nm in ((dX, rX, "dX"), (dA, rA, "dA"), (dB, rB, "dB"), (dm, rm[None], "dm")):
+        assert_close(got, ref, "bf16", nm)
+    ws_clear(ops)
+
+
+def test_persistent_mlp(ops, two_ctas):
+    case = D.scaled(D.WORKLOADS["mlp_swiglu_4096x14336_bf16"], M=400, H=200, I=520, r=16, alpha=24.0)
+    t = D.make_mlp(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
+    Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
+    args = tuple(x if isinstance(x, float) else f64(x) for x in
+                 (t["X"], t["Wg"], t["Ag"], t["Bg"], case.s, t["Wu"], t["Au"], t["Bu"], case.s,
+                  t["Wd"], t["Ad"], t["Bd"], case.s))
+    ry, re, ru, rh = O.mlp_swiglu_fwd(*args)
+    assert_close(Y, ry, "bf16", "y")
+    gr = ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
+    ref = O.mlp_swiglu_bwd(*args, f64(t["dY"]))
+    for k in ("dX", "dAg", "dBg", "dAu", "dBu", "dAd", "dBd"):
+        assert_close(gr[k], ref[k], "bf16", k)
+    ws_clear(ops)
+
+
+# ---------------------------------------------------------------------------- full size, sampled
+ROWS = [0, 1, 127, 128, 4095, 5000, 8191]
+
+
+def test_full_lora_4096(ops):
+    case = D.WORKLOADS["lora_4096_bf16"]
+    t = D.make_linear(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s)
+    dX, dA, dB, _ = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
+    torch.cuda.synchronize()
+    ws_clear(ops)
+    X, W0, A, B, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "dY"))
+    assert_close(Y[ROWS], O.lora_fwd_rows(X, W0, A, B, case.s, ROWS), "bf16", "Y rows")
+    cols, orows = [0, 63, 64, 2047, 4095], [0, 255, 256, 3000, 4095]
+    sX, sA, sB, _ = O.lora_bwd_sampled(X, W0, A, B, case.s, dY, ROWS, cols, orows)
+    assert_close(dX[ROWS], sX, "bf16", "dX rows")
+    assert_close(dA[:, cols].T, sA.T, "bf16", "dA columns")
+    assert_close(dB[orows], sB, "bf16", "dB rows")
+
+
+def test_full_dora_4096x11008(ops):
+    case = D.WORKLOADS["dora_4096x11008_bf16"]
+    t = D.make_linear(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    r0 = ops.dora_rownorm2(g["W0"])
+    Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps, g["bias"])
+    dX, dA, dB, dm, _ = ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V, g["dY"],
+                                            case.s, case.eps)
+    torch.cuda.synchronize()
+    ws_clear(ops)
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    rY, rn = O.dora_fwd_rows(X, W0, A, B, m, case.s, ROWS, case.eps, bias)
+    assert_close(Y[ROWS], rY, "bf16", "Y rows")
+    np.testing.assert_allclose(to64(n), rn, rtol=1e-4)
+    orows = [0, 255, 256, 5000, 11007]
+    sX, sB, sm = O.dora_bwd_rows_sampled(X, W0, A, B, m, case.s, dY, ROWS, orows, case.eps)
+    assert_close(dX[ROWS], sX, "bf16", "dX rows")
+    assert_close(dB[orows], sB, "bf16", "dB rows")
+    assert_close(dm[orows][None], sm[None], "bf16", "dm entries")
+    assert torch.isfinite(dA.float()).all()
+
+
+def test_full_mlp_swiglu(ops):
+    case = D.WORKLOADS["mlp_swiglu_4096x14336_bf16"]
+    t = D.make_mlp(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
+    Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
+    gr = ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
+    torch.cuda.synchronize()
+    ws_clear(ops)
+    rows = [0, 1, 8191, 16383]
+    args = tuple(x if isinstance(x, float) else f64(x) for x in
+                 (t["X"], t["Wg"], t["Ag"], t["Bg"], case.s, t["Wu"], t["Au"], t["Bu"], case.s,
+                  t["Wd"], t["Ad"], t["Bd"], case.s))
+    ry, re, ru, rh = O.mlp_fwd_rows(*args, rows)
+    assert_close(saved["e"][rows], re, "bf16", "e rows")
+    assert_close(saved["u"][rows], ru, "bf16", "u rows")
+    assert_close(saved["h"][rows], rh, "bf16", "h rows")
+    assert_close(Y[rows], ry, "bf16", "y rows")
+    assert_close(gr["dX"][rows], O.mlp_bwd_rows(*args, f64(t["dY"]), rows), "bf16", "dX rows")
+    for k in ("dAg", "dBg", "dAu", "dBu", "dAd", "dBd"):
+        assert torch.isfinite(gr[k].float()).all()
+
+
+def test_full_w8a8_3072(ops):
+    case = D.WORKLOADS["w8a8_lora_3072"]
+    t = D.make_w8a8(case)
+    Wq, sw = O.quantize_rows(t["W0"].numpy())
+    X = gpu(t["X"])
+    Xq, sx, Z = ops.w8a8_quantize_rows(X, gpu(t["A"]))
+    Y, acc = ops.w8a8_lora_fwd(Xq, sx, gpu(torch.from_numpy(Wq)), gpu(torch.from_numpy(sw)), Z, gpu(t["B"]), case.s,
+                               want_acc=True)
+    torch.cuda.synchronize()
+    rows = [0, 1, 777, 16383]
+    rq, rs = O.quantize_rows(t["X"][rows].float().numpy())
+    np.testing.assert_array_equal(Xq[rows].cpu().numpy(), rq)
+    np.testing.assert_array_equal(sx[rows].cpu().numpy(), rs)
+    racc = O.int8_accumulate(rq, Wq)
+    np.testing.assert_array_equal(acc[rows].cpu().numpy().astype(np.int64), racc)
+    Zr = f64(t["X"][rows]) @ f64(t["A"]).T
+    assert_close(Z[rows], Zr, "bf16", "Z rows")
+    ry, _ = O.w8a8_lora_fwd(rq, rs, Wq, sw, f64(Z[rows].cpu()), f64(t["B"]), case.s, acc=racc)
+    assert_close(Y[rows], ry, "bf16", "Y rows")

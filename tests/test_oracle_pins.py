@@ -339,6 +339,8 @@ def test_sampled_forms_match_full():
     gX, gA, gB, gm, gb = O.dora_bwd_sampled(X, W0, A, B, m, s, dY, rows, cols, orows)
     assert rel(gX, fX[rows]) < 1e-12 and rel(gA, fA[:, cols]) < 1e-12 and rel(gB, fB[orows]) < 1e-12
     assert rel(gm, fm) < 1e-12
+    hX, hB, hm = O.dora_bwd_rows_sampled(X, W0, A, B, m, s, dY, rows, orows)
+    assert rel(hX, fX[rows]) < 1e-12 and rel(hB, fB[orows]) < 1e-12 and rel(hm, fm[orows]) < 1e-12
     yf, nf = O.dora_linear_fwd(X, W0, A, B, m, s, 1e-12, bias)
     yr, nr = O.dora_fwd_rows(X, W0, A, B, m, s, rows, 1e-12, bias)
     assert rel(yr, yf[rows]) < 1e-14 and rel(nr, nf) == 0
