@@ -17,15 +17,19 @@ namespace rp {
 constexpr int BMR = 32;        // rows per CTA
 constexpr int BKC = 64;        // K per stage
 constexpr int PITCH = 72;      // padded smem row pitch (elements) -> conflict-free ldmatrix
-constexpr int STAGES = 4;
+constexpr int STAGES = 8;      // deep ring: ~28 KB of the streamed operand in flight per CTA
 constexpr int S_BYTES = BMR * PITCH * 2;       // 4608
-constexpr int U_BYTES = 64 * PITCH * 2;        // 9216 (covers [R<=64, 64] and [64, R<=64])
-constexpr int STAGE_BYTES = S_BYTES + U_BYTES;
+// U chunk: [R(+8 pad rows), 64] K-major or [64, R+8] R-major
+template <int R, bool KR>
+constexpr int u_bytes() { return KR ? 64 * (R + 8) * 2 : (R + 8) * PITCH * 2; }
+template <int R, bool KR>
+constexpr int stage_bytes() { return S_BYTES + u_bytes<R, KR>(); }
 }  // namespace rp
 
 template <int R, bool U_KR>
 __global__ void __launch_bounds__(128) rowproj_kernel(RowProjDesc d) {
   using namespace rp;
+  constexpr int STAGE_BYTES = stage_bytes<R, U_KR>();
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rg = warp & 1;        // 16-row group
@@ -148,7 +152,7 @@ __global__ void __launch_bounds__(128) rowproj_kernel(RowProjDesc d) {
 
 template <int R, bool KR>
 static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
-  const int smem = rp::STAGES * rp::STAGE_BYTES;
+  const int smem = rp::STAGES * rp::stage_bytes<R, KR>();
   auto k = rowproj_kernel<R, KR>;
   static bool set = false;
   if (!set) {
