@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_HERE, "liblora_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "lora_gb300.h")
 
 LORA_F32, LORA_BF16 = 0, 1
+LORA_NOALLOC_SCRATCH_BYTES = 4 << 20   # fixed scratch of lora_linear_fwd_noalloc (header macro)
 OP_LINEAR_FWD, OP_LINEAR_BWD, OP_DORA_FWD, OP_DORA_BWD, OP_MLP_FWD, OP_MLP_BWD = range(6)
 STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_UNSUPPORTED", 3: "LORA_ERR_MISALIGNED",
           4: "LORA_ERR_WORKSPACE", 5: "LORA_ERR_CUDA", 6: "LORA_ERR_DEVICE_TIMEOUT"}
@@ -60,6 +61,7 @@ _SIGS = {
     "w8a8_quantize_rows": (c_int, [c_int64, c_int64, P, P, P, P, c_int64, P, P]),
     "w8a8_lora_fwd": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, c_float, P, P, P, P]),
     "lora_debug_wait_timeout": (c_int, [P, c_uint32, P]),
+    "lora_linear_fwd_noalloc": (c_int, [POINTER(LoraShape), P, P, P, P, P, c_float, P, P, P]),
     "lora_launch_count": (ctypes.c_uint64, []),
     "lora_prof_enable": (c_int, [c_int]),
     "lora_prof_gemm": (c_int, [POINTER(ctypes.c_double), POINTER(c_int64), POINTER(ctypes.c_double), c_int]),
@@ -173,6 +175,12 @@ def lora_linear_fwd(sh, X, W0, A, B, bias, s, Y, Z_save, ws, stream=None):
     _ck(_lib().lora_linear_fwd(ctypes.byref(sh), ptr(X), ptr(W0), ptr(A), ptr(B), ptr(bias), float(s), ptr(Y),
                                ptr(Z_save), ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                _stream(stream)), "lora_linear_fwd")
+
+
+def lora_linear_fwd_noalloc(sh, X, W0, A, B, bias, s, Y, Z_save, stream=None):
+    """lora_linear_fwd with the library's fixed device scratch instead of a workspace."""
+    _ck(_lib().lora_linear_fwd_noalloc(ctypes.byref(sh), ptr(X), ptr(W0), ptr(A), ptr(B), ptr(bias), float(s),
+                                       ptr(Y), ptr(Z_save), _stream(stream)), "lora_linear_fwd_noalloc")
 
 
 def lora_linear_bwd(sh, X, W0, A, B, Z_saved, dY, s, dX, dA, dB, dbias, ws, stream=None):

@@ -114,6 +114,30 @@ lora_status lora_linear_fwd(const lora_shape* sh, const void* X, const void* W0,
                             const void* B, const void* bias, float s, void* Y, void* Z_save,
                             void* ws, size_t ws_bytes, void* stream);
 
+/* Size of the fixed device scratch used by lora_linear_fwd_noalloc (4 MiB). */
+#define LORA_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* lora_linear_fwd without a workspace argument, for callers that cannot allocate device
+ * memory: runtimes that plan all device memory before they start, plugin hosts that forbid
+ * allocation once running, or hot paths that must not enter an allocator.  The source pages
+ * have no counterpart to this entry point.
+ *   Same arguments, layouts and results as lora_linear_fwd, minus ws / ws_bytes.  It
+ *   allocates nothing (no cudaMalloc, no cudaFree, no allocating library call): its scratch
+ *   is one fixed array of LORA_NOALLOC_SCRATCH_BYTES inside this library's device image,
+ *   held by every GPU that loads the library until the process exits.
+ *   Limit: the problem must fit that scratch, i.e. lora_workspace_bytes(LORA_OP_LINEAR_FWD,
+ *   sh) <= LORA_NOALLOC_SCRATCH_BYTES (about M * r <= 2,097,000 for bf16, half that for
+ *   fp32); larger problems return LORA_ERR_WORKSPACE and launch nothing.
+ *   The first call on each device looks up the scratch's device address (with that device
+ *   current); make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents (each call clears
+ *   the part that must start at zero): two calls that overlap on the GPU, e.g. on two
+ *   streams without ordering, race and corrupt each other.  A timed-out device wait is
+ *   recorded only in that shared array and is not reported by this entry point. */
+lora_status lora_linear_fwd_noalloc(const lora_shape* sh, const void* X, const void* W0, const void* A,
+                                    const void* B, const void* bias, float s, void* Y, void* Z_save,
+                                    void* stream);
+
 /* Backward of lora_linear_fwd with W0 frozen:
  *   dX = dY W0 + s (dY B) A,  dA = s (dY B)^T X,  dB = s dY^T Z,  dbias = colsum(dY).
  * "How Unsloth's FastLoRA Kernel Differs ...", Custom Backward Pass Implementation (the
