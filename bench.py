@@ -269,7 +269,12 @@ def timed(fn, steps, warmup, dist=None):
     return e0.elapsed_time(e1) / steps, t0, t1
 
 
-def gemm_roofline(L, peaks, ms_step, sustained):
+# DRAM bytes (read + write) per GEMM launch from ncu captures, keyed by workload; a value is
+# dropped (None) whenever the kernel changes and is re-measured before it is put back.
+GEMM_TRAFFIC = {}
+
+
+def gemm_roofline(L, peaks, ms_step, steps_recorded, sustained, workload):
     """Roofline of the dominant kernel (tcgen05 GEMM) from the library's own event timing."""
     ms, n, fl = L.lora_prof_gemm(reset=True)
     if n == 0 or ms <= 0:
@@ -278,9 +283,10 @@ def gemm_roofline(L, peaks, ms_step, sustained):
     peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     return {"kernel": "tc_gemm_kernel (tcgen05 GEMM with fused rank-r tail)", "bound": "tensor",
             "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-            "peak_kind": ("sustained" if sustained else "burst") + " bf16, " + peaks["source"],
-            "launches": n, "avg_launch_ms": round(ms / n, 4), "share_of_step": round(ms / n * (n and 1) / 1, 4),
-            "traffic": None}
+            "peak_kind": ("sustained" if sustained else "burst") + " bf16, " + peaks["source"] + " (of measured)",
+            "launches": n, "avg_launch_ms": round(ms / n, 4),
+            "share_of_step": round(ms / (steps_recorded * ms_step), 4),
+            "flops_per_launch": fl / n, "traffic": GEMM_TRAFFIC.get(workload)}
 
 
 def headline(args, L, ops, dist, world, peaks):
@@ -301,9 +307,9 @@ def headline(args, L, ops, dist, world, peaks):
     wsf = torch.zeros(L.lora_workspace_bytes(L.OP_LINEAR_FWD, sh), dtype=torch.uint8, device=dev)
     wsb = torch.zeros(L.lora_workspace_bytes(L.OP_LINEAR_BWD, sh), dtype=torch.uint8, device=dev)
 
-    def step():
-        L.lora_linear_fwd(sh, X, W0, A, B, None, s, Y, Z, wsf)
-        L.lora_linear_bwd(sh, X, W0, A, B, Z, dY, s, dX, dA, dB, None, wsb)
+    def step(Xb=X, dYb=dY):
+        L.lora_linear_fwd(sh, Xb, W0, A, B, None, s, Y, Z, wsf)
+        L.lora_linear_bwd(sh, Xb, W0, A, B, Z, dYb, s, dX, dA, dB, None, wsb)
 
     fwd_fl, bwd_fl = lora_flops(M, d_in, d_out, r)
     clk = ClockSampler(torch.cuda.current_device())
@@ -319,9 +325,7 @@ def headline(args, L, ops, dist, world, peaks):
     launches = L.lora_launch_count() - n0
     # launches of the warm-up steps are in the count too: scale to the timed steps
     gpu_launches = launches * args.steps // (args.steps + args.warmup)
-    roof = gemm_roofline(L, peaks, ms, sustained=False)
-    if roof is not None:
-        roof["share_of_step"] = round(roof["avg_launch_ms"] * 2 / ms, 3)
+    roof = gemm_roofline(L, peaks, ms, args.steps + args.warmup, False, HEADLINE)
     nv.stop()
     clocks = nv.summary(t0, t1) or clk.summary(t0, t1)
     clk.stop()
@@ -329,21 +333,53 @@ def headline(args, L, ops, dist, world, peaks):
         if L.lora_check_device_error(ws) != 0:
             raise RuntimeError("a kernel recorded a timed-out wait during the benchmark")
 
-    # end to end: host (pinned) inputs copied in and adapter gradients read back every step
+    # end to end: every step copies its inputs from pinned host memory and reads the adapter
+    # gradients back; the next step's host->device copy runs on a second stream into the other
+    # half of a double buffer while the current step computes
     Xh = t["X"].pin_memory()
     dYh = t["dY"].pin_memory()
     dAh = torch.empty_like(dA, device="cpu").pin_memory()
     dBh = torch.empty_like(dB, device="cpu").pin_memory()
+    Xd, dYd = [X, torch.empty_like(X)], [dY, torch.empty_like(dY)]
+    cp = torch.cuda.Stream()
 
-    def e2e_step():
-        X.copy_(Xh, non_blocking=True)
-        dY.copy_(dYh, non_blocking=True)
-        step()
-        dAh.copy_(dA, non_blocking=True)
-        dBh.copy_(dB, non_blocking=True)
+    def e2e_run(n):
+        cur = torch.cuda.current_stream()
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        cp.wait_stream(cur)
+        with torch.cuda.stream(cp):
+            Xd[0].copy_(Xh, non_blocking=True)
+            dYd[0].copy_(dYh, non_blocking=True)
+            copied[0].record(cp)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                with torch.cuda.stream(cp):
+                    if i >= 1:
+                        cp.wait_event(done[1 - b])     # step i-1 used that half
+                    Xd[1 - b].copy_(Xh, non_blocking=True)
+                    dYd[1 - b].copy_(dYh, non_blocking=True)
+                    copied[1 - b].record(cp)
+            cur.wait_event(copied[b])
+            step(Xd[b], dYd[b])
+            done[b].record(cur)
+            dAh.copy_(dA, non_blocking=True)
+            dBh.copy_(dB, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 50))
-    ms_e2e, _, _ = timed(e2e_step, e2e_steps, 2, dist)
+    e2e_steps = max(4, min(args.steps, 50))
+    e2e_run(3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    q0.record()
+    e2e_run(e2e_steps)
+    q1.record()
+    torch.cuda.synchronize()
+    ms_e2e = q0.elapsed_time(q1) / e2e_steps
+    if dist is not None:
+        dist.barrier()
     ms_all, ms_e2e = reduce_max([ms, ms_e2e], dist, dev)
     return {
         "value": job_throughput(fwd_fl + bwd_fl, world, ms_all), "ms_per_step": ms_all, "clocks": clocks,
@@ -383,7 +419,8 @@ def extra_workloads(args, L, ops, peaks):
     f, b = dora_flops(case.M, case.d_in, case.d_out, case.r)
     out["dora_4096x11008_bf16"] = {"ms_per_step": ms, "tflops": (f + b) / (ms * 1e-3) / 1e12,
                                    "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                                   "roofline": gemm_roofline(L, peaks, ms, False)}
+                                   "roofline": gemm_roofline(L, peaks, ms, steps + warm, False,
+                                                             "dora_4096x11008_bf16")}
     del g, t
 
     # SwiGLU MLP
@@ -397,12 +434,14 @@ def extra_workloads(args, L, ops, peaks):
         ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
     L.lora_prof_gemm(reset=True)
     L.lora_prof_enable(True)
-    ms, _, _ = timed(mlp_step, max(3, steps // 2), 2)
+    mlp_steps = max(3, steps // 2)
+    ms, _, _ = timed(mlp_step, mlp_steps, 2)
     L.lora_prof_enable(False)
     f, b = mlp_flops(case.M, case.H, case.I, case.r)
     out["mlp_swiglu_4096x14336_bf16"] = {"ms_per_step": ms, "tflops": (f + b) / (ms * 1e-3) / 1e12,
                                          "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                                         "roofline": gemm_roofline(L, peaks, ms, True)}
+                                         "roofline": gemm_roofline(L, peaks, ms, mlp_steps + 2, True,
+                                                                   "mlp_swiglu_4096x14336_bf16")}
     del g, t, P
     torch.cuda.empty_cache()
 

@@ -8,18 +8,24 @@
 // the low-rank update is folded into the data GEMM without ever forming B A
 // ("LoRA/DoRA fast forward: no weight materialization", What section).
 //
-// Roles (one CTA per SM, 6 or 10 warps):
-//   warp 0      TMA producer: 128x64 A tiles and BNx64 B tiles into a STAGES-deep ring
-//   warp 1      TMEM allocator + MMA issuer (one thread), double-buffered accumulators
+// Two kernels share the stage layout, the epilogues and the A-tile scaling:
+//  * tc_gemm_kernel: one CTA per SM, 128 x 256 tile (cta_group::1).
+//  * tc_pair_kernel: a cluster of two CTAs on two SMs computes a 256 x 256 tile with
+//    cta_group::2 MMAs issued by the even CTA; each SM stages its 128 rows of A and half of
+//    B, so the operand bytes per SM and k-step drop from 48 KB to 32 KB.
+// Roles (per CTA, 6 or 10 warps):
+//   warp 0      TMA producer into a STAGES-deep ring of 128B-swizzled tiles
+//   warp 1      TMEM allocator; MMA issuer (one thread; in the pair kernel, the even CTA's)
 //   warps 2..5  epilogue: TMEM -> registers -> (row scale, bias, SwiGLU) -> bf16 ->
 //               swizzled SMEM staging -> TMA store
 //   warps 6..9  (DoRA backward only) scale the A tile in SMEM by c[k] along K
 // Every mbarrier wait is bounded (global timer); on expiry the CTA records the error in
-// the caller's error word, drains its in-flight copies and MMAs, frees TMEM and returns.
+// the caller's error word, lets its in-flight copies and MMAs finish, frees TMEM and returns.
 #include "common.cuh"
 #include "internal.h"
 
 #include <cudaTypedefs.h>
+#include <stdio.h>
 #include <stdlib.h>
 
 namespace lg {
@@ -41,30 +47,34 @@ struct TcParams {
   uint64_t timeout_ns;
 };
 
-constexpr int BM = 128;
+constexpr int BM = 128;     // rows of A per CTA
+constexpr int BN = 256;     // accumulator columns per tile
 constexpr int BK = 64;
 constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 
-template <int EPI>
+template <int EPI, bool PAIR>
 struct EpiCfg;
-template <>
-struct EpiCfg<EPI_SCALE_BIAS> { static constexpr int STAGES = 4, STG_BUFS = 2; };
-template <>
-struct EpiCfg<EPI_SWIGLU> { static constexpr int STAGES = 3, STG_BUFS = 3; };
-template <>
-struct EpiCfg<EPI_SWIGLU_BWD> { static constexpr int STAGES = 3, STG_BUFS = 4; };
+template <> struct EpiCfg<EPI_SCALE_BIAS, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
+template <> struct EpiCfg<EPI_SWIGLU, false> { static constexpr int STAGES = 3, STG_BUFS = 3; };
+template <> struct EpiCfg<EPI_SWIGLU_BWD, false> { static constexpr int STAGES = 3, STG_BUFS = 4; };
+template <> struct EpiCfg<EPI_SCALE_BIAS, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
+template <> struct EpiCfg<EPI_SWIGLU, true> { static constexpr int STAGES = 5, STG_BUFS = 3; };
+template <> struct EpiCfg<EPI_SWIGLU_BWD, true> { static constexpr int STAGES = 5, STG_BUFS = 4; };
 
-template <int BN, int EPI>
+template <int EPI, bool PAIR>
 struct Layout {
-  static constexpr int STAGES = EpiCfg<EPI>::STAGES;
-  static constexpr int B_STAGE_BYTES = BN * BK * 2;
+  static constexpr int STAGES = EpiCfg<EPI, PAIR>::STAGES;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;        // B rows (N) staged by one CTA
+  static constexpr int B_STAGE_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
   static constexpr int OFF_STG = OFF_B + STAGES * B_STAGE_BYTES;
-  static constexpr int STG_BYTES = 4 * EpiCfg<EPI>::STG_BUFS * 4096;
+  static constexpr int STG_BYTES = 4 * EpiCfg<EPI, PAIR>::STG_BUFS * 4096;
   static constexpr int OFF_BAR = OFF_STG + STG_BYTES;
   static constexpr int BAR_BYTES = 8 * (3 * STAGES + 5) + 16;
   static constexpr int TOTAL = OFF_BAR + BAR_BYTES + 1024;  // +1024 for base alignment
+  static_assert(TOTAL <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& mt, int& nt) {
@@ -90,14 +100,186 @@ __device__ __forceinline__ void stage_row(uint8_t* stg, int row, const uint32_t*
   }
 }
 
-template <int BN, bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
+// ---------------------------------------------------------------------------- epilogue of one tile
+// One warp drains its 32 TMEM lanes (rows row0 .. row0 + 31) of the accumulator at t_row.
+template <int EPI, int N_OUT>
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row, int row0, int n0, int lane,
+                                              uint8_t* my_stg, uint32_t& chunk_ctr) {
+  if constexpr (EPI == EPI_SCALE_BIAS) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c, ++chunk_ctr) {
+      uint8_t* stg = my_stg + (chunk_ctr & 1) * 4096;
+      if (lane == 0) tma_store_wait_read<1>();
+      __syncwarp();
+      uint32_t v[32];
+      uint32_t w[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, v);
+        tmem_ld_wait();
+        const int col = n0 + c * 64 + h * 32;
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float f0 = u2f(v[j]), f1 = u2f(v[j + 1]);
+          if (p.col_scale != nullptr && col + j < p.N) {
+            f0 *= __ldg(p.col_scale + col + j);
+            f1 *= __ldg(p.col_scale + col + j + 1);
+          }
+          if (p.bias != nullptr && col + j < p.N) {
+            f0 += __bfloat162float(p.bias[col + j]);
+            f1 += __bfloat162float(p.bias[col + j + 1]);
+          }
+          w[h * 16 + j / 2] = pack_bf16x2(f0, f1);
+        }
+      }
+      stage_row(stg, lane, w, 0);
+      stage_row(stg, lane, w + 16, 4);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tmOut[0], stg, n0 + c * 64, row0);
+        tma_store_commit();
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    // accumulator columns [0, BN/2) hold e, [BN/2, BN) hold u for outputs n0 .. n0 + BN/2
+#pragma unroll 1
+    for (int c = 0; c < N_OUT / 64; ++c) {
+      uint8_t* se = my_stg;
+      uint8_t* su = my_stg + 4096;
+      uint8_t* sh = my_stg + 8192;
+      if (lane == 0) tma_store_wait_read<0>();
+      __syncwarp();
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t ve[32], vu[32];
+        tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, ve);
+        tmem_ld_32x32b_x32(t_row + BN / 2 + c * 64 + h * 32, vu);
+        tmem_ld_wait();
+        uint32_t we[16], wu[16], wh[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float e0 = u2f(ve[j]), e1 = u2f(ve[j + 1]);
+          const float u0 = u2f(vu[j]), u1 = u2f(vu[j + 1]);
+          const float h0 = e0 / (1.0f + __expf(-e0)) * u0;
+          const float h1 = e1 / (1.0f + __expf(-e1)) * u1;
+          we[j / 2] = pack_bf16x2(e0, e1);
+          wu[j / 2] = pack_bf16x2(u0, u1);
+          wh[j / 2] = pack_bf16x2(h0, h1);
+        }
+        stage_row(se, lane, we, h * 4);
+        stage_row(su, lane, wu, h * 4);
+        stage_row(sh, lane, wh, h * 4);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tmOut[0], se, n0 + c * 64, row0);
+        tma_store_2d(&p.tmOut[1], su, n0 + c * 64, row0);
+        tma_store_2d(&p.tmOut[2], sh, n0 + c * 64, row0);
+        tma_store_commit();
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+    // accumulator = dh; read the saved e, u for this thread's row and form de, du
+    const int grow = row0 + lane;
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c, ++chunk_ctr) {
+      uint8_t* sde = my_stg + (chunk_ctr & 1) * 8192;
+      uint8_t* sdu = sde + 4096;
+      if (lane == 0) tma_store_wait_read<1>();
+      __syncwarp();
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t vd[32];
+        tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, vd);
+        tmem_ld_wait();
+        const int col = n0 + c * 64 + h * 32;
+        uint32_t ev[16], uv[16];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int cc = col + 8 * g;
+          if (grow < p.M && cc < p.N) {
+            const uint4 a = *reinterpret_cast<const uint4*>(p.e_in + (size_t)grow * p.ld_eu + cc);
+            const uint4 b = *reinterpret_cast<const uint4*>(p.u_in + (size_t)grow * p.ld_eu + cc);
+            ev[4 * g] = a.x; ev[4 * g + 1] = a.y; ev[4 * g + 2] = a.z; ev[4 * g + 3] = a.w;
+            uv[4 * g] = b.x; uv[4 * g + 1] = b.y; uv[4 * g + 2] = b.z; uv[4 * g + 3] = b.w;
+          } else {
+#pragma unroll
+            for (int z = 0; z < 4; ++z) ev[4 * g + z] = uv[4 * g + z] = 0u;
+          }
+        }
+        uint32_t wde[16], wdu[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 e = unpack_bf16x2(ev[j]);
+          const float2 u = unpack_bf16x2(uv[j]);
+          const float d0 = u2f(vd[2 * j]), d1 = u2f(vd[2 * j + 1]);
+          const float s0 = 1.0f / (1.0f + __expf(-e.x));
+          const float s1 = 1.0f / (1.0f + __expf(-e.y));
+          const float de0 = d0 * u.x * s0 * (1.0f + e.x * (1.0f - s0));
+          const float de1 = d1 * u.y * s1 * (1.0f + e.y * (1.0f - s1));
+          const float du0 = d0 * e.x * s0;
+          const float du1 = d1 * e.y * s1;
+          wde[j] = pack_bf16x2(de0, de1);
+          wdu[j] = pack_bf16x2(du0, du1);
+        }
+        stage_row(sde, lane, wde, h * 4);
+        stage_row(sdu, lane, wdu, h * 4);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tmOut[0], sde, n0 + c * 64, row0);
+        tma_store_2d(&p.tmOut[1], sdu, n0 + c * 64, row0);
+        tma_store_commit();
+      }
+    }
+  }
+}
+
+// Scale one staged 128 x 64 A tile in place by kscale[k] (DoRA backward: dY o c).
+// Thread tid (0..127) always owns physical 16-byte chunk pc = tid & 7 of rows (tid >> 3) + 16 i;
+// all those rows have the same (row & 7), so the logical K-chunk j and its 8 scales are the same
+// for the thread's 8 chunks: two vector loads per k-step.
+__device__ __forceinline__ void kscale_tile(const TcParams& p, uint8_t* a, int ks, int tid) {
+  const int pc = tid & 7;
+  const int j = pc ^ ((tid >> 3) & 7);
+  const int kb = ks * BK + 8 * j;
+  float sc[8];
+  if (kb < p.K0) {  // K0 is a multiple of 8: a group of 8 is wholly inside or outside
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.a_kscale + kb));
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.a_kscale + kb + 4));
+    sc[0] = s0.x; sc[1] = s0.y; sc[2] = s0.z; sc[3] = s0.w;
+    sc[4] = s1.x; sc[5] = s1.y; sc[6] = s1.z; sc[7] = s1.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sc[e] = 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = (tid >> 3) + 16 * i;
+    uint4* ptr = reinterpret_cast<uint4*>(a + r * 128 + pc * 16);
+    uint4 v = *ptr;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16x2(w[e]);
+      w[e] = pack_bf16x2(f.x * sc[2 * e], f.y * sc[2 * e + 1]);
+    }
+    *ptr = v;
+  }
+  fence_proxy_async_smem();
+}
+
+// ============================================================================ 1-CTA kernel
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
 __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using L = Layout<BN, EPI>;
+  using L = Layout<EPI, false>;
   constexpr int STAGES = L::STAGES;
   constexpr int BNB = STACKED ? BN / 2 : BN;          // rows per K-major B box
   constexpr int N_OUT = STACKED ? BN / 2 : BN;        // logical output columns per tile
   constexpr uint32_t TMEM_COLS = 2 * BN;
-  static_assert(TMEM_COLS <= 512, "TMEM budget");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -170,7 +352,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
             break;
           }
           const bool tail = HAS_TAIL && ks >= nk0;
-          mbar_expect_tx(&full[stage], A_STAGE_BYTES + L::B_STAGE_BYTES);
+          mbar_expect_tx(&full[stage], L::STAGE_BYTES);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           uint8_t* a_dst = sA + stage * A_STAGE_BYTES;
@@ -270,161 +452,22 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
   } else if (warp < 6) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int ew = warp - 2;                // epilogue warp index 0..3 (staging owner)
-    uint8_t* my_stg = sStg + ew * (EpiCfg<EPI>::STG_BUFS * 4096);
+    uint8_t* my_stg = sStg + (warp - 2) * (EpiCfg<EPI, false>::STG_BUFS * 4096);
     int it = 0;
     uint32_t chunk_ctr = 0;
-    bool ok = true;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       const int buf = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait(&acc_full[buf], acc_phase, p.timeout_ns, abort_flag, p.err, 0x104)) {
-        ok = false;
-        break;
-      }
+      if (!mbar_wait(&acc_full[buf], acc_phase, p.timeout_ns, abort_flag, p.err, 0x104)) break;
       tc_fence_after();
       int mt, nt;
       tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
-      const int row0 = mt * BM + 32 * q;         // global row of lane 0
-      const int n0 = nt * N_OUT;
       const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + buf * BN;
-
-      if constexpr (EPI == EPI_SCALE_BIAS) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c, ++chunk_ctr) {
-          uint8_t* stg = my_stg + (chunk_ctr & 1) * 4096;
-          if (lane == 0) tma_store_wait_read<1>();
-          __syncwarp();
-          uint32_t v[32];
-          uint32_t w[32];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, v);
-            tmem_ld_wait();
-            const int col = n0 + c * 64 + h * 32;
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float f0 = u2f(v[j]), f1 = u2f(v[j + 1]);
-              if (p.col_scale != nullptr && col + j < p.N) {
-                f0 *= __ldg(p.col_scale + col + j);
-                f1 *= __ldg(p.col_scale + col + j + 1);
-              }
-              if (p.bias != nullptr && col + j < p.N) {
-                f0 += __bfloat162float(p.bias[col + j]);
-                f1 += __bfloat162float(p.bias[col + j + 1]);
-              }
-              w[h * 16 + j / 2] = pack_bf16x2(f0, f1);
-            }
-          }
-          stage_row(stg, lane, w, 0);
-          stage_row(stg, lane, w + 16, 4);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&p.tmOut[0], stg, n0 + c * 64, row0);
-            tma_store_commit();
-          }
-        }
-      } else if constexpr (EPI == EPI_SWIGLU) {
-        // accumulator columns [0, BN/2) hold e, [BN/2, BN) hold u for outputs n0 .. n0 + BN/2
-#pragma unroll 1
-        for (int c = 0; c < N_OUT / 64; ++c) {
-          uint8_t* se = my_stg;
-          uint8_t* su = my_stg + 4096;
-          uint8_t* sh = my_stg + 8192;
-          if (lane == 0) tma_store_wait_read<0>();
-          __syncwarp();
-#pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
-            uint32_t ve[32], vu[32];
-            tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, ve);
-            tmem_ld_32x32b_x32(t_row + BN / 2 + c * 64 + h * 32, vu);
-            tmem_ld_wait();
-            uint32_t we[16], wu[16], wh[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float e0 = u2f(ve[j]), e1 = u2f(ve[j + 1]);
-              const float u0 = u2f(vu[j]), u1 = u2f(vu[j + 1]);
-              const float h0 = e0 / (1.0f + __expf(-e0)) * u0;
-              const float h1 = e1 / (1.0f + __expf(-e1)) * u1;
-              we[j / 2] = pack_bf16x2(e0, e1);
-              wu[j / 2] = pack_bf16x2(u0, u1);
-              wh[j / 2] = pack_bf16x2(h0, h1);
-            }
-            stage_row(se, lane, we, h * 4);
-            stage_row(su, lane, wu, h * 4);
-            stage_row(sh, lane, wh, h * 4);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&p.tmOut[0], se, n0 + c * 64, row0);
-            tma_store_2d(&p.tmOut[1], su, n0 + c * 64, row0);
-            tma_store_2d(&p.tmOut[2], sh, n0 + c * 64, row0);
-            tma_store_commit();
-          }
-        }
-      } else if constexpr (EPI == EPI_SWIGLU_BWD) {
-        // accumulator = dh; read the saved e, u for this thread's row and form de, du
-        const int grow = row0 + lane;
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c, ++chunk_ctr) {
-          uint8_t* sde = my_stg + (chunk_ctr & 1) * 8192;
-          uint8_t* sdu = sde + 4096;
-          if (lane == 0) tma_store_wait_read<1>();
-          __syncwarp();
-#pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
-            uint32_t vd[32];
-            tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, vd);
-            tmem_ld_wait();
-            const int col = n0 + c * 64 + h * 32;
-            uint32_t ev[16], uv[16];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const int cc = col + 8 * g;
-              if (grow < p.M && cc < p.N) {
-                const uint4 a = *reinterpret_cast<const uint4*>(p.e_in + (size_t)grow * p.ld_eu + cc);
-                const uint4 b = *reinterpret_cast<const uint4*>(p.u_in + (size_t)grow * p.ld_eu + cc);
-                ev[4 * g] = a.x; ev[4 * g + 1] = a.y; ev[4 * g + 2] = a.z; ev[4 * g + 3] = a.w;
-                uv[4 * g] = b.x; uv[4 * g + 1] = b.y; uv[4 * g + 2] = b.z; uv[4 * g + 3] = b.w;
-              } else {
-#pragma unroll
-                for (int z = 0; z < 4; ++z) ev[4 * g + z] = uv[4 * g + z] = 0u;
-              }
-            }
-            uint32_t wde[16], wdu[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 e = unpack_bf16x2(ev[j]);
-              const float2 u = unpack_bf16x2(uv[j]);
-              const float d0 = u2f(vd[2 * j]), d1 = u2f(vd[2 * j + 1]);
-              const float s0 = 1.0f / (1.0f + __expf(-e.x));
-              const float s1 = 1.0f / (1.0f + __expf(-e.y));
-              const float de0 = d0 * u.x * s0 * (1.0f + e.x * (1.0f - s0));
-              const float de1 = d1 * u.y * s1 * (1.0f + e.y * (1.0f - s1));
-              const float du0 = d0 * e.x * s0;
-              const float du1 = d1 * e.y * s1;
-              wde[j] = pack_bf16x2(de0, de1);
-              wdu[j] = pack_bf16x2(du0, du1);
-            }
-            stage_row(sde, lane, wde, h * 4);
-            stage_row(sdu, lane, wdu, h * 4);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&p.tmOut[0], sde, n0 + c * 64, row0);
-            tma_store_2d(&p.tmOut[1], sdu, n0 + c * 64, row0);
-            tma_store_commit();
-          }
-        }
-      }
+      epilogue_tile<EPI, N_OUT>(p, t_row, mt * BM + 32 * q, nt * N_OUT, lane, my_stg, chunk_ctr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
-    (void)ok;
     if (lane == 0) tma_store_wait_all<0>();
     __syncwarp();
   } else if (KSCALE) {
@@ -440,34 +483,8 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
           ok = false;
           break;
         }
-        if (tail) {
-          // the rank-r tail is not scaled: hand the stage straight on
-          mbar_arrive(&ready[stage]);
-        } else {
-          uint8_t* a = sA + stage * A_STAGE_BYTES;
-          const int k0 = ks * BK;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int ci = tid + 128 * i;
-            const int r = ci >> 3, pc = ci & 7;
-            const int j = pc ^ (r & 7);
-            const int kb = k0 + 8 * j;
-            uint4* ptr = reinterpret_cast<uint4*>(a + r * 128 + pc * 16);
-            uint4 v = *ptr;
-            float sc[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sc[e] = (kb + e < p.K0) ? __ldg(p.a_kscale + kb + e) : 0.0f;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = unpack_bf16x2(w[e]);
-              w[e] = pack_bf16x2(f.x * sc[2 * e], f.y * sc[2 * e + 1]);
-            }
-            *ptr = v;
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(&ready[stage]);
-        }
+        if (!tail) kscale_tile(p, sA + stage * A_STAGE_BYTES, ks, tid);  // the rank-r tail is not scaled
+        mbar_arrive(&ready[stage]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
@@ -480,6 +497,243 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ============================================================================ CTA-pair kernel
+// Cluster of 2: CTA rank 0 (leader) issues cta_group::2 MMAs of M = 256 (its 128 rows of A in
+// its SMEM, the peer's 128 rows in the peer's) x N = 256 (B columns 0..127 from the leader's
+// SMEM, 128..255 from the peer's); each CTA's TMEM receives its own 128 rows of D.
+//   full[s]      leader: 2 arrivals (both producers' expect_tx) + both CTAs' TMA bytes
+//                (K-scaling: each CTA's own loads, 1 arrival, waited by its scaling warps)
+//   ready[s]     leader, K-scaling only: one arrival per CTA after its scaling warps finish
+//   empty[s]     both CTAs: the leader's MMA commit, multicast to the pair
+//   acc_full[b]  both CTAs: the leader's MMA commit, multicast
+//   acc_empty[b] leader: 4 epilogue warps x 2 CTAs
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
+__global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __grid_constant__ TcParams p) {
+  using L = Layout<EPI, true>;
+  constexpr int STAGES = L::STAGES;
+  constexpr int N_OUT = STACKED ? BN / 2 : BN;        // logical output columns per tile
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  constexpr int PM = 2 * BM;                          // rows per pair tile
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + L::OFF_A;
+  uint8_t* sB = smem + L::OFF_B;
+  uint8_t* sStg = smem + L::OFF_STG;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* ready = bars + 2 * STAGES;
+  uint64_t* acc_full = bars + 3 * STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_full + 4;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;   // pair tiles (256 rows each)
+  const int nk0 = (p.K0 + BK - 1) / BK;
+  const int nk = nk0 + (HAS_TAIL ? 1 : 0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], KSCALE ? 1 : 2);
+      mbar_init(&empty[i], 1);
+      mbar_init(&ready[i], 2);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA0);
+    tma_prefetch_desc(&p.tmB0);
+    if (HAS_TAIL) {
+      tma_prefetch_desc(&p.tmA1);
+      tma_prefetch_desc(&p.tmB1);
+    }
+  }
+  if (warp == 1) {  // one warp in each CTA of the pair allocates the pair's TMEM columns
+    tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();   // barriers of both CTAs initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+        int mt, nt;
+        tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+        const int m0 = mt * PM + (int)rank * BM;
+        const int n0 = nt * N_OUT;
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait_cl(&empty[stage], phase ^ 1, p.timeout_ns, abort_flag, p.err, 0x201)) {
+            ok = false;
+            break;
+          }
+          const bool tail = HAS_TAIL && ks >= nk0;
+          uint32_t bar;
+          if (KSCALE) {
+            mbar_expect_tx(&full[stage], L::STAGE_BYTES);
+            bar = mapa_shared(smem_u32(&full[stage]), rank);
+          } else {
+            bar = mapa_shared(smem_u32(&full[stage]), 0);
+            mbar_expect_tx_cluster(bar, L::STAGE_BYTES);
+          }
+          uint8_t* a_dst = sA + stage * A_STAGE_BYTES;
+          uint8_t* b_dst = sB + stage * L::B_STAGE_BYTES;
+          if (!tail) {
+            const int kx = ks * BK;
+            tma_load_2d_pair(a_dst, &p.tmA0, bar, kx, m0);
+            if (B0_MN) {
+              const bool second = ks >= p.k0_split_steps;
+              const void* mp = second ? (const void*)&p.tmB0b : (const void*)&p.tmB0;
+              const int ky = second ? kx - p.k0_split_steps * BK : kx;
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                tma_load_2d_pair(b_dst + j * 8192, mp, bar, n0 + (int)rank * 128 + 64 * j, ky);
+            } else if (STACKED) {
+              tma_load_2d_pair(b_dst, rank ? (const void*)&p.tmB0b : (const void*)&p.tmB0, bar, kx, n0);
+            } else {
+              tma_load_2d_pair(b_dst, &p.tmB0, bar, kx, n0 + (int)rank * 128);
+            }
+          } else {
+            tma_load_2d_pair(a_dst, &p.tmA1, bar, 0, m0);
+            if (B1_MN) {
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                tma_load_2d_pair(b_dst + j * 8192, &p.tmB1, bar, n0 + (int)rank * 128 + 64 * j, 0);
+            } else if (STACKED) {
+              if (rank == 0) tma_load_2d_pair(b_dst, &p.tmB1, bar, 0, n0);
+              else tma_load_2d_pair(b_dst, &p.tmB1b, bar, p.tail_b1b_x, n0);
+            } else {
+              tma_load_2d_pair(b_dst, &p.tmB1, bar, 0, n0 + (int)rank * 128);
+            }
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) spin_ns(100000ull);  // unwind: give copies already issued time to land
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (leader CTA only)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc0 = umma_idesc_bf16(PM, BN, 0, B0_MN ? 1 : 0);
+      constexpr uint32_t idesc1 = umma_idesc_bf16(PM, BN, 0, B1_MN ? 1 : 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++it) {
+        const int buf = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_cl(&acc_empty[buf], acc_phase ^ 1, p.timeout_ns, abort_flag, p.err, 0x202)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int ks = 0; ks < nk; ++ks) {
+          const bool tail = HAS_TAIL && ks >= nk0;
+          uint64_t* wb = KSCALE ? &ready[stage] : &full[stage];
+          if (!mbar_wait_cl(wb, phase, p.timeout_ns, abort_flag, p.err, 0x203)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * A_STAGE_BYTES);
+          const uint32_t b_base = smem_u32(sB + stage * L::B_STAGE_BYTES);
+          const int nsub = tail ? (p.K1 + 15) / 16 : BK / 16;
+          const bool bmn = tail ? B1_MN : B0_MN;
+          for (int kk = 0; kk < nsub; ++kk) {
+            const uint64_t adesc = umma_smem_desc(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = bmn ? umma_smem_desc(b_base + kk * 2048, 8192, 1024)
+                                       : umma_smem_desc(b_base + kk * 32, 16, 1024);
+            umma_bf16_pair(d_tmem, adesc, bdesc, tail ? idesc1 : idesc0, (ks > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit_pair_mc(&empty[stage], 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(&acc_full[buf], 0x3);
+      }
+      umma_commit_pair_mc(drain, 0x1);
+      mbar_wait_drain(drain, 0, 20000000ull);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;
+    uint8_t* my_stg = sStg + (warp - 2) * (EpiCfg<EPI, true>::STG_BUFS * 4096);
+    int it = 0;
+    uint32_t chunk_ctr = 0;
+    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
+      const int buf = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait_cl(&acc_full[buf], acc_phase, p.timeout_ns, abort_flag, p.err, 0x204)) break;
+      tc_fence_after();
+      int mt, nt;
+      tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + buf * BN;
+      epilogue_tile<EPI, N_OUT>(p, t_row, mt * PM + (int)rank * BM + 32 * q, nt * N_OUT, lane, my_stg, chunk_ctr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[buf]), 0));
+    }
+    if (lane == 0) tma_store_wait_all<0>();
+    __syncwarp();
+  } else if (KSCALE) {
+    // ---------------------------------------------------------------- A-tile K-scaling (both CTAs)
+    const int tid = threadIdx.x - 192;  // 0..127
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
+      for (int ks = 0; ks < nk; ++ks) {
+        const bool tail = HAS_TAIL && ks >= nk0;
+        if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.err, 0x205)) {
+          ok = false;
+          break;
+        }
+        if (!tail) kscale_tile(p, sA + stage * A_STAGE_BYTES, ks, tid);
+        named_bar_sync(1, 128);
+        if (tid == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ready[stage]), 0));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();   // neither CTA leaves while its peer may still reach into it
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ============================================================================ host side
@@ -511,21 +765,6 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
-static cudaError_t launch_variant(const TcParams& p, cudaStream_t st, int grid) {
-  using L = Layout<BN, EPI>;
-  auto kern = tc_gemm_kernel<BN, B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  kern<<<grid, KSCALE ? 320 : 192, L::TOTAL, st>>>(p);
-  count_launch();
-  return cudaGetLastError();
-}
-
 int num_sms_current() {
   static int cached[64] = {0};
   int dev = 0;
@@ -539,18 +778,107 @@ int num_sms_current() {
   return cached[dev];
 }
 
-static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStream_t st, int grid);
+static int env_int(const char* name, int dflt) {
+  const char* e = getenv(name);
+  return e ? atoi(e) : dflt;
+}
+
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
+static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
+  using L = Layout<EPI, false>;
+  auto kern = tc_gemm_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int grid = num_sms_current();
+  // test knob: cap the persistent grid so that small problems still run several tiles per CTA
+  const int cap = env_int("LORA_GB300_MAX_CTAS", 0);
+  if (cap > 0 && cap < grid) grid = cap;
+  if (grid > tiles) grid = tiles;
+  kern<<<grid, KSCALE ? 320 : 192, L::TOTAL, st>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
+static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
+  using L = Layout<EPI, true>;
+  auto kern = tc_pair_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
+  static int max_clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(KSCALE ? 320 : 192, 1, 1);
+  cfg.dynamicSmemBytes = L::TOTAL;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * (num_sms_current() / 2), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters = n > 0 ? n : 1;
+    if (env_int("LORA_GB300_VERBOSE", 0))
+      fprintf(stderr, "[lora_gb300] pair GEMM: %d co-resident clusters of 2 CTAs, %d bytes smem\n", n, L::TOTAL);
+  }
+  int clusters = max_clusters;     // persistent: every cluster resident at once
+  const int cap = env_int("LORA_GB300_MAX_CTAS", 0) / 2;
+  if (cap > 0 && cap < clusters) clusters = cap;
+  if (clusters > tiles) clusters = tiles;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
+static cudaError_t launch_variant(const TcParams& p, cudaStream_t st, bool pair, int tiles) {
+  return pair ? launch_pair<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles)
+              : launch_one<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles);
+}
+
+static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStream_t st, bool pair, int tiles) {
+  switch (d.mode) {
+    case TC_FWD:
+      if (d.has_tail) return launch_variant<false, false, true, false, EPI_SCALE_BIAS, false>(p, st, pair, tiles);
+      return launch_variant<false, false, false, false, EPI_SCALE_BIAS, false>(p, st, pair, tiles);
+    case TC_BWD_DX:
+      if (d.a_kscale) {
+        if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS, true>(p, st, pair, tiles);
+        return launch_variant<true, false, false, true, EPI_SCALE_BIAS, true>(p, st, pair, tiles);
+      }
+      if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS, false>(p, st, pair, tiles);
+      return launch_variant<true, false, false, true, EPI_SCALE_BIAS, false>(p, st, pair, tiles);
+    case TC_SWIGLU_FWD:
+      return launch_variant<false, true, true, false, EPI_SWIGLU, false>(p, st, pair, tiles);
+    case TC_SWIGLU_BWD:
+      return launch_variant<true, false, true, true, EPI_SWIGLU_BWD, false>(p, st, pair, tiles);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// CTA-pair kernel unless LORA_GB300_GEMM_PAIR=0 (the one-CTA kernel is kept for comparison).
+static bool use_pair() { return env_int("LORA_GB300_GEMM_PAIR", 0) != 0; }
 
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   if (d.M <= 0 || d.N <= 0) return cudaSuccess;
+  const bool pair = use_pair();
   TcParams p;
   memset(&p, 0, sizeof(p));
-  constexpr int BN = 256;
   const bool stacked = d.mode == TC_SWIGLU_FWD;
-  const int bnb = stacked ? BN / 2 : BN;
-  const bool b0_mn = d.b0_mn, b1_mn = d.b1_mn;
+  // rows of a K-major B box: 256 (one CTA), 128 (stacked halves, or one CTA's half of a pair)
+  const int bnb = (stacked || pair) ? BN / 2 : BN;
   bool ok = make_map(&p.tmA0, d.A0, d.K0, d.M, d.lda0, BM);
-  if (b0_mn) {
+  if (d.b0_mn) {
     ok = ok && make_map(&p.tmB0, d.B0, d.N, d.b0_rows, d.ldb0, 64);
     if (d.B0b) ok = ok && make_map(&p.tmB0b, d.B0b, d.N, d.b0b_rows, d.ldb0, 64);
   } else {
@@ -559,7 +887,7 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   }
   if (d.has_tail) {
     ok = ok && make_map(&p.tmA1, d.A1, d.K1_a, d.M, d.lda1, BM);
-    if (b1_mn) ok = ok && make_map(&p.tmB1, d.B1, d.N, d.K1, d.ldb1, 64);
+    if (d.b1_mn) ok = ok && make_map(&p.tmB1, d.B1, d.N, d.K1, d.ldb1, 64);
     else {
       ok = ok && make_map(&p.tmB1, d.B1, d.K1_b, d.N, d.ldb1, bnb);
       if (stacked) ok = ok && make_map(&p.tmB1b, d.B1b, d.K1_b, d.N, d.ldb1, bnb);
@@ -573,11 +901,12 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.N = d.N;
   p.K0 = d.K0;
   p.K1 = d.K1;
-  p.num_m_tiles = (d.M + BM - 1) / BM;
+  const int tile_m = pair ? 2 * BM : BM;
+  p.num_m_tiles = (d.M + tile_m - 1) / tile_m;
   const int n_out = stacked ? BN / 2 : BN;
   p.num_n_tiles = (d.N + n_out - 1) / n_out;
-  p.group_m = 16;
-  p.k0_split_steps = b0_mn && d.B0b ? (d.k0_split / BK) : (1 << 30);
+  p.group_m = pair ? 8 : 16;
+  p.k0_split_steps = d.b0_mn && d.B0b ? (d.k0_split / BK) : (1 << 30);
   p.tail_b1b_x = d.b1b_x;
   p.col_scale = d.col_scale;
   p.bias = d.bias;
@@ -588,44 +917,15 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.err = d.err;
   p.timeout_ns = d.timeout_ns;
   const int tiles = p.num_m_tiles * p.num_n_tiles;
-  int grid = num_sms_current();
-  if (d.max_ctas > 0 && d.max_ctas < grid) grid = d.max_ctas;
-  // test knob: cap the persistent grid so that small problems still run several tiles per CTA
-  if (const char* env = getenv("LORA_GB300_MAX_CTAS")) {
-    const int v = atoi(env);
-    if (v > 0 && v < grid) grid = v;
-  }
-  if (grid > tiles) grid = tiles;
 
   // algorithmic flops of this launch: the base contraction plus the rank-r tail
   const double ntot = stacked ? 2.0 * d.N : (double)d.N;
   const double k1 = d.has_tail ? (stacked ? d.K1 / 2.0 : (double)d.K1) : 0.0;
   const double flops = 2.0 * d.M * ntot * ((double)d.K0 + k1);
   prof_mark(st, true, flops);
-  const cudaError_t e = launch_mode(d, p, st, grid);
+  const cudaError_t e = launch_mode(d, p, st, pair, tiles);
   prof_mark(st, false, 0.0);
   return e;
-}
-
-static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStream_t st, int grid) {
-  constexpr int BN = 256;
-  switch (d.mode) {
-    case TC_FWD:
-      if (d.has_tail) return launch_variant<BN, false, false, true, false, EPI_SCALE_BIAS, false>(p, st, grid);
-      return launch_variant<BN, false, false, false, false, EPI_SCALE_BIAS, false>(p, st, grid);
-    case TC_BWD_DX:
-      if (d.a_kscale) {
-        if (d.has_tail) return launch_variant<BN, true, false, true, true, EPI_SCALE_BIAS, true>(p, st, grid);
-        return launch_variant<BN, true, false, false, true, EPI_SCALE_BIAS, true>(p, st, grid);
-      }
-      if (d.has_tail) return launch_variant<BN, true, false, true, true, EPI_SCALE_BIAS, false>(p, st, grid);
-      return launch_variant<BN, true, false, false, true, EPI_SCALE_BIAS, false>(p, st, grid);
-    case TC_SWIGLU_FWD:
-      return launch_variant<BN, false, true, true, false, EPI_SWIGLU, false>(p, st, grid);
-    case TC_SWIGLU_BWD:
-      return launch_variant<BN, true, false, true, true, EPI_SWIGLU_BWD, false>(p, st, grid);
-  }
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace lg

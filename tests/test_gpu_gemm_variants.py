@@ -1,0 +1,93 @@
+"""Both tcgen05 GEMM kernels against the oracle: the one-CTA kernel (128 x 256 tiles) and the
+CTA-pair kernel (cta_group::2, 256 x 256 tiles over two SMs), selected per call with
+LORA_GB300_GEMM_PAIR, in every mode the layer uses (forward, dX with MN-major B, dX with the
+DoRA K-scaling warps, SwiGLU forward with stacked B, SwiGLU backward), with ragged M, N, K and
+with a capped grid so that every CTA (pair) runs several tiles."""
+import pytest
+import torch
+
+import datagen as D
+import oracle as O
+from parity import assert_close, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from dora_adapter_linear_gb300.build import build
+    build()
+    from dora_adapter_linear_gb300 import ops as _ops
+    return _ops
+
+
+@pytest.fixture(params=["one_cta", "pair"])
+def variant(request, monkeypatch):
+    monkeypatch.setenv("LORA_GB300_GEMM_PAIR", "1" if request.param == "pair" else "0")
+    return request.param
+
+
+def f64(t):
+    return None if t is None else to64(t)
+
+
+def _ws_ok(ops):
+    from dora_adapter_linear_gb300 import _lib as L
+    for buf in ops._WS.values():
+        assert L.lora_check_device_error(buf) == 0, "a kernel recorded a timed-out wait"
+
+
+@pytest.mark.parametrize("cap", ["0", "4"])
+def test_lora_fwd_bwd(ops, variant, cap, monkeypatch):
+    monkeypatch.setenv("LORA_GB300_MAX_CTAS", cap)
+    case = D.scaled(D.WORKLOADS["lora_4096_bf16"], M=600, d_in=328, d_out=776, r=16, bias=True)
+    t = D.make_linear(case)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s, g["bias"])
+    X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
+    assert_close(Y, O.lora_linear_fwd(X, W0, A, B, case.s, f64(t["bias"])), "bf16", "Y")
+    dX, dA, dB, _ = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
+    rX, rA, rB, _ = O.lora_linear_bwd(X, W0, A, B, case.s, f64(t["dY"]))
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    _ws_ok(ops)
+
+
+def test_dora_kscaled_dx(ops, variant, monkeypatch):
+    monkeypatch.setenv("LORA_GB300_MAX_CTAS", "4")
+    case = D.scaled(D.WORKLOADS["dora_4096x11008_bf16"], M=600, d_in=328, d_out=776, r=32)
+    t = D.make_linear(case)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    r0 = ops.dora_rownorm2(g["W0"])
+    Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps, g["bias"])
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    assert_close(Y, O.dora_linear_fwd(X, W0, A, B, m, case.s, case.eps, bias)[0], "bf16", "Y")
+    dX, dA, dB, dm, _ = ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V, g["dY"],
+                                            case.s, case.eps)
+    rX, rA, rB, rm, _ = O.dora_linear_bwd(X, W0, A, B, m, case.s, dY, case.eps)
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dm, rm[None], "bf16", "dm")
+    _ws_ok(ops)
+
+
+@pytest.mark.parametrize("I", [200, 384])
+def test_mlp_swiglu(ops, variant, I, monkeypatch):
+    monkeypatch.setenv("LORA_GB300_MAX_CTAS", "4")
+    case = D.scaled(D.WORKLOADS["mlp_swiglu_4096x14336_bf16"], M=600, H=200, I=I, r=16, alpha=24.0)
+    t = D.make_mlp(case)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
+    Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
+    args = tuple(x if isinstance(x, float) else f64(x) for x in
+                 (t["X"], t["Wg"], t["Ag"], t["Bg"], case.s, t["Wu"], t["Au"], t["Bu"], case.s,
+                  t["Wd"], t["Ad"], t["Bd"], case.s))
+    ry, re, ru, rh = O.mlp_swiglu_fwd(*args)
+    assert_close(saved["h"], rh, "bf16", "h")
+    assert_close(Y, ry, "bf16", "y")
+    gr = ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
+    ref = O.mlp_swiglu_bwd(*args, f64(t["dY"]))
+    for k in ("dX", "dAg", "dBu", "dAd"):
+        assert_close(gr[k], ref[k], "bf16", k)
+    _ws_ok(ops)
