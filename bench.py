@@ -392,7 +392,7 @@ def headline(args, L, ops, dist, world, peaks):
     }
 
 
-def extra_workloads(args, L, ops, peaks):
+def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8")):
     """DoRA, SwiGLU MLP and W8A8 workloads, each a fwd+bwd (fwd only for W8A8) step."""
     import torch
 
@@ -401,8 +401,17 @@ def extra_workloads(args, L, ops, peaks):
     dev = torch.device("cuda", torch.cuda.current_device())
     out = {}
     steps, warm = max(3, min(args.steps, 20)), 3
+    if "dora" in which:
+        out.update(_dora_workload(args, L, ops, peaks, D, dev, steps, warm))
+    if "mlp" in which:
+        out.update(_mlp_workload(args, L, ops, peaks, D, dev, steps, warm))
+    if "w8a8" in which:
+        out.update(_w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm))
+    return out
 
-    # DoRA rows
+
+def _dora_workload(args, L, ops, peaks, D, dev, steps, warm):
+    out = {}
     case = D.WORKLOADS["dora_4096x11008_bf16"]
     t = D.make_linear(case)
     g = {k: v.to(dev) for k, v in t.items() if v is not None}
@@ -421,9 +430,12 @@ def extra_workloads(args, L, ops, peaks):
                                    "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                                    "roofline": gemm_roofline(L, peaks, ms, steps + warm, False,
                                                              "dora_4096x11008_bf16")}
-    del g, t
+    return out
 
-    # SwiGLU MLP
+
+def _mlp_workload(args, L, ops, peaks, D, dev, steps, warm):
+    import torch
+    out = {}
     case = D.WORKLOADS["mlp_swiglu_4096x14336_bf16"]
     t = D.make_mlp(case)
     g = {k: v.to(dev) for k, v in t.items()}
@@ -444,8 +456,13 @@ def extra_workloads(args, L, ops, peaks):
                                                                    "mlp_swiglu_4096x14336_bf16")}
     del g, t, P
     torch.cuda.empty_cache()
+    return out
 
-    # W8A8 + LoRA forward (quantise X, int8 GEMM with LoRA epilogue)
+
+def _w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm):
+    """W8A8 + LoRA forward: quantise X (W-1), exact int8 product with the LoRA epilogue."""
+    import torch
+    out = {}
     case = D.WORKLOADS["w8a8_lora_3072"]
     t = D.make_w8a8(case)
     Wq, sw = O.quantize_rows(t["W0"].numpy())
@@ -458,15 +475,28 @@ def extra_workloads(args, L, ops, peaks):
     def w8_step():
         Xq, sx, Z = ops.w8a8_quantize_rows(X, A)
         ops.w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, case.s)
+    L.lora_prof_gemm(reset=True)
+    L.lora_prof_enable(True)
     ms, _, _ = timed(w8_step, steps, warm)
+    L.lora_prof_enable(False)
+    gms, gn, gfl = L.lora_prof_gemm(reset=True)
     for buf in ops._WS.values():
         if L.lora_check_device_error(buf) != 0:
             raise RuntimeError("a kernel recorded a timed-out wait in the workload breakdown")
     ops_int8 = 2 * case.M * case.d_in * case.d_out
     lora_fl = 2 * case.M * case.r * (case.d_in + case.d_out)
-    out["w8a8_lora_3072"] = {"ms_per_step": ms, "int8_tops": ops_int8 / (ms * 1e-3) / 1e12,
-                             "lora_tflops": lora_fl / (ms * 1e-3) / 1e12,
-                             "note": "int8 product on the warp-level integer MMA (sm_103a has no tcgen05 int8 kind)"}
+    rec = {"ms_per_step": ms, "int8_tops": ops_int8 / (ms * 1e-3) / 1e12,
+           "lora_tflops": lora_fl / (ms * 1e-3) / 1e12,
+           "note": "exact int8 product as two bf16 tcgen05 products of the split weight codes "
+                   "(w = 16 (w >> 4) + (w & 15)); sm_103a has no tcgen05 int8 kind"}
+    if gn:
+        ach = gfl / (gms * 1e-3) / 1e12   # bf16 tensor work of the split product
+        rec["roofline"] = {"kernel": "tc_gemm_kernel (W8A8 split-code mode)", "bound": "tensor",
+                           "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                           "frac": round(ach / peaks["bf16_tflops"], 4), "launches": gn,
+                           "avg_launch_ms": round(gms / gn, 4), "share_of_step": round(gms / ((steps + warm) * ms), 4),
+                           "flops_per_launch": gfl / gn, "traffic": None}
+    out["w8a8_lora_3072"] = rec
     return out
 
 
@@ -478,6 +508,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads", default="all", choices=["all", "headline"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None, choices=["dora", "mlp", "w8a8"],
+                    help="time one non-headline workload alone (for profiling) and print its record")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -506,6 +538,9 @@ def main():
     from dora_adapter_linear_gb300 import ops
 
     peaks = measured_peaks()
+    if args.only:
+        print(json.dumps(extra_workloads(args, L, ops, peaks, which=(args.only,))), flush=True)
+        return
     h = headline(args, L, ops, dist, world, peaks)
     extra = extra_workloads(args, L, ops, peaks) if args.workloads == "all" and rank == 0 else None
     cpu = None

@@ -59,7 +59,9 @@ _SIGS = {
     "lora_mlp_swiglu_bwd": (c_int, [POINTER(LoraMlpShape), P, POINTER(LoraProj), POINTER(LoraProj),
                                     POINTER(LoraProj), P, P, P, P, P, P, P, P, P, P, P, P, P, P, c_size_t, P]),
     "w8a8_quantize_rows": (c_int, [c_int64, c_int64, P, P, P, P, c_int64, P, P]),
-    "w8a8_lora_fwd": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, c_float, P, P, P, P]),
+    "w8a8_workspace_bytes": (c_size_t, [c_int64, c_int64, c_int64]),
+    "w8a8_lora_fwd": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, c_float, P, P, P, P, c_size_t,
+                              P]),
     "lora_debug_wait_timeout": (c_int, [P, c_uint32, P]),
     "lora_linear_fwd_noalloc": (c_int, [POINTER(LoraShape), P, P, P, P, P, c_float, P, P, P]),
     "lora_launch_count": (ctypes.c_uint64, []),
@@ -231,6 +233,11 @@ def w8a8_quantize_rows(rows, cols, X, Xq, sx, A=None, r=0, Z=None, stream=None):
         "w8a8_quantize_rows")
 
 
-def w8a8_lora_fwd(M, d_in, d_out, r, Xq, sx, Wq, sw, Z, B, s, bias, Y, acc_out=None, stream=None):
+def w8a8_workspace_bytes(M, d_in, d_out) -> int:
+    return _lib().w8a8_workspace_bytes(M, d_in, d_out)
+
+
+def w8a8_lora_fwd(M, d_in, d_out, r, Xq, sx, Wq, sw, Z, B, s, bias, Y, acc_out, ws, stream=None):
     _ck(_lib().w8a8_lora_fwd(M, d_in, d_out, r, ptr(Xq), ptr(sx), ptr(Wq), ptr(sw), ptr(Z), ptr(B), float(s),
-                             ptr(bias), ptr(Y), ptr(acc_out), _stream(stream)), "w8a8_lora_fwd")
+                             ptr(bias), ptr(Y), ptr(acc_out), ptr(ws),
+                             0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)), "w8a8_lora_fwd")

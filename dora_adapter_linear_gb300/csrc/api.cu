@@ -334,7 +334,7 @@ const char* lora_status_string(int status) {
   return "unknown status";
 }
 
-int lora_abi_version(void) { return 1; }
+int lora_abi_version(void) { return 2; }
 
 size_t lora_workspace_bytes(int op, const lora_shape* sh) {
   if (check_shape(sh) != LORA_OK) return 0;
@@ -951,9 +951,18 @@ lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t
   return LORA_OK;
 }
 
+// Largest d_in for which both split partial products keep every fp32 partial sum an integer
+// below 2^24 (|x| <= 127, |w >> 4| <= 8, |w & 15| <= 15: 127 * 15 * 8800 < 2^24).
+constexpr int64_t kW8ExactMaxK = 8800;
+
+size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out) {
+  if (M < 0 || d_in <= 0 || d_out <= 0) return 0;
+  return kErrBytes + al256((size_t)M * d_in * 2) + 2 * al256((size_t)d_out * d_in * 2);
+}
+
 lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq, const float* sx,
                           const int8_t* Wq, const float* sw, const void* Z, const void* B, float s, const void* bias,
-                          void* Y, int32_t* acc_out, void* stream) {
+                          void* Y, int32_t* acc_out, void* ws, size_t ws_bytes, void* stream) {
   if (M < 0 || d_in <= 0 || d_out <= 0) return LORA_ERR_INVALID_ARG;
   if (d_in % 32 || d_out % 8) return LORA_ERR_UNSUPPORTED;
   REQM(M, Xq); REQ(Wq);
@@ -963,10 +972,45 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
   if (Z && (r < 8 || r > 64 || r % 8)) return LORA_ERR_UNSUPPORTED;
   if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
   ALN(Xq); ALN(sx); ALN(Wq); ALN(sw); ALN(Z); ALN(B); ALN(bias); ALN(Y); ALN(acc_out);
+  lora_status e = check_ws(ws, ws_bytes, w8a8_workspace_bytes(M, d_in, d_out));
+  if (e != LORA_OK) return e;
   if (M == 0) return LORA_OK;
-  CK(w8a8_gemm(M, d_in, d_out, Z ? (int)r : 0, Xq, sx, Wq, sw, static_cast<const bf16*>(Z),
-               static_cast<const bf16*>(B), s, static_cast<const bf16*>(bias), static_cast<bf16*>(Y), acc_out,
-               (cudaStream_t)stream));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (d_in > kW8ExactMaxK || getenv("LORA_GB300_W8A8_IMMA")) {
+    CK(w8a8_gemm(M, d_in, d_out, Z ? (int)r : 0, Xq, sx, Wq, sw, static_cast<const bf16*>(Z),
+                 static_cast<const bf16*>(B), s, static_cast<const bf16*>(bias), static_cast<bf16*>(Y), acc_out, st));
+    return LORA_OK;
+  }
+  Carve c{static_cast<char*>(ws)};
+  uint32_t* err = c.take<uint32_t>(kErrBytes / 4);
+  bf16* Xb = c.take<bf16>((size_t)M * d_in);
+  bf16* Wh = c.take<bf16>((size_t)d_out * d_in);
+  bf16* Wl = c.take<bf16>((size_t)d_out * d_in);
+  CK(i8_to_bf16(Xq, M * d_in, Xb, st));
+  CK(i8_split_bf16(Wq, d_out * d_in, Wh, Wl, st));
+  TcGemmDesc d;
+  d.mode = TC_W8A8;
+  d.M = (int)M;
+  d.N = (int)d_out;
+  d.K0 = (int)d_in;
+  d.A0 = Xb;
+  d.lda0 = d_in;
+  d.B0 = Wh;
+  d.B0b = Wl;
+  d.ldb0 = d_in;
+  d.out[0] = Y;
+  d.ldo = d_out;
+  d.bias = static_cast<const bf16*>(bias);
+  d.sx = sx;
+  d.sw = sw;
+  d.lz = static_cast<const bf16*>(Z);
+  d.lb = static_cast<const bf16*>(B);
+  d.ls = s;
+  d.lr = Z ? (int)r : 0;
+  d.acc_out = acc_out;
+  d.err = err;
+  d.timeout_ns = wait_timeout_ns();
+  CK(tc_gemm(d, st));
   return LORA_OK;
 }
 

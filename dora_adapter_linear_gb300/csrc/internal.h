@@ -21,12 +21,14 @@ void prof_mark(cudaStream_t st, bool start, double flops);
 cudaError_t prof_collect(double* ms, int64_t* launches, double* flops, bool reset);
 
 // ------------------------------------------------------------------ tcgen05 GEMM engine
-enum EpiKind { EPI_SCALE_BIAS = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2 };
+enum EpiKind { EPI_SCALE_BIAS = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2, EPI_W8A8 = 3 };
 enum TcMode {
   TC_FWD = 0,          // A0 [M,K0] x B0 [N,K0]^T (+ A1 [M,K1] x B1 [N,K1]^T), epilogue scale/bias
   TC_BWD_DX = 1,       // A0 [M,K0] x B0 [K0,N] (MN-major) (+ A1 x B1 [K1,N]), optional A-scale along K
   TC_SWIGLU_FWD = 2,   // stacked gate/up weights, SwiGLU epilogue writing e, u, h
-  TC_SWIGLU_BWD = 3    // MN-major B, epilogue forms de, du from saved e, u
+  TC_SWIGLU_BWD = 3,   // MN-major B, epilogue forms de, du from saved e, u
+  TC_W8A8 = 4          // stacked [wh; wl] weight halves, epilogue forms the exact int32 product,
+                       // dequantises and adds the rank-r term
 };
 
 struct TcGemmDesc {
@@ -55,6 +57,14 @@ struct TcGemmDesc {
   const bf16* e_in = nullptr;
   const bf16* u_in = nullptr;
   int64_t ld_eu = 0;
+  // W8A8 epilogue: per-row / per-column dequant scales, rank-r term s * Z B^T, raw int32 output
+  const float* sx = nullptr;
+  const float* sw = nullptr;
+  const bf16* lz = nullptr;
+  const bf16* lb = nullptr;
+  float ls = 0.f;
+  int lr = 0;
+  int32_t* acc_out = nullptr;
   uint32_t* err = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int max_ctas = 0;
@@ -178,6 +188,9 @@ cudaError_t coldot_f32(const float* S, const float* Y, int64_t rows, int64_t K, 
 
 // ------------------------------------------------------------------ W8A8
 cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t* Xq, float* sx, cudaStream_t st);
+// int8 -> bf16 (exact), and the weight split w = 16 wh + wl (n multiple of 16)
+cudaError_t i8_to_bf16(const int8_t* q, int64_t n, bf16* out, cudaStream_t st);
+cudaError_t i8_split_bf16(const int8_t* q, int64_t n, bf16* hi, bf16* lo, cudaStream_t st);
 cudaError_t w8a8_gemm(int64_t M, int64_t K, int64_t N, int r, const int8_t* Xq, const float* sx, const int8_t* Wq,
                       const float* sw, const bf16* Z, const bf16* B, float s, const bf16* bias, bf16* Y,
                       int32_t* acc_out, cudaStream_t st);

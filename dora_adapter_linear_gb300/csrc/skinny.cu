@@ -15,13 +15,13 @@ namespace lg {
 // ============================================================================ rowproj
 namespace rp {
 constexpr int BMR = 32;        // rows per CTA
-constexpr int BKC = 64;        // K per stage
-constexpr int PITCH = 72;      // padded smem row pitch (elements) -> conflict-free ldmatrix
-constexpr int STAGES = 8;      // deep ring: ~28 KB of the streamed operand in flight per CTA
-constexpr int S_BYTES = BMR * PITCH * 2;       // 4608
-// U chunk: [R(+8 pad rows), 64] K-major or [64, R+8] R-major
+constexpr int BKC = 128;       // K per stage (256-byte row segments of S)
+constexpr int PITCH = BKC + 8; // padded smem row pitch (elements) -> conflict-free ldmatrix
+constexpr int STAGES = 6;      // deep ring: ~43 KB of the streamed operand in flight per CTA
+constexpr int S_BYTES = BMR * PITCH * 2;       // 8704
+// U chunk: [R(+8 pad rows), BKC] K-major or [BKC, R+8] R-major
 template <int R, bool KR>
-constexpr int u_bytes() { return KR ? 64 * (R + 8) * 2 : (R + 8) * PITCH * 2; }
+constexpr int u_bytes() { return KR ? BKC * (R + 8) * 2 : (R + 8) * PITCH * 2; }
 template <int R, bool KR>
 constexpr int stage_bytes() { return S_BYTES + u_bytes<R, KR>(); }
 }  // namespace rp
@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(128) rowproj_kernel(RowProjDesc d) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rg = warp & 1;        // 16-row group
-  const int kh = warp >> 1;       // which 32 columns of each 64-wide K chunk
+  const int kh = warp >> 1;       // which half of each BKC-wide K chunk
   const int64_t row0 = (int64_t)blockIdx.x * BMR;
   const int nkc = (int)((d.K + BKC - 1) / BKC);
   constexpr int UPITCH = U_KR ? (R + 8) : PITCH;
@@ -42,26 +42,27 @@ __global__ void __launch_bounds__(128) rowproj_kernel(RowProjDesc d) {
     uint8_t* sS = smem + stage * STAGE_BYTES;
     uint8_t* sU = sS + S_BYTES;
     const int64_t k0 = (int64_t)kc * BKC;
+    constexpr int CPS = BKC / 8;   // 16-byte chunks per staged row
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {  // 32 rows x 8 chunks = 256 chunks
+    for (int i = 0; i < BMR * CPS / 128; ++i) {
       const int ci = tid + 128 * i;
-      const int r = ci >> 3, c = ci & 7;
+      const int r = ci / CPS, c = ci % CPS;
       const int64_t gr = row0 + r, gk = k0 + c * 8;
       const bool ok = gr < d.rows && gk < d.K;
       const bf16* src = ok ? d.S + gr * d.lds + gk : d.S;
       cp_async16(sS + (r * PITCH + c * 8) * 2, src, ok);
     }
-    if (!U_KR) {  // U [R, K]: R rows x 8 chunks
-      for (int ci = tid; ci < R * 8; ci += 128) {
-        const int r = ci >> 3, c = ci & 7;
+    if (!U_KR) {  // U [R, K]: R rows x CPS chunks
+      for (int ci = tid; ci < R * CPS; ci += 128) {
+        const int r = ci / CPS, c = ci % CPS;
         const int64_t gk = k0 + c * 8;
         const bool ok = gk < d.K;
         const bf16* src = ok ? d.U + (int64_t)r * d.ldu + gk : d.U;
         cp_async16(sU + (r * UPITCH + c * 8) * 2, src, ok);
       }
-    } else {      // U [K, R]: 64 rows x R/8 chunks
+    } else {      // U [K, R]: BKC rows x R/8 chunks
       constexpr int CPR = R / 8;
-      for (int ci = tid; ci < 64 * CPR; ci += 128) {
+      for (int ci = tid; ci < BKC * CPR; ci += 128) {
         const int r = ci / CPR, c = ci % CPR;
         const int64_t gk = k0 + r;
         const bool ok = gk < d.K;
@@ -87,8 +88,8 @@ __global__ void __launch_bounds__(128) rowproj_kernel(RowProjDesc d) {
     const uint32_t sS = smem_u32(smem + stage * STAGE_BYTES);
     const uint32_t sU = sS + S_BYTES;
 #pragma unroll
-    for (int k2 = 0; k2 < 2; ++k2) {
-      const int kk = kh * 2 + k2;  // k16 step within the 64-wide chunk
+    for (int k2 = 0; k2 < BKC / 32; ++k2) {
+      const int kk = kh * (BKC / 32) + k2;  // k16 step within the BKC-wide chunk
       uint32_t a[4];
       ldsm_x4(a[0], a[1], a[2], a[3],
               sS + ((rg * 16 + (lane & 15)) * PITCH + kk * 16 + (lane >> 4) * 8) * 2);

@@ -43,6 +43,15 @@ struct TcParams {
   const bf16* e_in;
   const bf16* u_in;
   int ld_eu;
+  const float* sx;      // W8A8: per-row activation scales [M]
+  const float* sw;      // W8A8: per-column weight scales [N]
+  const bf16* lz;       // W8A8: rank-r input Z [M, lr] (or null)
+  const bf16* lb;       // W8A8: up-projection B [N, lr]
+  float ls;
+  int lr;
+  int32_t* acc_out;     // W8A8: raw int32 product [M, N] (or null)
+  int write_y;          // W8A8: 0 when only the raw product is wanted
+  int pair_leader_arms; // CTA pair: the leader posts the transaction bytes of both CTAs
   uint32_t* err;
   uint64_t timeout_ns;
 };
@@ -60,6 +69,8 @@ template <> struct EpiCfg<EPI_SWIGLU_BWD, false> { static constexpr int STAGES =
 template <> struct EpiCfg<EPI_SCALE_BIAS, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
 template <> struct EpiCfg<EPI_SWIGLU, true> { static constexpr int STAGES = 5, STG_BUFS = 3; };
 template <> struct EpiCfg<EPI_SWIGLU_BWD, true> { static constexpr int STAGES = 5, STG_BUFS = 4; };
+template <> struct EpiCfg<EPI_W8A8, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
+template <> struct EpiCfg<EPI_W8A8, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
 
 template <int EPI, bool PAIR>
 struct Layout {
@@ -233,6 +244,93 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
         tma_store_2d(&p.tmOut[0], sde, n0 + c * 64, row0);
         tma_store_2d(&p.tmOut[1], sdu, n0 + c * 64, row0);
         tma_store_commit();
+      }
+    }
+  } else if constexpr (EPI == EPI_W8A8) {
+    // accumulator columns [0, 128) = X wh^T, [128, 256) = X wl^T for outputs n0 .. n0 + 127;
+    // both are exact integers, so acc = 16 * hi + lo is the exact int32 product
+    const int grow = row0 + lane;
+    const bool row_ok = grow < p.M;
+    const float rs = (row_ok && p.write_y) ? p.sx[grow] : 0.f;
+    float zf[64];
+#pragma unroll
+    for (int j8 = 0; j8 < 8; ++j8) {
+      uint4 zv = make_uint4(0u, 0u, 0u, 0u);
+      if (row_ok && p.lz != nullptr && 8 * j8 < p.lr)
+        zv = *reinterpret_cast<const uint4*>(p.lz + (size_t)grow * p.lr + 8 * j8);
+      const uint32_t* zw = reinterpret_cast<const uint32_t*>(&zv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16x2(zw[e]);
+        zf[8 * j8 + 2 * e] = f.x;
+        zf[8 * j8 + 2 * e + 1] = f.y;
+      }
+    }
+#pragma unroll 1
+    for (int c = 0; c < N_OUT / 64; ++c, ++chunk_ctr) {
+      uint8_t* stg = my_stg + (chunk_ctr & 1) * 4096;
+      if (lane == 0) tma_store_wait_read<1>();
+      __syncwarp();
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t vh[32], vl[32];
+        tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, vh);
+        tmem_ld_32x32b_x32(t_row + BN / 2 + c * 64 + h * 32, vl);
+        tmem_ld_wait();
+        const int col0 = n0 + c * 64 + h * 32;
+        int acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 16 * __float2int_rn(u2f(vh[j])) + __float2int_rn(u2f(vl[j]));
+        if (p.acc_out != nullptr && row_ok) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (col0 + 4 * g < p.N)
+              *reinterpret_cast<int4*>(p.acc_out + (size_t)grow * p.N + col0 + 4 * g) =
+                  make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
+        }
+        if (p.write_y) {
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float y2[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int col = col0 + j + k;
+              float y = 0.f;
+              if (col < p.N) {
+                float lora = 0.f;
+                if (p.lz != nullptr) {
+#pragma unroll
+                  for (int j8 = 0; j8 < 8; ++j8) {
+                    if (8 * j8 < p.lr) {
+                      const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.lb + (size_t)col * p.lr + 8 * j8));
+                      const uint32_t* bw = reinterpret_cast<const uint32_t*>(&bv);
+#pragma unroll
+                      for (int e = 0; e < 4; ++e) {
+                        const float2 f = unpack_bf16x2(bw[e]);
+                        lora = fmaf(zf[8 * j8 + 2 * e], f.x, lora);
+                        lora = fmaf(zf[8 * j8 + 2 * e + 1], f.y, lora);
+                      }
+                    }
+                  }
+                }
+                y = (float)acc[j + k] * rs * __ldg(p.sw + col) + p.ls * lora;
+                if (p.bias != nullptr) y += __bfloat162float(p.bias[col]);
+              }
+              y2[k] = y;
+            }
+            w[j / 2] = pack_bf16x2(y2[0], y2[1]);
+          }
+          stage_row(stg, lane, w, h * 4);
+        }
+      }
+      if (p.write_y) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tmOut[0], stg, n0 + c * 64, row0);
+          tma_store_commit();
+        }
       }
     }
   }
@@ -543,7 +641,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], KSCALE ? 1 : 2);
+      mbar_init(&full[i], (KSCALE || p.pair_leader_arms) ? 1 : 2);
       mbar_init(&empty[i], 1);
       mbar_init(&ready[i], 2);
     }
@@ -595,7 +693,8 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
             bar = mapa_shared(smem_u32(&full[stage]), rank);
           } else {
             bar = mapa_shared(smem_u32(&full[stage]), 0);
-            mbar_expect_tx_cluster(bar, L::STAGE_BYTES);
+            if (!p.pair_leader_arms) mbar_expect_tx_cluster(bar, L::STAGE_BYTES);
+            else if (rank == 0) mbar_expect_tx(&full[stage], 2 * L::STAGE_BYTES);  // both CTAs' bytes
           }
           uint8_t* a_dst = sA + stage * A_STAGE_BYTES;
           uint8_t* b_dst = sB + stage * L::B_STAGE_BYTES;
@@ -809,7 +908,7 @@ static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
   auto kern = tc_pair_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
   static int max_clusters = 0;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -819,6 +918,12 @@ static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (const int pol = env_int("LORA_GB300_PAIR_POLICY", 0)) {  // 1 = spread, 2 = load balancing
+    attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+    attr[1].val.clusterSchedulingPolicyPreference =
+        pol == 2 ? cudaClusterSchedulingPolicyLoadBalancing : cudaClusterSchedulingPolicySpread;
+    cfg.numAttrs = 2;
+  }
   if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
     if (e != cudaSuccess) return e;
@@ -862,6 +967,8 @@ static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStrea
       return launch_variant<false, true, true, false, EPI_SWIGLU, false>(p, st, pair, tiles);
     case TC_SWIGLU_BWD:
       return launch_variant<true, false, true, true, EPI_SWIGLU_BWD, false>(p, st, pair, tiles);
+    case TC_W8A8:
+      return launch_variant<false, true, false, false, EPI_W8A8, false>(p, st, pair, tiles);
   }
   return cudaErrorInvalidValue;
 }
@@ -874,7 +981,7 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   const bool pair = use_pair();
   TcParams p;
   memset(&p, 0, sizeof(p));
-  const bool stacked = d.mode == TC_SWIGLU_FWD;
+  const bool stacked = d.mode == TC_SWIGLU_FWD || d.mode == TC_W8A8;
   // rows of a K-major B box: 256 (one CTA), 128 (stacked halves, or one CTA's half of a pair)
   const int bnb = (stacked || pair) ? BN / 2 : BN;
   bool ok = make_map(&p.tmA0, d.A0, d.K0, d.M, d.lda0, BM);
@@ -893,9 +1000,19 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
       if (stacked) ok = ok && make_map(&p.tmB1b, d.B1b, d.K1_b, d.N, d.ldb1, bnb);
     }
   }
-  const int nouts = d.mode == TC_SWIGLU_FWD ? 3 : (d.mode == TC_SWIGLU_BWD ? 2 : 1);
+  int nouts = d.mode == TC_SWIGLU_FWD ? 3 : (d.mode == TC_SWIGLU_BWD ? 2 : 1);
+  if (d.mode == TC_W8A8 && d.out[0] == nullptr) nouts = 0;   // raw int32 product only
   for (int i = 0; i < nouts; ++i) ok = ok && make_map(&p.tmOut[i], d.out[i], d.N, d.M, d.ldo, 32);
   if (!ok) return cudaErrorInvalidValue;
+  p.sx = d.sx;
+  p.sw = d.sw;
+  p.lz = d.lz;
+  p.lb = d.lb;
+  p.ls = d.ls;
+  p.lr = d.lr;
+  p.acc_out = d.acc_out;
+  p.write_y = d.out[0] != nullptr ? 1 : 0;
+  p.pair_leader_arms = env_int("LORA_GB300_PAIR_ARM", 0);
 
   p.M = d.M;
   p.N = d.N;

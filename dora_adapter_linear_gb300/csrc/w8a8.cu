@@ -62,6 +62,62 @@ cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ int8 codes as bf16 tensor-core operands
+// Every int8 value is exact in bf16.  The weight codes are split once more, w = 16 * wh + wl
+// with wh = w >> 4 in [-8, 7] (arithmetic shift) and wl = w & 15 in [0, 15], so that the two
+// bf16 GEMMs X wh^T and X wl^T accumulate integers whose every partial sum stays below 2^24
+// for d_in <= 8800: fp32 accumulation is then exact and acc = 16 acc_h + acc_l is the int32
+// product (the epilogue forms it).
+__global__ void i8_to_bf16_kernel(const int8_t* __restrict__ q, int64_t n16, bf16* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n16) return;
+  const uint4 raw = reinterpret_cast<const uint4*>(q)[i];
+  const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+  uint32_t w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2((float)b[2 * j], (float)b[2 * j + 1]);
+  uint4* o = reinterpret_cast<uint4*>(out) + 2 * i;
+  o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+__global__ void i8_split_bf16_kernel(const int8_t* __restrict__ q, int64_t n16, bf16* __restrict__ hi,
+                                     bf16* __restrict__ lo) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n16) return;
+  const uint4 raw = reinterpret_cast<const uint4*>(q)[i];
+  const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+  uint32_t wh[8], wl[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int x0 = b[2 * j], x1 = b[2 * j + 1];
+    wh[j] = pack_bf16x2((float)(x0 >> 4), (float)(x1 >> 4));
+    wl[j] = pack_bf16x2((float)(x0 & 15), (float)(x1 & 15));
+  }
+  uint4* oh = reinterpret_cast<uint4*>(hi) + 2 * i;
+  uint4* ol = reinterpret_cast<uint4*>(lo) + 2 * i;
+  oh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+  oh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+  ol[0] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+  ol[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
+}
+
+cudaError_t i8_to_bf16(const int8_t* q, int64_t n, bf16* out, cudaStream_t st) {
+  const int64_t n16 = n / 16;
+  if (n16 <= 0) return cudaSuccess;
+  i8_to_bf16_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(q, n16, out);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t i8_split_bf16(const int8_t* q, int64_t n, bf16* hi, bf16* lo, cudaStream_t st) {
+  const int64_t n16 = n / 16;
+  if (n16 <= 0) return cudaSuccess;
+  i8_split_bf16_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(q, n16, hi, lo);
+  count_launch();
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ int8 GEMM + epilogue
 namespace w8 {
 constexpr int BM = 128, BN = 128, BK = 64;  // BK in bytes (int8 elements)

@@ -122,5 +122,6 @@ def w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, s, bias=None, want_acc=False, want_y=Tru
     r = 0 if Z is None else Z.shape[1]
     Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=Xq.device) if want_y else None
     acc = torch.empty(M, d_out, dtype=torch.int32, device=Xq.device) if want_acc else None
-    L.w8a8_lora_fwd(M, d_in, d_out, r, Xq, sx, Wq, sw, Z, B, s, bias, Y, acc)
+    ws = workspace(L.w8a8_workspace_bytes(M, d_in, d_out), Xq.device)
+    L.w8a8_lora_fwd(M, d_in, d_out, r, Xq, sx, Wq, sw, Z, B, s, bias, Y, acc, ws)
     return Y, acc

@@ -233,6 +233,10 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
 lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t* Xq, float* sx,
                                const void* A, int64_t r, void* Z, void* stream);
 
+/* Bytes of workspace w8a8_lora_fwd needs: the error word plus the int8 codes re-laid out as
+ * bf16 tensor-core operands (X: M x d_in; W split into two d_out x d_in halves).  0 on bad input. */
+size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out);
+
 /* Y = float(acc) * sx[i] * sw[o] + s * (Z B^T)[i, o] (+ bias), acc = Xq Wq^T exact in int32.
  * "nunchaku-style kernel fusion" (OneTrainer #1680): commit reworking the 8-bit matmuls
  * (epilogues: raw product, per-row dequant, dequant plus rank-tiled low-rank update; no
@@ -242,11 +246,16 @@ lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t
  *   Z [M, r] bf16 ("lora_xd") and B [d_out, r] bf16 ("lora_up"): both NULL (no LoRA) or both set,
  *   bias [d_out] bf16 or NULL, Y [M, d_out] bf16 (or NULL when only acc_out is wanted),
  *   acc_out [M, d_out] int32 or NULL: the raw-product epilogue.  d_in multiple of 32.
+ *   ws: workspace of at least w8a8_workspace_bytes(M, d_in, d_out) bytes (256-byte aligned).
+ *   For d_in <= 8800 the product runs on the bf16 tensor cores with every weight code split as
+ *   w = 16 * (w >> 4) + (w & 15): both partial products accumulate integers below 2^24, so fp32
+ *   accumulation is exact and the int32 result is bit-identical to an integer GEMM.  Larger
+ *   d_in uses the warp-level integer MMA (sm_103a has no tcgen05 integer kind).
  */
 lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq,
                           const float* sx, const int8_t* Wq, const float* sw, const void* Z,
                           const void* B, float s, const void* bias, void* Y, int32_t* acc_out,
-                          void* stream);
+                          void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- tracing
  * Number of kernels this library has launched since it was loaded (host-side count of

@@ -233,6 +233,32 @@ def test_w8a8_acc_bit_exact_and_epilogue(ops, bias):
     assert_close(Y, ry, "bf16", "Y")
 
 
+@pytest.mark.parametrize("path", ["tensor_split", "integer_mma"])
+def test_w8a8_both_product_paths(ops, path, monkeypatch):
+    """The bf16 tensor-core path (w = 16 (w >> 4) + (w & 15)) and the integer MMA path give the
+    same exact int32 product and the same epilogue."""
+    if path == "integer_mma":
+        monkeypatch.setenv("LORA_GB300_W8A8_IMMA", "1")
+    case, t, Wq, sw, Xq, sx = w8_inputs(M=260, d_in=320, d_out=136, bias=True)
+    Z = (t["X"].double() @ t["A"].double().T).to(torch.bfloat16)
+    Y, acc = ops.w8a8_lora_fwd(gpu(torch.from_numpy(Xq)), gpu(torch.from_numpy(sx)), gpu(torch.from_numpy(Wq)),
+                               gpu(torch.from_numpy(sw)), gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]), want_acc=True)
+    ry, racc = O.w8a8_lora_fwd(Xq, sx, Wq, sw, f64(Z), f64(t["B"]), case.s, f64(t["bias"]))
+    np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), racc)
+    assert_close(Y, ry, "bf16", "Y")
+
+
+def test_w8a8_deep_k_uses_integer_path(ops):
+    """d_in above the exact-split bound (8800) runs the integer MMA; still bit-exact."""
+    rng = np.random.default_rng(5)
+    M, K, N = 64, 8832, 72
+    Xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    Wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    _, acc = ops.w8a8_lora_fwd(gpu(torch.from_numpy(Xq)), None, gpu(torch.from_numpy(Wq)), None, None, None, 0.0,
+                               want_acc=True, want_y=False)
+    np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), O.int8_accumulate(Xq, Wq))
+
+
 def test_w8a8_extreme_codes_exact(ops):
     """All-(+-127) operands: the worst-case |acc| = d_in * 127^2 stays exact in int32."""
     M, K, N = 130, 3072, 136
