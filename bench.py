@@ -497,6 +497,17 @@ def _w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm):
                            "avg_launch_ms": round(gms / gn, 4), "share_of_step": round(gms / ((steps + warm) * ms), 4),
                            "flops_per_launch": gfl / gn, "traffic": None}
     out["w8a8_lora_3072"] = rec
+
+    # backward through the int8 base (dX via the dequantised weight + LoRA dgrad, dA, dB)
+    dY = torch.randn(case.M, case.d_out, device=dev, dtype=torch.bfloat16)
+    Xq, sx, Z = ops.w8a8_quantize_rows(X, A)
+
+    def w8_bwd_step():
+        ops.w8a8_lora_bwd(X, Wq, sw, A, B, Z, dY, case.s)
+    ms_b, _, _ = timed(w8_bwd_step, steps, warm)
+    fb = 2 * case.M * case.d_in * case.d_out + 4 * case.M * case.r * (case.d_in + case.d_out)
+    out["w8a8_lora_3072_bwd"] = {"ms_per_step": ms_b, "tflops": fb / (ms_b * 1e-3) / 1e12,
+                                 "frac_of_bf16_peak": fb / (ms_b * 1e-3) / 1e12 / peaks["bf16_tflops"]}
     return out
 
 

@@ -64,6 +64,9 @@ _SIGS = {
                               P]),
     "lora_debug_wait_timeout": (c_int, [P, c_uint32, P]),
     "lora_linear_fwd_noalloc": (c_int, [POINTER(LoraShape), P, P, P, P, P, c_float, P, P, P]),
+    "w8a8_bwd_workspace_bytes": (c_size_t, [c_int64, c_int64, c_int64, c_int64]),
+    "w8a8_lora_bwd": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, P, c_float, P, P, P, P, P,
+                              c_size_t, P]),
     "lora_launch_count": (ctypes.c_uint64, []),
     "lora_prof_enable": (c_int, [c_int]),
     "lora_prof_gemm": (c_int, [POINTER(ctypes.c_double), POINTER(c_int64), POINTER(ctypes.c_double), c_int]),
@@ -231,6 +234,16 @@ def lora_mlp_swiglu_bwd(sh, X, gate, up, down, e_saved, u_saved, h_saved, Zgu_sa
 def w8a8_quantize_rows(rows, cols, X, Xq, sx, A=None, r=0, Z=None, stream=None):
     _ck(_lib().w8a8_quantize_rows(rows, cols, ptr(X), ptr(Xq), ptr(sx), ptr(A), r, ptr(Z), _stream(stream)),
         "w8a8_quantize_rows")
+
+
+def w8a8_bwd_workspace_bytes(M, d_in, d_out, r) -> int:
+    return _lib().w8a8_bwd_workspace_bytes(M, d_in, d_out, r)
+
+
+def w8a8_lora_bwd(M, d_in, d_out, r, X, Wq, sw, A, B, Z_saved, dY, s, dX, dA, dB, dbias, ws, stream=None):
+    _ck(_lib().w8a8_lora_bwd(M, d_in, d_out, r, ptr(X), ptr(Wq), ptr(sw), ptr(A), ptr(B), ptr(Z_saved), ptr(dY),
+                             float(s), ptr(dX), ptr(dA), ptr(dB), ptr(dbias), ptr(ws),
+                             0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)), "w8a8_lora_bwd")
 
 
 def w8a8_workspace_bytes(M, d_in, d_out) -> int:

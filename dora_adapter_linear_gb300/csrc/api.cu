@@ -1007,11 +1007,46 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
   d.lb = static_cast<const bf16*>(B);
   d.ls = s;
   d.lr = Z ? (int)r : 0;
+  if (Z) {  // rank-r term Z B^T as a tail MMA into its own accumulator region
+    d.has_tail = true;
+    d.A1 = Z;
+    d.lda1 = r;
+    d.K1 = (int)r;
+    d.K1_a = (int)r;
+    d.B1 = B;
+    d.ldb1 = r;
+    d.K1_b = (int)r;
+  }
   d.acc_out = acc_out;
   d.err = err;
   d.timeout_ns = wait_timeout_ns();
   CK(tc_gemm(d, st));
   return LORA_OK;
+}
+
+size_t w8a8_bwd_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int64_t r) {
+  lora_shape sh{M, d_in, d_out, r, LORA_BF16};
+  const size_t lin = lora_workspace_bytes(LORA_OP_LINEAR_BWD, &sh);
+  if (lin == 0) return 0;
+  return lin + al256((size_t)d_out * d_in * 2);
+}
+
+lora_status w8a8_lora_bwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const void* X, const int8_t* Wq,
+                          const float* sw, const void* A, const void* B, const void* Z_saved, const void* dY,
+                          float s, void* dX, void* dA, void* dB, void* dbias, void* ws, size_t ws_bytes,
+                          void* stream) {
+  lora_shape sh{M, d_in, d_out, r, LORA_BF16};
+  lora_status e = check_shape(&sh);
+  if (e != LORA_OK) return e;
+  if (d_in % 16) return LORA_ERR_UNSUPPORTED;
+  REQ(Wq); REQ(sw);
+  ALN(Wq); ALN(sw);
+  const size_t lin = lora_workspace_bytes(LORA_OP_LINEAR_BWD, &sh);
+  if ((e = check_ws(ws, ws_bytes, w8a8_bwd_workspace_bytes(M, d_in, d_out, r))) != LORA_OK) return e;
+  // the frozen int8 weight in real units, then the bf16 LoRA backward over it
+  bf16* Wd = reinterpret_cast<bf16*>(static_cast<char*>(ws) + lin);
+  if (M > 0) CK(i8_dequant_rows_bf16(Wq, sw, d_out, d_in, Wd, (cudaStream_t)stream));
+  return lora_linear_bwd(&sh, X, Wd, A, B, Z_saved, dY, s, dX, dA, dB, dbias, ws, lin, stream);
 }
 
 }  // extern "C"

@@ -191,6 +191,9 @@ cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t
 // int8 -> bf16 (exact), and the weight split w = 16 wh + wl (n multiple of 16)
 cudaError_t i8_to_bf16(const int8_t* q, int64_t n, bf16* out, cudaStream_t st);
 cudaError_t i8_split_bf16(const int8_t* q, int64_t n, bf16* hi, bf16* lo, cudaStream_t st);
+// out[o, k] = bf16(sw[o] * q[o, k]) (cols multiple of 16)
+cudaError_t i8_dequant_rows_bf16(const int8_t* q, const float* sw, int64_t rows, int64_t cols, bf16* out,
+                                 cudaStream_t st);
 cudaError_t w8a8_gemm(int64_t M, int64_t K, int64_t N, int r, const int8_t* Xq, const float* sx, const int8_t* Wq,
                       const float* sw, const bf16* Z, const bf16* B, float s, const bf16* bias, bf16* Y,
                       int32_t* acc_out, cudaStream_t st);

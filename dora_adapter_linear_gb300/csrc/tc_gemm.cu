@@ -248,24 +248,11 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
     }
   } else if constexpr (EPI == EPI_W8A8) {
     // accumulator columns [0, 128) = X wh^T, [128, 256) = X wl^T for outputs n0 .. n0 + 127;
-    // both are exact integers, so acc = 16 * hi + lo is the exact int32 product
+    // both are exact integers, so acc = 16 * hi + lo is the exact int32 product.  Columns
+    // [256, 384) hold the rank-r term Z B^T (tail MMA) when a low-rank input is given.
     const int grow = row0 + lane;
     const bool row_ok = grow < p.M;
     const float rs = (row_ok && p.write_y) ? p.sx[grow] : 0.f;
-    float zf[64];
-#pragma unroll
-    for (int j8 = 0; j8 < 8; ++j8) {
-      uint4 zv = make_uint4(0u, 0u, 0u, 0u);
-      if (row_ok && p.lz != nullptr && 8 * j8 < p.lr)
-        zv = *reinterpret_cast<const uint4*>(p.lz + (size_t)grow * p.lr + 8 * j8);
-      const uint32_t* zw = reinterpret_cast<const uint32_t*>(&zv);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_bf16x2(zw[e]);
-        zf[8 * j8 + 2 * e] = f.x;
-        zf[8 * j8 + 2 * e + 1] = f.y;
-      }
-    }
 #pragma unroll 1
     for (int c = 0; c < N_OUT / 64; ++c, ++chunk_ctr) {
       uint8_t* stg = my_stg + (chunk_ctr & 1) * 4096;
@@ -289,6 +276,14 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
                   make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
         }
         if (p.write_y) {
+          uint32_t vr[32];
+          if (p.lz != nullptr) {
+            tmem_ld_32x32b_x32(t_row + BN + c * 64 + h * 32, vr);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) vr[j] = 0u;
+          }
           uint32_t w[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
@@ -298,23 +293,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
               const int col = col0 + j + k;
               float y = 0.f;
               if (col < p.N) {
-                float lora = 0.f;
-                if (p.lz != nullptr) {
-#pragma unroll
-                  for (int j8 = 0; j8 < 8; ++j8) {
-                    if (8 * j8 < p.lr) {
-                      const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.lb + (size_t)col * p.lr + 8 * j8));
-                      const uint32_t* bw = reinterpret_cast<const uint32_t*>(&bv);
-#pragma unroll
-                      for (int e = 0; e < 4; ++e) {
-                        const float2 f = unpack_bf16x2(bw[e]);
-                        lora = fmaf(zf[8 * j8 + 2 * e], f.x, lora);
-                        lora = fmaf(zf[8 * j8 + 2 * e + 1], f.y, lora);
-                      }
-                    }
-                  }
-                }
-                y = (float)acc[j + k] * rs * __ldg(p.sw + col) + p.ls * lora;
+                y = (float)acc[j + k] * rs * __ldg(p.sw + col) + p.ls * u2f(vr[j + k]);
                 if (p.bias != nullptr) y += __bfloat162float(p.bias[col]);
               }
               y2[k] = y;
@@ -450,7 +429,8 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
             break;
           }
           const bool tail = HAS_TAIL && ks >= nk0;
-          mbar_expect_tx(&full[stage], L::STAGE_BYTES);
+          // the W8A8 tail stages only the rank-r B rows of this tile (no second stacked half)
+          mbar_expect_tx(&full[stage], (EPI == EPI_W8A8 && tail) ? A_STAGE_BYTES + BNB * 128 : L::STAGE_BYTES);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           uint8_t* a_dst = sA + stage * A_STAGE_BYTES;
@@ -477,7 +457,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
               for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &p.tmB1, &full[stage], n0 + 64 * j, 0);
             } else if (STACKED) {
               tma_load_2d(b_dst, &p.tmB1, &full[stage], 0, n0);
-              tma_load_2d(b_dst + BNB * 128, &p.tmB1b, &full[stage], p.tail_b1b_x, n0);
+              if (EPI != EPI_W8A8) tma_load_2d(b_dst + BNB * 128, &p.tmB1b, &full[stage], p.tail_b1b_x, n0);
             } else {
               tma_load_2d(b_dst, &p.tmB1, &full[stage], 0, n0);
             }
@@ -498,15 +478,18 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      // W8A8: one accumulator set per tile, [0,128) hi, [128,256) lo, [256,384) the rank-r term
+      // (N = 128 tail MMA), so that hi and lo stay exact integers
+      constexpr bool W8 = EPI == EPI_W8A8;
       constexpr uint32_t idesc0 = umma_idesc_bf16(BM, BN, 0, B0_MN ? 1 : 0);
-      constexpr uint32_t idesc1 = umma_idesc_bf16(BM, BN, 0, B1_MN ? 1 : 0);
+      constexpr uint32_t idesc1 = W8 ? umma_idesc_bf16(BM, BN / 2, 0, 0) : umma_idesc_bf16(BM, BN, 0, B1_MN ? 1 : 0);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
-        const int buf = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
+        const int buf = W8 ? 0 : (it & 1);
+        const uint32_t acc_phase = W8 ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
         if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, p.timeout_ns, abort_flag, p.err, 0x102)) {
           ok = false;
           break;
@@ -531,7 +514,10 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
             const uint64_t adesc = umma_smem_desc(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc = bmn ? umma_smem_desc(b_base + kk * 2048, 8192, 1024)
                                        : umma_smem_desc(b_base + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, tail ? idesc1 : idesc0, (ks > 0 || kk > 0) ? 1u : 0u);
+            if (W8 && tail)
+              umma_bf16(d_tmem + 2 * (BN / 2), adesc, bdesc, idesc1, kk > 0 ? 1u : 0u);
+            else
+              umma_bf16(d_tmem, adesc, bdesc, tail ? idesc1 : idesc0, (ks > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -554,8 +540,8 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
     int it = 0;
     uint32_t chunk_ctr = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-      const int buf = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
+      const int buf = (EPI == EPI_W8A8) ? 0 : (it & 1);
+      const uint32_t acc_phase = (EPI == EPI_W8A8) ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
       if (!mbar_wait(&acc_full[buf], acc_phase, p.timeout_ns, abort_flag, p.err, 0x104)) break;
       tc_fence_after();
       int mt, nt;
@@ -967,8 +953,9 @@ static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStrea
       return launch_variant<false, true, true, false, EPI_SWIGLU, false>(p, st, pair, tiles);
     case TC_SWIGLU_BWD:
       return launch_variant<true, false, true, true, EPI_SWIGLU_BWD, false>(p, st, pair, tiles);
-    case TC_W8A8:
-      return launch_variant<false, true, false, false, EPI_W8A8, false>(p, st, pair, tiles);
+    case TC_W8A8:  // one-CTA kernel only (its accumulator layout is per-CTA)
+      if (d.has_tail) return launch_one<false, true, true, false, EPI_W8A8, false>(p, st, tiles);
+      return launch_one<false, true, false, false, EPI_W8A8, false>(p, st, tiles);
   }
   return cudaErrorInvalidValue;
 }
@@ -978,7 +965,7 @@ static bool use_pair() { return env_int("LORA_GB300_GEMM_PAIR", 0) != 0; }
 
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   if (d.M <= 0 || d.N <= 0) return cudaSuccess;
-  const bool pair = use_pair();
+  const bool pair = use_pair() && d.mode != TC_W8A8;
   TcParams p;
   memset(&p, 0, sizeof(p));
   const bool stacked = d.mode == TC_SWIGLU_FWD || d.mode == TC_W8A8;
@@ -997,7 +984,7 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
     if (d.b1_mn) ok = ok && make_map(&p.tmB1, d.B1, d.N, d.K1, d.ldb1, 64);
     else {
       ok = ok && make_map(&p.tmB1, d.B1, d.K1_b, d.N, d.ldb1, bnb);
-      if (stacked) ok = ok && make_map(&p.tmB1b, d.B1b, d.K1_b, d.N, d.ldb1, bnb);
+      if (stacked && d.mode != TC_W8A8) ok = ok && make_map(&p.tmB1b, d.B1b, d.K1_b, d.N, d.ldb1, bnb);
     }
   }
   int nouts = d.mode == TC_SWIGLU_FWD ? 3 : (d.mode == TC_SWIGLU_BWD ? 2 : 1);
@@ -1012,7 +999,7 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.lr = d.lr;
   p.acc_out = d.acc_out;
   p.write_y = d.out[0] != nullptr ? 1 : 0;
-  p.pair_leader_arms = env_int("LORA_GB300_PAIR_ARM", 0);
+  p.pair_leader_arms = env_int("LORA_GB300_PAIR_ARM", 1);
 
   p.M = d.M;
   p.N = d.N;

@@ -102,6 +102,32 @@ __global__ void i8_split_bf16_kernel(const int8_t* __restrict__ q, int64_t n16, 
   ol[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
 }
 
+// W_deq[o, k] = bf16(sw[o] * q[o, k]): the int8 base weight in real units, the B operand of
+// the backward's dX product (the frozen weight, re-laid out once per call like a k-major copy).
+__global__ void i8_dequant_rows_kernel(const int8_t* __restrict__ q, const float* __restrict__ sw, int64_t cols,
+                                       int64_t n16, bf16* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n16) return;
+  const float sc = sw[(i * 16) / cols];
+  const uint4 raw = reinterpret_cast<const uint4*>(q)[i];
+  const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+  uint32_t w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(sc * (float)b[2 * j], sc * (float)b[2 * j + 1]);
+  uint4* o = reinterpret_cast<uint4*>(out) + 2 * i;
+  o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+cudaError_t i8_dequant_rows_bf16(const int8_t* q, const float* sw, int64_t rows, int64_t cols, bf16* out,
+                                 cudaStream_t st) {
+  const int64_t n16 = rows * cols / 16;  // cols is a multiple of 16: a group never straddles rows
+  if (n16 <= 0) return cudaSuccess;
+  i8_dequant_rows_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(q, sw, cols, n16, out);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t i8_to_bf16(const int8_t* q, int64_t n, bf16* out, cudaStream_t st) {
   const int64_t n16 = n / 16;
   if (n16 <= 0) return cudaSuccess;

@@ -116,6 +116,18 @@ def w8a8_quantize_rows(X, A=None):
     return Xq, sx, Z
 
 
+def w8a8_lora_bwd(X, Wq, sw, A, B, Z, dY, s, need_dx=True, need_dbias=False):
+    M, d_in = X.shape
+    d_out, r = Wq.shape[0], A.shape[0]
+    dX = torch.empty_like(X) if need_dx else None
+    dA = torch.empty_like(A)
+    dB = torch.empty_like(B)
+    dbias = torch.empty(d_out, dtype=X.dtype, device=X.device) if need_dbias else None
+    ws = workspace(L.w8a8_bwd_workspace_bytes(M, d_in, d_out, r), X.device)
+    L.w8a8_lora_bwd(M, d_in, d_out, r, X, Wq, sw, A, B, Z, dY, s, dX, dA, dB, dbias, ws)
+    return dX, dA, dB, dbias
+
+
 def w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, s, bias=None, want_acc=False, want_y=True):
     M, d_in = Xq.shape
     d_out = Wq.shape[0]

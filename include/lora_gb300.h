@@ -272,6 +272,27 @@ lora_status lora_prof_enable(int on);
  * recorded events.  Any output pointer may be NULL.  reset != 0 clears the record. */
 lora_status lora_prof_gemm(double* ms, int64_t* launches, double* flops, int reset);
 
+/* Bytes of workspace w8a8_lora_bwd needs (0 on bad input). */
+size_t w8a8_bwd_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int64_t r);
+
+/* Backward of the W8A8 + LoRA layer with the int8 base weight frozen.  The activation quantiser
+ * is taken as straight-through (its gradient passes unchanged; the pages do not say otherwise),
+ * so with W_deq = diag(sw) Wq:
+ *   dX = dY W_deq + s (dY B) A,  dA = s (dY B)^T X,  dB = s dY^T Z,  dbias = colsum(dY).
+ * "nunchaku-style kernel fusion" (OneTrainer #1680), commit reworking the 8-bit matmuls (the
+ * backward's B operand is re-laid out for the tensor cores; the LoRA dgrad folds into the
+ * backward; the autograd Function owns the down-projection).
+ *   X [M, d_in] bf16 (the unquantised input), Wq [d_out, d_in] int8, sw [d_out] fp32,
+ *   A [r, d_in], B [d_out, r], Z_saved [M, r] (X A^T) or NULL, dY [M, d_out] (all bf16);
+ *   dX [M, d_in] or NULL, dA [r, d_in], dB [d_out, r], dbias [d_out] or NULL.
+ *   d_in multiple of 16; ws of at least w8a8_bwd_workspace_bytes() bytes: the weight is
+ *   dequantised into it once per call (a bf16 [d_out, d_in] copy), then the bf16 LoRA backward
+ *   runs over it. */
+lora_status w8a8_lora_bwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const void* X, const int8_t* Wq,
+                          const float* sw, const void* A, const void* B, const void* Z_saved, const void* dY,
+                          float s, void* dX, void* dA, void* dB, void* dbias, void* ws, size_t ws_bytes,
+                          void* stream);
+
 /* Test hook for the bounded-wait machinery: launches one CTA that waits on an mbarrier
  * that nothing ever arrives on, with a limit of `timeout_us` microseconds; the kernel then
  * records LORA_ERR_DEVICE_TIMEOUT in the error word of `ws` and returns.  It faults and

@@ -26,7 +26,7 @@ import numpy as np
 __all__ = [
     "f64", "adapted_weight", "lora_linear_fwd", "lora_linear_bwd", "dora_rownorm2",
     "dora_linear_fwd", "dora_linear_bwd", "silu", "dsilu", "mlp_swiglu_fwd", "mlp_swiglu_bwd",
-    "quantize_rows", "int8_accumulate", "w8a8_lora_fwd",
+    "quantize_rows", "int8_accumulate", "w8a8_lora_fwd", "w8a8_dequant_weight", "w8a8_lora_bwd",
     "lora_fwd_rows", "lora_bwd_sampled", "dora_fwd_rows", "dora_bwd_sampled", "dora_bwd_rows_sampled",
     "mlp_fwd_rows", "mlp_bwd_rows",
 ]
@@ -254,6 +254,25 @@ def w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, s, bias=None, acc=None):
     if bias is not None:
         y = y + f64(bias)[None, :]
     return y, acc
+
+
+def w8a8_dequant_weight(Wq, sw):
+    """W_deq = diag(sw) Wq: the frozen int8 base weight in real units."""
+    return f64(sw)[:, None] * np.asarray(Wq, dtype=np.float64)
+
+
+def w8a8_lora_bwd(X, Wq, sw, A, B, s, dY):
+    """Backward of the W8A8 + LoRA layer with W_deq frozen.
+
+    "nunchaku-style kernel fusion" (#1680), commit reworking the 8-bit matmuls: the backward
+    runs dX through the 8-bit weight (its B operand rewritten k-major) and folds the LoRA dgrad
+    into the same pass; the autograd Function owns the down-projection.  The pages do not say
+    how the activation quantiser is differentiated; the reading taken is the straight-through
+    one (the quantiser passes gradients unchanged), so the layer's gradients are those of
+    y = X W_deq^T + s (X A^T) B^T + bias with X the unquantised input:
+      dX = dY W',  dA = s B^T dW',  dB = s dW' A^T,  dbias = colsum(dY),  W' = W_deq + s B A.
+    """
+    return lora_linear_bwd(f64(X), w8a8_dequant_weight(Wq, sw), f64(A), f64(B), s, f64(dY))
 
 
 # ----------------------------------------------------------------------------- sampled forms

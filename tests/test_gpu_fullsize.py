@@ -177,3 +177,15 @@ def test_full_w8a8_3072(ops):
     assert_close(Z[rows], Zr, "bf16", "Z rows")
     ry, _ = O.w8a8_lora_fwd(rq, rs, Wq, sw, f64(Z[rows].cpu()), f64(t["B"]), case.s, acc=racc)
     assert_close(Y[rows], ry, "bf16", "Y rows")
+    # backward through the int8 base, sampled rows / columns of the gradients
+    g = torch.Generator().manual_seed(78)
+    dY = torch.randn(case.M, case.d_out, generator=g).to(torch.bfloat16)
+    dX, dA, dB, _ = ops.w8a8_lora_bwd(X, gpu(torch.from_numpy(Wq)), gpu(torch.from_numpy(sw)), gpu(t["A"]),
+                                      gpu(t["B"]), Z, gpu(dY), case.s)
+    torch.cuda.synchronize()
+    cols, orows = [0, 1000, 3071], [0, 1500, 3071]
+    sX, sA, sB, _ = O.lora_bwd_sampled(f64(t["X"]), O.w8a8_dequant_weight(Wq, sw), f64(t["A"]), f64(t["B"]), case.s,
+                                       f64(dY), rows, cols, orows)
+    assert_close(dX[rows], sX, "bf16", "dX rows")
+    assert_close(dA[:, cols].T, sA.T, "bf16", "dA columns")
+    assert_close(dB[orows], sB, "bf16", "dB rows")

@@ -259,6 +259,23 @@ def test_w8a8_deep_k_uses_integer_path(ops):
     np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), O.int8_accumulate(Xq, Wq))
 
 
+@pytest.mark.parametrize("bias", [False, True])
+def test_w8a8_bwd(ops, bias):
+    """Backward through the int8 base (straight-through activation quantiser) with the LoRA dgrad."""
+    case, t, Wq, sw, Xq, sx = w8_inputs(M=300, d_in=352, d_out=264, bias=bias)
+    g = torch.Generator().manual_seed(77)
+    dY = torch.randn(case.M, case.d_out, generator=g).to(torch.bfloat16)
+    X, A, B = gpu(t["X"]), gpu(t["A"]), gpu(t["B"])
+    Z = (t["X"].double() @ t["A"].double().T).to(torch.bfloat16)
+    dX, dA, dB, db = ops.w8a8_lora_bwd(X, gpu(torch.from_numpy(Wq)), gpu(torch.from_numpy(sw)), A, B, gpu(Z), gpu(dY),
+                                       case.s, need_dbias=True)
+    rX, rA, rB, rb = O.w8a8_lora_bwd(f64(t["X"]), Wq, sw, f64(t["A"]), f64(t["B"]), case.s, f64(dY))
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dB, rB, "bf16", "dB")
+    assert_close(db, rb[None], "bf16", "dbias")
+
+
 def test_w8a8_extreme_codes_exact(ops):
     """All-(+-127) operands: the worst-case |acc| = d_in * 127^2 stays exact in int32."""
     M, K, N = 130, 3072, 136

@@ -326,6 +326,26 @@ def test_w8a8_dequant_approximates_float_linear():
     assert rel(y, X.astype(np.float64) @ W.T.astype(np.float64)) < 0.02
 
 
+def test_w8a8_bwd_straight_through_finite_difference():
+    """W8A8 backward = gradient of the layer with the activation quantiser as identity
+    (straight-through): finite differences of X W_deq^T + s (X A^T) B^T + bias."""
+    g = rng(25)
+    M, K, N, r = 4, 8, 6, 2
+    X = g.standard_normal((M, K))
+    Wq = g.integers(-127, 128, (N, K)).astype(np.int8)
+    sw = g.uniform(0.001, 0.01, N).astype(np.float32)
+    A = g.standard_normal((r, K)) / 3
+    B = g.standard_normal((N, r)) * 0.3
+    bias = g.standard_normal(N) * 0.1
+    dY = g.standard_normal((M, N))
+    s = 0.75
+    Wd = np.array([[float(sw[o]) * int(Wq[o, k]) for k in range(K)] for o in range(N)])  # written out
+    L = lambda: float((dY * (X @ Wd.T + s * (X @ A.T) @ B.T + bias)).sum())  # noqa: E731
+    dX, dA, dB, dbias = O.w8a8_lora_bwd(X, Wq, sw, A, B, s, dY)
+    for got, x in ((dX, X), (dA, A), (dB, B), (dbias, bias)):
+        assert rel(got, _fd_grad(L, x)) < 1e-8
+
+
 # ------------------------------------------------------------------ sampled forms
 def test_sampled_forms_match_full():
     X, W0, A, B, bias, m, dY = rand_case(M=40, d_in=24, d_out=18, r=4, seed=23)
