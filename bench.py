@@ -392,8 +392,8 @@ def headline(args, L, ops, dist, world, peaks):
     }
 
 
-def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8")):
-    """DoRA, SwiGLU MLP and W8A8 workloads, each a fwd+bwd (fwd only for W8A8) step."""
+def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8", "qkv")):
+    """DoRA, gated MLP, W8A8 and fused-QKV workloads, each a fwd+bwd step (W8A8 also fwd alone)."""
     import torch
 
     import datagen as D
@@ -407,6 +407,35 @@ def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8")):
         out.update(_mlp_workload(args, L, ops, peaks, D, dev, steps, warm))
     if "w8a8" in which:
         out.update(_w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm))
+    if "qkv" in which:
+        out.update(_qkv_workload(args, L, ops, peaks, D, dev, steps, warm))
+    return out
+
+
+def _qkv_workload(args, L, ops, peaks, D, dev, steps, warm):
+    """Fused query/key/value projection with one adapter per leaf, forward + backward."""
+    import torch
+    case = D.WORKLOADS["qkv_lora_4096_gqa_bf16"]
+    t = D.make_qkv(case)
+    g = {k: v.to(dev) for k, v in t.items() if v is not None}
+    leaves = [(g[f"A{l}"], g[f"B{l}"], case.s[l]) for l in range(len(case.n))]
+
+    def qkv_step():
+        Y, Z = ops.lora_qkv_fwd(g["X"], g["W0"], leaves)
+        ops.lora_qkv_bwd(g["X"], g["W0"], leaves, Z, g["dY"])
+    L.lora_prof_gemm(reset=True)
+    L.lora_prof_enable(True)
+    ms, _, _ = timed(qkv_step, steps, warm)
+    L.lora_prof_enable(False)
+    N = sum(case.n)
+    f = 2 * case.M * case.d_in * N + 2 * case.M * case.r * len(case.n) * case.d_in + 2 * case.M * case.r * N
+    b = 2 * case.M * case.d_in * N + 4 * case.M * case.r * (len(case.n) * case.d_in + N)
+    out = {case.name: {"ms_per_step": ms, "tokens_per_s": case.M / (ms * 1e-3),
+                       "tflops": (f + b) / (ms * 1e-3) / 1e12,
+                       "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                       "roofline": gemm_roofline(L, peaks, ms, steps + warm, False, case.name)}}
+    del g, t
+    torch.cuda.empty_cache()
     return out
 
 
@@ -441,19 +470,20 @@ def _mlp_workload(args, L, ops, peaks, D, dev, steps, warm):
     g = {k: v.to(dev) for k, v in t.items()}
     P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
 
-    def mlp_step():
-        Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
-        ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
-    L.lora_prof_gemm(reset=True)
-    L.lora_prof_enable(True)
-    mlp_steps = max(3, steps // 2)
-    ms, _, _ = timed(mlp_step, mlp_steps, 2)
-    L.lora_prof_enable(False)
     f, b = mlp_flops(case.M, case.H, case.I, case.r)
-    out["mlp_swiglu_4096x14336_bf16"] = {"ms_per_step": ms, "tflops": (f + b) / (ms * 1e-3) / 1e12,
-                                         "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                                         "roofline": gemm_roofline(L, peaks, ms, mlp_steps + 2, True,
-                                                                   "mlp_swiglu_4096x14336_bf16")}
+    # the same shapes and inputs with each gate activation (SwiGLU, GeGLU with exact GELU)
+    for name, act in (("mlp_swiglu_4096x14336_bf16", 0), ("mlp_geglu_4096x14336_bf16", 1)):
+        def mlp_step():
+            Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"], act=act)
+            ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"], act=act)
+        L.lora_prof_gemm(reset=True)
+        L.lora_prof_enable(True)
+        mlp_steps = max(3, steps // 2)
+        ms, _, _ = timed(mlp_step, mlp_steps, 2)
+        L.lora_prof_enable(False)
+        out[name] = {"ms_per_step": ms, "tflops": (f + b) / (ms * 1e-3) / 1e12,
+                     "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                     "roofline": gemm_roofline(L, peaks, ms, mlp_steps + 2, True, name)}
     del g, t, P
     torch.cuda.empty_cache()
     return out
@@ -519,7 +549,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads", default="all", choices=["all", "headline"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default=None, choices=["dora", "mlp", "w8a8"],
+    ap.add_argument("--only", default=None, choices=["dora", "mlp", "w8a8", "qkv"],
                     help="time one non-headline workload alone (for profiling) and print its record")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -25,8 +25,8 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["LinearCase", "MlpCase", "W8A8Case", "WORKLOADS", "make_linear", "make_mlp",
-           "make_w8a8", "scaled"]
+__all__ = ["LinearCase", "MlpCase", "W8A8Case", "QkvCase", "WORKLOADS", "make_linear", "make_mlp",
+           "make_w8a8", "make_qkv", "scaled"]
 
 
 @dataclass(frozen=True)
@@ -84,7 +84,25 @@ class W8A8Case:
         return self.alpha / self.r
 
 
-# The five workloads, named by what they are.  The tiny fp32 one and the
+@dataclass(frozen=True)
+class QkvCase:
+    """Fused query/key/value projection: W0 [sum n, d_in], one rank-r adapter per leaf."""
+    name: str
+    M: int
+    d_in: int
+    n: tuple              # output rows of each leaf
+    r: int
+    alpha: float
+    strengths: tuple = (1.0, 0.75, 1.25)   # per leaf, so that leaf scales are told apart
+    bias: bool = False
+    seed: int = 1005
+
+    @property
+    def s(self) -> tuple:
+        return tuple(st * self.alpha / self.r for st in self.strengths[:len(self.n)])
+
+
+# The workloads, named by what they are.  The tiny fp32 one and the
 # reduced ("small") variants are sized so the fp64 oracle finishes in seconds.
 WORKLOADS = {
     "lora_tiny_f32": LinearCase("lora_tiny_f32", 64, 256, 256, 8, 8.0, "f32", bias=True, seed=1000),
@@ -93,6 +111,8 @@ WORKLOADS = {
                                         dora=True, bias=True, seed=1002),
     "mlp_swiglu_4096x14336_bf16": MlpCase("mlp_swiglu_4096x14336_bf16", 16384, 4096, 14336, 16, 16.0),
     "w8a8_lora_3072": W8A8Case("w8a8_lora_3072", 16384, 3072, 3072, 32, 32.0),
+    # grouped-query attention block of a 4096-wide model: 32 query heads, 8 key/value heads of 128
+    "qkv_lora_4096_gqa_bf16": QkvCase("qkv_lora_4096_gqa_bf16", 16384, 4096, (4096, 1024, 1024), 16, 16.0),
 }
 
 
@@ -153,3 +173,18 @@ def make_w8a8(case: W8A8Case):
     B = _normal(g, (case.d_out, case.r), 0.02).to(torch.bfloat16)
     bias = _normal(g, (case.d_out,), 0.01).to(torch.bfloat16) if case.bias else None
     return {"X": X, "W0": W0, "A": A, "B": B, "bias": bias}
+
+
+def make_qkv(case: QkvCase):
+    """CPU bf16 tensors for the fused-leaf workload: X, W0, A<l>, B<l> per leaf, bias, dY."""
+    g = torch.Generator().manual_seed(case.seed)
+    dt = torch.bfloat16
+    N = sum(case.n)
+    out = {"X": _normal(g, (case.M, case.d_in), 1.0).to(dt),
+           "W0": _normal(g, (N, case.d_in), case.d_in ** -0.5).to(dt)}
+    for l, nl in enumerate(case.n):
+        out[f"A{l}"] = _normal(g, (case.r, case.d_in), case.d_in ** -0.5).to(dt)
+        out[f"B{l}"] = _normal(g, (nl, case.r), 0.02).to(dt)
+    out["bias"] = _normal(g, (N,), 0.01).to(dt) if case.bias else None
+    out["dY"] = _normal(g, (case.M, N), 1.0).to(dt)
+    return out

@@ -16,7 +16,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "lora_gb300.h")
 
 LORA_F32, LORA_BF16 = 0, 1
 LORA_NOALLOC_SCRATCH_BYTES = 4 << 20   # fixed scratch of lora_linear_fwd_noalloc (header macro)
-OP_LINEAR_FWD, OP_LINEAR_BWD, OP_DORA_FWD, OP_DORA_BWD, OP_MLP_FWD, OP_MLP_BWD = range(6)
+OP_LINEAR_FWD, OP_LINEAR_BWD, OP_DORA_FWD, OP_DORA_BWD, OP_MLP_FWD, OP_MLP_BWD, OP_QKV_FWD, OP_QKV_BWD = range(8)
 STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_UNSUPPORTED", 3: "LORA_ERR_MISALIGNED",
           4: "LORA_ERR_WORKSPACE", 5: "LORA_ERR_CUDA", 6: "LORA_ERR_DEVICE_TIMEOUT"}
 
@@ -32,11 +32,24 @@ class LoraShape(ctypes.Structure):
 
 
 class LoraMlpShape(ctypes.Structure):
-    _fields_ = [("M", c_int64), ("H", c_int64), ("I", c_int64), ("r", c_int64), ("dtype", c_int32)]
+    _fields_ = [("M", c_int64), ("H", c_int64), ("I", c_int64), ("r", c_int64), ("dtype", c_int32),
+                ("act", c_int32)]
+
+
+LORA_ACT_SWIGLU, LORA_ACT_GEGLU = 0, 1
 
 
 class LoraProj(ctypes.Structure):
     _fields_ = [("W", c_void_p), ("A", c_void_p), ("B", c_void_p), ("s", c_float)]
+
+
+class LoraQkvShape(ctypes.Structure):
+    _fields_ = [("M", c_int64), ("d_in", c_int64), ("n", c_int64 * 3), ("L", c_int32), ("r", c_int32),
+                ("dtype", c_int32)]
+
+
+class LoraAdapter(ctypes.Structure):
+    _fields_ = [("A", c_void_p), ("B", c_void_p), ("s", c_float)]
 
 
 P = c_void_p
@@ -67,6 +80,10 @@ _SIGS = {
     "w8a8_bwd_workspace_bytes": (c_size_t, [c_int64, c_int64, c_int64, c_int64]),
     "w8a8_lora_bwd": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, P, c_float, P, P, P, P, P,
                               c_size_t, P]),
+    "lora_qkv_workspace_bytes": (c_size_t, [c_int, POINTER(LoraQkvShape)]),
+    "lora_qkv_fwd": (c_int, [POINTER(LoraQkvShape), P, P, POINTER(LoraAdapter), P, P, P, P, c_size_t, P]),
+    "lora_qkv_bwd": (c_int, [POINTER(LoraQkvShape), P, P, POINTER(LoraAdapter), P, P, P, POINTER(c_void_p),
+                             POINTER(c_void_p), P, P, c_size_t, P]),
     "lora_launch_count": (ctypes.c_uint64, []),
     "lora_prof_enable": (c_int, [c_int]),
     "lora_prof_gemm": (c_int, [POINTER(ctypes.c_double), POINTER(c_int64), POINTER(ctypes.c_double), c_int]),
@@ -122,12 +139,29 @@ def shape(M, d_in, d_out, r, dtype) -> LoraShape:
     return LoraShape(M, d_in, d_out, r, dtype)
 
 
-def mlp_shape(M, H, I, r, dtype=LORA_BF16) -> LoraMlpShape:
-    return LoraMlpShape(M, H, I, r, dtype)
+def mlp_shape(M, H, I, r, dtype=LORA_BF16, act=0) -> LoraMlpShape:
+    return LoraMlpShape(M, H, I, r, dtype, act)
 
 
 def proj(W, A, B, s) -> LoraProj:
     return LoraProj(W.data_ptr(), A.data_ptr(), B.data_ptr(), float(s))
+
+
+def qkv_shape(M, d_in, n, r, dtype=LORA_BF16) -> LoraQkvShape:
+    n = list(n)
+    return LoraQkvShape(M, d_in, (c_int64 * 3)(*(n + [0] * (3 - len(n)))), len(n), r, dtype)
+
+
+def adapters(leaves):
+    """leaves: sequence of (A, B, s) -> a ctypes array of lora_adapter."""
+    arr = (LoraAdapter * max(len(leaves), 1))()
+    for i, (A, B, s) in enumerate(leaves):
+        arr[i] = LoraAdapter(ptr(A), ptr(B), float(s))
+    return arr
+
+
+def _ptrs(ts):
+    return (c_void_p * max(len(ts), 1))(*[ptr(t) for t in ts])
 
 
 # ------------------------------------------------------------------ entry points
@@ -229,6 +263,25 @@ def lora_mlp_swiglu_bwd(sh, X, gate, up, down, e_saved, u_saved, h_saved, Zgu_sa
                                    ptr(Zd_saved), ptr(dY), ptr(dX), ptr(dAg), ptr(dBg), ptr(dAu), ptr(dBu), ptr(dAd),
                                    ptr(dBd), ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                    _stream(stream)), "lora_mlp_swiglu_bwd")
+
+
+def lora_qkv_workspace_bytes(op: int, sh: LoraQkvShape) -> int:
+    return _lib().lora_qkv_workspace_bytes(op, ctypes.byref(sh))
+
+
+def lora_qkv_fwd(sh, X, W0, leaves, bias, Y, Z_save, ws, stream=None):
+    """leaves: a ctypes array from adapters()."""
+    _ck(_lib().lora_qkv_fwd(ctypes.byref(sh), ptr(X), ptr(W0), leaves, ptr(bias), ptr(Y), ptr(Z_save), ptr(ws),
+                            0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)), "lora_qkv_fwd")
+
+
+def lora_qkv_bwd(sh, X, W0, leaves, Z_saved, dY, dX, dA, dB, dbias, ws, stream=None):
+    """dA, dB: sequences of L tensors (or ctypes pointer arrays)."""
+    dA = dA if isinstance(dA, ctypes.Array) else _ptrs(dA)
+    dB = dB if isinstance(dB, ctypes.Array) else _ptrs(dB)
+    _ck(_lib().lora_qkv_bwd(ctypes.byref(sh), ptr(X), ptr(W0), leaves, ptr(Z_saved), ptr(dY), ptr(dX), dA, dB,
+                            ptr(dbias), ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                            _stream(stream)), "lora_qkv_bwd")
 
 
 def w8a8_quantize_rows(rows, cols, X, Xq, sx, A=None, r=0, Z=None, stream=None):

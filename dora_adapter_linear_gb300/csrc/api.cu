@@ -211,6 +211,57 @@ size_t plan_mlp_bwd(const lora_mlp_shape& sh, char* base, MlpBwdWs* w) {
   return c.off;
 }
 
+// fused-leaf (QKV) plans: packed operands A_stack [L r, in], B_blk [N, L r]
+int64_t qkv_N(const lora_qkv_shape& sh) {
+  int64_t n = 0;
+  for (int l = 0; l < sh.L; ++l) n += sh.n[l];
+  return n;
+}
+struct QkvFwdWs {
+  uint32_t* err;
+  bf16* A_stack;
+  bf16* B_blk;
+  bf16* Z;       // when no Z_save
+};
+size_t plan_qkv_fwd(const lora_qkv_shape& sh, char* base, QkvFwdWs* w) {
+  Carve c{base};
+  const int64_t R = (int64_t)sh.L * sh.r;
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  w->A_stack = c.take<bf16>(R * sh.d_in);
+  w->B_blk = c.take<bf16>(qkv_N(sh) * R);
+  w->Z = c.take<bf16>(sh.M * R);
+  return c.off;
+}
+struct QkvBwdWs {
+  uint32_t* err;
+  bf16* A_stack;
+  bf16* B_blk;
+  bf16* Gs;      // [M, L r] = [s_l dY_l B_l]
+  bf16* Zrec;    // [M, L r] when no Z_saved
+  float* PA;     // [splitsA, in, L r]
+  float* PB[kMaxLeaves];    // [splitsB[l], n_l, r]
+  float* csum[kMaxLeaves];  // [splitsB[l], n_l]
+  int splitsA, splitsB[kMaxLeaves];
+};
+size_t plan_qkv_bwd(const lora_qkv_shape& sh, char* base, QkvBwdWs* w) {
+  Carve c{base};
+  const int64_t R = (int64_t)sh.L * sh.r;
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  w->A_stack = c.take<bf16>(R * sh.d_in);
+  w->B_blk = c.take<bf16>(qkv_N(sh) * R);
+  w->Gs = c.take<bf16>(sh.M * R);
+  w->Zrec = c.take<bf16>(sh.M * R);
+  w->splitsA = colreduce_splits(sh.M, sh.d_in);
+  w->PA = c.take<float>((size_t)w->splitsA * sh.d_in * R);
+  for (int l = 0; l < kMaxLeaves; ++l) {
+    const bool live = l < sh.L;
+    w->splitsB[l] = live ? colreduce_splits(sh.M, sh.n[l]) : 0;
+    w->PB[l] = live ? c.take<float>((size_t)w->splitsB[l] * sh.n[l] * sh.r) : nullptr;
+    w->csum[l] = live ? c.take<float>((size_t)w->splitsB[l] * sh.n[l]) : nullptr;
+  }
+  return c.off;
+}
+
 // ------------------------------------------------------------------ bf16 helpers
 TcGemmDesc fwd_desc(int64_t M, int64_t N, int64_t K, const void* X, const void* W, const void* Zs, const void* B,
                     int r, void* Y, const bf16* bias, const float* cs, uint32_t* err) {
@@ -334,7 +385,7 @@ const char* lora_status_string(int status) {
   return "unknown status";
 }
 
-int lora_abi_version(void) { return 2; }
+int lora_abi_version(void) { return 4; }
 
 size_t lora_workspace_bytes(int op, const lora_shape* sh) {
   if (check_shape(sh) != LORA_OK) return 0;
@@ -351,6 +402,7 @@ static lora_status check_mlp_shape(const lora_mlp_shape* sh) {
   if (!sh) return LORA_ERR_INVALID_ARG;
   if (sh->M < 0 || sh->H <= 0 || sh->I <= 0 || sh->r <= 0) return LORA_ERR_INVALID_ARG;
   if (sh->dtype != LORA_BF16) return sh->dtype == LORA_F32 ? LORA_ERR_UNSUPPORTED : LORA_ERR_INVALID_ARG;
+  if (sh->act != LORA_ACT_SWIGLU && sh->act != LORA_ACT_GEGLU) return LORA_ERR_INVALID_ARG;
   if (sh->H % 8 || sh->I % 8 || sh->r % 8 || sh->r > 32) return LORA_ERR_UNSUPPORTED;
   if (sh->M > (1LL << 31) - 1 || 2 * mlp_ipad(*sh) > (1LL << 31) - 1) return LORA_ERR_UNSUPPORTED;
   return LORA_OK;
@@ -360,6 +412,27 @@ size_t lora_mlp_workspace_bytes(int op, const lora_mlp_shape* sh) {
   if (check_mlp_shape(sh) != LORA_OK) return 0;
   if (op == LORA_OP_MLP_FWD) { MlpFwdWs w; return plan_mlp_fwd(*sh, nullptr, &w); }
   if (op == LORA_OP_MLP_BWD) { MlpBwdWs w; return plan_mlp_bwd(*sh, nullptr, &w); }
+  return 0;
+}
+
+static lora_status check_qkv_shape(const lora_qkv_shape* sh) {
+  if (!sh) return LORA_ERR_INVALID_ARG;
+  if (sh->M < 0 || sh->d_in <= 0 || sh->r <= 0 || sh->L < 1 || sh->L > kMaxLeaves) return LORA_ERR_INVALID_ARG;
+  if (sh->dtype != LORA_BF16) return sh->dtype == LORA_F32 ? LORA_ERR_UNSUPPORTED : LORA_ERR_INVALID_ARG;
+  for (int l = 0; l < sh->L; ++l) {
+    if (sh->n[l] <= 0) return LORA_ERR_INVALID_ARG;
+    if (sh->n[l] % 8) return LORA_ERR_UNSUPPORTED;
+  }
+  if (sh->d_in % 8 || sh->r % 8 || sh->L * sh->r > 64) return LORA_ERR_UNSUPPORTED;
+  if (sh->M > (1LL << 31) - 1 || sh->d_in > (1LL << 31) - 1 || qkv_N(*sh) > (1LL << 31) - 1)
+    return LORA_ERR_UNSUPPORTED;
+  return LORA_OK;
+}
+
+size_t lora_qkv_workspace_bytes(int op, const lora_qkv_shape* sh) {
+  if (check_qkv_shape(sh) != LORA_OK) return 0;
+  if (op == LORA_OP_QKV_FWD) { QkvFwdWs w; return plan_qkv_fwd(*sh, nullptr, &w); }
+  if (op == LORA_OP_QKV_BWD) { QkvBwdWs w; return plan_qkv_bwd(*sh, nullptr, &w); }
   return 0;
 }
 
@@ -514,6 +587,149 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     if (dX) CK(sgemm_f32(sg(M, in, r, w.Gs, r, false, A, in, false, dX, in, s, 1.f), st));  // dX += s G A
     CK(sgemm_f32(sg(r, in, M, w.Gs, r, true, X, in, false, dA, in, s), st));            // dA = s G^T X
     CK(sgemm_f32(sg(out, r, M, dY, out, true, Z, r, false, dB, r, s), st));             // dB = s dY^T Z
+  }
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------------ fused-leaf (QKV) LoRA linear
+static lora_status check_leaves(const lora_qkv_shape& sh, const lora_adapter* lv, bool* any_live) {
+  REQ(lv);
+  *any_live = false;
+  for (int l = 0; l < sh.L; ++l) {
+    REQ(lv[l].A); REQ(lv[l].B);
+    ALN(lv[l].A); ALN(lv[l].B);
+    if (!isfinite(lv[l].s)) return LORA_ERR_INVALID_ARG;
+    if (lv[l].s != 0.f) *any_live = true;
+  }
+  return LORA_OK;
+}
+
+static LeafPack leaf_pack(const lora_qkv_shape& sh, const lora_adapter* lv, bf16* A_stack, bf16* B_blk) {
+  LeafPack p;
+  p.L = sh.L;
+  p.r = (int)sh.r;
+  p.in = sh.d_in;
+  p.N = qkv_N(sh);
+  int64_t row = 0;
+  for (int l = 0; l < sh.L; ++l) {
+    p.row0[l] = row;
+    row += sh.n[l];
+    p.A[l] = static_cast<const bf16*>(lv[l].A);
+    p.B[l] = static_cast<const bf16*>(lv[l].B);
+    p.s[l] = lv[l].s;
+  }
+  p.A_stack = A_stack;
+  p.B_blk = B_blk;
+  return p;
+}
+
+lora_status lora_qkv_fwd(const lora_qkv_shape* sh, const void* X, const void* W0, const lora_adapter* leaves,
+                         const void* bias, void* Y, void* Z_save, void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_qkv_shape(sh);
+  if (e != LORA_OK) return e;
+  REQM(sh->M, X); REQ(W0); REQM(sh->M, Y);
+  ALN(X); ALN(W0); ALN(bias); ALN(Y); ALN(Z_save);
+  bool live = false;
+  if ((e = check_leaves(*sh, leaves, &live)) != LORA_OK) return e;
+  QkvFwdWs w;
+  if ((e = check_ws(ws, ws_bytes, plan_qkv_fwd(*sh, nullptr, &w))) != LORA_OK) return e;
+  plan_qkv_fwd(*sh, static_cast<char*>(ws), &w);
+  if (sh->M == 0) return LORA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, N = qkv_N(*sh);
+  const int R = (int)(sh->L * sh->r);
+  CK(pack_leaves(leaf_pack(*sh, leaves, w.A_stack, w.B_blk), st));
+  bf16* Z = Z_save ? static_cast<bf16*>(Z_save) : w.Z;
+  if (live || Z_save) {  // one pass over X for every leaf's down-projection
+    RowProjDesc d = rp_desc(M, in, R, X, w.A_stack, false);
+    d.out_a = Z;
+    CK(rowproj(d, st));
+  }
+  // the base product of all leaves and the block-diagonal rank-(L r) tail in one GEMM
+  CK(tc_gemm(fwd_desc(M, N, in, X, W0, live ? Z : nullptr, w.B_blk, R, Y, static_cast<const bf16*>(bias), nullptr,
+                      w.err),
+             st));
+  return LORA_OK;
+}
+
+lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0, const lora_adapter* leaves,
+                         const void* Z_saved, const void* dY, void* dX, void* const* dA, void* const* dB,
+                         void* dbias, void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_qkv_shape(sh);
+  if (e != LORA_OK) return e;
+  REQM(sh->M, X); REQ(W0); REQM(sh->M, dY); REQ(dA); REQ(dB);
+  ALN(X); ALN(W0); ALN(Z_saved); ALN(dY); ALN(dX); ALN(dbias);
+  for (int l = 0; l < sh->L; ++l) {
+    REQ(dA[l]); REQ(dB[l]);
+    ALN(dA[l]); ALN(dB[l]);
+  }
+  bool live = false;
+  if ((e = check_leaves(*sh, leaves, &live)) != LORA_OK) return e;
+  QkvBwdWs w;
+  if ((e = check_ws(ws, ws_bytes, plan_qkv_bwd(*sh, nullptr, &w))) != LORA_OK) return e;
+  plan_qkv_bwd(*sh, static_cast<char*>(ws), &w);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, N = qkv_N(*sh);
+  const int r = (int)sh->r, R = (int)(sh->L * sh->r);
+  if (M == 0 || !live) {
+    // no tokens, or every strength 0: adapter gradients vanish; dX is the frozen base's
+    for (int l = 0; l < sh->L; ++l) {
+      CK(cudaMemsetAsync(dA[l], 0, (size_t)r * in * 2, st));
+      CK(cudaMemsetAsync(dB[l], 0, (size_t)sh->n[l] * r * 2, st));
+    }
+    if (M == 0) {
+      if (dbias) CK(cudaMemsetAsync(dbias, 0, (size_t)N * 2, st));
+      return LORA_OK;
+    }
+  }
+  int64_t row0[kMaxLeaves] = {0, 0, 0};
+  for (int l = 1; l < sh->L; ++l) row0[l] = row0[l - 1] + sh->n[l - 1];
+  const bf16* dYb = static_cast<const bf16*>(dY);
+  if (!live) {
+    if (dX) CK(tc_gemm(dx_desc(M, in, N, dY, W0, nullptr, nullptr, R, dX, nullptr, w.err), st));
+    if (dbias) {
+      for (int l = 0; l < sh->L; ++l) {
+        ColReduceDesc d = cr_desc(M, sh->n[l], 8, dYb + row0[l], dY, N, w.PB[l], w.splitsB[l]);
+        d.lds = N;
+        d.colsum = w.csum[l];
+        CK(colreduce(d, st));
+        CK(sum_splits<bf16>(w.csum[l], w.splitsB[l], sh->n[l], nullptr, static_cast<bf16*>(dbias) + row0[l], st));
+      }
+    }
+    return LORA_OK;
+  }
+  CK(pack_leaves(leaf_pack(*sh, leaves, w.A_stack, w.B_blk), st));
+  const bf16* Z = static_cast<const bf16*>(Z_saved);
+  if (!Z) {
+    RowProjDesc d = rp_desc(M, in, R, X, w.A_stack, false);
+    d.out_a = w.Zrec;
+    CK(rowproj(d, st));
+    Z = w.Zrec;
+  }
+  // dB partials of each leaf (its columns of dY against its block of Z) and dY column sums
+  for (int l = 0; l < sh->L; ++l) {
+    ColReduceDesc d = cr_desc(M, sh->n[l], r, dYb + row0[l], Z + l * r, R, w.PB[l], w.splitsB[l]);
+    d.lds = N;
+    d.colsum = dbias ? w.csum[l] : nullptr;
+    CK(colreduce(d, st));
+  }
+  {  // [s_l dY_l B_l] for all leaves in one pass over dY (B_blk is block-diagonal)
+    RowProjDesc d = rp_desc(M, N, R, dY, w.B_blk, true);
+    d.out_a = w.Gs;
+    CK(rowproj(d, st));
+  }
+  if (dX) CK(tc_gemm(dx_desc(M, in, N, dY, W0, w.Gs, w.A_stack, R, dX, nullptr, w.err), st));
+  CK(colreduce(cr_desc(M, in, R, X, w.Gs, R, w.PA, w.splitsA), st));
+  for (int l = 0; l < sh->L; ++l) {
+    Partial pa{w.PA, w.splitsA, R, l * r}, none{};
+    CK(finalize_dA<bf16>(r, in, pa, 1.f, none, 0.f, nullptr, 0.f, static_cast<const bf16*>(leaves[l].A),
+                         static_cast<bf16*>(dA[l]), st));
+    Partial pb{w.PB[l], w.splitsB[l], r, 0};
+    CK(finalize_dB<bf16>(sh->n[l], r, pb, leaves[l].s, nullptr, nullptr, nullptr,
+                         static_cast<const bf16*>(leaves[l].B), nullptr, leaves[l].s, false, static_cast<bf16*>(dB[l]),
+                         st));
+    if (dbias)
+      CK(sum_splits<bf16>(w.csum[l], w.splitsB[l], sh->n[l], nullptr, static_cast<bf16*>(dbias) + row0[l], st));
   }
   return LORA_OK;
 }
@@ -755,6 +971,7 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
   {  // e, u, h = gate/up GEMM with both adapters, SwiGLU epilogue
     TcGemmDesc d;
     d.mode = TC_SWIGLU_FWD;
+    d.act = sh->act;
     d.M = (int)M;
     d.N = (int)I;
     d.K0 = (int)H;
@@ -835,6 +1052,7 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
   {  // dh = dY Wd + (sd Gd) Ad, SwiGLU backward in the epilogue -> de, du
     TcGemmDesc d;
     d.mode = TC_SWIGLU_BWD;
+    d.act = sh->act;
     d.M = (int)M;
     d.N = (int)I;
     d.K0 = (int)H;

@@ -68,6 +68,7 @@ struct TcGemmDesc {
   uint32_t* err = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int max_ctas = 0;
+  int act = 0;                 // gated MLP activation: 0 SwiGLU, 1 GeGLU
 };
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st);
 
@@ -161,6 +162,20 @@ cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float*
 cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int64_t rows2, int64_t cols, bf16* dst,
                              cudaStream_t st);
 cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st);
+// Operands of the fused-leaf (QKV) layer: A_stack = [A_0; ..; A_{L-1}] and B_blk = blockdiag(s_l B_l)
+// (row0[l] = first row of leaf l in the fused output, row0[0] = 0; in multiple of 8).
+constexpr int kMaxLeaves = 3;
+struct LeafPack {
+  int L = 0, r = 0;
+  int64_t in = 0, N = 0;
+  int64_t row0[kMaxLeaves] = {0, 0, 0};
+  const bf16* A[kMaxLeaves] = {nullptr, nullptr, nullptr};
+  const bf16* B[kMaxLeaves] = {nullptr, nullptr, nullptr};
+  float s[kMaxLeaves] = {0.f, 0.f, 0.f};
+  bf16* A_stack = nullptr;
+  bf16* B_blk = nullptr;
+};
+cudaError_t pack_leaves(const LeafPack& p, cudaStream_t st);
 
 // ------------------------------------------------------------------ fp32 SIMT path
 // C[M,N] = alpha * op(A) op(B) (op(A) [M,K], op(B) [K,N]) + beta * C, with optional per-K scale of

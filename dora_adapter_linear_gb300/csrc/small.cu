@@ -290,6 +290,42 @@ cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int6
   count_launch();
   return cudaGetLastError();
 }
+// Fused-leaf operands: A_stack = [A_0; A_1; ...] ([L r, in]) and the block-diagonal
+// B_blk [N, L r] whose rows of leaf l hold s_l B_l in columns l r .. l r + r - 1, zeros elsewhere.
+__global__ void pack_leaves_kernel(LeafPack p) {
+  const int R = p.L * p.r;
+  const int64_t nA = (int64_t)R * p.in / 8;   // 16-byte chunks of A_stack
+  const int64_t nB = p.N * R;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nA + nB; i += stride) {
+    if (i < nA) {
+      const int64_t e = i * 8;
+      const int row = (int)(e / p.in);
+      const int leaf = row / p.r;
+      const int64_t off = (int64_t)(row - leaf * p.r) * p.in + (e - (int64_t)row * p.in);
+      *reinterpret_cast<uint4*>(p.A_stack + e) = *reinterpret_cast<const uint4*>(p.A[leaf] + off);
+    } else {
+      const int64_t e = i - nA;
+      const int64_t o = e / R;
+      const int j = (int)(e - o * R);
+      int leaf = 0;
+      while (leaf + 1 < p.L && o >= p.row0[leaf + 1]) ++leaf;
+      const int jl = j - leaf * p.r;
+      float v = 0.f;
+      if (jl >= 0 && jl < p.r) v = p.s[leaf] * __bfloat162float(p.B[leaf][(o - p.row0[leaf]) * p.r + jl]);
+      p.B_blk[e] = __float2bfloat16_rn(v);
+    }
+  }
+}
+cudaError_t pack_leaves(const LeafPack& p, cudaStream_t st) {
+  const int64_t n = (int64_t)p.L * p.r * p.in / 8 + p.N * p.L * p.r;
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = (n + 255) / 256;
+  pack_leaves_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st) {
   if (bytes == 0) return cudaSuccess;
   return cudaMemsetAsync(p, 0, bytes, st);

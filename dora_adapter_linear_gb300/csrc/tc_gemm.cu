@@ -52,6 +52,7 @@ struct TcParams {
   int32_t* acc_out;     // W8A8: raw int32 product [M, N] (or null)
   int write_y;          // W8A8: 0 when only the raw product is wanted
   int pair_leader_arms; // CTA pair: the leader posts the transaction bytes of both CTAs
+  int act;              // gated MLP activation: 0 SwiGLU, 1 GeGLU
   uint32_t* err;
   uint64_t timeout_ns;
 };
@@ -108,6 +109,26 @@ __device__ __forceinline__ void stage_row(uint8_t* stg, int row, const uint32_t*
     const int jj = jbase + j;
     uint4 v = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
     *reinterpret_cast<uint4*>(stg + row * 128 + ((jj ^ (row & 7)) << 4)) = v;
+  }
+}
+
+// ---------------------------------------------------------------------------- gated activations
+// act 0: silu(e) = e sigmoid(e); act 1: gelu(e) = e Phi(e) with the normal CDF
+// Phi(e) = (1 + erf(e / sqrt 2)) / 2 (CUDA's expf / erff are called, not re-implemented).
+__device__ __forceinline__ float gate_act(float e, int act) {
+  if (act == 0) return e / (1.0f + __expf(-e));
+  return 0.5f * e * (1.0f + erff(e * 0.70710678118654752f));
+}
+// a = act(e) and its derivative da
+__device__ __forceinline__ void gate_act_grad(float e, int act, float& a, float& da) {
+  if (act == 0) {
+    const float sg = 1.0f / (1.0f + __expf(-e));
+    a = e * sg;
+    da = sg * (1.0f + e * (1.0f - sg));
+  } else {
+    const float cdf = 0.5f * (1.0f + erff(e * 0.70710678118654752f));
+    a = e * cdf;
+    da = cdf + e * 0.39894228040143268f * __expf(-0.5f * e * e);  // + e * N(0,1) density
   }
 }
 
@@ -172,8 +193,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
         for (int j = 0; j < 32; j += 2) {
           const float e0 = u2f(ve[j]), e1 = u2f(ve[j + 1]);
           const float u0 = u2f(vu[j]), u1 = u2f(vu[j + 1]);
-          const float h0 = e0 / (1.0f + __expf(-e0)) * u0;
-          const float h1 = e1 / (1.0f + __expf(-e1)) * u1;
+          const float h0 = gate_act(e0, p.act) * u0;
+          const float h1 = gate_act(e1, p.act) * u1;
           we[j / 2] = pack_bf16x2(e0, e1);
           wu[j / 2] = pack_bf16x2(u0, u1);
           wh[j / 2] = pack_bf16x2(h0, h1);
@@ -226,12 +247,13 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
           const float2 e = unpack_bf16x2(ev[j]);
           const float2 u = unpack_bf16x2(uv[j]);
           const float d0 = u2f(vd[2 * j]), d1 = u2f(vd[2 * j + 1]);
-          const float s0 = 1.0f / (1.0f + __expf(-e.x));
-          const float s1 = 1.0f / (1.0f + __expf(-e.y));
-          const float de0 = d0 * u.x * s0 * (1.0f + e.x * (1.0f - s0));
-          const float de1 = d1 * u.y * s1 * (1.0f + e.y * (1.0f - s1));
-          const float du0 = d0 * e.x * s0;
-          const float du1 = d1 * e.y * s1;
+          float a0, da0, a1, da1;
+          gate_act_grad(e.x, p.act, a0, da0);
+          gate_act_grad(e.y, p.act, a1, da1);
+          const float de0 = d0 * u.x * da0;
+          const float de1 = d1 * u.y * da1;
+          const float du0 = d0 * a0;
+          const float du1 = d1 * a1;
           wde[j] = pack_bf16x2(de0, de1);
           wdu[j] = pack_bf16x2(du0, du1);
         }
@@ -319,20 +341,27 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
 // Thread tid (0..127) always owns physical 16-byte chunk pc = tid & 7 of rows (tid >> 3) + 16 i;
 // all those rows have the same (row & 7), so the logical K-chunk j and its 8 scales are the same
 // for the thread's 8 chunks: two vector loads per k-step.
-__device__ __forceinline__ void kscale_tile(const TcParams& p, uint8_t* a, int ks, int tid) {
-  const int pc = tid & 7;
-  const int j = pc ^ ((tid >> 3) & 7);
+struct KScales {
+  float4 lo, hi;
+};
+// The 8 scales thread tid needs at K-step ks (they do not depend on the tile, so they can be
+// fetched ahead of the tile data).
+__device__ __forceinline__ KScales kscale_fetch(const TcParams& p, int ks, int tid) {
+  const int j = (tid & 7) ^ ((tid >> 3) & 7);
   const int kb = ks * BK + 8 * j;
-  float sc[8];
+  KScales s;
   if (kb < p.K0) {  // K0 is a multiple of 8: a group of 8 is wholly inside or outside
-    const float4 s0 = __ldg(reinterpret_cast<const float4*>(p.a_kscale + kb));
-    const float4 s1 = __ldg(reinterpret_cast<const float4*>(p.a_kscale + kb + 4));
-    sc[0] = s0.x; sc[1] = s0.y; sc[2] = s0.z; sc[3] = s0.w;
-    sc[4] = s1.x; sc[5] = s1.y; sc[6] = s1.z; sc[7] = s1.w;
+    s.lo = __ldg(reinterpret_cast<const float4*>(p.a_kscale + kb));
+    s.hi = __ldg(reinterpret_cast<const float4*>(p.a_kscale + kb + 4));
   } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sc[e] = 0.0f;
+    s.lo = s.hi = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  return s;
+}
+
+__device__ __forceinline__ void kscale_tile(uint8_t* a, const KScales& ks8, int tid) {
+  const int pc = tid & 7;
+  const float sc[8] = {ks8.lo.x, ks8.lo.y, ks8.lo.z, ks8.lo.w, ks8.hi.x, ks8.hi.y, ks8.hi.z, ks8.hi.w};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = (tid >> 3) + 16 * i;
@@ -560,6 +589,9 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    // the scales of the next three scaled K-steps are in flight while a tile is being scaled
+    KScales s_cur = kscale_fetch(p, 0, tid), s_nx1 = kscale_fetch(p, 1 % nk0, tid),
+            s_nx2 = kscale_fetch(p, 2 % nk0, tid);
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       for (int ks = 0; ks < nk; ++ks) {
         const bool tail = HAS_TAIL && ks >= nk0;
@@ -567,7 +599,12 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
           ok = false;
           break;
         }
-        if (!tail) kscale_tile(p, sA + stage * A_STAGE_BYTES, ks, tid);  // the rank-r tail is not scaled
+        if (!tail) {  // the rank-r tail is not scaled
+          kscale_tile(sA + stage * A_STAGE_BYTES, s_cur, tid);
+          s_cur = s_nx1;
+          s_nx1 = s_nx2;
+          s_nx2 = kscale_fetch(p, (ks + 3) % nk0, tid);
+        }
         mbar_arrive(&ready[stage]);
         if (++stage == STAGES) {
           stage = 0;
@@ -797,6 +834,8 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    KScales s_cur = kscale_fetch(p, 0, tid), s_nx1 = kscale_fetch(p, 1 % nk0, tid),
+            s_nx2 = kscale_fetch(p, 2 % nk0, tid);
     for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
       for (int ks = 0; ks < nk; ++ks) {
         const bool tail = HAS_TAIL && ks >= nk0;
@@ -804,7 +843,12 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
           ok = false;
           break;
         }
-        if (!tail) kscale_tile(p, sA + stage * A_STAGE_BYTES, ks, tid);
+        if (!tail) {
+          kscale_tile(sA + stage * A_STAGE_BYTES, s_cur, tid);
+          s_cur = s_nx1;
+          s_nx1 = s_nx2;
+          s_nx2 = kscale_fetch(p, (ks + 3) % nk0, tid);
+        }
         named_bar_sync(1, 128);
         if (tid == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ready[stage]), 0));
         if (++stage == STAGES) {
@@ -1000,6 +1044,7 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.acc_out = d.acc_out;
   p.write_y = d.out[0] != nullptr ? 1 : 0;
   p.pair_leader_arms = env_int("LORA_GB300_PAIR_ARM", 1);
+  p.act = d.act;
 
   p.M = d.M;
   p.N = d.N;

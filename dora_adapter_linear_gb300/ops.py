@@ -74,11 +74,12 @@ def dora_linear_bwd(X, W0, A, B, m, bias, Y, Z, n, V, dY, s, eps=1e-12, need_dx=
     return dX, dA, dB, dm, dbias
 
 
-def lora_mlp_swiglu_fwd(X, g, u, d):
-    """g, u, d: dicts with W, A, B, s.  Returns (Y, saved) where saved holds e, u, h, Zgu, Zd."""
+def lora_mlp_swiglu_fwd(X, g, u, d, act=0):
+    """g, u, d: dicts with W, A, B, s; act 0 SwiGLU, 1 GeGLU.  Returns (Y, saved) where saved
+    holds e, u, h, Zgu, Zd."""
     M, H = X.shape
     I, r = g["W"].shape[0], g["A"].shape[0]
-    sh = L.mlp_shape(M, H, I, r)
+    sh = L.mlp_shape(M, H, I, r, act=act)
     dev = X.device
     e_ = torch.empty(M, I, dtype=X.dtype, device=dev)
     u_ = torch.empty_like(e_)
@@ -92,10 +93,10 @@ def lora_mlp_swiglu_fwd(X, g, u, d):
     return Y, {"e": e_, "u": u_, "h": h_, "Zgu": Zgu, "Zd": Zd}
 
 
-def lora_mlp_swiglu_bwd(X, g, u, d, saved, dY, need_dx=True):
+def lora_mlp_swiglu_bwd(X, g, u, d, saved, dY, need_dx=True, act=0):
     M, H = X.shape
     I, r = g["W"].shape[0], g["A"].shape[0]
-    sh = L.mlp_shape(M, H, I, r)
+    sh = L.mlp_shape(M, H, I, r, act=act)
     dX = torch.empty_like(X) if need_dx else None
     grads = {k: torch.empty_like(v) for k, v in
              (("dAg", g["A"]), ("dBg", g["B"]), ("dAu", u["A"]), ("dBu", u["B"]), ("dAd", d["A"]), ("dBd", d["B"]))}
@@ -137,3 +138,30 @@ def w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, s, bias=None, want_acc=False, want_y=Tru
     ws = workspace(L.w8a8_workspace_bytes(M, d_in, d_out), Xq.device)
     L.w8a8_lora_fwd(M, d_in, d_out, r, Xq, sx, Wq, sw, Z, B, s, bias, Y, acc, ws)
     return Y, acc
+
+
+def lora_qkv_fwd(X, W0, leaves, bias=None, save_z=True):
+    """leaves: [(A_l, B_l, s_l)] for the leaves of the fused weight W0 (rows in leaf order)."""
+    M, d_in = X.shape
+    n = [B.shape[0] for _, B, _ in leaves]
+    r = leaves[0][0].shape[0]
+    sh = L.qkv_shape(M, d_in, n, r)
+    Y = torch.empty(M, sum(n), dtype=X.dtype, device=X.device)
+    Z = torch.empty(M, len(leaves) * r, dtype=X.dtype, device=X.device) if save_z else None
+    ws = workspace(L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, sh), X.device)
+    L.lora_qkv_fwd(sh, X, W0, L.adapters(leaves), bias, Y, Z, ws)
+    return Y, Z
+
+
+def lora_qkv_bwd(X, W0, leaves, Z, dY, need_dx=True, need_dbias=False):
+    M, d_in = X.shape
+    n = [B.shape[0] for _, B, _ in leaves]
+    r = leaves[0][0].shape[0]
+    sh = L.qkv_shape(M, d_in, n, r)
+    dX = torch.empty_like(X) if need_dx else None
+    dA = [torch.empty_like(A) for A, _, _ in leaves]
+    dB = [torch.empty_like(B) for _, B, _ in leaves]
+    dbias = torch.empty(sum(n), dtype=X.dtype, device=X.device) if need_dbias else None
+    ws = workspace(L.lora_qkv_workspace_bytes(L.OP_QKV_BWD, sh), X.device)
+    L.lora_qkv_bwd(sh, X, W0, L.adapters(leaves), Z, dY, dX, dA, dB, dbias, ws)
+    return dX, dA, dB, dbias

@@ -60,7 +60,8 @@ typedef enum { LORA_F32 = 0, LORA_BF16 = 1 } lora_dtype;
 typedef enum {
     LORA_OP_LINEAR_FWD = 0, LORA_OP_LINEAR_BWD = 1,
     LORA_OP_DORA_FWD = 2, LORA_OP_DORA_BWD = 3,
-    LORA_OP_MLP_FWD = 4, LORA_OP_MLP_BWD = 5
+    LORA_OP_MLP_FWD = 4, LORA_OP_MLP_BWD = 5,
+    LORA_OP_QKV_FWD = 6, LORA_OP_QKV_BWD = 7
 } lora_op;
 
 typedef struct {
@@ -68,10 +69,17 @@ typedef struct {
     int32_t dtype;                /* lora_dtype */
 } lora_shape;
 
-/* SwiGLU MLP: X [M, H]; gate/up project H -> I, down projects I -> H; one rank r. */
+/* Gated MLP activation applied to the gate projection e (h = act(e) * u). */
+typedef enum {
+    LORA_ACT_SWIGLU = 0,          /* silu(e) = e * sigmoid(e) */
+    LORA_ACT_GEGLU = 1            /* gelu(e) = e * Phi(e), Phi the normal CDF (erf form) */
+} lora_act;
+
+/* Gated MLP: X [M, H]; gate/up project H -> I, down projects I -> H; one rank r. */
 typedef struct {
     int64_t M, H, I, r;
     int32_t dtype;                /* LORA_BF16 only */
+    int32_t act;                  /* lora_act */
 } lora_mlp_shape;
 
 /* One adapted projection of the MLP: W [n_out, n_in], A [r, n_in], B [n_out, r], scale s. */
@@ -81,6 +89,25 @@ typedef struct {
     const void* B;
     float s;
 } lora_proj;
+
+/* Fused projection whose N = n[0] + .. + n[L-1] output columns split into L leaves (the
+ * query / key / value heads of an attention block), each leaf with its own rank-r adapter.
+ * L in 1..3; L * r <= 64 and r a multiple of 8; every n[l] a positive multiple of 8
+ * (entries past L ignored); d_in a multiple of 8. */
+typedef struct {
+    int64_t M, d_in;
+    int64_t n[3];
+    int32_t L;
+    int32_t r;
+    int32_t dtype;                /* LORA_BF16 only */
+} lora_qkv_shape;
+
+/* One leaf's adapter: A [r, d_in] (down), B [n_l, r] (up), scale s. */
+typedef struct {
+    const void* A;
+    const void* B;
+    float s;
+} lora_adapter;
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* lora_status_string(int status);
@@ -93,6 +120,9 @@ size_t lora_workspace_bytes(int op, const lora_shape* sh);
 
 /* Bytes of workspace the MLP entry points need (op = LORA_OP_MLP_FWD / LORA_OP_MLP_BWD). */
 size_t lora_mlp_workspace_bytes(int op, const lora_mlp_shape* sh);
+
+/* Bytes of workspace the fused-leaf entry points need (op = LORA_OP_QKV_FWD / LORA_OP_QKV_BWD). */
+size_t lora_qkv_workspace_bytes(int op, const lora_qkv_shape* sh);
 
 /* Zero the device error word at the head of `ws` (asynchronous on `stream`). */
 lora_status lora_clear_device_error(void* ws, void* stream);
@@ -191,11 +221,11 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
                             void* dX, void* dA, void* dB, void* dm, void* dbias,
                             void* ws, size_t ws_bytes, void* stream);
 
-/* ---------------------------------------------------------------- LoRA SwiGLU MLP
- * e = X Wg^T + sg (X Ag^T) Bg^T,  u = X Wu^T + su (X Au^T) Bu^T,  h = silu(e) * u,
- * Y = h Wd^T + sd (h Ad^T) Bd^T.
+/* ---------------------------------------------------------------- LoRA gated MLP (SwiGLU / GeGLU)
+ * e = X Wg^T + sg (X Ag^T) Bg^T,  u = X Wu^T + su (X Au^T) Bu^T,  h = act(e) * u,
+ * Y = h Wd^T + sd (h Ad^T) Bd^T,  act = silu (sh->act = LORA_ACT_SWIGLU) or gelu (LORA_ACT_GEGLU).
  * "How Unsloth's FastLoRA Kernel Differs ...", Fused Forward Pass Architecture (LoRA_MLP)
- * and Activation Function Fusion (SwiGLU computed with the LoRA outputs).
+ * and Activation Function Fusion (SwiGLU and GeGLU computed with the LoRA outputs).
  *   gate, up: W [I, H], A [r, H], B [I, r];  down: W [H, I], A [r, I], B [H, r].
  *   Y [M, H]; e_save, u_save, h_save [M, I] (required: the backward reads them);
  *   Zgu_save [M, 2r] = [X Ag^T | X Au^T] and Zd_save [M, r] = h Ad^T (required).
@@ -206,7 +236,7 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
                                 void* Zd_save, void* ws, size_t ws_bytes, void* stream);
 
 /* Backward of lora_mlp_swiglu_fwd (base weights frozen):
- *   dh = dY Wd + sd (dY Bd) Ad,  de = dh u silu'(e),  du = dh silu(e),
+ *   dh = dY Wd + sd (dY Bd) Ad,  de = dh u act'(e),  du = dh act(e),
  *   dX = de Wg + du Wu + sg (de Bg) Ag + su (du Bu) Au,
  *   dA* = s* (d* B*)^T (input),  dB* = s* (d*)^T Z*.
  * "How Unsloth's FastLoRA Kernel Differs ...", Custom Backward Pass Implementation.
@@ -218,6 +248,33 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
                                 const void* Zgu_saved, const void* Zd_saved, const void* dY,
                                 void* dX, void* dAg, void* dBg, void* dAu, void* dBu,
                                 void* dAd, void* dBd, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- fused-leaf (QKV) LoRA linear
+ * One X stream against the fused base weight, each leaf's low-rank term added to its own
+ * output columns:
+ *   Y[:, leaf l] = X W0[leaf l]^T + s_l (X A_l^T) B_l^T  (+ bias),
+ * i.e. Y = X W0^T + Z blockdiag(s_0 B_0, .., s_{L-1} B_{L-1})^T with Z = X [A_0; ..]^T.
+ * "How Unsloth's FastLoRA Kernel Differs ...", Fused Forward Pass Architecture (LoRA_QKV:
+ * the attention query/key/value projections) and "nunchaku-style kernel fusion" (OneTrainer
+ * #1680, the fused-leaf forward: each leaf's up-projection narrowed to that leaf's rows).
+ *   X [M, d_in]; W0 [N, d_in] (leaf l owns rows n[0] + .. + n[l-1] onward); leaves[L];
+ *   bias [N] or NULL; Y [M, N]; Z_save [M, L r] = [X A_0^T | X A_1^T | ..] or NULL (all bf16).
+ *   A leaf with s == 0 adds exactly nothing to its columns.
+ */
+lora_status lora_qkv_fwd(const lora_qkv_shape* sh, const void* X, const void* W0, const lora_adapter* leaves,
+                         const void* bias, void* Y, void* Z_save, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of lora_qkv_fwd (W0 frozen), with dY_l the columns of dY that belong to leaf l:
+ *   dX = dY W0 + sum_l s_l (dY_l B_l) A_l,  dA_l = s_l (dY_l B_l)^T X,  dB_l = s_l dY_l^T Z_l,
+ *   dbias = colsum(dY).
+ * Same pages and sections as lora_qkv_fwd (custom backward of the fused projection).
+ *   Z_saved [M, L r] from the forward, or NULL (recomputed); dY [M, N];
+ *   dX [M, d_in] or NULL; dA[l] [r, d_in] and dB[l] [n_l, r] (arrays of L device pointers,
+ *   all required); dbias [N] or NULL.
+ */
+lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0, const lora_adapter* leaves,
+                         const void* Z_saved, const void* dY, void* dX, void* const* dA, void* const* dB,
+                         void* dbias, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- W8A8 + LoRA epilogue
  * Per-row symmetric int8 quantisation of a bf16 matrix, decided in fp32:

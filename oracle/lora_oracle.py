@@ -16,17 +16,19 @@ deliberately different route from the fused backward formulas of the kernels.
 Shapes (row-major): X [M, in], W0 [out, in], A [r, in] (down), B [out, r] (up),
 bias [out], m [out], dY [M, out].  s = strength * alpha / r.
 
-numpy's matmul (BLAS) is the only library primitive used; all arrays are
+numpy's matmul (BLAS) and scipy's erf (for GELU) are the only library primitives used; all arrays are
 float64 unless a function says otherwise.
 """
 from __future__ import annotations
 
 import numpy as np
+from scipy.special import erf as _erf
 
 __all__ = [
     "f64", "adapted_weight", "lora_linear_fwd", "lora_linear_bwd", "dora_rownorm2",
-    "dora_linear_fwd", "dora_linear_bwd", "silu", "dsilu", "mlp_swiglu_fwd", "mlp_swiglu_bwd",
+    "dora_linear_fwd", "dora_linear_bwd", "silu", "dsilu", "gelu", "dgelu", "mlp_swiglu_fwd", "mlp_swiglu_bwd",
     "quantize_rows", "int8_accumulate", "w8a8_lora_fwd", "w8a8_dequant_weight", "w8a8_lora_bwd",
+    "qkv_adapted_weight", "qkv_lora_fwd", "qkv_lora_bwd", "qkv_fwd_rows", "qkv_bwd_sampled",
     "lora_fwd_rows", "lora_bwd_sampled", "dora_fwd_rows", "dora_bwd_sampled", "dora_bwd_rows_sampled",
     "mlp_fwd_rows", "mlp_bwd_rows",
 ]
@@ -81,6 +83,48 @@ def lora_linear_bwd(X, W0, A, B, s, dY):
     dB = s * (dWp @ A.T)
     dbias = dY.sum(axis=0)
     return dX, dA, dB, dbias
+
+
+# ----------------------------------------------------------------------------- fused-leaf (QKV)
+def qkv_adapted_weight(W0, leaves):
+    """The fused projection's adapted weight, leaf by leaf.
+
+    W0 [N, in] stacks the leaves' base rows in order; leaf l = (A_l [r, in],
+    B_l [n_l, r], s_l) adapts only its own rows: W'[leaf l] = W0[leaf l] + s_l B_l A_l.
+    "How Unsloth's FastLoRA Kernel Differs ...", Fused Forward Pass Architecture
+    (LoRA_QKV) and "nunchaku-style kernel fusion" (#1680: fused-qkv adapters, each
+    lora_up narrowed to its leaf's rows).
+    """
+    parts, row = [], 0
+    for A, B, s in leaves:
+        n = B.shape[0]
+        parts.append(adapted_weight(W0[row:row + n], A, B, s))
+        row += n
+    assert row == W0.shape[0], "leaf rows must cover W0"
+    return np.concatenate(parts, axis=0)
+
+
+def qkv_lora_fwd(X, W0, leaves, bias=None):
+    """y = X W'^T (+ bias) with the leaf-wise adapted fused weight."""
+    Y = X @ qkv_adapted_weight(W0, leaves).T
+    if bias is not None:
+        Y = Y + bias[None, :]
+    return Y
+
+
+def qkv_lora_bwd(X, W0, leaves, dY):
+    """Gradients of qkv_lora_fwd (W0 frozen): dX = dY W', dW' = dY^T X and, per leaf,
+    dA_l = s_l B_l^T dW'[leaf l], dB_l = s_l dW'[leaf l] A_l^T; dbias = colsum(dY)."""
+    Wp = qkv_adapted_weight(W0, leaves)
+    dX = dY @ Wp
+    dWp = dY.T @ X
+    dA, dB, row = [], [], 0
+    for A, B, s in leaves:
+        n = B.shape[0]
+        dA.append(s * (B.T @ dWp[row:row + n]))
+        dB.append(s * (dWp[row:row + n] @ A.T))
+        row += n
+    return dX, dA, dB, dY.sum(axis=0)
 
 
 # ----------------------------------------------------------------------------- DoRA
@@ -170,22 +214,37 @@ def dsilu(x):
     return sg * (1.0 + x * (1.0 - sg))
 
 
-def mlp_swiglu_fwd(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd):
-    """LoRA SwiGLU MLP forward with each projection's adapter materialised.
+def gelu(x):
+    """Exact GELU: gelu(x) = x * Phi(x), Phi the standard normal CDF = (1 + erf(x / sqrt 2)) / 2."""
+    return x * 0.5 * (1.0 + _erf(x / np.sqrt(2.0)))
+
+
+def dgelu(x):
+    """d gelu / dx = Phi(x) + x * phi(x), phi(x) = exp(-x^2 / 2) / sqrt(2 pi)."""
+    return 0.5 * (1.0 + _erf(x / np.sqrt(2.0))) + x * np.exp(-0.5 * x * x) / np.sqrt(2.0 * np.pi)
+
+
+GATE_ACTS = {"swiglu": (silu, dsilu), "geglu": (gelu, dgelu)}
+
+
+def mlp_swiglu_fwd(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, act="swiglu"):
+    """LoRA gated MLP forward with each projection's adapter materialised.
 
     "How Unsloth's FastLoRA Kernel Differs ...", Fused Forward Pass
     Architecture and Activation Function Fusion: e = X Wg'^T, u = X Wu'^T,
-    h = silu(e) * u, y = h Wd'^T.  Returns (y, e, u, h).
+    h = act(e) * u, y = h Wd'^T, act = silu (SwiGLU) or gelu (GeGLU).
+    Returns (y, e, u, h).
     """
+    f, _ = GATE_ACTS[act]
     e = X @ adapted_weight(Wg, Ag, Bg, sg).T
     u = X @ adapted_weight(Wu, Au, Bu, su).T
-    h = silu(e) * u
+    h = f(e) * u
     y = h @ adapted_weight(Wd, Ad, Bd, sd).T
     return y, e, u, h
 
 
-def mlp_swiglu_bwd(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY):
-    """Backward of the LoRA SwiGLU MLP (base weights frozen).
+def mlp_swiglu_bwd(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY, act="swiglu"):
+    """Backward of the LoRA gated MLP (base weights frozen).
 
     "How Unsloth's FastLoRA Kernel Differs ...", Custom Backward Pass
     Implementation (down, up and gate adapter gradients, each pre-scaled).
@@ -194,13 +253,14 @@ def mlp_swiglu_bwd(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY):
     Wgp = adapted_weight(Wg, Ag, Bg, sg)
     Wup = adapted_weight(Wu, Au, Bu, su)
     Wdp = adapted_weight(Wd, Ad, Bd, sd)
+    f, df = GATE_ACTS[act]
     e = X @ Wgp.T
     u = X @ Wup.T
-    h = silu(e) * u
+    h = f(e) * u
     dh = dY @ Wdp
     dWdp = dY.T @ h
-    de = dh * u * dsilu(e)
-    du = dh * silu(e)
+    de = dh * u * df(e)
+    du = dh * f(e)
     dX = de @ Wgp + du @ Wup
     dWgp = de.T @ X
     dWup = du.T @ X
@@ -300,6 +360,26 @@ def lora_bwd_sampled(X, W0, A, B, s, dY, rows, in_cols, out_rows):
     return dX, dA, dB, dY.sum(axis=0)
 
 
+def qkv_fwd_rows(X, W0, leaves, rows, bias=None):
+    """Rows `rows` of the fused-leaf output."""
+    return qkv_lora_fwd(X[rows], W0, leaves, bias)
+
+
+def qkv_bwd_sampled(X, W0, leaves, dY, rows, in_cols, out_rows):
+    """Sampled fused-leaf gradients: dX[rows], and per leaf l dA_l[:, in_cols] and
+    dB_l[out_rows[l]] (rows within the leaf), with the column / row slices of
+    dW' = dY^T X formed as in lora_bwd_sampled."""
+    dX = dY[rows] @ qkv_adapted_weight(W0, leaves)
+    dA, dB, row = [], [], 0
+    for (A, B, s), orows in zip(leaves, out_rows):
+        n = B.shape[0]
+        dYl = dY[:, row:row + n]
+        dA.append(s * (B.T @ (dYl.T @ X[:, in_cols])))
+        dB.append(s * ((dYl[:, orows].T @ X) @ A.T))
+        row += n
+    return dX, dA, dB
+
+
 def dora_fwd_rows(X, W0, A, B, m, s, rows, eps=1e-12, bias=None):
     """Rows `rows` of the DoRA output, plus the full norm vector n."""
     return dora_linear_fwd(X[rows], W0, A, B, m, s, eps, bias)
@@ -352,11 +432,11 @@ def dora_bwd_rows_sampled(X, W0, A, B, m, s, dY, rows, out_rows, eps=1e-12):
     return dX, dB, dm
 
 
-def mlp_fwd_rows(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, rows):
-    """Rows `rows` of (y, e, u, h) of the SwiGLU MLP."""
-    return mlp_swiglu_fwd(X[rows], Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd)
+def mlp_fwd_rows(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, rows, act="swiglu"):
+    """Rows `rows` of (y, e, u, h) of the gated MLP."""
+    return mlp_swiglu_fwd(X[rows], Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, act=act)
 
 
-def mlp_bwd_rows(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY, rows):
-    """Rows `rows` of dX of the SwiGLU MLP (each row of dX depends on its own row only)."""
-    return mlp_swiglu_bwd(X[rows], Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY[rows])["dX"]
+def mlp_bwd_rows(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY, rows, act="swiglu"):
+    """Rows `rows` of dX of the gated MLP (each row of dX depends on its own row only)."""
+    return mlp_swiglu_bwd(X[rows], Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY[rows], act=act)["dX"]

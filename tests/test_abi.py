@@ -38,7 +38,7 @@ def test_status_strings(lib):
     assert L.lora_status_string(0) == "ok"
     assert "workspace" in L.lora_status_string(4)
     assert L.lora_status_string(99) == "unknown status"
-    assert L.lora_abi_version() == 2
+    assert L.lora_abi_version() == 4
 
 
 def test_workspace_bytes_rejects_bad_shapes(lib):
@@ -51,6 +51,8 @@ def test_workspace_bytes_rejects_bad_shapes(lib):
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16)) > 0
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 40)) == 0          # r > 32
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, L.LORA_F32)) == 0
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, act=L.LORA_ACT_GEGLU)) > 0
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, act=2)) == 0         # unknown act
 
 
 def test_entry_points_validate_before_launch(lib):
@@ -92,3 +94,34 @@ def test_entry_points_validate_before_launch(lib):
     r = lib.lora_mlp_swiglu_fwd(ctypes.byref(mlp), fake, ctypes.byref(pr), None, ctypes.byref(pr), fake, fake, fake,
                                 fake, fake, fake, fake, 1 << 30, None)
     assert r == 1  # up projection missing
+
+
+def test_qkv_validation(lib):
+    """Fused-leaf shapes and arguments are validated before anything is launched."""
+    ok = L.qkv_shape(64, 256, [256, 64, 64], 16)
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, ok) > 0
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_BWD, ok) > 0
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 64, 64], 32)) == 0  # L r > 64
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 60], 16)) == 0      # n % 8
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 0], 16)) == 0       # empty leaf
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256], 16, L.LORA_F32)) == 0
+    four = L.qkv_shape(64, 256, [64, 64, 64], 8)
+    four.L = 4
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, four) == 0
+    fake = ctypes.c_void_p(1 << 20)
+    odd = 1 << 20 | 8
+    lv = (L.LoraAdapter * 3)(*[L.LoraAdapter(1 << 20, 1 << 20, 1.0) for _ in range(3)])
+    r = lib.lora_qkv_fwd(ctypes.byref(ok), fake, fake, None, None, fake, None, fake, 1 << 30, None)
+    assert r == 1  # leaves missing
+    lv[1] = L.LoraAdapter(1 << 20, odd, 1.0)
+    r = lib.lora_qkv_fwd(ctypes.byref(ok), fake, fake, lv, None, fake, None, fake, 1 << 30, None)
+    assert r == 3  # misaligned B of leaf 1
+    lv[1] = L.LoraAdapter(1 << 20, 1 << 20, float("inf"))
+    r = lib.lora_qkv_fwd(ctypes.byref(ok), fake, fake, lv, None, fake, None, fake, 1 << 30, None)
+    assert r == 1  # non-finite s
+    lv[1] = L.LoraAdapter(1 << 20, 1 << 20, 1.0)
+    r = lib.lora_qkv_fwd(ctypes.byref(ok), fake, fake, lv, None, fake, None, fake, 16, None)
+    assert r == 4  # workspace too small
+    ptrs = (ctypes.c_void_p * 3)(1 << 20, None, 1 << 20)
+    r = lib.lora_qkv_bwd(ctypes.byref(ok), fake, fake, lv, None, fake, None, ptrs, ptrs, None, fake, 1 << 30, None)
+    assert r == 1  # dA[1] missing

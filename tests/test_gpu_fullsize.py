@@ -74,19 +74,21 @@ def test_persistent_dora(ops, two_ctas):
     ws_clear(ops)
 
 
-def test_persistent_mlp(ops, two_ctas):
+@pytest.mark.parametrize("act", ["swiglu", "geglu"])
+def test_persistent_mlp(ops, two_ctas, act):
     case = D.scaled(D.WORKLOADS["mlp_swiglu_4096x14336_bf16"], M=400, H=200, I=520, r=16, alpha=24.0)
     t = D.make_mlp(case)
     g = {k: gpu(v) for k, v in t.items()}
     P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
-    Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
+    code = {"swiglu": 0, "geglu": 1}[act]
+    Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"], act=code)
     args = tuple(x if isinstance(x, float) else f64(x) for x in
                  (t["X"], t["Wg"], t["Ag"], t["Bg"], case.s, t["Wu"], t["Au"], t["Bu"], case.s,
                   t["Wd"], t["Ad"], t["Bd"], case.s))
-    ry, re, ru, rh = O.mlp_swiglu_fwd(*args)
+    ry, re, ru, rh = O.mlp_swiglu_fwd(*args, act=act)
     assert_close(Y, ry, "bf16", "y")
-    gr = ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
-    ref = O.mlp_swiglu_bwd(*args, f64(t["dY"]))
+    gr = ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"], act=code)
+    ref = O.mlp_swiglu_bwd(*args, f64(t["dY"]), act=act)
     for k in ("dX", "dAg", "dBg", "dAu", "dBu", "dAd", "dBd"):
         assert_close(gr[k], ref[k], "bf16", k)
     ws_clear(ops)
@@ -156,6 +158,28 @@ def test_full_mlp_swiglu(ops):
     assert_close(gr["dX"][rows], O.mlp_bwd_rows(*args, f64(t["dY"]), rows), "bf16", "dX rows")
     for k in ("dAg", "dBg", "dAu", "dBu", "dAd", "dBd"):
         assert torch.isfinite(gr[k].float()).all()
+
+
+def test_full_qkv_gqa(ops):
+    case = D.WORKLOADS["qkv_lora_4096_gqa_bf16"]
+    t = D.make_qkv(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    leaves = [(g[f"A{l}"], g[f"B{l}"], case.s[l]) for l in range(3)]
+    Y, Z = ops.lora_qkv_fwd(g["X"], g["W0"], leaves)
+    dX, dA, dB, _ = ops.lora_qkv_bwd(g["X"], g["W0"], leaves, Z, g["dY"])
+    torch.cuda.synchronize()
+    ws_clear(ops)
+    l64 = [(f64(t[f"A{l}"]), f64(t[f"B{l}"]), case.s[l]) for l in range(3)]
+    X, W0, dY = f64(t["X"]), f64(t["W0"]), f64(t["dY"])
+    rows = [0, 1, 127, 128, 8191, 16383]
+    assert_close(Y[rows], O.qkv_fwd_rows(X, W0, l64, rows), "bf16", "Y rows")
+    cols = [0, 63, 64, 2047, 4095]
+    orows = [[0, 255, 4095], [0, 1023], [1, 1000]]
+    sX, sA, sB = O.qkv_bwd_sampled(X, W0, l64, dY, rows, cols, orows)
+    assert_close(dX[rows], sX, "bf16", "dX rows")
+    for l in range(3):
+        assert_close(dA[l][:, cols].T, sA[l].T, "bf16", f"dA{l} cols")
+        assert_close(dB[l][orows[l]], sB[l], "bf16", f"dB{l} rows")
 
 
 def test_full_w8a8_3072(ops):

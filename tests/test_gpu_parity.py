@@ -186,20 +186,82 @@ def _mlp_args64(t, s):
             f64(t["Wd"]), f64(t["Ad"]), f64(t["Bd"]), s)
 
 
+ACTS = {"swiglu": 0, "geglu": 1}
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu"])
 @pytest.mark.parametrize("I", [200, 256])
-def test_mlp_fwd_bwd(ops, I):
+def test_mlp_fwd_bwd(ops, I, act):
     case, t, g, P = mlp_inputs(M=300, H=136, I=I, r=16, alpha=24.0)
-    Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
+    Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"], act=ACTS[act])
     args = _mlp_args64(t, case.s)
-    ry, re, ru, rh = O.mlp_swiglu_fwd(*args)
+    ry, re, ru, rh = O.mlp_swiglu_fwd(*args, act=act)
     assert_close(saved["e"], re, "bf16", "e")
     assert_close(saved["u"], ru, "bf16", "u")
     assert_close(saved["h"], rh, "bf16", "h")
     assert_close(Y, ry, "bf16", "y")
-    gr = ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
-    ref = O.mlp_swiglu_bwd(*args, f64(t["dY"]))
+    gr = ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"], act=ACTS[act])
+    ref = O.mlp_swiglu_bwd(*args, f64(t["dY"]), act=act)
     for k in ("dX", "dAg", "dBg", "dAu", "dBu", "dAd", "dBd"):
         assert_close(gr[k], ref[k], "bf16", k)
+
+
+# ---------------------------------------------------------------------------- fused-leaf (QKV)
+def qkv_inputs(**kw):
+    case = D.scaled(D.WORKLOADS["qkv_lora_4096_gqa_bf16"], **kw)
+    t = D.make_qkv(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    L = len(case.n)
+    leaves_g = [(g[f"A{l}"], g[f"B{l}"], case.s[l]) for l in range(L)]
+    leaves_64 = [(f64(t[f"A{l}"]), f64(t[f"B{l}"]), case.s[l]) for l in range(L)]
+    return case, t, g, leaves_g, leaves_64
+
+
+@pytest.mark.parametrize("n,r,bias", [((256, 72, 72), 16, True), ((256, 72, 72), 8, False),
+                                      ((136, 264), 32, False), ((200,), 64, True)])
+def test_qkv_fwd_bwd(ops, n, r, bias):
+    case, t, g, lg_, l64 = qkv_inputs(M=300, d_in=200, n=n, r=r, bias=bias)
+    Y, Z = ops.lora_qkv_fwd(g["X"], g["W0"], lg_, g["bias"])
+    X, W0, dY, b = f64(t["X"]), f64(t["W0"]), f64(t["dY"]), f64(t["bias"])
+    assert_close(Y, O.qkv_lora_fwd(X, W0, l64, b), "bf16", "Y")
+    assert_close(Z, np.concatenate([X @ A.T for A, _, _ in l64], axis=1), "bf16", "Z")
+    dX, dA, dB, db = ops.lora_qkv_bwd(g["X"], g["W0"], lg_, Z, g["dY"], need_dbias=True)
+    rX, rA, rB, rb = O.qkv_lora_bwd(X, W0, l64, dY)
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(db[None], rb[None], "bf16", "dbias")
+    for i in range(len(n)):
+        assert_close(dA[i], rA[i], "bf16", f"dA{i}")
+        assert_close(dB[i], rB[i], "bf16", f"dB{i}")
+    # without the saved Z the backward recomputes it: same kernels, same bits
+    dX2, dA2, dB2, _ = ops.lora_qkv_bwd(g["X"], g["W0"], lg_, None, g["dY"])
+    assert torch.equal(dX, dX2)
+    assert all(torch.equal(a, b_) for a, b_ in zip(dA + dB, dA2 + dB2))
+
+
+def test_qkv_zero_strength_leaf_is_frozen_base_bits(ops):
+    case, t, g, lg_, _ = qkv_inputs(M=260, d_in=264, n=(256, 64, 64), r=16)
+    mixed = [lg_[0], (lg_[1][0], lg_[1][1], 0.0), lg_[2]]
+    off = [(A, B, 0.0) for A, B, _ in lg_]
+    Y, _ = ops.lora_qkv_fwd(g["X"], g["W0"], mixed)
+    Y0, _ = ops.lora_qkv_fwd(g["X"], g["W0"], off)
+    assert torch.equal(Y[:, 256:320], Y0[:, 256:320])
+    assert not torch.equal(Y[:, :256], Y0[:, :256])
+    dX, dA, dB, _ = ops.lora_qkv_bwd(g["X"], g["W0"], mixed, None, g["dY"])
+    assert not dA[1].any() and not dB[1].any()
+    dX0, dA0, dB0, _ = ops.lora_qkv_bwd(g["X"], g["W0"], off, None, g["dY"])
+    assert all(not a.any() for a in dA0 + dB0)
+    Bz = torch.zeros(384, 16, dtype=torch.bfloat16, device=DEV)
+    ref = ops.lora_linear_bwd(g["X"], g["W0"], lg_[0][0], Bz, None, g["dY"], 0.0)[0]
+    assert torch.equal(dX0, ref)    # every strength 0: dX is the frozen base's, bit for bit
+
+
+def test_qkv_m_zero_is_noop(ops):
+    case, t, g, lg_, _ = qkv_inputs(M=8, d_in=64, n=(64, 16, 16), r=8)
+    X = g["X"][:0]
+    Y, Z = ops.lora_qkv_fwd(X, g["W0"], lg_)
+    assert Y.shape == (0, 96) and Z.shape == (0, 24)
+    dX, dA, dB, db = ops.lora_qkv_bwd(X, g["W0"], lg_, Z, g["dY"][:0], need_dbias=True)
+    assert all(not a.any() for a in dA + dB) and not db.any()
 
 
 # ---------------------------------------------------------------------------- W8A8

@@ -8,6 +8,7 @@ dropped term, a wrong sign or index, or a transposed operand in the oracle
 fails at least one of them.
 """
 import itertools
+import math
 import os
 
 import numpy as np
@@ -271,6 +272,142 @@ def test_mlp_grads_match_library_autograd():
     got = O.mlp_swiglu_bwd(*_mlp_args(d), d["dY"])
     for key in ("dX", "dAg", "dBg", "dAu", "dBu", "dAd", "dBd"):
         assert rel(got[key], t[key[1:]].grad.numpy()) < 1e-12, key
+
+
+# ------------------------------------------------------------------ GeGLU MLP
+def test_gelu_special_values_and_derivative():
+    # gelu(0) = 0, gelu(1) = Phi(1), gelu(x) -> x and -> 0 in the tails
+    assert O.gelu(np.array(0.0)) == 0.0
+    np.testing.assert_allclose(O.gelu(np.array(1.0)), 0.8413447460685429, rtol=1e-15)
+    np.testing.assert_allclose(O.gelu(np.array([12.0, -12.0])), [12.0, 0.0], atol=1e-15)
+    # Phi(-x) = 1 - Phi(x) gives gelu(x) - gelu(-x) = x
+    x = np.linspace(-5, 5, 41)
+    np.testing.assert_allclose(O.gelu(x) - O.gelu(-x), x, atol=1e-14)
+    # derivative: dgelu(0) = 1/2, finite differences elsewhere
+    assert O.dgelu(np.array(0.0)) == 0.5
+    fd = (O.gelu(x + 1e-6) - O.gelu(x - 1e-6)) / 2e-6
+    np.testing.assert_allclose(O.dgelu(x), fd, rtol=1e-8, atol=1e-10)
+    # library cross-check (exact, erf-based variant)
+    np.testing.assert_allclose(O.gelu(x), torch.nn.functional.gelu(torch.from_numpy(x)).numpy(), rtol=1e-14,
+                               atol=1e-16)
+
+
+def test_geglu_differs_from_swiglu_and_matches_explicit():
+    d = mlp_case(M=6, H=8, I=10, r=2, seed=25)
+    args = _mlp_args(d)
+    y, e, u, h = O.mlp_swiglu_fwd(*args, act="geglu")
+    h2 = np.array([[ev * 0.5 * (1 + math.erf(ev / math.sqrt(2))) for ev in row] for row in e]) * u
+    assert rel(h, h2) < 1e-14
+    assert rel(y, O.mlp_swiglu_fwd(*args)[0]) > 1e-2
+
+
+def test_geglu_grads_finite_difference():
+    d = mlp_case(seed=26)
+    args = list(_mlp_args(d))
+    L = lambda: float((d["dY"] * O.mlp_swiglu_fwd(*args, act="geglu")[0]).sum())  # noqa: E731
+    got = O.mlp_swiglu_bwd(*args, d["dY"], act="geglu")
+    for key, idx in (("dX", 0), ("dAg", 2), ("dBg", 3), ("dAu", 6), ("dBu", 7), ("dAd", 10), ("dBd", 11)):
+        assert rel(got[key], _fd_grad(L, args[idx])) < 1e-7, key
+
+
+def test_geglu_grads_match_library_autograd():
+    d = mlp_case(M=5, H=7, I=9, r=2, seed=27)
+    t = {k: torch.tensor(v, requires_grad=True) for k, v in d.items()}
+    s = dict(g=1.1, u=0.9, d=1.3)
+    W = {p: t["W" + p].detach() + s[p] * t["B" + p] @ t["A" + p] for p in "gud"}
+    e = t["X"] @ W["g"].T
+    u = t["X"] @ W["u"].T
+    y = (torch.nn.functional.gelu(e) * u) @ W["d"].T
+    y.backward(t["dY"].detach())
+    got = O.mlp_swiglu_bwd(*_mlp_args(d), d["dY"], act="geglu")
+    for key in ("dX", "dAg", "dBg", "dAu", "dBu", "dAd", "dBd"):
+        assert rel(got[key], t[key[1:]].grad.numpy()) < 1e-12, key
+
+
+# ------------------------------------------------------------------ fused-leaf (QKV)
+def qkv_case(M=6, d_in=10, n=(8, 4, 4), r=2, seed=30):
+    g = rng(seed)
+    X = g.standard_normal((M, d_in))
+    W0 = g.standard_normal((sum(n), d_in)) / np.sqrt(d_in)
+    leaves = [(g.standard_normal((r, d_in)) / np.sqrt(d_in), g.standard_normal((nl, r)) * 0.3, 0.5 + 0.4 * i)
+              for i, nl in enumerate(n)]
+    bias = g.standard_normal(sum(n)) * 0.1
+    dY = g.standard_normal((M, sum(n)))
+    return X, W0, leaves, bias, dY
+
+
+def test_qkv_fused_equals_per_leaf_low_rank_sum():
+    """y[:, leaf l] = X W0[leaf l]^T + s_l (X A_l^T) B_l^T + bias, each leaf's B narrowed to its rows."""
+    X, W0, leaves, bias, _ = qkv_case(M=11, d_in=16, n=(16, 8, 8), r=3, seed=31)
+    cols, row = [], 0
+    for A, B, s in leaves:
+        n = B.shape[0]
+        cols.append(X @ W0[row:row + n].T + s * ((X @ A.T) @ B.T))
+        row += n
+    assert rel(O.qkv_lora_fwd(X, W0, leaves, bias), np.concatenate(cols, axis=1) + bias) < 1e-13
+
+
+def test_qkv_single_leaf_is_lora_linear():
+    X, W0, leaves, bias, dY = qkv_case(n=(8,), seed=32)
+    A, B, s = leaves[0]
+    assert rel(O.qkv_lora_fwd(X, W0, leaves, bias), O.lora_linear_fwd(X, W0, A, B, s, bias)) < 1e-15
+    dX, dA, dB, db = O.qkv_lora_bwd(X, W0, leaves, dY)
+    rX, rA, rB, rb = O.lora_linear_bwd(X, W0, A, B, s, dY)
+    for a, b in ((dX, rX), (dA[0], rA), (dB[0], rB), (db, rb)):
+        assert rel(a, b) < 1e-15
+
+
+def test_qkv_leaf_isolation_and_zero_strength():
+    """A leaf's adapter touches only its own columns; strength 0 leaves them the frozen base, bit for bit."""
+    X, W0, leaves, _, _ = qkv_case(seed=33)
+    y = O.qkv_lora_fwd(X, W0, leaves)
+    A1, B1, _ = leaves[1]
+    changed = [leaves[0], (A1, B1 * 5.0, leaves[1][2]), leaves[2]]
+    y2 = O.qkv_lora_fwd(X, W0, changed)
+    assert np.array_equal(y[:, :8], y2[:, :8]) and np.array_equal(y[:, 12:], y2[:, 12:])
+    assert not np.allclose(y[:, 8:12], y2[:, 8:12])
+    off = [leaves[0], (A1, B1, 0.0), leaves[2]]
+    assert np.array_equal(O.qkv_lora_fwd(X, W0, off)[:, 8:12], X @ W0[8:12].T)
+
+
+def test_qkv_grads_finite_difference():
+    X, W0, leaves, bias, dY = qkv_case(M=4, d_in=6, n=(8, 4, 4), r=2, seed=34)
+    leaves = [(A.copy(), B.copy(), s) for A, B, s in leaves]
+    L = lambda: float((dY * O.qkv_lora_fwd(X, W0, leaves, bias)).sum())  # noqa: E731
+    dX, dA, dB, db = O.qkv_lora_bwd(X, W0, leaves, dY)
+    assert rel(dX, _fd_grad(L, X)) < 1e-8
+    assert rel(db, _fd_grad(L, bias)) < 1e-8
+    for i, (A, B, _) in enumerate(leaves):
+        assert rel(dA[i], _fd_grad(L, A)) < 1e-8, i
+        assert rel(dB[i], _fd_grad(L, B)) < 1e-8, i
+
+
+def test_qkv_grads_match_library_autograd():
+    X, W0, leaves, bias, dY = qkv_case(M=7, d_in=12, n=(16, 8, 8), r=3, seed=35)
+    tX = torch.tensor(X, requires_grad=True)
+    tl = [(torch.tensor(A, requires_grad=True), torch.tensor(B, requires_grad=True), s) for A, B, s in leaves]
+    Wp, row = [], 0
+    for A, B, s in tl:
+        Wp.append(torch.tensor(W0[row:row + B.shape[0]]) + s * B @ A)
+        row += B.shape[0]
+    y = torch.nn.functional.linear(tX, torch.cat(Wp), torch.tensor(bias))
+    y.backward(torch.tensor(dY))
+    dX, dA, dB, _ = O.qkv_lora_bwd(X, W0, leaves, dY)
+    assert rel(dX, tX.grad.numpy()) < 1e-13
+    for i, (A, B, _) in enumerate(tl):
+        assert rel(dA[i], A.grad.numpy()) < 1e-13 and rel(dB[i], B.grad.numpy()) < 1e-13
+
+
+def test_qkv_sampled_forms_match_full():
+    X, W0, leaves, bias, dY = qkv_case(M=9, d_in=12, n=(16, 8, 8), r=3, seed=36)
+    assert rel(O.qkv_fwd_rows(X, W0, leaves, [1, 7], bias), O.qkv_lora_fwd(X, W0, leaves, bias)[[1, 7]]) < 1e-14
+    fX, fA, fB, _ = O.qkv_lora_bwd(X, W0, leaves, dY)
+    orows = [[0, 15], [3], [2, 7]]
+    sX, sA, sB = O.qkv_bwd_sampled(X, W0, leaves, dY, [2, 8], [0, 5, 11], orows)
+    assert rel(sX, fX[[2, 8]]) < 1e-13
+    for i in range(3):
+        assert rel(sA[i], fA[i][:, [0, 5, 11]]) < 1e-13
+        assert rel(sB[i], fB[i][orows[i]]) < 1e-13
 
 
 # ------------------------------------------------------------------ W8A8
