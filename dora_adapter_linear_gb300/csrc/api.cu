@@ -36,6 +36,11 @@ uint64_t wait_timeout_ns() {
   return v;
 }
 
+bool env_flag(const char* name) {
+  const char* e = getenv(name);
+  return e && atoi(e) != 0;
+}
+
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 #define CK(x)                                  \
   do {                                         \
@@ -135,6 +140,7 @@ struct DoraBwdWs {
   uint32_t* err;
   float *c, *g, *dot, *csum, *dotp, *csump, *Kr, *Kg;
   void *Bc, *gB, *Gs, *Zrec;
+  bf16* dYc;     // [M, out] dY o c (bf16 path)
   float *PB, *PA, *PW;
   int splitsB, splitsA, splitsW;
 };
@@ -162,10 +168,12 @@ size_t plan_dora_bwd(const lora_shape& sh, char* base, DoraBwdWs* w) {
     w->PW = c.take<float>(w->splitsW * in * r);
     w->dotp = c.take<float>(w->splitsB * out);
     w->csump = c.take<float>(w->splitsB * out);
+    w->dYc = c.take<bf16>(M * out);
   } else {
     w->splitsB = w->splitsA = w->splitsW = 1;
     w->PB = w->PA = w->PW = nullptr;
     w->dotp = w->csump = nullptr;
+    w->dYc = nullptr;
   }
   return c.off;
 }
@@ -862,12 +870,19 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       CK(rowproj(d, st));
       Z = w.Zrec;
     }
-    {  // one pass over dY and Y: dY^T Z partials, colsum(dY), colsum(dY o Y)
+    // dP = dY o c enters the dX GEMM either as a copy written by the pass below (default) or
+    // scaled tile by tile in the GEMM's shared memory (LORA_GB300_DORA_KSCALE=1); same bits.
+    const bool kscale = env_flag("LORA_GB300_DORA_KSCALE");
+    {  // one pass over dY and Y: dY^T Z partials, colsum(dY), colsum(dY o Y), and dY o c
       ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB);
       d.Y = static_cast<const bf16*>(Y);
       d.ldy = out;
       d.colsum = w.csump;
       d.coldot = w.dotp;
+      if (!kscale) {
+        d.sc = w.c;
+        d.sc_out = w.dYc;
+      }
       CK(colreduce(d, st));
     }
     CK(sum_splits<float>(w.dotp, w.splitsB, out, w.dot, nullptr, st));
@@ -882,7 +897,10 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       d.scale_b = s;
       CK(rowproj(d, st));
     }
-    if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, w.c, w.err), st));
+    if (dX) {
+      if (kscale) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, w.c, w.err), st));
+      else CK(tc_gemm(dx_desc(M, in, out, w.dYc, W0, w.Gs, A, r, dX, nullptr, w.err), st));
+    }
     CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA), st));        // X^T (s G)
     CK(colreduce(cr_desc(out, in, r, W0, w.gB, r, w.PW, w.splitsW), st));     // W0^T (g o B)
     CK(gram_rows<bf16>(static_cast<const bf16*>(A), r, in, w.Kr, st));

@@ -111,6 +111,9 @@ struct ColReduceDesc {
   float* colsum = nullptr;     // [splits, K] or null
   float* coldot = nullptr;     // [splits, K] or null
   int splits = 1;
+  // with Y: optional column-scaled copy of S written on the way, sc_out[row, k] = bf16(S[row, k] * sc[k])
+  const float* sc = nullptr;
+  bf16* sc_out = nullptr;      // [rows, K], leading dimension K
 };
 int colreduce_splits(int64_t rows, int64_t K);
 cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st);

@@ -273,6 +273,31 @@ __global__ void __launch_bounds__(128) colreduce_kernel(ColReduceDesc d, int64_t
         if (nt + 1 < R / 8) mma_bf16_16816(acc[nt + 1], a, b2, b3);
       }
     }
+    if (HAS_Y && d.sc_out) {
+      // the column-scaled copy of this 64 x 64 tile: thread tid owns 16-byte chunk (tid & 7) of rows
+      // (tid >> 3) + 16 i, so its 8 scales are fixed for the whole kernel
+      const int c8 = tid & 7;
+      const int64_t gk = k0 + c8 * 8;
+      if (gk < d.K) {
+        const float4 lo = __ldg(reinterpret_cast<const float4*>(d.sc + gk));
+        const float4 hi = __ldg(reinterpret_cast<const float4*>(d.sc + gk + 4));
+        const float sc8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        const int64_t rb = r_begin + (int64_t)rc * BR;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = (tid >> 3) + 16 * i;
+          if (rb + r >= r_end) break;
+          uint4 v = *reinterpret_cast<const uint4*>(pS + (r * PITCH + c8 * 8) * 2);
+          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(w[e]);
+            w[e] = pack_bf16x2(f.x * sc8[2 * e], f.y * sc8[2 * e + 1]);
+          }
+          *reinterpret_cast<uint4*>(d.sc_out + (rb + r) * d.K + gk) = v;
+        }
+      }
+    }
     if (SUMS) {
       const bf16* ps = reinterpret_cast<const bf16*>(pS);
       const bf16* py = reinterpret_cast<const bf16*>(pS + S_BYTES + T_BYTES);
