@@ -459,6 +459,25 @@ def _dora_workload(args, L, ops, peaks, D, dev, steps, warm):
                                    "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                                    "roofline": gemm_roofline(L, peaks, ms, steps + warm, False,
                                                              "dora_4096x11008_bf16")}
+    del g, t
+    # the column variant on the same shapes: magnitude per input column
+    case = D.WORKLOADS["dora_cols_4096x11008_bf16"]
+    t = D.make_linear(case)
+    g = {k: v.to(dev) for k, v in t.items() if v is not None}
+    c0 = ops.dora_colnorm2(g["W0"])
+
+    def cols_step():
+        Y, Z, n, U = ops.dora_cols_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], c0, case.s, case.eps, g["bias"])
+        ops.dora_cols_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], Z, n, U, g["dY"], case.s, case.eps)
+    L.lora_prof_gemm(reset=True)
+    L.lora_prof_enable(True)
+    ms, _, _ = timed(cols_step, steps, warm)
+    L.lora_prof_enable(False)
+    f, b = dora_flops(case.M, case.d_in, case.d_out, case.r)
+    out[case.name] = {"ms_per_step": ms, "tflops": (f + b) / (ms * 1e-3) / 1e12,
+                      "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                      "roofline": gemm_roofline(L, peaks, ms, steps + warm, False, case.name)}
+    del g, t
     return out
 
 

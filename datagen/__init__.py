@@ -10,8 +10,9 @@ fp32 in a fixed order, then rounded to the storage dtype; the oracle receives
 the rounded values upcast to fp64):
 
 * X, dY ~ N(0, 1); W0, A ~ N(0, 1/in); B ~ N(0, 0.02^2); bias ~ N(0, 0.01^2)
-* DoRA magnitude m = rownorm(W0) * U(0.9, 1.1)  (the workload's own recipe
-  for the magnitude vector; it is an input, not part of the forward pass)
+* DoRA magnitude m = rownorm(W0) * U(0.9, 1.1) (column variant: colnorm(W0) *
+  U(0.9, 1.1), one entry per input feature) -- the workload's own recipe for the
+  magnitude vector; it is an input, not part of the forward pass
 * W8A8: X and W0 are drawn as above and left unquantised; quantisation is part
   of the method and lives on each side separately.
 
@@ -40,6 +41,7 @@ class LinearCase:
     alpha: float
     dtype: str            # "f32" or "bf16"
     dora: bool = False
+    dora_cols: bool = False   # DoRA column variant: magnitude per input column
     bias: bool = False
     eps: float = 1e-12
     strength: float = 1.0
@@ -109,6 +111,8 @@ WORKLOADS = {
     "lora_4096_bf16": LinearCase("lora_4096_bf16", 8192, 4096, 4096, 16, 32.0, "bf16", seed=1001),
     "dora_4096x11008_bf16": LinearCase("dora_4096x11008_bf16", 8192, 4096, 11008, 32, 32.0, "bf16",
                                         dora=True, bias=True, seed=1002),
+    "dora_cols_4096x11008_bf16": LinearCase("dora_cols_4096x11008_bf16", 8192, 4096, 11008, 32, 32.0, "bf16",
+                                             dora_cols=True, bias=True, seed=1006),
     "mlp_swiglu_4096x14336_bf16": MlpCase("mlp_swiglu_4096x14336_bf16", 16384, 4096, 14336, 16, 16.0),
     "w8a8_lora_3072": W8A8Case("w8a8_lora_3072", 16384, 3072, 3072, 32, 32.0),
     # grouped-query attention block of a 4096-wide model: 32 query heads, 8 key/value heads of 128
@@ -139,14 +143,15 @@ def make_linear(case: LinearCase):
     A = _normal(g, (case.r, case.d_in), case.d_in ** -0.5)
     B = _normal(g, (case.d_out, case.r), 0.02)
     bias = _normal(g, (case.d_out,), 0.01) if case.bias else None
-    m_noise = torch.rand(case.d_out, generator=g, dtype=torch.float32) * 0.2 + 0.9
+    m_noise = torch.rand(case.d_in if case.dora_cols else case.d_out, generator=g, dtype=torch.float32) * 0.2 + 0.9
     dY = _normal(g, (case.M, case.d_out), 1.0)
     out = {"X": X.to(dt), "W0": W0.to(dt), "A": A.to(dt), "B": B.to(dt), "dY": dY.to(dt),
            "bias": None if bias is None else bias.to(dt)}
-    if case.dora:
-        # magnitude recipe of the workload: row norm of the stored W0 times U(0.9, 1.1)
+    if case.dora or case.dora_cols:
+        # magnitude recipe of the workload: row (column, for the column variant) norm of the
+        # stored W0 times U(0.9, 1.1)
         w = out["W0"].float()
-        out["m"] = (torch.sqrt((w * w).sum(1)) * m_noise).to(dt)
+        out["m"] = (torch.sqrt((w * w).sum(0 if case.dora_cols else 1)) * m_noise).to(dt)
     return out
 
 

@@ -16,7 +16,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "lora_gb300.h")
 
 LORA_F32, LORA_BF16 = 0, 1
 LORA_NOALLOC_SCRATCH_BYTES = 4 << 20   # fixed scratch of lora_linear_fwd_noalloc (header macro)
-OP_LINEAR_FWD, OP_LINEAR_BWD, OP_DORA_FWD, OP_DORA_BWD, OP_MLP_FWD, OP_MLP_BWD, OP_QKV_FWD, OP_QKV_BWD = range(8)
+(OP_LINEAR_FWD, OP_LINEAR_BWD, OP_DORA_FWD, OP_DORA_BWD, OP_MLP_FWD, OP_MLP_BWD, OP_QKV_FWD, OP_QKV_BWD,
+ OP_DORA_COLS_FWD, OP_DORA_COLS_BWD) = range(10)
 STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_UNSUPPORTED", 3: "LORA_ERR_MISALIGNED",
           4: "LORA_ERR_WORKSPACE", 5: "LORA_ERR_CUDA", 6: "LORA_ERR_DEVICE_TIMEOUT"}
 
@@ -67,6 +68,11 @@ _SIGS = {
                                 c_size_t, P]),
     "dora_linear_bwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, P, P, P, P, P, P, c_float, c_float,
                                 P, P, P, P, P, P, c_size_t, P]),
+    "dora_colnorm2": (c_int, [POINTER(LoraShape), P, P, P]),
+    "dora_cols_fwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, P, P, c_float, c_float, P, P, P, P, P,
+                              c_size_t, P]),
+    "dora_cols_bwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, P, P, P, P, c_float, c_float,
+                              P, P, P, P, P, P, c_size_t, P]),
     "lora_mlp_swiglu_fwd": (c_int, [POINTER(LoraMlpShape), P, POINTER(LoraProj), POINTER(LoraProj),
                                     POINTER(LoraProj), P, P, P, P, P, P, P, c_size_t, P]),
     "lora_mlp_swiglu_bwd": (c_int, [POINTER(LoraMlpShape), P, POINTER(LoraProj), POINTER(LoraProj),
@@ -247,6 +253,24 @@ def dora_linear_bwd(sh, X, W0, A, B, m, bias, Y, Z_saved, n_saved, V_saved, dY, 
                                ptr(dA), ptr(dB), ptr(dm), ptr(dbias), ptr(ws),
                                0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
         "dora_linear_bwd")
+
+
+def dora_colnorm2(sh, W0, c0, stream=None):
+    _ck(_lib().dora_colnorm2(ctypes.byref(sh), ptr(W0), ptr(c0), _stream(stream)), "dora_colnorm2")
+
+
+def dora_cols_fwd(sh, X, W0, A, B, m, bias, c0, s, eps, Y, Z_save, n_save, U_save, ws, stream=None):
+    _ck(_lib().dora_cols_fwd(ctypes.byref(sh), ptr(X), ptr(W0), ptr(A), ptr(B), ptr(m), ptr(bias), ptr(c0),
+                             float(s), float(eps), ptr(Y), ptr(Z_save), ptr(n_save), ptr(U_save), ptr(ws),
+                             0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)), "dora_cols_fwd")
+
+
+def dora_cols_bwd(sh, X, W0, A, B, m, Z_saved, n_saved, U_saved, dY, s, eps, dX, dA, dB, dm, dbias, ws,
+                  stream=None):
+    _ck(_lib().dora_cols_bwd(ctypes.byref(sh), ptr(X), ptr(W0), ptr(A), ptr(B), ptr(m), ptr(Z_saved), ptr(n_saved),
+                             ptr(U_saved), ptr(dY), float(s), float(eps), ptr(dX), ptr(dA), ptr(dB), ptr(dm),
+                             ptr(dbias), ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                             _stream(stream)), "dora_cols_bwd")
 
 
 def lora_mlp_swiglu_fwd(sh, X, gate, up, down, Y, e_save, u_save, h_save, Zgu_save, Zd_save, ws, stream=None):

@@ -178,6 +178,61 @@ size_t plan_dora_bwd(const lora_shape& sh, char* base, DoraBwdWs* w) {
   return c.off;
 }
 
+// DoRA column variant (bf16 only)
+struct DoraColsFwdWs {
+  uint32_t* err;
+  float* PU;     // [splitsW, in, r] partials of W0^T B
+  float* Kb;     // [r, r] B^T B
+  float* c;      // [in]
+  bf16* Ac;      // [r, in] A diag(c)
+  bf16* Zs;      // [M, r] s Z
+  bf16* Xc;      // [M, in] X diag(c)
+  int splitsW;
+};
+size_t plan_dora_cols_fwd(const lora_shape& sh, char* base, DoraColsFwdWs* w) {
+  Carve c{base};
+  const int64_t out = sh.d_out, in = sh.d_in, r = sh.r, M = sh.M;
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  w->splitsW = colreduce_splits(out, in);
+  w->PU = c.take<float>(w->splitsW * in * r);
+  w->Kb = c.take<float>(r * r);
+  w->c = c.take<float>(in);
+  w->Ac = c.take<bf16>(r * in);
+  w->Zs = c.take<bf16>(M * r);
+  w->Xc = c.take<bf16>(M * in);
+  return c.off;
+}
+
+struct DoraColsBwdWs {
+  uint32_t* err;
+  float *c, *g, *dot, *dotp, *Kb, *Kga, *Vg, *PA, *PB, *csump;
+  bf16 *Ac, *Ag, *Gs, *Zrec, *dXt;
+  int splitsA, splitsB;
+};
+size_t plan_dora_cols_bwd(const lora_shape& sh, char* base, DoraColsBwdWs* w) {
+  Carve c{base};
+  const int64_t out = sh.d_out, in = sh.d_in, r = sh.r, M = sh.M;
+  w->err = c.take<uint32_t>(kErrBytes / 4);
+  w->splitsA = colreduce_splits(M, in);
+  w->splitsB = colreduce_splits(M, out);
+  w->c = c.take<float>(in);
+  w->g = c.take<float>(in);
+  w->dot = c.take<float>(in);
+  w->dotp = c.take<float>(w->splitsA * in);
+  w->Kb = c.take<float>(r * r);
+  w->Kga = c.take<float>(r * r);
+  w->Vg = c.take<float>(out * r);
+  w->PA = c.take<float>(w->splitsA * in * r);
+  w->PB = c.take<float>(w->splitsB * out * r);
+  w->csump = c.take<float>(w->splitsB * out);
+  w->Ac = c.take<bf16>(r * in);
+  w->Ag = c.take<bf16>(r * in);
+  w->Gs = c.take<bf16>(M * r);
+  w->Zrec = c.take<bf16>(M * r);
+  w->dXt = c.take<bf16>(M * in);
+  return c.off;
+}
+
 struct MlpFwdWs {
   uint32_t* err;
   bf16 *Agu, *Zgus, *Zds;
@@ -393,7 +448,7 @@ const char* lora_status_string(int status) {
   return "unknown status";
 }
 
-int lora_abi_version(void) { return 4; }
+int lora_abi_version(void) { return 5; }
 
 size_t lora_workspace_bytes(int op, const lora_shape* sh) {
   if (check_shape(sh) != LORA_OK) return 0;
@@ -402,6 +457,12 @@ size_t lora_workspace_bytes(int op, const lora_shape* sh) {
     case LORA_OP_LINEAR_BWD: { LinBwdWs w; return plan_lin_bwd(*sh, nullptr, &w); }
     case LORA_OP_DORA_FWD: { DoraFwdWs w; return plan_dora_fwd(*sh, nullptr, &w); }
     case LORA_OP_DORA_BWD: { DoraBwdWs w; return plan_dora_bwd(*sh, nullptr, &w); }
+    case LORA_OP_DORA_COLS_FWD:
+      if (sh->dtype != LORA_BF16) return 0;
+      { DoraColsFwdWs w; return plan_dora_cols_fwd(*sh, nullptr, &w); }
+    case LORA_OP_DORA_COLS_BWD:
+      if (sh->dtype != LORA_BF16) return 0;
+      { DoraColsBwdWs w; return plan_dora_cols_bwd(*sh, nullptr, &w); }
   }
   return 0;
 }
@@ -947,6 +1008,150 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     CK(finalize_dB<float>(out, r, none, 0.f, nullptr, w.g, V_saved, static_cast<const float*>(B), w.Kr, s, true,
                           static_cast<float*>(dB), st));
   }
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------------ DoRA (cols)
+lora_status dora_colnorm2(const lora_shape* sh, const void* W0, float* c0, void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  if (sh->dtype != LORA_BF16) return LORA_ERR_UNSUPPORTED;
+  REQ(W0); REQ(c0);
+  ALN(W0); ALN(c0);
+  CK(colnorm2_bf16(static_cast<const bf16*>(W0), sh->d_out, sh->d_in, c0, (cudaStream_t)stream));
+  return LORA_OK;
+}
+
+lora_status dora_cols_fwd(const lora_shape* sh, const void* X, const void* W0, const void* A, const void* B,
+                          const void* m, const void* bias, const float* c0, float s, float eps, void* Y, void* Z_save,
+                          float* n_save, float* U_save, void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  if (sh->dtype != LORA_BF16) return LORA_ERR_UNSUPPORTED;
+  REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQ(m); REQ(c0); REQM(sh->M, Y); REQ(n_save); REQ(U_save);
+  ALN(X); ALN(W0); ALN(A); ALN(B); ALN(m); ALN(bias); ALN(c0); ALN(Y); ALN(Z_save); ALN(n_save); ALN(U_save);
+  if (!isfinite(s) || !isfinite(eps) || eps < 0.f) return LORA_ERR_INVALID_ARG;
+  DoraColsFwdWs w;
+  if ((e = check_ws(ws, ws_bytes, plan_dora_cols_fwd(*sh, nullptr, &w))) != LORA_OK) return e;
+  plan_dora_cols_fwd(*sh, static_cast<char*>(ws), &w);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
+  const int r = (int)sh->r;
+  const bf16* Ab = static_cast<const bf16*>(A);
+  const bf16* Bb = static_cast<const bf16*>(B);
+  // U = (B^T W0)^T [in, r] in one pass over W0, K_b = B^T B, then the column norm and c = m / n
+  CK(colreduce(cr_desc(out, in, r, W0, B, r, w.PU, w.splitsW), st));
+  CK(sum_splits<float>(w.PU, w.splitsW, in * r, U_save, nullptr, st));
+  CK(gram_weighted<bf16>(Bb, out, r, nullptr, w.Kb, st));
+  CK(dora_colnorm(in, r, c0, U_save, Ab, w.Kb, static_cast<const bf16*>(m), s, eps, n_save, w.c, w.Ac, st));
+  if (M == 0) return LORA_OK;
+  if (s != 0.f || Z_save) {
+    // one pass over X: Z = X (A diag(c))^T, s Z, and the scaled copy X diag(c) for the GEMM
+    RowProjDesc d = rp_desc(M, in, r, X, w.Ac, false);
+    d.out_a = static_cast<bf16*>(Z_save);
+    if (s != 0.f) {
+      d.out_b = w.Zs;
+      d.scale_b = s;
+      d.s_scale = w.c;
+      d.s_out = w.Xc;
+    }
+    CK(rowproj(d, st));
+  }
+  if (s == 0.f)  // strength 0: frozen base X W0^T + bias
+    CK(tc_gemm(fwd_desc(M, out, in, X, W0, nullptr, B, r, Y, static_cast<const bf16*>(bias), nullptr, w.err), st));
+  else
+    CK(tc_gemm(fwd_desc(M, out, in, w.Xc, W0, w.Zs, B, r, Y, static_cast<const bf16*>(bias), nullptr, w.err), st));
+  return LORA_OK;
+}
+
+lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, const void* A, const void* B,
+                          const void* m, const void* Z_saved, const float* n_saved, const float* U_saved,
+                          const void* dY, float s, float eps, void* dX, void* dA, void* dB, void* dm, void* dbias,
+                          void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  if (sh->dtype != LORA_BF16) return LORA_ERR_UNSUPPORTED;
+  REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQ(m); REQ(n_saved); REQ(U_saved); REQM(sh->M, dY);
+  REQ(dA); REQ(dB); REQ(dm);
+  ALN(X); ALN(W0); ALN(A); ALN(B); ALN(m); ALN(Z_saved); ALN(n_saved); ALN(U_saved); ALN(dY);
+  ALN(dX); ALN(dA); ALN(dB); ALN(dm); ALN(dbias);
+  if (!isfinite(s) || !isfinite(eps) || eps < 0.f) return LORA_ERR_INVALID_ARG;
+  DoraColsBwdWs w;
+  if ((e = check_ws(ws, ws_bytes, plan_dora_cols_bwd(*sh, nullptr, &w))) != LORA_OK) return e;
+  plan_dora_cols_bwd(*sh, static_cast<char*>(ws), &w);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
+  const int r = (int)sh->r;
+  const bf16* Ab = static_cast<const bf16*>(A);
+  const bf16* Bb = static_cast<const bf16*>(B);
+  const bf16* mb = static_cast<const bf16*>(m);
+  if (M == 0 || s == 0.f) {
+    CK(cudaMemsetAsync(dA, 0, (size_t)r * in * 2, st));
+    CK(cudaMemsetAsync(dB, 0, (size_t)out * r * 2, st));
+    CK(cudaMemsetAsync(dm, 0, (size_t)in * 2, st));
+    if (M == 0) {
+      if (dbias) CK(cudaMemsetAsync(dbias, 0, (size_t)out * 2, st));
+      return LORA_OK;
+    }
+    // strength 0: frozen base, dX = dY W0, dbias = colsum(dY)
+    if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, nullptr, A, r, dX, nullptr, w.err), st));
+    if (dbias) {
+      ColReduceDesc d = cr_desc(M, out, 8, dY, dY, out, w.PB, w.splitsB);
+      d.colsum = w.csump;
+      CK(colreduce(d, st));
+      CK(sum_splits<bf16>(w.csump, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
+    }
+    return LORA_OK;
+  }
+  CK(dora_c<bf16>(in, mb, n_saved, w.c, st));
+  const void* Z = Z_saved;
+  if (!Z) {
+    CK(scale_cols_bf16(Ab, r, in, w.c, w.Ac, st));
+    RowProjDesc d = rp_desc(M, in, r, X, w.Ac, false);
+    d.out_a = w.Zrec;
+    CK(rowproj(d, st));
+    Z = w.Zrec;
+  }
+  {  // dY^T Z partials and colsum(dY), one pass over dY
+    ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB);
+    d.colsum = dbias ? w.csump : nullptr;
+    CK(colreduce(d, st));
+  }
+  {  // G = s dY B
+    RowProjDesc d = rp_desc(M, out, r, dY, B, true);
+    d.out_b = w.Gs;
+    d.scale_b = s;
+    CK(rowproj(d, st));
+  }
+  // dX = (dY W0 + G A) diag(c): the column scale is the GEMM epilogue's
+  bf16* dXo = dX ? static_cast<bf16*>(dX) : w.dXt;
+  {
+    TcGemmDesc d = dx_desc(M, in, out, dY, W0, w.Gs, A, r, dXo, nullptr, w.err);
+    d.col_scale = w.c;
+    CK(tc_gemm(d, st));
+  }
+  {  // (X^T G) partials and colsum(X o dX) = c o colsum(X o dXt), one pass over X and dX
+    ColReduceDesc d = cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA);
+    d.Y = dXo;
+    d.ldy = in;
+    d.coldot = w.dotp;
+    CK(colreduce(d, st));
+  }
+  CK(sum_splits<float>(w.dotp, w.splitsA, in, w.dot, nullptr, st));
+  // dc = dot / c (no bias term), dm = dc / n, g = -m dc / (2 n^3)
+  CK(dora_dc<bf16>(in, w.dot, w.dot, nullptr, w.c, n_saved, mb, eps, w.g, static_cast<bf16*>(dm), nullptr, st));
+  CK(gram_weighted<bf16>(Bb, out, r, nullptr, w.Kb, st));
+  CK(gram_rows_weighted(Ab, r, in, w.g, w.Kga, st));
+  CK(scale_cols_bf16(Ab, r, in, w.g, w.Ag, st));
+  {  // W0 diag(g) A^T (fp32), one pass over W0
+    RowProjDesc d = rp_desc(out, in, r, W0, w.Ag, false);
+    d.out_f = w.Vg;
+    CK(rowproj(d, st));
+  }
+  Partial pa{w.PA, w.splitsA, r, 0}, pb{w.PB, w.splitsB, r, 0};
+  CK(finalize_dA_cols(r, in, pa, w.c, w.g, U_saved, w.Kb, Ab, s, static_cast<bf16*>(dA), st));
+  CK(finalize_dB<bf16>(out, r, pb, s, nullptr, nullptr, w.Vg, Bb, w.Kga, s, false, static_cast<bf16*>(dB), st));
+  if (dbias) CK(sum_splits<bf16>(w.csump, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
   return LORA_OK;
 }
 

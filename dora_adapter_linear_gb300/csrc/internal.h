@@ -92,6 +92,9 @@ struct RowProjDesc {
   int64_t ldo = 0;              // leading dimension of the outputs (0 -> R)
   int split_col = 1 << 30;      // columns >= split_col of out_b use scale_b_hi
   float scale_b_hi = 1.f;
+  // optional column-scaled copy of S written on the way: s_out[row, k] = bf16(S[row, k] * s_scale[k])
+  const float* s_scale = nullptr;
+  bf16* s_out = nullptr;        // [rows, K], leading dimension K
 };
 cudaError_t rowproj(const RowProjDesc& d, cudaStream_t st);
 
@@ -145,6 +148,7 @@ cudaError_t scale_rows(const T* B, int64_t rows, int r, const float* scale, floa
 // Final LoRA/DoRA gradient assembly from fp32 partials:
 //   dA[j, k] = sA * sum_s PA[s][k][j] + sW * sum_s PW[s][k][j] + s2 * sum_l Kg[j,l] A[l,k]
 //   dB[o, j] = sB * rs[o] * sum_s PB[s][o][j] + 2 s g[o] V[o,j] + 2 s^2 g[o] (B Kr)[o,j]
+//   (rs null: 1; V null: no norm terms; g null with V: g = 1)
 // Partials are laid out [splits][n][ldp] and read at columns j0 .. j0 + r - 1.
 struct Partial {
   const float* p = nullptr;
@@ -158,13 +162,23 @@ cudaError_t finalize_dA(int r, int64_t in, Partial PA, float sA, Partial PW, flo
 template <typename T>
 cudaError_t finalize_dB(int64_t out, int r, Partial PB, float sB, const float* rs, const float* g, const float* V,
                         const T* B, const float* Kr, float s, bool accumulate, T* dB, cudaStream_t st);
-// Kg = B^T diag(g) B  (fp32 [r, r])
+// Kg = B^T diag(g) B  (fp32 [r, r]; g null = all ones)
 template <typename T>
 cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float* Kg, cudaStream_t st);
 // rows of two matrices stacked: dst = [X1 ; X2] (rows1 + rows2, cols), same dtype
 cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int64_t rows2, int64_t cols, bf16* dst,
                              cudaStream_t st);
 cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st);
+// DoRA column variant (bf16): c0 = colsum(W^2); the closed-form column norm n, c = m / n and
+// A_c = A diag(c); out = A diag(w); K = A diag(w) A^T; and the dA assembly
+//   dA[j, k] = c[k] sum_s PA[s][k][j] + 2 s g[k] U[k, j] + 2 s^2 g[k] (Kb A)[j, k].
+cudaError_t colnorm2_bf16(const bf16* W, int64_t rows, int64_t cols, float* c0, cudaStream_t st);
+cudaError_t dora_colnorm(int64_t in, int r, const float* c0, const float* U, const bf16* A, const float* Kb,
+                         const bf16* m, float s, float eps, float* n_out, float* c, bf16* A_c, cudaStream_t st);
+cudaError_t scale_cols_bf16(const bf16* A, int r, int64_t in, const float* w, bf16* out, cudaStream_t st);
+cudaError_t gram_rows_weighted(const bf16* A, int r, int64_t cols, const float* w, float* K, cudaStream_t st);
+cudaError_t finalize_dA_cols(int r, int64_t in, Partial PA, const float* c, const float* g, const float* U,
+                             const float* Kb, const bf16* A, float s, bf16* dA, cudaStream_t st);
 // Operands of the fused-leaf (QKV) layer: A_stack = [A_0; ..; A_{L-1}] and B_blk = blockdiag(s_l B_l)
 // (row0[l] = first row of leaf l in the fused output, row0[0] = 0; in multiple of 8).
 constexpr int kMaxLeaves = 3;

@@ -87,6 +87,31 @@ __global__ void __launch_bounds__(128) rowproj_kernel(RowProjDesc d) {
     const int stage = kc % STAGES;
     const uint32_t sS = smem_u32(smem + stage * STAGE_BYTES);
     const uint32_t sU = sS + S_BYTES;
+    if (d.s_out) {
+      // column-scaled copy of this 32 x 128 tile of S: thread tid owns 16-byte chunk (tid & 15)
+      // of rows (tid >> 4) + 8 i
+      const int c16 = tid & 15;
+      const int64_t gk = (int64_t)kc * BKC + c16 * 8;
+      if (gk < d.K) {
+        const float4 lo = __ldg(reinterpret_cast<const float4*>(d.s_scale + gk));
+        const float4 hi = __ldg(reinterpret_cast<const float4*>(d.s_scale + gk + 4));
+        const float sc8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        const uint8_t* tile = smem + stage * STAGE_BYTES;
+#pragma unroll
+        for (int i = 0; i < BMR / 8; ++i) {
+          const int r = (tid >> 4) + 8 * i;
+          if (row0 + r >= d.rows) break;
+          uint4 v = *reinterpret_cast<const uint4*>(tile + (r * PITCH + c16 * 8) * 2);
+          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(w[e]);
+            w[e] = pack_bf16x2(f.x * sc8[2 * e], f.y * sc8[2 * e + 1]);
+          }
+          *reinterpret_cast<uint4*>(d.s_out + (row0 + r) * d.K + gk) = v;
+        }
+      }
+    }
 #pragma unroll
     for (int k2 = 0; k2 < BKC / 32; ++k2) {
       const int kk = kh * (BKC / 32) + k2;  // k16 step within the BKC-wide chunk

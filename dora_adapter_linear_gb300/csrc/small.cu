@@ -89,7 +89,8 @@ __global__ void gram_weighted_kernel(const T* B, int64_t out, int r, const float
   const int i = blockIdx.x / r, j = blockIdx.x % r;
   if (j < i) return;
   float acc = 0.f;
-  for (int64_t o = threadIdx.x; o < out; o += blockDim.x) acc = fmaf(g[o] * ldf(B, o * r + i), ldf(B, o * r + j), acc);
+  for (int64_t o = threadIdx.x; o < out; o += blockDim.x)
+    acc = fmaf((g ? g[o] : 1.f) * ldf(B, o * r + i), ldf(B, o * r + j), acc);
   acc = block_sum<256>(acc);
   if (threadIdx.x == 0) {
     Kg[i * r + j] = acc;
@@ -257,10 +258,11 @@ __global__ void finalize_dB_kernel(int64_t out, int r, Partial PB, float sB, con
     for (int sp = 0; sp < PB.splits; ++sp) t += PB.p[((int64_t)sp * out + o) * PB.ldp + PB.j0 + j];
   float a = sB * (rs ? rs[o] : 1.f) * t;
   if (accumulate) a += ldf(dB, i);
-  if (g) {
+  if (V) {  // norm terms; g == null: the weights are already inside V and Kr
+    const float go = g ? g[o] : 1.f;
     float bk = 0.f;
     for (int l = 0; l < r; ++l) bk = fmaf(ldf(B, o * r + l), Kr[l * r + j], bk);
-    a += 2.f * s * g[o] * V[o * r + j] + 2.f * s * s * g[o] * bk;
+    a += 2.f * s * go * V[o * r + j] + 2.f * s * s * go * bk;
   }
   dB[i] = from_f<T>(a);
 }
@@ -322,6 +324,124 @@ cudaError_t pack_leaves(const LeafPack& p, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   const int64_t blocks = (n + 255) / 256;
   pack_leaves_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ DoRA column variant (bf16)
+// c0[k] = sum_o W[o, k]^2: 32 columns per block, 8 row phases reduced through shared memory
+__global__ void colnorm2_kernel(const bf16* W, int64_t rows, int64_t cols, float* c0) {
+  __shared__ float red[8][33];
+  const int64_t k = (int64_t)blockIdx.x * 32 + threadIdx.x;
+  float acc = 0.f;
+  if (k < cols)
+    for (int64_t o = threadIdx.y; o < rows; o += 8) {
+      const float f = __bfloat162float(W[o * cols + k]);
+      acc = fmaf(f, f, acc);
+    }
+  red[threadIdx.y][threadIdx.x] = acc;
+  __syncthreads();
+  if (threadIdx.y == 0 && k < cols) {
+    float t = 0.f;
+    for (int y = 0; y < 8; ++y) t += red[y][threadIdx.x];
+    c0[k] = t;
+  }
+}
+cudaError_t colnorm2_bf16(const bf16* W, int64_t rows, int64_t cols, float* c0, cudaStream_t st) {
+  if (cols <= 0) return cudaSuccess;
+  colnorm2_kernel<<<(unsigned)((cols + 31) / 32), dim3(32, 8), 0, st>>>(W, rows, cols, c0);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// closed-form column norm, one thread per input column k:
+//   q = c0[k] + 2s sum_j A[j,k] U[k,j] + s^2 sum_j A[j,k] (Kb A)[j,k],  n = max(sqrt(max(q, 0)), eps),
+//   c = m / n, and (optionally) A_c[:, k] = bf16(A[:, k] c[k]).
+__global__ void dora_colnorm_kernel(int64_t in, int r, const float* c0, const float* U, const bf16* A,
+                                    const float* Kb, const bf16* m, float s, float eps, float* n_out, float* c,
+                                    bf16* A_c) {
+  extern __shared__ float sK[];
+  for (int i = threadIdx.x; i < r * r; i += blockDim.x) sK[i] = Kb[i];
+  __syncthreads();
+  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= in) return;
+  float a[64];
+  for (int j = 0; j < r; ++j) a[j] = __bfloat162float(A[(int64_t)j * in + k]);
+  float t1 = 0.f, t2 = 0.f;
+  for (int j = 0; j < r; ++j) {
+    t1 = fmaf(a[j], U[k * r + j], t1);
+    float ka = 0.f;
+    for (int l = 0; l < r; ++l) ka = fmaf(sK[j * r + l], a[l], ka);
+    t2 = fmaf(a[j], ka, t2);
+  }
+  const float q = c0[k] + 2.f * s * t1 + s * s * t2;
+  const float n = fmaxf(sqrtf(fmaxf(q, 0.f)), eps);
+  const float cc = __bfloat162float(m[k]) / n;
+  n_out[k] = n;
+  c[k] = cc;
+  if (A_c)
+    for (int j = 0; j < r; ++j) A_c[(int64_t)j * in + k] = __float2bfloat16_rn(a[j] * cc);
+}
+cudaError_t dora_colnorm(int64_t in, int r, const float* c0, const float* U, const bf16* A, const float* Kb,
+                         const bf16* m, float s, float eps, float* n_out, float* c, bf16* A_c, cudaStream_t st) {
+  if (in <= 0) return cudaSuccess;
+  dora_colnorm_kernel<<<(unsigned)((in + 127) / 128), 128, r * r * sizeof(float), st>>>(in, r, c0, U, A, Kb, m, s,
+                                                                                        eps, n_out, c, A_c);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// out[j, k] = bf16(A[j, k] * w[k])  (A [r, in])
+__global__ void scale_cols_kernel(const bf16* A, int r, int64_t in, const float* w, bf16* out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)r * in) return;
+  out[i] = __float2bfloat16_rn(__bfloat162float(A[i]) * w[i % in]);
+}
+cudaError_t scale_cols_bf16(const bf16* A, int r, int64_t in, const float* w, bf16* out, cudaStream_t st) {
+  const int64_t n = (int64_t)r * in;
+  if (n <= 0) return cudaSuccess;
+  scale_cols_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(A, r, in, w, out);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// K = A diag(w) A^T (fp32 [r, r]), one block per (i, j >= i)
+__global__ void gram_rows_weighted_kernel(const bf16* A, int r, int64_t cols, const float* w, float* K) {
+  const int i = blockIdx.x / r, j = blockIdx.x % r;
+  if (j < i) return;
+  float acc = 0.f;
+  for (int64_t k = threadIdx.x; k < cols; k += blockDim.x)
+    acc = fmaf(w[k] * __bfloat162float(A[i * cols + k]), __bfloat162float(A[j * cols + k]), acc);
+  acc = block_sum<256>(acc);
+  if (threadIdx.x == 0) {
+    K[i * r + j] = acc;
+    K[j * r + i] = acc;
+  }
+}
+cudaError_t gram_rows_weighted(const bf16* A, int r, int64_t cols, const float* w, float* K, cudaStream_t st) {
+  gram_rows_weighted_kernel<<<r * r, 256, 0, st>>>(A, r, cols, w, K);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// dA[j, k] = c[k] sum_s PA[s][k][j] + 2 s g[k] U[k, j] + 2 s^2 g[k] (Kb A)[j, k]
+__global__ void finalize_dA_cols_kernel(int r, int64_t in, Partial PA, const float* c, const float* g,
+                                        const float* U, const float* Kb, const bf16* A, float s, bf16* dA) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)r * in) return;
+  const int j = (int)(i / in);
+  const int64_t k = i - (int64_t)j * in;
+  float t = 0.f;
+  for (int sp = 0; sp < PA.splits; ++sp) t += PA.p[((int64_t)sp * in + k) * PA.ldp + PA.j0 + j];
+  float ka = 0.f;
+  for (int l = 0; l < r; ++l) ka = fmaf(Kb[j * r + l], __bfloat162float(A[(int64_t)l * in + k]), ka);
+  dA[i] = __float2bfloat16_rn(c[k] * t + 2.f * s * g[k] * U[k * r + j] + 2.f * s * s * g[k] * ka);
+}
+cudaError_t finalize_dA_cols(int r, int64_t in, Partial PA, const float* c, const float* g, const float* U,
+                             const float* Kb, const bf16* A, float s, bf16* dA, cudaStream_t st) {
+  const int64_t n = (int64_t)r * in;
+  if (n <= 0) return cudaSuccess;
+  finalize_dA_cols_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(r, in, PA, c, g, U, Kb, A, s, dA);
   count_launch();
   return cudaGetLastError();
 }

@@ -74,6 +74,38 @@ def dora_linear_bwd(X, W0, A, B, m, bias, Y, Z, n, V, dY, s, eps=1e-12, need_dx=
     return dX, dA, dB, dm, dbias
 
 
+def dora_colnorm2(W0):
+    sh = L.shape(0, W0.shape[1], W0.shape[0], 8, L.dtype_code(W0))
+    c0 = torch.empty(W0.shape[1], dtype=torch.float32, device=W0.device)
+    L.dora_colnorm2(sh, W0, c0)
+    return c0
+
+
+def dora_cols_fwd(X, W0, A, B, m, c0, s, eps=1e-12, bias=None, save_z=True):
+    """m, c0: [d_in].  Returns Y, Z, n [d_in], U [d_in, r] (the last three saved for the backward)."""
+    sh = _shape_of(X, W0, A)
+    dev = X.device
+    Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=dev)
+    Z = torch.empty(X.shape[0], A.shape[0], dtype=X.dtype, device=dev) if save_z else None
+    n = torch.empty(W0.shape[1], dtype=torch.float32, device=dev)
+    U = torch.empty(W0.shape[1], A.shape[0], dtype=torch.float32, device=dev)
+    ws = workspace(L.lora_workspace_bytes(L.OP_DORA_COLS_FWD, sh), dev)
+    L.dora_cols_fwd(sh, X, W0, A, B, m, bias, c0, s, eps, Y, Z, n, U, ws)
+    return Y, Z, n, U
+
+
+def dora_cols_bwd(X, W0, A, B, m, Z, n, U, dY, s, eps=1e-12, need_dx=True, need_dbias=False):
+    sh = _shape_of(X, W0, A)
+    dX = torch.empty_like(X) if need_dx else None
+    dA = torch.empty_like(A)
+    dB = torch.empty_like(B)
+    dm = torch.empty_like(m)
+    dbias = torch.empty(W0.shape[0], dtype=X.dtype, device=X.device) if need_dbias else None
+    ws = workspace(L.lora_workspace_bytes(L.OP_DORA_COLS_BWD, sh), X.device)
+    L.dora_cols_bwd(sh, X, W0, A, B, m, Z, n, U, dY, s, eps, dX, dA, dB, dm, dbias, ws)
+    return dX, dA, dB, dm, dbias
+
+
 def lora_mlp_swiglu_fwd(X, g, u, d, act=0):
     """g, u, d: dicts with W, A, B, s; act 0 SwiGLU, 1 GeGLU.  Returns (Y, saved) where saved
     holds e, u, h, Zgu, Zd."""

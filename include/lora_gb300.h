@@ -2,9 +2,10 @@
  * lora_gb300.h -- C ABI of the fused low-rank-adapted linear layer for GB300 (sm_103a).
  *
  * The layer:  y = X W0^T + s (X A^T) B^T (+ bias)   forward and backward, computed
- * without ever forming the dense update dW = B A or its gradient; the DoRA row-scale
- * variant with its closed-form norm; a SwiGLU MLP built from three such projections;
- * and an int8 (W8A8) base weight with a per-row dequant scale and a LoRA epilogue.
+ * without ever forming the dense update dW = B A or its gradient; the DoRA row-scale and
+ * column-scale variants with their closed-form norms; a gated (SwiGLU / GeGLU) MLP built from
+ * three such projections; a fused query/key/value projection with one adapter per leaf; and an
+ * int8 (W8A8) base weight with a per-row dequant scale and a LoRA epilogue.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -61,7 +62,8 @@ typedef enum {
     LORA_OP_LINEAR_FWD = 0, LORA_OP_LINEAR_BWD = 1,
     LORA_OP_DORA_FWD = 2, LORA_OP_DORA_BWD = 3,
     LORA_OP_MLP_FWD = 4, LORA_OP_MLP_BWD = 5,
-    LORA_OP_QKV_FWD = 6, LORA_OP_QKV_BWD = 7
+    LORA_OP_QKV_FWD = 6, LORA_OP_QKV_BWD = 7,
+    LORA_OP_DORA_COLS_FWD = 8, LORA_OP_DORA_COLS_BWD = 9
 } lora_op;
 
 typedef struct {
@@ -115,7 +117,8 @@ const char* lora_status_string(int status);
 /* Library ABI version (increments on any signature change). */
 int lora_abi_version(void);
 
-/* Bytes of workspace `op` needs for `sh` (LORA_OP_LINEAR_* and LORA_OP_DORA_*). 0 on bad input. */
+/* Bytes of workspace `op` needs for `sh` (LORA_OP_LINEAR_*, LORA_OP_DORA_* and
+ * LORA_OP_DORA_COLS_*). 0 on bad input. */
 size_t lora_workspace_bytes(int op, const lora_shape* sh);
 
 /* Bytes of workspace the MLP entry points need (op = LORA_OP_MLP_FWD / LORA_OP_MLP_BWD). */
@@ -220,6 +223,45 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
                             const void* dY, float s, float eps,
                             void* dX, void* dA, void* dB, void* dm, void* dbias,
                             void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- DoRA (cols)
+ * The column variant: the norm is taken per INPUT column of the adapted weight W' = W0 + s B A,
+ * n[k] = max(||W'[:, k]||, eps), and the decomposed weight is W' diag(m / n) with m [d_in].
+ * "LoRA/DoRA fast forward ...", What section (lora / dora-rows / dora-cols need no materialised
+ * weight) and commit message (the row/col norm from the closed-form norm^2 expansion).
+ *
+ * c0[k] = sum_o W0[o,k]^2 in fp32: the cached per-layer constant.  c0: [d_in] fp32 output.
+ * LORA_BF16 only.
+ */
+lora_status dora_colnorm2(const lora_shape* sh, const void* W0, float* c0, void* stream);
+
+/* Forward:  q[k] = c0[k] + 2s colsum(A o (B^T W0))[k] + s^2 colsum(A o ((B^T B) A))[k],
+ *   n = max(sqrt(max(q, 0)), eps),  c = m / n  (an input-column scale),
+ *   Y = (X diag(c)) W0^T + s ((X diag(c)) A^T) B^T + bias.
+ * Same pages and sections as dora_colnorm2; strength 0 returns X W0^T + bias.
+ *   m [d_in] (bf16, nonzero), bias [d_out] or NULL, c0 [d_in] fp32 from dora_colnorm2.
+ *   Y [M, d_out]; Z_save [M, r] = (X diag(c)) A^T or NULL; n_save [d_in] fp32 (required);
+ *   U_save [d_in, r] fp32 (required): (B^T W0)^T, reused by the backward's norm gradient.
+ */
+lora_status dora_cols_fwd(const lora_shape* sh, const void* X, const void* W0, const void* A,
+                          const void* B, const void* m, const void* bias, const float* c0,
+                          float s, float eps, void* Y, void* Z_save, float* n_save, float* U_save,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of dora_cols_fwd, the norm kept in the graph:
+ *   G = s dY B;  dXt = dY W0 + G A (the gradient of X diag(c));  dX = dXt diag(c);
+ *   dc = colsum(X o dXt);  dm = dc / n;  g = -m dc / (2 n^3) (0 where n was clamped at eps);
+ *   dA = (G^T X) diag(c) + 2s U^T diag(g) + 2s^2 (B^T B) A diag(g);
+ *   dB = s dY^T Z + 2s W0 diag(g) A^T + 2s^2 B (A diag(g) A^T);  dbias = colsum(dY).
+ * Same pages as dora_colnorm2 and the Fidelity section of "LoRA/DoRA fast forward ..." (norm in
+ * the autograd graph).  Z_saved, n_saved, U_saved from the forward (Z_saved may be NULL).
+ *   dX [M, d_in] or NULL; dA [r, d_in]; dB [d_out, r]; dm [d_in]; dbias [d_out] or NULL.
+ */
+lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, const void* A,
+                          const void* B, const void* m, const void* Z_saved, const float* n_saved,
+                          const float* U_saved, const void* dY, float s, float eps,
+                          void* dX, void* dA, void* dB, void* dm, void* dbias,
+                          void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- LoRA gated MLP (SwiGLU / GeGLU)
  * e = X Wg^T + sg (X Ag^T) Bg^T,  u = X Wu^T + su (X Au^T) Bu^T,  h = act(e) * u,

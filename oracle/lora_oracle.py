@@ -26,7 +26,8 @@ from scipy.special import erf as _erf
 
 __all__ = [
     "f64", "adapted_weight", "lora_linear_fwd", "lora_linear_bwd", "dora_rownorm2",
-    "dora_linear_fwd", "dora_linear_bwd", "silu", "dsilu", "gelu", "dgelu", "mlp_swiglu_fwd", "mlp_swiglu_bwd",
+    "dora_linear_fwd", "dora_linear_bwd", "dora_colnorm2", "dora_cols_fwd", "dora_cols_bwd",
+    "dora_cols_fwd_rows", "dora_cols_bwd_sampled", "silu", "dsilu", "gelu", "dgelu", "mlp_swiglu_fwd", "mlp_swiglu_bwd",
     "quantize_rows", "int8_accumulate", "w8a8_lora_fwd", "w8a8_dequant_weight", "w8a8_lora_bwd",
     "qkv_adapted_weight", "qkv_lora_fwd", "qkv_lora_bwd", "qkv_fwd_rows", "qkv_bwd_sampled",
     "lora_fwd_rows", "lora_bwd_sampled", "dora_fwd_rows", "dora_bwd_sampled", "dora_bwd_rows_sampled",
@@ -200,6 +201,62 @@ def dora_linear_bwd(X, W0, A, B, m, s, dY, eps=1e-12):
     dB = s * (dWp @ A.T)
     dbias = dY.sum(axis=0)
     return dX, dA, dB, dm, dbias
+
+
+# ----------------------------------------------------------------------------- DoRA (cols)
+def dora_colnorm2(W0):
+    """colsum(W0^2): the cached constant of the column variant's closed-form norm.
+
+    "LoRA/DoRA fast forward ...", commit message (row/col norm from the closed-form
+    norm^2 expansion with a cached constant).
+    """
+    return (W0 * W0).sum(axis=0)
+
+
+def dora_cols_fwd(X, W0, A, B, m, s, eps=1e-12, bias=None):
+    """DoRA cols: y = X (W' diag(m / n))^T + bias, n[k] = max(||W'[:, k]||_2, eps), m [in].
+
+    "LoRA/DoRA fast forward ...", What section (dora-cols, like dora-rows, needs no
+    materialised weight) and Fidelity section (in-graph norm, 1e-12 eps, un-scaled
+    bias, strength 0 = frozen base).  The norm is taken explicitly, column by column,
+    on the materialised W'.  Returns (y, n).
+    """
+    Wp = adapted_weight(W0, A, B, s)
+    n = np.maximum(np.sqrt((Wp * Wp).sum(axis=0)), eps)
+    if s == 0:
+        Y = X @ W0.T
+        return (Y if bias is None else Y + bias[None, :]), n
+    Y = X @ (Wp * (m / n)[None, :]).T
+    if bias is not None:
+        Y = Y + bias[None, :]
+    return Y, n
+
+
+def dora_cols_bwd(X, W0, A, B, m, s, dY, eps=1e-12):
+    """Gradients of DoRA cols w.r.t. X, A, B, m and bias, norm kept in the graph.
+
+    Weight-space chain rule with Wd = W' diag(c), c = m / n:
+      dWd = dY^T X,  t_k = <dWd[:, k], W'[:, k]>,  dm = t / n,
+      dW' = dWd diag(c) - W' diag(t m / (n^2 nraw))   (second term 0 where n was clamped),
+      dA = s B^T dW',  dB = s dW' A^T,  dX = dY Wd,  dbias = colsum(dY).
+    Strength 0: the frozen base (dX = dY W0, dA = dB = dm = 0).
+    """
+    if s == 0:
+        z = np.zeros
+        return dY @ W0, z(A.shape), z(B.shape), z(m.shape), dY.sum(axis=0)
+    Wp = adapted_weight(W0, A, B, s)
+    nraw = np.sqrt((Wp * Wp).sum(axis=0))
+    n = np.maximum(nraw, eps)
+    c = m / n
+    Wd = Wp * c[None, :]
+    dX = dY @ Wd
+    dWd = dY.T @ X
+    t = (dWd * Wp).sum(axis=0)
+    dm = t / n
+    live = nraw > eps
+    coef = np.where(live, (-t * m / (n * n)) / np.where(live, nraw, 1.0), 0.0)
+    dWp = dWd * c[None, :] + Wp * coef[None, :]
+    return dX, s * (B.T @ dWp), s * (dWp @ A.T), dm, dY.sum(axis=0)
 
 
 # ----------------------------------------------------------------------------- SwiGLU MLP
@@ -378,6 +435,33 @@ def qkv_bwd_sampled(X, W0, leaves, dY, rows, in_cols, out_rows):
         dB.append(s * ((dYl[:, orows].T @ X) @ A.T))
         row += n
     return dX, dA, dB
+
+
+def dora_cols_fwd_rows(X, W0, A, B, m, s, rows, eps=1e-12, bias=None):
+    """Rows `rows` of the DoRA-cols output, plus the full column-norm vector n."""
+    return dora_cols_fwd(X[rows], W0, A, B, m, s, eps, bias)
+
+
+def dora_cols_bwd_sampled(X, W0, A, B, m, s, dY, rows, in_cols, eps=1e-12):
+    """Sampled DoRA-cols gradients: dX[rows], dA[:, in_cols], dm[in_cols].
+
+    Column k of the weight-space gradient needs only column k of dWd = dY^T X:
+    dWd[:, k] = dY^T X[:, k], t_k = <dWd[:, k], W'[:, k]>, and dW'[:, k] follows
+    as in dora_cols_bwd; dA[:, k] = s B^T dW'[:, k].
+    """
+    Wp = adapted_weight(W0, A, B, s)
+    nraw = np.sqrt((Wp * Wp).sum(axis=0))
+    n = np.maximum(nraw, eps)
+    c = m / n
+    dX = dY[rows] @ (Wp * c[None, :])
+    Wk = Wp[:, in_cols]
+    dWd_k = dY.T @ X[:, in_cols]
+    t = (dWd_k * Wk).sum(axis=0)
+    nk, rk, mk, ck = n[in_cols], nraw[in_cols], m[in_cols], c[in_cols]
+    live = rk > eps
+    coef = np.where(live, (-t * mk / (nk * nk)) / np.where(live, rk, 1.0), 0.0)
+    dWp_k = dWd_k * ck[None, :] + Wk * coef[None, :]
+    return dX, s * (B.T @ dWp_k), t / nk
 
 
 def dora_fwd_rows(X, W0, A, B, m, s, rows, eps=1e-12, bias=None):

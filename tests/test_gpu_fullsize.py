@@ -137,6 +137,28 @@ def test_full_dora_4096x11008(ops):
     assert torch.isfinite(dA.float()).all()
 
 
+def test_full_dora_cols(ops):
+    case = D.WORKLOADS["dora_cols_4096x11008_bf16"]
+    t = D.make_linear(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    c0 = ops.dora_colnorm2(g["W0"])
+    Y, Z, n, U = ops.dora_cols_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], c0, case.s, case.eps, g["bias"])
+    dX, dA, dB, dm, _ = ops.dora_cols_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], Z, n, U, g["dY"], case.s,
+                                          case.eps)
+    torch.cuda.synchronize()
+    ws_clear(ops)
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    ry, rn = O.dora_cols_fwd_rows(X, W0, A, B, m, case.s, ROWS, case.eps, bias)
+    assert_close(Y[ROWS], ry, "bf16", "Y rows")
+    np.testing.assert_allclose(to64(n), rn, rtol=1e-4)
+    cols = [0, 1, 63, 64, 2047, 4095]
+    sX, sA, sm = O.dora_cols_bwd_sampled(X, W0, A, B, m, case.s, dY, ROWS, cols, case.eps)
+    assert_close(dX[ROWS], sX, "bf16", "dX rows")
+    assert_close(dA[:, cols].T, sA.T, "bf16", "dA columns")
+    assert_close(dm[cols][None], sm[None], "bf16", "dm entries")
+    assert torch.isfinite(dB.float()).all()
+
+
 def test_full_mlp_swiglu(ops):
     case = D.WORKLOADS["mlp_swiglu_4096x14336_bf16"]
     t = D.make_mlp(case)

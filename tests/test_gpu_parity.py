@@ -172,6 +172,43 @@ def test_dora_strength0_is_frozen_base_bits(ops):
     assert torch.equal(Yd, Yl)
 
 
+# ---------------------------------------------------------------------------- DoRA (cols)
+@pytest.mark.parametrize("r", [32, 16])
+def test_dora_cols_fwd_bwd(ops, r):
+    case, t, g = lin_inputs("dora_cols_4096x11008_bf16", M=300, d_in=328, d_out=520, r=r)
+    c0 = ops.dora_colnorm2(g["W0"])
+    np.testing.assert_allclose(to64(c0), O.dora_colnorm2(f64(t["W0"])), rtol=1e-5)
+    Y, Z, n, U = ops.dora_cols_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], c0, case.s, case.eps, g["bias"])
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    rY, rn = O.dora_cols_fwd(X, W0, A, B, m, case.s, case.eps, bias)
+    assert_close(Y, rY, "bf16", "Y")
+    np.testing.assert_allclose(to64(n), rn, rtol=1e-4)
+    np.testing.assert_allclose(to64(U), (B.T @ W0).T, rtol=1e-4, atol=1e-5)
+    dX, dA, dB, dm, dbias = ops.dora_cols_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], Z, n, U, g["dY"], case.s,
+                                              case.eps, need_dbias=True)
+    rX, rA, rB, rm, rb = O.dora_cols_bwd(X, W0, A, B, m, case.s, dY, case.eps)
+    for got, ref, nm in ((dX, rX, "dX"), (dA, rA, "dA"), (dB, rB, "dB"), (dm, rm[None], "dm"),
+                         (dbias, rb[None], "dbias")):
+        assert_close(got, ref, "bf16", nm)
+    # without dX and without the saved Z: same adapter gradients, bit for bit
+    _, dA2, dB2, dm2, _ = ops.dora_cols_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], None, n, U, g["dY"], case.s,
+                                            case.eps, need_dx=False)
+    assert torch.equal(dA, dA2) and torch.equal(dB, dB2) and torch.equal(dm, dm2)
+
+
+def test_dora_cols_init_and_strength0(ops):
+    case, t, g = lin_inputs("dora_cols_4096x11008_bf16", M=256, d_in=264, d_out=256, r=16)
+    c0 = ops.dora_colnorm2(g["W0"])
+    Yl, _ = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], 0.0, g["bias"])
+    Y0, *_ = ops.dora_cols_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], c0, 0.0, case.eps, g["bias"])
+    assert torch.equal(Y0, Yl)   # strength 0: the frozen base, bit for bit
+    g["B"].zero_()
+    m0 = torch.sqrt(c0).to(torch.bfloat16)
+    Yi, *_ = ops.dora_cols_fwd(g["X"], g["W0"], g["A"], g["B"], m0, c0, case.s, case.eps, g["bias"])
+    X, W0, bias = f64(t["X"]), f64(t["W0"]), f64(t["bias"])
+    assert_close(Yi, X @ W0.T + bias, "bf16", "Y at init")
+
+
 # ---------------------------------------------------------------------------- SwiGLU MLP
 def mlp_inputs(**kw):
     case = D.scaled(D.WORKLOADS["mlp_swiglu_4096x14336_bf16"], **kw)

@@ -212,6 +212,100 @@ def test_dora_grads_match_library_autograd():
         assert rel(g_, t[k].grad.numpy()) < 1e-12
 
 
+# ------------------------------------------------------------------ DoRA (cols)
+def cols_case(M=5, d_in=7, d_out=6, r=3, seed=40):
+    X, W0, A, B, bias, _, dY = rand_case(M, d_in, d_out, r, seed)
+    m = np.sqrt((W0 * W0).sum(0)) * rng(seed + 100).uniform(0.9, 1.1, d_in)
+    return X, W0, A, B, bias, m, dY
+
+
+def test_dora_cols_closed_form_norm_equals_explicit():
+    """||W0 + sBA||^2_col = colsum(W0^2) + 2s colsum(A o (B^T W0)) + s^2 colsum(A o ((B^T B) A))."""
+    _, W0, A, B, _, m, _ = cols_case(d_in=30, d_out=50, r=4, seed=41)
+    s = 0.9
+    q = O.dora_colnorm2(W0) + 2 * s * (A * (B.T @ W0)).sum(0) + s * s * (A * ((B.T @ B) @ A)).sum(0)
+    _, n = O.dora_cols_fwd(np.zeros((1, 30)), W0, A, B, m, s)
+    assert rel(np.sqrt(q), n) < 1e-13
+
+
+def test_dora_colnorm2_explicit_loop():
+    W0 = rng(42).standard_normal((5, 9))
+    want = [sum(W0[o, k] ** 2 for o in range(5)) for k in range(9)]
+    np.testing.assert_allclose(O.dora_colnorm2(W0), want, rtol=1e-15)
+
+
+def test_dora_cols_is_transpose_of_rows_variant():
+    """The column variant of (W0, A, B) is the row variant of the transposed problem
+    (W0^T, B^T as the down factor, A^T as the up factor): feeding identity inputs
+    returns each decomposed weight, and the two must be transposes of each other."""
+    _, W0, A, B, _, m, _ = cols_case(d_in=8, d_out=11, r=3, seed=43)
+    s = 1.3
+    Wc, nc = O.dora_cols_fwd(np.eye(8), W0, A, B, m, s)          # = (W' diag(c))^T
+    Wr, nr = O.dora_linear_fwd(np.eye(11), W0.T, B.T, A.T, m, s)  # = (diag(c) W'^T)^T
+    assert rel(nc, nr) < 1e-14
+    assert rel(Wc.T, Wr) < 1e-14
+
+
+def test_dora_cols_at_init_is_plain_linear():
+    X, W0, A, B, bias, _, _ = cols_case(seed=44)
+    m = np.linalg.norm(W0, axis=0)
+    y, _ = O.dora_cols_fwd(X, W0, A, np.zeros_like(B), m, 1.5, 1e-12, bias)
+    ref = torch.nn.functional.linear(torch.from_numpy(X), torch.from_numpy(W0), torch.from_numpy(bias)).numpy()
+    assert rel(y, ref) < 1e-14
+
+
+def test_dora_cols_is_input_scale_of_lora():
+    """DoRA cols = the LoRA layer applied to X diag(m / n)."""
+    X, W0, A, B, bias, m, _ = cols_case(seed=45)
+    s = 0.8
+    y, n = O.dora_cols_fwd(X, W0, A, B, m, s, 1e-12, bias)
+    assert rel(y, O.lora_linear_fwd(X * (m / n)[None, :], W0, A, B, s, bias)) < 1e-14
+
+
+def test_dora_cols_direction_scale_invariance_and_strength_zero():
+    X, W0, A, B, bias, m, dY = cols_case(seed=46)
+    y1, _ = O.dora_cols_fwd(X, W0, A, B, m, 1.1, 1e-12, bias)
+    y2, _ = O.dora_cols_fwd(X, 2.5 * W0, A, 2.5 * B, m, 1.1, 1e-12, bias)
+    assert rel(y2, y1) < 1e-14
+    y0, _ = O.dora_cols_fwd(X, W0, A, B, m, 0.0, 1e-12, bias)
+    assert np.array_equal(y0, X @ W0.T + bias)
+    dX, dA, dB, dm, _ = O.dora_cols_bwd(X, W0, A, B, m, 0.0, dY)
+    assert np.array_equal(dX, dY @ W0) and not dA.any() and not dB.any() and not dm.any()
+
+
+def test_dora_cols_grads_finite_difference():
+    X, W0, A, B, bias, m, dY = cols_case(M=4, d_in=6, d_out=8, r=2, seed=47)
+    s = 1.2
+    L = lambda: float((dY * O.dora_cols_fwd(X, W0, A, B, m, s, 1e-12, bias)[0]).sum())  # noqa: E731
+    dX, dA, dB, dm, db = O.dora_cols_bwd(X, W0, A, B, m, s, dY)
+    for got, x in ((dX, X), (dA, A), (dB, B), (dm, m), (db, bias)):
+        assert rel(got, _fd_grad(L, x)) < 1e-7
+
+
+def test_dora_cols_grads_match_library_autograd():
+    X, W0, A, B, bias, m, dY = cols_case(M=9, d_in=12, d_out=10, r=3, seed=48)
+    s = 0.7
+    t = {k: torch.tensor(v, requires_grad=True) for k, v in dict(X=X, A=A, B=B, m=m, bias=bias).items()}
+    Wp = torch.tensor(W0) + s * t["B"] @ t["A"]
+    n = torch.linalg.vector_norm(Wp, dim=0).clamp_min(1e-12)
+    y = torch.nn.functional.linear(t["X"], Wp * (t["m"] / n)[None, :], t["bias"])
+    y.backward(torch.tensor(dY))
+    got = O.dora_cols_bwd(X, W0, A, B, m, s, dY)
+    for g_, k in zip(got, ("X", "A", "B", "m", "bias")):
+        assert rel(g_, t[k].grad.numpy()) < 1e-12, k
+
+
+def test_dora_cols_sampled_forms_match_full():
+    X, W0, A, B, bias, m, dY = cols_case(M=9, d_in=12, d_out=10, r=3, seed=49)
+    s = 0.9
+    y, n = O.dora_cols_fwd(X, W0, A, B, m, s, 1e-12, bias)
+    yr, nr = O.dora_cols_fwd_rows(X, W0, A, B, m, s, [1, 6], 1e-12, bias)
+    assert rel(yr, y[[1, 6]]) < 1e-14 and rel(nr, n) == 0
+    dX, dA, _, dm, _ = O.dora_cols_bwd(X, W0, A, B, m, s, dY)
+    sX, sA, sm = O.dora_cols_bwd_sampled(X, W0, A, B, m, s, dY, [0, 8], [2, 3, 11])
+    assert rel(sX, dX[[0, 8]]) < 1e-13 and rel(sA, dA[:, [2, 3, 11]]) < 1e-13 and rel(sm, dm[[2, 3, 11]]) < 1e-13
+
+
 # ------------------------------------------------------------------ SwiGLU MLP
 def mlp_case(M=4, H=6, I=8, r=2, seed=14):
     g = rng(seed)
