@@ -383,7 +383,7 @@ TcGemmDesc dx_desc(int64_t M, int64_t N /*in*/, int64_t K /*out*/, const void* d
   return d;
 }
 
-RowProjDesc rp_desc(int64_t rows, int64_t K, int R, const void* S, const void* U, bool kr) {
+RowProjDesc rp_desc(int64_t rows, int64_t K, int R, const void* S, const void* U, bool kr, uint32_t* err) {
   RowProjDesc d;
   d.rows = rows;
   d.K = K;
@@ -393,11 +393,13 @@ RowProjDesc rp_desc(int64_t rows, int64_t K, int R, const void* S, const void* U
   d.U = static_cast<const bf16*>(U);
   d.u_kr = kr;
   d.ldu = kr ? R : K;
+  d.err = err;
+  d.timeout_ns = wait_timeout_ns();
   return d;
 }
 
 ColReduceDesc cr_desc(int64_t rows, int64_t K, int R, const void* S, const void* T, int64_t ldt, float* part,
-                      int splits) {
+                      int splits, uint32_t* err) {
   ColReduceDesc d;
   d.rows = rows;
   d.K = K;
@@ -408,6 +410,8 @@ ColReduceDesc cr_desc(int64_t rows, int64_t K, int R, const void* S, const void*
   d.ldt = ldt;
   d.part = part;
   d.splits = splits;
+  d.err = err;
+  d.timeout_ns = wait_timeout_ns();
   return d;
 }
 
@@ -558,7 +562,7 @@ lora_status lora_linear_fwd(const lora_shape* sh, const void* X, const void* W0,
   const int r = (int)sh->r;
   if (sh->dtype == LORA_BF16) {
     if (s != 0.f || Z_save) {
-      RowProjDesc d = rp_desc(M, in, r, X, A, false);
+      RowProjDesc d = rp_desc(M, in, r, X, A, false, w.err);
       d.out_a = static_cast<bf16*>(Z_save);
       d.out_b = s != 0.f ? static_cast<bf16*>(w.Zs) : nullptr;
       d.scale_b = s;
@@ -606,7 +610,7 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     if (s == 0.f) {
       if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, nullptr, A, r, dX, nullptr, w.err), st));
       if (dbias) {
-        ColReduceDesc d = cr_desc(M, out, 8, dY, dY, out, w.PB, w.splitsB);  // T unused beyond 8 cols
+        ColReduceDesc d = cr_desc(M, out, 8, dY, dY, out, w.PB, w.splitsB, w.err);  // T unused beyond 8 cols
         d.colsum = w.csum;
         CK(colreduce(d, st));
         CK(sum_splits<bf16>(w.csum, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
@@ -615,24 +619,24 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     }
     const void* Z = Z_saved;
     if (!Z) {
-      RowProjDesc d = rp_desc(M, in, r, X, A, false);
+      RowProjDesc d = rp_desc(M, in, r, X, A, false, w.err);
       d.out_a = static_cast<bf16*>(w.Zrec);
       CK(rowproj(d, st));
       Z = w.Zrec;
     }
     {  // dB partials (dY^T Z) and column sums of dY, one pass over dY
-      ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB);
+      ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
       d.colsum = dbias ? w.csum : nullptr;
       CK(colreduce(d, st));
     }
     {  // s*G = s * dY B
-      RowProjDesc d = rp_desc(M, out, r, dY, B, true);
+      RowProjDesc d = rp_desc(M, out, r, dY, B, true, w.err);
       d.out_b = static_cast<bf16*>(w.Gs);
       d.scale_b = s;
       CK(rowproj(d, st));
     }
     if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, nullptr, w.err), st));
-    CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA), st));
+    CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA, w.err), st));
     Partial pa{w.PA, w.splitsA, r, 0}, none{};
     CK(finalize_dA<bf16>(r, in, pa, 1.f, none, 0.f, nullptr, 0.f, static_cast<const bf16*>(A), static_cast<bf16*>(dA),
                          st));
@@ -710,7 +714,7 @@ lora_status lora_qkv_fwd(const lora_qkv_shape* sh, const void* X, const void* W0
   CK(pack_leaves(leaf_pack(*sh, leaves, w.A_stack, w.B_blk), st));
   bf16* Z = Z_save ? static_cast<bf16*>(Z_save) : w.Z;
   if (live || Z_save) {  // one pass over X for every leaf's down-projection
-    RowProjDesc d = rp_desc(M, in, R, X, w.A_stack, false);
+    RowProjDesc d = rp_desc(M, in, R, X, w.A_stack, false, w.err);
     d.out_a = Z;
     CK(rowproj(d, st));
   }
@@ -758,7 +762,7 @@ lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0
     if (dX) CK(tc_gemm(dx_desc(M, in, N, dY, W0, nullptr, nullptr, R, dX, nullptr, w.err), st));
     if (dbias) {
       for (int l = 0; l < sh->L; ++l) {
-        ColReduceDesc d = cr_desc(M, sh->n[l], 8, dYb + row0[l], dY, N, w.PB[l], w.splitsB[l]);
+        ColReduceDesc d = cr_desc(M, sh->n[l], 8, dYb + row0[l], dY, N, w.PB[l], w.splitsB[l], w.err);
         d.lds = N;
         d.colsum = w.csum[l];
         CK(colreduce(d, st));
@@ -770,25 +774,25 @@ lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0
   CK(pack_leaves(leaf_pack(*sh, leaves, w.A_stack, w.B_blk), st));
   const bf16* Z = static_cast<const bf16*>(Z_saved);
   if (!Z) {
-    RowProjDesc d = rp_desc(M, in, R, X, w.A_stack, false);
+    RowProjDesc d = rp_desc(M, in, R, X, w.A_stack, false, w.err);
     d.out_a = w.Zrec;
     CK(rowproj(d, st));
     Z = w.Zrec;
   }
   // dB partials of each leaf (its columns of dY against its block of Z) and dY column sums
   for (int l = 0; l < sh->L; ++l) {
-    ColReduceDesc d = cr_desc(M, sh->n[l], r, dYb + row0[l], Z + l * r, R, w.PB[l], w.splitsB[l]);
+    ColReduceDesc d = cr_desc(M, sh->n[l], r, dYb + row0[l], Z + l * r, R, w.PB[l], w.splitsB[l], w.err);
     d.lds = N;
     d.colsum = dbias ? w.csum[l] : nullptr;
     CK(colreduce(d, st));
   }
   {  // [s_l dY_l B_l] for all leaves in one pass over dY (B_blk is block-diagonal)
-    RowProjDesc d = rp_desc(M, N, R, dY, w.B_blk, true);
+    RowProjDesc d = rp_desc(M, N, R, dY, w.B_blk, true, w.err);
     d.out_a = w.Gs;
     CK(rowproj(d, st));
   }
   if (dX) CK(tc_gemm(dx_desc(M, in, N, dY, W0, w.Gs, w.A_stack, R, dX, nullptr, w.err), st));
-  CK(colreduce(cr_desc(M, in, R, X, w.Gs, R, w.PA, w.splitsA), st));
+  CK(colreduce(cr_desc(M, in, R, X, w.Gs, R, w.PA, w.splitsA, w.err), st));
   for (int l = 0; l < sh->L; ++l) {
     Partial pa{w.PA, w.splitsA, R, l * r}, none{};
     CK(finalize_dA<bf16>(r, in, pa, 1.f, none, 0.f, nullptr, 0.f, static_cast<const bf16*>(leaves[l].A),
@@ -832,7 +836,7 @@ lora_status dora_linear_fwd(const lora_shape* sh, const void* X, const void* W0,
   const int r = (int)sh->r;
   if (sh->dtype == LORA_BF16) {
     {  // V = W0 A^T (fp32), one pass over W0
-      RowProjDesc d = rp_desc(out, in, r, W0, A, false);
+      RowProjDesc d = rp_desc(out, in, r, W0, A, false, w.err);
       d.out_f = V_save;
       CK(rowproj(d, st));
     }
@@ -841,7 +845,7 @@ lora_status dora_linear_fwd(const lora_shape* sh, const void* X, const void* W0,
                        n_save, w.c, st));
     if (M == 0) return LORA_OK;
     if (s != 0.f || Z_save) {
-      RowProjDesc d = rp_desc(M, in, r, X, A, false);
+      RowProjDesc d = rp_desc(M, in, r, X, A, false, w.err);
       d.out_a = static_cast<bf16*>(Z_save);
       d.out_b = s != 0.f ? static_cast<bf16*>(w.Zs) : nullptr;
       d.scale_b = s;
@@ -907,7 +911,7 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     if (bf) {
       if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, nullptr, A, r, dX, nullptr, w.err), st));
       if (dbias) {
-        ColReduceDesc d = cr_desc(M, out, 8, dY, dY, out, w.PB, w.splitsB);
+        ColReduceDesc d = cr_desc(M, out, 8, dY, dY, out, w.PB, w.splitsB, w.err);
         d.colsum = w.csump;
         CK(colreduce(d, st));
         CK(sum_splits<bf16>(w.csump, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
@@ -926,7 +930,7 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     CK(dora_c<bf16>(out, mb, n_saved, w.c, st));
     const void* Z = Z_saved;
     if (!Z) {
-      RowProjDesc d = rp_desc(M, in, r, X, A, false);
+      RowProjDesc d = rp_desc(M, in, r, X, A, false, w.err);
       d.out_a = static_cast<bf16*>(w.Zrec);
       CK(rowproj(d, st));
       Z = w.Zrec;
@@ -935,7 +939,7 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     // scaled tile by tile in the GEMM's shared memory (LORA_GB300_DORA_KSCALE=1); same bits.
     const bool kscale = env_flag("LORA_GB300_DORA_KSCALE");
     {  // one pass over dY and Y: dY^T Z partials, colsum(dY), colsum(dY o Y), and dY o c
-      ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB);
+      ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
       d.Y = static_cast<const bf16*>(Y);
       d.ldy = out;
       d.colsum = w.csump;
@@ -953,7 +957,7 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     CK(scale_rows<bf16>(static_cast<const bf16*>(B), out, r, w.c, 1.f, static_cast<bf16*>(w.Bc), st));
     CK(scale_rows<bf16>(static_cast<const bf16*>(B), out, r, w.g, 1.f, static_cast<bf16*>(w.gB), st));
     {  // s * G = s (dY o c) B  =  s dY (c o B)
-      RowProjDesc d = rp_desc(M, out, r, dY, w.Bc, true);
+      RowProjDesc d = rp_desc(M, out, r, dY, w.Bc, true, w.err);
       d.out_b = static_cast<bf16*>(w.Gs);
       d.scale_b = s;
       CK(rowproj(d, st));
@@ -962,8 +966,8 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       if (kscale) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, w.c, w.err), st));
       else CK(tc_gemm(dx_desc(M, in, out, w.dYc, W0, w.Gs, A, r, dX, nullptr, w.err), st));
     }
-    CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA), st));        // X^T (s G)
-    CK(colreduce(cr_desc(out, in, r, W0, w.gB, r, w.PW, w.splitsW), st));     // W0^T (g o B)
+    CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA, w.err), st));        // X^T (s G)
+    CK(colreduce(cr_desc(out, in, r, W0, w.gB, r, w.PW, w.splitsW, w.err), st));     // W0^T (g o B)
     CK(gram_rows<bf16>(static_cast<const bf16*>(A), r, in, w.Kr, st));
     CK(gram_weighted<bf16>(static_cast<const bf16*>(B), out, r, w.g, w.Kg, st));
     Partial pa{w.PA, w.splitsA, r, 0}, pw{w.PW, w.splitsW, r, 0}, pb{w.PB, w.splitsB, r, 0};
@@ -1040,14 +1044,14 @@ lora_status dora_cols_fwd(const lora_shape* sh, const void* X, const void* W0, c
   const bf16* Ab = static_cast<const bf16*>(A);
   const bf16* Bb = static_cast<const bf16*>(B);
   // U = (B^T W0)^T [in, r] in one pass over W0, K_b = B^T B, then the column norm and c = m / n
-  CK(colreduce(cr_desc(out, in, r, W0, B, r, w.PU, w.splitsW), st));
+  CK(colreduce(cr_desc(out, in, r, W0, B, r, w.PU, w.splitsW, w.err), st));
   CK(sum_splits<float>(w.PU, w.splitsW, in * r, U_save, nullptr, st));
   CK(gram_weighted<bf16>(Bb, out, r, nullptr, w.Kb, st));
   CK(dora_colnorm(in, r, c0, U_save, Ab, w.Kb, static_cast<const bf16*>(m), s, eps, n_save, w.c, w.Ac, st));
   if (M == 0) return LORA_OK;
   if (s != 0.f || Z_save) {
     // one pass over X: Z = X (A diag(c))^T, s Z, and the scaled copy X diag(c) for the GEMM
-    RowProjDesc d = rp_desc(M, in, r, X, w.Ac, false);
+    RowProjDesc d = rp_desc(M, in, r, X, w.Ac, false, w.err);
     d.out_a = static_cast<bf16*>(Z_save);
     if (s != 0.f) {
       d.out_b = w.Zs;
@@ -1096,7 +1100,7 @@ lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, c
     // strength 0: frozen base, dX = dY W0, dbias = colsum(dY)
     if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, nullptr, A, r, dX, nullptr, w.err), st));
     if (dbias) {
-      ColReduceDesc d = cr_desc(M, out, 8, dY, dY, out, w.PB, w.splitsB);
+      ColReduceDesc d = cr_desc(M, out, 8, dY, dY, out, w.PB, w.splitsB, w.err);
       d.colsum = w.csump;
       CK(colreduce(d, st));
       CK(sum_splits<bf16>(w.csump, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
@@ -1107,18 +1111,18 @@ lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, c
   const void* Z = Z_saved;
   if (!Z) {
     CK(scale_cols_bf16(Ab, r, in, w.c, w.Ac, st));
-    RowProjDesc d = rp_desc(M, in, r, X, w.Ac, false);
+    RowProjDesc d = rp_desc(M, in, r, X, w.Ac, false, w.err);
     d.out_a = w.Zrec;
     CK(rowproj(d, st));
     Z = w.Zrec;
   }
   {  // dY^T Z partials and colsum(dY), one pass over dY
-    ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB);
+    ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
     d.colsum = dbias ? w.csump : nullptr;
     CK(colreduce(d, st));
   }
   {  // G = s dY B
-    RowProjDesc d = rp_desc(M, out, r, dY, B, true);
+    RowProjDesc d = rp_desc(M, out, r, dY, B, true, w.err);
     d.out_b = w.Gs;
     d.scale_b = s;
     CK(rowproj(d, st));
@@ -1131,7 +1135,7 @@ lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, c
     CK(tc_gemm(d, st));
   }
   {  // (X^T G) partials and colsum(X o dX) = c o colsum(X o dXt), one pass over X and dX
-    ColReduceDesc d = cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA);
+    ColReduceDesc d = cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA, w.err);
     d.Y = dXo;
     d.ldy = in;
     d.coldot = w.dotp;
@@ -1144,7 +1148,7 @@ lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, c
   CK(gram_rows_weighted(Ab, r, in, w.g, w.Kga, st));
   CK(scale_cols_bf16(Ab, r, in, w.g, w.Ag, st));
   {  // W0 diag(g) A^T (fp32), one pass over W0
-    RowProjDesc d = rp_desc(out, in, r, W0, w.Ag, false);
+    RowProjDesc d = rp_desc(out, in, r, W0, w.Ag, false, w.err);
     d.out_f = w.Vg;
     CK(rowproj(d, st));
   }
@@ -1183,7 +1187,7 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
   const int r = (int)sh->r;
   CK(concat_rows_bf16(static_cast<const bf16*>(gate->A), r, static_cast<const bf16*>(up->A), r, H, w.Agu, st));
   {  // [Zg | Zu] = X [Ag ; Au]^T, saved unscaled and scaled per half
-    RowProjDesc d = rp_desc(M, H, 2 * r, X, w.Agu, false);
+    RowProjDesc d = rp_desc(M, H, 2 * r, X, w.Agu, false, w.err);
     d.out_a = static_cast<bf16*>(Zgu_save);
     d.out_b = w.Zgus;
     d.scale_b = gate->s;
@@ -1222,7 +1226,7 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
     CK(tc_gemm(d, st));
   }
   {  // Zd = h Ad^T
-    RowProjDesc d = rp_desc(M, I, r, h_save, down->A, false);
+    RowProjDesc d = rp_desc(M, I, r, h_save, down->A, false, w.err);
     d.out_a = static_cast<bf16*>(Zd_save);
     d.out_b = w.Zds;
     d.scale_b = down->s;
@@ -1264,9 +1268,9 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
   }
   const bf16* Zgu = static_cast<const bf16*>(Zgu_saved);
   // down projection: dBd partials (dY^T Zd), sd*Gd = sd dY Bd
-  CK(colreduce(cr_desc(M, H, r, dY, Zd_saved, r, w.PBd, w.sBd), st));
+  CK(colreduce(cr_desc(M, H, r, dY, Zd_saved, r, w.PBd, w.sBd, w.err), st));
   {
-    RowProjDesc d = rp_desc(M, H, r, dY, down->B, true);
+    RowProjDesc d = rp_desc(M, H, r, dY, down->B, true, w.err);
     d.out_b = w.Gds;
     d.scale_b = down->s;
     CK(rowproj(d, st));
@@ -1303,23 +1307,23 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     d.timeout_ns = wait_timeout_ns();
     CK(tc_gemm(d, st));
   }
-  CK(colreduce(cr_desc(M, I, r, h_saved, w.Gds, r, w.PAd, w.sAd), st));     // h^T (sd Gd)
+  CK(colreduce(cr_desc(M, I, r, h_saved, w.Gds, r, w.PAd, w.sAd, w.err), st));     // h^T (sd Gd)
   {  // de^T Zg and du^T Zu
-    ColReduceDesc d = cr_desc(M, I, r, w.dedu, Zgu, 2 * r, w.PBg, w.sBg);
+    ColReduceDesc d = cr_desc(M, I, r, w.dedu, Zgu, 2 * r, w.PBg, w.sBg, w.err);
     d.lds = 2 * Ip;
     CK(colreduce(d, st));
-    ColReduceDesc d2 = cr_desc(M, I, r, w.dedu + Ip, Zgu + r, 2 * r, w.PBu, w.sBg);
+    ColReduceDesc d2 = cr_desc(M, I, r, w.dedu + Ip, Zgu + r, 2 * r, w.PBu, w.sBg, w.err);
     d2.lds = 2 * Ip;
     CK(colreduce(d2, st));
   }
   {  // [sg Gg | su Gu] = [sg de Bg | su du Bu]
-    RowProjDesc d = rp_desc(M, I, r, w.dedu, gate->B, true);
+    RowProjDesc d = rp_desc(M, I, r, w.dedu, gate->B, true, w.err);
     d.lds = 2 * Ip;
     d.out_b = w.Ggus;
     d.scale_b = gate->s;
     d.ldo = 2 * r;
     CK(rowproj(d, st));
-    RowProjDesc d2 = rp_desc(M, I, r, w.dedu + Ip, up->B, true);
+    RowProjDesc d2 = rp_desc(M, I, r, w.dedu + Ip, up->B, true, w.err);
     d2.lds = 2 * Ip;
     d2.out_b = w.Ggus + r;
     d2.scale_b = up->s;
@@ -1356,7 +1360,7 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     d.timeout_ns = wait_timeout_ns();
     CK(tc_gemm(d, st));
   }
-  CK(colreduce(cr_desc(M, H, 2 * r, X, w.Ggus, 2 * r, w.PAgu, w.sAgu), st));  // X^T [sg Gg | su Gu]
+  CK(colreduce(cr_desc(M, H, 2 * r, X, w.Ggus, 2 * r, w.PAgu, w.sAgu, w.err), st));  // X^T [sg Gg | su Gu]
   Partial none{};
   Partial pag{w.PAgu, w.sAgu, 2 * r, 0}, pau{w.PAgu, w.sAgu, 2 * r, r};
   CK(finalize_dA<bf16>(r, H, pag, 1.f, none, 0.f, nullptr, 0.f, nullptr, static_cast<bf16*>(dAg), st));
@@ -1385,7 +1389,7 @@ lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t
   if (rows == 0) return LORA_OK;
   CK(quantize_rows_bf16(static_cast<const bf16*>(X), rows, cols, Xq, sx, st));
   if (A) {
-    RowProjDesc d = rp_desc(rows, cols, (int)r, X, A, false);
+    RowProjDesc d = rp_desc(rows, cols, (int)r, X, A, false, nullptr);  // no workspace: no error word
     d.out_a = static_cast<bf16*>(Z);
     CK(rowproj(d, st));
   }

@@ -1,6 +1,7 @@
 // Host-side declarations shared by the translation units of the library (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -11,6 +12,10 @@ namespace lg {
 typedef __nv_bfloat16 bf16;
 
 int num_sms_current();
+// 2-D bf16 tensor map over `outer` rows of `inner` contiguous elements (row stride `ld` elements),
+// box {box_inner, box_outer}, swizzle of 0 / 32 / 64 / 128 bytes; out-of-bounds elements read as zero.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                    uint32_t box_inner, uint32_t box_outer, int swizzle_bytes);
 
 // tracing (prof.cu)
 void count_launch(int n = 1);
@@ -95,6 +100,8 @@ struct RowProjDesc {
   // optional column-scaled copy of S written on the way: s_out[row, k] = bf16(S[row, k] * s_scale[k])
   const float* s_scale = nullptr;
   bf16* s_out = nullptr;        // [rows, K], leading dimension K
+  uint32_t* err = nullptr;      // device error word for bounded waits
+  uint64_t timeout_ns = 2000000000ull;
 };
 cudaError_t rowproj(const RowProjDesc& d, cudaStream_t st);
 
@@ -117,6 +124,8 @@ struct ColReduceDesc {
   // with Y: optional column-scaled copy of S written on the way, sc_out[row, k] = bf16(S[row, k] * sc[k])
   const float* sc = nullptr;
   bf16* sc_out = nullptr;      // [rows, K], leading dimension K
+  uint32_t* err = nullptr;     // device error word for bounded waits
+  uint64_t timeout_ns = 2000000000ull;
 };
 int colreduce_splits(int64_t rows, int64_t K);
 cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st);

@@ -13,95 +13,135 @@
 namespace lg {
 
 // ============================================================================ rowproj
+// One CTA owns 32 rows of S and streams them across K in 64-wide stages: a producer warp
+// issues one TMA box for the S tile (32 x 64, 128B-swizzled) and one for the matching U tile,
+// two consumer warps (16 rows each) run the warp MMAs straight from the swizzled tiles.
 namespace rp {
-constexpr int BMR = 32;        // rows per CTA
-constexpr int BKC = 128;       // K per stage (256-byte row segments of S)
-constexpr int PITCH = BKC + 8; // padded smem row pitch (elements) -> conflict-free ldmatrix
-constexpr int STAGES = 6;      // deep ring: ~43 KB of the streamed operand in flight per CTA
-constexpr int S_BYTES = BMR * PITCH * 2;       // 8704
-// U chunk: [R(+8 pad rows), BKC] K-major or [BKC, R+8] R-major
-template <int R, bool KR>
-constexpr int u_bytes() { return KR ? BKC * (R + 8) * 2 : (R + 8) * PITCH * 2; }
-template <int R, bool KR>
-constexpr int stage_bytes() { return S_BYTES + u_bytes<R, KR>(); }
-}  // namespace rp
+constexpr int BMR = 32;   // rows per CTA
+constexpr int BK = 64;    // K per stage (one 128-byte swizzle row)
+constexpr int NST = 8;    // stages in flight per CTA
+constexpr int S_BYTES = BMR * 128;
+
+// byte offset of 16-byte chunk `chunk` of row `row` in a TMA-swizzled tile whose rows are
+// `pitch` bytes: the chunk index is XORed with address bits 7.. (mask 7 / 3 / 1 / 0 for the
+// 128 / 64 / 32-byte / no swizzle)
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk, uint32_t pitch, uint32_t mask) {
+  return row * pitch + ((chunk ^ (((row * pitch) >> 7) & mask)) << 4);
+}
 
 template <int R, bool U_KR>
-__global__ void __launch_bounds__(128) rowproj_kernel(RowProjDesc d) {
+struct Cfg {
+  // U [K, R]: the TMA box spans RPAD >= R columns (power of two, zero-filled past R)
+  static constexpr int RPAD = R <= 8 ? 8 : (R <= 16 ? 16 : (R <= 32 ? 32 : 64));
+  static constexpr int UPITCH = U_KR ? RPAD * 2 : 128;
+  static constexpr int UMASK = U_KR ? (RPAD == 8 ? 0 : RPAD == 16 ? 1 : RPAD == 32 ? 3 : 7) : 7;
+  static constexpr int USWZ = U_KR ? (RPAD == 8 ? 0 : RPAD * 2) : 128;
+  static constexpr int UROWS = (R + 15) / 16 * 16;              // U [R, K]: rows reserved (even n-tiles)
+  static constexpr int U_BYTES = U_KR ? BK * RPAD * 2 : UROWS * 128;
+  static constexpr int U_TX = U_KR ? BK * RPAD * 2 : R * 128;   // bytes the U box delivers
+  static constexpr int STAGE = (S_BYTES + U_BYTES + 1023) / 1024 * 1024;
+  static constexpr int SMEM = NST * STAGE + 1024 + 2 * NST * 8 + 16;
+};
+}  // namespace rp
+
+struct RpParams {
+  CUtensorMap tmS;
+  CUtensorMap tmU;
+  RowProjDesc d;
+};
+
+template <int R, bool U_KR>
+__global__ void __launch_bounds__(96) rowproj_kernel(const __grid_constant__ RpParams P) {
   using namespace rp;
-  constexpr int STAGE_BYTES = stage_bytes<R, U_KR>();
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rg = warp & 1;        // 16-row group
-  const int kh = warp >> 1;       // which half of each BKC-wide K chunk
+  using C = Cfg<R, U_KR>;
+  const RowProjDesc& d = P.d;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * C::STAGE);
+  uint64_t* empty = full + NST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NST);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row0 = (int64_t)blockIdx.x * BMR;
-  const int nkc = (int)((d.K + BKC - 1) / BKC);
-  constexpr int UPITCH = U_KR ? (R + 8) : PITCH;
-
-  auto load_stage = [&](int stage, int kc) {
-    uint8_t* sS = smem + stage * STAGE_BYTES;
-    uint8_t* sU = sS + S_BYTES;
-    const int64_t k0 = (int64_t)kc * BKC;
-    constexpr int CPS = BKC / 8;   // 16-byte chunks per staged row
-#pragma unroll
-    for (int i = 0; i < BMR * CPS / 128; ++i) {
-      const int ci = tid + 128 * i;
-      const int r = ci / CPS, c = ci % CPS;
-      const int64_t gr = row0 + r, gk = k0 + c * 8;
-      const bool ok = gr < d.rows && gk < d.K;
-      const bf16* src = ok ? d.S + gr * d.lds + gk : d.S;
-      cp_async16(sS + (r * PITCH + c * 8) * 2, src, ok);
+  const int nkc = (int)((d.K + BK - 1) / BK);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 2);
     }
-    if (!U_KR) {  // U [R, K]: R rows x CPS chunks
-      for (int ci = tid; ci < R * CPS; ci += 128) {
-        const int r = ci / CPS, c = ci % CPS;
-        const int64_t gk = k0 + c * 8;
-        const bool ok = gk < d.K;
-        const bf16* src = ok ? d.U + (int64_t)r * d.ldu + gk : d.U;
-        cp_async16(sU + (r * UPITCH + c * 8) * 2, src, ok);
-      }
-    } else {      // U [K, R]: BKC rows x R/8 chunks
-      constexpr int CPR = R / 8;
-      for (int ci = tid; ci < BKC * CPR; ci += 128) {
-        const int r = ci / CPR, c = ci % CPR;
-        const int64_t gk = k0 + r;
-        const bool ok = gk < d.K;
-        const bf16* src = ok ? d.U + gk * d.ldu + c * 8 : d.U;
-        cp_async16(sU + (r * UPITCH + c * 8) * 2, src, ok);
-      }
-    }
-  };
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
 
+  if (warp == 2) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&P.tmS);
+      tma_prefetch_desc(&P.tmU);
+      bool ok = true;
+      for (int kc = 0; kc < nkc; ++kc) {
+        const int s = kc % NST;
+        const uint32_t ph = (uint32_t)(kc / NST) & 1u;
+        if (kc >= NST && !mbar_wait(&empty[s], ph ^ 1u, d.timeout_ns, abort_flag, d.err, 0x301)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * C::STAGE;
+        mbar_expect_tx(&full[s], S_BYTES + C::U_TX);
+        tma_load_2d(st, &P.tmS, &full[s], kc * BK, (int)row0);
+        if (U_KR) tma_load_2d(st + S_BYTES, &P.tmU, &full[s], 0, kc * BK);
+        else tma_load_2d(st + S_BYTES, &P.tmU, &full[s], kc * BK, 0);
+      }
+      if (!ok) spin_ns(100000ull);  // unwind: let copies already issued land
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers: 16 rows each
   float acc[R / 8][4];
 #pragma unroll
   for (int i = 0; i < R / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-
-#pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < nkc) load_stage(s, s);
-    cp_async_commit();
-  }
+  const int c8 = lane & 7;  // the 16-byte chunk this lane copies in the scaled side output
   for (int kc = 0; kc < nkc; ++kc) {
-    cp_async_wait<STAGES - 2>();
-    __syncthreads();
-    const int stage = kc % STAGES;
-    const uint32_t sS = smem_u32(smem + stage * STAGE_BYTES);
+    const int s = kc % NST;
+    const uint32_t ph = (uint32_t)(kc / NST) & 1u;
+    if (!mbar_wait(&full[s], ph, d.timeout_ns, abort_flag, d.err, 0x302)) break;
+    const uint8_t* tile = smem + s * C::STAGE;
+    const uint32_t sS = smem_u32(tile);
     const uint32_t sU = sS + S_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < BK / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(a[0], a[1], a[2], a[3], sS + swz(warp * 16 + (lane & 15), kk * 2 + (lane >> 4), 128, 7));
+#pragma unroll
+      for (int nt = 0; nt < R / 8; nt += 2) {
+        uint32_t b0, b1, b2 = 0, b3 = 0;
+        if (!U_KR) {
+          const int n = nt * 8 + (lane & 7) + ((lane >> 4) << 3);
+          const int c = kk * 2 + ((lane >> 3) & 1);
+          if (nt + 1 < R / 8) ldsm_x4(b0, b1, b2, b3, sU + swz(n, c, 128, 7));
+          else ldsm_x2(b0, b1, sU + swz(nt * 8 + (lane & 7), c, 128, 7));
+        } else {
+          const int krow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+          if (nt + 1 < R / 8) ldsm_x4_t(b0, b1, b2, b3, sU + swz(krow, nt + (lane >> 4), C::UPITCH, C::UMASK));
+          else ldsm_x2_t(b0, b1, sU + swz(krow, nt, C::UPITCH, C::UMASK));
+        }
+        mma_bf16_16816(acc[nt], a, b0, b1);
+        if (nt + 1 < R / 8) mma_bf16_16816(acc[nt + 1], a, b2, b3);
+      }
+    }
     if (d.s_out) {
-      // column-scaled copy of this 32 x 128 tile of S: thread tid owns 16-byte chunk (tid & 15)
-      // of rows (tid >> 4) + 8 i
-      const int c16 = tid & 15;
-      const int64_t gk = (int64_t)kc * BKC + c16 * 8;
+      // column-scaled copy of this warp's 16 x 64 slice of S (lane: chunk c8 of rows lane/8 + 4 i)
+      const int64_t gk = (int64_t)kc * BK + c8 * 8;
       if (gk < d.K) {
         const float4 lo = __ldg(reinterpret_cast<const float4*>(d.s_scale + gk));
         const float4 hi = __ldg(reinterpret_cast<const float4*>(d.s_scale + gk + 4));
         const float sc8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        const uint8_t* tile = smem + stage * STAGE_BYTES;
 #pragma unroll
-        for (int i = 0; i < BMR / 8; ++i) {
-          const int r = (tid >> 4) + 8 * i;
+        for (int i = 0; i < 4; ++i) {
+          const int r = warp * 16 + (lane >> 3) + 4 * i;
           if (row0 + r >= d.rows) break;
-          uint4 v = *reinterpret_cast<const uint4*>(tile + (r * PITCH + c16 * 8) * 2);
+          uint4 v = *reinterpret_cast<const uint4*>(tile + swz(r, c8, 128, 7));
           uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -112,82 +152,50 @@ __global__ void __launch_bounds__(128) rowproj_kernel(RowProjDesc d) {
         }
       }
     }
-#pragma unroll
-    for (int k2 = 0; k2 < BKC / 32; ++k2) {
-      const int kk = kh * (BKC / 32) + k2;  // k16 step within the BKC-wide chunk
-      uint32_t a[4];
-      ldsm_x4(a[0], a[1], a[2], a[3],
-              sS + ((rg * 16 + (lane & 15)) * PITCH + kk * 16 + (lane >> 4) * 8) * 2);
-#pragma unroll
-      for (int nt = 0; nt < R / 8; nt += 2) {
-        uint32_t b0, b1, b2, b3;
-        if (!U_KR) {
-          // rows n (8 + 8), 8 contiguous k at kk*16 and kk*16+8
-          const int n = nt * 8 + (lane & 7) + ((lane >> 4) << 3);
-          const int kcol = kk * 16 + ((lane >> 3) & 1) * 8;
-          ldsm_x4(b0, b1, b2, b3, sU + (n * UPITCH + kcol) * 2);
-        } else {
-          const int krow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-          const int ncol = nt * 8 + (lane >> 4) * 8;
-          ldsm_x4_t(b0, b1, b2, b3, sU + (krow * UPITCH + ncol) * 2);
-        }
-        mma_bf16_16816(acc[nt], a, b0, b1);
-        if (nt + 1 < R / 8) mma_bf16_16816(acc[nt + 1], a, b2, b3);
-      }
-    }
-    const int nxt = kc + STAGES - 1;
-    if (nxt < nkc) load_stage(nxt % STAGES, nxt);
-    cp_async_commit();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
-  cp_async_wait<0>();
-  __syncthreads();
 
-  // combine the two K halves: warps with kh == 1 hand their partial sums over via smem
-  float* red = reinterpret_cast<float*>(smem);  // [2 row groups][32 lanes][R/2]
-  if (kh == 1) {
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t ldo = d.ldo > 0 ? d.ldo : R;
 #pragma unroll
-    for (int nt = 0; nt < R / 8; ++nt)
+  for (int nt = 0; nt < R / 8; ++nt) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) red[(rg * 32 + lane) * (R / 2) + nt * 4 + e] = acc[nt][e];
-  }
-  __syncthreads();
-  if (kh == 0) {
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < R / 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nt][e] += red[(rg * 32 + lane) * (R / 2) + nt * 4 + e];
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int64_t grow = row0 + rg * 16 + g + hr * 8;
-        if (grow >= d.rows) continue;
-        const int col = nt * 8 + 2 * t;
-        const int64_t ldo = d.ldo > 0 ? d.ldo : R;
-        const float v0 = acc[nt][2 * hr], v1 = acc[nt][2 * hr + 1];
-        if (d.out_a)
-          *reinterpret_cast<uint32_t*>(d.out_a + grow * ldo + col) = pack_bf16x2(v0 * d.scale_a, v1 * d.scale_a);
-        if (d.out_b) {
-          const float sb = col >= d.split_col ? d.scale_b_hi : d.scale_b;
-          *reinterpret_cast<uint32_t*>(d.out_b + grow * ldo + col) = pack_bf16x2(v0 * sb, v1 * sb);
-        }
-        if (d.out_f) *reinterpret_cast<float2*>(d.out_f + grow * ldo + col) = make_float2(v0, v1);
+    for (int hr = 0; hr < 2; ++hr) {
+      const int64_t grow = row0 + warp * 16 + g + hr * 8;
+      if (grow >= d.rows) continue;
+      const int col = nt * 8 + 2 * t;
+      const float v0 = acc[nt][2 * hr], v1 = acc[nt][2 * hr + 1];
+      if (d.out_a)
+        *reinterpret_cast<uint32_t*>(d.out_a + grow * ldo + col) = pack_bf16x2(v0 * d.scale_a, v1 * d.scale_a);
+      if (d.out_b) {
+        const float sb = col >= d.split_col ? d.scale_b_hi : d.scale_b;
+        *reinterpret_cast<uint32_t*>(d.out_b + grow * ldo + col) = pack_bf16x2(v0 * sb, v1 * sb);
       }
+      if (d.out_f) *reinterpret_cast<float2*>(d.out_f + grow * ldo + col) = make_float2(v0, v1);
     }
   }
 }
 
 template <int R, bool KR>
 static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
-  const int smem = rp::STAGES * rp::stage_bytes<R, KR>();
+  using C = rp::Cfg<R, KR>;
   auto k = rowproj_kernel<R, KR>;
   static bool set = false;
   if (!set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     set = true;
   }
+  RpParams P;
+  memset(&P, 0, sizeof(P));
+  P.d = d;
+  bool ok = make_tmap_bf16(&P.tmS, d.S, (uint64_t)d.K, (uint64_t)d.rows, (uint64_t)d.lds, rp::BK, rp::BMR, 128);
+  if (KR) ok = ok && make_tmap_bf16(&P.tmU, d.U, R, (uint64_t)d.K, (uint64_t)d.ldu, C::RPAD, rp::BK, C::USWZ);
+  else ok = ok && make_tmap_bf16(&P.tmU, d.U, (uint64_t)d.K, R, (uint64_t)d.ldu, rp::BK, R, 128);
+  if (!ok) return cudaErrorInvalidValue;
   const int64_t grid = (d.rows + rp::BMR - 1) / rp::BMR;
-  k<<<(unsigned)grid, 128, smem, st>>>(d);
+  k<<<(unsigned)grid, 96, C::SMEM, st>>>(P);
   count_launch();
   return cudaGetLastError();
 }
