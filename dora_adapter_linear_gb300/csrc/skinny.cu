@@ -1,6 +1,6 @@
 // Rank-r ("skinny") kernels of the bf16 path.  These touch every element of a large
-// activation once and do 2r flops per element, so they are HBM-bound: the design goal is
-// coalesced 16-byte loads, a deep cp.async pipeline and enough CTAs in flight per SM.
+// activation once and do 2r flops per element, so they are HBM-bound: tiles arrive by TMA
+// (one producer warp per CTA, a deep mbarrier ring) and enough CTAs are in flight per SM.
 // The arithmetic runs on the legacy warp MMA (mma.sync m16n8k16, fp32 accumulate), which
 // keeps up with HBM at these ranks.
 //
@@ -220,107 +220,135 @@ cudaError_t rowproj(const RowProjDesc& d, cudaStream_t st) {
 }
 
 // ============================================================================ colreduce
+// One CTA owns 64 columns of S and one split of the rows.  A producer warp brings in, per
+// 64-row stage, the 64 x 64 tile of S (and of Y), 128B-swizzled, and the 64 x R tile of T by
+// TMA; four consumer warps (16 columns each) run the warp MMAs S^T T straight from the tiles.
 namespace cr {
 constexpr int BKC = 64;       // columns (K) per CTA
 constexpr int BR = 64;        // rows per stage
-constexpr int PITCH = 72;
-constexpr int S_BYTES = BR * PITCH * 2;   // 9216
+constexpr int S_BYTES = BR * 128;
+
+template <int R, bool HAS_Y>
+struct Cfg {
+  static constexpr int RPAD = R <= 8 ? 8 : (R <= 16 ? 16 : (R <= 32 ? 32 : 64));
+  static constexpr int TPITCH = RPAD * 2;
+  static constexpr int TMASK = RPAD == 8 ? 0 : RPAD == 16 ? 1 : RPAD == 32 ? 3 : 7;
+  static constexpr int TSWZ = RPAD == 8 ? 0 : RPAD * 2;
+  static constexpr int T_BYTES = BR * RPAD * 2;
+  static constexpr int OFF_Y = S_BYTES + ((T_BYTES + 1023) / 1024) * 1024;
+  static constexpr int STAGE = OFF_Y + (HAS_Y ? S_BYTES : 0);
+  static constexpr int TX = S_BYTES + T_BYTES + (HAS_Y ? S_BYTES : 0);
+  static constexpr int NST = HAS_Y ? 4 : 6;
+  static constexpr int SMEM = NST * STAGE + 1024 + 2 * NST * 8 + 16;
+};
 }  // namespace cr
 
+struct CrParams {
+  CUtensorMap tmS;
+  CUtensorMap tmT;
+  CUtensorMap tmY;
+  ColReduceDesc d;
+  int64_t rows_per_split;
+};
+
 template <int R, bool HAS_Y, bool SUMS>
-__global__ void __launch_bounds__(128) colreduce_kernel(ColReduceDesc d, int64_t rows_per_split) {
+__global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ CrParams P) {
   using namespace cr;
-  constexpr int TPITCH = R + 8;
-  constexpr int T_BYTES = BR * TPITCH * 2;
-  constexpr int STAGE_BYTES = S_BYTES + T_BYTES + (HAS_Y ? S_BYTES : 0);
-  constexpr int STAGES = HAS_Y ? 3 : 4;
-  extern __shared__ __align__(16) uint8_t smem[];
+  using rp::swz;
+  using C = Cfg<R, HAS_Y>;
+  constexpr int NST = C::NST;
+  const ColReduceDesc& d = P.d;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * C::STAGE);
+  uint64_t* empty = full + NST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NST);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t k0 = (int64_t)blockIdx.x * BKC;
   const int split = blockIdx.y;
-  const int64_t r_begin = (int64_t)split * rows_per_split;
-  const int64_t r_end = min(d.rows, r_begin + rows_per_split);
+  const int64_t r_begin = (int64_t)split * P.rows_per_split;   // a multiple of BR
+  const int64_t r_end = min(d.rows, r_begin + P.rows_per_split);
   const int nrc = r_end > r_begin ? (int)((r_end - r_begin + BR - 1) / BR) : 0;
-
-  auto load_stage = [&](int stage, int rc) {
-    uint8_t* sS = smem + stage * STAGE_BYTES;
-    uint8_t* sT = sS + S_BYTES;
-    uint8_t* sY = sT + T_BYTES;
-    const int64_t rb = r_begin + (int64_t)rc * BR;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {  // 64 rows x 8 chunks
-      const int ci = tid + 128 * i;
-      const int r = ci >> 3, c = ci & 7;
-      const int64_t gr = rb + r, gk = k0 + c * 8;
-      const bool ok = gr < r_end && gk < d.K;
-      cp_async16(sS + (r * PITCH + c * 8) * 2, ok ? d.S + gr * d.lds + gk : d.S, ok);
-      if (HAS_Y) cp_async16(sY + (r * PITCH + c * 8) * 2, ok ? d.Y + gr * d.ldy + gk : d.Y, ok);
+  if (tid == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 4);
     }
-    constexpr int CPR = R / 8;
-    for (int ci = tid; ci < BR * CPR; ci += 128) {
-      const int r = ci / CPR, c = ci % CPR;
-      const int64_t gr = rb + r;
-      const bool ok = gr < r_end;
-      cp_async16(sT + (r * TPITCH + c * 8) * 2, ok ? d.T + gr * d.ldt + c * 8 : d.T, ok);
-    }
-  };
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
 
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&P.tmS);
+      tma_prefetch_desc(&P.tmT);
+      if (HAS_Y) tma_prefetch_desc(&P.tmY);
+      bool ok = true;
+      for (int rc = 0; rc < nrc; ++rc) {
+        const int s = rc % NST;
+        const uint32_t ph = (uint32_t)(rc / NST) & 1u;
+        if (rc >= NST && !mbar_wait(&empty[s], ph ^ 1u, d.timeout_ns, abort_flag, d.err, 0x311)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * C::STAGE;
+        const int y = (int)(r_begin + (int64_t)rc * BR);
+        mbar_expect_tx(&full[s], C::TX);
+        tma_load_2d(st, &P.tmS, &full[s], (int)k0, y);
+        tma_load_2d(st + S_BYTES, &P.tmT, &full[s], 0, y);
+        if (HAS_Y) tma_load_2d(st + C::OFF_Y, &P.tmY, &full[s], (int)k0, y);
+      }
+      if (!ok) spin_ns(100000ull);  // unwind: let copies already issued land
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers: 16 columns each
   float acc[R / 8][4];
 #pragma unroll
   for (int i = 0; i < R / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
   float csum = 0.f, cdot = 0.f;
-  const int my_col = tid & 63, my_par = tid >> 6;
-
-#pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < nrc) load_stage(s, s);
-    cp_async_commit();
-  }
+  const int my_col = tid & 63, my_par = tid >> 6;   // column sums: 2 row phases x 64 columns
+  const int c8 = tid & 7;                            // scaled copy: 16-byte chunk of this thread
   for (int rc = 0; rc < nrc; ++rc) {
-    cp_async_wait<STAGES - 2>();
-    __syncthreads();
-    const int stage = rc % STAGES;
-    uint8_t* pS = smem + stage * STAGE_BYTES;
-    const uint32_t sS = smem_u32(pS);
+    const int s = rc % NST;
+    const uint32_t ph = (uint32_t)(rc / NST) & 1u;
+    if (!mbar_wait(&full[s], ph, d.timeout_ns, abort_flag, d.err, 0x312)) break;
+    const uint8_t* tile = smem + s * C::STAGE;
+    const uint32_t sS = smem_u32(tile);
     const uint32_t sT = sS + S_BYTES;
 #pragma unroll
     for (int kk = 0; kk < BR / 16; ++kk) {
       uint32_t a[4];
-      {
+      {  // A = S^T: 16 columns of this warp x 16 rows, transposed out of the row-major tile
         const int row = kk * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int col = warp * 16 + ((lane >> 3) & 1) * 8;
-        ldsm_x4_t(a[0], a[1], a[2], a[3], sS + (row * PITCH + col) * 2);
+        ldsm_x4_t(a[0], a[1], a[2], a[3], sS + swz(row, warp * 2 + ((lane >> 3) & 1), 128, 7));
       }
 #pragma unroll
       for (int nt = 0; nt < R / 8; nt += 2) {
-        uint32_t b0, b1, b2, b3;
+        uint32_t b0, b1, b2 = 0, b3 = 0;
         const int row = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int col = nt * 8 + (lane >> 4) * 8;
-        if (nt + 1 < R / 8) {
-          ldsm_x4_t(b0, b1, b2, b3, sT + (row * TPITCH + col) * 2);
-        } else {
-          ldsm_x2_t(b0, b1, sT + (row * TPITCH + nt * 8) * 2);
-          b2 = b3 = 0;
-        }
+        if (nt + 1 < R / 8) ldsm_x4_t(b0, b1, b2, b3, sT + swz(row, nt + (lane >> 4), C::TPITCH, C::TMASK));
+        else ldsm_x2_t(b0, b1, sT + swz(row, nt, C::TPITCH, C::TMASK));
         mma_bf16_16816(acc[nt], a, b0, b1);
         if (nt + 1 < R / 8) mma_bf16_16816(acc[nt + 1], a, b2, b3);
       }
     }
+    const int64_t rb = r_begin + (int64_t)rc * BR;
     if (HAS_Y && d.sc_out) {
-      // the column-scaled copy of this 64 x 64 tile: thread tid owns 16-byte chunk (tid & 7) of rows
-      // (tid >> 3) + 16 i, so its 8 scales are fixed for the whole kernel
-      const int c8 = tid & 7;
+      // column-scaled copy of the S tile: thread tid owns chunk c8 of rows tid/8 + 16 i
       const int64_t gk = k0 + c8 * 8;
       if (gk < d.K) {
         const float4 lo = __ldg(reinterpret_cast<const float4*>(d.sc + gk));
         const float4 hi = __ldg(reinterpret_cast<const float4*>(d.sc + gk + 4));
         const float sc8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        const int64_t rb = r_begin + (int64_t)rc * BR;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = (tid >> 3) + 16 * i;
           if (rb + r >= r_end) break;
-          uint4 v = *reinterpret_cast<const uint4*>(pS + (r * PITCH + c8 * 8) * 2);
+          uint4 v = *reinterpret_cast<const uint4*>(tile + swz(r, c8, 128, 7));
           uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -332,23 +360,20 @@ __global__ void __launch_bounds__(128) colreduce_kernel(ColReduceDesc d, int64_t
       }
     }
     if (SUMS) {
-      const bf16* ps = reinterpret_cast<const bf16*>(pS);
-      const bf16* py = reinterpret_cast<const bf16*>(pS + S_BYTES + T_BYTES);
+      // rows past the end of the tensor were zero-filled by the TMA, so they add nothing
 #pragma unroll 8
       for (int r = my_par; r < BR; r += 2) {
-        const float sv = __bfloat162float(ps[r * PITCH + my_col]);
+        const uint32_t o = swz(r, my_col >> 3, 128, 7) + (my_col & 7) * 2;
+        const float sv = __bfloat162float(*reinterpret_cast<const bf16*>(tile + o));
         csum += sv;
-        if (HAS_Y) cdot += sv * __bfloat162float(py[r * PITCH + my_col]);
+        if (HAS_Y) cdot += sv * __bfloat162float(*reinterpret_cast<const bf16*>(tile + C::OFF_Y + o));
       }
     }
-    const int nxt = rc + STAGES - 1;
-    __syncthreads();
-    if (nxt < nrc) load_stage(nxt % STAGES, nxt);
-    cp_async_commit();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
-  cp_async_wait<0>();
-  __syncthreads();
 
+  // ------------------------------------------------------------------ partials of this split
   const int g = lane >> 2, t = lane & 3;
   float* part = d.part + ((int64_t)split * d.K) * R;
 #pragma unroll
@@ -360,12 +385,15 @@ __global__ void __launch_bounds__(128) colreduce_kernel(ColReduceDesc d, int64_t
         *reinterpret_cast<float2*>(part + k * R + nt * 8 + 2 * t) = make_float2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
     }
   if (SUMS) {
+    // the two row phases of each column meet in shared memory; stage 0 is free once all four
+    // consumer warps are past their last wait (the producer issues nothing more by then)
     float* red = reinterpret_cast<float*>(smem);
+    named_bar_sync(1, 128);
     if (my_par == 1) {
       red[my_col] = csum;
       red[64 + my_col] = cdot;
     }
-    __syncthreads();
+    named_bar_sync(1, 128);
     if (my_par == 0) {
       const int64_t k = k0 + my_col;
       if (k < d.K) {
@@ -388,21 +416,26 @@ int colreduce_splits(int64_t rows, int64_t K) {
 
 template <int R, bool HAS_Y, bool SUMS>
 static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
-  constexpr int T_BYTES = cr::BR * (R + 8) * 2;
-  constexpr int STAGE_BYTES = cr::S_BYTES + T_BYTES + (HAS_Y ? cr::S_BYTES : 0);
-  constexpr int STAGES = HAS_Y ? 3 : 4;
-  const int smem = STAGES * STAGE_BYTES;
+  using C = cr::Cfg<R, HAS_Y>;
   auto k = colreduce_kernel<R, HAS_Y, SUMS>;
   static bool set = false;
   if (!set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     set = true;
   }
-  int64_t rps = (d.rows + d.splits - 1) / d.splits;
-  rps = (rps + cr::BR - 1) / cr::BR * cr::BR;
+  CrParams P;
+  memset(&P, 0, sizeof(P));
+  P.d = d;
+  const int64_t rps = (d.rows + d.splits - 1) / d.splits;
+  P.rows_per_split = (rps + cr::BR - 1) / cr::BR * cr::BR;
+  bool ok = make_tmap_bf16(&P.tmS, d.S, (uint64_t)d.K, (uint64_t)d.rows, (uint64_t)d.lds, cr::BKC, cr::BR, 128);
+  ok = ok && make_tmap_bf16(&P.tmT, d.T, R, (uint64_t)d.rows, (uint64_t)d.ldt, C::RPAD, cr::BR, C::TSWZ);
+  if (HAS_Y)
+    ok = ok && make_tmap_bf16(&P.tmY, d.Y, (uint64_t)d.K, (uint64_t)d.rows, (uint64_t)d.ldy, cr::BKC, cr::BR, 128);
+  if (!ok) return cudaErrorInvalidValue;
   dim3 grid((unsigned)((d.K + cr::BKC - 1) / cr::BKC), (unsigned)d.splits);
-  k<<<grid, 128, smem, st>>>(d, rps);
+  k<<<grid, 160, C::SMEM, st>>>(P);
   count_launch();
   return cudaGetLastError();
 }
