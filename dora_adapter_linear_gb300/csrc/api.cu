@@ -637,12 +637,9 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     }
     if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, nullptr, w.err), st));
     CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA, w.err), st));
-    Partial pa{w.PA, w.splitsA, r, 0}, none{};
-    CK(finalize_dA<bf16>(r, in, pa, 1.f, none, 0.f, nullptr, 0.f, static_cast<const bf16*>(A), static_cast<bf16*>(dA),
-                         st));
-    Partial pb{w.PB, w.splitsB, r, 0};
-    CK(finalize_dB<bf16>(out, r, pb, s, nullptr, nullptr, nullptr, static_cast<const bf16*>(B), nullptr, s, false,
-                         static_cast<bf16*>(dB), st));
+    const FinJob fin[2] = {fin_dA(r, in, Partial{w.PA, w.splitsA, r, 0}, 1.f, A, dA),
+                           fin_dB(out, r, Partial{w.PB, w.splitsB, r, 0}, s, B, dB)};
+    CK(finalize_batch(fin, 2, st));
     if (dbias) CK(sum_splits<bf16>(w.csum, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
   } else {
     if (dX) CK(sgemm_f32(sg(M, in, out, dY, out, false, W0, in, false, dX, in), st));
@@ -793,17 +790,15 @@ lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0
   }
   if (dX) CK(tc_gemm(dx_desc(M, in, N, dY, W0, w.Gs, w.A_stack, R, dX, nullptr, w.err), st));
   CK(colreduce(cr_desc(M, in, R, X, w.Gs, R, w.PA, w.splitsA, w.err), st));
+  FinJob fin[2 * kMaxLeaves];
   for (int l = 0; l < sh->L; ++l) {
-    Partial pa{w.PA, w.splitsA, R, l * r}, none{};
-    CK(finalize_dA<bf16>(r, in, pa, 1.f, none, 0.f, nullptr, 0.f, static_cast<const bf16*>(leaves[l].A),
-                         static_cast<bf16*>(dA[l]), st));
-    Partial pb{w.PB[l], w.splitsB[l], r, 0};
-    CK(finalize_dB<bf16>(sh->n[l], r, pb, leaves[l].s, nullptr, nullptr, nullptr,
-                         static_cast<const bf16*>(leaves[l].B), nullptr, leaves[l].s, false, static_cast<bf16*>(dB[l]),
-                         st));
-    if (dbias)
-      CK(sum_splits<bf16>(w.csum[l], w.splitsB[l], sh->n[l], nullptr, static_cast<bf16*>(dbias) + row0[l], st));
+    fin[2 * l] = fin_dA(r, in, Partial{w.PA, w.splitsA, R, l * r}, 1.f, leaves[l].A, dA[l]);
+    fin[2 * l + 1] = fin_dB(sh->n[l], r, Partial{w.PB[l], w.splitsB[l], r, 0}, leaves[l].s, leaves[l].B, dB[l]);
   }
+  CK(finalize_batch(fin, 2 * sh->L, st));
+  if (dbias)
+    for (int l = 0; l < sh->L; ++l)
+      CK(sum_splits<bf16>(w.csum[l], w.splitsB[l], sh->n[l], nullptr, static_cast<bf16*>(dbias) + row0[l], st));
   return LORA_OK;
 }
 
@@ -970,11 +965,18 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     CK(colreduce(cr_desc(out, in, r, W0, w.gB, r, w.PW, w.splitsW, w.err), st));     // W0^T (g o B)
     CK(gram_rows<bf16>(static_cast<const bf16*>(A), r, in, w.Kr, st));
     CK(gram_weighted<bf16>(static_cast<const bf16*>(B), out, r, w.g, w.Kg, st));
-    Partial pa{w.PA, w.splitsA, r, 0}, pw{w.PW, w.splitsW, r, 0}, pb{w.PB, w.splitsB, r, 0};
-    CK(finalize_dA<bf16>(r, in, pa, 1.f, pw, 2.f * s, w.Kg, 2.f * s * s, static_cast<const bf16*>(A),
-                         static_cast<bf16*>(dA), st));
-    CK(finalize_dB<bf16>(out, r, pb, s, w.c, w.g, V_saved, static_cast<const bf16*>(B), w.Kr, s, false,
-                         static_cast<bf16*>(dB), st));
+    FinJob fin[2] = {fin_dA(r, in, Partial{w.PA, w.splitsA, r, 0}, 1.f, A, dA),
+                     fin_dB(out, r, Partial{w.PB, w.splitsB, r, 0}, s, B, dB)};
+    fin[0].PW = Partial{w.PW, w.splitsW, r, 0};   // + 2s (g o B)^T W0 + 2s^2 (B^T diag(g) B) A
+    fin[0].sW = 2.f * s;
+    fin[0].Kx = w.Kg;
+    fin[0].s2 = 2.f * s * s;
+    fin[1].rs = w.c;                               // c o (s dY^T Z) + 2s g o V + 2s^2 g o (B (A A^T))
+    fin[1].g = w.g;
+    fin[1].V = V_saved;
+    fin[1].Kx = w.Kr;
+    fin[1].s = s;
+    CK(finalize_batch(fin, 2, st));
   } else {
     const float* mf = static_cast<const float*>(m);
     CK(dora_c<float>(out, mf, n_saved, w.c, st));
@@ -1361,19 +1363,13 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     CK(tc_gemm(d, st));
   }
   CK(colreduce(cr_desc(M, H, 2 * r, X, w.Ggus, 2 * r, w.PAgu, w.sAgu, w.err), st));  // X^T [sg Gg | su Gu]
-  Partial none{};
-  Partial pag{w.PAgu, w.sAgu, 2 * r, 0}, pau{w.PAgu, w.sAgu, 2 * r, r};
-  CK(finalize_dA<bf16>(r, H, pag, 1.f, none, 0.f, nullptr, 0.f, nullptr, static_cast<bf16*>(dAg), st));
-  CK(finalize_dA<bf16>(r, H, pau, 1.f, none, 0.f, nullptr, 0.f, nullptr, static_cast<bf16*>(dAu), st));
-  Partial pad{w.PAd, w.sAd, r, 0};
-  CK(finalize_dA<bf16>(r, I, pad, 1.f, none, 0.f, nullptr, 0.f, nullptr, static_cast<bf16*>(dAd), st));
-  Partial pbd{w.PBd, w.sBd, r, 0}, pbg{w.PBg, w.sBg, r, 0}, pbu{w.PBu, w.sBg, r, 0};
-  CK(finalize_dB<bf16>(H, r, pbd, down->s, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, false,
-                       static_cast<bf16*>(dBd), st));
-  CK(finalize_dB<bf16>(I, r, pbg, gate->s, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, false,
-                       static_cast<bf16*>(dBg), st));
-  CK(finalize_dB<bf16>(I, r, pbu, up->s, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, false,
-                       static_cast<bf16*>(dBu), st));
+  const FinJob fin[6] = {fin_dA(r, H, Partial{w.PAgu, w.sAgu, 2 * r, 0}, 1.f, nullptr, dAg),
+                         fin_dA(r, H, Partial{w.PAgu, w.sAgu, 2 * r, r}, 1.f, nullptr, dAu),
+                         fin_dA(r, I, Partial{w.PAd, w.sAd, r, 0}, 1.f, nullptr, dAd),
+                         fin_dB(H, r, Partial{w.PBd, w.sBd, r, 0}, down->s, nullptr, dBd),
+                         fin_dB(I, r, Partial{w.PBg, w.sBg, r, 0}, gate->s, nullptr, dBg),
+                         fin_dB(I, r, Partial{w.PBu, w.sBg, r, 0}, up->s, nullptr, dBu)};
+  CK(finalize_batch(fin, 6, st));
   return LORA_OK;
 }
 

@@ -101,9 +101,13 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* map, uin
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
+// Output tiles are written once and not read back by this kernel: they go to L2 with an
+// evict-first policy so that they do not push out operand tiles that are still being reused.
 __device__ __forceinline__ void tma_store_2d(const void* map, const void* smem_src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
-               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
+               ::"l"(map), "r"(smem_u32(smem_src)), "r"(x), "r"(y), "l"(pol)
                : "memory");
 }
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

@@ -171,6 +171,49 @@ cudaError_t finalize_dA(int r, int64_t in, Partial PA, float sA, Partial PW, flo
 template <typename T>
 cudaError_t finalize_dB(int64_t out, int r, Partial PB, float sB, const float* rs, const float* g, const float* V,
                         const T* B, const float* Kr, float s, bool accumulate, T* dB, cudaStream_t st);
+// One bf16 gradient assembly of a batch (finalize_batch runs up to kMaxFinJobs in one launch):
+//   is_dB == 0: dA [r, rows] as finalize_dA(r, rows, P, sP, PW, sW, Kx (= Kg), s2, M (= A), out)
+//   is_dB == 1: dB [rows, r] as finalize_dB(rows, r, P, sP, rs, g, V, M (= B), Kx (= Kr), s, false, out)
+constexpr int kMaxFinJobs = 8;
+struct FinJob {
+  int is_dB = 0;
+  int r = 0;
+  int64_t rows = 0;
+  Partial P{};
+  float sP = 0.f;
+  Partial PW{};
+  float sW = 0.f;
+  const float* Kx = nullptr;
+  float s2 = 0.f;
+  const float* rs = nullptr;
+  const float* g = nullptr;
+  const float* V = nullptr;
+  float s = 0.f;
+  const bf16* M = nullptr;
+  bf16* out = nullptr;
+};
+cudaError_t finalize_batch(const FinJob* jobs, int n, cudaStream_t st);
+inline FinJob fin_dA(int r, int64_t in, Partial PA, float sA, const void* A, void* dA) {
+  FinJob f;
+  f.r = r;
+  f.rows = in;
+  f.P = PA;
+  f.sP = sA;
+  f.M = static_cast<const bf16*>(A);
+  f.out = static_cast<bf16*>(dA);
+  return f;
+}
+inline FinJob fin_dB(int64_t out, int r, Partial PB, float sB, const void* B, void* dB) {
+  FinJob f;
+  f.is_dB = 1;
+  f.r = r;
+  f.rows = out;
+  f.P = PB;
+  f.sP = sB;
+  f.M = static_cast<const bf16*>(B);
+  f.out = static_cast<bf16*>(dB);
+  return f;
+}
 // Kg = B^T diag(g) B  (fp32 [r, r]; g null = all ones)
 template <typename T>
 cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float* Kg, cudaStream_t st);

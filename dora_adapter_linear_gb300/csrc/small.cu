@@ -212,10 +212,9 @@ cudaError_t scale_rows(const T* B, int64_t rows, int r, const float* scale, floa
 
 // ------------------------------------------------------------------ gradient assembly
 template <typename T>
-__global__ void finalize_dA_kernel(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg,
-                                   float s2, const T* A, T* dA) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // index into dA [r, in]
-  if (i >= (int64_t)r * in) return;
+__device__ __forceinline__ void finalize_dA_elem(int64_t i, int r, int64_t in, const Partial& PA, float sA,
+                                                 const Partial& PW, float sW, const float* Kg, float s2, const T* A,
+                                                 T* dA) {
   const int j = (int)(i / in);
   const int64_t k = i - (int64_t)j * in;
   float a = 0.f;
@@ -236,21 +235,11 @@ __global__ void finalize_dA_kernel(int r, int64_t in, Partial PA, float sA, Part
   }
   dA[i] = from_f<T>(a);
 }
-template <typename T>
-cudaError_t finalize_dA(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg, float s2,
-                        const T* A, T* dA, cudaStream_t st) {
-  const int64_t n = (int64_t)r * in;
-  if (n <= 0) return cudaSuccess;
-  finalize_dA_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(r, in, PA, sA, PW, sW, Kg, s2, A, dA);
-  count_launch();
-  return cudaGetLastError();
-}
 
 template <typename T>
-__global__ void finalize_dB_kernel(int64_t out, int r, Partial PB, float sB, const float* rs, const float* g,
-                                   const float* V, const T* B, const float* Kr, float s, bool accumulate, T* dB) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // index into dB [out, r]
-  if (i >= out * r) return;
+__device__ __forceinline__ void finalize_dB_elem(int64_t i, int64_t out, int r, const Partial& PB, float sB,
+                                                 const float* rs, const float* g, const float* V, const T* B,
+                                                 const float* Kr, float s, bool accumulate, T* dB) {
   const int64_t o = i / r;
   const int j = (int)(i - o * r);
   float t = 0.f;
@@ -266,6 +255,29 @@ __global__ void finalize_dB_kernel(int64_t out, int r, Partial PB, float sB, con
   }
   dB[i] = from_f<T>(a);
 }
+
+template <typename T>
+__global__ void finalize_dA_kernel(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg,
+                                   float s2, const T* A, T* dA) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // index into dA [r, in]
+  if (i < (int64_t)r * in) finalize_dA_elem<T>(i, r, in, PA, sA, PW, sW, Kg, s2, A, dA);
+}
+template <typename T>
+cudaError_t finalize_dA(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg, float s2,
+                        const T* A, T* dA, cudaStream_t st) {
+  const int64_t n = (int64_t)r * in;
+  if (n <= 0) return cudaSuccess;
+  finalize_dA_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(r, in, PA, sA, PW, sW, Kg, s2, A, dA);
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <typename T>
+__global__ void finalize_dB_kernel(int64_t out, int r, Partial PB, float sB, const float* rs, const float* g,
+                                   const float* V, const T* B, const float* Kr, float s, bool accumulate, T* dB) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // index into dB [out, r]
+  if (i < out * r) finalize_dB_elem<T>(i, out, r, PB, sB, rs, g, V, B, Kr, s, accumulate, dB);
+}
 template <typename T>
 cudaError_t finalize_dB(int64_t out, int r, Partial PB, float sB, const float* rs, const float* g, const float* V,
                         const T* B, const float* Kr, float s, bool accumulate, T* dB, cudaStream_t st) {
@@ -273,6 +285,44 @@ cudaError_t finalize_dB(int64_t out, int r, Partial PB, float sB, const float* r
   if (n <= 0) return cudaSuccess;
   finalize_dB_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(out, r, PB, sB, rs, g, V, B, Kr, s, accumulate,
                                                                       dB);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// Several dA / dB assemblies in one launch: job j owns blocks [first[j], first[j + 1]).
+struct FinBatch {
+  FinJob job[kMaxFinJobs];
+  int first[kMaxFinJobs + 1];
+  int n = 0;
+};
+__global__ void finalize_batch_kernel(const __grid_constant__ FinBatch b) {
+  int j = 0;
+  while (j + 1 < b.n && (int)blockIdx.x >= b.first[j + 1]) ++j;
+  const FinJob& f = b.job[j];
+  const int64_t i = (int64_t)(blockIdx.x - b.first[j]) * blockDim.x + threadIdx.x;
+  if (f.is_dB) {
+    if (i < f.rows * f.r)
+      finalize_dB_elem<bf16>(i, f.rows, f.r, f.P, f.sP, f.rs, f.g, f.V, f.M, f.Kx, f.s, false, f.out);
+  } else {
+    if (i < (int64_t)f.r * f.rows)
+      finalize_dA_elem<bf16>(i, f.r, f.rows, f.P, f.sP, f.PW, f.sW, f.Kx, f.s2, f.M, f.out);
+  }
+}
+cudaError_t finalize_batch(const FinJob* jobs, int n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (n > kMaxFinJobs) return cudaErrorInvalidValue;
+  FinBatch b;
+  int64_t blocks = 0;
+  for (int j = 0; j < n; ++j) {
+    b.job[j] = jobs[j];
+    b.first[j] = (int)blocks;
+    blocks += (jobs[j].rows * jobs[j].r + 255) / 256;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  }
+  b.first[n] = (int)blocks;
+  b.n = n;
+  if (blocks <= 0) return cudaSuccess;
+  finalize_batch_kernel<<<(unsigned)blocks, 256, 0, st>>>(b);
   count_launch();
   return cudaGetLastError();
 }
