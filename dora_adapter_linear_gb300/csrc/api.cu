@@ -138,7 +138,7 @@ size_t plan_dora_fwd(const lora_shape& sh, char* base, DoraFwdWs* w) {
 
 struct DoraBwdWs {
   uint32_t* err;
-  float *c, *g, *dot, *csum, *dotp, *csump, *Kr, *Kg;
+  float *c, *g, *dot, *csum, *dotp, *csump, *Kr, *Kg, *Gw;
   void *Bc, *gB, *Gs, *Zrec;
   bf16* dYc;     // [M, out] dY o c (bf16 path)
   float *PB, *PA, *PW;
@@ -155,6 +155,7 @@ size_t plan_dora_bwd(const lora_shape& sh, char* base, DoraBwdWs* w) {
   w->csum = c.take<float>(out);
   w->Kr = c.take<float>(r * r);
   w->Kg = c.take<float>(r * r);
+  w->Gw = c.take<float>(gram_work_floats((int)r));
   w->Bc = c.take<char>(out * r * es);
   w->gB = c.take<char>(out * r * es);
   w->Gs = c.take<char>(M * r * es);
@@ -183,6 +184,7 @@ struct DoraColsFwdWs {
   uint32_t* err;
   float* PU;     // [splitsW, in, r] partials of W0^T B
   float* Kb;     // [r, r] B^T B
+  float* Gw;     // gram partials
   float* c;      // [in]
   bf16* Ac;      // [r, in] A diag(c)
   bf16* Zs;      // [M, r] s Z
@@ -196,6 +198,7 @@ size_t plan_dora_cols_fwd(const lora_shape& sh, char* base, DoraColsFwdWs* w) {
   w->splitsW = colreduce_splits(out, in);
   w->PU = c.take<float>(w->splitsW * in * r);
   w->Kb = c.take<float>(r * r);
+  w->Gw = c.take<float>(gram_work_floats((int)r));
   w->c = c.take<float>(in);
   w->Ac = c.take<bf16>(r * in);
   w->Zs = c.take<bf16>(M * r);
@@ -205,7 +208,7 @@ size_t plan_dora_cols_fwd(const lora_shape& sh, char* base, DoraColsFwdWs* w) {
 
 struct DoraColsBwdWs {
   uint32_t* err;
-  float *c, *g, *dot, *dotp, *Kb, *Kga, *Vg, *PA, *PB, *csump;
+  float *c, *g, *dot, *dotp, *Kb, *Kga, *Vg, *PA, *PB, *csump, *Gw;
   bf16 *Ac, *Ag, *Gs, *Zrec, *dXt;
   int splitsA, splitsB;
 };
@@ -221,6 +224,7 @@ size_t plan_dora_cols_bwd(const lora_shape& sh, char* base, DoraColsBwdWs* w) {
   w->dotp = c.take<float>(w->splitsA * in);
   w->Kb = c.take<float>(r * r);
   w->Kga = c.take<float>(r * r);
+  w->Gw = c.take<float>(gram_work_floats((int)r));
   w->Vg = c.take<float>(out * r);
   w->PA = c.take<float>(w->splitsA * in * r);
   w->PB = c.take<float>(w->splitsB * out * r);
@@ -413,6 +417,17 @@ ColReduceDesc cr_desc(int64_t rows, int64_t K, int R, const void* S, const void*
   d.err = err;
   d.timeout_ns = wait_timeout_ns();
   return d;
+}
+
+// K = B^T T (fp32 [r, r]) for bf16 B, T [rows, r]: a column reduction of B against T on the warp
+// MMAs (T = B gives B^T B, T = g o B gives B^T diag(g) B), then the split partials summed in
+// order.  `work` holds gram_work_floats(r) floats.
+cudaError_t gram_bf16(const void* B, const void* T, int64_t rows, int r, float* K, float* work, uint32_t* err,
+                      cudaStream_t st) {
+  const int splits = colreduce_splits(rows, r);
+  cudaError_t e = colreduce(cr_desc(rows, r, r, B, T, r, work, splits, err), st);
+  if (e != cudaSuccess) return e;
+  return sum_splits<float>(work, splits, (int64_t)r * r, K, nullptr, st);
 }
 
 SgemmDesc sg(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, bool ta, const void* B, int64_t ldb, bool tb,
@@ -964,7 +979,7 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA, w.err), st));        // X^T (s G)
     CK(colreduce(cr_desc(out, in, r, W0, w.gB, r, w.PW, w.splitsW, w.err), st));     // W0^T (g o B)
     CK(gram_rows<bf16>(static_cast<const bf16*>(A), r, in, w.Kr, st));
-    CK(gram_weighted<bf16>(static_cast<const bf16*>(B), out, r, w.g, w.Kg, st));
+    CK(gram_bf16(B, w.gB, out, r, w.Kg, w.Gw, w.err, st));
     FinJob fin[2] = {fin_dA(r, in, Partial{w.PA, w.splitsA, r, 0}, 1.f, A, dA),
                      fin_dB(out, r, Partial{w.PB, w.splitsB, r, 0}, s, B, dB)};
     fin[0].PW = Partial{w.PW, w.splitsW, r, 0};   // + 2s (g o B)^T W0 + 2s^2 (B^T diag(g) B) A
@@ -1000,7 +1015,7 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       CK(sgemm_f32(sg(M, in, r, w.Gs, r, false, A, in, false, dX, in, s, 1.f), st));
     }
     CK(gram_rows<float>(static_cast<const float*>(A), r, in, w.Kr, st));
-    CK(gram_weighted<float>(static_cast<const float*>(B), out, r, w.g, w.Kg, st));
+    CK(gram_weighted<float>(static_cast<const float*>(B), out, r, w.g, w.Kg, w.Gw, st));
     CK(scale_rows<float>(static_cast<const float*>(B), out, r, w.g, 1.f, static_cast<float*>(w.gB), st));
     CK(sgemm_f32(sg(r, in, M, w.Gs, r, true, X, in, false, dA, in, s), st));                 // s G^T X
     CK(sgemm_f32(sg(r, in, out, w.gB, r, true, W0, in, false, dA, in, 2.f * s, 1.f), st));  // + 2s (gB)^T W0
@@ -1048,7 +1063,7 @@ lora_status dora_cols_fwd(const lora_shape* sh, const void* X, const void* W0, c
   // U = (B^T W0)^T [in, r] in one pass over W0, K_b = B^T B, then the column norm and c = m / n
   CK(colreduce(cr_desc(out, in, r, W0, B, r, w.PU, w.splitsW, w.err), st));
   CK(sum_splits<float>(w.PU, w.splitsW, in * r, U_save, nullptr, st));
-  CK(gram_weighted<bf16>(Bb, out, r, nullptr, w.Kb, st));
+  CK(gram_bf16(B, B, out, r, w.Kb, w.Gw, w.err, st));
   CK(dora_colnorm(in, r, c0, U_save, Ab, w.Kb, static_cast<const bf16*>(m), s, eps, n_save, w.c, w.Ac, st));
   if (M == 0) return LORA_OK;
   if (s != 0.f || Z_save) {
@@ -1146,7 +1161,7 @@ lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, c
   CK(sum_splits<float>(w.dotp, w.splitsA, in, w.dot, nullptr, st));
   // dc = dot / c (no bias term), dm = dc / n, g = -m dc / (2 n^3)
   CK(dora_dc<bf16>(in, w.dot, w.dot, nullptr, w.c, n_saved, mb, eps, w.g, static_cast<bf16*>(dm), nullptr, st));
-  CK(gram_weighted<bf16>(Bb, out, r, nullptr, w.Kb, st));
+  CK(gram_bf16(B, B, out, r, w.Kb, w.Gw, w.err, st));
   CK(gram_rows_weighted(Ab, r, in, w.g, w.Kga, st));
   CK(scale_cols_bf16(Ab, r, in, w.g, w.Ag, st));
   {  // W0 diag(g) A^T (fp32), one pass over W0

@@ -214,9 +214,11 @@ inline FinJob fin_dB(int64_t out, int r, Partial PB, float sB, const void* B, vo
   f.out = static_cast<bf16*>(dB);
   return f;
 }
-// Kg = B^T diag(g) B  (fp32 [r, r]; g null = all ones)
+// Kg = B^T diag(g) B  (fp32 [r, r]; g null = all ones), r <= 64; `work` holds at least
+// gram_work_floats(r) floats of chunk partials
+size_t gram_work_floats(int r);
 template <typename T>
-cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float* Kg, cudaStream_t st);
+cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float* Kg, float* work, cudaStream_t st);
 // rows of two matrices stacked: dst = [X1 ; X2] (rows1 + rows2, cols), same dtype
 cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int64_t rows2, int64_t cols, bf16* dst,
                              cudaStream_t st);

@@ -40,6 +40,11 @@ struct Cfg {
   static constexpr int U_BYTES = U_KR ? BK * RPAD * 2 : UROWS * 128;
   static constexpr int U_TX = U_KR ? BK * RPAD * 2 : R * 128;   // bytes the U box delivers
   static constexpr int STAGE = (S_BYTES + U_BYTES + 1023) / 1024 * 1024;
+  // consumer warps: 2 row groups of 16 x NG groups of output columns (split when R / 8 is even
+  // and large enough, so that more warps share the MMA work of one tile)
+  static constexpr int NG = (R % 16 == 0 && R >= 32) ? 2 : 1;
+  static constexpr int NTW = R / 8 / NG;   // n-tiles of 8 per consumer warp
+  static constexpr int THREADS = 32 * (2 * NG + 1);
   static constexpr int SMEM = NST * STAGE + 1024 + 2 * NST * 8 + 16;
 };
 }  // namespace rp
@@ -51,7 +56,7 @@ struct RpParams {
 };
 
 template <int R, bool U_KR>
-__global__ void __launch_bounds__(96) rowproj_kernel(const __grid_constant__ RpParams P) {
+__global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(const __grid_constant__ RpParams P) {
   using namespace rp;
   using C = Cfg<R, U_KR>;
   const RowProjDesc& d = P.d;
@@ -66,14 +71,14 @@ __global__ void __launch_bounds__(96) rowproj_kernel(const __grid_constant__ RpP
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 2);
+      mbar_init(&empty[i], 2 * C::NG);
     }
     *abort_flag = 0;
     mbar_fence_init();
   }
   __syncthreads();
 
-  if (warp == 2) {
+  if (warp == 2 * C::NG) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&P.tmS);
@@ -97,10 +102,13 @@ __global__ void __launch_bounds__(96) rowproj_kernel(const __grid_constant__ RpP
     return;
   }
 
-  // ------------------------------------------------------------------ consumers: 16 rows each
-  float acc[R / 8][4];
+  // ------------------------------------------------------------------ consumers: 16 rows x R / NG each
+  constexpr int NTW = C::NTW;
+  const int rg = warp & 1;    // row group (rows 16 rg .. 16 rg + 15 of the tile)
+  const int nh = warp >> 1;   // column group (n-tiles nh NTW .. nh NTW + NTW - 1)
+  float acc[NTW][4];
 #pragma unroll
-  for (int i = 0; i < R / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  for (int i = 0; i < NTW; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
   const int c8 = lane & 7;  // the 16-byte chunk this lane copies in the scaled side output
   for (int kc = 0; kc < nkc; ++kc) {
     const int s = kc % NST;
@@ -112,25 +120,26 @@ __global__ void __launch_bounds__(96) rowproj_kernel(const __grid_constant__ RpP
 #pragma unroll
     for (int kk = 0; kk < BK / 16; ++kk) {
       uint32_t a[4];
-      ldsm_x4(a[0], a[1], a[2], a[3], sS + swz(warp * 16 + (lane & 15), kk * 2 + (lane >> 4), 128, 7));
+      ldsm_x4(a[0], a[1], a[2], a[3], sS + swz(rg * 16 + (lane & 15), kk * 2 + (lane >> 4), 128, 7));
 #pragma unroll
-      for (int nt = 0; nt < R / 8; nt += 2) {
+      for (int q = 0; q < NTW; q += 2) {
+        const int nt = nh * NTW + q;
         uint32_t b0, b1, b2 = 0, b3 = 0;
         if (!U_KR) {
           const int n = nt * 8 + (lane & 7) + ((lane >> 4) << 3);
           const int c = kk * 2 + ((lane >> 3) & 1);
-          if (nt + 1 < R / 8) ldsm_x4(b0, b1, b2, b3, sU + swz(n, c, 128, 7));
+          if (q + 1 < NTW) ldsm_x4(b0, b1, b2, b3, sU + swz(n, c, 128, 7));
           else ldsm_x2(b0, b1, sU + swz(nt * 8 + (lane & 7), c, 128, 7));
         } else {
           const int krow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-          if (nt + 1 < R / 8) ldsm_x4_t(b0, b1, b2, b3, sU + swz(krow, nt + (lane >> 4), C::UPITCH, C::UMASK));
+          if (q + 1 < NTW) ldsm_x4_t(b0, b1, b2, b3, sU + swz(krow, nt + (lane >> 4), C::UPITCH, C::UMASK));
           else ldsm_x2_t(b0, b1, sU + swz(krow, nt, C::UPITCH, C::UMASK));
         }
-        mma_bf16_16816(acc[nt], a, b0, b1);
-        if (nt + 1 < R / 8) mma_bf16_16816(acc[nt + 1], a, b2, b3);
+        mma_bf16_16816(acc[q], a, b0, b1);
+        if (q + 1 < NTW) mma_bf16_16816(acc[q + 1], a, b2, b3);
       }
     }
-    if (d.s_out) {
+    if (d.s_out && nh == 0) {
       // column-scaled copy of this warp's 16 x 64 slice of S (lane: chunk c8 of rows lane/8 + 4 i)
       const int64_t gk = (int64_t)kc * BK + c8 * 8;
       if (gk < d.K) {
@@ -139,7 +148,7 @@ __global__ void __launch_bounds__(96) rowproj_kernel(const __grid_constant__ RpP
         const float sc8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int r = warp * 16 + (lane >> 3) + 4 * i;
+          const int r = rg * 16 + (lane >> 3) + 4 * i;
           if (row0 + r >= d.rows) break;
           uint4 v = *reinterpret_cast<const uint4*>(tile + swz(r, c8, 128, 7));
           uint32_t* w = reinterpret_cast<uint32_t*>(&v);
@@ -159,13 +168,13 @@ __global__ void __launch_bounds__(96) rowproj_kernel(const __grid_constant__ RpP
   const int g = lane >> 2, t = lane & 3;
   const int64_t ldo = d.ldo > 0 ? d.ldo : R;
 #pragma unroll
-  for (int nt = 0; nt < R / 8; ++nt) {
+  for (int q = 0; q < NTW; ++q) {
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
-      const int64_t grow = row0 + warp * 16 + g + hr * 8;
+      const int64_t grow = row0 + rg * 16 + g + hr * 8;
       if (grow >= d.rows) continue;
-      const int col = nt * 8 + 2 * t;
-      const float v0 = acc[nt][2 * hr], v1 = acc[nt][2 * hr + 1];
+      const int col = (nh * NTW + q) * 8 + 2 * t;
+      const float v0 = acc[q][2 * hr], v1 = acc[q][2 * hr + 1];
       if (d.out_a)
         *reinterpret_cast<uint32_t*>(d.out_a + grow * ldo + col) = pack_bf16x2(v0 * d.scale_a, v1 * d.scale_a);
       if (d.out_b) {
@@ -195,7 +204,7 @@ static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
   else ok = ok && make_tmap_bf16(&P.tmU, d.U, (uint64_t)d.K, R, (uint64_t)d.ldu, rp::BK, R, 128);
   if (!ok) return cudaErrorInvalidValue;
   const int64_t grid = (d.rows + rp::BMR - 1) / rp::BMR;
-  k<<<(unsigned)grid, 96, C::SMEM, st>>>(P);
+  k<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(P);
   count_launch();
   return cudaGetLastError();
 }

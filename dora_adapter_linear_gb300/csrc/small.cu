@@ -84,55 +84,103 @@ cudaError_t gram_rows(const T* A, int r, int64_t cols, float* K, cudaStream_t st
 }
 
 // ------------------------------------------------------------------ Kg = B^T diag(g) B
+// Pass 1: block c takes a contiguous chunk of the rows of B, stages 32 rows at a time in shared
+// memory and accumulates its share of every entry (i, j); pass 2 sums the chunk partials in a
+// fixed order (deterministic, no atomics).
+constexpr int kGramChunks = 64;
 template <typename T>
-__global__ void gram_weighted_kernel(const T* B, int64_t out, int r, const float* g, float* Kg) {
-  const int i = blockIdx.x / r, j = blockIdx.x % r;
-  if (j < i) return;
-  float acc = 0.f;
-  for (int64_t o = threadIdx.x; o < out; o += blockDim.x)
-    acc = fmaf((g ? g[o] : 1.f) * ldf(B, o * r + i), ldf(B, o * r + j), acc);
-  acc = block_sum<256>(acc);
-  if (threadIdx.x == 0) {
-    Kg[i * r + j] = acc;
-    Kg[j * r + i] = acc;
+__global__ void __launch_bounds__(256) gram_partial_kernel(const T* B, int64_t out, int r, const float* g,
+                                                           int64_t rows_per, float* part) {
+  __shared__ float tile[32][65];
+  __shared__ float gw[32];
+  const int c = blockIdx.x;
+  const int64_t o0 = (int64_t)c * rows_per;
+  const int64_t o1 = min(out, o0 + rows_per);
+  const int rr2 = r * r;
+  float acc[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+  for (int64_t ob = o0; ob < o1; ob += 32) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < 32 * r; e += 256) {
+      const int rr = e / r, j = e - (e / r) * r;
+      const int64_t o = ob + rr;
+      tile[rr][j] = o < o1 ? ldf(B, o * r + j) : 0.f;
+    }
+    if (threadIdx.x < 32) {
+      const int64_t o = ob + threadIdx.x;
+      gw[threadIdx.x] = o < o1 ? (g ? g[o] : 1.f) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = threadIdx.x + 256 * q;
+      if (e < rr2) {
+        const int i = e / r, j = e - (e / r) * r;
+        float t = acc[q];
+        for (int rr = 0; rr < 32; ++rr) t = fmaf(gw[rr] * tile[rr][i], tile[rr][j], t);
+        acc[q] = t;
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int e = threadIdx.x + 256 * q;
+    if (e < rr2) part[(int64_t)c * rr2 + e] = acc[q];
   }
 }
+size_t gram_work_floats(int r) { return (size_t)kGramChunks * r * r; }
 template <typename T>
-cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float* Kg, cudaStream_t st) {
-  gram_weighted_kernel<T><<<r * r, 256, 0, st>>>(B, out, r, g, Kg);
+cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float* Kg, float* work, cudaStream_t st) {
+  if (r <= 0 || r > 64 || out <= 0) return cudaErrorInvalidValue;
+  int nch = (int)((out + 31) / 32);
+  if (nch > kGramChunks) nch = kGramChunks;
+  const int64_t rows_per = (out + nch - 1) / nch;
+  gram_partial_kernel<T><<<nch, 256, 0, st>>>(B, out, r, g, rows_per, work);
   count_launch();
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return sum_splits<float>(work, nch, (int64_t)r * r, Kg, nullptr, st);
 }
 
-// ------------------------------------------------------------------ closed-form DoRA norm, one thread per row
+// ------------------------------------------------------------------ closed-form DoRA norm, one warp per row
+// Lane j holds B[o, j] and B[o, j + 32]; (B Kr)[o, j] is formed with the row broadcast lane by lane.
 template <typename T>
 __global__ void dora_norm_kernel(int64_t out, int r, const float* r0, const float* V, const T* B, const float* Kr,
                                  const T* m, float s, float eps, float* n_out, float* c) {
   extern __shared__ float sKr[];
   for (int i = threadIdx.x; i < r * r; i += blockDim.x) sKr[i] = Kr[i];
   __syncthreads();
-  const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t o = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (o >= out) return;
-  float b[64];
-  for (int j = 0; j < r; ++j) b[j] = ldf(B, o * r + j);
-  float t1 = 0.f, t2 = 0.f;
-  for (int j = 0; j < r; ++j) {
-    t1 = fmaf(V[o * r + j], b[j], t1);
-    float bk = 0.f;
-    for (int l = 0; l < r; ++l) bk = fmaf(b[l], sKr[l * r + j], bk);
-    t2 = fmaf(bk, b[j], t2);
+  const bool h0 = lane < r, h1 = lane + 32 < r;
+  const float b0 = h0 ? ldf(B, o * r + lane) : 0.f;
+  const float b1 = h1 ? ldf(B, o * r + lane + 32) : 0.f;
+  float t1 = (h0 ? V[o * r + lane] * b0 : 0.f) + (h1 ? V[o * r + lane + 32] * b1 : 0.f);
+  float k0 = 0.f, k1 = 0.f;
+  for (int l = 0; l < r; ++l) {
+    const float bl = __shfl_sync(0xffffffffu, l < 32 ? b0 : b1, l & 31);
+    if (h0) k0 = fmaf(bl, sKr[l * r + lane], k0);
+    if (h1) k1 = fmaf(bl, sKr[l * r + lane + 32], k1);
   }
-  const float q = r0[o] + 2.f * s * t1 + s * s * t2;
-  const float n = fmaxf(sqrtf(fmaxf(q, 0.f)), eps);
-  n_out[o] = n;
-  if (c) c[o] = ldf(m, o) / n;
+  float t2 = k0 * b0 + k1 * b1;
+  t1 = warp_sum(t1);
+  t2 = warp_sum(t2);
+  if (lane == 0) {
+    const float q = r0[o] + 2.f * s * t1 + s * s * t2;
+    const float n = fmaxf(sqrtf(fmaxf(q, 0.f)), eps);
+    n_out[o] = n;
+    if (c) c[o] = ldf(m, o) / n;
+  }
 }
 template <typename T>
 cudaError_t dora_norm(int64_t out, int r, const float* r0, const float* V, const T* B, const float* Kr, const T* m,
                       float s, float eps, float* n_out, float* c, cudaStream_t st) {
   if (out <= 0) return cudaSuccess;
-  dora_norm_kernel<T><<<(unsigned)((out + 127) / 128), 128, r * r * sizeof(float), st>>>(out, r, r0, V, B, Kr, m, s,
-                                                                                         eps, n_out, c);
+  if (r > 64) return cudaErrorInvalidValue;
+  dora_norm_kernel<T><<<(unsigned)((out + 7) / 8), 256, r * r * sizeof(float), st>>>(out, r, r0, V, B, Kr, m, s, eps,
+                                                                                    n_out, c);
   count_launch();
   return cudaGetLastError();
 }
@@ -211,12 +259,11 @@ cudaError_t scale_rows(const T* B, int64_t rows, int r, const float* scale, floa
 }
 
 // ------------------------------------------------------------------ gradient assembly
+// One entry dA[j, k] of a dA assembly.
 template <typename T>
-__device__ __forceinline__ void finalize_dA_elem(int64_t i, int r, int64_t in, const Partial& PA, float sA,
-                                                 const Partial& PW, float sW, const float* Kg, float s2, const T* A,
-                                                 T* dA) {
-  const int j = (int)(i / in);
-  const int64_t k = i - (int64_t)j * in;
+__device__ __forceinline__ float finalize_dA_val(int64_t k, int j, int r, int64_t in, const Partial& PA, float sA,
+                                                 const Partial& PW, float sW, const float* Kg, float s2,
+                                                 const T* A) {
   float a = 0.f;
   if (PA.p) {
     float t = 0.f;
@@ -233,7 +280,7 @@ __device__ __forceinline__ void finalize_dA_elem(int64_t i, int r, int64_t in, c
     for (int l = 0; l < r; ++l) t = fmaf(Kg[j * r + l], ldf(A, (int64_t)l * in + k), t);
     a += s2 * t;
   }
-  dA[i] = from_f<T>(a);
+  return a;
 }
 
 template <typename T>
@@ -260,7 +307,10 @@ template <typename T>
 __global__ void finalize_dA_kernel(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg,
                                    float s2, const T* A, T* dA) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // index into dA [r, in]
-  if (i < (int64_t)r * in) finalize_dA_elem<T>(i, r, in, PA, sA, PW, sW, Kg, s2, A, dA);
+  if (i >= (int64_t)r * in) return;
+  const int j = (int)(i / in);
+  const int64_t k = i - (int64_t)j * in;
+  dA[i] = from_f<T>(finalize_dA_val<T>(k, j, r, in, PA, sA, PW, sW, Kg, s2, A));
 }
 template <typename T>
 cudaError_t finalize_dA(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg, float s2,
@@ -304,8 +354,11 @@ __global__ void finalize_batch_kernel(const __grid_constant__ FinBatch b) {
     if (i < f.rows * f.r)
       finalize_dB_elem<bf16>(i, f.rows, f.r, f.P, f.sP, f.rs, f.g, f.V, f.M, f.Kx, f.s, false, f.out);
   } else {
-    if (i < (int64_t)f.r * f.rows)
-      finalize_dA_elem<bf16>(i, f.r, f.rows, f.P, f.sP, f.PW, f.sW, f.Kx, f.s2, f.M, f.out);
+    if (i < (int64_t)f.r * f.rows) {
+      const int jj = (int)(i / f.rows);
+      const int64_t k = i - (int64_t)jj * f.rows;
+      f.out[i] = from_f<bf16>(finalize_dA_val<bf16>(k, jj, f.r, f.rows, f.P, f.sP, f.PW, f.sW, f.Kx, f.s2, f.M));
+    }
   }
 }
 cudaError_t finalize_batch(const FinJob* jobs, int n, cudaStream_t st) {
@@ -404,7 +457,7 @@ cudaError_t colnorm2_bf16(const bf16* W, int64_t rows, int64_t cols, float* c0, 
   return cudaGetLastError();
 }
 
-// closed-form column norm, one thread per input column k:
+// closed-form column norm, one warp per input column k (lane j holds A[j, k] and A[j + 32, k]):
 //   q = c0[k] + 2s sum_j A[j,k] U[k,j] + s^2 sum_j A[j,k] (Kb A)[j,k],  n = max(sqrt(max(q, 0)), eps),
 //   c = m / n, and (optionally) A_c[:, k] = bf16(A[:, k] c[k]).
 __global__ void dora_colnorm_kernel(int64_t in, int r, const float* c0, const float* U, const bf16* A,
@@ -413,30 +466,40 @@ __global__ void dora_colnorm_kernel(int64_t in, int r, const float* c0, const fl
   extern __shared__ float sK[];
   for (int i = threadIdx.x; i < r * r; i += blockDim.x) sK[i] = Kb[i];
   __syncthreads();
-  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t k = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (k >= in) return;
-  float a[64];
-  for (int j = 0; j < r; ++j) a[j] = __bfloat162float(A[(int64_t)j * in + k]);
-  float t1 = 0.f, t2 = 0.f;
-  for (int j = 0; j < r; ++j) {
-    t1 = fmaf(a[j], U[k * r + j], t1);
-    float ka = 0.f;
-    for (int l = 0; l < r; ++l) ka = fmaf(sK[j * r + l], a[l], ka);
-    t2 = fmaf(a[j], ka, t2);
+  const bool h0 = lane < r, h1 = lane + 32 < r;
+  const float a0 = h0 ? __bfloat162float(A[(int64_t)lane * in + k]) : 0.f;
+  const float a1 = h1 ? __bfloat162float(A[(int64_t)(lane + 32) * in + k]) : 0.f;
+  float t1 = (h0 ? a0 * U[k * r + lane] : 0.f) + (h1 ? a1 * U[k * r + lane + 32] : 0.f);
+  float k0 = 0.f, k1 = 0.f;   // (Kb A)[j, k] for j = lane, lane + 32 (Kb symmetric)
+  for (int l = 0; l < r; ++l) {
+    const float al = __shfl_sync(0xffffffffu, l < 32 ? a0 : a1, l & 31);
+    if (h0) k0 = fmaf(sK[l * r + lane], al, k0);
+    if (h1) k1 = fmaf(sK[l * r + lane + 32], al, k1);
   }
+  float t2 = a0 * k0 + a1 * k1;
+  t1 = warp_sum(t1);
+  t2 = warp_sum(t2);
   const float q = c0[k] + 2.f * s * t1 + s * s * t2;
   const float n = fmaxf(sqrtf(fmaxf(q, 0.f)), eps);
   const float cc = __bfloat162float(m[k]) / n;
-  n_out[k] = n;
-  c[k] = cc;
-  if (A_c)
-    for (int j = 0; j < r; ++j) A_c[(int64_t)j * in + k] = __float2bfloat16_rn(a[j] * cc);
+  if (lane == 0) {
+    n_out[k] = n;
+    c[k] = cc;
+  }
+  if (A_c) {
+    if (h0) A_c[(int64_t)lane * in + k] = __float2bfloat16_rn(a0 * cc);
+    if (h1) A_c[(int64_t)(lane + 32) * in + k] = __float2bfloat16_rn(a1 * cc);
+  }
 }
 cudaError_t dora_colnorm(int64_t in, int r, const float* c0, const float* U, const bf16* A, const float* Kb,
                          const bf16* m, float s, float eps, float* n_out, float* c, bf16* A_c, cudaStream_t st) {
   if (in <= 0) return cudaSuccess;
-  dora_colnorm_kernel<<<(unsigned)((in + 127) / 128), 128, r * r * sizeof(float), st>>>(in, r, c0, U, A, Kb, m, s,
-                                                                                        eps, n_out, c, A_c);
+  if (r > 64) return cudaErrorInvalidValue;
+  dora_colnorm_kernel<<<(unsigned)((in + 7) / 8), 256, r * r * sizeof(float), st>>>(in, r, c0, U, A, Kb, m, s, eps,
+                                                                                    n_out, c, A_c);
   count_launch();
   return cudaGetLastError();
 }
@@ -527,7 +590,7 @@ cudaError_t debug_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t 
 #define INST(T)                                                                                                    \
   template cudaError_t rownorm2<T>(const T*, int64_t, int64_t, float*, cudaStream_t);                               \
   template cudaError_t gram_rows<T>(const T*, int, int64_t, float*, cudaStream_t);                                  \
-  template cudaError_t gram_weighted<T>(const T*, int64_t, int, const float*, float*, cudaStream_t);                \
+  template cudaError_t gram_weighted<T>(const T*, int64_t, int, const float*, float*, float*, cudaStream_t);                \
   template cudaError_t dora_norm<T>(int64_t, int, const float*, const float*, const T*, const float*, const T*,     \
                                     float, float, float*, float*, cudaStream_t);                                    \
   template cudaError_t dora_c<T>(int64_t, const T*, const float*, float*, cudaStream_t);                            \
