@@ -66,10 +66,10 @@ template <int EPI, bool PAIR>
 struct EpiCfg;
 template <> struct EpiCfg<EPI_SCALE_BIAS, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
 template <> struct EpiCfg<EPI_SWIGLU, false> { static constexpr int STAGES = 3, STG_BUFS = 3; };
-template <> struct EpiCfg<EPI_SWIGLU_BWD, false> { static constexpr int STAGES = 3, STG_BUFS = 4; };
+template <> struct EpiCfg<EPI_SWIGLU_BWD, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
 template <> struct EpiCfg<EPI_SCALE_BIAS, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
 template <> struct EpiCfg<EPI_SWIGLU, true> { static constexpr int STAGES = 5, STG_BUFS = 3; };
-template <> struct EpiCfg<EPI_SWIGLU_BWD, true> { static constexpr int STAGES = 5, STG_BUFS = 4; };
+template <> struct EpiCfg<EPI_SWIGLU_BWD, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
 template <> struct EpiCfg<EPI_W8A8, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
 template <> struct EpiCfg<EPI_W8A8, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
 
@@ -213,34 +213,42 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU_BWD) {
-    // accumulator = dh; read the saved e, u for this thread's row and form de, du
+    // accumulator = dh; read the saved e, u for this thread's row and form de, du.  The e, u
+    // values of the next 32-column slice are loaded while the current one is being processed.
     const int grow = row0 + lane;
+    uint32_t ev[16], uv[16], en[16], un[16];
+    auto load_eu = [&](int slice, uint32_t* e_, uint32_t* u_) {
+      const int col = n0 + slice * 32;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int cc = col + 8 * g;
+        if (grow < p.M && cc < p.N) {
+          const uint4 a = *reinterpret_cast<const uint4*>(p.e_in + (size_t)grow * p.ld_eu + cc);
+          const uint4 b = *reinterpret_cast<const uint4*>(p.u_in + (size_t)grow * p.ld_eu + cc);
+          e_[4 * g] = a.x; e_[4 * g + 1] = a.y; e_[4 * g + 2] = a.z; e_[4 * g + 3] = a.w;
+          u_[4 * g] = b.x; u_[4 * g + 1] = b.y; u_[4 * g + 2] = b.z; u_[4 * g + 3] = b.w;
+        } else {
+#pragma unroll
+          for (int z = 0; z < 4; ++z) e_[4 * g + z] = u_[4 * g + z] = 0u;
+        }
+      }
+    };
+    load_eu(0, ev, uv);
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c, ++chunk_ctr) {
-      uint8_t* sde = my_stg + (chunk_ctr & 1) * 8192;
+      // one staging pair per warp (it buys the GEMM a deeper operand ring): the previous chunk's
+      // stores must have read it before it is overwritten
+      uint8_t* sde = my_stg;
       uint8_t* sdu = sde + 4096;
-      if (lane == 0) tma_store_wait_read<1>();
+      if (lane == 0) tma_store_wait_read<0>();
       __syncwarp();
-#pragma unroll 1
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
+        const int slice = c * 2 + h;
+        if (slice + 1 < BN / 32) load_eu(slice + 1, en, un);
         uint32_t vd[32];
         tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, vd);
         tmem_ld_wait();
-        const int col = n0 + c * 64 + h * 32;
-        uint32_t ev[16], uv[16];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int cc = col + 8 * g;
-          if (grow < p.M && cc < p.N) {
-            const uint4 a = *reinterpret_cast<const uint4*>(p.e_in + (size_t)grow * p.ld_eu + cc);
-            const uint4 b = *reinterpret_cast<const uint4*>(p.u_in + (size_t)grow * p.ld_eu + cc);
-            ev[4 * g] = a.x; ev[4 * g + 1] = a.y; ev[4 * g + 2] = a.z; ev[4 * g + 3] = a.w;
-            uv[4 * g] = b.x; uv[4 * g + 1] = b.y; uv[4 * g + 2] = b.z; uv[4 * g + 3] = b.w;
-          } else {
-#pragma unroll
-            for (int z = 0; z < 4; ++z) ev[4 * g + z] = uv[4 * g + z] = 0u;
-          }
-        }
         uint32_t wde[16], wdu[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -259,6 +267,11 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
         }
         stage_row(sde, lane, wde, h * 4);
         stage_row(sdu, lane, wdu, h * 4);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          ev[j] = en[j];
+          uv[j] = un[j];
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
