@@ -1034,12 +1034,19 @@ static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStrea
   return cudaErrorInvalidValue;
 }
 
-// CTA-pair kernel unless LORA_GB300_GEMM_PAIR=0 (the one-CTA kernel is kept for comparison).
-static bool use_pair() { return env_int("LORA_GB300_GEMM_PAIR", 0) != 0; }
+// Kernel choice per mode: the CTA pair stages half of B per CTA, which leaves room for a deeper
+// operand ring; that pays off for the stacked gate/up forward (5 stages instead of 3 beside its
+// three output staging buffers) and nowhere else measurably.  LORA_GB300_GEMM_PAIR=0 / 1 forces
+// the one-CTA / pair kernel for every mode (W8A8 always runs one-CTA).
+static bool use_pair(int mode) {
+  const char* e = getenv("LORA_GB300_GEMM_PAIR");
+  if (e && *e) return atoi(e) != 0;
+  return mode == TC_SWIGLU_FWD;
+}
 
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   if (d.M <= 0 || d.N <= 0) return cudaSuccess;
-  const bool pair = use_pair() && d.mode != TC_W8A8;
+  const bool pair = use_pair(d.mode) && d.mode != TC_W8A8;
   TcParams p;
   memset(&p, 0, sizeof(p));
   const bool stacked = d.mode == TC_SWIGLU_FWD || d.mode == TC_W8A8;
