@@ -12,6 +12,9 @@ namespace lg {
 typedef __nv_bfloat16 bf16;
 
 int num_sms_current();
+// Fills *a with the programmatic-stream-serialization launch attribute and returns 1, or returns 0
+// when LORA_GB300_PDL=0.  Only kernels that call pdl_wait() before touching global memory use it.
+int pdl_attr(cudaLaunchAttribute* a);
 // 2-D bf16 tensor map over `outer` rows of `inner` contiguous elements (row stride `ld` elements),
 // box {box_inner, box_outer}, swizzle of 0 / 32 / 64 / 128 bytes; out-of-bounds elements read as zero.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,

@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();      // S and U may come from the previous kernel in the stream
+  if (threadIdx.x == 0) pdl_trigger();
 
   if (warp == 2 * C::NG) {
     // ---------------------------------------------------------------- TMA producer
@@ -204,9 +206,17 @@ static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
   else ok = ok && make_tmap_bf16(&P.tmU, d.U, (uint64_t)d.K, R, (uint64_t)d.ldu, rp::BK, R, 128);
   if (!ok) return cudaErrorInvalidValue;
   const int64_t grid = (d.rows + rp::BMR - 1) / rp::BMR;
-  k<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(P);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, P);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t rowproj(const RowProjDesc& d, cudaStream_t st) {
@@ -287,6 +297,8 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();      // S, T and Y may come from the previous kernel in the stream
+  if (threadIdx.x == 0) pdl_trigger();
 
   if (warp == 4) {
     // ---------------------------------------------------------------- TMA producer
@@ -444,9 +456,17 @@ static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
     ok = ok && make_tmap_bf16(&P.tmY, d.Y, (uint64_t)d.K, (uint64_t)d.rows, (uint64_t)d.ldy, cr::BKC, cr::BR, 128);
   if (!ok) return cudaErrorInvalidValue;
   dim3 grid((unsigned)((d.K + cr::BKC - 1) / cr::BKC), (unsigned)d.splits);
-  k<<<grid, 160, C::SMEM, st>>>(P);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(160, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, P);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st) {

@@ -346,6 +346,8 @@ struct FinBatch {
   int n = 0;
 };
 __global__ void finalize_batch_kernel(const __grid_constant__ FinBatch b) {
+  pdl_wait();      // the partials come from the previous kernels in the stream
+  if (threadIdx.x == 0) pdl_trigger();
   int j = 0;
   while (j + 1 < b.n && (int)blockIdx.x >= b.first[j + 1]) ++j;
   const FinJob& f = b.job[j];
@@ -375,9 +377,16 @@ cudaError_t finalize_batch(const FinJob* jobs, int n, cudaStream_t st) {
   b.first[n] = (int)blocks;
   b.n = n;
   if (blocks <= 0) return cudaSuccess;
-  finalize_batch_kernel<<<(unsigned)blocks, 256, 0, st>>>(b);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, finalize_batch_kernel, b);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ concat / zero

@@ -451,6 +451,8 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  pdl_wait();      // the operands may come from the previous kernel in the stream
+  if (threadIdx.x == 0) pdl_trigger();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -705,6 +707,8 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
   cluster_sync_all();   // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  pdl_wait();      // the operands may come from the previous kernel in the stream
+  if (threadIdx.x == 0) pdl_trigger();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
@@ -942,6 +946,20 @@ static int env_int(const char* name, int dflt) {
   return e ? atoi(e) : dflt;
 }
 
+// Programmatic dependent launch for the kernels of the hot path (all of them wait for their
+// predecessor before touching global memory); LORA_GB300_PDL=0 launches them plainly.
+int pdl_attr(cudaLaunchAttribute* a) {
+  static int on = -1;
+  if (on < 0) {
+    const char* e = getenv("LORA_GB300_PDL");
+    on = (e && *e) ? (atoi(e) != 0) : 1;
+  }
+  if (!on) return 0;
+  a->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a->val.programmaticStreamSerializationAllowed = 1;
+  return 1;
+}
+
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
 static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
   using L = Layout<EPI, false>;
@@ -957,9 +975,17 @@ static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
   const int cap = env_int("LORA_GB300_MAX_CTAS", 0);
   if (cap > 0 && cap < grid) grid = cap;
   if (grid > tiles) grid = tiles;
-  kern<<<grid, KSCALE ? 320 : 192, L::TOTAL, st>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(KSCALE ? 320 : 192, 1, 1);
+  cfg.dynamicSmemBytes = L::TOTAL;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
@@ -968,7 +994,7 @@ static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
   auto kern = tc_pair_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
   static int max_clusters = 0;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -1000,6 +1026,7 @@ static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
   if (cap > 0 && cap < clusters) clusters = cap;
   if (clusters > tiles) clusters = tiles;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.numAttrs += (unsigned)pdl_attr(&attr[cfg.numAttrs]);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
