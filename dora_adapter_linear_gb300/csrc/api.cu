@@ -511,7 +511,7 @@ static lora_status check_qkv_shape(const lora_qkv_shape* sh) {
     if (sh->n[l] <= 0) return LORA_ERR_INVALID_ARG;
     if (sh->n[l] % 8) return LORA_ERR_UNSUPPORTED;
   }
-  if (sh->d_in % 8 || sh->r % 8 || sh->L * sh->r > 64) return LORA_ERR_UNSUPPORTED;
+  if (sh->d_in % 8 || sh->r % 8 || sh->r > 64) return LORA_ERR_UNSUPPORTED;
   if (sh->M > (1LL << 31) - 1 || sh->d_in > (1LL << 31) - 1 || qkv_N(*sh) > (1LL << 31) - 1)
     return LORA_ERR_UNSUPPORTED;
   return LORA_OK;
@@ -708,6 +708,36 @@ static LeafPack leaf_pack(const lora_qkv_shape& sh, const lora_adapter* lv, bf16
   return p;
 }
 
+// Leaves are handled in groups of at most 64 adapter columns (the width of the rank-r kernels):
+// group g covers leaves [first, last) with columns [first r, last r) of Z, G and the partials.
+struct LeafGroups {
+  int n = 0;
+  int first[kMaxLeaves + 1] = {0, 0, 0, 0};
+};
+static LeafGroups leaf_groups(const lora_qkv_shape& sh) {
+  LeafGroups g;
+  const int per = (int)(64 / sh.r) > 0 ? (int)(64 / sh.r) : 1;
+  for (int l = 0; l < sh.L; l += per) g.first[g.n++] = l;
+  g.first[g.n] = (int)sh.L;
+  return g;
+}
+
+// Z[:, group] = X A_group^T for every group (one pass over X per group; one pass in all when
+// L r <= 64)
+static lora_status qkv_down(const lora_qkv_shape& sh, const void* X, const bf16* A_stack, bf16* Z, uint32_t* err,
+                            cudaStream_t st) {
+  const LeafGroups g = leaf_groups(sh);
+  const int r = (int)sh.r, R = (int)(sh.L * sh.r);
+  for (int i = 0; i < g.n; ++i) {
+    const int c0 = g.first[i] * r, Rg = (g.first[i + 1] - g.first[i]) * r;
+    RowProjDesc d = rp_desc(sh.M, sh.d_in, Rg, X, A_stack + (int64_t)c0 * sh.d_in, false, err);
+    d.out_a = Z + c0;
+    d.ldo = R;
+    CK(rowproj(d, st));
+  }
+  return LORA_OK;
+}
+
 lora_status lora_qkv_fwd(const lora_qkv_shape* sh, const void* X, const void* W0, const lora_adapter* leaves,
                          const void* bias, void* Y, void* Z_save, void* ws, size_t ws_bytes, void* stream) {
   lora_status e = check_qkv_shape(sh);
@@ -725,10 +755,8 @@ lora_status lora_qkv_fwd(const lora_qkv_shape* sh, const void* X, const void* W0
   const int R = (int)(sh->L * sh->r);
   CK(pack_leaves(leaf_pack(*sh, leaves, w.A_stack, w.B_blk), st));
   bf16* Z = Z_save ? static_cast<bf16*>(Z_save) : w.Z;
-  if (live || Z_save) {  // one pass over X for every leaf's down-projection
-    RowProjDesc d = rp_desc(M, in, R, X, w.A_stack, false, w.err);
-    d.out_a = Z;
-    CK(rowproj(d, st));
+  if (live || Z_save) {  // every leaf's down-projection (one pass over X when L r <= 64)
+    if ((e = qkv_down(*sh, X, w.A_stack, Z, w.err, st)) != LORA_OK) return e;
   }
   // the base product of all leaves and the block-diagonal rank-(L r) tail in one GEMM
   CK(tc_gemm(fwd_desc(M, N, in, X, W0, live ? Z : nullptr, w.B_blk, R, Y, static_cast<const bf16*>(bias), nullptr,
@@ -786,9 +814,7 @@ lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0
   CK(pack_leaves(leaf_pack(*sh, leaves, w.A_stack, w.B_blk), st));
   const bf16* Z = static_cast<const bf16*>(Z_saved);
   if (!Z) {
-    RowProjDesc d = rp_desc(M, in, R, X, w.A_stack, false, w.err);
-    d.out_a = w.Zrec;
-    CK(rowproj(d, st));
+    if ((e = qkv_down(*sh, X, w.A_stack, w.Zrec, w.err, st)) != LORA_OK) return e;
     Z = w.Zrec;
   }
   // dB partials of each leaf (its columns of dY against its block of Z) and dY column sums
@@ -798,16 +824,34 @@ lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0
     d.colsum = dbias ? w.csum[l] : nullptr;
     CK(colreduce(d, st));
   }
-  {  // [s_l dY_l B_l] for all leaves in one pass over dY (B_blk is block-diagonal)
+  if (R <= 64) {  // [s_l dY_l B_l] for all leaves in one pass over dY (B_blk is block-diagonal)
     RowProjDesc d = rp_desc(M, N, R, dY, w.B_blk, true, w.err);
     d.out_a = w.Gs;
     CK(rowproj(d, st));
+  } else {  // leaf by leaf over its own columns of dY: still one pass over dY in all
+    for (int l = 0; l < sh->L; ++l) {
+      RowProjDesc d = rp_desc(M, sh->n[l], r, dYb + row0[l], leaves[l].B, true, w.err);
+      d.lds = N;
+      d.out_b = w.Gs + l * r;
+      d.scale_b = leaves[l].s;
+      d.ldo = R;
+      CK(rowproj(d, st));
+    }
   }
   if (dX) CK(tc_gemm(dx_desc(M, in, N, dY, W0, w.Gs, w.A_stack, R, dX, nullptr, w.err), st));
-  CK(colreduce(cr_desc(M, in, R, X, w.Gs, R, w.PA, w.splitsA, w.err), st));
+  // X^T G partials per leaf group: group i's array [splitsA, in, R_i] starts at column offset c0
+  const LeafGroups grp = leaf_groups(*sh);
+  int grp_of[kMaxLeaves] = {0, 0, 0};
+  for (int i = 0; i < grp.n; ++i) {
+    const int c0 = grp.first[i] * r, Rg = (grp.first[i + 1] - grp.first[i]) * r;
+    CK(colreduce(cr_desc(M, in, Rg, X, w.Gs + c0, R, w.PA + (size_t)w.splitsA * in * c0, w.splitsA, w.err), st));
+    for (int l = grp.first[i]; l < grp.first[i + 1]; ++l) grp_of[l] = i;
+  }
   FinJob fin[2 * kMaxLeaves];
   for (int l = 0; l < sh->L; ++l) {
-    fin[2 * l] = fin_dA(r, in, Partial{w.PA, w.splitsA, R, l * r}, 1.f, leaves[l].A, dA[l]);
+    const int gi = grp_of[l], c0 = grp.first[gi] * r, Rg = (grp.first[gi + 1] - grp.first[gi]) * r;
+    fin[2 * l] = fin_dA(r, in, Partial{w.PA + (size_t)w.splitsA * in * c0, w.splitsA, Rg, l * r - c0}, 1.f,
+                        leaves[l].A, dA[l]);
     fin[2 * l + 1] = fin_dB(sh->n[l], r, Partial{w.PB[l], w.splitsB[l], r, 0}, leaves[l].s, leaves[l].B, dB[l]);
   }
   CK(finalize_batch(fin, 2 * sh->L, st));

@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
   const int lane = threadIdx.x & 31;
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
   const int nk0 = (p.K0 + BK - 1) / BK;
-  const int nk = nk0 + (HAS_TAIL ? 1 : 0);
+  const int nk = nk0 + (HAS_TAIL ? (p.K1 + BK - 1) / BK : 0);   // the rank-r tail may span several K-steps
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -495,15 +495,16 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
               tma_load_2d(b_dst, &p.tmB0, &full[stage], kx, n0);
             }
           } else {
-            tma_load_2d(a_dst, &p.tmA1, &full[stage], 0, m0);
+            const int kt = (ks - nk0) * BK;   // K offset inside the rank-r tail
+            tma_load_2d(a_dst, &p.tmA1, &full[stage], kt, m0);
             if (B1_MN) {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &p.tmB1, &full[stage], n0 + 64 * j, 0);
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &p.tmB1, &full[stage], n0 + 64 * j, kt);
             } else if (STACKED) {
-              tma_load_2d(b_dst, &p.tmB1, &full[stage], 0, n0);
-              if (EPI != EPI_W8A8) tma_load_2d(b_dst + BNB * 128, &p.tmB1b, &full[stage], p.tail_b1b_x, n0);
+              tma_load_2d(b_dst, &p.tmB1, &full[stage], kt, n0);
+              if (EPI != EPI_W8A8) tma_load_2d(b_dst + BNB * 128, &p.tmB1b, &full[stage], p.tail_b1b_x + kt, n0);
             } else {
-              tma_load_2d(b_dst, &p.tmB1, &full[stage], 0, n0);
+              tma_load_2d(b_dst, &p.tmB1, &full[stage], kt, n0);
             }
           }
           if (++stage == STAGES) {
@@ -552,14 +553,14 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + stage * A_STAGE_BYTES);
           const uint32_t b_base = smem_u32(sB + stage * L::B_STAGE_BYTES);
-          const int nsub = tail ? (p.K1 + 15) / 16 : BK / 16;
+          const int nsub = tail ? (min(p.K1 - (ks - nk0) * BK, BK) + 15) / 16 : BK / 16;
           const bool bmn = tail ? B1_MN : B0_MN;
           for (int kk = 0; kk < nsub; ++kk) {
             const uint64_t adesc = umma_smem_desc(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc = bmn ? umma_smem_desc(b_base + kk * 2048, 8192, 1024)
                                        : umma_smem_desc(b_base + kk * 32, 16, 1024);
             if (W8 && tail)
-              umma_bf16(d_tmem + 2 * (BN / 2), adesc, bdesc, idesc1, kk > 0 ? 1u : 0u);
+              umma_bf16(d_tmem + 2 * (BN / 2), adesc, bdesc, idesc1, (ks > nk0 || kk > 0) ? 1u : 0u);
             else
               umma_bf16(d_tmem, adesc, bdesc, tail ? idesc1 : idesc0, (ks > 0 || kk > 0) ? 1u : 0u);
           }
@@ -675,7 +676,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
   const int num_clusters = gridDim.x >> 1;
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;   // pair tiles (256 rows each)
   const int nk0 = (p.K0 + BK - 1) / BK;
-  const int nk = nk0 + (HAS_TAIL ? 1 : 0);
+  const int nk = nk0 + (HAS_TAIL ? (p.K1 + BK - 1) / BK : 0);   // the rank-r tail may span several K-steps
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -754,16 +755,17 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
               tma_load_2d_pair(b_dst, &p.tmB0, bar, kx, n0 + (int)rank * 128);
             }
           } else {
-            tma_load_2d_pair(a_dst, &p.tmA1, bar, 0, m0);
+            const int kt = (ks - nk0) * BK;   // K offset inside the rank-r tail
+            tma_load_2d_pair(a_dst, &p.tmA1, bar, kt, m0);
             if (B1_MN) {
 #pragma unroll
               for (int j = 0; j < 2; ++j)
-                tma_load_2d_pair(b_dst + j * 8192, &p.tmB1, bar, n0 + (int)rank * 128 + 64 * j, 0);
+                tma_load_2d_pair(b_dst + j * 8192, &p.tmB1, bar, n0 + (int)rank * 128 + 64 * j, kt);
             } else if (STACKED) {
-              if (rank == 0) tma_load_2d_pair(b_dst, &p.tmB1, bar, 0, n0);
-              else tma_load_2d_pair(b_dst, &p.tmB1b, bar, p.tail_b1b_x, n0);
+              if (rank == 0) tma_load_2d_pair(b_dst, &p.tmB1, bar, kt, n0);
+              else tma_load_2d_pair(b_dst, &p.tmB1b, bar, p.tail_b1b_x + kt, n0);
             } else {
-              tma_load_2d_pair(b_dst, &p.tmB1, bar, 0, n0 + (int)rank * 128);
+              tma_load_2d_pair(b_dst, &p.tmB1, bar, kt, n0 + (int)rank * 128);
             }
           }
           if (++stage == STAGES) {
@@ -803,7 +805,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + stage * A_STAGE_BYTES);
           const uint32_t b_base = smem_u32(sB + stage * L::B_STAGE_BYTES);
-          const int nsub = tail ? (p.K1 + 15) / 16 : BK / 16;
+          const int nsub = tail ? (min(p.K1 - (ks - nk0) * BK, BK) + 15) / 16 : BK / 16;
           const bool bmn = tail ? B1_MN : B0_MN;
           for (int kk = 0; kk < nsub; ++kk) {
             const uint64_t adesc = umma_smem_desc(a_base + kk * 32, 16, 1024);

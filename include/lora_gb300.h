@@ -94,7 +94,8 @@ typedef struct {
 
 /* Fused projection whose N = n[0] + .. + n[L-1] output columns split into L leaves (the
  * query / key / value heads of an attention block), each leaf with its own rank-r adapter.
- * L in 1..3; L * r <= 64 and r a multiple of 8; every n[l] a positive multiple of 8
+ * L in 1..3; r a multiple of 8, at most 64 (when L * r > 64 the leaves are processed in groups of
+ * at most 64 adapter columns, one extra pass over X per extra group); every n[l] a positive multiple of 8
  * (entries past L ignored); d_in a multiple of 8. */
 typedef struct {
     int64_t M, d_in;

@@ -101,7 +101,9 @@ def test_qkv_validation(lib):
     ok = L.qkv_shape(64, 256, [256, 64, 64], 16)
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, ok) > 0
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_BWD, ok) > 0
-    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 64, 64], 32)) == 0  # L r > 64
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 64, 64], 32)) > 0   # L r = 96
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 64, 64], 72)) == 0  # r > 64
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 64, 64], 12)) == 0  # r % 8
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 60], 16)) == 0      # n % 8
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 0], 16)) == 0       # empty leaf
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256], 16, L.LORA_F32)) == 0

@@ -100,3 +100,23 @@ def test_mlp_swiglu(ops, variant, I, monkeypatch):
     for k in ("dX", "dAg", "dBu", "dAd"):
         assert_close(gr[k], ref[k], "bf16", k)
     _ws_ok(ops)
+
+
+def test_qkv_multistep_tail(ops, variant, monkeypatch):
+    """L r = 96: the rank-r tail of both GEMMs spans two K-steps (leaves in two groups)."""
+    monkeypatch.setenv("LORA_GB300_MAX_CTAS", "4")
+    case = D.scaled(D.WORKLOADS["qkv_lora_4096_gqa_bf16"], M=300, d_in=200, n=(256, 72, 72), r=32)
+    t = D.make_qkv(case)
+    g = {k: None if v is None else v.to(DEV) for k, v in t.items()}
+    lg_ = [(g[f"A{l}"], g[f"B{l}"], case.s[l]) for l in range(3)]
+    l64 = [(f64(t[f"A{l}"]), f64(t[f"B{l}"]), case.s[l]) for l in range(3)]
+    Y, Z = ops.lora_qkv_fwd(g["X"], g["W0"], lg_)
+    X, W0, dY = f64(t["X"]), f64(t["W0"]), f64(t["dY"])
+    assert_close(Y, O.qkv_lora_fwd(X, W0, l64), "bf16", "Y")
+    dX, dA, dB, _ = ops.lora_qkv_bwd(g["X"], g["W0"], lg_, Z, g["dY"])
+    rX, rA, rB, _ = O.qkv_lora_bwd(X, W0, l64, dY)
+    assert_close(dX, rX, "bf16", "dX")
+    for i in range(3):
+        assert_close(dA[i], rA[i], "bf16", f"dA{i}")
+        assert_close(dB[i], rB[i], "bf16", f"dB{i}")
+    _ws_ok(ops)

@@ -255,7 +255,8 @@ def qkv_inputs(**kw):
 
 
 @pytest.mark.parametrize("n,r,bias", [((256, 72, 72), 16, True), ((256, 72, 72), 8, False),
-                                      ((136, 264), 32, False), ((200,), 64, True)])
+                                      ((136, 264), 32, False), ((200,), 64, True),
+                                      ((256, 72, 72), 32, True), ((128, 64, 64), 64, False)])
 def test_qkv_fwd_bwd(ops, n, r, bias):
     case, t, g, lg_, l64 = qkv_inputs(M=300, d_in=200, n=n, r=r, bias=bias)
     Y, Z = ops.lora_qkv_fwd(g["X"], g["W0"], lg_, g["bias"])
