@@ -491,7 +491,7 @@ static lora_status check_mlp_shape(const lora_mlp_shape* sh) {
   if (sh->M < 0 || sh->H <= 0 || sh->I <= 0 || sh->r <= 0) return LORA_ERR_INVALID_ARG;
   if (sh->dtype != LORA_BF16) return sh->dtype == LORA_F32 ? LORA_ERR_UNSUPPORTED : LORA_ERR_INVALID_ARG;
   if (sh->act != LORA_ACT_SWIGLU && sh->act != LORA_ACT_GEGLU) return LORA_ERR_INVALID_ARG;
-  if (sh->H % 8 || sh->I % 8 || sh->r % 8 || sh->r > 32) return LORA_ERR_UNSUPPORTED;
+  if (sh->H % 8 || sh->I % 8 || sh->r % 8 || sh->r > 64) return LORA_ERR_UNSUPPORTED;
   if (sh->M > (1LL << 31) - 1 || 2 * mlp_ipad(*sh) > (1LL << 31) - 1) return LORA_ERR_UNSUPPORTED;
   return LORA_OK;
 }
@@ -1247,7 +1247,7 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
   const int64_t M = sh->M, H = sh->H, I = sh->I;
   const int r = (int)sh->r;
   CK(concat_rows_bf16(static_cast<const bf16*>(gate->A), r, static_cast<const bf16*>(up->A), r, H, w.Agu, st));
-  {  // [Zg | Zu] = X [Ag ; Au]^T, saved unscaled and scaled per half
+  if (2 * r <= 64) {  // [Zg | Zu] = X [Ag ; Au]^T in one pass, saved unscaled and scaled per half
     RowProjDesc d = rp_desc(M, H, 2 * r, X, w.Agu, false, w.err);
     d.out_a = static_cast<bf16*>(Zgu_save);
     d.out_b = w.Zgus;
@@ -1255,6 +1255,16 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
     d.split_col = r;
     d.scale_b_hi = up->s;
     CK(rowproj(d, st));
+  } else {  // ranks above 32: one pass per half (the rank-r kernels take at most 64 columns)
+    const lora_proj* pr[2] = {gate, up};
+    for (int h = 0; h < 2; ++h) {
+      RowProjDesc d = rp_desc(M, H, r, X, pr[h]->A, false, w.err);
+      d.out_a = static_cast<bf16*>(Zgu_save) + h * r;
+      d.out_b = w.Zgus + h * r;
+      d.scale_b = pr[h]->s;
+      d.ldo = 2 * r;
+      CK(rowproj(d, st));
+    }
   }
   {  // e, u, h = gate/up GEMM with both adapters, SwiGLU epilogue
     TcGemmDesc d;
@@ -1421,9 +1431,19 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     d.timeout_ns = wait_timeout_ns();
     CK(tc_gemm(d, st));
   }
-  CK(colreduce(cr_desc(M, H, 2 * r, X, w.Ggus, 2 * r, w.PAgu, w.sAgu, w.err), st));  // X^T [sg Gg | su Gu]
-  const FinJob fin[6] = {fin_dA(r, H, Partial{w.PAgu, w.sAgu, 2 * r, 0}, 1.f, nullptr, dAg),
-                         fin_dA(r, H, Partial{w.PAgu, w.sAgu, 2 * r, r}, 1.f, nullptr, dAu),
+  // X^T [sg Gg | su Gu]: one pass for ranks up to 32, one pass per half above
+  Partial pag{w.PAgu, w.sAgu, 2 * r, 0}, pau{w.PAgu, w.sAgu, 2 * r, r};
+  if (2 * r <= 64) {
+    CK(colreduce(cr_desc(M, H, 2 * r, X, w.Ggus, 2 * r, w.PAgu, w.sAgu, w.err), st));
+  } else {
+    float* half2 = w.PAgu + (size_t)w.sAgu * H * r;
+    CK(colreduce(cr_desc(M, H, r, X, w.Ggus, 2 * r, w.PAgu, w.sAgu, w.err), st));
+    CK(colreduce(cr_desc(M, H, r, X, w.Ggus + r, 2 * r, half2, w.sAgu, w.err), st));
+    pag = Partial{w.PAgu, w.sAgu, r, 0};
+    pau = Partial{half2, w.sAgu, r, 0};
+  }
+  const FinJob fin[6] = {fin_dA(r, H, pag, 1.f, nullptr, dAg),
+                         fin_dA(r, H, pau, 1.f, nullptr, dAu),
                          fin_dA(r, I, Partial{w.PAd, w.sAd, r, 0}, 1.f, nullptr, dAd),
                          fin_dB(H, r, Partial{w.PBd, w.sBd, r, 0}, down->s, nullptr, dBd),
                          fin_dB(I, r, Partial{w.PBg, w.sBg, r, 0}, gate->s, nullptr, dBg),

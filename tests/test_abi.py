@@ -49,7 +49,8 @@ def test_workspace_bytes_rejects_bad_shapes(lib):
     assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 8, 7)) == 0             # dtype
     assert L.lora_workspace_bytes(99, L.shape(64, 256, 256, 8, L.LORA_F32)) == 0
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16)) > 0
-    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 40)) == 0          # r > 32
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 40)) > 0           # r 33..64
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 72)) == 0          # r > 64
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, L.LORA_F32)) == 0
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, act=L.LORA_ACT_GEGLU)) > 0
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, act=2)) == 0         # unknown act

@@ -302,6 +302,21 @@ def test_qkv_m_zero_is_noop(ops):
     assert all(not a.any() for a in dA + dB) and not db.any()
 
 
+@pytest.mark.parametrize("r", [48, 64])
+def test_mlp_large_rank(ops, r):
+    """Ranks above 32: one rank-r pass per gate/up half and a tail of several K-steps."""
+    case, t, g, P = mlp_inputs(M=260, H=136, I=200, r=r, alpha=2.0 * r)
+    Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
+    args = _mlp_args64(t, case.s)
+    ry, re, ru, rh = O.mlp_swiglu_fwd(*args)
+    for got, ref, nm in ((saved["e"], re, "e"), (saved["u"], ru, "u"), (saved["h"], rh, "h"), (Y, ry, "y")):
+        assert_close(got, ref, "bf16", nm)
+    gr = ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
+    ref = O.mlp_swiglu_bwd(*args, f64(t["dY"]))
+    for k in ("dX", "dAg", "dBg", "dAu", "dBu", "dAd", "dBd"):
+        assert_close(gr[k], ref[k], "bf16", k)
+
+
 # ---------------------------------------------------------------------------- W8A8
 def w8_inputs(**kw):
     case = D.scaled(D.WORKLOADS["w8a8_lora_3072"], **kw)
