@@ -1477,7 +1477,9 @@ constexpr int64_t kW8ExactMaxK = 8800;
 
 size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out) {
   if (M < 0 || d_in <= 0 || d_out <= 0) return 0;
-  return kErrBytes + al256((size_t)M * d_in * 2) + 2 * al256((size_t)d_out * d_in * 2);
+  // + the rank-r operands of the fused epilogue, pre-divided by the dequant scales (r <= 64)
+  return kErrBytes + al256((size_t)M * d_in * 2) + 2 * al256((size_t)d_out * d_in * 2) +
+         al256((size_t)M * 64 * 2) + al256((size_t)d_out * 64 * 2);
 }
 
 lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq, const float* sx,
@@ -1509,6 +1511,47 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
   CK(i8_to_bf16(Xq, M * d_in, Xb, st));
   CK(i8_split_bf16(Wq, d_out * d_in, Wh, Wl, st));
   TcGemmDesc d;
+  if (acc_out == nullptr && !env_flag("LORA_GB300_W8A8_EXACT")) {
+    // Only the dequantised output is wanted: fold the rank-r term into the low half as
+    // (s Z / sx) (B / sw)^T, so the epilogue is y = (16 hi + lo) sx sw + bias and the accumulators
+    // fit twice in TMEM (double-buffered, like every other mode).  The low half then holds the
+    // exact integer partial sum plus that term, rounded once in fp32.
+    bf16* Zt = c.take<bf16>((size_t)M * 64);
+    bf16* Bt = c.take<bf16>((size_t)d_out * 64);
+    d.mode = TC_W8A8F;
+    d.M = (int)M;
+    d.N = (int)d_out;
+    d.K0 = (int)d_in;
+    d.A0 = Xb;
+    d.lda0 = d_in;
+    d.B0 = Wh;
+    d.B0b = Wl;
+    d.ldb0 = d_in;
+    d.out[0] = Y;
+    d.ldo = d_out;
+    d.bias = static_cast<const bf16*>(bias);
+    d.sx = sx;
+    d.sw = sw;
+    if (Z && s != 0.f) {
+      CK(scale_rows_recip_bf16(static_cast<const bf16*>(Z), M, (int)r, sx, s, Zt, st));
+      CK(scale_rows_recip_bf16(static_cast<const bf16*>(B), d_out, (int)r, sw, 1.f, Bt, st));
+      d.has_tail = true;
+      d.A1 = Zt;
+      d.lda1 = r;
+      d.K1 = (int)r;
+      d.K1_a = (int)r;
+      d.B1 = Bt;          // first (high) half: read past its r columns, i.e. zeros
+      d.B1b = Bt;         // second (low) half
+      d.ldb1 = r;
+      d.K1_b = (int)r;
+      d.b1_x = 64;
+      d.b1b_x = 0;
+    }
+    d.err = err;
+    d.timeout_ns = wait_timeout_ns();
+    CK(tc_gemm(d, st));
+    return LORA_OK;
+  }
   d.mode = TC_W8A8;
   d.M = (int)M;
   d.N = (int)d_out;

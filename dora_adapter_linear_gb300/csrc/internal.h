@@ -29,14 +29,16 @@ void prof_mark(cudaStream_t st, bool start, double flops);
 cudaError_t prof_collect(double* ms, int64_t* launches, double* flops, bool reset);
 
 // ------------------------------------------------------------------ tcgen05 GEMM engine
-enum EpiKind { EPI_SCALE_BIAS = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2, EPI_W8A8 = 3 };
+enum EpiKind { EPI_SCALE_BIAS = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2, EPI_W8A8 = 3, EPI_W8A8F = 4 };
 enum TcMode {
   TC_FWD = 0,          // A0 [M,K0] x B0 [N,K0]^T (+ A1 [M,K1] x B1 [N,K1]^T), epilogue scale/bias
   TC_BWD_DX = 1,       // A0 [M,K0] x B0 [K0,N] (MN-major) (+ A1 x B1 [K1,N]), optional A-scale along K
   TC_SWIGLU_FWD = 2,   // stacked gate/up weights, SwiGLU epilogue writing e, u, h
   TC_SWIGLU_BWD = 3,   // MN-major B, epilogue forms de, du from saved e, u
-  TC_W8A8 = 4          // stacked [wh; wl] weight halves, epilogue forms the exact int32 product,
+  TC_W8A8 = 4,         // stacked [wh; wl] weight halves, epilogue forms the exact int32 product,
                        // dequantises and adds the rank-r term
+  TC_W8A8F = 5         // the same product with the rank-r term pre-divided by the dequant scales
+                       // and accumulated into the low half (double-buffered; no int32 output)
 };
 
 struct TcGemmDesc {
@@ -57,6 +59,7 @@ struct TcGemmDesc {
   int64_t ldb1 = 0;
   int K1_b = 0;                // columns of a K-major B1 tensor
   int b1b_x = 0;
+  int b1_x = 0;                // stacked tail: x coordinate of the first half (past the tensor = zeros)
   void* out[3] = {nullptr, nullptr, nullptr};
   int64_t ldo = 0;
   const float* col_scale = nullptr;
@@ -226,6 +229,9 @@ cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float*
 cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int64_t rows2, int64_t cols, bf16* dst,
                              cudaStream_t st);
 cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st);
+// out[o, j] = bf16(f * in[o, j] / d[o]) for in [rows, r] (a zero d[o] counts as 1)
+cudaError_t scale_rows_recip_bf16(const bf16* in, int64_t rows, int r, const float* d, float f, bf16* out,
+                                  cudaStream_t st);
 // DoRA column variant (bf16): c0 = colsum(W^2); the closed-form column norm n, c = m / n and
 // A_c = A diag(c); out = A diag(w); K = A diag(w) A^T; and the dA assembly
 //   dA[j, k] = c[k] sum_s PA[s][k][j] + 2 s g[k] U[k, j] + 2 s^2 g[k] (Kb A)[j, k].

@@ -568,6 +568,21 @@ cudaError_t finalize_dA_cols(int r, int64_t in, Partial PA, const float* c, cons
   return cudaGetLastError();
 }
 
+__global__ void scale_rows_recip_kernel(const bf16* in, int64_t rows, int r, const float* d, float f, bf16* out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= rows * r) return;
+  const float dv = d[i / r];
+  out[i] = __float2bfloat16_rn(f * __bfloat162float(in[i]) / (dv != 0.f ? dv : 1.f));
+}
+cudaError_t scale_rows_recip_bf16(const bf16* in, int64_t rows, int r, const float* d, float f, bf16* out,
+                                  cudaStream_t st) {
+  const int64_t n = rows * r;
+  if (n <= 0) return cudaSuccess;
+  scale_rows_recip_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(in, rows, r, d, f, out);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st) {
   if (bytes == 0) return cudaSuccess;
   return cudaMemsetAsync(p, 0, bytes, st);

@@ -37,6 +37,7 @@ struct TcParams {
   int num_m_tiles, num_n_tiles, group_m;
   int k0_split_steps;   // MN-major B0: k-steps taken from tmB0 before switching to tmB0b
   int tail_b1b_x;       // stacked tail: x coordinate (K shift) of the second half
+  int tail_b1_x;        // stacked tail: x coordinate of the first half
   const float* col_scale;
   const bf16* bias;
   const float* a_kscale;
@@ -72,6 +73,8 @@ template <> struct EpiCfg<EPI_SWIGLU, true> { static constexpr int STAGES = 5, S
 template <> struct EpiCfg<EPI_SWIGLU_BWD, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
 template <> struct EpiCfg<EPI_W8A8, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
 template <> struct EpiCfg<EPI_W8A8, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
+template <> struct EpiCfg<EPI_W8A8F, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
+template <> struct EpiCfg<EPI_W8A8F, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
 
 template <int EPI, bool PAIR>
 struct Layout {
@@ -278,6 +281,52 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
       if (lane == 0) {
         tma_store_2d(&p.tmOut[0], sde, n0 + c * 64, row0);
         tma_store_2d(&p.tmOut[1], sdu, n0 + c * 64, row0);
+        tma_store_commit();
+      }
+    }
+  } else if constexpr (EPI == EPI_W8A8F) {
+    // accumulator columns [0, 128) = X wh^T, [128, 256) = X wl^T + s Z B^T / (sx sw) for outputs
+    // n0 .. n0 + 127: y = (16 hi + lo) sx sw (+ bias), with a zero scale read as 1 (its row or
+    // column of the integer product is zero then, and the rank-r term was divided by 1)
+    const int grow = row0 + lane;
+    float rs = grow < p.M ? p.sx[grow] : 0.f;
+    rs = rs != 0.f ? rs : 1.f;
+#pragma unroll 1
+    for (int c = 0; c < N_OUT / 64; ++c, ++chunk_ctr) {
+      uint8_t* stg = my_stg + (chunk_ctr & 1) * 4096;
+      if (lane == 0) tma_store_wait_read<1>();
+      __syncwarp();
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t vh[32], vl[32];
+        tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, vh);
+        tmem_ld_32x32b_x32(t_row + BN / 2 + c * 64 + h * 32, vl);
+        tmem_ld_wait();
+        const int col0 = n0 + c * 64 + h * 32;
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float y2[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int col = col0 + j + k;
+            float y = 0.f;
+            if (col < p.N) {
+              float cs = __ldg(p.sw + col);
+              cs = cs != 0.f ? cs : 1.f;
+              y = fmaf(16.f, u2f(vh[j + k]), u2f(vl[j + k])) * rs * cs;
+              if (p.bias != nullptr) y += __bfloat162float(p.bias[col]);
+            }
+            y2[k] = y;
+          }
+          w[j / 2] = pack_bf16x2(y2[0], y2[1]);
+        }
+        stage_row(stg, lane, w, h * 4);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tmOut[0], stg, n0 + c * 64, row0);
         tma_store_commit();
       }
     }
@@ -501,7 +550,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &p.tmB1, &full[stage], n0 + 64 * j, kt);
             } else if (STACKED) {
-              tma_load_2d(b_dst, &p.tmB1, &full[stage], kt, n0);
+              tma_load_2d(b_dst, &p.tmB1, &full[stage], p.tail_b1_x + kt, n0);
               if (EPI != EPI_W8A8) tma_load_2d(b_dst + BNB * 128, &p.tmB1b, &full[stage], p.tail_b1b_x + kt, n0);
             } else {
               tma_load_2d(b_dst, &p.tmB1, &full[stage], kt, n0);
@@ -762,7 +811,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
               for (int j = 0; j < 2; ++j)
                 tma_load_2d_pair(b_dst + j * 8192, &p.tmB1, bar, n0 + (int)rank * 128 + 64 * j, kt);
             } else if (STACKED) {
-              if (rank == 0) tma_load_2d_pair(b_dst, &p.tmB1, bar, kt, n0);
+              if (rank == 0) tma_load_2d_pair(b_dst, &p.tmB1, bar, p.tail_b1_x + kt, n0);
               else tma_load_2d_pair(b_dst, &p.tmB1b, bar, p.tail_b1b_x + kt, n0);
             } else {
               tma_load_2d_pair(b_dst, &p.tmB1, bar, kt, n0 + (int)rank * 128);
@@ -1056,6 +1105,9 @@ static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStrea
       return launch_variant<false, true, true, false, EPI_SWIGLU, false>(p, st, pair, tiles);
     case TC_SWIGLU_BWD:
       return launch_variant<true, false, true, true, EPI_SWIGLU_BWD, false>(p, st, pair, tiles);
+    case TC_W8A8F:
+      if (d.has_tail) return launch_variant<false, true, true, false, EPI_W8A8F, false>(p, st, pair, tiles);
+      return launch_variant<false, true, false, false, EPI_W8A8F, false>(p, st, pair, tiles);
     case TC_W8A8:  // one-CTA kernel only (its accumulator layout is per-CTA)
       if (d.has_tail) return launch_one<false, true, true, false, EPI_W8A8, false>(p, st, tiles);
       return launch_one<false, true, false, false, EPI_W8A8, false>(p, st, tiles);
@@ -1070,7 +1122,7 @@ static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStrea
 static bool use_pair(int mode) {
   const char* e = getenv("LORA_GB300_GEMM_PAIR");
   if (e && *e) return atoi(e) != 0;
-  return mode == TC_SWIGLU_FWD;
+  return mode == TC_SWIGLU_FWD || mode == TC_W8A8F;
 }
 
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
@@ -1078,7 +1130,7 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   const bool pair = use_pair(d.mode) && d.mode != TC_W8A8;
   TcParams p;
   memset(&p, 0, sizeof(p));
-  const bool stacked = d.mode == TC_SWIGLU_FWD || d.mode == TC_W8A8;
+  const bool stacked = d.mode == TC_SWIGLU_FWD || d.mode == TC_W8A8 || d.mode == TC_W8A8F;
   // rows of a K-major B box: 256 (one CTA), 128 (stacked halves, or one CTA's half of a pair)
   const int bnb = (stacked || pair) ? BN / 2 : BN;
   bool ok = make_map(&p.tmA0, d.A0, d.K0, d.M, d.lda0, BM);
@@ -1123,6 +1175,7 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.group_m = pair ? 8 : 16;
   p.k0_split_steps = d.b0_mn && d.B0b ? (d.k0_split / BK) : (1 << 30);
   p.tail_b1b_x = d.b1b_x;
+  p.tail_b1_x = d.b1_x;
   p.col_scale = d.col_scale;
   p.bias = d.bias;
   p.a_kscale = d.a_kscale;

@@ -333,8 +333,9 @@ lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0
 lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t* Xq, float* sx,
                                const void* A, int64_t r, void* Z, void* stream);
 
-/* Bytes of workspace w8a8_lora_fwd needs: the error word plus the int8 codes re-laid out as
- * bf16 tensor-core operands (X: M x d_in; W split into two d_out x d_in halves).  0 on bad input. */
+/* Bytes of workspace w8a8_lora_fwd needs: the error word, the int8 codes re-laid out as bf16
+ * tensor-core operands (X: M x d_in; W split into two d_out x d_in halves) and the rank-r
+ * operands divided by the dequant scales (M x 64 and d_out x 64 bf16).  0 on bad input. */
 size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out);
 
 /* Y = float(acc) * sx[i] * sw[o] + s * (Z B^T)[i, o] (+ bias), acc = Xq Wq^T exact in int32.
@@ -351,6 +352,8 @@ size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out);
  *   w = 16 * (w >> 4) + (w & 15): both partial products accumulate integers below 2^24, so fp32
  *   accumulation is exact and the int32 result is bit-identical to an integer GEMM.  Larger
  *   d_in uses the warp-level integer MMA (sm_103a has no tcgen05 integer kind).
+ *   When acc_out is NULL the low-rank term enters the low partial sum as (s Z / sx)(B / sw)^T and
+ *   Y = (16 hi + lo) sx sw (+ bias): the same value up to one fp32 rounding of that sum.
  */
 lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq,
                           const float* sx, const int8_t* Wq, const float* sw, const void* Z,

@@ -363,6 +363,30 @@ def test_w8a8_both_product_paths(ops, path, monkeypatch):
     assert_close(Y, ry, "bf16", "Y")
 
 
+@pytest.mark.parametrize("bias,zero_rows", [(False, False), (True, True)])
+def test_w8a8_fused_output_path(ops, bias, zero_rows, monkeypatch):
+    """Output-only calls fold the rank-r term into the low accumulator half (pre-divided by the
+    dequant scales): same result as the exact-integer path and the oracle, including an all-zero
+    input row and an all-zero weight row (scale 0)."""
+    case, t, Wq, sw, Xq, sx = w8_inputs(M=300, d_in=352, d_out=264, bias=bias)
+    if zero_rows:
+        Xq[5] = 0
+        sx[5] = 0.0
+        Wq[9] = 0
+        sw[9] = 0.0
+    Z = (t["X"].double() @ t["A"].double().T).to(torch.bfloat16)
+    if zero_rows:
+        Z[5] = 0
+    args = (gpu(torch.from_numpy(Xq)), gpu(torch.from_numpy(sx)), gpu(torch.from_numpy(Wq)),
+            gpu(torch.from_numpy(sw)), gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]))
+    Y, _ = ops.w8a8_lora_fwd(*args)
+    ry, _ = O.w8a8_lora_fwd(Xq, sx, Wq, sw, f64(Z), f64(t["B"]), case.s, f64(t["bias"]))
+    assert_close(Y, ry, "bf16", "Y")
+    monkeypatch.setenv("LORA_GB300_W8A8_EXACT", "1")
+    Ye, _ = ops.w8a8_lora_fwd(*args)
+    assert_close(Y, f64(Ye.cpu()), "bf16", "fused vs exact path")
+
+
 def test_w8a8_deep_k_uses_integer_path(ops):
     """d_in above the exact-split bound (8800) runs the integer MMA; still bit-exact."""
     rng = np.random.default_rng(5)
