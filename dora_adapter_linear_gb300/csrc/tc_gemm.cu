@@ -142,9 +142,13 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
                                               uint8_t* my_stg, uint32_t& chunk_ctr) {
   if constexpr (EPI == EPI_SCALE_BIAS) {
 #pragma unroll 1
-    for (int c = 0; c < BN / 64; ++c, ++chunk_ctr) {
-      uint8_t* stg = my_stg + (chunk_ctr & 1) * 4096;
-      if (lane == 0) tma_store_wait_read<1>();
+    for (int c = 0; c < N_OUT / 64; ++c, ++chunk_ctr) {
+      // a whole-tile epilogue warp double-buffers its staging; a half-tile one has a single buffer
+      uint8_t* stg = my_stg + (N_OUT == BN ? (chunk_ctr & 1) * 4096 : 0);
+      if (lane == 0) {
+        if (N_OUT == BN) tma_store_wait_read<1>();
+        else tma_store_wait_read<0>();
+      }
       __syncwarp();
       uint32_t v[32];
       uint32_t w[32];
@@ -441,8 +445,18 @@ __device__ __forceinline__ void kscale_tile(uint8_t* a, const KScales& ks8, int 
 }
 
 // ============================================================================ 1-CTA kernel
+// Threads of the one-CTA kernel: producer, MMA and 4 epilogue warps; 4 more warps either scale
+// A tiles (K-scaling) or, for the plain scale/bias epilogue, drain the second half of each
+// accumulator (8 epilogue warps, two per TMEM lane quarter, finish a tile's epilogue in half
+// the time).
+template <int EPI, bool KSCALE>
+struct OneCta {
+  static constexpr bool EPI8 = EPI == EPI_SCALE_BIAS && !KSCALE;
+  static constexpr int THREADS = (KSCALE || EPI8) ? 320 : 192;
+};
+
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
-__global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using L = Layout<EPI, false>;
   constexpr int STAGES = L::STAGES;
   constexpr int BNB = STACKED ? BN / 2 : BN;          // rows per K-major B box
@@ -478,7 +492,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], OneCta<EPI, KSCALE>::EPI8 ? 8 : 4);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -627,10 +641,12 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
       mbar_wait_drain(drain, 0, 20000000ull);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < (OneCta<EPI, KSCALE>::EPI8 ? 10 : 6)) {
     // ---------------------------------------------------------------- epilogue
+    constexpr bool EPI8 = OneCta<EPI, KSCALE>::EPI8;
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    uint8_t* my_stg = sStg + (warp - 2) * (EpiCfg<EPI, false>::STG_BUFS * 4096);
+    const int half = EPI8 ? (warp - 2) >> 2 : 0;   // with 8 warps: which half of the columns
+    uint8_t* my_stg = sStg + (warp - 2) * (EPI8 ? 4096 : EpiCfg<EPI, false>::STG_BUFS * 4096);
     int it = 0;
     uint32_t chunk_ctr = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
@@ -640,8 +656,12 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_gemm_kernel(const __
       tc_fence_after();
       int mt, nt;
       tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
-      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + buf * BN;
-      epilogue_tile<EPI, N_OUT>(p, t_row, mt * BM + 32 * q, nt * N_OUT, lane, my_stg, chunk_ctr);
+      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + buf * BN + half * (N_OUT / 2);
+      if constexpr (EPI8)
+        epilogue_tile<EPI, N_OUT / 2>(p, t_row, mt * BM + 32 * q, nt * N_OUT + half * (N_OUT / 2), lane, my_stg,
+                                      chunk_ctr);
+      else
+        epilogue_tile<EPI, N_OUT>(p, t_row, mt * BM + 32 * q, nt * N_OUT, lane, my_stg, chunk_ctr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -1029,7 +1049,7 @@ static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(KSCALE ? 320 : 192, 1, 1);
+  cfg.blockDim = dim3(OneCta<EPI, KSCALE>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = L::TOTAL;
   cfg.stream = st;
   cfg.attrs = attr;
