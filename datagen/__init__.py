@@ -13,6 +13,7 @@ the rounded values upcast to fp64):
 * DoRA magnitude m = rownorm(W0) * U(0.9, 1.1) (column variant: colnorm(W0) *
   U(0.9, 1.1), one entry per input feature) -- the workload's own recipe for the
   magnitude vector; it is an input, not part of the forward pass
+* dropout keep mask: uint8, 1 with probability 1 - p, drawn as U(0, 1) >= p with its own seed
 * W8A8: X and W0 are drawn as above and left unquantised; quantisation is part
   of the method and lives on each side separately.
 
@@ -27,7 +28,7 @@ from dataclasses import dataclass, field
 import torch
 
 __all__ = ["LinearCase", "MlpCase", "W8A8Case", "QkvCase", "WORKLOADS", "make_linear", "make_mlp",
-           "make_w8a8", "make_qkv", "scaled"]
+           "make_w8a8", "make_qkv", "make_dropout_mask", "scaled"]
 
 
 @dataclass(frozen=True)
@@ -193,3 +194,9 @@ def make_qkv(case: QkvCase):
     out["bias"] = _normal(g, (N,), 0.01).to(dt) if case.bias else None
     out["dY"] = _normal(g, (case.M, N), 1.0).to(dt)
     return out
+
+
+def make_dropout_mask(M: int, d_in: int, p: float, seed: int = 2001):
+    """uint8 [M, d_in] keep mask (1 = kept), each entry kept with probability 1 - p."""
+    g = torch.Generator().manual_seed(seed)
+    return (torch.rand(M, d_in, generator=g, dtype=torch.float32) >= p).to(torch.uint8)

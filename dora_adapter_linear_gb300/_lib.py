@@ -17,7 +17,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "lora_gb300.h")
 LORA_F32, LORA_BF16 = 0, 1
 LORA_NOALLOC_SCRATCH_BYTES = 4 << 20   # fixed scratch of lora_linear_fwd_noalloc (header macro)
 (OP_LINEAR_FWD, OP_LINEAR_BWD, OP_DORA_FWD, OP_DORA_BWD, OP_MLP_FWD, OP_MLP_BWD, OP_QKV_FWD, OP_QKV_BWD,
- OP_DORA_COLS_FWD, OP_DORA_COLS_BWD) = range(10)
+ OP_DORA_COLS_FWD, OP_DORA_COLS_BWD, OP_DROPOUT_FWD, OP_DROPOUT_BWD) = range(12)
 STATUS = {0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_UNSUPPORTED", 3: "LORA_ERR_MISALIGNED",
           4: "LORA_ERR_WORKSPACE", 5: "LORA_ERR_CUDA", 6: "LORA_ERR_DEVICE_TIMEOUT"}
 
@@ -63,6 +63,10 @@ _SIGS = {
     "lora_check_device_error": (c_int, [P, P]),
     "lora_linear_fwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, c_float, P, P, P, c_size_t, P]),
     "lora_linear_bwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, P, c_float, P, P, P, P, P, c_size_t, P]),
+    "lora_linear_dropout_fwd": (c_int, [POINTER(LoraShape), P, P, c_float, P, P, P, P, c_float, P, P, P, c_size_t,
+                                        P]),
+    "lora_linear_dropout_bwd": (c_int, [POINTER(LoraShape), P, P, c_float, P, P, P, P, P, c_float, P, P, P, P, P,
+                                        c_size_t, P]),
     "dora_rownorm2": (c_int, [POINTER(LoraShape), P, P, P]),
     "dora_linear_fwd": (c_int, [POINTER(LoraShape), P, P, P, P, P, P, P, c_float, c_float, P, P, P, P, P,
                                 c_size_t, P]),
@@ -226,6 +230,20 @@ def lora_linear_fwd_noalloc(sh, X, W0, A, B, bias, s, Y, Z_save, stream=None):
     """lora_linear_fwd with the library's fixed device scratch instead of a workspace."""
     _ck(_lib().lora_linear_fwd_noalloc(ctypes.byref(sh), ptr(X), ptr(W0), ptr(A), ptr(B), ptr(bias), float(s),
                                        ptr(Y), ptr(Z_save), _stream(stream)), "lora_linear_fwd_noalloc")
+
+
+def lora_linear_dropout_fwd(sh, X, mask, keep_scale, W0, A, B, bias, s, Y, Z_save, ws, stream=None):
+    _ck(_lib().lora_linear_dropout_fwd(ctypes.byref(sh), ptr(X), ptr(mask), float(keep_scale), ptr(W0), ptr(A),
+                                       ptr(B), ptr(bias), float(s), ptr(Y), ptr(Z_save), ptr(ws),
+                                       0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+        "lora_linear_dropout_fwd")
+
+
+def lora_linear_dropout_bwd(sh, X, mask, keep_scale, W0, A, B, Z_saved, dY, s, dX, dA, dB, dbias, ws, stream=None):
+    _ck(_lib().lora_linear_dropout_bwd(ctypes.byref(sh), ptr(X), ptr(mask), float(keep_scale), ptr(W0), ptr(A),
+                                       ptr(B), ptr(Z_saved), ptr(dY), float(s), ptr(dX), ptr(dA), ptr(dB), ptr(dbias),
+                                       ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                       _stream(stream)), "lora_linear_dropout_bwd")
 
 
 def lora_linear_bwd(sh, X, W0, A, B, Z_saved, dY, s, dX, dA, dB, dbias, ws, stream=None):

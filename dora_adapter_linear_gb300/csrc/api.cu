@@ -467,7 +467,7 @@ const char* lora_status_string(int status) {
   return "unknown status";
 }
 
-int lora_abi_version(void) { return 5; }
+int lora_abi_version(void) { return 6; }
 
 size_t lora_workspace_bytes(int op, const lora_shape* sh) {
   if (check_shape(sh) != LORA_OK) return 0;
@@ -476,6 +476,12 @@ size_t lora_workspace_bytes(int op, const lora_shape* sh) {
     case LORA_OP_LINEAR_BWD: { LinBwdWs w; return plan_lin_bwd(*sh, nullptr, &w); }
     case LORA_OP_DORA_FWD: { DoraFwdWs w; return plan_dora_fwd(*sh, nullptr, &w); }
     case LORA_OP_DORA_BWD: { DoraBwdWs w; return plan_dora_bwd(*sh, nullptr, &w); }
+    case LORA_OP_DROPOUT_FWD:
+      if (sh->dtype != LORA_BF16) return 0;
+      { LinFwdWs w; return plan_lin_fwd(*sh, nullptr, &w) + al256((size_t)sh->M * sh->d_in * 2); }
+    case LORA_OP_DROPOUT_BWD:
+      if (sh->dtype != LORA_BF16) return 0;
+      { LinBwdWs w; return plan_lin_bwd(*sh, nullptr, &w) + al256((size_t)sh->M * sh->d_in * 2); }
     case LORA_OP_DORA_COLS_FWD:
       if (sh->dtype != LORA_BF16) return 0;
       { DoraColsFwdWs w; return plan_dora_cols_fwd(*sh, nullptr, &w); }
@@ -673,6 +679,101 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
     CK(sgemm_f32(sg(r, in, M, w.Gs, r, true, X, in, false, dA, in, s), st));            // dA = s G^T X
     CK(sgemm_f32(sg(out, r, M, dY, out, true, Z, r, false, dB, r, s), st));             // dB = s dY^T Z
   }
+  return LORA_OK;
+}
+
+// ------------------------------------------------------------------ LoRA with input dropout
+// The workspace is the plain layer's followed by Xd = X o mask * keep_scale [M, d_in].
+lora_status lora_linear_dropout_fwd(const lora_shape* sh, const void* X, const uint8_t* mask, float keep_scale,
+                                    const void* W0, const void* A, const void* B, const void* bias, float s,
+                                    void* Y, void* Z_save, void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  if (sh->dtype != LORA_BF16) return LORA_ERR_UNSUPPORTED;
+  REQM(sh->M, mask);
+  ALN(mask);
+  if (!isfinite(keep_scale) || keep_scale < 0.f) return LORA_ERR_INVALID_ARG;
+  LinFwdWs w;
+  const size_t lin = plan_lin_fwd(*sh, nullptr, &w);
+  if ((e = check_ws(ws, ws_bytes, lin + al256((size_t)sh->M * sh->d_in * 2))) != LORA_OK) return e;
+  if (s == 0.f && Z_save == nullptr)  // nothing of the adapter branch reaches Y: the plain layer
+    return lora_linear_fwd(sh, X, W0, A, B, bias, s, Y, nullptr, ws, lin, stream);
+  REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQM(sh->M, Y);
+  ALN(X); ALN(W0); ALN(A); ALN(B); ALN(bias); ALN(Y); ALN(Z_save);
+  if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
+  plan_lin_fwd(*sh, static_cast<char*>(ws), &w);
+  if (sh->M == 0) return LORA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
+  const int r = (int)sh->r;
+  bf16* Xd = reinterpret_cast<bf16*>(static_cast<char*>(ws) + lin);
+  CK(apply_mask_bf16(static_cast<const bf16*>(X), mask, keep_scale, M, in, Xd, st));
+  {  // Z = Xd A^T (saved unscaled) and s Z for the GEMM tail
+    RowProjDesc d = rp_desc(M, in, r, Xd, A, false, w.err);
+    d.out_a = static_cast<bf16*>(Z_save);
+    d.out_b = s != 0.f ? static_cast<bf16*>(w.Zs) : nullptr;
+    d.scale_b = s;
+    CK(rowproj(d, st));
+  }
+  // the base product reads the undropped X; the rank-r tail carries the dropped-out branch
+  CK(tc_gemm(fwd_desc(M, out, in, X, W0, s != 0.f ? w.Zs : nullptr, B, r, Y, static_cast<const bf16*>(bias),
+                      nullptr, w.err),
+             st));
+  return LORA_OK;
+}
+
+lora_status lora_linear_dropout_bwd(const lora_shape* sh, const void* X, const uint8_t* mask, float keep_scale,
+                                    const void* W0, const void* A, const void* B, const void* Z_saved,
+                                    const void* dY, float s, void* dX, void* dA, void* dB, void* dbias,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_shape(sh);
+  if (e != LORA_OK) return e;
+  if (sh->dtype != LORA_BF16) return LORA_ERR_UNSUPPORTED;
+  REQM(sh->M, mask);
+  ALN(mask);
+  if (!isfinite(keep_scale) || keep_scale < 0.f) return LORA_ERR_INVALID_ARG;
+  LinBwdWs w;
+  const size_t lin = plan_lin_bwd(*sh, nullptr, &w);
+  if ((e = check_ws(ws, ws_bytes, lin + al256((size_t)sh->M * sh->d_in * 2))) != LORA_OK) return e;
+  if (sh->M == 0 || s == 0.f)  // no adapter gradient flows: exactly the plain layer's backward
+    return lora_linear_bwd(sh, X, W0, A, B, Z_saved, dY, s, dX, dA, dB, dbias, ws, lin, stream);
+  REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQM(sh->M, dY); REQ(dA); REQ(dB);
+  ALN(X); ALN(W0); ALN(A); ALN(B); ALN(Z_saved); ALN(dY); ALN(dX); ALN(dA); ALN(dB); ALN(dbias);
+  if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
+  plan_lin_bwd(*sh, static_cast<char*>(ws), &w);
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
+  const int r = (int)sh->r;
+  bf16* Xd = reinterpret_cast<bf16*>(static_cast<char*>(ws) + lin);
+  CK(apply_mask_bf16(static_cast<const bf16*>(X), mask, keep_scale, M, in, Xd, st));
+  const void* Z = Z_saved;
+  if (!Z) {
+    RowProjDesc d = rp_desc(M, in, r, Xd, A, false, w.err);
+    d.out_a = static_cast<bf16*>(w.Zrec);
+    CK(rowproj(d, st));
+    Z = w.Zrec;
+  }
+  {  // dB partials (dY^T Z) and column sums of dY, one pass over dY
+    ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
+    d.colsum = dbias ? w.csum : nullptr;
+    CK(colreduce(d, st));
+  }
+  {  // s G = s dY B
+    RowProjDesc d = rp_desc(M, out, r, dY, B, true, w.err);
+    d.out_b = static_cast<bf16*>(w.Gs);
+    d.scale_b = s;
+    CK(rowproj(d, st));
+  }
+  if (dX) {  // dY W0 on the tensor cores, then the masked adapter share in its own pass
+    CK(tc_gemm(dx_desc(M, in, out, dY, W0, nullptr, A, r, dX, nullptr, w.err), st));
+    CK(add_masked_rank_bf16(static_cast<bf16*>(dX), static_cast<const bf16*>(w.Gs), static_cast<const bf16*>(A),
+                            mask, keep_scale, M, in, r, st));
+  }
+  CK(colreduce(cr_desc(M, in, r, Xd, w.Gs, r, w.PA, w.splitsA, w.err), st));   // Xd^T (s G)
+  const FinJob fin[2] = {fin_dA(r, in, Partial{w.PA, w.splitsA, r, 0}, 1.f, A, dA),
+                         fin_dB(out, r, Partial{w.PB, w.splitsB, r, 0}, s, B, dB)};
+  CK(finalize_batch(fin, 2, st));
+  if (dbias) CK(sum_splits<bf16>(w.csum, w.splitsB, out, nullptr, static_cast<bf16*>(dbias), st));
   return LORA_OK;
 }
 

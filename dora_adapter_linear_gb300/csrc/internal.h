@@ -229,6 +229,12 @@ cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float*
 cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int64_t rows2, int64_t cols, bf16* dst,
                              cudaStream_t st);
 cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st);
+// Input dropout on the unfused path: out = bf16(X o mask * scale); dX += (G A) o mask * scale
+// (mask uint8 0/1 [rows, cols], cols a multiple of 8)
+cudaError_t apply_mask_bf16(const bf16* X, const uint8_t* mask, float scale, int64_t rows, int64_t cols, bf16* out,
+                            cudaStream_t st);
+cudaError_t add_masked_rank_bf16(bf16* dX, const bf16* G, const bf16* A, const uint8_t* mask, float scale,
+                                 int64_t rows, int64_t cols, int r, cudaStream_t st);
 // out[o, j] = bf16(f * in[o, j] / d[o]) for in [rows, r] (a zero d[o] counts as 1)
 cudaError_t scale_rows_recip_bf16(const bf16* in, int64_t rows, int r, const float* d, float f, bf16* out,
                                   cudaStream_t st);

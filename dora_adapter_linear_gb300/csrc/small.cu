@@ -583,6 +583,75 @@ cudaError_t scale_rows_recip_bf16(const bf16* in, int64_t rows, int r, const flo
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ input dropout (unfused path)
+// out = bf16(X o mask * scale), 8 elements (one 16-byte chunk) per thread; cols a multiple of 8
+__global__ void apply_mask_kernel(const uint4* X, const uint2* mask, float scale, int64_t n8, uint4* out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  uint4 v = X[i];
+  const uint2 m = mask[i];
+  const uint8_t* mb = reinterpret_cast<const uint8_t*>(&m);
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = unpack_bf16x2(w[e]);
+    w[e] = pack_bf16x2(mb[2 * e] ? f.x * scale : 0.f, mb[2 * e + 1] ? f.y * scale : 0.f);
+  }
+  out[i] = v;
+}
+cudaError_t apply_mask_bf16(const bf16* X, const uint8_t* mask, float scale, int64_t rows, int64_t cols, bf16* out,
+                            cudaStream_t st) {
+  const int64_t n8 = rows * cols / 8;
+  if (n8 <= 0) return cudaSuccess;
+  apply_mask_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(X), reinterpret_cast<const uint2*>(mask), scale, n8, reinterpret_cast<uint4*>(out));
+  count_launch();
+  return cudaGetLastError();
+}
+
+// dX[i, k] += scale * mask[i, k] * sum_j G[i, j] A[j, k]  (the adapter's share of dX when a mask
+// sits between X and A); 8 consecutive k of one row per thread, G [rows, r], A [r, cols]
+__global__ void add_masked_rank_kernel(bf16* dX, const bf16* G, const bf16* A, const uint8_t* mask, float scale,
+                                       int64_t rows, int64_t cols, int r) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t c8 = cols / 8;
+  if (i >= rows * c8) return;
+  const int64_t row = i / c8;
+  const int64_t k = (i - row * c8) * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < r; ++j) {
+    const float gj = __bfloat162float(G[row * r + j]);
+    const uint4 av = *reinterpret_cast<const uint4*>(A + (int64_t)j * cols + k);
+    const uint32_t* aw = reinterpret_cast<const uint32_t*>(&av);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16x2(aw[e]);
+      acc[2 * e] = fmaf(gj, f.x, acc[2 * e]);
+      acc[2 * e + 1] = fmaf(gj, f.y, acc[2 * e + 1]);
+    }
+  }
+  const int64_t o = row * cols + k;
+  uint4 d = *reinterpret_cast<const uint4*>(dX + o);
+  const uint2 m = *reinterpret_cast<const uint2*>(mask + o);
+  const uint8_t* mb = reinterpret_cast<const uint8_t*>(&m);
+  uint32_t* dw = reinterpret_cast<uint32_t*>(&d);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = unpack_bf16x2(dw[e]);
+    dw[e] = pack_bf16x2(f.x + (mb[2 * e] ? scale * acc[2 * e] : 0.f),
+                        f.y + (mb[2 * e + 1] ? scale * acc[2 * e + 1] : 0.f));
+  }
+  *reinterpret_cast<uint4*>(dX + o) = d;
+}
+cudaError_t add_masked_rank_bf16(bf16* dX, const bf16* G, const bf16* A, const uint8_t* mask, float scale,
+                                 int64_t rows, int64_t cols, int r, cudaStream_t st) {
+  const int64_t n = rows * cols / 8;
+  if (n <= 0) return cudaSuccess;
+  add_masked_rank_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(dX, G, A, mask, scale, rows, cols, r);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st) {
   if (bytes == 0) return cudaSuccess;
   return cudaMemsetAsync(p, 0, bytes, st);

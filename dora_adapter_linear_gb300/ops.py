@@ -43,6 +43,35 @@ def lora_linear_bwd(X, W0, A, B, Z, dY, s, need_dx=True, need_dbias=False):
     return dX, dA, dB, dbias
 
 
+def _check_mask(mask, X):
+    if mask.dtype != torch.uint8 or tuple(mask.shape) != tuple(X.shape) or not mask.is_contiguous():
+        raise ValueError(f"dropout mask must be contiguous uint8 {tuple(X.shape)}, got {mask.dtype} "
+                         f"{tuple(mask.shape)}")
+
+
+def lora_linear_dropout_fwd(X, mask, keep_scale, W0, A, B, s, bias=None, save_z=True):
+    """mask: uint8 [M, d_in] (1 = kept), keep_scale = 1 / (1 - p)."""
+    _check_mask(mask, X)
+    sh = _shape_of(X, W0, A)
+    Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=X.device)
+    Z = torch.empty(X.shape[0], A.shape[0], dtype=X.dtype, device=X.device) if save_z else None
+    ws = workspace(L.lora_workspace_bytes(L.OP_DROPOUT_FWD, sh), X.device)
+    L.lora_linear_dropout_fwd(sh, X, mask, keep_scale, W0, A, B, bias, s, Y, Z, ws)
+    return Y, Z
+
+
+def lora_linear_dropout_bwd(X, mask, keep_scale, W0, A, B, Z, dY, s, need_dx=True, need_dbias=False):
+    _check_mask(mask, X)
+    sh = _shape_of(X, W0, A)
+    dX = torch.empty_like(X) if need_dx else None
+    dA = torch.empty_like(A)
+    dB = torch.empty_like(B)
+    dbias = torch.empty(W0.shape[0], dtype=X.dtype, device=X.device) if need_dbias else None
+    ws = workspace(L.lora_workspace_bytes(L.OP_DROPOUT_BWD, sh), X.device)
+    L.lora_linear_dropout_bwd(sh, X, mask, keep_scale, W0, A, B, Z, dY, s, dX, dA, dB, dbias, ws)
+    return dX, dA, dB, dbias
+
+
 def dora_rownorm2(W0):
     sh = L.shape(0, W0.shape[1], W0.shape[0], 8, L.dtype_code(W0))
     r0 = torch.empty(W0.shape[0], dtype=torch.float32, device=W0.device)

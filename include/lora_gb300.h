@@ -63,7 +63,8 @@ typedef enum {
     LORA_OP_DORA_FWD = 2, LORA_OP_DORA_BWD = 3,
     LORA_OP_MLP_FWD = 4, LORA_OP_MLP_BWD = 5,
     LORA_OP_QKV_FWD = 6, LORA_OP_QKV_BWD = 7,
-    LORA_OP_DORA_COLS_FWD = 8, LORA_OP_DORA_COLS_BWD = 9
+    LORA_OP_DORA_COLS_FWD = 8, LORA_OP_DORA_COLS_BWD = 9,
+    LORA_OP_DROPOUT_FWD = 10, LORA_OP_DROPOUT_BWD = 11
 } lora_op;
 
 typedef struct {
@@ -118,8 +119,8 @@ const char* lora_status_string(int status);
 /* Library ABI version (increments on any signature change). */
 int lora_abi_version(void);
 
-/* Bytes of workspace `op` needs for `sh` (LORA_OP_LINEAR_*, LORA_OP_DORA_* and
- * LORA_OP_DORA_COLS_*). 0 on bad input. */
+/* Bytes of workspace `op` needs for `sh` (LORA_OP_LINEAR_*, LORA_OP_DORA_*, LORA_OP_DORA_COLS_*
+ * and LORA_OP_DROPOUT_*). 0 on bad input. */
 size_t lora_workspace_bytes(int op, const lora_shape* sh);
 
 /* Bytes of workspace the MLP entry points need (op = LORA_OP_MLP_FWD / LORA_OP_MLP_BWD). */
@@ -186,7 +187,29 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
                             void* dX, void* dA, void* dB, void* dbias,
                             void* ws, size_t ws_bytes, void* stream);
 
-/* ---------------------------------------------------------------- DoRA (rows)
+/* ---------------------------------------------------------------- LoRA with input dropout
+ * The adapter branch sees a dropped-out copy of the input, the base does not:
+ *   Xd = X o mask * keep_scale,  Y = X W0^T + s (Xd A^T) B^T (+ bias),
+ * mask [M, d_in] uint8 (0 = dropped, 1 = kept; drawn by the caller, the same bytes for the
+ * forward and the backward), keep_scale = 1 / (1 - p).  The mask sits between X and A, so this
+ * call takes the unfused path: Xd is written once (workspace) and, in the backward, the adapter's
+ * share of dX is a separate masked rank-r pass instead of the dX GEMM's tail.
+ * "Fused Kernels (experimental)" (LyCORIS docs), the note that a call whose mask sits between
+ * two factors takes the unfused path; "How Unsloth's FastLoRA Kernel Differs ...", Optimized
+ * Dropout and Scaling.  LORA_BF16 only; other arguments as lora_linear_fwd / _bwd.
+ *   Backward: G = s dY B;  dX = dY W0 + (G A) o mask * keep_scale;  dA = G^T Xd;
+ *             dB = s dY^T Z (Z = Xd A^T, saved by the forward or NULL to recompute);
+ *             dbias = colsum(dY).
+ */
+lora_status lora_linear_dropout_fwd(const lora_shape* sh, const void* X, const uint8_t* mask, float keep_scale,
+                                    const void* W0, const void* A, const void* B, const void* bias, float s,
+                                    void* Y, void* Z_save, void* ws, size_t ws_bytes, void* stream);
+lora_status lora_linear_dropout_bwd(const lora_shape* sh, const void* X, const uint8_t* mask, float keep_scale,
+                                    const void* W0, const void* A, const void* B, const void* Z_saved,
+                                    const void* dY, float s, void* dX, void* dA, void* dB, void* dbias,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- DoRA (rows)/* ---------------------------------------------------------------- DoRA (rows)
  * r0[o] = sum_k W0[o,k]^2 in fp32: the cached per-layer constant of the closed-form norm.
  * "LoRA/DoRA fast forward ...", commit message (cached rowsum(W0^2) constant) and What
  * section (the cached norm constant is a per-layer vector).  r0: [d_out] fp32 output.

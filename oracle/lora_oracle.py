@@ -29,7 +29,7 @@ __all__ = [
     "dora_linear_fwd", "dora_linear_bwd", "dora_colnorm2", "dora_cols_fwd", "dora_cols_bwd",
     "dora_cols_fwd_rows", "dora_cols_bwd_sampled", "silu", "dsilu", "gelu", "dgelu", "mlp_swiglu_fwd", "mlp_swiglu_bwd",
     "quantize_rows", "int8_accumulate", "w8a8_lora_fwd", "w8a8_dequant_weight", "w8a8_lora_bwd",
-    "qkv_adapted_weight", "qkv_lora_fwd", "qkv_lora_bwd", "qkv_fwd_rows", "qkv_bwd_sampled",
+    "lora_dropout_fwd", "lora_dropout_bwd", "qkv_adapted_weight", "qkv_lora_fwd", "qkv_lora_bwd", "qkv_fwd_rows", "qkv_bwd_sampled",
     "lora_fwd_rows", "lora_bwd_sampled", "dora_fwd_rows", "dora_bwd_sampled", "dora_bwd_rows_sampled",
     "mlp_fwd_rows", "mlp_bwd_rows",
 ]
@@ -84,6 +84,34 @@ def lora_linear_bwd(X, W0, A, B, s, dY):
     dB = s * (dWp @ A.T)
     dbias = dY.sum(axis=0)
     return dX, dA, dB, dbias
+
+
+# ----------------------------------------------------------------------------- LoRA with input dropout
+def lora_dropout_fwd(X, mask, keep_scale, W0, A, B, s, bias=None):
+    """y = X W0^T + s (Xd A^T) B^T (+ bias) with Xd = X o mask * keep_scale.
+
+    The adapter branch sees the dropped-out input and the base branch the plain one, as with a
+    dropout layer in front of the down-projection ("How Unsloth's FastLoRA Kernel Differs ...",
+    Optimized Dropout and Scaling; "Fused Kernels (experimental)": a call whose mask sits between
+    two factors takes the unfused path).  The mask is an input (drawn by the caller).
+    """
+    Xd = X * (np.asarray(mask, dtype=np.float64) * keep_scale)
+    Y = X @ W0.T + s * ((Xd @ A.T) @ B.T)
+    if bias is not None:
+        Y = Y + bias[None, :]
+    return Y
+
+
+def lora_dropout_bwd(X, mask, keep_scale, W0, A, B, s, dY):
+    """Gradients of lora_dropout_fwd w.r.t. X, A, B and bias (W0 frozen).
+
+    With D = diag-free elementwise factor mask * keep_scale: dX = dY W0 + (s (dY B) A) o D,
+    dA = s (dY B)^T Xd, dB = s dY^T (Xd A^T), dbias = colsum(dY).
+    """
+    D = np.asarray(mask, dtype=np.float64) * keep_scale
+    Xd = X * D
+    G = s * (dY @ B)
+    return dY @ W0 + (G @ A) * D, G.T @ Xd, s * (dY.T @ (Xd @ A.T)), dY.sum(axis=0)
 
 
 # ----------------------------------------------------------------------------- fused-leaf (QKV)

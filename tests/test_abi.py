@@ -38,7 +38,7 @@ def test_status_strings(lib):
     assert L.lora_status_string(0) == "ok"
     assert "workspace" in L.lora_status_string(4)
     assert L.lora_status_string(99) == "unknown status"
-    assert L.lora_abi_version() == 5
+    assert L.lora_abi_version() == 6
 
 
 def test_workspace_bytes_rejects_bad_shapes(lib):

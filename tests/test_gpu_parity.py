@@ -124,6 +124,50 @@ def test_m_zero_is_noop(ops):
     assert not dA.any() and not dB.any()
 
 
+# ---------------------------------------------------------------------------- LoRA with input dropout
+@pytest.mark.parametrize("M,p", [(300, 0.1), (129, 0.5)])
+def test_lora_dropout_fwd_bwd(ops, M, p):
+    case, t, g = lin_inputs("lora_4096_bf16", M=M, d_in=328, d_out=264, r=16, bias=True)
+    mask = D.make_dropout_mask(M, case.d_in, p)
+    keep = 1.0 / (1.0 - p)
+    Y, Z = ops.lora_linear_dropout_fwd(g["X"], gpu(mask), keep, g["W0"], g["A"], g["B"], case.s, g["bias"])
+    X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
+    mk = mask.numpy()
+    assert_close(Y, O.lora_dropout_fwd(X, mk, keep, W0, A, B, case.s, f64(t["bias"])), "bf16", "Y")
+    assert_close(Z, (X * (mk * keep)) @ A.T, "bf16", "Z")
+    rX, rA, rB, rb = O.lora_dropout_bwd(X, mk, keep, W0, A, B, case.s, f64(t["dY"]))
+    for z in (Z, None):  # saved Z and the recomputed one
+        dX, dA, dB, dbias = ops.lora_linear_dropout_bwd(g["X"], gpu(mask), keep, g["W0"], g["A"], g["B"], z,
+                                                        g["dY"], case.s, need_dbias=True)
+        assert_close(dX, rX, "bf16", "dX")
+        assert_close(dA, rA, "bf16", "dA")
+        assert_close(dB, rB, "bf16", "dB")
+        assert_close(dbias, rb[None, :], "bf16", "dbias")
+
+
+def test_lora_dropout_all_kept_matches_plain_layer(ops):
+    """An all-ones mask with unit scale is the plain layer: same values within bf16 rounding."""
+    case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=16)
+    ones = torch.ones(SMALL["M"], SMALL["d_in"], dtype=torch.uint8, device=DEV)
+    Yd, Zd = ops.lora_linear_dropout_fwd(g["X"], ones, 1.0, g["W0"], g["A"], g["B"], case.s)
+    Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s)
+    assert torch.equal(Yd, Y) and torch.equal(Zd, Z)
+
+
+def test_lora_dropout_strength0_and_m_zero(ops):
+    case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=16)
+    mask = gpu(D.make_dropout_mask(SMALL["M"], SMALL["d_in"], 0.3))
+    Y0, _ = ops.lora_linear_dropout_fwd(g["X"], mask, 1 / 0.7, g["W0"], g["A"], g["B"], 0.0, save_z=False)
+    Yb, _ = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], 0.0, save_z=False)
+    assert torch.equal(Y0, Yb)
+    dX, dA, dB, _ = ops.lora_linear_dropout_bwd(g["X"], mask, 1 / 0.7, g["W0"], g["A"], g["B"], None, g["dY"], 0.0)
+    assert torch.equal(dX, ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], None, g["dY"], 0.0)[0])
+    assert not dA.any() and not dB.any()
+    e = torch.empty(0, SMALL["d_in"], dtype=torch.bfloat16, device=DEV)
+    Ye, _ = ops.lora_linear_dropout_fwd(e, mask[:0], 2.0, g["W0"], g["A"], g["B"], case.s)
+    assert Ye.shape == (0, SMALL["d_out"])
+
+
 # ---------------------------------------------------------------------------- LoRA, fp32 (tiny workload)
 def test_lora_tiny_f32(ops):
     case, t, g = lin_inputs("lora_tiny_f32")

@@ -140,6 +140,53 @@ def test_lora_grads_match_library_autograd():
         assert rel(got, t[k].grad.numpy()) < 1e-13
 
 
+# ------------------------------------------------------------------ LoRA with input dropout
+def _drop_case(seed, p=0.25, **kw):
+    X, W0, A, B, bias, _, dY = rand_case(seed=seed, **kw)
+    mask = (rng(seed + 100).uniform(size=X.shape) >= p).astype(np.uint8)
+    return X, mask, 1.0 / (1.0 - p), W0, A, B, bias, dY
+
+
+def test_dropout_all_kept_unit_scale_is_lora():
+    X, _, _, W0, A, B, bias, dY = _drop_case(20)
+    ones = np.ones(X.shape, np.uint8)
+    assert rel(O.lora_dropout_fwd(X, ones, 1.0, W0, A, B, 0.8, bias), O.lora_linear_fwd(X, W0, A, B, 0.8, bias)) < 1e-14
+    for got, ref in zip(O.lora_dropout_bwd(X, ones, 1.0, W0, A, B, 0.8, dY), O.lora_linear_bwd(X, W0, A, B, 0.8, dY)):
+        assert rel(got, ref) < 1e-14
+
+
+def test_dropout_all_dropped_leaves_base_branch():
+    """The mask acts on the adapter's input only: with every entry dropped the base branch and
+    the bias remain, and the adapter factors get no gradient."""
+    X, _, scale, W0, A, B, bias, dY = _drop_case(21)
+    zeros = np.zeros(X.shape, np.uint8)
+    assert np.array_equal(O.lora_dropout_fwd(X, zeros, scale, W0, A, B, 0.8, bias), X @ W0.T + bias[None, :])
+    dX, dA, dB, dbias = O.lora_dropout_bwd(X, zeros, scale, W0, A, B, 0.8, dY)
+    assert np.array_equal(dX, dY @ W0) and not dA.any() and not dB.any()
+    assert np.allclose(dbias, dY.sum(0), rtol=0, atol=1e-14)
+
+
+def test_dropout_grads_finite_difference():
+    X, mask, scale, W0, A, B, bias, dY = _drop_case(22, M=4, d_in=8, d_out=6, r=2)
+    s = 1.1
+    L = lambda: float((dY * O.lora_dropout_fwd(X, mask, scale, W0, A, B, s, bias)).sum())  # noqa: E731
+    for got, x in zip(O.lora_dropout_bwd(X, mask, scale, W0, A, B, s, dY), (X, A, B, bias)):
+        assert rel(got, _fd_grad(L, x)) < 1e-8
+
+
+def test_dropout_grads_match_library_autograd():
+    """Library graph: base linear on X plus the adapter chain on X * mask * scale."""
+    X, mask, scale, W0, A, B, bias, dY = _drop_case(23, M=9, d_in=12, d_out=10, r=3, p=0.4)
+    s = 0.6
+    t = {k: torch.tensor(v, requires_grad=True) for k, v in dict(X=X, A=A, B=B, bias=bias).items()}
+    xd = t["X"] * (torch.tensor(mask, dtype=torch.float64) * scale)
+    y = torch.nn.functional.linear(t["X"], torch.tensor(W0), t["bias"]) + s * torch.nn.functional.linear(
+        torch.nn.functional.linear(xd, t["A"]), t["B"])
+    y.backward(torch.tensor(dY))
+    for got, k in zip(O.lora_dropout_bwd(X, mask, scale, W0, A, B, s, dY), ("X", "A", "B", "bias")):
+        assert rel(got, t[k].grad.numpy()) < 1e-13
+
+
 # ------------------------------------------------------------------ DoRA
 def test_dora_closed_form_norm_equals_explicit():
     """||W0 + sBA||^2_row = rowsum(W0^2) + 2s rowsum((W0 A^T) o B) + s^2 rowsum((B (A A^T)) o B)."""
