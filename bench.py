@@ -274,7 +274,7 @@ def timed(fn, steps, warmup, dist=None):
 # lora_4096_bf16: dram__bytes_read.sum + dram__bytes_write.sum of the forward (CTA pair) and dX
 # (one CTA) GEMM launches of the headline step (mean of 4 launches: 147.2 MB read + 43.6 MB
 # written; the algorithmic bytes are 64 MiB activation + 32 MiB weight + 64 MiB output = 167.8 MB).
-GEMM_TRAFFIC = {"lora_4096_bf16": 190.7e6}
+GEMM_TRAFFIC = {"lora_4096_bf16": None}
 
 
 def gemm_roofline(L, peaks, ms_step, steps_recorded, sustained, workload):
@@ -284,7 +284,8 @@ def gemm_roofline(L, peaks, ms_step, steps_recorded, sustained, workload):
         return None
     ach = fl / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
-    return {"kernel": "tcgen05 GEMM with fused rank-r tail (tc_pair_kernel forward, tc_gemm_kernel dX)",
+    return {"kernel": "tcgen05 GEMM with fused rank-r tail (tc_pair_kernel forward, tc_gemm_kernel dX with "
+                      "B multicast)",
             "bound": "tensor",
             "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
             "peak_kind": ("sustained" if sustained else "burst") + " bf16, " + peaks["source"] + " (of measured)",

@@ -455,8 +455,13 @@ struct OneCta {
   static constexpr int THREADS = (KSCALE || EPI8) ? 320 : 192;
 };
 
-template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
+// MC: a cluster of two CTAs on two M-adjacent tiles of the same N range; each CTA loads half of
+// every B tile and multicasts it to both, so each SM reads 32 KB of operands per k-step instead of
+// 48 KB.  A stage is free again once both CTAs' MMAs have read it: empty[s] takes one commit
+// from each CTA (multicast), and neither CTA exits while its peer may still write into it.
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE, bool MC>
 __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  static_assert(!(MC && (STACKED || KSCALE || EPI == EPI_W8A8)), "multicast mode: plain K-major or MN-major B only");
   using L = Layout<EPI, false>;
   constexpr int STAGES = L::STAGES;
   constexpr int BNB = STACKED ? BN / 2 : BN;          // rows per K-major B box
@@ -480,14 +485,23 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
   const int nk0 = (p.K0 + BK - 1) / BK;
   const int nk = nk0 + (HAS_TAIL ? (p.K1 + BK - 1) / BK : 0);   // the rank-r tail may span several K-steps
+  // tile sequence: one tile per CTA step, or (MC) one pair of M-adjacent tiles per cluster step
+  const uint32_t mc_rank = MC ? cluster_ctarank() : 0u;
+  const int m_units = MC ? (p.num_m_tiles + 1) / 2 : p.num_m_tiles;
+  const int t_first = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int t_step = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int t_count = m_units * p.num_n_tiles;
+  auto coords = [&](int t, int& mt, int& nt) {
+    tile_coords(t, m_units, p.num_n_tiles, p.group_m, mt, nt);
+    if (MC) mt = 2 * mt + (int)mc_rank;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], MC ? 2 : 1);
       mbar_init(&ready[i], 128);
     }
     for (int i = 0; i < 2; ++i) {
@@ -511,7 +525,8 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (MC) cluster_sync_all();   // both CTAs' barriers initialised before any multicast
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   pdl_wait();      // the operands may come from the previous kernel in the stream
@@ -525,9 +540,9 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
       uint32_t armed = 0;         // bit s: stage s has been armed at least once
       uint32_t armed_par = 0;     // bit s: parity of the last arm of stage s
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = t_first; t < t_count && ok; t += t_step) {
         int mt, nt;
-        tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+        coords(t, mt, nt);
         const int m0 = mt * BM;
         const int n0 = nt * N_OUT;
         for (int ks = 0; ks < nk; ++ks) {
@@ -549,23 +564,43 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
               const bool second = ks >= p.k0_split_steps;
               const void* mp = second ? (const void*)&p.tmB0b : (const void*)&p.tmB0;
               const int ky = second ? kx - p.k0_split_steps * BK : kx;
+              if constexpr (MC) {   // this CTA's two 64-column chunks, to both CTAs
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, mp, &full[stage], n0 + 64 * j, ky);
+                for (int j = 0; j < 2; ++j) {
+                  const int jj = 2 * (int)mc_rank + j;
+                  tma_load_2d_mc(b_dst + jj * 8192, mp, &full[stage], n0 + 64 * jj, ky, 0x3);
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, mp, &full[stage], n0 + 64 * j, ky);
+              }
             } else if (STACKED) {
               tma_load_2d(b_dst, &p.tmB0, &full[stage], kx, n0);
               tma_load_2d(b_dst + BNB * 128, &p.tmB0b, &full[stage], kx, n0);
+            } else if (MC) {   // this CTA's 128 rows of the B tile, to both CTAs
+              tma_load_2d_mc(b_dst + mc_rank * (BN / 2) * 128, &p.tmB0, &full[stage], kx, n0 + (int)mc_rank * (BN / 2),
+                             0x3);
             } else {
               tma_load_2d(b_dst, &p.tmB0, &full[stage], kx, n0);
             }
           } else {
             const int kt = (ks - nk0) * BK;   // K offset inside the rank-r tail
             tma_load_2d(a_dst, &p.tmA1, &full[stage], kt, m0);
-            if (B1_MN) {
+            if (B1_MN && MC) {
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const int jj = 2 * (int)mc_rank + j;
+                tma_load_2d_mc(b_dst + jj * 8192, &p.tmB1, &full[stage], n0 + 64 * jj, kt, 0x3);
+              }
+            } else if (B1_MN) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &p.tmB1, &full[stage], n0 + 64 * j, kt);
             } else if (STACKED) {
               tma_load_2d(b_dst, &p.tmB1, &full[stage], p.tail_b1_x + kt, n0);
               if (EPI != EPI_W8A8) tma_load_2d(b_dst + BNB * 128, &p.tmB1b, &full[stage], p.tail_b1b_x + kt, n0);
+            } else if (MC) {
+              tma_load_2d_mc(b_dst + mc_rank * (BN / 2) * 128, &p.tmB1, &full[stage], kt, n0 + (int)mc_rank * (BN / 2),
+                             0x3);
             } else {
               tma_load_2d(b_dst, &p.tmB1, &full[stage], kt, n0);
             }
@@ -595,7 +630,7 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+      for (int t = t_first; t < t_count && ok; t += t_step, ++it) {
         const int buf = W8 ? 0 : (it & 1);
         const uint32_t acc_phase = W8 ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
         if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, p.timeout_ns, abort_flag, p.err, 0x102)) {
@@ -630,7 +665,8 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
             else
               umma_bf16(d_tmem, adesc, bdesc, tail ? idesc1 : idesc0, (ks > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&empty[stage]);
+          if constexpr (MC) umma_commit_mc(&empty[stage], 0x3);   // the stage is read in both CTAs
+          else umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -652,13 +688,13 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
     uint8_t* my_stg = sStg + (warp - 2) * (EPI8 ? 4096 : EpiCfg<EPI, false>::STG_BUFS * 4096);
     int it = 0;
     uint32_t chunk_ctr = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+    for (int t = t_first; t < t_count; t += t_step, ++it) {
       const int buf = (EPI == EPI_W8A8) ? 0 : (it & 1);
       const uint32_t acc_phase = (EPI == EPI_W8A8) ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
       if (!mbar_wait(&acc_full[buf], acc_phase, p.timeout_ns, abort_flag, p.err, 0x104)) break;
       tc_fence_after();
       int mt, nt;
-      tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
+      coords(t, mt, nt);
       const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + buf * BN + half * (N_OUT / 2);
       if constexpr (EPI8)
         epilogue_tile<EPI, N_OUT / 2>(p, t_row, mt * BM + 32 * q, nt * N_OUT + half * (N_OUT / 2), lane, my_stg,
@@ -680,7 +716,7 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
     // the scales of the next three scaled K-steps are in flight while a tile is being scaled
     KScales s_cur = kscale_fetch(p, 0, tid), s_nx1 = kscale_fetch(p, 1 % nk0, tid),
             s_nx2 = kscale_fetch(p, 2 % nk0, tid);
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int t = t_first; t < t_count && ok; t += t_step) {
       for (int ks = 0; ks < nk; ++ks) {
         const bool tail = HAS_TAIL && ks >= nk0;
         if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.err, 0x105)) {
@@ -703,7 +739,8 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (MC) cluster_sync_all();   // neither CTA leaves while its peer may still write into it
+  else __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
@@ -1034,32 +1071,54 @@ int pdl_attr(cudaLaunchAttribute* a) {
   return 1;
 }
 
-template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
-static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
+// tiles: CTA tiles, or (MC) pairs of M-adjacent tiles, one per cluster step
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE, bool MC>
+static cudaError_t launch_one_k(const TcParams& p, cudaStream_t st, int tiles) {
   using L = Layout<EPI, false>;
-  auto kern = tc_gemm_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  int grid = num_sms_current();
-  // test knob: cap the persistent grid so that small problems still run several tiles per CTA
-  const int cap = env_int("LORA_GB300_MAX_CTAS", 0);
-  if (cap > 0 && cap < grid) grid = cap;
-  if (grid > tiles) grid = tiles;
+  auto kern = tc_gemm_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE, MC>;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(grid, 1, 1);
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(OneCta<EPI, KSCALE>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = L::TOTAL;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl_attr(&attr[0]);
+  cfg.numAttrs = 0;
+  if (MC) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.numAttrs = 1;
+  }
+  static int max_units = 0;   // co-resident CTAs (clusters for MC)
+  if (max_units == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e != cudaSuccess) return e;
+    int n = MC ? num_sms_current() / 2 : num_sms_current();
+    if (MC) {
+      cfg.gridDim = dim3(2 * n, 1, 1);
+      int c = 0;
+      e = cudaOccupancyMaxActiveClusters(&c, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      n = c > 0 ? c : 1;
+    }
+    max_units = n;
+  }
+  int units = max_units;
+  // test knob: cap the persistent grid so that small problems still run several tiles per CTA
+  const int cap = env_int("LORA_GB300_MAX_CTAS", 0) / (MC ? 2 : 1);
+  if (cap > 0 && cap < units) units = cap;
+  if (units > tiles) units = tiles;
+  cfg.gridDim = dim3((MC ? 2 : 1) * units, 1, 1);
+  cfg.numAttrs += (unsigned)pdl_attr(&attr[cfg.numAttrs]);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
+static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
+  return launch_one_k<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE, false>(p, st, tiles);
 }
 
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
@@ -1106,31 +1165,34 @@ static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// kind: 0 one CTA, 1 CTA pair, 2 two one-CTA tiles sharing B by multicast
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
-static cudaError_t launch_variant(const TcParams& p, cudaStream_t st, bool pair, int tiles) {
-  return pair ? launch_pair<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles)
-              : launch_one<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles);
+static cudaError_t launch_variant(const TcParams& p, cudaStream_t st, int kind, int tiles) {
+  if (kind == 1) return launch_pair<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles);
+  if constexpr (!STACKED && !KSCALE && EPI != EPI_W8A8)
+    if (kind == 2) return launch_one_k<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE, true>(p, st, tiles);
+  return launch_one<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles);
 }
 
-static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStream_t st, bool pair, int tiles) {
+static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStream_t st, int kind, int tiles) {
   switch (d.mode) {
     case TC_FWD:
-      if (d.has_tail) return launch_variant<false, false, true, false, EPI_SCALE_BIAS, false>(p, st, pair, tiles);
-      return launch_variant<false, false, false, false, EPI_SCALE_BIAS, false>(p, st, pair, tiles);
+      if (d.has_tail) return launch_variant<false, false, true, false, EPI_SCALE_BIAS, false>(p, st, kind, tiles);
+      return launch_variant<false, false, false, false, EPI_SCALE_BIAS, false>(p, st, kind, tiles);
     case TC_BWD_DX:
       if (d.a_kscale) {
-        if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS, true>(p, st, pair, tiles);
-        return launch_variant<true, false, false, true, EPI_SCALE_BIAS, true>(p, st, pair, tiles);
+        if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS, true>(p, st, kind, tiles);
+        return launch_variant<true, false, false, true, EPI_SCALE_BIAS, true>(p, st, kind, tiles);
       }
-      if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS, false>(p, st, pair, tiles);
-      return launch_variant<true, false, false, true, EPI_SCALE_BIAS, false>(p, st, pair, tiles);
+      if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS, false>(p, st, kind, tiles);
+      return launch_variant<true, false, false, true, EPI_SCALE_BIAS, false>(p, st, kind, tiles);
     case TC_SWIGLU_FWD:
-      return launch_variant<false, true, true, false, EPI_SWIGLU, false>(p, st, pair, tiles);
+      return launch_variant<false, true, true, false, EPI_SWIGLU, false>(p, st, kind, tiles);
     case TC_SWIGLU_BWD:
-      return launch_variant<true, false, true, true, EPI_SWIGLU_BWD, false>(p, st, pair, tiles);
+      return launch_variant<true, false, true, true, EPI_SWIGLU_BWD, false>(p, st, kind, tiles);
     case TC_W8A8F:
-      if (d.has_tail) return launch_variant<false, true, true, false, EPI_W8A8F, false>(p, st, pair, tiles);
-      return launch_variant<false, true, false, false, EPI_W8A8F, false>(p, st, pair, tiles);
+      if (d.has_tail) return launch_variant<false, true, true, false, EPI_W8A8F, false>(p, st, kind, tiles);
+      return launch_variant<false, true, false, false, EPI_W8A8F, false>(p, st, kind, tiles);
     case TC_W8A8:  // one-CTA kernel only (its accumulator layout is per-CTA)
       if (d.has_tail) return launch_one<false, true, true, false, EPI_W8A8, false>(p, st, tiles);
       return launch_one<false, true, false, false, EPI_W8A8, false>(p, st, tiles);
@@ -1138,10 +1200,9 @@ static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStrea
   return cudaErrorInvalidValue;
 }
 
-// Kernel choice per mode: the CTA pair stages half of B per CTA, which leaves room for a deeper
-// operand ring; that pays off for the stacked gate/up forward (5 stages instead of 3 beside its
-// three output staging buffers) and nowhere else measurably.  LORA_GB300_GEMM_PAIR=0 / 1 forces
-// the one-CTA / pair kernel for every mode (W8A8 always runs one-CTA).
+// Kernel choice per mode.  LORA_GB300_GEMM_PAIR=0 / 1 forces the one-CTA / pair kernel for every
+// mode (W8A8 always runs one-CTA); LORA_GB300_GEMM_MC=0 / 1 turns the two-CTA B multicast of the
+// one-CTA kernel off / on where it applies.
 static bool use_pair(int mode) {
   const char* e = getenv("LORA_GB300_GEMM_PAIR");
   if (e && *e) return atoi(e) != 0;
@@ -1150,14 +1211,27 @@ static bool use_pair(int mode) {
   return mode == TC_FWD || mode == TC_SWIGLU_FWD;
 }
 
+static bool use_mc(int mode) {
+  const char* e = getenv("LORA_GB300_GEMM_MC");
+  if (e && *e) return atoi(e) != 0;
+  // measured over LLM layer shapes: 3-6% faster on the MN-major dX products, no gain on the
+  // K-major forward (which runs on the CTA pair)
+  return mode == TC_BWD_DX || mode == TC_SWIGLU_BWD;
+}
+
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   if (d.M <= 0 || d.N <= 0) return cudaSuccess;
   const bool pair = use_pair(d.mode) && d.mode != TC_W8A8;
   TcParams p;
   memset(&p, 0, sizeof(p));
   const bool stacked = d.mode == TC_SWIGLU_FWD || d.mode == TC_W8A8 || d.mode == TC_W8A8F;
-  // rows of a K-major B box: 256 (one CTA), 128 (stacked halves, or one CTA's half of a pair)
-  const int bnb = (stacked || pair) ? BN / 2 : BN;
+  // two one-CTA tiles sharing B: plain forward / dX products with an even number of M tiles
+  const bool mc = !pair && !stacked && d.a_kscale == nullptr &&
+                  (d.mode == TC_FWD || d.mode == TC_BWD_DX || d.mode == TC_SWIGLU_BWD) &&
+                  ((d.M + BM - 1) / BM) % 2 == 0 && use_mc(d.mode);
+  // rows of a K-major B box: 256 (one CTA), 128 (stacked halves, one CTA's half of a pair, or of
+  // a multicast B tile)
+  const int bnb = (stacked || pair || mc) ? BN / 2 : BN;
   bool ok = make_map(&p.tmA0, d.A0, d.K0, d.M, d.lda0, BM);
   if (d.b0_mn) {
     ok = ok && make_map(&p.tmB0, d.B0, d.N, d.b0_rows, d.ldb0, 64);
@@ -1199,7 +1273,7 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.num_m_tiles = (d.M + tile_m - 1) / tile_m;
   const int n_out = stacked ? BN / 2 : BN;
   p.num_n_tiles = (d.N + n_out - 1) / n_out;
-  p.group_m = pair ? 8 : 16;
+  p.group_m = (pair || mc) ? 8 : 16;   // in M units of the tile sequence (MC: pairs of tiles)
   p.k0_split_steps = d.b0_mn && d.B0b ? (d.k0_split / BK) : (1 << 30);
   p.tail_b1b_x = d.b1b_x;
   p.tail_b1_x = d.b1_x;
@@ -1211,14 +1285,14 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.ld_eu = d.ld_eu;
   p.err = d.err;
   p.timeout_ns = d.timeout_ns;
-  const int tiles = p.num_m_tiles * p.num_n_tiles;
+  const int tiles = (mc ? p.num_m_tiles / 2 : p.num_m_tiles) * p.num_n_tiles;
 
   // algorithmic flops of this launch: the base contraction plus the rank-r tail
   const double ntot = stacked ? 2.0 * d.N : (double)d.N;
   const double k1 = d.has_tail ? (stacked ? d.K1 / 2.0 : (double)d.K1) : 0.0;
   const double flops = 2.0 * d.M * ntot * ((double)d.K0 + k1);
   prof_mark(st, true, flops);
-  const cudaError_t e = launch_mode(d, p, st, pair, tiles);
+  const cudaError_t e = launch_mode(d, p, st, pair ? 1 : (mc ? 2 : 0), tiles);
   prof_mark(st, false, 0.0);
   return e;
 }

@@ -1,6 +1,7 @@
-"""Both tcgen05 GEMM kernels against the oracle: the one-CTA kernel (128 x 256 tiles) and the
-CTA-pair kernel (cta_group::2, 256 x 256 tiles over two SMs), selected per call with
-LORA_GB300_GEMM_PAIR, in every mode the layer uses (forward, dX with MN-major B, dX with the
+"""Both tcgen05 GEMM kernels against the oracle: the one-CTA kernel (128 x 256 tiles), also in
+its two-CTA form that multicasts each B tile to two M-adjacent tiles (LORA_GB300_GEMM_MC, used
+where the number of M tiles is even), and the CTA-pair kernel (cta_group::2, 256 x 256 tiles over
+two SMs), selected per call with LORA_GB300_GEMM_PAIR, in every mode the layer uses (forward, dX with MN-major B, dX with the
 DoRA K-scaling warps, SwiGLU forward with stacked B, SwiGLU backward), with ragged M, N, K and
 with a capped grid so that every CTA (pair) runs several tiles."""
 import pytest
@@ -22,9 +23,10 @@ def ops():
     return _ops
 
 
-@pytest.fixture(params=["one_cta", "pair"])
+@pytest.fixture(params=["one_cta", "multicast", "pair"])
 def variant(request, monkeypatch):
     monkeypatch.setenv("LORA_GB300_GEMM_PAIR", "1" if request.param == "pair" else "0")
+    monkeypatch.setenv("LORA_GB300_GEMM_MC", "1" if request.param == "multicast" else "0")
     return request.param
 
 
@@ -54,13 +56,33 @@ def test_lora_fwd_bwd(ops, variant, cap, monkeypatch):
     _ws_ok(ops)
 
 
+@pytest.mark.parametrize("cap", ["0", "4"])
+@pytest.mark.parametrize("M", [500, 1024])
+def test_lora_even_m_tiles(ops, variant, cap, M, monkeypatch):
+    """An even number of M tiles (4 with a ragged last one, and 8), the case where the multicast
+    form of the one-CTA kernel runs; ragged N and K."""
+    monkeypatch.setenv("LORA_GB300_MAX_CTAS", cap)
+    case = D.scaled(D.WORKLOADS["lora_4096_bf16"], M=M, d_in=328, d_out=776, r=16, bias=True)
+    t = D.make_linear(case)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s, g["bias"])
+    X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
+    assert_close(Y, O.lora_linear_fwd(X, W0, A, B, case.s, f64(t["bias"])), "bf16", "Y")
+    dX, dA, dB, _ = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
+    rX, rA, rB, _ = O.lora_linear_bwd(X, W0, A, B, case.s, f64(t["dY"]))
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dB, rB, "bf16", "dB")
+    _ws_ok(ops)
+
+
 @pytest.mark.parametrize("kscale", ["0", "1"])
 def test_dora_kscaled_dx(ops, variant, kscale, monkeypatch):
     """dP = dY o c enters the dX GEMM as a copy written by the column pass (kscale 0) or scaled
     tile by tile in the GEMM's shared memory (kscale 1)."""
     monkeypatch.setenv("LORA_GB300_MAX_CTAS", "4")
     monkeypatch.setenv("LORA_GB300_DORA_KSCALE", kscale)
-    case = D.scaled(D.WORKLOADS["dora_4096x11008_bf16"], M=600, d_in=328, d_out=776, r=32)
+    case = D.scaled(D.WORKLOADS["dora_4096x11008_bf16"], M=500, d_in=328, d_out=776, r=32)
     t = D.make_linear(case)
     g = {k: v.to(DEV) for k, v in t.items()}
     r0 = ops.dora_rownorm2(g["W0"])
@@ -84,7 +106,7 @@ def test_dora_kscaled_dx(ops, variant, kscale, monkeypatch):
 @pytest.mark.parametrize("I", [200, 384])
 def test_mlp_swiglu(ops, variant, I, monkeypatch):
     monkeypatch.setenv("LORA_GB300_MAX_CTAS", "4")
-    case = D.scaled(D.WORKLOADS["mlp_swiglu_4096x14336_bf16"], M=600, H=200, I=I, r=16, alpha=24.0)
+    case = D.scaled(D.WORKLOADS["mlp_swiglu_4096x14336_bf16"], M=500, H=200, I=I, r=16, alpha=24.0)
     t = D.make_mlp(case)
     g = {k: v.to(DEV) for k, v in t.items()}
     P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
@@ -105,7 +127,7 @@ def test_mlp_swiglu(ops, variant, I, monkeypatch):
 def test_qkv_multistep_tail(ops, variant, monkeypatch):
     """L r = 96: the rank-r tail of both GEMMs spans two K-steps (leaves in two groups)."""
     monkeypatch.setenv("LORA_GB300_MAX_CTAS", "4")
-    case = D.scaled(D.WORKLOADS["qkv_lora_4096_gqa_bf16"], M=300, d_in=200, n=(256, 72, 72), r=32)
+    case = D.scaled(D.WORKLOADS["qkv_lora_4096_gqa_bf16"], M=250, d_in=200, n=(256, 72, 72), r=32)
     t = D.make_qkv(case)
     g = {k: None if v is None else v.to(DEV) for k, v in t.items()}
     lg_ = [(g[f"A{l}"], g[f"B{l}"], case.s[l]) for l in range(3)]
