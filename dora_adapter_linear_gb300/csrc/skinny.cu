@@ -14,12 +14,14 @@ namespace lg {
 
 // ============================================================================ rowproj
 // One CTA owns 32 rows of S and streams them across K in 64-wide stages: a producer warp
-// issues one TMA box for the S tile (32 x 64, 128B-swizzled) and one for the matching U tile,
-// two consumer warps (16 rows each) run the warp MMAs straight from the swizzled tiles.
+// issues one TMA box for the S tile (32 x 64, 128B-swizzled) and one for the matching U tile;
+// the consumer warps (16 rows each, two K groups taking alternate stages) run the warp MMAs
+// straight from the swizzled tiles, and the second K group's sums are added through shared
+// memory at the end.  One K group left the MMA chain of each warp, not the memory system, as
+// the limit (3.2 TB/s from L2).
 namespace rp {
 constexpr int BMR = 32;   // rows per CTA
 constexpr int BK = 64;    // K per stage (one 128-byte swizzle row)
-constexpr int NST = 8;    // stages in flight per CTA
 constexpr int S_BYTES = BMR * 128;
 
 // byte offset of 16-byte chunk `chunk` of row `row` in a TMA-swizzled tile whose rows are
@@ -40,12 +42,18 @@ struct Cfg {
   static constexpr int U_BYTES = U_KR ? BK * RPAD * 2 : UROWS * 128;
   static constexpr int U_TX = U_KR ? BK * RPAD * 2 : R * 128;   // bytes the U box delivers
   static constexpr int STAGE = (S_BYTES + U_BYTES + 1023) / 1024 * 1024;
+  // stages in flight: about 96 KB per CTA (two CTAs per SM); 8 stages of the small ranks left
+  // the pass latency-bound
+  static constexpr int NST = (96 * 1024 / STAGE) > 16 ? 16 : ((96 * 1024 / STAGE) < 8 ? 8 : 96 * 1024 / STAGE);
   // consumer warps: 2 row groups of 16 x NG groups of output columns (split when R / 8 is even
   // and large enough, so that more warps share the MMA work of one tile)
   static constexpr int NG = (R % 16 == 0 && R >= 32) ? 2 : 1;
   static constexpr int NTW = R / 8 / NG;   // n-tiles of 8 per consumer warp
-  static constexpr int THREADS = 32 * (2 * NG + 1);
-  static constexpr int SMEM = NST * STAGE + 1024 + 2 * NST * 8 + 16;
+  static constexpr int KG = 2;             // K groups: consumer warp sets taking alternate stages
+  static constexpr int NCW = 2 * NG * KG;  // consumer warps; the producer is warp NCW
+  static constexpr int THREADS = 32 * (NCW + 1);
+  static constexpr int RED = (NCW - 2 * NG) * 32 * NTW * 4 * 4;   // partial sums of the K groups > 0
+  static constexpr int SMEM = NST * STAGE + RED + 1024 + 2 * NST * 8 + 16;
 };
 }  // namespace rp
 
@@ -62,14 +70,15 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
   const RowProjDesc& d = P.d;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * C::STAGE);
-  uint64_t* empty = full + NST;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NST);
+  float* red = reinterpret_cast<float*>(smem + C::NST * C::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::NST * C::STAGE + C::RED);
+  uint64_t* empty = full + C::NST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::NST);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row0 = (int64_t)blockIdx.x * BMR;
   const int nkc = (int)((d.K + BK - 1) / BK);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) {
+    for (int i = 0; i < C::NST; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 2 * C::NG);
     }
@@ -80,16 +89,16 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
   pdl_wait();      // S and U may come from the previous kernel in the stream
   if (threadIdx.x == 0) pdl_trigger();
 
-  if (warp == 2 * C::NG) {
+  if (warp == C::NCW) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&P.tmS);
       tma_prefetch_desc(&P.tmU);
       bool ok = true;
       for (int kc = 0; kc < nkc; ++kc) {
-        const int s = kc % NST;
-        const uint32_t ph = (uint32_t)(kc / NST) & 1u;
-        if (kc >= NST && !mbar_wait(&empty[s], ph ^ 1u, d.timeout_ns, abort_flag, d.err, 0x301)) {
+        const int s = kc % C::NST;
+        const uint32_t ph = (uint32_t)(kc / C::NST) & 1u;
+        if (kc >= C::NST && !mbar_wait(&empty[s], ph ^ 1u, d.timeout_ns, abort_flag, d.err, 0x301)) {
           ok = false;
           break;
         }
@@ -106,15 +115,16 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
 
   // ------------------------------------------------------------------ consumers: 16 rows x R / NG each
   constexpr int NTW = C::NTW;
-  const int rg = warp & 1;    // row group (rows 16 rg .. 16 rg + 15 of the tile)
-  const int nh = warp >> 1;   // column group (n-tiles nh NTW .. nh NTW + NTW - 1)
+  const int rg = warp & 1;                  // row group (rows 16 rg .. 16 rg + 15 of the tile)
+  const int nh = (warp >> 1) % C::NG;       // column group (n-tiles nh NTW .. nh NTW + NTW - 1)
+  const int kg = warp / (2 * C::NG);        // K group: stages kg, kg + KG, ...
   float acc[NTW][4];
 #pragma unroll
   for (int i = 0; i < NTW; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
   const int c8 = lane & 7;  // the 16-byte chunk this lane copies in the scaled side output
-  for (int kc = 0; kc < nkc; ++kc) {
-    const int s = kc % NST;
-    const uint32_t ph = (uint32_t)(kc / NST) & 1u;
+  for (int kc = kg; kc < nkc; kc += C::KG) {
+    const int s = kc % C::NST;
+    const uint32_t ph = (uint32_t)(kc / C::NST) & 1u;
     if (!mbar_wait(&full[s], ph, d.timeout_ns, abort_flag, d.err, 0x302)) break;
     const uint8_t* tile = smem + s * C::STAGE;
     const uint32_t sS = smem_u32(tile);
@@ -165,6 +175,28 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // add the other K groups' sums into K group 0, which writes the outputs
+  {
+    const int slot = warp % (2 * C::NG);
+    if (kg > 0) {
+      float* dst = red + (((kg - 1) * 2 * C::NG + slot) * 32 + lane) * NTW * 4;
+#pragma unroll
+      for (int q = 0; q < NTW; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[q * 4 + e] = acc[q][e];
+    }
+    named_bar_sync(1, 32 * C::NCW);
+    if (kg > 0) return;
+#pragma unroll
+    for (int j = 1; j < C::KG; ++j) {
+      const float* src = red + (((j - 1) * 2 * C::NG + slot) * 32 + lane) * NTW * 4;
+#pragma unroll
+      for (int q = 0; q < NTW; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[q][e] += src[q * 4 + e];
+    }
   }
 
   const int g = lane >> 2, t = lane & 3;
@@ -427,12 +459,24 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
 
 int colreduce_splits(int64_t rows, int64_t K) {
   const int64_t kb = (K + cr::BKC - 1) / cr::BKC;
-  int64_t want = (4LL * num_sms_current() + kb - 1) / kb;
-  const int64_t maxs = (rows + cr::BR - 1) / cr::BR;
-  if (want > maxs) want = maxs;
-  if (want < 1) want = 1;
-  if (want > 64) want = 64;
-  return (int)want;
+  // Row splits per column block: with three CTAs resident per SM, a launch of kb * s CTAs runs
+  // in ceil(kb s / slots) waves of CTAs that each stream ceil(rows / (64 s)) row stages plus a
+  // fixed cost of about four stages (ring fill, partial sums); pick the s with the least total,
+  // the fewest splits among equals.  A half-empty last wave cost ~1% of a LoRA step.
+  const int64_t slots = 3LL * num_sms_current();
+  int64_t maxs = (rows + cr::BR - 1) / cr::BR;
+  if (maxs > 64) maxs = 64;
+  int64_t best = 1;
+  double best_t = 1e30;
+  for (int64_t sp = 1; sp <= maxs; ++sp) {
+    const int64_t stages = (rows + cr::BR * sp - 1) / (cr::BR * sp);
+    const double t = (double)((kb * sp + slots - 1) / slots) * (double)(stages + 4);
+    if (t < best_t - 1e-12) {
+      best_t = t;
+      best = sp;
+    }
+  }
+  return (int)best;
 }
 
 template <int R, bool HAS_Y, bool SUMS>
