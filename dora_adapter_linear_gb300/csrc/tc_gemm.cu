@@ -754,9 +754,9 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
 //   ready[s]     leader, K-scaling only: one arrival per CTA after its scaling warps finish
 //   empty[s]     both CTAs: the leader's MMA commit, multicast to the pair
 //   acc_full[b]  both CTAs: the leader's MMA commit, multicast
-//   acc_empty[b] leader: 4 epilogue warps x 2 CTAs
+//   acc_empty[b] leader: 4 epilogue warps (8 for the plain scale/bias epilogue) x 2 CTAs
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
-__global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_pair_kernel(const __grid_constant__ TcParams p) {
   using L = Layout<EPI, true>;
   constexpr int STAGES = L::STAGES;
   constexpr int N_OUT = STACKED ? BN / 2 : BN;        // logical output columns per tile
@@ -795,7 +795,7 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 8);
+      mbar_init(&acc_empty[i], OneCta<EPI, KSCALE>::EPI8 ? 16 : 8);   // epilogue warps x 2 CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -935,10 +935,12 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
       mbar_wait_drain(drain, 0, 20000000ull);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < (OneCta<EPI, KSCALE>::EPI8 ? 10 : 6)) {
     // ---------------------------------------------------------------- epilogue (both CTAs)
-    const int q = warp & 3;
-    uint8_t* my_stg = sStg + (warp - 2) * (EpiCfg<EPI, true>::STG_BUFS * 4096);
+    constexpr bool EPI8 = OneCta<EPI, KSCALE>::EPI8;
+    const int q = warp & 3;                         // TMEM lane quarter this warp may access
+    const int half = EPI8 ? (warp - 2) >> 2 : 0;    // with 8 warps: which half of the columns
+    uint8_t* my_stg = sStg + (warp - 2) * (EPI8 ? 4096 : EpiCfg<EPI, true>::STG_BUFS * 4096);
     int it = 0;
     uint32_t chunk_ctr = 0;
     for (int t = cluster_id; t < num_tiles; t += num_clusters, ++it) {
@@ -948,8 +950,12 @@ __global__ void __launch_bounds__(KSCALE ? 320 : 192, 1) tc_pair_kernel(const __
       tc_fence_after();
       int mt, nt;
       tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt);
-      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + buf * BN;
-      epilogue_tile<EPI, N_OUT>(p, t_row, mt * PM + (int)rank * BM + 32 * q, nt * N_OUT, lane, my_stg, chunk_ctr);
+      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + buf * BN + half * (N_OUT / 2);
+      const int row0 = mt * PM + (int)rank * BM + 32 * q;
+      if constexpr (EPI8)
+        epilogue_tile<EPI, N_OUT / 2>(p, t_row, row0, nt * N_OUT + half * (N_OUT / 2), lane, my_stg, chunk_ctr);
+      else
+        epilogue_tile<EPI, N_OUT>(p, t_row, row0, nt * N_OUT, lane, my_stg, chunk_ctr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[buf]), 0));
@@ -1132,7 +1138,7 @@ static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(KSCALE ? 320 : 192, 1, 1);
+  cfg.blockDim = dim3(OneCta<EPI, KSCALE>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = L::TOTAL;
   cfg.stream = st;
   cfg.attrs = attr;
