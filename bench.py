@@ -272,9 +272,10 @@ def timed(fn, steps, warmup, dist=None):
 # DRAM bytes (read + write) per GEMM launch from ncu captures, keyed by workload; a value is
 # dropped (None) whenever the kernel changes and is re-measured before it is put back.
 # lora_4096_bf16: dram__bytes_read.sum + dram__bytes_write.sum of the forward (CTA pair) and dX
-# (one CTA) GEMM launches of the headline step (mean of 4 launches: 147.2 MB read + 43.6 MB
-# written; the algorithmic bytes are 64 MiB activation + 32 MiB weight + 64 MiB output = 167.8 MB).
-GEMM_TRAFFIC = {"lora_4096_bf16": None}
+# (one-CTA kernel, two-CTA clusters sharing B) GEMM launches of the headline step (mean of 4
+# launches: 150.4 MB read + 45.3 MB written; the algorithmic bytes are 64 MiB activation +
+# 32 MiB weight + 64 MiB output = 167.8 MB).
+GEMM_TRAFFIC = {"lora_4096_bf16": 195.7e6}
 
 
 def gemm_roofline(L, peaks, ms_step, steps_recorded, sustained, workload):
