@@ -1105,9 +1105,7 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       }
       CK(colreduce(d, st));
     }
-    CK(sum_splits<float>(w.dotp, w.splitsB, out, w.dot, nullptr, st));
-    CK(sum_splits<float>(w.csump, w.splitsB, out, w.csum, nullptr, st));
-    CK(dora_dc<bf16>(out, w.dot, w.csum, static_cast<const bf16*>(bias), w.c, n_saved, mb, eps, w.g,
+    CK(dora_dc<bf16>(out, w.dotp, w.csump, w.splitsB, static_cast<const bf16*>(bias), w.c, n_saved, mb, eps, w.g,
                      static_cast<bf16*>(dm), static_cast<bf16*>(dbias), st));
     CK(scale_rows<bf16>(static_cast<const bf16*>(B), out, r, w.c, 1.f, static_cast<bf16*>(w.Bc), st));
     CK(scale_rows<bf16>(static_cast<const bf16*>(B), out, r, w.g, 1.f, static_cast<bf16*>(w.gB), st));
@@ -1146,7 +1144,7 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       Z = w.Zrec;
     }
     CK(coldot_f32(static_cast<const float*>(dY), static_cast<const float*>(Y), M, out, w.csum, w.dot, st));
-    CK(dora_dc<float>(out, w.dot, w.csum, static_cast<const float*>(bias), w.c, n_saved, mf, eps, w.g,
+    CK(dora_dc<float>(out, w.dot, w.csum, 1, static_cast<const float*>(bias), w.c, n_saved, mf, eps, w.g,
                       static_cast<float*>(dm), static_cast<float*>(dbias), st));
     {  // G = (dY o c) B
       SgemmDesc d = sg(M, r, out, dY, out, false, B, r, false, w.Gs, r);
@@ -1303,9 +1301,9 @@ lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, c
     d.coldot = w.dotp;
     CK(colreduce(d, st));
   }
-  CK(sum_splits<float>(w.dotp, w.splitsA, in, w.dot, nullptr, st));
   // dc = dot / c (no bias term), dm = dc / n, g = -m dc / (2 n^3)
-  CK(dora_dc<bf16>(in, w.dot, w.dot, nullptr, w.c, n_saved, mb, eps, w.g, static_cast<bf16*>(dm), nullptr, st));
+  CK(dora_dc<bf16>(in, w.dotp, nullptr, w.splitsA, nullptr, w.c, n_saved, mb, eps, w.g, static_cast<bf16*>(dm), nullptr,
+                   st));
   CK(gram_bf16(B, B, out, r, w.Kb, w.Gw, w.err, st));
   CK(gram_rows_weighted(Ab, r, in, w.g, w.Kga, st));
   CK(scale_cols_bf16(Ab, r, in, w.g, w.Ag, st));

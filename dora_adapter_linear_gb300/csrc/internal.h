@@ -153,9 +153,10 @@ cudaError_t sum_splits(const float* src, int splits, int64_t n, float* dst_f, T*
 // c = m / n
 template <typename T>
 cudaError_t dora_c(int64_t out, const T* m, const float* n, float* c, cudaStream_t st);
-// DoRA backward small step: dc = (dot - bias*colsum)/c ; dm = dc/n ; g = -m dc/(2 n^3) (0 if n<=eps)
+// DoRA backward small step: dc = (dot - bias*colsum)/c ; dm = dc/n ; g = -m dc/(2 n^3) (0 if n<=eps);
+// dot and csum are [splits, out] partials (csum read only with a bias or dbias).
 template <typename T>
-cudaError_t dora_dc(int64_t out, const float* dot, const float* csum, const T* bias, const float* c,
+cudaError_t dora_dc(int64_t out, const float* dot, const float* csum, int splits, const T* bias, const float* c,
                     const float* n, const T* m, float eps, float* g, T* dm, T* dbias, cudaStream_t st);
 // out[o, j] = scale[o] * B[o, j] (bf16 / T out), scale may be null (=1), with extra factor f.
 template <typename T>

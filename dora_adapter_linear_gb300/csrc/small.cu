@@ -218,24 +218,31 @@ cudaError_t sum_splits(const float* src, int splits, int64_t n, float* dst_f, T*
 }
 
 // ------------------------------------------------------------------ DoRA dc -> dm, g, dbias
+// dot and csum are [splits, out] partial sums (of the row splits of the column pass), added here.
 template <typename T>
-__global__ void dora_dc_kernel(int64_t out, const float* dot, const float* csum, const T* bias, const float* c,
-                               const float* n, const T* m, float eps, float* g, T* dm, T* dbias) {
+__global__ void dora_dc_kernel(int64_t out, const float* dot, const float* csum, int splits, const T* bias,
+                               const float* c, const float* n, const T* m, float eps, float* g, T* dm, T* dbias) {
   const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (o >= out) return;
+  float dt = 0.f, cs = 0.f;
+  for (int sp = 0; sp < splits; ++sp) dt += dot[(int64_t)sp * out + o];
+  if (bias || dbias)
+    for (int sp = 0; sp < splits; ++sp) cs += csum[(int64_t)sp * out + o];
   const float b = bias ? ldf(bias, o) : 0.f;
   // P = (Y - bias) / c  =>  sum dY * P = (sum dY*Y - bias * sum dY) / c
-  const float dc = (dot[o] - b * csum[o]) / c[o];
+  const float dc = (dt - b * cs) / c[o];
   const float nn = n[o];
   dm[o] = from_f<T>(dc / nn);
   g[o] = nn > eps ? -ldf(m, o) * dc / (2.f * nn * nn * nn) : 0.f;
-  if (dbias) dbias[o] = from_f<T>(csum[o]);
+  if (dbias) dbias[o] = from_f<T>(cs);
 }
 template <typename T>
-cudaError_t dora_dc(int64_t out, const float* dot, const float* csum, const T* bias, const float* c, const float* n,
-                    const T* m, float eps, float* g, T* dm, T* dbias, cudaStream_t st) {
+cudaError_t dora_dc(int64_t out, const float* dot, const float* csum, int splits, const T* bias, const float* c,
+                    const float* n, const T* m, float eps, float* g, T* dm, T* dbias, cudaStream_t st) {
   if (out <= 0) return cudaSuccess;
-  dora_dc_kernel<T><<<(unsigned)((out + 255) / 256), 256, 0, st>>>(out, dot, csum, bias, c, n, m, eps, g, dm, dbias);
+  if ((bias || dbias) && !csum) return cudaErrorInvalidValue;
+  dora_dc_kernel<T><<<(unsigned)((out + 255) / 256), 256, 0, st>>>(out, dot, csum, splits, bias, c, n, m, eps, g,
+                                                                     dm, dbias);
   count_launch();
   return cudaGetLastError();
 }
@@ -688,7 +695,7 @@ cudaError_t debug_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t 
                                     float, float, float*, float*, cudaStream_t);                                    \
   template cudaError_t dora_c<T>(int64_t, const T*, const float*, float*, cudaStream_t);                            \
   template cudaError_t sum_splits<T>(const float*, int, int64_t, float*, T*, cudaStream_t);                         \
-  template cudaError_t dora_dc<T>(int64_t, const float*, const float*, const T*, const float*, const float*,        \
+  template cudaError_t dora_dc<T>(int64_t, const float*, const float*, int, const T*, const float*, const float*,        \
                                   const T*, float, float*, T*, T*, cudaStream_t);                                   \
   template cudaError_t scale_rows<T>(const T*, int64_t, int, const float*, float, T*, cudaStream_t);                \
   template cudaError_t finalize_dA<T>(int, int64_t, Partial, float, Partial, float, const float*, float, const T*,  \
