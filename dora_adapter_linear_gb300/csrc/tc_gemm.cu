@@ -9,7 +9,8 @@
 // ("LoRA/DoRA fast forward: no weight materialization", What section).
 //
 // Two kernels share the stage layout, the epilogues and the A-tile scaling:
-//  * tc_gemm_kernel: one CTA per SM, 128 x 256 tile (cta_group::1).
+//  * tc_gemm_kernel: one CTA per SM, 128 x 256 tile (cta_group::1); for the MN-major products
+//    it runs in clusters of two CTAs on M-adjacent tiles that share each B tile by TMA multicast.
 //  * tc_pair_kernel: a cluster of two CTAs on two SMs computes a 256 x 256 tile with
 //    cta_group::2 MMAs issued by the even CTA; each SM stages its 128 rows of A and half of
 //    B, so the operand bytes per SM and k-step drop from 48 KB to 32 KB.
@@ -456,9 +457,10 @@ struct OneCta {
 };
 
 // MC: a cluster of two CTAs on two M-adjacent tiles of the same N range; each CTA loads half of
-// every B tile and multicasts it to both, so each SM reads 32 KB of operands per k-step instead of
-// 48 KB.  A stage is free again once both CTAs' MMAs have read it: empty[s] takes one commit
-// from each CTA (multicast), and neither CTA exits while its peer may still write into it.
+// every B tile and multicasts it to both, so L2 serves 32 KB of operand reads per SM and k-step
+// instead of 48 KB (each SM still receives 48 KB).  A stage is free again once both CTAs' MMAs
+// have read it: empty[s] takes one commit from each CTA (multicast), and neither CTA exits while
+// its peer may still write into it.
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE, bool MC>
 __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   static_assert(!(MC && (STACKED || KSCALE || EPI == EPI_W8A8)), "multicast mode: plain K-major or MN-major B only");
