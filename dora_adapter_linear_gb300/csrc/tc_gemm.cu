@@ -1282,8 +1282,9 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   const int n_out = stacked ? BN / 2 : BN;
   p.num_n_tiles = (d.N + n_out - 1) / n_out;
   // raster group in M units of the tile sequence (pair tiles, or MC pairs of tiles): measured,
-  // the multicast dX runs best with 4 pairs at K <= 4096 and 8 above
-  p.group_m = pair ? 8 : (mc ? (d.K0 <= 4096 ? 4 : 8) : 16);
+  // the multicast dX runs best with 4 pairs when both K and N are at most 4096 (the whole
+  // weight then stays in L2 across groups) and with 8 otherwise (4 costs 8-10% at N = 11008)
+  p.group_m = pair ? 8 : (mc ? ((d.K0 <= 4096 && d.N <= 4096) ? 4 : 8) : 16);
   p.k0_split_steps = d.b0_mn && d.B0b ? (d.k0_split / BK) : (1 << 30);
   p.tail_b1b_x = d.b1b_x;
   p.tail_b1_x = d.b1_x;
