@@ -1060,6 +1060,13 @@ int num_sms_current() {
   return cached[dev];
 }
 
+// index of the current device in the per-device caches of the launch helpers
+static int current_device_slot() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return (dev < 0 || dev >= 64) ? 0 : dev;
+}
+
 static int env_int(const char* name, int dflt) {
   const char* e = getenv(name);
   return e ? atoi(e) : dflt;
@@ -1098,7 +1105,8 @@ static cudaError_t launch_one_k(const TcParams& p, cudaStream_t st, int tiles) {
     attr[0].val.clusterDim.z = 1;
     cfg.numAttrs = 1;
   }
-  static int max_units = 0;   // co-resident CTAs (clusters for MC)
+  static int max_units_dev[64] = {0};   // co-resident CTAs (clusters for MC), per device
+  int& max_units = max_units_dev[current_device_slot()];
   if (max_units == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
     if (e != cudaSuccess) return e;
@@ -1133,7 +1141,8 @@ template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSC
 static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
   using L = Layout<EPI, true>;
   auto kern = tc_pair_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
-  static int max_clusters = 0;
+  static int max_clusters_dev[64] = {0};   // co-resident clusters, per device
+  int& max_clusters = max_clusters_dev[current_device_slot()];
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
