@@ -97,6 +97,36 @@ def test_entry_points_validate_before_launch(lib):
     assert r == 1  # up projection missing
 
 
+def test_dropout_entry_points_validate_before_launch(lib):
+    """The input-dropout calls: bf16 only, a mask for M > 0, a finite non-negative keep scale and
+    a workspace that also holds the masked input; nothing is launched on any of these errors."""
+    sh = L.shape(64, 256, 256, 8, L.LORA_BF16)
+    fake = ctypes.c_void_p(1 << 20)
+    ws_need = L.lora_workspace_bytes(L.OP_DROPOUT_FWD, sh)
+    assert ws_need >= L.lora_workspace_bytes(L.OP_LINEAR_FWD, sh) + 64 * 256 * 2
+    f32 = L.shape(64, 256, 256, 8, L.LORA_F32)
+    r = lib.lora_linear_dropout_fwd(ctypes.byref(f32), fake, fake, 2.0, fake, fake, fake, None, 1.0, fake, None,
+                                    fake, 1 << 30, None)
+    assert r == 2  # UNSUPPORTED: bf16 only
+    r = lib.lora_linear_dropout_fwd(ctypes.byref(sh), fake, None, 2.0, fake, fake, fake, None, 1.0, fake, None,
+                                    fake, 1 << 30, None)
+    assert r == 1  # mask is NULL
+    for bad_scale in (-1.0, float("nan"), float("inf")):
+        r = lib.lora_linear_dropout_fwd(ctypes.byref(sh), fake, fake, bad_scale, fake, fake, fake, None, 1.0, fake,
+                                        None, fake, 1 << 30, None)
+        assert r == 1
+    r = lib.lora_linear_dropout_fwd(ctypes.byref(sh), fake, fake, 2.0, fake, fake, fake, None, 1.0, fake, None,
+                                    fake, ws_need - 256, None)
+    assert r == 4  # workspace too small for the masked input
+    wb = L.lora_workspace_bytes(L.OP_DROPOUT_BWD, sh)
+    r = lib.lora_linear_dropout_bwd(ctypes.byref(sh), fake, None, 2.0, fake, fake, fake, None, fake, 1.0, fake, fake,
+                                    fake, None, fake, wb, None)
+    assert r == 1  # mask is NULL
+    r = lib.lora_linear_dropout_bwd(ctypes.byref(sh), fake, fake, 2.0, fake, fake, fake, None, fake, 1.0, fake, fake,
+                                    fake, None, fake, wb - 256, None)
+    assert r == 4
+
+
 def test_qkv_validation(lib):
     """Fused-leaf shapes and arguments are validated before anything is launched."""
     ok = L.qkv_shape(64, 256, [256, 64, 64], 16)
