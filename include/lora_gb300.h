@@ -196,7 +196,10 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
  * share of dX is a separate masked rank-r pass instead of the dX GEMM's tail.
  * "Fused Kernels (experimental)" (LyCORIS docs), the note that a call whose mask sits between
  * two factors takes the unfused path; "How Unsloth's FastLoRA Kernel Differs ...", Optimized
- * Dropout and Scaling.  LORA_BF16 only; other arguments as lora_linear_fwd / _bwd.
+ * Dropout and Scaling.  LORA_BF16 only (else LORA_ERR_UNSUPPORTED); other arguments as
+ * lora_linear_fwd / _bwd.  mask must be 16-byte aligned and non-NULL when M > 0, keep_scale finite
+ * and >= 0 (else LORA_ERR_INVALID_ARG); the workspace is the plain layer's plus M * d_in * 2 bytes
+ * (lora_workspace_bytes with LORA_OP_DROPOUT_FWD / _BWD).
  *   Backward: G = s dY B;  dX = dY W0 + (G A) o mask * keep_scale;  dA = G^T Xd;
  *             dB = s dY^T Z (Z = Xd A^T, saved by the forward or NULL to recompute);
  *             dbias = colsum(dY).
@@ -209,7 +212,7 @@ lora_status lora_linear_dropout_bwd(const lora_shape* sh, const void* X, const u
                                     const void* dY, float s, void* dX, void* dA, void* dB, void* dbias,
                                     void* ws, size_t ws_bytes, void* stream);
 
-/* ---------------------------------------------------------------- DoRA (rows)/* ---------------------------------------------------------------- DoRA (rows)
+/* ---------------------------------------------------------------- DoRA (rows)
  * r0[o] = sum_k W0[o,k]^2 in fp32: the cached per-layer constant of the closed-form norm.
  * "LoRA/DoRA fast forward ...", commit message (cached rowsum(W0^2) constant) and What
  * section (the cached norm constant is a per-layer vector).  r0: [d_out] fp32 output.
