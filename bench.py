@@ -432,8 +432,9 @@ def headline(args, L, ops, dist, world, peaks):
     }
 
 
-def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8", "qkv")):
-    """DoRA, gated MLP, W8A8 and fused-QKV workloads, each a fwd+bwd step (W8A8 also fwd alone)."""
+def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8", "qkv", "dropout")):
+    """DoRA, gated MLP, W8A8, fused-QKV and input-dropout workloads, each a fwd+bwd step (W8A8 also
+    fwd alone)."""
     import torch
 
     import datagen as D
@@ -449,6 +450,37 @@ def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8", "qkv")):
         out.update(_w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm))
     if "qkv" in which:
         out.update(_qkv_workload(args, L, ops, peaks, D, dev, steps, warm))
+    if "dropout" in which:
+        out.update(_dropout_workload(args, L, ops, peaks, D, dev, steps, warm))
+    return out
+
+
+def _dropout_workload(args, L, ops, peaks, D, dev, steps, warm, p=0.1):
+    """The headline LoRA layer with input dropout (keep mask drawn once, p = 0.1), forward +
+    backward on the unfused path; the flops counted are the plain layer's."""
+    import torch
+    case = D.WORKLOADS[HEADLINE]
+    t = D.make_linear(case)
+    g = {k: v.to(dev) for k, v in t.items() if v is not None}
+    mask = D.make_dropout_mask(case.M, case.d_in, p).to(dev)
+    keep = 1.0 / (1.0 - p)
+
+    def drop_step():
+        Y, Z = ops.lora_linear_dropout_fwd(g["X"], mask, keep, g["W0"], g["A"], g["B"], case.s)
+        ops.lora_linear_dropout_bwd(g["X"], mask, keep, g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
+    ms, _, _ = timed(drop_step, steps, warm)
+    ms_ev = timed_gemm_events(L, drop_step, steps)
+    f, b = lora_flops(case.M, case.d_in, case.d_out, case.r)
+    name = "lora_dropout_4096_bf16"
+    out = {name: {"ms_per_step": ms, "tflops": (f + b) / (ms * 1e-3) / 1e12,
+                  "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                  "note": f"keep mask with p = {p}; unfused: the masked input is written once per call",
+                  "roofline": gemm_roofline(L, peaks, ms_ev, steps + 1, False, name)}}
+    for buf in ops._WS.values():
+        if L.lora_check_device_error(buf) != 0:
+            raise RuntimeError("a kernel recorded a timed-out wait in the dropout workload")
+    del g, t, mask
+    torch.cuda.empty_cache()
     return out
 
 
@@ -599,7 +631,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads", default="all", choices=["all", "headline"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default=None, choices=["dora", "mlp", "w8a8", "qkv"],
+    ap.add_argument("--only", default=None, choices=["dora", "mlp", "w8a8", "qkv", "dropout"],
                     help="time one non-headline workload alone (for profiling) and print its record")
     args = ap.parse_args()
     if args.warmup < 3:
