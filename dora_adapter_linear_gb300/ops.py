@@ -23,7 +23,34 @@ def _shape_of(X, W0, A):
     return L.shape(X.shape[0], X.shape[1], W0.shape[0], A.shape[0], L.dtype_code(X))
 
 
+def _check_linear(X, W0, A, B, bias=None, Z=None, dY=None, Y=None):
+    """The kernels trust the shapes they are given (tensor maps and strides come from them), so a
+    mismatched tensor would be read out of bounds: check every operand against X [M, in],
+    W0 [out, in], A [r, in] before anything is launched."""
+    if X.dim() != 2 or W0.dim() != 2:
+        raise ValueError("X and W0 must be 2-D")
+    M, d_in = X.shape
+    d_out, r = W0.shape[0], A.shape[0]
+    want = {"W0": (W0, (d_out, d_in)), "A": (A, (r, d_in)), "B": (B, (d_out, r)), "bias": (bias, (d_out,)),
+            "Z": (Z, (M, r)), "dY": (dY, (M, d_out)), "Y": (Y, (M, d_out))}
+    if W0.shape[1] != d_in:
+        raise ValueError(f"W0 {tuple(W0.shape)} does not match X {tuple(X.shape)}")
+    for name, (t, shape) in [("X", (X, (M, d_in)))] + list(want.items()):
+        if t is None:
+            continue
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {shape}, got {tuple(t.shape)}")
+        if t.dtype != X.dtype or t.device != X.device or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {X.dtype} tensor on {X.device}")
+
+
+def _check_vec(name, t, n, X):
+    if t is not None and (tuple(t.shape) != (n,) or t.device != X.device or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous [{n}] tensor on {X.device}")
+
+
 def lora_linear_fwd(X, W0, A, B, s, bias=None, save_z=True):
+    _check_linear(X, W0, A, B, bias)
     sh = _shape_of(X, W0, A)
     Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=X.device)
     Z = torch.empty(X.shape[0], A.shape[0], dtype=X.dtype, device=X.device) if save_z else None
@@ -33,6 +60,7 @@ def lora_linear_fwd(X, W0, A, B, s, bias=None, save_z=True):
 
 
 def lora_linear_bwd(X, W0, A, B, Z, dY, s, need_dx=True, need_dbias=False):
+    _check_linear(X, W0, A, B, Z=Z, dY=dY)
     sh = _shape_of(X, W0, A)
     dX = torch.empty_like(X) if need_dx else None
     dA = torch.empty_like(A)
@@ -44,13 +72,15 @@ def lora_linear_bwd(X, W0, A, B, Z, dY, s, need_dx=True, need_dbias=False):
 
 
 def _check_mask(mask, X):
-    if mask.dtype != torch.uint8 or tuple(mask.shape) != tuple(X.shape) or not mask.is_contiguous():
+    if (mask.dtype != torch.uint8 or tuple(mask.shape) != tuple(X.shape) or not mask.is_contiguous()
+            or mask.device != X.device):
         raise ValueError(f"dropout mask must be contiguous uint8 {tuple(X.shape)}, got {mask.dtype} "
                          f"{tuple(mask.shape)}")
 
 
 def lora_linear_dropout_fwd(X, mask, keep_scale, W0, A, B, s, bias=None, save_z=True):
     """mask: uint8 [M, d_in] (1 = kept), keep_scale = 1 / (1 - p)."""
+    _check_linear(X, W0, A, B, bias)
     _check_mask(mask, X)
     sh = _shape_of(X, W0, A)
     Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=X.device)
@@ -61,6 +91,7 @@ def lora_linear_dropout_fwd(X, mask, keep_scale, W0, A, B, s, bias=None, save_z=
 
 
 def lora_linear_dropout_bwd(X, mask, keep_scale, W0, A, B, Z, dY, s, need_dx=True, need_dbias=False):
+    _check_linear(X, W0, A, B, Z=Z, dY=dY)
     _check_mask(mask, X)
     sh = _shape_of(X, W0, A)
     dX = torch.empty_like(X) if need_dx else None
@@ -80,6 +111,9 @@ def dora_rownorm2(W0):
 
 
 def dora_linear_fwd(X, W0, A, B, m, r0, s, eps=1e-12, bias=None, save_z=True):
+    _check_linear(X, W0, A, B, bias)
+    _check_vec("m", m, W0.shape[0], X)
+    _check_vec("r0", r0, W0.shape[0], X)
     sh = _shape_of(X, W0, A)
     dev = X.device
     Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=dev)
@@ -92,6 +126,9 @@ def dora_linear_fwd(X, W0, A, B, m, r0, s, eps=1e-12, bias=None, save_z=True):
 
 
 def dora_linear_bwd(X, W0, A, B, m, bias, Y, Z, n, V, dY, s, eps=1e-12, need_dx=True, need_dbias=False):
+    _check_linear(X, W0, A, B, bias, Z=Z, dY=dY, Y=Y)
+    _check_vec("m", m, W0.shape[0], X)
+    _check_vec("n", n, W0.shape[0], X)
     sh = _shape_of(X, W0, A)
     dX = torch.empty_like(X) if need_dx else None
     dA = torch.empty_like(A)
@@ -112,6 +149,9 @@ def dora_colnorm2(W0):
 
 def dora_cols_fwd(X, W0, A, B, m, c0, s, eps=1e-12, bias=None, save_z=True):
     """m, c0: [d_in].  Returns Y, Z, n [d_in], U [d_in, r] (the last three saved for the backward)."""
+    _check_linear(X, W0, A, B, bias)
+    _check_vec("m", m, W0.shape[1], X)
+    _check_vec("c0", c0, W0.shape[1], X)
     sh = _shape_of(X, W0, A)
     dev = X.device
     Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=dev)
@@ -124,6 +164,9 @@ def dora_cols_fwd(X, W0, A, B, m, c0, s, eps=1e-12, bias=None, save_z=True):
 
 
 def dora_cols_bwd(X, W0, A, B, m, Z, n, U, dY, s, eps=1e-12, need_dx=True, need_dbias=False):
+    _check_linear(X, W0, A, B, Z=Z, dY=dY)
+    _check_vec("m", m, W0.shape[1], X)
+    _check_vec("n", n, W0.shape[1], X)
     sh = _shape_of(X, W0, A)
     dX = torch.empty_like(X) if need_dx else None
     dA = torch.empty_like(A)

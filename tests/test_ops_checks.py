@@ -1,0 +1,52 @@
+"""The Python wrappers check every operand against X [M, in], W0 [out, in] and A [r, in] before
+they allocate or launch anything (the kernels take shapes and strides on trust): CPU tensors are
+enough to see the checks fire."""
+import pytest
+import torch
+
+from dora_adapter_linear_gb300 import ops
+
+
+def _t(*shape, dtype=torch.bfloat16):
+    return torch.zeros(*shape, dtype=dtype)
+
+
+def _ok():
+    return dict(X=_t(8, 32), W0=_t(16, 32), A=_t(4, 32), B=_t(16, 4))
+
+
+@pytest.mark.parametrize("name,bad", [
+    ("W0", _t(16, 24)),          # in mismatch
+    ("A", _t(4, 24)),            # in mismatch
+    ("B", _t(16, 8)),            # r mismatch
+    ("B", _t(12, 4)),            # out mismatch
+    ("B", _t(16, 4, dtype=torch.float32)),   # dtype mismatch
+    ("B", _t(4, 16).t()),        # not contiguous
+])
+def test_linear_forward_rejects_mismatched_operands(name, bad):
+    a = _ok()
+    a[name] = bad
+    with pytest.raises(ValueError):
+        ops.lora_linear_fwd(a["X"], a["W0"], a["A"], a["B"], 1.0)
+
+
+def test_linear_forward_rejects_bias_and_backward_rejects_dy_z():
+    a = _ok()
+    with pytest.raises(ValueError):
+        ops.lora_linear_fwd(a["X"], a["W0"], a["A"], a["B"], 1.0, bias=_t(15))
+    with pytest.raises(ValueError):
+        ops.lora_linear_bwd(a["X"], a["W0"], a["A"], a["B"], _t(8, 4), _t(8, 15), 1.0)      # dY
+    with pytest.raises(ValueError):
+        ops.lora_linear_bwd(a["X"], a["W0"], a["A"], a["B"], _t(8, 5), _t(8, 16), 1.0)      # Z
+
+
+def test_dropout_and_dora_checks():
+    a = _ok()
+    with pytest.raises(ValueError):
+        ops.lora_linear_dropout_fwd(a["X"], torch.ones(8, 32, dtype=torch.int32), 2.0, a["W0"], a["A"], a["B"], 1.0)
+    with pytest.raises(ValueError):
+        ops.lora_linear_dropout_fwd(a["X"], torch.ones(8, 31, dtype=torch.uint8), 2.0, a["W0"], a["A"], a["B"], 1.0)
+    with pytest.raises(ValueError):   # rows variant: m has one entry per output row
+        ops.dora_linear_fwd(a["X"], a["W0"], a["A"], a["B"], _t(32), _t(16, dtype=torch.float32), 1.0)
+    with pytest.raises(ValueError):   # column variant: m has one entry per input column
+        ops.dora_cols_fwd(a["X"], a["W0"], a["A"], a["B"], _t(16), _t(32, dtype=torch.float32), 1.0)
