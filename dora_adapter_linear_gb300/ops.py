@@ -44,6 +44,48 @@ def _check_linear(X, W0, A, B, bias=None, Z=None, dY=None, Y=None):
             raise ValueError(f"{name} must be a contiguous {X.dtype} tensor on {X.device}")
 
 
+def _check_like(name, t, shape, X):
+    """t (if given) must have `shape`, X's dtype and device, and a contiguous layout."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != X.dtype or t.device != X.device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {X.dtype} tensor on {X.device}")
+
+
+def _check_mlp(X, g, u, d, saved=None, dY=None):
+    if X.dim() != 2:
+        raise ValueError("X must be 2-D")
+    M, H = X.shape
+    I, r = g["W"].shape[0], g["A"].shape[0]
+    for nm, p, n_out, n_in in (("gate", g, I, H), ("up", u, I, H), ("down", d, H, I)):
+        _check_like(nm + " W", p["W"], (n_out, n_in), X)
+        _check_like(nm + " A", p["A"], (r, n_in), X)
+        _check_like(nm + " B", p["B"], (n_out, r), X)
+    if saved is not None:
+        for k in ("e", "u", "h"):
+            _check_like(k, saved[k], (M, I), X)
+        _check_like("Zgu", saved["Zgu"], (M, 2 * r), X)
+        _check_like("Zd", saved["Zd"], (M, r), X)
+    _check_like("dY", dY, (M, H), X)
+
+
+def _check_qkv(X, W0, leaves, bias=None, Z=None, dY=None):
+    if X.dim() != 2 or W0.dim() != 2 or not leaves:
+        raise ValueError("X and W0 must be 2-D and there must be at least one leaf")
+    M, d_in = X.shape
+    r = leaves[0][0].shape[0]
+    N = sum(B.shape[0] for _, B, _ in leaves)
+    _check_like("W0", W0, (N, d_in), X)
+    for l, (A, B, _) in enumerate(leaves):
+        _check_like(f"A{l}", A, (r, d_in), X)
+        _check_like(f"B{l}", B, (B.shape[0], r), X)
+    _check_like("bias", bias, (N,), X)
+    _check_like("Z", Z, (M, len(leaves) * r), X)
+    _check_like("dY", dY, (M, N), X)
+
+
 def _check_vec(name, t, n, X):
     if t is not None and (tuple(t.shape) != (n,) or t.device != X.device or not t.is_contiguous()):
         raise ValueError(f"{name} must be a contiguous [{n}] tensor on {X.device}")
@@ -181,6 +223,7 @@ def dora_cols_bwd(X, W0, A, B, m, Z, n, U, dY, s, eps=1e-12, need_dx=True, need_
 def lora_mlp_swiglu_fwd(X, g, u, d, act=0):
     """g, u, d: dicts with W, A, B, s; act 0 SwiGLU, 1 GeGLU.  Returns (Y, saved) where saved
     holds e, u, h, Zgu, Zd."""
+    _check_mlp(X, g, u, d)
     M, H = X.shape
     I, r = g["W"].shape[0], g["A"].shape[0]
     sh = L.mlp_shape(M, H, I, r, act=act)
@@ -198,6 +241,7 @@ def lora_mlp_swiglu_fwd(X, g, u, d, act=0):
 
 
 def lora_mlp_swiglu_bwd(X, g, u, d, saved, dY, need_dx=True, act=0):
+    _check_mlp(X, g, u, d, saved, dY)
     M, H = X.shape
     I, r = g["W"].shape[0], g["A"].shape[0]
     sh = L.mlp_shape(M, H, I, r, act=act)
@@ -246,6 +290,7 @@ def w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, s, bias=None, want_acc=False, want_y=Tru
 
 def lora_qkv_fwd(X, W0, leaves, bias=None, save_z=True):
     """leaves: [(A_l, B_l, s_l)] for the leaves of the fused weight W0 (rows in leaf order)."""
+    _check_qkv(X, W0, leaves, bias)
     M, d_in = X.shape
     n = [B.shape[0] for _, B, _ in leaves]
     r = leaves[0][0].shape[0]
@@ -258,6 +303,7 @@ def lora_qkv_fwd(X, W0, leaves, bias=None, save_z=True):
 
 
 def lora_qkv_bwd(X, W0, leaves, Z, dY, need_dx=True, need_dbias=False):
+    _check_qkv(X, W0, leaves, Z=Z, dY=dY)
     M, d_in = X.shape
     n = [B.shape[0] for _, B, _ in leaves]
     r = leaves[0][0].shape[0]

@@ -50,3 +50,24 @@ def test_dropout_and_dora_checks():
         ops.dora_linear_fwd(a["X"], a["W0"], a["A"], a["B"], _t(32), _t(16, dtype=torch.float32), 1.0)
     with pytest.raises(ValueError):   # column variant: m has one entry per input column
         ops.dora_cols_fwd(a["X"], a["W0"], a["A"], a["B"], _t(16), _t(32, dtype=torch.float32), 1.0)
+
+
+def test_mlp_and_qkv_checks():
+    X = _t(8, 32)
+    P = {"g": {"W": _t(48, 32), "A": _t(4, 32), "B": _t(48, 4), "s": 1.0},
+         "u": {"W": _t(48, 32), "A": _t(4, 32), "B": _t(48, 4), "s": 1.0},
+         "d": {"W": _t(32, 48), "A": _t(4, 48), "B": _t(32, 4), "s": 1.0}}
+    bad = dict(P, d=dict(P["d"], A=_t(4, 32)))          # down-projection A must span I = 48
+    with pytest.raises(ValueError):
+        ops.lora_mlp_swiglu_fwd(X, bad["g"], bad["u"], bad["d"])
+    bad = dict(P, u=dict(P["u"], B=_t(48, 8)))           # one rank for all three projections
+    with pytest.raises(ValueError):
+        ops.lora_mlp_swiglu_fwd(X, bad["g"], bad["u"], bad["d"])
+    W0 = _t(96, 32)
+    leaves = [(_t(4, 32), _t(64, 4), 1.0), (_t(4, 32), _t(16, 4), 1.0), (_t(4, 32), _t(16, 4), 1.0)]
+    with pytest.raises(ValueError):                       # W0 rows must be the leaves' rows
+        ops.lora_qkv_fwd(X, _t(80, 32), leaves)
+    with pytest.raises(ValueError):                       # one rank for all leaves
+        ops.lora_qkv_fwd(X, W0, leaves[:2] + [(_t(8, 32), _t(16, 8), 1.0)])
+    with pytest.raises(ValueError):
+        ops.lora_qkv_bwd(X, W0, leaves, _t(8, 12), _t(8, 95))
