@@ -86,6 +86,17 @@ def _check_qkv(X, W0, leaves, bias=None, Z=None, dY=None):
     _check_like("dY", dY, (M, N), X)
 
 
+def _check_shapes(ref, **named):
+    """Each named tensor (None allowed) must have the given shape, ref's device and a contiguous
+    layout; named values are (tensor, shape) pairs."""
+    for name, (t, shape) in named.items():
+        if t is None:
+            continue
+        if tuple(t.shape) != tuple(shape) or t.device != ref.device or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {tuple(shape)} tensor on {ref.device}, "
+                             f"got {tuple(t.shape)} on {t.device}")
+
+
 def _check_vec(name, t, n, X):
     if t is not None and (tuple(t.shape) != (n,) or t.device != X.device or not t.is_contiguous()):
         raise ValueError(f"{name} must be a contiguous [{n}] tensor on {X.device}")
@@ -257,7 +268,10 @@ def lora_mlp_swiglu_bwd(X, g, u, d, saved, dY, need_dx=True, act=0):
 
 
 def w8a8_quantize_rows(X, A=None):
+    if X.dim() != 2:
+        raise ValueError("X must be 2-D")
     rows, cols = X.shape
+    _check_shapes(X, X=(X, (rows, cols)), A=(A, (None if A is None else A.shape[0], cols)))
     Xq = torch.empty(rows, cols, dtype=torch.int8, device=X.device)
     sx = torch.empty(rows, dtype=torch.float32, device=X.device)
     Z = torch.empty(rows, A.shape[0], dtype=X.dtype, device=X.device) if A is not None else None
@@ -268,6 +282,10 @@ def w8a8_quantize_rows(X, A=None):
 def w8a8_lora_bwd(X, Wq, sw, A, B, Z, dY, s, need_dx=True, need_dbias=False):
     M, d_in = X.shape
     d_out, r = Wq.shape[0], A.shape[0]
+    if Wq.dtype != torch.int8:
+        raise ValueError("Wq must be int8")
+    _check_shapes(X, X=(X, (M, d_in)), Wq=(Wq, (d_out, d_in)), sw=(sw, (d_out,)), A=(A, (r, d_in)),
+                  B=(B, (d_out, r)), Z=(Z, (M, r)), dY=(dY, (M, d_out)))
     dX = torch.empty_like(X) if need_dx else None
     dA = torch.empty_like(A)
     dB = torch.empty_like(B)
@@ -281,6 +299,10 @@ def w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, s, bias=None, want_acc=False, want_y=Tru
     M, d_in = Xq.shape
     d_out = Wq.shape[0]
     r = 0 if Z is None else Z.shape[1]
+    if Xq.dtype != torch.int8 or Wq.dtype != torch.int8:
+        raise ValueError("Xq and Wq must be int8")
+    _check_shapes(Xq, Xq=(Xq, (M, d_in)), sx=(sx, (M,)), Wq=(Wq, (d_out, d_in)), sw=(sw, (d_out,)),
+                  Z=(Z, (M, r)), B=(B, (d_out, r)), bias=(bias, (d_out,)))
     Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=Xq.device) if want_y else None
     acc = torch.empty(M, d_out, dtype=torch.int32, device=Xq.device) if want_acc else None
     ws = workspace(L.w8a8_workspace_bytes(M, d_in, d_out), Xq.device)

@@ -71,3 +71,16 @@ def test_mlp_and_qkv_checks():
         ops.lora_qkv_fwd(X, W0, leaves[:2] + [(_t(8, 32), _t(16, 8), 1.0)])
     with pytest.raises(ValueError):
         ops.lora_qkv_bwd(X, W0, leaves, _t(8, 12), _t(8, 95))
+
+
+def test_w8a8_checks():
+    Xq, Wq = torch.zeros(8, 32, dtype=torch.int8), torch.zeros(16, 32, dtype=torch.int8)
+    sx, sw = torch.ones(8), torch.ones(16)
+    with pytest.raises(ValueError):          # weight scales: one per output row
+        ops.w8a8_lora_fwd(Xq, sx, Wq, torch.ones(15), None, None, 1.0)
+    with pytest.raises(ValueError):          # rank-r input and up-projection disagree
+        ops.w8a8_lora_fwd(Xq, sx, Wq, sw, _t(8, 4), _t(16, 8), 1.0)
+    with pytest.raises(ValueError):
+        ops.w8a8_lora_fwd(Xq.float(), sx, Wq, sw, None, None, 1.0)
+    with pytest.raises(ValueError):
+        ops.w8a8_lora_bwd(_t(8, 32), Wq, sw, _t(4, 32), _t(16, 4), None, _t(8, 12), 1.0)
