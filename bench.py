@@ -311,8 +311,7 @@ def gemm_roofline(L, peaks, ms_step, steps_recorded, sustained, workload):
         return None
     ach = fl / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
-    return {"kernel": "tcgen05 GEMM with fused rank-r tail (tc_pair_kernel forward, tc_gemm_kernel dX with "
-                      "B multicast)",
+    return {"kernel": "tcgen05 GEMM with fused rank-r tail (tc_pair_kernel, forward and dX)",
             "bound": "tensor",
             "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
             "peak_kind": ("sustained" if sustained else "burst") + " bf16, " + peaks["source"] + " (of measured)",

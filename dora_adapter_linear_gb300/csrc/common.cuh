@@ -299,25 +299,6 @@ __device__ __forceinline__ void umma_commit_pair_mc(uint64_t* bar, uint16_t mask
       "h"(mask)
       : "memory");
 }
-// ------------------------------------------------------------------ two-CTA multicast (one-CTA MMAs)
-// Commit whose arrival goes to the barrier at the same SMEM offset in every CTA of `mask`.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-// Tile load written to the same SMEM offset of every CTA in `mask`, each CTA's barrier at the same
-// offset receiving the bytes that land in that CTA.
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const void* map, uint64_t* bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

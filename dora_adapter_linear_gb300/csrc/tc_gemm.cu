@@ -9,8 +9,7 @@
 // ("LoRA/DoRA fast forward: no weight materialization", What section).
 //
 // Two kernels share the stage layout, the epilogues and the A-tile scaling:
-//  * tc_gemm_kernel: one CTA per SM, 128 x 256 tile (cta_group::1); for the MN-major products
-//    it runs in clusters of two CTAs on M-adjacent tiles that share each B tile by TMA multicast.
+//  * tc_gemm_kernel: one CTA per SM, 128 x 256 tile (cta_group::1).
 //  * tc_pair_kernel: a cluster of two CTAs on two SMs computes a 256 x 256 tile with
 //    cta_group::2 MMAs issued by the even CTA; each SM stages its 128 rows of A and half of
 //    B, so the operand bytes per SM and k-step drop from 48 KB to 32 KB.
@@ -456,14 +455,8 @@ struct OneCta {
   static constexpr int THREADS = (KSCALE || EPI8) ? 320 : 192;
 };
 
-// MC: a cluster of two CTAs on two M-adjacent tiles of the same N range; each CTA loads half of
-// every B tile and multicasts it to both, so L2 serves 32 KB of operand reads per SM and k-step
-// instead of 48 KB (each SM still receives 48 KB).  A stage is free again once both CTAs' MMAs
-// have read it: empty[s] takes one commit from each CTA (multicast), and neither CTA exits while
-// its peer may still write into it.
-template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE, bool MC>
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
 __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  static_assert(!(MC && (STACKED || KSCALE || EPI == EPI_W8A8)), "multicast mode: plain K-major or MN-major B only");
   using L = Layout<EPI, false>;
   constexpr int STAGES = L::STAGES;
   constexpr int BNB = STACKED ? BN / 2 : BN;          // rows per K-major B box
@@ -489,21 +482,15 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
   const int lane = threadIdx.x & 31;
   const int nk0 = (p.K0 + BK - 1) / BK;
   const int nk = nk0 + (HAS_TAIL ? (p.K1 + BK - 1) / BK : 0);   // the rank-r tail may span several K-steps
-  // tile sequence: one tile per CTA step, or (MC) one pair of M-adjacent tiles per cluster step
-  const uint32_t mc_rank = MC ? cluster_ctarank() : 0u;
-  const int m_units = MC ? (p.num_m_tiles + 1) / 2 : p.num_m_tiles;
-  const int t_first = MC ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int t_step = MC ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  const int t_count = m_units * p.num_n_tiles;
-  auto coords = [&](int t, int& mt, int& nt) {
-    tile_coords(t, m_units, p.num_n_tiles, p.group_m, mt, nt);
-    if (MC) mt = 2 * mt + (int)mc_rank;
-  };
+  const int t_first = (int)blockIdx.x;
+  const int t_step = (int)gridDim.x;
+  const int t_count = p.num_m_tiles * p.num_n_tiles;
+  auto coords = [&](int t, int& mt, int& nt) { tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, mt, nt); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], MC ? 2 : 1);
+      mbar_init(&empty[i], 1);
       mbar_init(&ready[i], 128);
     }
     for (int i = 0; i < 2; ++i) {
@@ -527,8 +514,7 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
     tmem_relinquish();
   }
   tc_fence_before();
-  if constexpr (MC) cluster_sync_all();   // both CTAs' barriers initialised before any multicast
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   pdl_wait();      // the operands may come from the previous kernel in the stream
@@ -566,43 +552,23 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
               const bool second = ks >= p.k0_split_steps;
               const void* mp = second ? (const void*)&p.tmB0b : (const void*)&p.tmB0;
               const int ky = second ? kx - p.k0_split_steps * BK : kx;
-              if constexpr (MC) {   // this CTA's two 64-column chunks, to both CTAs
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                  const int jj = 2 * (int)mc_rank + j;
-                  tma_load_2d_mc(b_dst + jj * 8192, mp, &full[stage], n0 + 64 * jj, ky, 0x3);
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, mp, &full[stage], n0 + 64 * j, ky);
-              }
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, mp, &full[stage], n0 + 64 * j, ky);
             } else if (STACKED) {
               tma_load_2d(b_dst, &p.tmB0, &full[stage], kx, n0);
               tma_load_2d(b_dst + BNB * 128, &p.tmB0b, &full[stage], kx, n0);
-            } else if (MC) {   // this CTA's 128 rows of the B tile, to both CTAs
-              tma_load_2d_mc(b_dst + mc_rank * (BN / 2) * 128, &p.tmB0, &full[stage], kx, n0 + (int)mc_rank * (BN / 2),
-                             0x3);
             } else {
               tma_load_2d(b_dst, &p.tmB0, &full[stage], kx, n0);
             }
           } else {
             const int kt = (ks - nk0) * BK;   // K offset inside the rank-r tail
             tma_load_2d(a_dst, &p.tmA1, &full[stage], kt, m0);
-            if (B1_MN && MC) {
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                const int jj = 2 * (int)mc_rank + j;
-                tma_load_2d_mc(b_dst + jj * 8192, &p.tmB1, &full[stage], n0 + 64 * jj, kt, 0x3);
-              }
-            } else if (B1_MN) {
+            if (B1_MN) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &p.tmB1, &full[stage], n0 + 64 * j, kt);
             } else if (STACKED) {
               tma_load_2d(b_dst, &p.tmB1, &full[stage], p.tail_b1_x + kt, n0);
               if (EPI != EPI_W8A8) tma_load_2d(b_dst + BNB * 128, &p.tmB1b, &full[stage], p.tail_b1b_x + kt, n0);
-            } else if (MC) {
-              tma_load_2d_mc(b_dst + mc_rank * (BN / 2) * 128, &p.tmB1, &full[stage], kt, n0 + (int)mc_rank * (BN / 2),
-                             0x3);
             } else {
               tma_load_2d(b_dst, &p.tmB1, &full[stage], kt, n0);
             }
@@ -667,8 +633,7 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
             else
               umma_bf16(d_tmem, adesc, bdesc, tail ? idesc1 : idesc0, (ks > 0 || kk > 0) ? 1u : 0u);
           }
-          if constexpr (MC) umma_commit_mc(&empty[stage], 0x3);   // the stage is read in both CTAs
-          else umma_commit(&empty[stage]);
+          umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -741,8 +706,7 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
   }
 
   tc_fence_before();
-  if constexpr (MC) cluster_sync_all();   // neither CTA leaves while its peer may still write into it
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
@@ -1086,55 +1050,34 @@ int pdl_attr(cudaLaunchAttribute* a) {
   return 1;
 }
 
-// tiles: CTA tiles, or (MC) pairs of M-adjacent tiles, one per cluster step
-template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE, bool MC>
-static cudaError_t launch_one_k(const TcParams& p, cudaStream_t st, int tiles) {
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
+static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
   using L = Layout<EPI, false>;
-  auto kern = tc_gemm_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE, MC>;
+  auto kern = tc_gemm_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(OneCta<EPI, KSCALE>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = L::TOTAL;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 0;
-  if (MC) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.numAttrs = 1;
-  }
-  static int max_units_dev[64] = {0};   // co-resident CTAs (clusters for MC), per device
+  static int max_units_dev[64] = {0};   // co-resident CTAs, per device
   int& max_units = max_units_dev[current_device_slot()];
   if (max_units == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
     if (e != cudaSuccess) return e;
-    int n = MC ? num_sms_current() / 2 : num_sms_current();
-    if (MC) {
-      cfg.gridDim = dim3(2 * n, 1, 1);
-      int c = 0;
-      e = cudaOccupancyMaxActiveClusters(&c, kern, &cfg);
-      if (e != cudaSuccess) return e;
-      n = c > 0 ? c : 1;
-    }
-    max_units = n;
+    max_units = num_sms_current();
   }
   int units = max_units;
   // test knob: cap the persistent grid so that small problems still run several tiles per CTA
-  const int cap = env_int("LORA_GB300_MAX_CTAS", 0) / (MC ? 2 : 1);
+  const int cap = env_int("LORA_GB300_MAX_CTAS", 0);
   if (cap > 0 && cap < units) units = cap;
   if (units > tiles) units = tiles;
-  cfg.gridDim = dim3((MC ? 2 : 1) * units, 1, 1);
+  cfg.gridDim = dim3(units, 1, 1);
   cfg.numAttrs += (unsigned)pdl_attr(&attr[cfg.numAttrs]);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
-static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
-  return launch_one_k<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE, false>(p, st, tiles);
 }
 
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
@@ -1182,12 +1125,10 @@ static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// kind: 0 one CTA, 1 CTA pair, 2 two one-CTA tiles sharing B by multicast
+// kind: 0 one CTA, 1 CTA pair
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE>
 static cudaError_t launch_variant(const TcParams& p, cudaStream_t st, int kind, int tiles) {
   if (kind == 1) return launch_pair<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles);
-  if constexpr (!STACKED && !KSCALE && EPI != EPI_W8A8)
-    if (kind == 2) return launch_one_k<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE, true>(p, st, tiles);
   return launch_one<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles);
 }
 
@@ -1218,22 +1159,14 @@ static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStrea
 }
 
 // Kernel choice per mode.  LORA_GB300_GEMM_PAIR=0 / 1 forces the one-CTA / pair kernel for every
-// mode (W8A8 always runs one-CTA); LORA_GB300_GEMM_MC=0 / 1 turns the two-CTA B multicast of the
-// one-CTA kernel off / on where it applies.
+// mode (W8A8 with the int32 output always runs one-CTA).
 static bool use_pair(int mode) {
   const char* e = getenv("LORA_GB300_GEMM_PAIR");
   if (e && *e) return atoi(e) != 0;
   // measured over LLM layer shapes: the pair is 4-7% faster on the K-major products; on the
-  // MN-major dX products and the fused W8A8 output path the one-CTA kernel is as fast or faster
+  // MN-major dX products (one-CTA 168 us against 174 us for the pair at 8192 x 4096 x 4096) and
+  // the fused W8A8 output path the one-CTA kernel is as fast or faster
   return mode == TC_FWD || mode == TC_SWIGLU_FWD;
-}
-
-static bool use_mc(int mode) {
-  const char* e = getenv("LORA_GB300_GEMM_MC");
-  if (e && *e) return atoi(e) != 0;
-  // measured over LLM layer shapes: 3-6% faster on the MN-major dX products, no gain on the
-  // K-major forward (which runs on the CTA pair)
-  return mode == TC_BWD_DX || mode == TC_SWIGLU_BWD;
 }
 
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
@@ -1242,13 +1175,8 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   TcParams p;
   memset(&p, 0, sizeof(p));
   const bool stacked = d.mode == TC_SWIGLU_FWD || d.mode == TC_W8A8 || d.mode == TC_W8A8F;
-  // two one-CTA tiles sharing B: plain forward / dX products with an even number of M tiles
-  const bool mc = !pair && !stacked && d.a_kscale == nullptr &&
-                  (d.mode == TC_FWD || d.mode == TC_BWD_DX || d.mode == TC_SWIGLU_BWD) &&
-                  ((d.M + BM - 1) / BM) % 2 == 0 && use_mc(d.mode);
-  // rows of a K-major B box: 256 (one CTA), 128 (stacked halves, one CTA's half of a pair, or of
-  // a multicast B tile)
-  const int bnb = (stacked || pair || mc) ? BN / 2 : BN;
+  // rows of a K-major B box: 256 (one CTA), 128 (stacked halves, or one CTA's half of a pair)
+  const int bnb = (stacked || pair) ? BN / 2 : BN;
   bool ok = make_map(&p.tmA0, d.A0, d.K0, d.M, d.lda0, BM);
   if (d.b0_mn) {
     ok = ok && make_map(&p.tmB0, d.B0, d.N, d.b0_rows, d.ldb0, 64);
@@ -1290,10 +1218,11 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.num_m_tiles = (d.M + tile_m - 1) / tile_m;
   const int n_out = stacked ? BN / 2 : BN;
   p.num_n_tiles = (d.N + n_out - 1) / n_out;
-  // raster group in M units of the tile sequence (pair tiles, or MC pairs of tiles): measured,
-  // the multicast dX runs best with 4 pairs when both K and N are at most 4096 (the whole
-  // weight then stays in L2 across groups) and with 8 otherwise (4 costs 8-10% at N = 11008)
-  p.group_m = pair ? 8 : (mc ? ((d.K0 <= 4096 && d.N <= 4096) ? 4 : 8) : 16);
+  // raster group in M tiles of the tile sequence (pair tiles of 256 rows, or one-CTA tiles of 128):
+  // measured, the MN-major dX products run best with groups of 4-8 one-CTA tiles (8192 x 4096 x
+  // 4096: 168-169 us against 176 us with 16)
+  const int gm_env = env_int("LORA_GB300_GROUP_M", 0);
+  p.group_m = gm_env > 0 ? gm_env : (pair ? 8 : (d.b0_mn ? 8 : 16));
   p.k0_split_steps = d.b0_mn && d.B0b ? (d.k0_split / BK) : (1 << 30);
   p.tail_b1b_x = d.b1b_x;
   p.tail_b1_x = d.b1_x;
@@ -1305,14 +1234,14 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.ld_eu = d.ld_eu;
   p.err = d.err;
   p.timeout_ns = d.timeout_ns;
-  const int tiles = (mc ? p.num_m_tiles / 2 : p.num_m_tiles) * p.num_n_tiles;
+  const int tiles = p.num_m_tiles * p.num_n_tiles;
 
   // algorithmic flops of this launch: the base contraction plus the rank-r tail
   const double ntot = stacked ? 2.0 * d.N : (double)d.N;
   const double k1 = d.has_tail ? (stacked ? d.K1 / 2.0 : (double)d.K1) : 0.0;
   const double flops = 2.0 * d.M * ntot * ((double)d.K0 + k1);
   prof_mark(st, true, flops);
-  const cudaError_t e = launch_mode(d, p, st, pair ? 1 : (mc ? 2 : 0), tiles);
+  const cudaError_t e = launch_mode(d, p, st, pair ? 1 : 0, tiles);
   prof_mark(st, false, 0.0);
   return e;
 }

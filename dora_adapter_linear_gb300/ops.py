@@ -87,19 +87,28 @@ def _check_qkv(X, W0, leaves, bias=None, Z=None, dY=None):
 
 
 def _check_shapes(ref, **named):
-    """Each named tensor (None allowed) must have the given shape, ref's device and a contiguous
-    layout; named values are (tensor, shape) pairs."""
-    for name, (t, shape) in named.items():
+    """Each named tensor (None allowed) must have the given shape and dtype, ref's device and a
+    contiguous layout; named values are (tensor, shape, dtype) triples.  The kernels read every
+    operand with the element size its dtype implies, so a wrong dtype is an out-of-bounds read."""
+    for name, (t, shape, dtype) in named.items():
         if t is None:
             continue
-        if tuple(t.shape) != tuple(shape) or t.device != ref.device or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous {tuple(shape)} tensor on {ref.device}, "
-                             f"got {tuple(t.shape)} on {t.device}")
+        if (tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != ref.device
+                or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous {tuple(shape)} {dtype} tensor on {ref.device}, "
+                             f"got {tuple(t.shape)} {t.dtype} on {t.device}")
 
 
-def _check_vec(name, t, n, X):
-    if t is not None and (tuple(t.shape) != (n,) or t.device != X.device or not t.is_contiguous()):
-        raise ValueError(f"{name} must be a contiguous [{n}] tensor on {X.device}")
+def _check_vec(name, t, n, X, dtype):
+    """t (if given) must be a contiguous [n] tensor of `dtype` on X's device."""
+    if t is not None and (tuple(t.shape) != (n,) or t.dtype != dtype or t.device != X.device
+                          or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous [{n}] {dtype} tensor on {X.device}, "
+                         f"got {tuple(t.shape)} {t.dtype} on {t.device}")
+
+
+F32 = torch.float32
+BF16 = torch.bfloat16
 
 
 def lora_linear_fwd(X, W0, A, B, s, bias=None, save_z=True):
@@ -165,8 +174,8 @@ def dora_rownorm2(W0):
 
 def dora_linear_fwd(X, W0, A, B, m, r0, s, eps=1e-12, bias=None, save_z=True):
     _check_linear(X, W0, A, B, bias)
-    _check_vec("m", m, W0.shape[0], X)
-    _check_vec("r0", r0, W0.shape[0], X)
+    _check_vec("m", m, W0.shape[0], X, X.dtype)
+    _check_vec("r0", r0, W0.shape[0], X, F32)
     sh = _shape_of(X, W0, A)
     dev = X.device
     Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=dev)
@@ -180,8 +189,9 @@ def dora_linear_fwd(X, W0, A, B, m, r0, s, eps=1e-12, bias=None, save_z=True):
 
 def dora_linear_bwd(X, W0, A, B, m, bias, Y, Z, n, V, dY, s, eps=1e-12, need_dx=True, need_dbias=False):
     _check_linear(X, W0, A, B, bias, Z=Z, dY=dY, Y=Y)
-    _check_vec("m", m, W0.shape[0], X)
-    _check_vec("n", n, W0.shape[0], X)
+    _check_vec("m", m, W0.shape[0], X, X.dtype)
+    _check_vec("n", n, W0.shape[0], X, F32)
+    _check_shapes(X, V=(V, (W0.shape[0], A.shape[0]), F32))
     sh = _shape_of(X, W0, A)
     dX = torch.empty_like(X) if need_dx else None
     dA = torch.empty_like(A)
@@ -203,8 +213,8 @@ def dora_colnorm2(W0):
 def dora_cols_fwd(X, W0, A, B, m, c0, s, eps=1e-12, bias=None, save_z=True):
     """m, c0: [d_in].  Returns Y, Z, n [d_in], U [d_in, r] (the last three saved for the backward)."""
     _check_linear(X, W0, A, B, bias)
-    _check_vec("m", m, W0.shape[1], X)
-    _check_vec("c0", c0, W0.shape[1], X)
+    _check_vec("m", m, W0.shape[1], X, X.dtype)
+    _check_vec("c0", c0, W0.shape[1], X, F32)
     sh = _shape_of(X, W0, A)
     dev = X.device
     Y = torch.empty(X.shape[0], W0.shape[0], dtype=X.dtype, device=dev)
@@ -218,8 +228,9 @@ def dora_cols_fwd(X, W0, A, B, m, c0, s, eps=1e-12, bias=None, save_z=True):
 
 def dora_cols_bwd(X, W0, A, B, m, Z, n, U, dY, s, eps=1e-12, need_dx=True, need_dbias=False):
     _check_linear(X, W0, A, B, Z=Z, dY=dY)
-    _check_vec("m", m, W0.shape[1], X)
-    _check_vec("n", n, W0.shape[1], X)
+    _check_vec("m", m, W0.shape[1], X, X.dtype)
+    _check_vec("n", n, W0.shape[1], X, F32)
+    _check_shapes(X, U=(U, (W0.shape[1], A.shape[0]), F32))
     sh = _shape_of(X, W0, A)
     dX = torch.empty_like(X) if need_dx else None
     dA = torch.empty_like(A)
@@ -271,7 +282,7 @@ def w8a8_quantize_rows(X, A=None):
     if X.dim() != 2:
         raise ValueError("X must be 2-D")
     rows, cols = X.shape
-    _check_shapes(X, X=(X, (rows, cols)), A=(A, (None if A is None else A.shape[0], cols)))
+    _check_shapes(X, X=(X, (rows, cols), BF16), A=(A, (None if A is None else A.shape[0], cols), BF16))
     Xq = torch.empty(rows, cols, dtype=torch.int8, device=X.device)
     sx = torch.empty(rows, dtype=torch.float32, device=X.device)
     Z = torch.empty(rows, A.shape[0], dtype=X.dtype, device=X.device) if A is not None else None
@@ -284,8 +295,8 @@ def w8a8_lora_bwd(X, Wq, sw, A, B, Z, dY, s, need_dx=True, need_dbias=False):
     d_out, r = Wq.shape[0], A.shape[0]
     if Wq.dtype != torch.int8:
         raise ValueError("Wq must be int8")
-    _check_shapes(X, X=(X, (M, d_in)), Wq=(Wq, (d_out, d_in)), sw=(sw, (d_out,)), A=(A, (r, d_in)),
-                  B=(B, (d_out, r)), Z=(Z, (M, r)), dY=(dY, (M, d_out)))
+    _check_shapes(X, X=(X, (M, d_in), BF16), Wq=(Wq, (d_out, d_in), torch.int8), sw=(sw, (d_out,), F32),
+                  A=(A, (r, d_in), BF16), B=(B, (d_out, r), BF16), Z=(Z, (M, r), BF16), dY=(dY, (M, d_out), BF16))
     dX = torch.empty_like(X) if need_dx else None
     dA = torch.empty_like(A)
     dB = torch.empty_like(B)
@@ -301,8 +312,8 @@ def w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, s, bias=None, want_acc=False, want_y=Tru
     r = 0 if Z is None else Z.shape[1]
     if Xq.dtype != torch.int8 or Wq.dtype != torch.int8:
         raise ValueError("Xq and Wq must be int8")
-    _check_shapes(Xq, Xq=(Xq, (M, d_in)), sx=(sx, (M,)), Wq=(Wq, (d_out, d_in)), sw=(sw, (d_out,)),
-                  Z=(Z, (M, r)), B=(B, (d_out, r)), bias=(bias, (d_out,)))
+    _check_shapes(Xq, Xq=(Xq, (M, d_in), torch.int8), sx=(sx, (M,), F32), Wq=(Wq, (d_out, d_in), torch.int8),
+                  sw=(sw, (d_out,), F32), Z=(Z, (M, r), BF16), B=(B, (d_out, r), BF16), bias=(bias, (d_out,), BF16))
     Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=Xq.device) if want_y else None
     acc = torch.empty(M, d_out, dtype=torch.int32, device=Xq.device) if want_acc else None
     ws = workspace(L.w8a8_workspace_bytes(M, d_in, d_out), Xq.device)

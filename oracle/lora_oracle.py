@@ -27,11 +27,11 @@ from scipy.special import erf as _erf
 __all__ = [
     "f64", "adapted_weight", "lora_linear_fwd", "lora_linear_bwd", "dora_rownorm2",
     "dora_linear_fwd", "dora_linear_bwd", "dora_colnorm2", "dora_cols_fwd", "dora_cols_bwd",
-    "dora_cols_fwd_rows", "dora_cols_bwd_sampled", "silu", "dsilu", "gelu", "dgelu", "mlp_swiglu_fwd", "mlp_swiglu_bwd",
+    "dora_cols_fwd_rows", "dora_cols_bwd_sampled", "dora_cols_bwd_rows_sampled", "silu", "dsilu", "gelu", "dgelu", "mlp_swiglu_fwd", "mlp_swiglu_bwd",
     "quantize_rows", "int8_accumulate", "w8a8_lora_fwd", "w8a8_dequant_weight", "w8a8_lora_bwd",
     "lora_dropout_fwd", "lora_dropout_bwd", "qkv_adapted_weight", "qkv_lora_fwd", "qkv_lora_bwd", "qkv_fwd_rows", "qkv_bwd_sampled",
     "lora_fwd_rows", "lora_bwd_sampled", "dora_fwd_rows", "dora_bwd_sampled", "dora_bwd_rows_sampled",
-    "mlp_fwd_rows", "mlp_bwd_rows",
+    "mlp_fwd_rows", "mlp_bwd_rows", "mlp_bwd_sparse_dy",
 ]
 
 
@@ -492,6 +492,28 @@ def dora_cols_bwd_sampled(X, W0, A, B, m, s, dY, rows, in_cols, eps=1e-12):
     return dX, s * (B.T @ dWp_k), t / nk
 
 
+def dora_cols_bwd_rows_sampled(X, W0, A, B, m, s, dY, out_rows, eps=1e-12):
+    """Sampled DoRA-cols up-projection gradient: dB[out_rows].
+
+    Row o of dW' = dWd diag(c) + W' diag(coef) needs coef_k for every input column k, i.e.
+    t_k = <dWd[:, k], W'[:, k]> for all k.  It is evaluated as colsum(X * (dY W')) (the same
+    number summed in another order), a block of token rows at a time, so that no [out, in]
+    gradient is formed; then dB[o] = s dW'[o] A^T as in dora_cols_bwd.
+    """
+    Wp = adapted_weight(W0, A, B, s)
+    nraw = np.sqrt((Wp * Wp).sum(axis=0))
+    n = np.maximum(nraw, eps)
+    c = m / n
+    t = np.zeros(W0.shape[1])
+    for i0 in range(0, X.shape[0], 1024):
+        t += (X[i0:i0 + 1024] * (dY[i0:i0 + 1024] @ Wp)).sum(axis=0)
+    live = nraw > eps
+    coef = np.where(live, (-t * m / (n * n)) / np.where(live, nraw, 1.0), 0.0)
+    dWd_rows = dY[:, out_rows].T @ X
+    dWp_rows = dWd_rows * c[None, :] + Wp[out_rows] * coef[None, :]
+    return s * (dWp_rows @ A.T)
+
+
 def dora_fwd_rows(X, W0, A, B, m, s, rows, eps=1e-12, bias=None):
     """Rows `rows` of the DoRA output, plus the full norm vector n."""
     return dora_linear_fwd(X[rows], W0, A, B, m, s, eps, bias)
@@ -552,3 +574,14 @@ def mlp_fwd_rows(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, rows, act="s
 def mlp_bwd_rows(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY, rows, act="swiglu"):
     """Rows `rows` of dX of the gated MLP (each row of dX depends on its own row only)."""
     return mlp_swiglu_bwd(X[rows], Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY[rows], act=act)["dX"]
+
+
+def mlp_bwd_sparse_dy(X, Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY, rows, act="swiglu"):
+    """All gradients of the gated MLP for an upstream gradient that is zero outside `rows`.
+
+    Every gradient is linear in dY and each token row's contribution depends on that row alone,
+    so the rows where dY vanishes add nothing: the adapter gradients are those of the sub-batch
+    X[rows], dY[rows], and dX is zero outside `rows`.  Returns the dict of mlp_swiglu_bwd with
+    dX restricted to `rows`.
+    """
+    return mlp_swiglu_bwd(X[rows], Wg, Ag, Bg, sg, Wu, Au, Bu, su, Wd, Ad, Bd, sd, dY[rows], act=act)

@@ -1,7 +1,6 @@
-"""Both tcgen05 GEMM kernels against the oracle: the one-CTA kernel (128 x 256 tiles), also in
-its two-CTA form that multicasts each B tile to two M-adjacent tiles (LORA_GB300_GEMM_MC, used
-where the number of M tiles is even), and the CTA-pair kernel (cta_group::2, 256 x 256 tiles over
-two SMs), selected per call with LORA_GB300_GEMM_PAIR, in every mode the layer uses (forward, dX with MN-major B, dX with the
+"""Both tcgen05 GEMM kernels against the oracle: the one-CTA kernel (128 x 256 tiles) and the
+CTA-pair kernel (cta_group::2, 256 x 256 tiles over two SMs), selected per call with
+LORA_GB300_GEMM_PAIR, in every mode the layer uses (forward, dX with MN-major B, dX with the
 DoRA K-scaling warps, SwiGLU forward with stacked B, SwiGLU backward), with ragged M, N, K and
 with a capped grid so that every CTA (pair) runs several tiles."""
 import pytest
@@ -23,10 +22,9 @@ def ops():
     return _ops
 
 
-@pytest.fixture(params=["one_cta", "multicast", "pair"])
+@pytest.fixture(params=["one_cta", "pair"])
 def variant(request, monkeypatch):
     monkeypatch.setenv("LORA_GB300_GEMM_PAIR", "1" if request.param == "pair" else "0")
-    monkeypatch.setenv("LORA_GB300_GEMM_MC", "1" if request.param == "multicast" else "0")
     return request.param
 
 
@@ -59,8 +57,8 @@ def test_lora_fwd_bwd(ops, variant, cap, monkeypatch):
 @pytest.mark.parametrize("cap", ["0", "4"])
 @pytest.mark.parametrize("M", [500, 1024])
 def test_lora_even_m_tiles(ops, variant, cap, M, monkeypatch):
-    """An even number of M tiles (4 with a ragged last one, and 8), the case where the multicast
-    form of the one-CTA kernel runs; ragged N and K."""
+    """An even number of M tiles (4 with a ragged last one, and 8), so that the pair kernel's
+    256-row tiles are whole or half empty; ragged N and K."""
     monkeypatch.setenv("LORA_GB300_MAX_CTAS", cap)
     case = D.scaled(D.WORKLOADS["lora_4096_bf16"], M=M, d_in=328, d_out=776, r=16, bias=True)
     t = D.make_linear(case)

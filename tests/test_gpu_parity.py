@@ -216,6 +216,56 @@ def test_dora_strength0_is_frozen_base_bits(ops):
     assert torch.equal(Yd, Yl)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_dora_eps_floor_rows(ops, dtype):
+    """eps above some rows' adapted norm: those rows take the floor n = eps and pass no gradient
+    through the norm (the clamped branch of the norm and of g), the others stay live."""
+    case = D.scaled(D.WORKLOADS["dora_4096x11008_bf16"], M=300, d_in=328, d_out=520, r=32, dtype=dtype)
+    t = D.make_linear(case)
+    low = [0, 3, 130, 517]
+    for k in ("W0", "B"):
+        t[k][low] = (t[k][low].float() * 0.05).to(t[k].dtype)
+    eps = 0.3
+    g = {k: gpu(v) for k, v in t.items()}
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    nraw = np.linalg.norm(O.adapted_weight(W0, A, B, case.s), axis=1)
+    assert (nraw[low] < eps).all() and (np.delete(nraw, low) > eps).all()
+    r0 = ops.dora_rownorm2(g["W0"])
+    Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, eps, g["bias"])
+    rY, rn = O.dora_linear_fwd(X, W0, A, B, m, case.s, eps, bias)
+    assert (to64(n)[low] == np.float32(eps)).all()
+    np.testing.assert_allclose(to64(n), rn, rtol=1e-4)
+    assert_close(Y, rY, dtype, "Y")
+    dX, dA, dB, dm, _ = ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V,
+                                            g["dY"], case.s, eps)
+    rX, rA, rB, rm, _ = O.dora_linear_bwd(X, W0, A, B, m, case.s, dY, eps)
+    for got, ref, nm in ((dX, rX, "dX"), (dA, rA, "dA"), (dB, rB, "dB"), (dm, rm[None], "dm")):
+        assert_close(got, ref, dtype, nm)
+
+
+def test_dora_zero_row_at_default_eps(ops):
+    """A row of W0 and B that is exactly zero: its norm is the 1e-12 floor, its output the bias,
+    and its up-projection gradient carries the scale m / eps."""
+    case = D.scaled(D.WORKLOADS["dora_4096x11008_bf16"], M=260, d_in=200, d_out=264, r=16)
+    t = D.make_linear(case)
+    t["W0"][7] = 0
+    t["B"][7] = 0
+    t["m"][7] = 1.5
+    g = {k: gpu(v) for k, v in t.items()}
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    r0 = ops.dora_rownorm2(g["W0"])
+    Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps, g["bias"])
+    assert float(n[7]) == np.float32(case.eps)
+    rY, _ = O.dora_linear_fwd(X, W0, A, B, m, case.s, case.eps, bias)
+    assert_close(Y, rY, "bf16", "Y")
+    dX, dA, dB, dm, _ = ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V,
+                                            g["dY"], case.s, case.eps)
+    rX, rA, rB, rm, _ = O.dora_linear_bwd(X, W0, A, B, m, case.s, dY, case.eps)
+    assert abs(rB[7]).max() > 1e9
+    for got, ref, nm in ((dX, rX, "dX"), (dA, rA, "dA"), (dB, rB, "dB"), (dm, rm[None], "dm")):
+        assert_close(got, ref, "bf16", nm)
+
+
 # ---------------------------------------------------------------------------- DoRA (cols)
 @pytest.mark.parametrize("r", [32, 16])
 def test_dora_cols_fwd_bwd(ops, r):
@@ -238,6 +288,29 @@ def test_dora_cols_fwd_bwd(ops, r):
     _, dA2, dB2, dm2, _ = ops.dora_cols_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], None, n, U, g["dY"], case.s,
                                             case.eps, need_dx=False)
     assert torch.equal(dA, dA2) and torch.equal(dB, dB2) and torch.equal(dm, dm2)
+
+
+def test_dora_cols_eps_floor_columns(ops):
+    """Column variant with eps above some columns' adapted norm (floor branch) and the rest live."""
+    case = D.scaled(D.WORKLOADS["dora_cols_4096x11008_bf16"], M=300, d_in=328, d_out=520, r=16)
+    t = D.make_linear(case)
+    low = [0, 5, 200, 327]
+    t["W0"][:, low] = (t["W0"][:, low].float() * 0.05).to(torch.bfloat16)
+    t["A"][:, low] = (t["A"][:, low].float() * 0.05).to(torch.bfloat16)
+    eps = 0.3
+    g = {k: gpu(v) for k, v in t.items()}
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    nraw = np.linalg.norm(O.adapted_weight(W0, A, B, case.s), axis=0)
+    assert (nraw[low] < eps).all() and (np.delete(nraw, low) > eps).all()
+    c0 = ops.dora_colnorm2(g["W0"])
+    Y, Z, n, U = ops.dora_cols_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], c0, case.s, eps, g["bias"])
+    rY, rn = O.dora_cols_fwd(X, W0, A, B, m, case.s, eps, bias)
+    assert (to64(n)[low] == np.float32(eps)).all()
+    assert_close(Y, rY, "bf16", "Y")
+    dX, dA, dB, dm, _ = ops.dora_cols_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], Z, n, U, g["dY"], case.s, eps)
+    rX, rA, rB, rm, _ = O.dora_cols_bwd(X, W0, A, B, m, case.s, dY, eps)
+    for got, ref, nm in ((dX, rX, "dX"), (dA, rA, "dA"), (dB, rB, "dB"), (dm, rm[None], "dm")):
+        assert_close(got, ref, "bf16", nm)
 
 
 def test_dora_cols_init_and_strength0(ops):

@@ -84,3 +84,38 @@ def test_w8a8_checks():
         ops.w8a8_lora_fwd(Xq.float(), sx, Wq, sw, None, None, 1.0)
     with pytest.raises(ValueError):
         ops.w8a8_lora_bwd(_t(8, 32), Wq, sw, _t(4, 32), _t(16, 4), None, _t(8, 12), 1.0)
+
+
+def test_fp32_side_inputs_must_be_fp32():
+    """Vectors and saved factors the kernels read as fp32 (r0, n, c0, V, U, sx, sw) are rejected in
+    any other dtype: a bf16 tensor of the right shape holds half the bytes the kernel would read."""
+    a = _ok()
+    m_rows, m_cols = _t(16), _t(32)
+    with pytest.raises(ValueError):   # r0 in bf16
+        ops.dora_linear_fwd(a["X"], a["W0"], a["A"], a["B"], m_rows, _t(16), 1.0)
+    with pytest.raises(ValueError):   # m in the wrong dtype
+        ops.dora_linear_fwd(a["X"], a["W0"], a["A"], a["B"], _t(16, dtype=torch.float32),
+                            _t(16, dtype=torch.float32), 1.0)
+    Y, Z, dY = _t(8, 16), _t(8, 4), _t(8, 16)
+    with pytest.raises(ValueError):   # n in bf16
+        ops.dora_linear_bwd(a["X"], a["W0"], a["A"], a["B"], m_rows, None, Y, Z, _t(16),
+                            _t(16, 4, dtype=torch.float32), dY, 1.0)
+    with pytest.raises(ValueError):   # V in bf16
+        ops.dora_linear_bwd(a["X"], a["W0"], a["A"], a["B"], m_rows, None, Y, Z, _t(16, dtype=torch.float32),
+                            _t(16, 4), dY, 1.0)
+    with pytest.raises(ValueError):   # c0 in bf16
+        ops.dora_cols_fwd(a["X"], a["W0"], a["A"], a["B"], m_cols, _t(32), 1.0)
+    with pytest.raises(ValueError):   # U in bf16
+        ops.dora_cols_bwd(a["X"], a["W0"], a["A"], a["B"], m_cols, Z, _t(32, dtype=torch.float32), _t(32, 4),
+                          dY, 1.0)
+    Xq, Wq = torch.zeros(8, 32, dtype=torch.int8), torch.zeros(16, 32, dtype=torch.int8)
+    with pytest.raises(ValueError):   # sx in bf16
+        ops.w8a8_lora_fwd(Xq, _t(8), Wq, torch.ones(16), None, None, 1.0)
+    with pytest.raises(ValueError):   # sw in bf16
+        ops.w8a8_lora_fwd(Xq, torch.ones(8), Wq, _t(16), None, None, 1.0)
+    with pytest.raises(ValueError):   # rank-r input in fp32
+        ops.w8a8_lora_fwd(Xq, torch.ones(8), Wq, torch.ones(16), _t(8, 8, dtype=torch.float32), _t(16, 8), 1.0)
+    with pytest.raises(ValueError):   # backward: sw in bf16
+        ops.w8a8_lora_bwd(_t(8, 32), Wq, _t(16), _t(4, 32), _t(16, 4), None, _t(8, 16), 1.0)
+    with pytest.raises(ValueError):   # quantiser input in fp32
+        ops.w8a8_quantize_rows(_t(8, 32, dtype=torch.float32))

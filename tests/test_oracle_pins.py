@@ -259,6 +259,71 @@ def test_dora_grads_match_library_autograd():
         assert rel(g_, t[k].grad.numpy()) < 1e-12
 
 
+def test_golden_dora_eps_clamped_row():
+    """A row whose adapted weight is exactly zero: its norm sits on the eps floor and no
+    gradient flows through the norm there (hand-worked values)."""
+    g = _read_golden("dora_eps_clamped_row.txt")
+    X, W0, A, B = g["X"].reshape(1, 2), g["W0"].reshape(2, 2), g["A"].reshape(1, 2), g["B"].reshape(2, 1)
+    s, eps, dY = float(g["s"][0]), float(g["eps"][0]), g["dY"].reshape(1, 2)
+    y, n = O.dora_linear_fwd(X, W0, A, B, g["m"], s, eps, g["bias"])
+    np.testing.assert_allclose(n, g["n"], rtol=1e-15, atol=0)
+    np.testing.assert_allclose(y[0], g["y"], rtol=1e-15, atol=1e-15)
+    dX, dA, dB, dm, dbias = O.dora_linear_bwd(X, W0, A, B, g["m"], s, dY, eps)
+    for got, k in ((dX[0], "dX"), (dA[0], "dA"), (dB[:, 0], "dB"), (dm, "dm"), (dbias, "dbias")):
+        np.testing.assert_allclose(got, g[k], rtol=1e-14, atol=1e-15, err_msg=k)
+    sX, sA, sB, sm, _ = O.dora_bwd_sampled(X, W0, A, B, g["m"], s, dY, [0], [0, 1], [0, 1], eps)
+    np.testing.assert_allclose(sA, dA, rtol=1e-14)
+    np.testing.assert_allclose(sB, dB, rtol=1e-14)
+    np.testing.assert_allclose(sm, dm, rtol=1e-14, atol=1e-15)
+
+
+def _clamped_rows_case(seed, rows=(1, 4), shrink=0.05):
+    """rand_case with some rows of W0 and B shrunk so that their adapted norm (~0.05) is below
+    an eps of 0.3 while every other row (~1) is above it."""
+    X, W0, A, B, bias, m, dY = rand_case(M=4, d_in=8, d_out=6, r=2, seed=seed)
+    W0[list(rows)] *= shrink
+    B[list(rows)] *= shrink
+    return X, W0, A, B, bias, m, dY
+
+
+def test_dora_eps_clamped_rows_finite_difference():
+    """eps above some rows' norms: those rows take the floor (n = eps, no norm gradient) and the
+    others stay live; finite differences of the clamped function agree with the oracle's
+    gradients in both branches, and the sampled forms agree with the full ones."""
+    X, W0, A, B, bias, m, dY = _clamped_rows_case(15)
+    s, eps = 1.2, 0.3
+    _, n = O.dora_linear_fwd(X, W0, A, B, m, s, eps, bias)
+    nraw = np.linalg.norm(O.adapted_weight(W0, A, B, s), axis=1)
+    assert (nraw[[1, 4]] < 0.2).all() and (np.delete(nraw, [1, 4]) > 0.5).all()
+    assert (n[[1, 4]] == eps).all()
+    L = lambda: float((dY * O.dora_linear_fwd(X, W0, A, B, m, s, eps, bias)[0]).sum())  # noqa: E731
+    dX, dA, dB, dm, dbias = O.dora_linear_bwd(X, W0, A, B, m, s, dY, eps)
+    for got, x in ((dX, X), (dA, A), (dB, B), (dm, m), (dbias, bias)):
+        assert rel(got, _fd_grad(L, x)) < 1e-7
+    sX, sA, sB, sm, _ = O.dora_bwd_sampled(X, W0, A, B, m, s, dY, [0, 3], list(range(8)), [1, 2, 4], eps)
+    assert rel(sA, dA) < 1e-13 and rel(sB, dB[[1, 2, 4]]) < 1e-13 and rel(sm, dm) < 1e-13
+    rX, rB, rm = O.dora_bwd_rows_sampled(X, W0, A, B, m, s, dY, [0, 3], [1, 2, 4], eps)
+    assert rel(rX, dX[[0, 3]]) < 1e-13 and rel(rB, dB[[1, 2, 4]]) < 1e-13 and rel(rm, dm[[1, 2, 4]]) < 1e-13
+
+
+def test_dora_eps_zero_row_matches_library_autograd():
+    """A zero adapted row at eps = 1e-12, against torch autograd through clamp_min."""
+    X, W0, A, B, bias, m, dY = rand_case(M=7, d_in=11, d_out=9, r=3, seed=16)
+    W0[2] = 0.0
+    B[2] = 0.0
+    m[2] = 1.5
+    s = 0.6
+    t = {k: torch.tensor(v, requires_grad=True) for k, v in dict(X=X, A=A, B=B, m=m, bias=bias).items()}
+    Wp = torch.tensor(W0) + s * t["B"] @ t["A"]
+    n = torch.linalg.vector_norm(Wp, dim=1).clamp_min(1e-12)
+    y = torch.nn.functional.linear(t["X"], (t["m"] / n)[:, None] * Wp, t["bias"])
+    y.backward(torch.tensor(dY))
+    got = O.dora_linear_bwd(X, W0, A, B, m, s, dY)
+    for g_, k in zip(got, ("X", "A", "B", "m", "bias")):
+        assert rel(g_, t[k].grad.numpy()) < 1e-12, k
+    assert abs(got[2][2]).max() > 1e9      # the floor makes row 2's scale m / eps
+
+
 # ------------------------------------------------------------------ DoRA (cols)
 def cols_case(M=5, d_in=7, d_out=6, r=3, seed=40):
     X, W0, A, B, bias, _, dY = rand_case(M, d_in, d_out, r, seed)
@@ -342,6 +407,43 @@ def test_dora_cols_grads_match_library_autograd():
         assert rel(g_, t[k].grad.numpy()) < 1e-12, k
 
 
+def test_dora_cols_eps_clamped_columns_finite_difference():
+    """Column variant with eps above some columns' norms: floor branch and live branch both
+    agree with finite differences, and the sampled forms with the full ones."""
+    X, W0, A, B, bias, m, dY = cols_case(M=4, d_in=6, d_out=8, r=2, seed=50)
+    W0[:, [1, 4]] *= 0.05
+    A[:, [1, 4]] *= 0.05
+    s, eps = 1.2, 0.3
+    nraw = np.linalg.norm(O.adapted_weight(W0, A, B, s), axis=0)
+    assert (nraw[[1, 4]] < 0.2).all() and (np.delete(nraw, [1, 4]) > 0.5).all()
+    _, n = O.dora_cols_fwd(X, W0, A, B, m, s, eps, bias)
+    assert (n[[1, 4]] == eps).all()
+    L = lambda: float((dY * O.dora_cols_fwd(X, W0, A, B, m, s, eps, bias)[0]).sum())  # noqa: E731
+    dX, dA, dB, dm, db = O.dora_cols_bwd(X, W0, A, B, m, s, dY, eps)
+    for got, x in ((dX, X), (dA, A), (dB, B), (dm, m), (db, bias)):
+        assert rel(got, _fd_grad(L, x)) < 1e-7
+    sX, sA, sm = O.dora_cols_bwd_sampled(X, W0, A, B, m, s, dY, [0, 3], [1, 2, 4], eps)
+    assert rel(sA, dA[:, [1, 2, 4]]) < 1e-13 and rel(sm, dm[[1, 2, 4]]) < 1e-13
+    sB = O.dora_cols_bwd_rows_sampled(X, W0, A, B, m, s, dY, [0, 5, 7], eps)
+    assert rel(sB, dB[[0, 5, 7]]) < 1e-13
+
+
+def test_dora_cols_eps_zero_column_matches_library_autograd():
+    X, W0, A, B, bias, m, dY = cols_case(M=9, d_in=12, d_out=10, r=3, seed=51)
+    W0[:, 3] = 0.0
+    A[:, 3] = 0.0
+    m[3] = 1.5
+    s = 0.7
+    t = {k: torch.tensor(v, requires_grad=True) for k, v in dict(X=X, A=A, B=B, m=m, bias=bias).items()}
+    Wp = torch.tensor(W0) + s * t["B"] @ t["A"]
+    n = torch.linalg.vector_norm(Wp, dim=0).clamp_min(1e-12)
+    y = torch.nn.functional.linear(t["X"], Wp * (t["m"] / n)[None, :], t["bias"])
+    y.backward(torch.tensor(dY))
+    got = O.dora_cols_bwd(X, W0, A, B, m, s, dY)
+    for g_, k in zip(got, ("X", "A", "B", "m", "bias")):
+        assert rel(g_, t[k].grad.numpy()) < 1e-12, k
+
+
 def test_dora_cols_sampled_forms_match_full():
     X, W0, A, B, bias, m, dY = cols_case(M=9, d_in=12, d_out=10, r=3, seed=49)
     s = 0.9
@@ -351,6 +453,8 @@ def test_dora_cols_sampled_forms_match_full():
     dX, dA, _, dm, _ = O.dora_cols_bwd(X, W0, A, B, m, s, dY)
     sX, sA, sm = O.dora_cols_bwd_sampled(X, W0, A, B, m, s, dY, [0, 8], [2, 3, 11])
     assert rel(sX, dX[[0, 8]]) < 1e-13 and rel(sA, dA[:, [2, 3, 11]]) < 1e-13 and rel(sm, dm[[2, 3, 11]]) < 1e-13
+    _, _, dB, _, _ = O.dora_cols_bwd(X, W0, A, B, m, s, dY)
+    assert rel(O.dora_cols_bwd_rows_sampled(X, W0, A, B, m, s, dY, [0, 4, 9]), dB[[0, 4, 9]]) < 1e-13
 
 
 # ------------------------------------------------------------------ SwiGLU MLP

@@ -1,14 +1,16 @@
 """lora_linear_fwd_noalloc: the forward for callers that cannot allocate device memory.
 
-It must give the same result as lora_linear_fwd with a caller workspace, call after call
-(the shared scratch keeps the previous call's contents), and refuse problems larger than its
-fixed scratch.  This file is collected last so a stop-at-first-failure run has already run
-every other test; it also passes on its own in a fresh process.
+It runs the same kernels as lora_linear_fwd with a caller workspace, so its outputs must have
+the very same bits, call after call (the shared scratch keeps the previous call's contents);
+both are also held to the fp64 oracle.  It must refuse problems larger than its fixed scratch.
+This file is collected last so a stop-at-first-failure run has already run every other test;
+it also passes on its own in a fresh process.
 """
 import pytest
 import torch
 
 import datagen as D
+import oracle as O
 from parity import assert_close, to64
 
 pytestmark = pytest.mark.gpu
@@ -52,8 +54,11 @@ def test_no_alloc_matches_workspace_entry_point_twice(L):
         Yn, Zn = _no_alloc(L, case, g)
         Yw, Zw = _with_workspace(L, case, g)
         torch.cuda.synchronize()
-        assert_close(Yn, to64(Yw), "bf16", f"Y (seed {seed})")
-        assert_close(Zn, to64(Zw), "bf16", f"Z (seed {seed})")
+        assert torch.equal(Yn, Yw), f"Y differs from the workspace entry point (seed {seed})"
+        assert torch.equal(Zn, Zw), f"Z differs from the workspace entry point (seed {seed})"
+        X, W0, A, B, bias = (to64(g[k]) for k in ("X", "W0", "A", "B", "bias"))
+        assert_close(Yn, O.lora_linear_fwd(X, W0, A, B, case.s, bias), "bf16", f"Y vs oracle (seed {seed})")
+        assert_close(Zn, X @ A.T, "bf16", f"Z vs oracle (seed {seed})")
 
 
 def test_no_alloc_rejects_problems_beyond_its_scratch(L):
