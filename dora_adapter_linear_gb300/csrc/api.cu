@@ -140,7 +140,6 @@ struct DoraBwdWs {
   uint32_t* err;
   float *c, *g, *dot, *csum, *dotp, *csump, *Kr, *Kg, *Gw;
   void *Bc, *gB, *Gs, *Zrec;
-  bf16* dYc;     // [M, out] dY o c (bf16 path)
   float *PB, *PA, *PW;
   int splitsB, splitsA, splitsW;
 };
@@ -149,7 +148,7 @@ size_t plan_dora_bwd(const lora_shape& sh, char* base, DoraBwdWs* w) {
   const size_t es = sh.dtype == LORA_BF16 ? 2 : 4;
   const int64_t out = sh.d_out, in = sh.d_in, r = sh.r, M = sh.M;
   w->err = c.take<uint32_t>(kErrBytes / 4);
-  w->c = c.take<float>(out);
+  w->c = c.take<float>((out + 63) / 64 * 64);   // zero past out: the dX GEMM fetches 64 scales per k-step
   w->g = c.take<float>(out);
   w->dot = c.take<float>(out);
   w->csum = c.take<float>(out);
@@ -169,12 +168,10 @@ size_t plan_dora_bwd(const lora_shape& sh, char* base, DoraBwdWs* w) {
     w->PW = c.take<float>(w->splitsW * in * r);
     w->dotp = c.take<float>(w->splitsB * out);
     w->csump = c.take<float>(w->splitsB * out);
-    w->dYc = c.take<bf16>(M * out);
   } else {
     w->splitsB = w->splitsA = w->splitsW = 1;
     w->PB = w->PA = w->PW = nullptr;
     w->dotp = w->csump = nullptr;
-    w->dYc = nullptr;
   }
   return c.off;
 }
@@ -1082,7 +1079,7 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
   }
   if (bf) {
     const bf16* mb = static_cast<const bf16*>(m);
-    CK(dora_c<bf16>(out, mb, n_saved, w.c, st));
+    CK(dora_c<bf16>(out, mb, n_saved, w.c, st, (out + 63) / 64 * 64));
     const void* Z = Z_saved;
     if (!Z) {
       RowProjDesc d = rp_desc(M, in, r, X, A, false, w.err);
@@ -1090,19 +1087,12 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       CK(rowproj(d, st));
       Z = w.Zrec;
     }
-    // dP = dY o c enters the dX GEMM either as a copy written by the pass below (default) or
-    // scaled tile by tile in the GEMM's shared memory (LORA_GB300_DORA_KSCALE=1); same bits.
-    const bool kscale = env_flag("LORA_GB300_DORA_KSCALE");
-    {  // one pass over dY and Y: dY^T Z partials, colsum(dY), colsum(dY o Y), and dY o c
+    {  // one pass over dY and Y: dY^T Z partials, colsum(dY) and colsum(dY o Y)
       ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
       d.Y = static_cast<const bf16*>(Y);
       d.ldy = out;
       d.colsum = w.csump;
       d.coldot = w.dotp;
-      if (!kscale) {
-        d.sc = w.c;
-        d.sc_out = w.dYc;
-      }
       CK(colreduce(d, st));
     }
     CK(dora_dc<bf16>(out, w.dotp, w.csump, w.splitsB, static_cast<const bf16*>(bias), w.c, n_saved, mb, eps, w.g,
@@ -1115,10 +1105,9 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       d.scale_b = s;
       CK(rowproj(d, st));
     }
-    if (dX) {
-      if (kscale) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, w.c, w.err), st));
-      else CK(tc_gemm(dx_desc(M, in, out, w.dYc, W0, w.Gs, A, r, dX, nullptr, w.err), st));
-    }
+    // dX = (dY o c) W0 + s G A: dP = dY o c is formed tile by tile inside the GEMM (its A tiles are
+    // scaled by c in shared memory), so no [M, out] copy of it is ever written
+    if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, w.c, w.err), st));
     CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA, w.err), st));        // X^T (s G)
     CK(colreduce(cr_desc(out, in, r, W0, w.gB, r, w.PW, w.splitsW, w.err), st));     // W0^T (g o B)
     CK(gram_rows<bf16>(static_cast<const bf16*>(A), r, in, w.Kr, st));

@@ -64,7 +64,7 @@ struct TcGemmDesc {
   int64_t ldo = 0;
   const float* col_scale = nullptr;
   const bf16* bias = nullptr;
-  const float* a_kscale = nullptr;
+  const float* a_kscale = nullptr;   // [ceil(K0 / 64) * 64] fp32, zero past K0, 16-byte aligned
   const bf16* e_in = nullptr;
   const bf16* u_in = nullptr;
   int64_t ld_eu = 0;
@@ -127,9 +127,6 @@ struct ColReduceDesc {
   float* colsum = nullptr;     // [splits, K] or null
   float* coldot = nullptr;     // [splits, K] or null
   int splits = 1;
-  // with Y: optional column-scaled copy of S written on the way, sc_out[row, k] = bf16(S[row, k] * sc[k])
-  const float* sc = nullptr;
-  bf16* sc_out = nullptr;      // [rows, K], leading dimension K
   uint32_t* err = nullptr;     // device error word for bounded waits
   uint64_t timeout_ns = 2000000000ull;
 };
@@ -150,9 +147,10 @@ cudaError_t dora_norm(int64_t out, int r, const float* r0, const float* V, const
 // sum over splits of column partials: dst[k] = sum_s src[s][k]  (fp32 and, optionally, as T)
 template <typename T>
 cudaError_t sum_splits(const float* src, int splits, int64_t n, float* dst_f, T* dst_t, cudaStream_t st);
-// c = m / n
+// c = m / n for o < out, and c = 0 for out <= o < padded (a zero tail for readers that fetch whole
+// 64-entry blocks)
 template <typename T>
-cudaError_t dora_c(int64_t out, const T* m, const float* n, float* c, cudaStream_t st);
+cudaError_t dora_c(int64_t out, const T* m, const float* n, float* c, cudaStream_t st, int64_t padded = 0);
 // DoRA backward small step: dc = (dot - bias*colsum)/c ; dm = dc/n ; g = -m dc/(2 n^3) (0 if n<=eps);
 // dot and csum are [splits, out] partials (csum read only with a bias or dbias).
 template <typename T>

@@ -364,7 +364,6 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
   for (int i = 0; i < R / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
   float csum = 0.f, cdot = 0.f;
   const int my_col = tid & 63, my_par = tid >> 6;   // column sums: 2 row phases x 64 columns
-  const int c8 = tid & 7;                            // scaled copy: 16-byte chunk of this thread
   for (int rc = 0; rc < nrc; ++rc) {
     const int s = rc % NST;
     const uint32_t ph = (uint32_t)(rc / NST) & 1u;
@@ -387,29 +386,6 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
         else ldsm_x2_t(b0, b1, sT + swz(row, nt, C::TPITCH, C::TMASK));
         mma_bf16_16816(acc[nt], a, b0, b1);
         if (nt + 1 < R / 8) mma_bf16_16816(acc[nt + 1], a, b2, b3);
-      }
-    }
-    const int64_t rb = r_begin + (int64_t)rc * BR;
-    if (HAS_Y && d.sc_out) {
-      // column-scaled copy of the S tile: thread tid owns chunk c8 of rows tid/8 + 16 i
-      const int64_t gk = k0 + c8 * 8;
-      if (gk < d.K) {
-        const float4 lo = __ldg(reinterpret_cast<const float4*>(d.sc + gk));
-        const float4 hi = __ldg(reinterpret_cast<const float4*>(d.sc + gk + 4));
-        const float sc8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = (tid >> 3) + 16 * i;
-          if (rb + r >= r_end) break;
-          uint4 v = *reinterpret_cast<const uint4*>(tile + swz(r, c8, 128, 7));
-          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = unpack_bf16x2(w[e]);
-            w[e] = pack_bf16x2(f.x * sc8[2 * e], f.y * sc8[2 * e + 1]);
-          }
-          *reinterpret_cast<uint4*>(d.sc_out + (rb + r) * d.K + gk) = v;
-        }
       }
     }
     if (SUMS) {

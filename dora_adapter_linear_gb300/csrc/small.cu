@@ -187,14 +187,16 @@ cudaError_t dora_norm(int64_t out, int r, const float* r0, const float* V, const
 
 // ------------------------------------------------------------------ c = m / n
 template <typename T>
-__global__ void dora_c_kernel(int64_t out, const T* m, const float* n, float* c) {
+__global__ void dora_c_kernel(int64_t out, int64_t padded, const T* m, const float* n, float* c) {
   const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (o < out) c[o] = ldf(m, o) / n[o];
+  else if (o < padded) c[o] = 0.f;
 }
 template <typename T>
-cudaError_t dora_c(int64_t out, const T* m, const float* n, float* c, cudaStream_t st) {
+cudaError_t dora_c(int64_t out, const T* m, const float* n, float* c, cudaStream_t st, int64_t padded) {
   if (out <= 0) return cudaSuccess;
-  dora_c_kernel<T><<<(unsigned)((out + 255) / 256), 256, 0, st>>>(out, m, n, c);
+  if (padded < out) padded = out;
+  dora_c_kernel<T><<<(unsigned)((padded + 255) / 256), 256, 0, st>>>(out, padded, m, n, c);
   count_launch();
   return cudaGetLastError();
 }
@@ -693,7 +695,7 @@ cudaError_t debug_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t 
   template cudaError_t gram_weighted<T>(const T*, int64_t, int, const float*, float*, float*, cudaStream_t);                \
   template cudaError_t dora_norm<T>(int64_t, int, const float*, const float*, const T*, const float*, const T*,     \
                                     float, float, float*, float*, cudaStream_t);                                    \
-  template cudaError_t dora_c<T>(int64_t, const T*, const float*, float*, cudaStream_t);                            \
+  template cudaError_t dora_c<T>(int64_t, const T*, const float*, float*, cudaStream_t, int64_t);                            \
   template cudaError_t sum_splits<T>(const float*, int, int64_t, float*, T*, cudaStream_t);                         \
   template cudaError_t dora_dc<T>(int64_t, const float*, const float*, int, const T*, const float*, const float*,        \
                                   const T*, float, float*, T*, T*, cudaStream_t);                                   \
