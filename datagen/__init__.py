@@ -55,7 +55,8 @@ class LinearCase:
 
 @dataclass(frozen=True)
 class MlpCase:
-    """LoRA SwiGLU MLP: h = silu(X Wg'^T) * (X Wu'^T), y = h Wd'^T."""
+    """LoRA SwiGLU MLP: h = silu(X Wg'^T) * (X Wu'^T), y = h Wd'^T.  r is the gate projection's
+    rank; r_u and r_d (None: the same as r) those of the up and down projections."""
     name: str
     M: int
     H: int
@@ -64,10 +65,21 @@ class MlpCase:
     alpha: float
     dtype: str = "bf16"
     seed: int = 1003
+    r_u: int = None
+    r_d: int = None
+
+    @property
+    def ranks(self) -> dict:
+        return {"g": self.r, "u": self.r_u or self.r, "d": self.r_d or self.r}
 
     @property
     def s(self) -> float:
         return self.alpha / self.r
+
+    @property
+    def scales(self) -> dict:
+        """s = alpha / rank of each projection."""
+        return {p: self.alpha / rk for p, rk in self.ranks.items()}
 
 
 @dataclass(frozen=True)
@@ -160,9 +172,10 @@ def make_mlp(case: MlpCase):
     """CPU tensors for the SwiGLU MLP: X, (Wg, Ag, Bg), (Wu, Au, Bu), (Wd, Ad, Bd), dY."""
     g = torch.Generator().manual_seed(case.seed)
     dt = _TORCH_DT[case.dtype]
-    H, I, r = case.H, case.I, case.r
+    H, I = case.H, case.I
     out = {"X": _normal(g, (case.M, H), 1.0).to(dt)}
     for p, (n_out, n_in) in (("g", (I, H)), ("u", (I, H)), ("d", (H, I))):
+        r = case.ranks[p]
         out["W" + p] = _normal(g, (n_out, n_in), n_in ** -0.5).to(dt)
         out["A" + p] = _normal(g, (r, n_in), n_in ** -0.5).to(dt)
         out["B" + p] = _normal(g, (n_out, r), 0.02).to(dt)

@@ -33,8 +33,8 @@ class LoraShape(ctypes.Structure):
 
 
 class LoraMlpShape(ctypes.Structure):
-    _fields_ = [("M", c_int64), ("H", c_int64), ("I", c_int64), ("r", c_int64), ("dtype", c_int32),
-                ("act", c_int32)]
+    _fields_ = [("M", c_int64), ("H", c_int64), ("I", c_int64), ("r_g", c_int64), ("r_u", c_int64),
+                ("r_d", c_int64), ("dtype", c_int32), ("act", c_int32)]
 
 
 LORA_ACT_SWIGLU, LORA_ACT_GEGLU = 0, 1
@@ -149,8 +149,11 @@ def shape(M, d_in, d_out, r, dtype) -> LoraShape:
     return LoraShape(M, d_in, d_out, r, dtype)
 
 
-def mlp_shape(M, H, I, r, dtype=LORA_BF16, act=0) -> LoraMlpShape:
-    return LoraMlpShape(M, H, I, r, dtype, act)
+def mlp_shape(M, H, I, r_g, r_u=None, r_d=None, dtype=LORA_BF16, act=0) -> LoraMlpShape:
+    """Ranks of the gate, up and down projections (r_u, r_d default to r_g)."""
+    r_u = r_g if r_u is None else r_u
+    r_d = r_g if r_d is None else r_d
+    return LoraMlpShape(M, H, I, r_g, r_u, r_d, dtype, act)
 
 
 def proj(W, A, B, s) -> LoraProj:

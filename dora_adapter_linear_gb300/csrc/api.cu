@@ -65,7 +65,7 @@ lora_status check_shape(const lora_shape* sh) {
   if (sh->M < 0 || sh->d_in <= 0 || sh->d_out <= 0 || sh->r <= 0) return LORA_ERR_INVALID_ARG;
   if (sh->dtype != LORA_F32 && sh->dtype != LORA_BF16) return LORA_ERR_INVALID_ARG;
   if (sh->d_in % 8 || sh->d_out % 8) return LORA_ERR_UNSUPPORTED;
-  if (sh->r > 64) return LORA_ERR_UNSUPPORTED;
+  if (sh->r > 128) return LORA_ERR_UNSUPPORTED;
   if (sh->dtype == LORA_BF16 && sh->r % 8) return LORA_ERR_UNSUPPORTED;
   if (sh->M > (1LL << 31) - 1 || sh->d_in > (1LL << 31) - 1 || sh->d_out > (1LL << 31) - 1)
     return LORA_ERR_UNSUPPORTED;
@@ -240,10 +240,11 @@ struct MlpFwdWs {
 };
 size_t plan_mlp_fwd(const lora_mlp_shape& sh, char* base, MlpFwdWs* w) {
   Carve c{base};
+  const int64_t rgu = sh.r_g + sh.r_u;
   w->err = c.take<uint32_t>(kErrBytes / 4);
-  w->Agu = c.take<bf16>(2 * sh.r * sh.H);
-  w->Zgus = c.take<bf16>(sh.M * 2 * sh.r);
-  w->Zds = c.take<bf16>(sh.M * sh.r);
+  w->Agu = c.take<bf16>(rgu * sh.H);
+  w->Zgus = c.take<bf16>(sh.M * rgu);
+  w->Zds = c.take<bf16>(sh.M * sh.r_d);
   return c.off;
 }
 
@@ -257,21 +258,22 @@ struct MlpBwdWs {
 };
 size_t plan_mlp_bwd(const lora_mlp_shape& sh, char* base, MlpBwdWs* w) {
   Carve c{base};
-  const int64_t M = sh.M, H = sh.H, I = sh.I, r = sh.r, Ip = mlp_ipad(sh);
+  const int64_t M = sh.M, H = sh.H, I = sh.I, Ip = mlp_ipad(sh);
+  const int64_t rg = sh.r_g, ru = sh.r_u, rd = sh.r_d, rgu = rg + ru;
   w->err = c.take<uint32_t>(kErrBytes / 4);
   w->dedu = c.take<bf16>(M * 2 * Ip);
-  w->Gds = c.take<bf16>(M * r);
-  w->Ggus = c.take<bf16>(M * 2 * r);
-  w->Agu = c.take<bf16>(2 * r * H);
+  w->Gds = c.take<bf16>(M * rd);
+  w->Ggus = c.take<bf16>(M * rgu);
+  w->Agu = c.take<bf16>(rgu * H);
   w->sBd = colreduce_splits(M, H);
   w->sAd = colreduce_splits(M, I);
   w->sBg = w->sAd;
   w->sAgu = colreduce_splits(M, H);
-  w->PBd = c.take<float>(w->sBd * H * r);
-  w->PAd = c.take<float>(w->sAd * I * r);
-  w->PBg = c.take<float>(w->sBg * I * r);
-  w->PBu = c.take<float>(w->sBg * I * r);
-  w->PAgu = c.take<float>(w->sAgu * H * 2 * r);
+  w->PBd = c.take<float>(w->sBd * H * rd);
+  w->PAd = c.take<float>(w->sAd * I * rd);
+  w->PBg = c.take<float>(w->sBg * I * rg);
+  w->PBu = c.take<float>(w->sBg * I * ru);
+  w->PAgu = c.take<float>(w->sAgu * H * rgu);
   return c.off;
 }
 
@@ -464,7 +466,7 @@ const char* lora_status_string(int status) {
   return "unknown status";
 }
 
-int lora_abi_version(void) { return 6; }
+int lora_abi_version(void) { return 7; }
 
 size_t lora_workspace_bytes(int op, const lora_shape* sh) {
   if (check_shape(sh) != LORA_OK) return 0;
@@ -491,10 +493,13 @@ size_t lora_workspace_bytes(int op, const lora_shape* sh) {
 
 static lora_status check_mlp_shape(const lora_mlp_shape* sh) {
   if (!sh) return LORA_ERR_INVALID_ARG;
-  if (sh->M < 0 || sh->H <= 0 || sh->I <= 0 || sh->r <= 0) return LORA_ERR_INVALID_ARG;
+  if (sh->M < 0 || sh->H <= 0 || sh->I <= 0 || sh->r_g <= 0 || sh->r_u <= 0 || sh->r_d <= 0)
+    return LORA_ERR_INVALID_ARG;
   if (sh->dtype != LORA_BF16) return sh->dtype == LORA_F32 ? LORA_ERR_UNSUPPORTED : LORA_ERR_INVALID_ARG;
   if (sh->act != LORA_ACT_SWIGLU && sh->act != LORA_ACT_GEGLU) return LORA_ERR_INVALID_ARG;
-  if (sh->H % 8 || sh->I % 8 || sh->r % 8 || sh->r > 64) return LORA_ERR_UNSUPPORTED;
+  if (sh->H % 8 || sh->I % 8) return LORA_ERR_UNSUPPORTED;
+  for (const int64_t r : {sh->r_g, sh->r_u, sh->r_d})
+    if (r % 8 || r > 128) return LORA_ERR_UNSUPPORTED;
   if (sh->M > (1LL << 31) - 1 || 2 * mlp_ipad(*sh) > (1LL << 31) - 1) return LORA_ERR_UNSUPPORTED;
   return LORA_OK;
 }
@@ -514,7 +519,7 @@ static lora_status check_qkv_shape(const lora_qkv_shape* sh) {
     if (sh->n[l] <= 0) return LORA_ERR_INVALID_ARG;
     if (sh->n[l] % 8) return LORA_ERR_UNSUPPORTED;
   }
-  if (sh->d_in % 8 || sh->r % 8 || sh->r > 64) return LORA_ERR_UNSUPPORTED;
+  if (sh->d_in % 8 || sh->r % 8 || sh->r > 128) return LORA_ERR_UNSUPPORTED;
   if (sh->M > (1LL << 31) - 1 || sh->d_in > (1LL << 31) - 1 || qkv_N(*sh) > (1LL << 31) - 1)
     return LORA_ERR_UNSUPPORTED;
   return LORA_OK;
@@ -1333,28 +1338,18 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
   if (sh->M == 0) return LORA_OK;
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t M = sh->M, H = sh->H, I = sh->I;
-  const int r = (int)sh->r;
-  CK(concat_rows_bf16(static_cast<const bf16*>(gate->A), r, static_cast<const bf16*>(up->A), r, H, w.Agu, st));
-  if (2 * r <= 64) {  // [Zg | Zu] = X [Ag ; Au]^T in one pass, saved unscaled and scaled per half
-    RowProjDesc d = rp_desc(M, H, 2 * r, X, w.Agu, false, w.err);
+  const int rg = (int)sh->r_g, ru = (int)sh->r_u, rd = (int)sh->r_d, rgu = rg + ru;
+  CK(concat_rows_bf16(static_cast<const bf16*>(gate->A), rg, static_cast<const bf16*>(up->A), ru, H, w.Agu, st));
+  {  // [Zg | Zu] = X [Ag ; Au]^T (one pass per 64 columns), saved unscaled and scaled per half
+    RowProjDesc d = rp_desc(M, H, rgu, X, w.Agu, false, w.err);
     d.out_a = static_cast<bf16*>(Zgu_save);
     d.out_b = w.Zgus;
     d.scale_b = gate->s;
-    d.split_col = r;
+    d.split_col = rg;
     d.scale_b_hi = up->s;
     CK(rowproj(d, st));
-  } else {  // ranks above 32: one pass per half (the rank-r kernels take at most 64 columns)
-    const lora_proj* pr[2] = {gate, up};
-    for (int h = 0; h < 2; ++h) {
-      RowProjDesc d = rp_desc(M, H, r, X, pr[h]->A, false, w.err);
-      d.out_a = static_cast<bf16*>(Zgu_save) + h * r;
-      d.out_b = w.Zgus + h * r;
-      d.scale_b = pr[h]->s;
-      d.ldo = 2 * r;
-      CK(rowproj(d, st));
-    }
   }
-  {  // e, u, h = gate/up GEMM with both adapters, SwiGLU epilogue
+  {  // e, u, h = gate/up GEMM with both adapters, gated epilogue
     TcGemmDesc d;
     d.mode = TC_SWIGLU_FWD;
     d.act = sh->act;
@@ -1366,16 +1361,18 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
     d.B0 = gate->W;
     d.B0b = up->W;
     d.ldb0 = H;
-    d.has_tail = true;
+    d.has_tail = true;   // tail K = [Zg | Zu] against [Bg | 0] (gate half) and [0 | Bu] (up half)
     d.A1 = w.Zgus;
-    d.lda1 = 2 * r;
-    d.K1 = 2 * r;
-    d.K1_a = 2 * r;
+    d.lda1 = rgu;
+    d.K1 = rgu;
+    d.K1_a = rgu;
     d.B1 = gate->B;
+    d.ldb1 = rg;
+    d.K1_b = rg;
     d.B1b = up->B;
-    d.ldb1 = r;
-    d.K1_b = r;
-    d.b1b_x = -r;
+    d.ldb1b = ru;
+    d.K1_bb = ru;
+    d.b1b_x = -rg;       // the up half's columns start after the gate rank (left of them: zero fill)
     d.out[0] = e_save;
     d.out[1] = u_save;
     d.out[2] = h_save;
@@ -1385,13 +1382,13 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
     CK(tc_gemm(d, st));
   }
   {  // Zd = h Ad^T
-    RowProjDesc d = rp_desc(M, I, r, h_save, down->A, false, w.err);
+    RowProjDesc d = rp_desc(M, I, rd, h_save, down->A, false, w.err);
     d.out_a = static_cast<bf16*>(Zd_save);
     d.out_b = w.Zds;
     d.scale_b = down->s;
     CK(rowproj(d, st));
   }
-  CK(tc_gemm(fwd_desc(M, H, I, h_save, down->W, w.Zds, down->B, r, Y, nullptr, nullptr, w.err), st));
+  CK(tc_gemm(fwd_desc(M, H, I, h_save, down->W, w.Zds, down->B, rd, Y, nullptr, nullptr, w.err), st));
   return LORA_OK;
 }
 
@@ -1415,27 +1412,27 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
   plan_mlp_bwd(*sh, static_cast<char*>(ws), &w);
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t M = sh->M, H = sh->H, I = sh->I, Ip = mlp_ipad(*sh);
-  const int r = (int)sh->r;
+  const int rg = (int)sh->r_g, ru = (int)sh->r_u, rd = (int)sh->r_d, rgu = rg + ru;
   if (M == 0) {
-    CK(cudaMemsetAsync(dAg, 0, (size_t)r * H * 2, st));
-    CK(cudaMemsetAsync(dAu, 0, (size_t)r * H * 2, st));
-    CK(cudaMemsetAsync(dBg, 0, (size_t)I * r * 2, st));
-    CK(cudaMemsetAsync(dBu, 0, (size_t)I * r * 2, st));
-    CK(cudaMemsetAsync(dAd, 0, (size_t)r * I * 2, st));
-    CK(cudaMemsetAsync(dBd, 0, (size_t)H * r * 2, st));
+    CK(cudaMemsetAsync(dAg, 0, (size_t)rg * H * 2, st));
+    CK(cudaMemsetAsync(dAu, 0, (size_t)ru * H * 2, st));
+    CK(cudaMemsetAsync(dBg, 0, (size_t)I * rg * 2, st));
+    CK(cudaMemsetAsync(dBu, 0, (size_t)I * ru * 2, st));
+    CK(cudaMemsetAsync(dAd, 0, (size_t)rd * I * 2, st));
+    CK(cudaMemsetAsync(dBd, 0, (size_t)H * rd * 2, st));
     return LORA_OK;
   }
   const bf16* Zgu = static_cast<const bf16*>(Zgu_saved);
   // down projection: dBd partials (dY^T Zd), sd*Gd = sd dY Bd
-  CK(colreduce(cr_desc(M, H, r, dY, Zd_saved, r, w.PBd, w.sBd, w.err), st));
+  CK(colreduce(cr_desc(M, H, rd, dY, Zd_saved, rd, w.PBd, w.sBd, w.err), st));
   {
-    RowProjDesc d = rp_desc(M, H, r, dY, down->B, true, w.err);
+    RowProjDesc d = rp_desc(M, H, rd, dY, down->B, true, w.err);
     d.out_b = w.Gds;
     d.scale_b = down->s;
     CK(rowproj(d, st));
   }
   if (Ip != I) CK(cudaMemsetAsync(w.dedu, 0, (size_t)M * 2 * Ip * 2, st));
-  {  // dh = dY Wd + (sd Gd) Ad, SwiGLU backward in the epilogue -> de, du
+  {  // dh = dY Wd + (sd Gd) Ad, gated backward in the epilogue -> de, du
     TcGemmDesc d;
     d.mode = TC_SWIGLU_BWD;
     d.act = sh->act;
@@ -1451,9 +1448,9 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     d.has_tail = true;
     d.b1_mn = true;
     d.A1 = w.Gds;
-    d.lda1 = r;
-    d.K1 = r;
-    d.K1_a = r;
+    d.lda1 = rd;
+    d.K1 = rd;
+    d.K1_a = rd;
     d.B1 = down->A;
     d.ldb1 = I;
     d.out[0] = w.dedu;
@@ -1466,30 +1463,30 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     d.timeout_ns = wait_timeout_ns();
     CK(tc_gemm(d, st));
   }
-  CK(colreduce(cr_desc(M, I, r, h_saved, w.Gds, r, w.PAd, w.sAd, w.err), st));     // h^T (sd Gd)
+  CK(colreduce(cr_desc(M, I, rd, h_saved, w.Gds, rd, w.PAd, w.sAd, w.err), st));     // h^T (sd Gd)
   {  // de^T Zg and du^T Zu
-    ColReduceDesc d = cr_desc(M, I, r, w.dedu, Zgu, 2 * r, w.PBg, w.sBg, w.err);
+    ColReduceDesc d = cr_desc(M, I, rg, w.dedu, Zgu, rgu, w.PBg, w.sBg, w.err);
     d.lds = 2 * Ip;
     CK(colreduce(d, st));
-    ColReduceDesc d2 = cr_desc(M, I, r, w.dedu + Ip, Zgu + r, 2 * r, w.PBu, w.sBg, w.err);
+    ColReduceDesc d2 = cr_desc(M, I, ru, w.dedu + Ip, Zgu + rg, rgu, w.PBu, w.sBg, w.err);
     d2.lds = 2 * Ip;
     CK(colreduce(d2, st));
   }
   {  // [sg Gg | su Gu] = [sg de Bg | su du Bu]
-    RowProjDesc d = rp_desc(M, I, r, w.dedu, gate->B, true, w.err);
+    RowProjDesc d = rp_desc(M, I, rg, w.dedu, gate->B, true, w.err);
     d.lds = 2 * Ip;
     d.out_b = w.Ggus;
     d.scale_b = gate->s;
-    d.ldo = 2 * r;
+    d.ldo = rgu;
     CK(rowproj(d, st));
-    RowProjDesc d2 = rp_desc(M, I, r, w.dedu + Ip, up->B, true, w.err);
+    RowProjDesc d2 = rp_desc(M, I, ru, w.dedu + Ip, up->B, true, w.err);
     d2.lds = 2 * Ip;
-    d2.out_b = w.Ggus + r;
+    d2.out_b = w.Ggus + rg;
     d2.scale_b = up->s;
-    d2.ldo = 2 * r;
+    d2.ldo = rgu;
     CK(rowproj(d2, st));
   }
-  CK(concat_rows_bf16(static_cast<const bf16*>(gate->A), r, static_cast<const bf16*>(up->A), r, H, w.Agu, st));
+  CK(concat_rows_bf16(static_cast<const bf16*>(gate->A), rg, static_cast<const bf16*>(up->A), ru, H, w.Agu, st));
   if (dX) {  // dX = [de | du] [Wg ; Wu] + [sg Gg | su Gu] [Ag ; Au]
     TcGemmDesc d;
     d.mode = TC_BWD_DX;
@@ -1508,9 +1505,9 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     d.has_tail = true;
     d.b1_mn = true;
     d.A1 = w.Ggus;
-    d.lda1 = 2 * r;
-    d.K1 = 2 * r;
-    d.K1_a = 2 * r;
+    d.lda1 = rgu;
+    d.K1 = rgu;
+    d.K1_a = rgu;
     d.B1 = w.Agu;
     d.ldb1 = H;
     d.out[0] = dX;
@@ -1519,23 +1516,14 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     d.timeout_ns = wait_timeout_ns();
     CK(tc_gemm(d, st));
   }
-  // X^T [sg Gg | su Gu]: one pass for ranks up to 32, one pass per half above
-  Partial pag{w.PAgu, w.sAgu, 2 * r, 0}, pau{w.PAgu, w.sAgu, 2 * r, r};
-  if (2 * r <= 64) {
-    CK(colreduce(cr_desc(M, H, 2 * r, X, w.Ggus, 2 * r, w.PAgu, w.sAgu, w.err), st));
-  } else {
-    float* half2 = w.PAgu + (size_t)w.sAgu * H * r;
-    CK(colreduce(cr_desc(M, H, r, X, w.Ggus, 2 * r, w.PAgu, w.sAgu, w.err), st));
-    CK(colreduce(cr_desc(M, H, r, X, w.Ggus + r, 2 * r, half2, w.sAgu, w.err), st));
-    pag = Partial{w.PAgu, w.sAgu, r, 0};
-    pau = Partial{half2, w.sAgu, r, 0};
-  }
-  const FinJob fin[6] = {fin_dA(r, H, pag, 1.f, nullptr, dAg),
-                         fin_dA(r, H, pau, 1.f, nullptr, dAu),
-                         fin_dA(r, I, Partial{w.PAd, w.sAd, r, 0}, 1.f, nullptr, dAd),
-                         fin_dB(H, r, Partial{w.PBd, w.sBd, r, 0}, down->s, nullptr, dBd),
-                         fin_dB(I, r, Partial{w.PBg, w.sBg, r, 0}, gate->s, nullptr, dBg),
-                         fin_dB(I, r, Partial{w.PBu, w.sBg, r, 0}, up->s, nullptr, dBu)};
+  // X^T [sg Gg | su Gu] (one pass over X per 64 columns)
+  CK(colreduce(cr_desc(M, H, rgu, X, w.Ggus, rgu, w.PAgu, w.sAgu, w.err), st));
+  const FinJob fin[6] = {fin_dA(rg, H, Partial{w.PAgu, w.sAgu, rgu, 0}, 1.f, nullptr, dAg),
+                         fin_dA(ru, H, Partial{w.PAgu, w.sAgu, rgu, rg}, 1.f, nullptr, dAu),
+                         fin_dA(rd, I, Partial{w.PAd, w.sAd, rd, 0}, 1.f, nullptr, dAd),
+                         fin_dB(H, rd, Partial{w.PBd, w.sBd, rd, 0}, down->s, nullptr, dBd),
+                         fin_dB(I, rg, Partial{w.PBg, w.sBg, rg, 0}, gate->s, nullptr, dBg),
+                         fin_dB(I, ru, Partial{w.PBu, w.sBg, ru, 0}, up->s, nullptr, dBu)};
   CK(finalize_batch(fin, 6, st));
   return LORA_OK;
 }
@@ -1547,7 +1535,7 @@ lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t
   REQM(rows, X); REQM(rows, Xq); REQM(rows, sx);
   ALN(X); ALN(Xq); ALN(A); ALN(Z);
   if ((A == nullptr) != (Z == nullptr)) return LORA_ERR_INVALID_ARG;
-  if (A && (r < 8 || r > 64 || r % 8)) return LORA_ERR_UNSUPPORTED;
+  if (A && (r < 8 || r > 128 || r % 8)) return LORA_ERR_UNSUPPORTED;
   cudaStream_t st = (cudaStream_t)stream;
   if (rows == 0) return LORA_OK;
   CK(quantize_rows_bf16(static_cast<const bf16*>(X), rows, cols, Xq, sx, st));
@@ -1562,12 +1550,13 @@ lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t
 // Largest d_in for which both split partial products keep every fp32 partial sum an integer
 // below 2^24 (|x| <= 127, |w >> 4| <= 8, |w & 15| <= 15: 127 * 15 * 8800 < 2^24).
 constexpr int64_t kW8ExactMaxK = 8800;
+constexpr int64_t kW8MaxR = 128;   // largest rank of the low-rank term
 
 size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out) {
   if (M < 0 || d_in <= 0 || d_out <= 0) return 0;
-  // + the rank-r operands of the fused epilogue, pre-divided by the dequant scales (r <= 64)
+  // + the rank-r operands of the fused epilogue, pre-divided by the dequant scales (r <= 128)
   return kErrBytes + al256((size_t)M * d_in * 2) + 2 * al256((size_t)d_out * d_in * 2) +
-         al256((size_t)M * 64 * 2) + al256((size_t)d_out * 64 * 2);
+         al256((size_t)M * kW8MaxR * 2) + al256((size_t)d_out * kW8MaxR * 2);
 }
 
 lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq, const float* sx,
@@ -1579,7 +1568,7 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
   if (Y == nullptr && acc_out == nullptr) return LORA_ERR_INVALID_ARG;
   if (Y && (!sx || !sw)) return LORA_ERR_INVALID_ARG;
   if ((Z == nullptr) != (B == nullptr)) return LORA_ERR_INVALID_ARG;
-  if (Z && (r < 8 || r > 64 || r % 8)) return LORA_ERR_UNSUPPORTED;
+  if (Z && (r < 8 || r > kW8MaxR || r % 8)) return LORA_ERR_UNSUPPORTED;
   if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
   ALN(Xq); ALN(sx); ALN(Wq); ALN(sw); ALN(Z); ALN(B); ALN(bias); ALN(Y); ALN(acc_out);
   lora_status e = check_ws(ws, ws_bytes, w8a8_workspace_bytes(M, d_in, d_out));
@@ -1604,8 +1593,8 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
     // (s Z / sx) (B / sw)^T, so the epilogue is y = (16 hi + lo) sx sw + bias and the accumulators
     // fit twice in TMEM (double-buffered, like every other mode).  The low half then holds the
     // exact integer partial sum plus that term, rounded once in fp32.
-    bf16* Zt = c.take<bf16>((size_t)M * 64);
-    bf16* Bt = c.take<bf16>((size_t)d_out * 64);
+    bf16* Zt = c.take<bf16>((size_t)M * kW8MaxR);
+    bf16* Bt = c.take<bf16>((size_t)d_out * kW8MaxR);
     d.mode = TC_W8A8F;
     d.M = (int)M;
     d.N = (int)d_out;
@@ -1632,7 +1621,9 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
       d.B1b = Bt;         // second (low) half
       d.ldb1 = r;
       d.K1_b = (int)r;
-      d.b1_x = 64;
+      d.ldb1b = r;
+      d.K1_bb = (int)r;
+      d.b1_x = kW8MaxR;   // at or past r for every tail step
       d.b1b_x = 0;
     }
     d.err = err;

@@ -58,6 +58,8 @@ struct TcGemmDesc {
   const void* B1b = nullptr;
   int64_t ldb1 = 0;
   int K1_b = 0;                // columns of a K-major B1 tensor
+  int64_t ldb1b = 0;           // stacked tail: row stride and columns of the second half's tensor
+  int K1_bb = 0;               //   (0: those of the first half)
   int b1b_x = 0;
   int b1_x = 0;                // stacked tail: x coordinate of the first half (past the tensor = zeros)
   void* out[3] = {nullptr, nullptr, nullptr};
@@ -86,7 +88,8 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st);
 // ------------------------------------------------------------------ skinny (rank-r) kernels, bf16
 // T = S U^T : S [rows, K] (ld lds), U either [R, K] (u_kr = false) or [K, R] (u_kr = true).
 // Outputs (each optional): out_a = bf16(scale_a * T), out_b = bf16(scale_b * T), out_f = T (fp32),
-// all with leading dimension R.  R multiple of 8, 8 <= R <= 64.
+// all with leading dimension R.  R multiple of 8, 8 <= R <= 512; above 64 the columns go in
+// chunks of 64, one pass over S each (the scaled copy of S is written by the first).
 struct RowProjDesc {
   int64_t rows = 0, K = 0;
   int R = 0;
@@ -111,9 +114,11 @@ struct RowProjDesc {
 };
 cudaError_t rowproj(const RowProjDesc& d, cudaStream_t st);
 
-// Column reduction over rows: part[split][k][j] = sum_{rows of split} S[row, k] * T[row, j]
-// (S [rows, K] ld lds, T [rows, R] ld ldt), plus optional per-column sums
-// colsum[split][k] = sum S[row,k] and coldot[split][k] = sum S[row,k] * Y[row,k].
+// Column reduction over rows: part[(split K + k) ldp + j0 + j] = sum_{rows of split} S[row, k] T[row, j]
+// (S [rows, K] ld lds, T [rows, R] ld ldt; ldp defaults to R, j0 to 0), plus optional per-column
+// sums colsum[split][k] = sum S[row,k] and coldot[split][k] = sum S[row,k] * Y[row,k].  R multiple
+// of 8 up to 512; above 64 the columns of T go in chunks of 64, one pass over S each (the column
+// sums come with the first).
 struct ColReduceDesc {
   int64_t rows = 0, K = 0;
   int R = 0;
@@ -123,7 +128,9 @@ struct ColReduceDesc {
   int64_t ldt = 0;
   const bf16* Y = nullptr;     // optional second [rows, K] input for coldot
   int64_t ldy = 0;
-  float* part = nullptr;       // [splits, K, R]
+  float* part = nullptr;       // [splits, K, ldp]
+  int ldp = 0;                 // leading dimension of part (0 -> R)
+  int j0 = 0;                  // first column of part written
   float* colsum = nullptr;     // [splits, K] or null
   float* coldot = nullptr;     // [splits, K] or null
   int splits = 1;
@@ -219,7 +226,7 @@ inline FinJob fin_dB(int64_t out, int r, Partial PB, float sB, const void* B, vo
   f.out = static_cast<bf16*>(dB);
   return f;
 }
-// Kg = B^T diag(g) B  (fp32 [r, r]; g null = all ones), r <= 64; `work` holds at least
+// Kg = B^T diag(g) B  (fp32 [r, r]; g null = all ones), r <= 128; `work` holds at least
 // gram_work_floats(r) floats of chunk partials
 size_t gram_work_floats(int r);
 template <typename T>

@@ -253,6 +253,27 @@ static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
 
 cudaError_t rowproj(const RowProjDesc& d, cudaStream_t st) {
   if (d.rows <= 0) return cudaSuccess;
+  if (d.R > 64) {   // columns in chunks of 64: one pass over S per chunk
+    if (d.R > 512 || d.R % 8) return cudaErrorInvalidValue;
+    const int64_t ldo = d.ldo > 0 ? d.ldo : d.R;
+    for (int c0 = 0; c0 < d.R; c0 += 64) {
+      RowProjDesc c = d;
+      c.R = d.R - c0 < 64 ? d.R - c0 : 64;
+      c.U = d.u_kr ? d.U + c0 : d.U + (int64_t)c0 * d.ldu;
+      c.out_a = d.out_a ? d.out_a + c0 : nullptr;
+      c.out_b = d.out_b ? d.out_b + c0 : nullptr;
+      c.out_f = d.out_f ? d.out_f + c0 : nullptr;
+      c.ldo = ldo;
+      c.split_col = d.split_col >= (1 << 29) ? d.split_col : d.split_col - c0;
+      if (c0 > 0) {   // the scaled copy of S comes with the first chunk
+        c.s_scale = nullptr;
+        c.s_out = nullptr;
+      }
+      const cudaError_t e = rowproj(c, st);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
 #define RP_CASE(RR)                                                                   \
   case RR:                                                                            \
     return d.u_kr ? rowproj_launch<RR, true>(d, st) : rowproj_launch<RR, false>(d, st);
@@ -404,14 +425,15 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
 
   // ------------------------------------------------------------------ partials of this split
   const int g = lane >> 2, t = lane & 3;
-  float* part = d.part + ((int64_t)split * d.K) * R;
+  const int64_t ldp = d.ldp > 0 ? d.ldp : R;
+  float* part = d.part + ((int64_t)split * d.K) * ldp + d.j0;
 #pragma unroll
   for (int nt = 0; nt < R / 8; ++nt)
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
       const int64_t k = k0 + warp * 16 + g + hr * 8;
       if (k < d.K)
-        *reinterpret_cast<float2*>(part + k * R + nt * 8 + 2 * t) = make_float2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+        *reinterpret_cast<float2*>(part + k * ldp + nt * 8 + 2 * t) = make_float2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
     }
   if (SUMS) {
     // the two row phases of each column meet in shared memory; stage 0 is free once all four
@@ -491,6 +513,24 @@ static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
 
 cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st) {
   if (d.K <= 0) return cudaSuccess;
+  if (d.R > 64) {   // columns of T in chunks of 64: one pass over S per chunk
+    if (d.R > 512 || d.R % 8) return cudaErrorInvalidValue;
+    for (int c0 = 0; c0 < d.R; c0 += 64) {
+      ColReduceDesc c = d;
+      c.R = d.R - c0 < 64 ? d.R - c0 : 64;
+      c.T = d.T + c0;
+      c.ldp = d.ldp > 0 ? d.ldp : d.R;
+      c.j0 = d.j0 + c0;
+      if (c0 > 0) {   // the column sums come with the first chunk
+        c.Y = nullptr;
+        c.colsum = nullptr;
+        c.coldot = nullptr;
+      }
+      const cudaError_t e = colreduce(c, st);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   const bool has_y = d.Y != nullptr;
   const bool sums = d.colsum != nullptr || d.coldot != nullptr;
 #define CR_CASE(RR)                                                          \

@@ -88,18 +88,20 @@ cudaError_t gram_rows(const T* A, int r, int64_t cols, float* K, cudaStream_t st
 // memory and accumulates its share of every entry (i, j); pass 2 sums the chunk partials in a
 // fixed order (deterministic, no atomics).
 constexpr int kGramChunks = 64;
+constexpr int kGramMaxR = 128;
 template <typename T>
 __global__ void __launch_bounds__(256) gram_partial_kernel(const T* B, int64_t out, int r, const float* g,
                                                            int64_t rows_per, float* part) {
-  __shared__ float tile[32][65];
+  constexpr int NQ = kGramMaxR * kGramMaxR / 256;   // entries (i, j) per thread
+  __shared__ float tile[32][kGramMaxR + 1];
   __shared__ float gw[32];
   const int c = blockIdx.x;
   const int64_t o0 = (int64_t)c * rows_per;
   const int64_t o1 = min(out, o0 + rows_per);
   const int rr2 = r * r;
-  float acc[16];
+  float acc[NQ];
 #pragma unroll
-  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+  for (int q = 0; q < NQ; ++q) acc[q] = 0.f;
   for (int64_t ob = o0; ob < o1; ob += 32) {
     __syncthreads();
     for (int e = threadIdx.x; e < 32 * r; e += 256) {
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(256) gram_partial_kernel(const T* B, int64_t o
     }
     __syncthreads();
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
+    for (int q = 0; q < NQ; ++q) {
       const int e = threadIdx.x + 256 * q;
       if (e < rr2) {
         const int i = e / r, j = e - (e / r) * r;
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(256) gram_partial_kernel(const T* B, int64_t o
     }
   }
 #pragma unroll
-  for (int q = 0; q < 16; ++q) {
+  for (int q = 0; q < NQ; ++q) {
     const int e = threadIdx.x + 256 * q;
     if (e < rr2) part[(int64_t)c * rr2 + e] = acc[q];
   }
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(256) gram_partial_kernel(const T* B, int64_t o
 size_t gram_work_floats(int r) { return (size_t)kGramChunks * r * r; }
 template <typename T>
 cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float* Kg, float* work, cudaStream_t st) {
-  if (r <= 0 || r > 64 || out <= 0) return cudaErrorInvalidValue;
+  if (r <= 0 || r > kGramMaxR || out <= 0) return cudaErrorInvalidValue;
   int nch = (int)((out + 31) / 32);
   if (nch > kGramChunks) nch = kGramChunks;
   const int64_t rows_per = (out + nch - 1) / nch;
@@ -144,7 +146,9 @@ cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float*
 }
 
 // ------------------------------------------------------------------ closed-form DoRA norm, one warp per row
-// Lane j holds B[o, j] and B[o, j + 32]; (B Kr)[o, j] is formed with the row broadcast lane by lane.
+// Lane j holds B[o, j + 32 h] (h < 4, r <= 128); (B Kr)[o, j] is formed with the row broadcast
+// lane by lane; Kr (r x r) sits in shared memory.
+constexpr int kNormMaxR = 128;
 template <typename T>
 __global__ void dora_norm_kernel(int64_t out, int r, const float* r0, const float* V, const T* B, const float* Kr,
                                  const T* m, float s, float eps, float* n_out, float* c) {
@@ -154,17 +158,23 @@ __global__ void dora_norm_kernel(int64_t out, int r, const float* r0, const floa
   const int lane = threadIdx.x & 31;
   const int64_t o = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (o >= out) return;
-  const bool h0 = lane < r, h1 = lane + 32 < r;
-  const float b0 = h0 ? ldf(B, o * r + lane) : 0.f;
-  const float b1 = h1 ? ldf(B, o * r + lane + 32) : 0.f;
-  float t1 = (h0 ? V[o * r + lane] * b0 : 0.f) + (h1 ? V[o * r + lane + 32] * b1 : 0.f);
-  float k0 = 0.f, k1 = 0.f;
-  for (int l = 0; l < r; ++l) {
-    const float bl = __shfl_sync(0xffffffffu, l < 32 ? b0 : b1, l & 31);
-    if (h0) k0 = fmaf(bl, sKr[l * r + lane], k0);
-    if (h1) k1 = fmaf(bl, sKr[l * r + lane + 32], k1);
+  float b[4], t1 = 0.f;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const int j = lane + 32 * h;
+    b[h] = j < r ? ldf(B, o * r + j) : 0.f;
+    if (j < r) t1 = fmaf(V[o * r + j], b[h], t1);
   }
-  float t2 = k0 * b0 + k1 * b1;
+  float k[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int l = 0; l < r; ++l) {
+    const float bl = __shfl_sync(0xffffffffu, b[l >> 5], l & 31);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      if (lane + 32 * h < r) k[h] = fmaf(bl, sKr[l * r + lane + 32 * h], k[h]);
+  }
+  float t2 = 0.f;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) t2 = fmaf(k[h], b[h], t2);
   t1 = warp_sum(t1);
   t2 = warp_sum(t2);
   if (lane == 0) {
@@ -174,11 +184,19 @@ __global__ void dora_norm_kernel(int64_t out, int r, const float* r0, const floa
     if (c) c[o] = ldf(m, o) / n;
   }
 }
+// dynamic shared memory for an r x r fp32 matrix (64 KB at r = 128: above the default limit)
+template <typename K>
+static cudaError_t allow_rr_smem(K kern) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)(kNormMaxR * kNormMaxR * sizeof(float)));
+}
 template <typename T>
 cudaError_t dora_norm(int64_t out, int r, const float* r0, const float* V, const T* B, const float* Kr, const T* m,
                       float s, float eps, float* n_out, float* c, cudaStream_t st) {
   if (out <= 0) return cudaSuccess;
-  if (r > 64) return cudaErrorInvalidValue;
+  if (r > kNormMaxR) return cudaErrorInvalidValue;
+  const cudaError_t ea = allow_rr_smem(dora_norm_kernel<T>);
+  if (ea != cudaSuccess) return ea;
   dora_norm_kernel<T><<<(unsigned)((out + 7) / 8), 256, r * r * sizeof(float), st>>>(out, r, r0, V, B, Kr, m, s, eps,
                                                                                     n_out, c);
   count_launch();
@@ -475,7 +493,7 @@ cudaError_t colnorm2_bf16(const bf16* W, int64_t rows, int64_t cols, float* c0, 
   return cudaGetLastError();
 }
 
-// closed-form column norm, one warp per input column k (lane j holds A[j, k] and A[j + 32, k]):
+// closed-form column norm, one warp per input column k (lane j holds A[j + 32 h, k], h < 4):
 //   q = c0[k] + 2s sum_j A[j,k] U[k,j] + s^2 sum_j A[j,k] (Kb A)[j,k],  n = max(sqrt(max(q, 0)), eps),
 //   c = m / n, and (optionally) A_c[:, k] = bf16(A[:, k] c[k]).
 __global__ void dora_colnorm_kernel(int64_t in, int r, const float* c0, const float* U, const bf16* A,
@@ -487,17 +505,23 @@ __global__ void dora_colnorm_kernel(int64_t in, int r, const float* c0, const fl
   const int lane = threadIdx.x & 31;
   const int64_t k = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (k >= in) return;
-  const bool h0 = lane < r, h1 = lane + 32 < r;
-  const float a0 = h0 ? __bfloat162float(A[(int64_t)lane * in + k]) : 0.f;
-  const float a1 = h1 ? __bfloat162float(A[(int64_t)(lane + 32) * in + k]) : 0.f;
-  float t1 = (h0 ? a0 * U[k * r + lane] : 0.f) + (h1 ? a1 * U[k * r + lane + 32] : 0.f);
-  float k0 = 0.f, k1 = 0.f;   // (Kb A)[j, k] for j = lane, lane + 32 (Kb symmetric)
-  for (int l = 0; l < r; ++l) {
-    const float al = __shfl_sync(0xffffffffu, l < 32 ? a0 : a1, l & 31);
-    if (h0) k0 = fmaf(sK[l * r + lane], al, k0);
-    if (h1) k1 = fmaf(sK[l * r + lane + 32], al, k1);
+  float a[4], t1 = 0.f;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const int j = lane + 32 * h;
+    a[h] = j < r ? __bfloat162float(A[(int64_t)j * in + k]) : 0.f;
+    if (j < r) t1 = fmaf(a[h], U[k * r + j], t1);
   }
-  float t2 = a0 * k0 + a1 * k1;
+  float kk[4] = {0.f, 0.f, 0.f, 0.f};   // (Kb A)[j, k] for j = lane + 32 h (Kb symmetric)
+  for (int l = 0; l < r; ++l) {
+    const float al = __shfl_sync(0xffffffffu, a[l >> 5], l & 31);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      if (lane + 32 * h < r) kk[h] = fmaf(sK[l * r + lane + 32 * h], al, kk[h]);
+  }
+  float t2 = 0.f;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) t2 = fmaf(a[h], kk[h], t2);
   t1 = warp_sum(t1);
   t2 = warp_sum(t2);
   const float q = c0[k] + 2.f * s * t1 + s * s * t2;
@@ -508,14 +532,17 @@ __global__ void dora_colnorm_kernel(int64_t in, int r, const float* c0, const fl
     c[k] = cc;
   }
   if (A_c) {
-    if (h0) A_c[(int64_t)lane * in + k] = __float2bfloat16_rn(a0 * cc);
-    if (h1) A_c[(int64_t)(lane + 32) * in + k] = __float2bfloat16_rn(a1 * cc);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      if (lane + 32 * h < r) A_c[(int64_t)(lane + 32 * h) * in + k] = __float2bfloat16_rn(a[h] * cc);
   }
 }
 cudaError_t dora_colnorm(int64_t in, int r, const float* c0, const float* U, const bf16* A, const float* Kb,
                          const bf16* m, float s, float eps, float* n_out, float* c, bf16* A_c, cudaStream_t st) {
   if (in <= 0) return cudaSuccess;
-  if (r > 64) return cudaErrorInvalidValue;
+  if (r > kNormMaxR) return cudaErrorInvalidValue;
+  const cudaError_t ea = allow_rr_smem(dora_colnorm_kernel);
+  if (ea != cudaSuccess) return ea;
   dora_colnorm_kernel<<<(unsigned)((in + 7) / 8), 256, r * r * sizeof(float), st>>>(in, r, c0, U, A, Kb, m, s, eps,
                                                                                     n_out, c, A_c);
   count_launch();

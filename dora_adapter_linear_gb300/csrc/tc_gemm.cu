@@ -1192,7 +1192,8 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
     if (d.b1_mn) ok = ok && make_map(&p.tmB1, d.B1, d.N, d.K1, d.ldb1, 64);
     else {
       ok = ok && make_map(&p.tmB1, d.B1, d.K1_b, d.N, d.ldb1, bnb);
-      if (stacked && d.mode != TC_W8A8) ok = ok && make_map(&p.tmB1b, d.B1b, d.K1_b, d.N, d.ldb1, bnb);
+      if (stacked && d.mode != TC_W8A8)
+        ok = ok && make_map(&p.tmB1b, d.B1b, d.K1_bb > 0 ? d.K1_bb : d.K1_b, d.N, d.ldb1b > 0 ? d.ldb1b : d.ldb1, bnb);
     }
   }
   int nouts = d.mode == TC_SWIGLU_FWD ? 3 : (d.mode == TC_SWIGLU_BWD ? 2 : 1);

@@ -55,20 +55,28 @@ def _check_like(name, t, shape, X):
 
 
 def _check_mlp(X, g, u, d, saved=None, dY=None):
+    """Each projection has its own rank: A [r, n_in], B [n_out, r] with r = A.shape[0]."""
     if X.dim() != 2:
         raise ValueError("X must be 2-D")
     M, H = X.shape
-    I, r = g["W"].shape[0], g["A"].shape[0]
+    I = g["W"].shape[0]
     for nm, p, n_out, n_in in (("gate", g, I, H), ("up", u, I, H), ("down", d, H, I)):
+        r = p["A"].shape[0]
         _check_like(nm + " W", p["W"], (n_out, n_in), X)
         _check_like(nm + " A", p["A"], (r, n_in), X)
         _check_like(nm + " B", p["B"], (n_out, r), X)
+    rg, ru, rd = g["A"].shape[0], u["A"].shape[0], d["A"].shape[0]
     if saved is not None:
         for k in ("e", "u", "h"):
             _check_like(k, saved[k], (M, I), X)
-        _check_like("Zgu", saved["Zgu"], (M, 2 * r), X)
-        _check_like("Zd", saved["Zd"], (M, r), X)
+        _check_like("Zgu", saved["Zgu"], (M, rg + ru), X)
+        _check_like("Zd", saved["Zd"], (M, rd), X)
     _check_like("dY", dY, (M, H), X)
+
+
+def _mlp_shape(X, g, u, d, act):
+    M, H = X.shape
+    return L.mlp_shape(M, H, g["W"].shape[0], g["A"].shape[0], u["A"].shape[0], d["A"].shape[0], act=act)
 
 
 def _check_qkv(X, W0, leaves, bias=None, Z=None, dY=None):
@@ -247,14 +255,14 @@ def lora_mlp_swiglu_fwd(X, g, u, d, act=0):
     holds e, u, h, Zgu, Zd."""
     _check_mlp(X, g, u, d)
     M, H = X.shape
-    I, r = g["W"].shape[0], g["A"].shape[0]
-    sh = L.mlp_shape(M, H, I, r, act=act)
+    I = g["W"].shape[0]
+    sh = _mlp_shape(X, g, u, d, act)
     dev = X.device
     e_ = torch.empty(M, I, dtype=X.dtype, device=dev)
     u_ = torch.empty_like(e_)
     h_ = torch.empty_like(e_)
-    Zgu = torch.empty(M, 2 * r, dtype=X.dtype, device=dev)
-    Zd = torch.empty(M, r, dtype=X.dtype, device=dev)
+    Zgu = torch.empty(M, sh.r_g + sh.r_u, dtype=X.dtype, device=dev)
+    Zd = torch.empty(M, sh.r_d, dtype=X.dtype, device=dev)
     Y = torch.empty(M, H, dtype=X.dtype, device=dev)
     ws = workspace(L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, sh), dev)
     pg, pu, pd = (L.proj(p["W"], p["A"], p["B"], p["s"]) for p in (g, u, d))
@@ -264,9 +272,7 @@ def lora_mlp_swiglu_fwd(X, g, u, d, act=0):
 
 def lora_mlp_swiglu_bwd(X, g, u, d, saved, dY, need_dx=True, act=0):
     _check_mlp(X, g, u, d, saved, dY)
-    M, H = X.shape
-    I, r = g["W"].shape[0], g["A"].shape[0]
-    sh = L.mlp_shape(M, H, I, r, act=act)
+    sh = _mlp_shape(X, g, u, d, act)
     dX = torch.empty_like(X) if need_dx else None
     grads = {k: torch.empty_like(v) for k, v in
              (("dAg", g["A"]), ("dBg", g["B"]), ("dAu", u["A"]), ("dBu", u["B"]), ("dAd", d["A"]), ("dBd", d["B"]))}

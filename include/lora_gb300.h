@@ -17,7 +17,7 @@
  *    dtype LORA_F32: fp32 storage, fp32 FMA accumulation (no TF32), fp32 outputs.
  *  - s is the complete scale strength * alpha / r (the caller folds strength in).
  *  - Every pointer must be 16-byte aligned; d_in, d_out must be multiples of 8,
- *    r a multiple of 8 with 8 <= r <= 64 (LORA_BF16) or 1 <= r <= 64 (LORA_F32).
+ *    r a multiple of 8 with 8 <= r <= 128 (LORA_BF16) or 1 <= r <= 128 (LORA_F32).
  *    M >= 0 (M == 0 is a no-op).  Violations return an error before anything is
  *    launched and leave every output untouched.
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
@@ -48,7 +48,7 @@ extern "C" {
 typedef enum {
     LORA_OK = 0,
     LORA_ERR_INVALID_ARG = 1,     /* null required pointer, bad shape, bad dtype, non-finite s */
-    LORA_ERR_UNSUPPORTED = 2,     /* valid request this library does not implement (e.g. r > 64) */
+    LORA_ERR_UNSUPPORTED = 2,     /* valid request this library does not implement (e.g. r > 128) */
     LORA_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned (ws: 256-byte) */
     LORA_ERR_WORKSPACE = 4,       /* ws is NULL or ws_bytes is below the required size */
     LORA_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed (launch, tensor map) */
@@ -78,9 +78,11 @@ typedef enum {
     LORA_ACT_GEGLU = 1            /* gelu(e) = e * Phi(e), Phi the normal CDF (erf form) */
 } lora_act;
 
-/* Gated MLP: X [M, H]; gate/up project H -> I, down projects I -> H; one rank r. */
+/* Gated MLP: X [M, H]; gate/up project H -> I, down projects I -> H; each projection has its
+ * own rank (r_g, r_u, r_d: multiples of 8 in 8..128). */
 typedef struct {
-    int64_t M, H, I, r;
+    int64_t M, H, I;
+    int64_t r_g, r_u, r_d;
     int32_t dtype;                /* LORA_BF16 only */
     int32_t act;                  /* lora_act */
 } lora_mlp_shape;
@@ -95,8 +97,9 @@ typedef struct {
 
 /* Fused projection whose N = n[0] + .. + n[L-1] output columns split into L leaves (the
  * query / key / value heads of an attention block), each leaf with its own rank-r adapter.
- * L in 1..3; r a multiple of 8, at most 64 (when L * r > 64 the leaves are processed in groups of
- * at most 64 adapter columns, one extra pass over X per extra group); every n[l] a positive multiple of 8
+ * L in 1..3; r a multiple of 8, at most 128 (the rank-r passes take at most 64 adapter columns at
+ * a time: when L * r > 64 the leaves go in groups of at most 64 columns, or one leaf of more than
+ * 64 columns, one extra pass over X per extra group or chunk); every n[l] a positive multiple of 8
  * (entries past L ignored); d_in a multiple of 8. */
 typedef struct {
     int64_t M, d_in;
@@ -295,9 +298,10 @@ lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, c
  * Y = h Wd^T + sd (h Ad^T) Bd^T,  act = silu (sh->act = LORA_ACT_SWIGLU) or gelu (LORA_ACT_GEGLU).
  * "How Unsloth's FastLoRA Kernel Differs ...", Fused Forward Pass Architecture (LoRA_MLP)
  * and Activation Function Fusion (SwiGLU and GeGLU computed with the LoRA outputs).
- *   gate, up: W [I, H], A [r, H], B [I, r];  down: W [H, I], A [r, I], B [H, r].
+ *   gate: W [I, H], A [r_g, H], B [I, r_g];  up: W [I, H], A [r_u, H], B [I, r_u];
+ *   down: W [H, I], A [r_d, I], B [H, r_d].
  *   Y [M, H]; e_save, u_save, h_save [M, I] (required: the backward reads them);
- *   Zgu_save [M, 2r] = [X Ag^T | X Au^T] and Zd_save [M, r] = h Ad^T (required).
+ *   Zgu_save [M, r_g + r_u] = [X Ag^T | X Au^T] and Zd_save [M, r_d] = h Ad^T (required).
  */
 lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const lora_proj* gate,
                                 const lora_proj* up, const lora_proj* down, void* Y,
@@ -309,7 +313,8 @@ lora_status lora_mlp_swiglu_fwd(const lora_mlp_shape* sh, const void* X, const l
  *   dX = de Wg + du Wu + sg (de Bg) Ag + su (du Bu) Au,
  *   dA* = s* (d* B*)^T (input),  dB* = s* (d*)^T Z*.
  * "How Unsloth's FastLoRA Kernel Differs ...", Custom Backward Pass Implementation.
- *   dX [M, H] or NULL; dAg, dAu [r, H]; dBg, dBu [I, r]; dAd [r, I]; dBd [H, r].
+ *   dX [M, H] or NULL; dAg [r_g, H], dBg [I, r_g]; dAu [r_u, H], dBu [I, r_u];
+ *   dAd [r_d, I], dBd [H, r_d].
  */
 lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const lora_proj* gate,
                                 const lora_proj* up, const lora_proj* down,
@@ -354,14 +359,14 @@ lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0
  * (axis-wise quantisation for the 8-bit matmul; the autograd Function owns the
  * down-projection).
  *   X [rows, cols] bf16; Xq [rows, cols] int8; sx [rows] fp32;
- *   A [r, cols] bf16 and Z [rows, r] bf16, both NULL or both non-NULL (then r in 8..64).
+ *   A [r, cols] bf16 and Z [rows, r] bf16, both NULL or both non-NULL (then r in 8..128).
  */
 lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t* Xq, float* sx,
                                const void* A, int64_t r, void* Z, void* stream);
 
 /* Bytes of workspace w8a8_lora_fwd needs: the error word, the int8 codes re-laid out as bf16
  * tensor-core operands (X: M x d_in; W split into two d_out x d_in halves) and the rank-r
- * operands divided by the dequant scales (M x 64 and d_out x 64 bf16).  0 on bad input. */
+ * operands divided by the dequant scales (M x 128 and d_out x 128 bf16).  0 on bad input. */
 size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out);
 
 /* Y = float(acc) * sx[i] * sw[o] + s * (Z B^T)[i, o] (+ bias), acc = Xq Wq^T exact in int32.
@@ -370,7 +375,8 @@ size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out);
  * int32 (M, d_out) materialisation) and commit unifying the five entry points
  * (mm_8bit(a, b, out_dtype, scale_m, scale_n, lora_xd, lora_up)).
  *   Xq [M, d_in] int8, sx [M] fp32, Wq [d_out, d_in] int8, sw [d_out] fp32,
- *   Z [M, r] bf16 ("lora_xd") and B [d_out, r] bf16 ("lora_up"): both NULL (no LoRA) or both set,
+ *   Z [M, r] bf16 ("lora_xd") and B [d_out, r] bf16 ("lora_up"): both NULL (no LoRA) or both set
+ *   (r a multiple of 8 in 8..128),
  *   bias [d_out] bf16 or NULL, Y [M, d_out] bf16 (or NULL when only acc_out is wanted),
  *   acc_out [M, d_out] int32 or NULL: the raw-product epilogue.  d_in multiple of 32.
  *   ws: workspace of at least w8a8_workspace_bytes(M, d_in, d_out) bytes (256-byte aligned).

@@ -38,21 +38,32 @@ def test_status_strings(lib):
     assert L.lora_status_string(0) == "ok"
     assert "workspace" in L.lora_status_string(4)
     assert L.lora_status_string(99) == "unknown status"
-    assert L.lora_abi_version() == 6
+    assert L.lora_abi_version() == 7
 
 
 def test_workspace_bytes_rejects_bad_shapes(lib):
     assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 8, L.LORA_F32)) > 0
     assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 250, 256, 8, L.LORA_F32)) == 0   # in % 8
-    assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 65, L.LORA_BF16)) == 0  # r > 64
+    for r in range(8, 129, 8):                                                                   # r 8..128
+        for op in (L.OP_LINEAR_FWD, L.OP_LINEAR_BWD, L.OP_DORA_FWD, L.OP_DORA_BWD, L.OP_DORA_COLS_BWD):
+            assert L.lora_workspace_bytes(op, L.shape(64, 256, 256, r, L.LORA_BF16)) > 0, (op, r)
+    assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 136, L.LORA_BF16)) == 0  # r > 128
+    assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 128, L.LORA_F32)) > 0
+    assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 129, L.LORA_F32)) == 0
     assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 12, L.LORA_BF16)) == 0  # r % 8 (bf16)
     assert L.lora_workspace_bytes(L.OP_LINEAR_FWD, L.shape(64, 256, 256, 8, 7)) == 0             # dtype
     assert L.lora_workspace_bytes(99, L.shape(64, 256, 256, 8, L.LORA_F32)) == 0
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16)) > 0
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 40)) > 0           # r 33..64
-    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 72)) == 0          # r > 64
-    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, L.LORA_F32)) == 0
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_BWD, L.mlp_shape(64, 128, 256, 128, 72, 96)) > 0   # per projection
+    small = L.lora_mlp_workspace_bytes(L.OP_MLP_BWD, L.mlp_shape(64, 128, 256, 8, 8, 8))
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_BWD, L.mlp_shape(64, 128, 256, 8, 8, 128)) > small
+    for bad_ranks in ((136, 16, 16), (16, 136, 16), (16, 16, 136), (16, 12, 16), (16, 16, 0)):
+        assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, *bad_ranks)) == 0, bad_ranks
+    assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, dtype=L.LORA_F32)) == 0
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, act=L.LORA_ACT_GEGLU)) > 0
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 128, [64, 32, 32], 128)) > 0
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 128, [64, 32, 32], 136)) == 0
     assert L.lora_mlp_workspace_bytes(L.OP_MLP_FWD, L.mlp_shape(64, 128, 256, 16, act=2)) == 0         # unknown act
 
 
@@ -133,7 +144,8 @@ def test_qkv_validation(lib):
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, ok) > 0
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_BWD, ok) > 0
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 64, 64], 32)) > 0   # L r = 96
-    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 64, 64], 72)) == 0  # r > 64
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_BWD, L.qkv_shape(64, 256, [256, 64, 64], 72)) > 0   # r 72..128
+    assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 64, 64], 136)) == 0  # r > 128
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 64, 64], 12)) == 0  # r % 8
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 60], 16)) == 0      # n % 8
     assert L.lora_qkv_workspace_bytes(L.OP_QKV_FWD, L.qkv_shape(64, 256, [256, 0], 16)) == 0       # empty leaf

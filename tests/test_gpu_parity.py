@@ -65,7 +65,7 @@ def test_base_gemm_mnmajor_strength0(ops):
     assert not dA.any() and not dB.any()
 
 
-@pytest.mark.parametrize("r", [8, 16, 32, 64])
+@pytest.mark.parametrize("r", [8, 16, 32, 64, 96, 128])
 @pytest.mark.parametrize("bias", [False, True])
 def test_lora_fwd_bf16(ops, r, bias):
     case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=r, bias=bias)
@@ -75,7 +75,7 @@ def test_lora_fwd_bf16(ops, r, bias):
     assert_close(Z, X @ A.T, "bf16", "Z")
 
 
-@pytest.mark.parametrize("r", [8, 16, 32, 64])
+@pytest.mark.parametrize("r", [8, 16, 32, 64, 96, 128])
 def test_lora_bwd_bf16(ops, r):
     case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=r)
     _, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s)
@@ -181,9 +181,9 @@ def test_lora_tiny_f32(ops):
 
 
 # ---------------------------------------------------------------------------- DoRA
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_dora_fwd_bwd(ops, dtype):
-    case, t, g = lin_inputs("dora_4096x11008_bf16", M=300, d_in=328, d_out=520, r=32, dtype=dtype)
+@pytest.mark.parametrize("dtype,r", [("bf16", 32), ("f32", 32), ("bf16", 96), ("bf16", 128), ("f32", 128)])
+def test_dora_fwd_bwd(ops, dtype, r):
+    case, t, g = lin_inputs("dora_4096x11008_bf16", M=300, d_in=328, d_out=520, r=r, dtype=dtype)
     r0 = ops.dora_rownorm2(g["W0"])
     np.testing.assert_allclose(to64(r0), O.dora_rownorm2(f64(t["W0"])), rtol=1e-5)
     Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps, g["bias"])
@@ -267,7 +267,7 @@ def test_dora_zero_row_at_default_eps(ops):
 
 
 # ---------------------------------------------------------------------------- DoRA (cols)
-@pytest.mark.parametrize("r", [32, 16])
+@pytest.mark.parametrize("r", [32, 16, 128])
 def test_dora_cols_fwd_bwd(ops, r):
     case, t, g = lin_inputs("dora_cols_4096x11008_bf16", M=300, d_in=328, d_out=520, r=r)
     c0 = ops.dora_colnorm2(g["W0"])
@@ -331,13 +331,15 @@ def mlp_inputs(**kw):
     case = D.scaled(D.WORKLOADS["mlp_swiglu_4096x14336_bf16"], **kw)
     t = D.make_mlp(case)
     g = {k: gpu(v) for k, v in t.items()}
-    P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
+    P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.scales[p]} for p in "gud"}
     return case, t, g, P
 
 
 def _mlp_args64(t, s):
-    return (f64(t["X"]), f64(t["Wg"]), f64(t["Ag"]), f64(t["Bg"]), s, f64(t["Wu"]), f64(t["Au"]), f64(t["Bu"]), s,
-            f64(t["Wd"]), f64(t["Ad"]), f64(t["Bd"]), s)
+    """Oracle arguments; s is one scale for all projections or a dict of per-projection scales."""
+    sc = s if isinstance(s, dict) else {p: s for p in "gud"}
+    return (f64(t["X"]), f64(t["Wg"]), f64(t["Ag"]), f64(t["Bg"]), sc["g"], f64(t["Wu"]), f64(t["Au"]), f64(t["Bu"]),
+            sc["u"], f64(t["Wd"]), f64(t["Ad"]), f64(t["Bd"]), sc["d"])
 
 
 ACTS = {"swiglu": 0, "geglu": 1}
@@ -373,7 +375,8 @@ def qkv_inputs(**kw):
 
 @pytest.mark.parametrize("n,r,bias", [((256, 72, 72), 16, True), ((256, 72, 72), 8, False),
                                       ((136, 264), 32, False), ((200,), 64, True),
-                                      ((256, 72, 72), 32, True), ((128, 64, 64), 64, False)])
+                                      ((256, 72, 72), 32, True), ((128, 64, 64), 64, False),
+                                      ((256, 72, 72), 96, True), ((128, 64, 64), 128, False)])
 def test_qkv_fwd_bwd(ops, n, r, bias):
     case, t, g, lg_, l64 = qkv_inputs(M=300, d_in=200, n=n, r=r, bias=bias)
     Y, Z = ops.lora_qkv_fwd(g["X"], g["W0"], lg_, g["bias"])
@@ -419,12 +422,15 @@ def test_qkv_m_zero_is_noop(ops):
     assert all(not a.any() for a in dA + dB) and not db.any()
 
 
-@pytest.mark.parametrize("r", [48, 64])
-def test_mlp_large_rank(ops, r):
-    """Ranks above 32: one rank-r pass per gate/up half and a tail of several K-steps."""
-    case, t, g, P = mlp_inputs(M=260, H=136, I=200, r=r, alpha=2.0 * r)
+@pytest.mark.parametrize("ranks", [(48, 48, 48), (64, 64, 64), (128, 128, 128), (16, 48, 128), (128, 8, 40)])
+def test_mlp_large_rank(ops, ranks):
+    """Large and unequal ranks per projection: the gate/up down-projection [Zg | Zu] spans several
+    64-column passes, the stacked tail several K-steps with the up half shifted by r_g."""
+    rg, ru, rd = ranks
+    case, t, g, P = mlp_inputs(M=260, H=136, I=200, r=rg, r_u=ru, r_d=rd, alpha=32.0)
     Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
-    args = _mlp_args64(t, case.s)
+    assert saved["Zgu"].shape == (260, rg + ru) and saved["Zd"].shape == (260, rd)
+    args = _mlp_args64(t, case.scales)
     ry, re, ru, rh = O.mlp_swiglu_fwd(*args)
     for got, ref, nm in ((saved["e"], re, "e"), (saved["u"], ru, "u"), (saved["h"], rh, "h"), (Y, ry, "y")):
         assert_close(got, ref, "bf16", nm)
@@ -513,6 +519,34 @@ def test_w8a8_deep_k_uses_integer_path(ops):
     _, acc = ops.w8a8_lora_fwd(gpu(torch.from_numpy(Xq)), None, gpu(torch.from_numpy(Wq)), None, None, None, 0.0,
                                want_acc=True, want_y=False)
     np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), O.int8_accumulate(Xq, Wq))
+
+
+@pytest.mark.parametrize("r", [96, 128])
+def test_w8a8_large_rank(ops, r, monkeypatch):
+    """Ranks above 64: the quantiser's down-projection in two passes, both epilogues' rank-r
+    tail over several K-steps, and the backward through the int8 base."""
+    case, t, Wq, sw, Xq, sx = w8_inputs(M=300, d_in=352, d_out=264, r=r, bias=True)
+    X = gpu(t["X"])
+    gXq, gsx, gZ = ops.w8a8_quantize_rows(X, gpu(t["A"]))
+    np.testing.assert_array_equal(gXq.cpu().numpy(), Xq)
+    Z = (t["X"].double() @ t["A"].double().T).to(torch.bfloat16)   # the oracle's Z, shared bytes
+    assert_close(gZ, f64(Z), "bf16", "Z")
+    args = (gpu(torch.from_numpy(Xq)), gpu(torch.from_numpy(sx)), gpu(torch.from_numpy(Wq)),
+            gpu(torch.from_numpy(sw)), gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]))
+    ry, racc = O.w8a8_lora_fwd(Xq, sx, Wq, sw, f64(Z), f64(t["B"]), case.s, f64(t["bias"]))
+    Y, acc = ops.w8a8_lora_fwd(*args, want_acc=True)                # exact-integer epilogue
+    np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), racc)
+    assert_close(Y, ry, "bf16", "Y (exact epilogue)")
+    Yf, _ = ops.w8a8_lora_fwd(*args)                                # folded output-only epilogue
+    assert_close(Yf, ry, "bf16", "Y (folded epilogue)")
+    g = torch.Generator().manual_seed(79)
+    dY = torch.randn(case.M, case.d_out, generator=g).to(torch.bfloat16)
+    dX, dA, dB, _ = ops.w8a8_lora_bwd(X, gpu(torch.from_numpy(Wq)), gpu(torch.from_numpy(sw)), gpu(t["A"]),
+                                      gpu(t["B"]), gpu(Z), gpu(dY), case.s)
+    rX, rA, rB, _ = O.w8a8_lora_bwd(f64(t["X"]), Wq, sw, f64(t["A"]), f64(t["B"]), case.s, f64(dY))
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dB, rB, "bf16", "dB")
 
 
 @pytest.mark.parametrize("bias", [False, True])

@@ -60,9 +60,16 @@ def test_mlp_and_qkv_checks():
     bad = dict(P, d=dict(P["d"], A=_t(4, 32)))          # down-projection A must span I = 48
     with pytest.raises(ValueError):
         ops.lora_mlp_swiglu_fwd(X, bad["g"], bad["u"], bad["d"])
-    bad = dict(P, u=dict(P["u"], B=_t(48, 8)))           # one rank for all three projections
+    bad = dict(P, u=dict(P["u"], B=_t(48, 8)))           # up-projection B rank differs from its A
     with pytest.raises(ValueError):
         ops.lora_mlp_swiglu_fwd(X, bad["g"], bad["u"], bad["d"])
+    # each projection has its own rank: the saved Zgu is [M, r_g + r_u], Zd [M, r_d]
+    P3 = dict(P, u=dict(P["u"], A=_t(8, 32), B=_t(48, 8)), d=dict(P["d"], A=_t(16, 48), B=_t(32, 16)))
+    saved = {"e": _t(8, 48), "u": _t(8, 48), "h": _t(8, 48), "Zgu": _t(8, 4 + 8), "Zd": _t(8, 16)}
+    with pytest.raises(ValueError):   # Zgu sized for one shared rank
+        ops.lora_mlp_swiglu_bwd(X, P3["g"], P3["u"], P3["d"], dict(saved, Zgu=_t(8, 8)), _t(8, 32))
+    with pytest.raises(ValueError):   # Zd of the wrong rank
+        ops.lora_mlp_swiglu_bwd(X, P3["g"], P3["u"], P3["d"], dict(saved, Zd=_t(8, 4)), _t(8, 32))
     W0 = _t(96, 32)
     leaves = [(_t(4, 32), _t(64, 4), 1.0), (_t(4, 32), _t(16, 4), 1.0), (_t(4, 32), _t(16, 4), 1.0)]
     with pytest.raises(ValueError):                       # W0 rows must be the leaves' rows
