@@ -280,6 +280,24 @@ def timed(fn, steps, warmup, dist=None):
     return e0.elapsed_time(e1) / steps, t0, t1
 
 
+def timed_reps(fn, steps, warmup, dist=None, min_s=1.0, max_reps=200):
+    """Timed regions of exactly `steps` steps each (barrier and synchronize on both sides), repeated
+    until they cover at least min_s seconds: (median ms per step, per-region ms, t0, t1)."""
+    per, t_first, t_last = [], None, None
+    ms, t0, t1 = timed(fn, steps, warmup, dist)
+    per.append(ms)
+    t_first, t_last = t0, t1
+    if dist is not None:   # every rank runs the same number of regions (each one ends in a barrier)
+        import torch
+        ms = reduce_max([ms], dist, torch.device("cuda", torch.cuda.current_device()))[0]
+    reps = max(1, min(max_reps, int(min_s / max(1e-9, ms * steps * 1e-3))))
+    for _ in range(reps - 1):
+        ms, _, t1 = timed(fn, steps, 0, dist)
+        per.append(ms)
+        t_last = t1
+    return statistics.median(per), per, t_first, t_last
+
+
 # DRAM bytes (read + write) per GEMM launch from ncu captures, keyed by workload; a value is
 # dropped (None) whenever the kernel changes and is re-measured before it is put back.
 # lora_4096_bf16: dram__bytes_read.sum + dram__bytes_write.sum of the forward (CTA pair) and dX
@@ -323,6 +341,19 @@ def gemm_roofline(L, peaks, ms_step, steps_recorded, sustained, workload):
             "flops_per_launch": fl / n, "traffic": GEMM_TRAFFIC.get(workload)}
 
 
+def rank_pass_roofline(L, peaks):
+    """HBM roofline of the rank-r passes recorded in the events pass (their algorithmic bytes over
+    their event time)."""
+    ms, n, by = L.lora_prof_rank(reset=True)
+    if n == 0 or ms <= 0:
+        return None
+    ach = by / (ms * 1e-3) / 1e9
+    return {"kernels": "rowproj_kernel / colreduce_kernel (rank-r passes)", "bound": "hbm",
+            "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / peaks["hbm_gbs"], 4), "launches": n, "avg_launch_ms": round(ms / n, 4),
+            "bytes_per_launch": by / n}
+
+
 def headline(args, L, ops, dist, world, peaks):
     import torch
 
@@ -333,17 +364,23 @@ def headline(args, L, ops, dist, world, peaks):
     X, W0, A, B, dY = (t[k].to(dev) for k in ("X", "W0", "A", "B", "dY"))
     M, d_in, d_out, r, s = case.M, case.d_in, case.d_out, case.r, case.s
     sh = L.shape(M, d_in, d_out, r, L.LORA_BF16)
-    Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=dev)
-    Z = torch.empty(M, r, dtype=torch.bfloat16, device=dev)
-    dX = torch.empty_like(X)
-    dA = torch.empty_like(A)
-    dB = torch.empty_like(B)
+    Ys = [torch.empty(M, d_out, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    Zs = [torch.empty(M, r, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    dXs = [torch.empty_like(X) for _ in range(2)]
+    dAs = [torch.empty_like(A) for _ in range(2)]
+    dBs = [torch.empty_like(B) for _ in range(2)]
     wsf = torch.zeros(L.lora_workspace_bytes(L.OP_LINEAR_FWD, sh), dtype=torch.uint8, device=dev)
     wsb = torch.zeros(L.lora_workspace_bytes(L.OP_LINEAR_BWD, sh), dtype=torch.uint8, device=dev)
 
-    def step(Xb=X, dYb=dY):
-        L.lora_linear_fwd(sh, Xb, W0, A, B, None, s, Y, Z, wsf)
-        L.lora_linear_bwd(sh, Xb, W0, A, B, Z, dYb, s, dX, dA, dB, None, wsb)
+    def fwd(Xb=X, b=0):
+        L.lora_linear_fwd(sh, Xb, W0, A, B, None, s, Ys[b], Zs[b], wsf)
+
+    def bwd(Xb=X, dYb=dY, b=0):
+        L.lora_linear_bwd(sh, Xb, W0, A, B, Zs[b], dYb, s, dXs[b], dAs[b], dBs[b], None, wsb)
+
+    def step(Xb=X, dYb=dY, b=0):
+        fwd(Xb, b)
+        bwd(Xb, dYb, b)
 
     fwd_fl, bwd_fl = lora_flops(M, d_in, d_out, r)
     clk = ClockSampler(torch.cuda.current_device())
@@ -352,59 +389,82 @@ def headline(args, L, ops, dist, world, peaks):
     nv.start()
     time.sleep(0.3)
     n0 = L.lora_launch_count()
-    ms, t0, t1 = timed(step, args.steps, args.warmup, dist)
+    ms, per, t0, t1 = timed_reps(step, args.steps, args.warmup, dist, args.min_timed_s)
     launches = L.lora_launch_count() - n0
-    # launches of the warm-up steps are in the count too: scale to the timed steps
-    gpu_launches = launches * args.steps // (args.steps + args.warmup)
+    # the count includes the warm-up steps: scale it to one timed region of exactly K steps
+    gpu_launches = round(launches * args.steps / (args.steps * len(per) + args.warmup))
     clocks = nv.summary(t0, t1) or clk.summary(t0, t1)
     if dist is None and clocks_rejected(clocks):
-        # a record the measurement rules reject: take the timed region once more (one process
+        # a record the measurement rules reject: take the timed regions once more (one process
         # only: with several ranks the decision would have to be collective)
         first = clocks
-        ms, t0, t1 = timed(step, args.steps, args.warmup, dist)
+        ms, per, t0, t1 = timed_reps(step, args.steps, args.warmup, dist, args.min_timed_s)
         clocks = dict(nv.summary(t0, t1) or clk.summary(t0, t1) or {},
                       remeasured_after=first.get("reasons") or ["SM clock below 85% of max"])
     nv.stop()
+    # each direction alone (the same calls), for the split of the step
+    ms_fwd, _, _, _ = timed_reps(fwd, args.steps, 2, dist, args.min_timed_s / 4)
+    ms_bwd, _, _, _ = timed_reps(bwd, args.steps, 2, dist, args.min_timed_s / 4)
+    # a second pass with CUDA events around every GEMM and rank-r launch (the library's tracing)
+    L.lora_prof_rank(reset=True)
     ms_ev = timed_gemm_events(L, step, args.steps)
     roof = gemm_roofline(L, peaks, ms_ev, args.steps + 1, False, HEADLINE)
+    rank_roof = rank_pass_roofline(L, peaks)
     clk.stop()
     for ws in (wsf, wsb):
         if L.lora_check_device_error(ws) != 0:
             raise RuntimeError("a kernel recorded a timed-out wait during the benchmark")
 
-    # end to end: every step copies its inputs from pinned host memory and reads the adapter
-    # gradients back; the next step's host->device copy runs on a second stream into the other
-    # half of a double buffer while the current step computes
+    # End to end through the same entry points: every step copies its inputs X and dY from pinned
+    # host memory and reads its results Y, dX, dA and dB back into pinned host memory.  Device
+    # buffers are doubled: step i+1's inputs arrive (copy stream) and step i-1's results leave
+    # (second copy stream) while step i computes.
     Xh = t["X"].pin_memory()
     dYh = t["dY"].pin_memory()
-    dAh = torch.empty_like(dA, device="cpu").pin_memory()
-    dBh = torch.empty_like(dB, device="cpu").pin_memory()
+    Yh = [torch.empty(M, d_out, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dXh = [torch.empty(M, d_in, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dAh = [torch.empty_like(A, device="cpu").pin_memory() for _ in range(2)]
+    dBh = [torch.empty_like(B, device="cpu").pin_memory() for _ in range(2)]
     Xd, dYd = [X, torch.empty_like(X)], [dY, torch.empty_like(dY)]
-    cp = torch.cuda.Stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
 
     def e2e_run(n):
         cur = torch.cuda.current_stream()
         copied = [torch.cuda.Event(), torch.cuda.Event()]
         done = [torch.cuda.Event(), torch.cuda.Event()]
-        cp.wait_stream(cur)
-        with torch.cuda.stream(cp):
+        fdone = [torch.cuda.Event(), torch.cuda.Event()]
+        out = [torch.cuda.Event(), torch.cuda.Event()]
+        cin.wait_stream(cur)
+        cout.wait_stream(cur)
+        with torch.cuda.stream(cin):
             Xd[0].copy_(Xh, non_blocking=True)
             dYd[0].copy_(dYh, non_blocking=True)
-            copied[0].record(cp)
+            copied[0].record(cin)
         for i in range(n):
             b = i & 1
             if i + 1 < n:
-                with torch.cuda.stream(cp):
+                with torch.cuda.stream(cin):
                     if i >= 1:
-                        cp.wait_event(done[1 - b])     # step i-1 used that half
+                        cin.wait_event(done[1 - b])     # step i-1 has read that half of the inputs
                     Xd[1 - b].copy_(Xh, non_blocking=True)
                     dYd[1 - b].copy_(dYh, non_blocking=True)
-                    copied[1 - b].record(cp)
+                    copied[1 - b].record(cin)
             cur.wait_event(copied[b])
-            step(Xd[b], dYd[b])
+            if i >= 2:
+                cur.wait_event(out[b])                  # step i-2's results have left these buffers
+            fwd(Xd[b], b)
+            fdone[b].record(cur)
+            bwd(Xd[b], dYd[b], b)
             done[b].record(cur)
-            dAh.copy_(dA, non_blocking=True)
-            dBh.copy_(dB, non_blocking=True)
+            with torch.cuda.stream(cout):
+                cout.wait_event(fdone[b])
+                Yh[b].copy_(Ys[b], non_blocking=True)
+                cout.wait_event(done[b])
+                dXh[b].copy_(dXs[b], non_blocking=True)
+                dAh[b].copy_(dAs[b], non_blocking=True)
+                dBh[b].copy_(dBs[b], non_blocking=True)
+                out[b].record(cout)
+        cur.wait_stream(cout)
 
     e2e_steps = max(4, min(args.steps, 50))
     e2e_run(3)
@@ -419,16 +479,55 @@ def headline(args, L, ops, dist, world, peaks):
     ms_e2e = q0.elapsed_time(q1) / e2e_steps
     if dist is not None:
         dist.barrier()
-    ms_all, ms_e2e = reduce_max([ms, ms_e2e], dist, dev)
+
+    context = same_box_context(case, X, W0, A, B, dY, dev, peaks) if dist is None or dist.get_rank() == 0 else None
+    ms_all, ms_e2e, ms_fwd, ms_bwd = reduce_max([ms, ms_e2e, ms_fwd, ms_bwd], dist, dev)
+    h2d = X.numel() * 2 + dY.numel() * 2
+    d2h = Ys[0].numel() * 2 + dXs[0].numel() * 2 + dAs[0].numel() * 2 + dBs[0].numel() * 2
     return {
         "value": job_throughput(fwd_fl + bwd_fl, world, ms_all), "ms_per_step": ms_all, "clocks": clocks,
-        "roofline": roof, "gpu_launches": gpu_launches,
+        "timed_regions": {"regions": len(per), "steps_each": args.steps,
+                          "ms_per_step_each": [round(x, 4) for x in per], "ms_per_step": "median of the regions",
+                          "seconds": round(t1 - t0, 3)},
+        "roofline": roof, "rank_passes": rank_roof, "gpu_launches": gpu_launches,
+        "fwd": {"ms": round(ms_fwd, 4), "tflops": round(fwd_fl / (ms_fwd * 1e-3) / 1e12, 1)},
+        "bwd": {"ms": round(ms_bwd, 4), "tflops": round(bwd_fl / (ms_bwd * 1e-3) / 1e12, 1)},
         "e2e": {"value": job_throughput(fwd_fl + bwd_fl, world, ms_e2e), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": X.numel() * 2 + dY.numel() * 2,
-                "d2h_bytes_per_step": dA.numel() * 2 + dB.numel() * 2, "ms_per_step": ms_e2e},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "copies": "h2d X, dY; d2h Y, dX, dA, dB (pinned host, separate copy streams, double-buffered)"},
         "tokens_per_s": M * world / (ms_all * 1e-3),
         "frac_of_bf16_peak_step": (fwd_fl + bwd_fl) / (ms_all * 1e-3) / 1e12 / peaks["bf16_tflops"],
+        "context": context,
     }
+
+
+def same_box_context(case, X, W0, A, B, dY, dev, peaks, steps=20):
+    """Context on the same GPU (not the product): the plain X W0^T product through cuBLAS
+    (torch.matmul), and the unfused bypass of eager PyTorch (F.linear plus two low-rank matmuls,
+    backward by autograd, W0 frozen) for the same forward + backward."""
+    import torch
+    M, d_in, d_out, r, s = case.M, case.d_in, case.d_out, case.r, case.s
+
+    def mm():
+        torch.matmul(X, W0.t())
+    ms_mm, _, _ = timed(mm, steps, 3)
+    Ag = A.detach().clone().requires_grad_(True)
+    Bg = B.detach().clone().requires_grad_(True)
+    Xg = X.detach().clone().requires_grad_(True)
+
+    def eager():
+        y = torch.nn.functional.linear(Xg, W0) + s * ((Xg @ Ag.t()) @ Bg.t())
+        y.backward(dY)
+        Xg.grad = None
+        Ag.grad = None
+        Bg.grad = None
+    ms_eager, _, _ = timed(eager, steps, 3)
+    fwd, bwd = lora_flops(M, d_in, d_out, r)
+    return {"cublas_matmul_x_w0t": {"ms": round(ms_mm, 4), "tflops": round(2 * M * d_in * d_out / (ms_mm * 1e-3) / 1e12, 1),
+                                    "frac_of_bf16_peak": round(2 * M * d_in * d_out / (ms_mm * 1e-3) / 1e12 /
+                                                               peaks["bf16_tflops"], 4)},
+            "torch_eager_unfused_bypass_fwd_bwd": {"ms": round(ms_eager, 4),
+                                                   "tflops": round((fwd + bwd) / (ms_eager * 1e-3) / 1e12, 1)}}
 
 
 def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8", "qkv", "dropout")):
@@ -584,9 +683,18 @@ def _w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm):
     Wq = torch.from_numpy(Wq).to(dev)
     sw = torch.from_numpy(sw).to(dev)
 
-    def w8_step():
+    # the frozen weight laid out once (split codes for the forward, dequantised copy for the
+    # backward), outside the timed steps like loading the model
+    Wh, Wl, Wd = ops.w8a8_prepack_weight(Wq, sw)
+
+    def w8_step():   # W-1 (codes written as bf16) + the packed product with the LoRA epilogue
+        Xc, sx, Z = ops.w8a8_quantize_rows_bf16(X, A)
+        ops.w8a8_lora_fwd_packed(Xc, sx, Wh, Wl, sw, Z, B, case.s)
+
+    def w8_step_int8():   # the same through the int8 interface (re-lays out codes and weight per call)
         Xq, sx, Z = ops.w8a8_quantize_rows(X, A)
         ops.w8a8_lora_fwd(Xq, sx, Wq, sw, Z, B, case.s)
+    ms_int8, _, _ = timed(w8_step_int8, steps, warm)
     ms, _, _ = timed(w8_step, steps, warm)
     ms_ev = timed_gemm_events(L, w8_step, steps)
     gms, gn, gfl = L.lora_prof_gemm(reset=True)
@@ -597,15 +705,26 @@ def _w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm):
     lora_fl = 2 * case.M * case.r * (case.d_in + case.d_out)
     rec = {"ms_per_step": ms, "int8_tops": ops_int8 / (ms * 1e-3) / 1e12,
            "lora_tflops": lora_fl / (ms * 1e-3) / 1e12,
+           "path": "w8a8_quantize_rows_bf16 + w8a8_lora_fwd_packed (weight prepacked once)",
+           "int8_interface_ms_per_step": ms_int8,
            "note": "exact int8 product as two bf16 tcgen05 products of the split weight codes "
                    "(w = 16 (w >> 4) + (w & 15)); sm_103a has no tcgen05 int8 kind"}
     if gn:
-        ach = gfl / (gms * 1e-3) / 1e12   # bf16 tensor work of the split product
+        # the method's own work per launch: the int8 product 2 M N K plus the rank-r term 2 M N r;
+        # the kernel does twice the int8 product on the bf16 tensor cores (two split-code halves)
+        own = ops_int8 + 2 * case.M * case.d_out * case.r
+        ach = own * gn / (gms * 1e-3) / 1e12
         rec["roofline"] = {"kernel": "tc_gemm_kernel (W8A8 split-code mode)", "bound": "tensor",
-                           "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                           "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "T-ops/s",
                            "frac": round(ach / peaks["bf16_tflops"], 4), "launches": gn,
                            "avg_launch_ms": round(gms / gn, 4), "share_of_step": round(gms / ((steps + 1) * ms_ev), 4),
-                           "flops_per_launch": gfl / gn, "traffic": None,
+                           "ops_per_launch": own, "traffic": None,
+                           "split_factor": 2,
+                           "tensor_work_per_launch": gfl / gn,
+                           "tensor_frac": round(gfl / (gms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                           "note": "achieved counts the method's own work (2 M N K int8 + 2 M N r bf16); the split "
+                                   "codes w = 16 (w >> 4) + (w & 15) make the bf16 tensor cores do 2x the int8 "
+                                   "product (tensor_frac)",
                            "timing": "CUDA events around each GEMM launch in a second pass of the timed steps"}
     out["w8a8_lora_3072"] = rec
 
@@ -613,8 +732,8 @@ def _w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm):
     dY = torch.randn(case.M, case.d_out, device=dev, dtype=torch.bfloat16)
     Xq, sx, Z = ops.w8a8_quantize_rows(X, A)
 
-    def w8_bwd_step():
-        ops.w8a8_lora_bwd(X, Wq, sw, A, B, Z, dY, case.s)
+    def w8_bwd_step():   # through the prepacked dequantised weight
+        ops.lora_linear_bwd(X, Wd, A, B, Z, dY, case.s)
     ms_b, _, _ = timed(w8_bwd_step, steps, warm)
     fb = 2 * case.M * case.d_in * case.d_out + 4 * case.M * case.r * (case.d_in + case.d_out)
     out["w8a8_lora_3072_bwd"] = {"ms_per_step": ms_b, "tflops": fb / (ms_b * 1e-3) / 1e12,
@@ -630,6 +749,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads", default="all", choices=["all", "headline"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="repeat the timed region of K steps until the regions cover this many seconds")
     ap.add_argument("--only", default=None, choices=["dora", "mlp", "w8a8", "qkv", "dropout"],
                     help="time one non-headline workload alone (for profiling) and print its record")
     args = ap.parse_args()
@@ -680,8 +801,14 @@ def main():
                        "l2": "inputs larger than L2: X, dY 64 MiB each + W0 32 MiB + outputs per step (no flush)",
                        "flops_per_step": sum(lora_flops(8192, 4096, 4096, 16))},
             "tokens_per_s": round(h["tokens_per_s"]), "frac_of_bf16_peak": round(h["frac_of_bf16_peak_step"], 4),
-            "peaks": peaks, "roofline": h["roofline"], "cpu_baseline": cpu, "e2e": h["e2e"],
-            "gpu_launches": h["gpu_launches"], "clocks": h["clocks"], "workloads": extra,
+            "timed_regions": h["timed_regions"], "fwd": h["fwd"], "bwd": h["bwd"],
+            "peaks": peaks, "roofline": h["roofline"], "rank_passes": h["rank_passes"], "cpu_baseline": cpu,
+            "e2e": h["e2e"], "gpu_launches": h["gpu_launches"], "clocks": h["clocks"], "context": h["context"],
+            "largest_linear_config": None if not extra else {
+                "workload": "dora_4096x11008_bf16 (DoRA rows fwd+bwd, M 8192, 4096 -> 11008, r 32)",
+                "tflops": round(extra["dora_4096x11008_bf16"]["tflops"], 1),
+                "frac_of_bf16_peak": round(extra["dora_4096x11008_bf16"]["frac_of_bf16_peak"], 4)},
+            "workloads": extra,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -85,6 +85,11 @@ _SIGS = {
     "w8a8_workspace_bytes": (c_size_t, [c_int64, c_int64, c_int64]),
     "w8a8_lora_fwd": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, c_float, P, P, P, P, c_size_t,
                               P]),
+    "w8a8_quantize_rows_bf16": (c_int, [c_int64, c_int64, P, P, P, P, c_int64, P, P]),
+    "w8a8_prepack_weight": (c_int, [c_int64, c_int64, P, P, P, P, P, P]),
+    "w8a8_packed_workspace_bytes": (c_size_t, [c_int64, c_int64]),
+    "w8a8_lora_fwd_packed": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, P, c_float, P, P, P, P,
+                                     c_size_t, P]),
     "lora_debug_wait_timeout": (c_int, [P, c_uint32, P]),
     "lora_linear_fwd_noalloc": (c_int, [POINTER(LoraShape), P, P, P, P, P, c_float, P, P, P]),
     "w8a8_bwd_workspace_bytes": (c_size_t, [c_int64, c_int64, c_int64, c_int64]),
@@ -97,6 +102,7 @@ _SIGS = {
     "lora_launch_count": (ctypes.c_uint64, []),
     "lora_prof_enable": (c_int, [c_int]),
     "lora_prof_gemm": (c_int, [POINTER(ctypes.c_double), POINTER(c_int64), POINTER(ctypes.c_double), c_int]),
+    "lora_prof_rank": (c_int, [POINTER(ctypes.c_double), POINTER(c_int64), POINTER(ctypes.c_double), c_int]),
 }
 
 _LIB = None
@@ -221,6 +227,14 @@ def lora_prof_gemm(reset: bool = True):
     _ck(_lib().lora_prof_gemm(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl), 1 if reset else 0),
         "lora_prof_gemm")
     return ms.value, n.value, fl.value
+
+
+def lora_prof_rank(reset: bool = True):
+    """(device ms, launches, algorithmic HBM bytes) of the rank-r passes recorded since the last reset."""
+    ms, n, by = ctypes.c_double(), c_int64(), ctypes.c_double()
+    _ck(_lib().lora_prof_rank(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(by), 1 if reset else 0),
+        "lora_prof_rank")
+    return ms.value, n.value, by.value
 
 
 def lora_linear_fwd(sh, X, W0, A, B, bias, s, Y, Z_save, ws, stream=None):
@@ -352,3 +366,24 @@ def w8a8_lora_fwd(M, d_in, d_out, r, Xq, sx, Wq, sw, Z, B, s, bias, Y, acc_out, 
     _ck(_lib().w8a8_lora_fwd(M, d_in, d_out, r, ptr(Xq), ptr(sx), ptr(Wq), ptr(sw), ptr(Z), ptr(B), float(s),
                              ptr(bias), ptr(Y), ptr(acc_out), ptr(ws),
                              0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)), "w8a8_lora_fwd")
+
+
+def w8a8_quantize_rows_bf16(rows, cols, X, Xcodes, sx, A=None, r=0, Z=None, stream=None):
+    _ck(_lib().w8a8_quantize_rows_bf16(rows, cols, ptr(X), ptr(Xcodes), ptr(sx), ptr(A), r, ptr(Z),
+                                       _stream(stream)), "w8a8_quantize_rows_bf16")
+
+
+def w8a8_prepack_weight(d_out, d_in, Wq, sw, Wh, Wl, Wd, stream=None):
+    _ck(_lib().w8a8_prepack_weight(d_out, d_in, ptr(Wq), ptr(sw), ptr(Wh), ptr(Wl), ptr(Wd), _stream(stream)),
+        "w8a8_prepack_weight")
+
+
+def w8a8_packed_workspace_bytes(M, d_out) -> int:
+    return _lib().w8a8_packed_workspace_bytes(M, d_out)
+
+
+def w8a8_lora_fwd_packed(M, d_in, d_out, r, Xcodes, sx, Wh, Wl, sw, Z, B, s, bias, Y, acc_out, ws, stream=None):
+    _ck(_lib().w8a8_lora_fwd_packed(M, d_in, d_out, r, ptr(Xcodes), ptr(sx), ptr(Wh), ptr(Wl), ptr(sw), ptr(Z),
+                                    ptr(B), float(s), ptr(bias), ptr(Y), ptr(acc_out), ptr(ws),
+                                    0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
+        "w8a8_lora_fwd_packed")

@@ -555,7 +555,12 @@ lora_status lora_prof_enable(int on) {
 }
 
 lora_status lora_prof_gemm(double* ms, int64_t* launches, double* flops, int reset) {
-  CK(prof_collect(ms, launches, flops, reset != 0));
+  CK(prof_collect(0, ms, launches, flops, reset != 0));
+  return LORA_OK;
+}
+
+lora_status lora_prof_rank(double* ms, int64_t* launches, double* bytes, int reset) {
+  CK(prof_collect(1, ms, launches, bytes, reset != 0));
   return LORA_OK;
 }
 
@@ -1559,56 +1564,39 @@ size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out) {
          al256((size_t)M * kW8MaxR * 2) + al256((size_t)d_out * kW8MaxR * 2);
 }
 
-lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq, const float* sx,
-                          const int8_t* Wq, const float* sw, const void* Z, const void* B, float s, const void* bias,
-                          void* Y, int32_t* acc_out, void* ws, size_t ws_bytes, void* stream) {
-  if (M < 0 || d_in <= 0 || d_out <= 0) return LORA_ERR_INVALID_ARG;
-  if (d_in % 32 || d_out % 8) return LORA_ERR_UNSUPPORTED;
-  REQM(M, Xq); REQ(Wq);
-  if (Y == nullptr && acc_out == nullptr) return LORA_ERR_INVALID_ARG;
-  if (Y && (!sx || !sw)) return LORA_ERR_INVALID_ARG;
-  if ((Z == nullptr) != (B == nullptr)) return LORA_ERR_INVALID_ARG;
-  if (Z && (r < 8 || r > kW8MaxR || r % 8)) return LORA_ERR_UNSUPPORTED;
-  if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
-  ALN(Xq); ALN(sx); ALN(Wq); ALN(sw); ALN(Z); ALN(B); ALN(bias); ALN(Y); ALN(acc_out);
-  lora_status e = check_ws(ws, ws_bytes, w8a8_workspace_bytes(M, d_in, d_out));
-  if (e != LORA_OK) return e;
-  if (M == 0) return LORA_OK;
-  cudaStream_t st = (cudaStream_t)stream;
-  if (d_in > kW8ExactMaxK || getenv("LORA_GB300_W8A8_IMMA")) {
-    CK(w8a8_gemm(M, d_in, d_out, Z ? (int)r : 0, Xq, sx, Wq, sw, static_cast<const bf16*>(Z),
-                 static_cast<const bf16*>(B), s, static_cast<const bf16*>(bias), static_cast<bf16*>(Y), acc_out, st));
-    return LORA_OK;
-  }
-  Carve c{static_cast<char*>(ws)};
-  uint32_t* err = c.take<uint32_t>(kErrBytes / 4);
-  bf16* Xb = c.take<bf16>((size_t)M * d_in);
-  bf16* Wh = c.take<bf16>((size_t)d_out * d_in);
-  bf16* Wl = c.take<bf16>((size_t)d_out * d_in);
-  CK(i8_to_bf16(Xq, M * d_in, Xb, st));
-  CK(i8_split_bf16(Wq, d_out * d_in, Wh, Wl, st));
+}  // extern "C"
+
+namespace {
+// The split-code tensor-core product and its epilogue on operands already laid out for it:
+// Xb [M, d_in] the activation codes as bf16, Wh / Wl [d_out, d_in] the weight codes' high and
+// low parts as bf16; Zt / Bt (each room for kW8MaxR columns) hold the rank-r operands divided by
+// the dequant scales when the folded output-only epilogue runs.
+lora_status w8a8_fwd_core(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const bf16* Xb, const float* sx,
+                          const bf16* Wh, const bf16* Wl, const float* sw, const void* Z, const void* B, float s,
+                          const void* bias, void* Y, int32_t* acc_out, uint32_t* err, bf16* Zt, bf16* Bt,
+                          cudaStream_t st) {
   TcGemmDesc d;
+  d.M = (int)M;
+  d.N = (int)d_out;
+  d.K0 = (int)d_in;
+  d.A0 = Xb;
+  d.lda0 = d_in;
+  d.B0 = Wh;
+  d.B0b = Wl;
+  d.ldb0 = d_in;
+  d.out[0] = Y;
+  d.ldo = d_out;
+  d.bias = static_cast<const bf16*>(bias);
+  d.sx = sx;
+  d.sw = sw;
+  d.err = err;
+  d.timeout_ns = wait_timeout_ns();
   if (acc_out == nullptr && !env_flag("LORA_GB300_W8A8_EXACT")) {
     // Only the dequantised output is wanted: fold the rank-r term into the low half as
     // (s Z / sx) (B / sw)^T, so the epilogue is y = (16 hi + lo) sx sw + bias and the accumulators
     // fit twice in TMEM (double-buffered, like every other mode).  The low half then holds the
     // exact integer partial sum plus that term, rounded once in fp32.
-    bf16* Zt = c.take<bf16>((size_t)M * kW8MaxR);
-    bf16* Bt = c.take<bf16>((size_t)d_out * kW8MaxR);
     d.mode = TC_W8A8F;
-    d.M = (int)M;
-    d.N = (int)d_out;
-    d.K0 = (int)d_in;
-    d.A0 = Xb;
-    d.lda0 = d_in;
-    d.B0 = Wh;
-    d.B0b = Wl;
-    d.ldb0 = d_in;
-    d.out[0] = Y;
-    d.ldo = d_out;
-    d.bias = static_cast<const bf16*>(bias);
-    d.sx = sx;
-    d.sw = sw;
     if (Z && s != 0.f) {
       CK(scale_rows_recip_bf16(static_cast<const bf16*>(Z), M, (int)r, sx, s, Zt, st));
       CK(scale_rows_recip_bf16(static_cast<const bf16*>(B), d_out, (int)r, sw, 1.f, Bt, st));
@@ -1626,25 +1614,10 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
       d.b1_x = kW8MaxR;   // at or past r for every tail step
       d.b1b_x = 0;
     }
-    d.err = err;
-    d.timeout_ns = wait_timeout_ns();
     CK(tc_gemm(d, st));
     return LORA_OK;
   }
   d.mode = TC_W8A8;
-  d.M = (int)M;
-  d.N = (int)d_out;
-  d.K0 = (int)d_in;
-  d.A0 = Xb;
-  d.lda0 = d_in;
-  d.B0 = Wh;
-  d.B0b = Wl;
-  d.ldb0 = d_in;
-  d.out[0] = Y;
-  d.ldo = d_out;
-  d.bias = static_cast<const bf16*>(bias);
-  d.sx = sx;
-  d.sw = sw;
   d.lz = static_cast<const bf16*>(Z);
   d.lb = static_cast<const bf16*>(B);
   d.ls = s;
@@ -1660,10 +1633,106 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
     d.K1_b = (int)r;
   }
   d.acc_out = acc_out;
-  d.err = err;
-  d.timeout_ns = wait_timeout_ns();
   CK(tc_gemm(d, st));
   return LORA_OK;
+}
+
+lora_status check_w8a8(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const void* Z, const void* B, float s,
+                       const void* Y, const int32_t* acc_out, const float* sx, const float* sw) {
+  if (M < 0 || d_in <= 0 || d_out <= 0) return LORA_ERR_INVALID_ARG;
+  if (d_in % 32 || d_out % 8) return LORA_ERR_UNSUPPORTED;
+  if (Y == nullptr && acc_out == nullptr) return LORA_ERR_INVALID_ARG;
+  if (Y && (!sx || !sw)) return LORA_ERR_INVALID_ARG;
+  if ((Z == nullptr) != (B == nullptr)) return LORA_ERR_INVALID_ARG;
+  if (Z && (r < 8 || r > kW8MaxR || r % 8)) return LORA_ERR_UNSUPPORTED;
+  if (!isfinite(s)) return LORA_ERR_INVALID_ARG;
+  return LORA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq, const float* sx,
+                          const int8_t* Wq, const float* sw, const void* Z, const void* B, float s, const void* bias,
+                          void* Y, int32_t* acc_out, void* ws, size_t ws_bytes, void* stream) {
+  lora_status e = check_w8a8(M, d_in, d_out, r, Z, B, s, Y, acc_out, sx, sw);
+  if (e != LORA_OK) return e;
+  REQM(M, Xq); REQ(Wq);
+  ALN(Xq); ALN(sx); ALN(Wq); ALN(sw); ALN(Z); ALN(B); ALN(bias); ALN(Y); ALN(acc_out);
+  if ((e = check_ws(ws, ws_bytes, w8a8_workspace_bytes(M, d_in, d_out))) != LORA_OK) return e;
+  if (M == 0) return LORA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (d_in > kW8ExactMaxK || getenv("LORA_GB300_W8A8_IMMA")) {
+    CK(w8a8_gemm(M, d_in, d_out, Z ? (int)r : 0, Xq, sx, Wq, sw, static_cast<const bf16*>(Z),
+                 static_cast<const bf16*>(B), s, static_cast<const bf16*>(bias), static_cast<bf16*>(Y), acc_out, st));
+    return LORA_OK;
+  }
+  Carve c{static_cast<char*>(ws)};
+  uint32_t* err = c.take<uint32_t>(kErrBytes / 4);
+  bf16* Xb = c.take<bf16>((size_t)M * d_in);
+  bf16* Wh = c.take<bf16>((size_t)d_out * d_in);
+  bf16* Wl = c.take<bf16>((size_t)d_out * d_in);
+  bf16* Zt = c.take<bf16>((size_t)M * kW8MaxR);
+  bf16* Bt = c.take<bf16>((size_t)d_out * kW8MaxR);
+  CK(i8_to_bf16(Xq, M * d_in, Xb, st));
+  CK(i8_split_bf16(Wq, d_out * d_in, Wh, Wl, st));
+  return w8a8_fwd_core(M, d_in, d_out, r, Xb, sx, Wh, Wl, sw, Z, B, s, bias, Y, acc_out, err, Zt, Bt, st);
+}
+
+lora_status w8a8_quantize_rows_bf16(int64_t rows, int64_t cols, const void* X, void* Xcodes, float* sx,
+                                    const void* A, int64_t r, void* Z, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 8) return rows < 0 || cols <= 0 ? LORA_ERR_INVALID_ARG : LORA_ERR_UNSUPPORTED;
+  REQM(rows, X); REQM(rows, Xcodes); REQM(rows, sx);
+  ALN(X); ALN(Xcodes); ALN(A); ALN(Z);
+  if ((A == nullptr) != (Z == nullptr)) return LORA_ERR_INVALID_ARG;
+  if (A && (r < 8 || r > kW8MaxR || r % 8)) return LORA_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (rows == 0) return LORA_OK;
+  CK(quantize_rows_bf16(static_cast<const bf16*>(X), rows, cols, nullptr, sx, st, static_cast<bf16*>(Xcodes)));
+  if (A) {
+    RowProjDesc d = rp_desc(rows, cols, (int)r, X, A, false, nullptr);  // no workspace: no error word
+    d.out_a = static_cast<bf16*>(Z);
+    CK(rowproj(d, st));
+  }
+  return LORA_OK;
+}
+
+lora_status w8a8_prepack_weight(int64_t d_out, int64_t d_in, const int8_t* Wq, const float* sw, void* Wh, void* Wl,
+                                void* Wd, void* stream) {
+  if (d_out <= 0 || d_in <= 0) return LORA_ERR_INVALID_ARG;
+  if (d_in % 32 || d_out % 8) return LORA_ERR_UNSUPPORTED;
+  REQ(Wq);
+  if ((Wh == nullptr) != (Wl == nullptr)) return LORA_ERR_INVALID_ARG;
+  if (Wd && !sw) return LORA_ERR_INVALID_ARG;
+  ALN(Wq); ALN(sw); ALN(Wh); ALN(Wl); ALN(Wd);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (Wh) CK(i8_split_bf16(Wq, d_out * d_in, static_cast<bf16*>(Wh), static_cast<bf16*>(Wl), st));
+  if (Wd) CK(i8_dequant_rows_bf16(Wq, sw, d_out, d_in, static_cast<bf16*>(Wd), st));
+  return LORA_OK;
+}
+
+size_t w8a8_packed_workspace_bytes(int64_t M, int64_t d_out) {
+  if (M < 0 || d_out <= 0) return 0;
+  return kErrBytes + al256((size_t)M * kW8MaxR * 2) + al256((size_t)d_out * kW8MaxR * 2);
+}
+
+lora_status w8a8_lora_fwd_packed(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const void* Xcodes,
+                                 const float* sx, const void* Wh, const void* Wl, const float* sw, const void* Z,
+                                 const void* B, float s, const void* bias, void* Y, int32_t* acc_out, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  lora_status e = check_w8a8(M, d_in, d_out, r, Z, B, s, Y, acc_out, sx, sw);
+  if (e != LORA_OK) return e;
+  if (d_in > kW8ExactMaxK) return LORA_ERR_UNSUPPORTED;   // the split-code product is exact up to here
+  REQM(M, Xcodes); REQ(Wh); REQ(Wl);
+  ALN(Xcodes); ALN(sx); ALN(Wh); ALN(Wl); ALN(sw); ALN(Z); ALN(B); ALN(bias); ALN(Y); ALN(acc_out);
+  if ((e = check_ws(ws, ws_bytes, w8a8_packed_workspace_bytes(M, d_out))) != LORA_OK) return e;
+  if (M == 0) return LORA_OK;
+  Carve c{static_cast<char*>(ws)};
+  uint32_t* err = c.take<uint32_t>(kErrBytes / 4);
+  bf16* Zt = c.take<bf16>((size_t)M * kW8MaxR);
+  bf16* Bt = c.take<bf16>((size_t)d_out * kW8MaxR);
+  return w8a8_fwd_core(M, d_in, d_out, r, static_cast<const bf16*>(Xcodes), sx, static_cast<const bf16*>(Wh),
+                       static_cast<const bf16*>(Wl), sw, Z, B, s, bias, Y, acc_out, err, Zt, Bt, (cudaStream_t)stream);
 }
 
 size_t w8a8_bwd_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int64_t r) {

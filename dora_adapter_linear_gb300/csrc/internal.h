@@ -25,8 +25,10 @@ void count_launch(int n = 1);
 uint64_t launch_count();
 bool prof_enabled();
 void prof_set(bool on);
-void prof_mark(cudaStream_t st, bool start, double flops);
-cudaError_t prof_collect(double* ms, int64_t* launches, double* flops, bool reset);
+// kind 0: tcgen05 GEMM launches (work = algorithmic flops); kind 1: rank-r passes (work =
+// algorithmic HBM bytes)
+void prof_mark(cudaStream_t st, bool start, double work, int kind = 0);
+cudaError_t prof_collect(int kind, double* ms, int64_t* launches, double* work, bool reset);
 
 // ------------------------------------------------------------------ tcgen05 GEMM engine
 enum EpiKind { EPI_SCALE_BIAS = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2, EPI_W8A8 = 3, EPI_W8A8F = 4 };
@@ -294,7 +296,9 @@ cudaError_t coldot_f32(const float* S, const float* Y, int64_t rows, int64_t K, 
                        cudaStream_t st);
 
 // ------------------------------------------------------------------ W8A8
-cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t* Xq, float* sx, cudaStream_t st);
+// per-row absmax quantisation: codes as int8 (Xq) and/or as bf16 values (Xb), either may be null
+cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t* Xq, float* sx, cudaStream_t st,
+                               bf16* Xb = nullptr);
 // int8 -> bf16 (exact), and the weight split w = 16 wh + wl (n multiple of 16)
 cudaError_t i8_to_bf16(const int8_t* q, int64_t n, bf16* out, cudaStream_t st);
 cudaError_t i8_split_bf16(const int8_t* q, int64_t n, bf16* hi, bf16* lo, cudaStream_t st);

@@ -1,6 +1,7 @@
 // Native tracing: a host-side count of every kernel launch the library issues, and optional
-// CUDA-event timing of the tcgen05 GEMM launches (two events on the launching stream per
-// launch), so a benchmark can time the dominant kernel inside a long step without a profiler.
+// CUDA-event timing (two events on the launching stream per launch) of the tcgen05 GEMM
+// launches (kind 0, with their algorithmic flops) and of the rank-r passes (kind 1, with their
+// algorithmic HBM bytes), so a benchmark can time them inside a long step without a profiler.
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -13,7 +14,8 @@ static std::atomic<uint64_t> g_launches{0};
 
 struct ProfRec {
   cudaEvent_t a, b;
-  double flops;
+  double work;   // flops (GEMM) or bytes (rank-r pass)
+  int kind;
 };
 static std::mutex g_mu;
 static bool g_prof_on = false;
@@ -41,12 +43,12 @@ void prof_set(bool on) {
   g_prof_on = on;
 }
 
-// Bracket one launch: call with `start` = true before, false after.
-void prof_mark(cudaStream_t st, bool start, double flops) {
+// Bracket one launch: call with `start` = true before, false after (records nest one deep).
+void prof_mark(cudaStream_t st, bool start, double work, int kind) {
   if (!g_prof_on) return;
   std::lock_guard<std::mutex> lk(g_mu);
   if (start) {
-    ProfRec r{take_event(), take_event(), flops};
+    ProfRec r{take_event(), take_event(), work, kind};
     if (r.a && r.b) {
       cudaEventRecord(r.a, st);
       g_recs.push_back(r);
@@ -56,27 +58,35 @@ void prof_mark(cudaStream_t st, bool start, double flops) {
   }
 }
 
-cudaError_t prof_collect(double* ms, int64_t* launches, double* flops, bool reset) {
+cudaError_t prof_collect(int kind, double* ms, int64_t* launches, double* work, bool reset) {
   std::lock_guard<std::mutex> lk(g_mu);
   double t = 0.0, f = 0.0;
+  int64_t n = 0;
   for (auto& r : g_recs) {
+    if (r.kind != kind) continue;
     cudaError_t e = cudaEventSynchronize(r.b);
     if (e != cudaSuccess) return e;
     float x = 0.f;
     e = cudaEventElapsedTime(&x, r.a, r.b);
     if (e != cudaSuccess) return e;
     t += x;
-    f += r.flops;
+    f += r.work;
+    ++n;
   }
   if (ms) *ms = t;
-  if (launches) *launches = (int64_t)g_recs.size();
-  if (flops) *flops = f;
+  if (launches) *launches = n;
+  if (work) *work = f;
   if (reset) {
+    std::vector<ProfRec> keep;
     for (auto& r : g_recs) {
-      g_pool.push_back(r.a);
-      g_pool.push_back(r.b);
+      if (r.kind == kind) {
+        g_pool.push_back(r.a);
+        g_pool.push_back(r.b);
+      } else {
+        keep.push_back(r);
+      }
     }
-    g_recs.clear();
+    g_recs.swap(keep);
   }
   return cudaSuccess;
 }

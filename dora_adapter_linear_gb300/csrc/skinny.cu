@@ -246,7 +246,12 @@ static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_attr(&attr[0]);
+  // algorithmic HBM bytes: S once, U, the outputs (and the scaled copy of S)
+  const double outs = (d.out_a ? 2.0 : 0.0) + (d.out_b ? 2.0 : 0.0) + (d.out_f ? 4.0 : 0.0);
+  const double bytes = 2.0 * d.rows * d.K * (d.s_out ? 2.0 : 1.0) + 2.0 * R * d.K + outs * d.rows * R;
+  prof_mark(st, true, bytes, 1);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k, P);
+  prof_mark(st, false, 0.0, 1);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -506,7 +511,12 @@ static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_attr(&attr[0]);
+  // algorithmic HBM bytes: S (and Y) once, T, the fp32 partials (and column sums)
+  const double bytes = 2.0 * d.rows * d.K * (HAS_Y ? 2.0 : 1.0) + 2.0 * d.rows * R +
+                       4.0 * d.splits * d.K * (R + (SUMS ? 2.0 : 0.0));
+  prof_mark(st, true, bytes, 1);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k, P);
+  prof_mark(st, false, 0.0, 1);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -14,7 +14,10 @@
 namespace lg {
 
 // ------------------------------------------------------------------ per-row absmax quantisation
-__global__ void __launch_bounds__(256) quantize_rows_kernel(const bf16* X, int64_t cols, int8_t* Xq, float* sx) {
+// Writes the codes as int8 (Xq) and/or as bf16 values (Xb: the same integers, exact in bf16, ready
+// to be the A operand of the split-code tensor-core product); either may be null.
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const bf16* X, int64_t cols, int8_t* Xq, float* sx,
+                                                            bf16* Xb) {
   const int64_t row = blockIdx.x;
   const bf16* x = X + row * cols;
   float amax = 0.f;
@@ -41,6 +44,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const bf16* X, int64
     const uint4 raw = *reinterpret_cast<const uint4*>(x + k);
     const uint32_t* w = reinterpret_cast<const uint32_t*>(&raw);
     uint32_t packed[2] = {0u, 0u};
+    uint32_t codes[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 f = unpack_bf16x2(w[i]);
@@ -50,14 +54,17 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const bf16* X, int64
         q1 = min(127, max(-127, __float2int_rn(__fdiv_rn(f.y, scale))));
       }
       packed[i >> 1] |= ((uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8)) << ((i & 1) * 16);
+      codes[i] = pack_bf16x2((float)q0, (float)q1);
     }
-    *reinterpret_cast<uint2*>(Xq + row * cols + k) = make_uint2(packed[0], packed[1]);
+    if (Xq) *reinterpret_cast<uint2*>(Xq + row * cols + k) = make_uint2(packed[0], packed[1]);
+    if (Xb) *reinterpret_cast<uint4*>(Xb + row * cols + k) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
   }
 }
 
-cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t* Xq, float* sx, cudaStream_t st) {
+cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t* Xq, float* sx, cudaStream_t st,
+                               bf16* Xb) {
   if (rows <= 0) return cudaSuccess;
-  quantize_rows_kernel<<<(unsigned)rows, 256, 0, st>>>(X, cols, Xq, sx);
+  quantize_rows_kernel<<<(unsigned)rows, 256, 0, st>>>(X, cols, Xq, sx, Xb);
   count_launch();
   return cudaGetLastError();
 }

@@ -364,6 +364,36 @@ lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0
 lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t* Xq, float* sx,
                                const void* A, int64_t r, void* Z, void* stream);
 
+/* Step W-1 for the prepacked product: the same quantisation, with the codes written as bf16
+ * values (the same integers, exact in bf16) instead of int8, ready to be the A operand of
+ * w8a8_lora_fwd_packed (no re-layout in the forward).  Xcodes [rows, cols] bf16; the rest as
+ * w8a8_quantize_rows.  Same page and passage as w8a8_quantize_rows. */
+lora_status w8a8_quantize_rows_bf16(int64_t rows, int64_t cols, const void* X, void* Xcodes, float* sx,
+                                    const void* A, int64_t r, void* Z, void* stream);
+
+/* One-time preparation of the frozen int8 weight Wq [d_out, d_in] (sw [d_out] fp32):
+ *   Wh, Wl [d_out, d_in] bf16: the code split w = 16 * (w >> 4) + (w & 15) used by the tensor-core
+ *   product (both NULL or both set);  Wd [d_out, d_in] bf16 = sw[o] * Wq[o, k], the dequantised
+ *   weight of the backward (NULL to skip).  The backward through the int8 base given Wd is
+ *   lora_linear_bwd with W0 = Wd (what w8a8_lora_bwd does after dequantising per call).
+ * "nunchaku-style kernel fusion" (OneTrainer #1680), commit reworking the 8-bit matmuls (the
+ * frozen 8-bit weight, re-laid out for the product once).  d_in a multiple of 32. */
+lora_status w8a8_prepack_weight(int64_t d_out, int64_t d_in, const int8_t* Wq, const float* sw, void* Wh,
+                                void* Wl, void* Wd, void* stream);
+
+/* Workspace of w8a8_lora_fwd_packed: the error word and the rank-r operands divided by the
+ * dequant scales (M x 128 and d_out x 128 bf16).  0 on bad input. */
+size_t w8a8_packed_workspace_bytes(int64_t M, int64_t d_out);
+
+/* w8a8_lora_fwd on prepacked operands: Xcodes [M, d_in] bf16 from w8a8_quantize_rows_bf16 and
+ * Wh, Wl [d_out, d_in] bf16 from w8a8_prepack_weight; every other argument, the result and its
+ * exactness as w8a8_lora_fwd.  d_in <= 8800 (the split-code product is exact up to there;
+ * LORA_ERR_UNSUPPORTED beyond).  Same pages and passages as w8a8_lora_fwd. */
+lora_status w8a8_lora_fwd_packed(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const void* Xcodes,
+                                 const float* sx, const void* Wh, const void* Wl, const float* sw, const void* Z,
+                                 const void* B, float s, const void* bias, void* Y, int32_t* acc_out, void* ws,
+                                 size_t ws_bytes, void* stream);
+
 /* Bytes of workspace w8a8_lora_fwd needs: the error word, the int8 codes re-laid out as bf16
  * tensor-core operands (X: M x d_in; W split into two d_out x d_in halves) and the rank-r
  * operands divided by the dequant scales (M x 128 and d_out x 128 bf16).  0 on bad input. */
@@ -406,6 +436,11 @@ lora_status lora_prof_enable(int on);
  * rank-r tail, 2*M*N*K) of the GEMM launches recorded since the last reset; waits for the
  * recorded events.  Any output pointer may be NULL.  reset != 0 clears the record. */
 lora_status lora_prof_gemm(double* ms, int64_t* launches, double* flops, int reset);
+
+/* The same for the rank-r passes (the skinny HBM-bound kernels: down-projections, column
+ * reductions): total event time, launches, and their algorithmic HBM bytes (each input read
+ * once, outputs written once).  No counterpart on the pages (tracing). */
+lora_status lora_prof_rank(double* ms, int64_t* launches, double* bytes, int reset);
 
 /* Bytes of workspace w8a8_lora_bwd needs (0 on bad input). */
 size_t w8a8_bwd_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int64_t r);

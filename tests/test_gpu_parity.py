@@ -521,6 +521,38 @@ def test_w8a8_deep_k_uses_integer_path(ops):
     np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), O.int8_accumulate(Xq, Wq))
 
 
+@pytest.mark.parametrize("bias", [False, True])
+def test_w8a8_packed_path(ops, bias):
+    """Prepacked operands: the quantiser's bf16 codes, the weight's split halves and dequantised
+    copy made once; the packed forward gives the same bits as w8a8_lora_fwd and the exact int32
+    product; the backward through the dequantised weight matches the oracle."""
+    case, t, Wq, sw, Xq, sx = w8_inputs(M=300, d_in=352, d_out=264, bias=bias)
+    X, A = gpu(t["X"]), gpu(t["A"])
+    Xc, gsx, gZ = ops.w8a8_quantize_rows_bf16(X, A)
+    np.testing.assert_array_equal(Xc.float().cpu().numpy(), Xq.astype(np.float32))    # codes, exactly
+    np.testing.assert_array_equal(gsx.cpu().numpy(), sx)
+    gWq, gsw = gpu(torch.from_numpy(Wq)), gpu(torch.from_numpy(sw))
+    Wh, Wl, Wd = ops.w8a8_prepack_weight(gWq, gsw)
+    np.testing.assert_array_equal((16 * Wh.float() + Wl.float()).cpu().numpy(), Wq.astype(np.float32))
+    assert_close(Wd, O.w8a8_dequant_weight(Wq, sw), "bf16", "Wd")
+    Z = (t["X"].double() @ t["A"].double().T).to(torch.bfloat16)
+    ry, racc = O.w8a8_lora_fwd(Xq, sx, Wq, sw, f64(Z), f64(t["B"]), case.s, f64(t["bias"]))
+    Yp, accp = ops.w8a8_lora_fwd_packed(Xc, gsx, Wh, Wl, gsw, gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]),
+                                        want_acc=True)
+    np.testing.assert_array_equal(accp.cpu().numpy().astype(np.int64), racc)
+    assert_close(Yp, ry, "bf16", "Y packed (exact epilogue)")
+    Yf, _ = ops.w8a8_lora_fwd_packed(Xc, gsx, Wh, Wl, gsw, gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]))
+    Yu, _ = ops.w8a8_lora_fwd(gpu(torch.from_numpy(Xq)), gsx, gWq, gsw, gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]))
+    assert torch.equal(Yf, Yu), "the packed forward runs the same product and epilogue"
+    assert_close(Yf, ry, "bf16", "Y packed (folded epilogue)")
+    g = torch.Generator().manual_seed(80)
+    dY = torch.randn(case.M, case.d_out, generator=g).to(torch.bfloat16)
+    dX, dA, dB, db = ops.lora_linear_bwd(X, Wd, A, gpu(t["B"]), gpu(Z), gpu(dY), case.s, need_dbias=True)
+    rX, rA, rB, rb = O.w8a8_lora_bwd(f64(t["X"]), Wq, sw, f64(t["A"]), f64(t["B"]), case.s, f64(dY))
+    for got, ref, nm in ((dX, rX, "dX"), (dA, rA, "dA"), (dB, rB, "dB"), (db, rb[None], "dbias")):
+        assert_close(got, ref, "bf16", nm)
+
+
 @pytest.mark.parametrize("r", [96, 128])
 def test_w8a8_large_rank(ops, r, monkeypatch):
     """Ranks above 64: the quantiser's down-projection in two passes, both epilogues' rank-r
