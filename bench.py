@@ -301,10 +301,10 @@ def timed_reps(fn, steps, warmup, dist=None, min_s=1.0, max_reps=200):
 # DRAM bytes (read + write) per GEMM launch from ncu captures, keyed by workload; a value is
 # dropped (None) whenever the kernel changes and is re-measured before it is put back.
 # lora_4096_bf16: dram__bytes_read.sum + dram__bytes_write.sum of the forward (CTA pair) and dX
-# (one-CTA kernel, two-CTA clusters sharing B) GEMM launches of the headline step (mean of 4
-# launches: 132.7 MB read + 45.3 MB written; the algorithmic bytes are 64 MiB activation +
-# 32 MiB weight + 64 MiB output = 167.8 MB).
-GEMM_TRAFFIC = {"lora_4096_bf16": 178.0e6}
+# (one-CTA kernel, no cluster) GEMM launches of the headline step, one full capture of each:
+# forward 153.1 + 48.0 MB, dX 119.5 + 43.5 MB, mean 182.1 MB per launch; the algorithmic bytes
+# are 64 MiB activation + 32 MiB weight + 64 MiB output = 167.8 MB.
+GEMM_TRAFFIC = {"lora_4096_bf16": 182.1e6}
 
 
 def timed_gemm_events(L, fn, steps, warmup=1):
@@ -741,6 +741,62 @@ def _w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm):
     return out
 
 
+def profile_steps(args, ops):
+    """W + K forward + backward steps of one workload and nothing else (a profiler's view)."""
+    import torch
+
+    import datagen as D
+    import oracle as O
+    dev = torch.device("cuda", torch.cuda.current_device())
+    kw = {"M": args.profile_m} if args.profile_m > 0 else {}
+    if args.profile in ("lora", "dora"):
+        case = D.scaled(D.WORKLOADS[HEADLINE if args.profile == "lora" else "dora_4096x11008_bf16"], **kw)
+        g = {k: v.to(dev) for k, v in D.make_linear(case).items() if v is not None}
+        if args.profile == "lora":
+            def step():
+                Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s)
+                ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
+        else:
+            r0 = ops.dora_rownorm2(g["W0"])
+
+            def step():
+                Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps,
+                                                 g["bias"])
+                ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V, g["dY"], case.s,
+                                    case.eps)
+    elif args.profile == "mlp":
+        case = D.scaled(D.WORKLOADS["mlp_swiglu_4096x14336_bf16"], **kw)
+        g = {k: v.to(dev) for k, v in D.make_mlp(case).items()}
+        P = {p: {"W": g["W" + p], "A": g["A" + p], "B": g["B" + p], "s": case.s} for p in "gud"}
+
+        def step():
+            Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
+            ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
+    elif args.profile == "qkv":
+        case = D.scaled(D.WORKLOADS["qkv_lora_4096_gqa_bf16"], **kw)
+        g = {k: v.to(dev) for k, v in D.make_qkv(case).items() if v is not None}
+        leaves = [(g[f"A{l}"], g[f"B{l}"], case.s[l]) for l in range(len(case.n))]
+
+        def step():
+            Y, Z = ops.lora_qkv_fwd(g["X"], g["W0"], leaves)
+            ops.lora_qkv_bwd(g["X"], g["W0"], leaves, Z, g["dY"])
+    else:
+        case = D.scaled(D.WORKLOADS["w8a8_lora_3072"], **kw)
+        t = D.make_w8a8(case)
+        Wq, sw = O.quantize_rows(t["W0"].numpy())
+        X, A, B = t["X"].to(dev), t["A"].to(dev), t["B"].to(dev)
+        Wh, Wl, Wd = ops.w8a8_prepack_weight(torch.from_numpy(Wq).to(dev), torch.from_numpy(sw).to(dev))
+        swd = torch.from_numpy(sw).to(dev)
+
+        def step():
+            Xc, sx, Z = ops.w8a8_quantize_rows_bf16(X, A)
+            ops.w8a8_lora_fwd_packed(Xc, sx, Wh, Wl, swd, Z, B, case.s)
+    for _ in range(args.warmup + args.steps):
+        step()
+    torch.cuda.synchronize()
+    return {"profile": args.profile, "M": case.M, "steps": args.steps, "warmup": args.warmup}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -751,6 +807,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-timed-s", type=float, default=1.0,
                     help="repeat the timed region of K steps until the regions cover this many seconds")
+    ap.add_argument("--profile", default=None, choices=["lora", "dora", "mlp", "qkv", "w8a8"],
+                    help="profiling aid: run only W + K steps of this workload (no timing, no context) so that a "
+                         "profiler's launch list holds just those kernels")
+    ap.add_argument("--profile-m", type=int, default=0, help="token rows of the --profile workload (0: its own)")
     ap.add_argument("--only", default=None, choices=["dora", "mlp", "w8a8", "qkv", "dropout"],
                     help="time one non-headline workload alone (for profiling) and print its record")
     args = ap.parse_args()
@@ -781,6 +841,9 @@ def main():
     from dora_adapter_linear_gb300 import ops
 
     peaks = measured_peaks()
+    if args.profile:
+        print(json.dumps(profile_steps(args, ops)), flush=True)
+        return
     if args.only:
         print(json.dumps(extra_workloads(args, L, ops, peaks, which=(args.only,))), flush=True)
         return

@@ -443,9 +443,8 @@ __device__ __forceinline__ void kscale_tile_inplace(uint8_t* a_tile, const float
 // 4 scaling warps (warps 6..9) then multiply the tile in place, 16-byte chunk by chunk, and hand
 // the stage to the MMA through `ready` (one arrival per warp, made by its lane 0; rank-r tail
 // stages pass through unscaled).  No scaled copy of dY exists anywhere.  The scaling reads and
-// writes every A tile once more in shared memory; the one-CTA tile already uses most of an SM's
-// shared-memory bandwidth, so this mode runs by default on the CTA pair, whose SMs stage half as
-// much of B.
+// writes every A tile once more in shared memory.  It runs on the one-CTA kernel (the CTA pair
+// with the same scaling warps measured 1.7x slower).
 template <int EPI, bool KSCALE = false>
 struct OneCta {
   static constexpr bool EPI8 = EPI == EPI_SCALE_BIAS && !KSCALE;
@@ -538,8 +537,8 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
             break;
           }
           const bool tail = HAS_TAIL && ks >= nk0;
-          // the W8A8 tail stages only the rank-r B rows of this tile (no second stacked half); with
-          // K-scaling the loader warps fill the A tile of a main step
+          // the W8A8 tail stages only the rank-r B rows of this tile (no second stacked half); a
+          // K-scaled main step also brings the 64 scales of its K range
           mbar_expect_tx(&full[stage], (EPI == EPI_W8A8 && tail) ? A_STAGE_BYTES + BNB * 128
                                        : ((KSCALE && !tail) ? L::STAGE_BYTES + L::KSC_BYTES : L::STAGE_BYTES));
           armed |= 1u << stage;
@@ -1157,16 +1156,10 @@ static bool use_pair(int mode) {
   const char* e = getenv("LORA_GB300_GEMM_PAIR");
   if (e && *e) return atoi(e) != 0;
   // measured over LLM layer shapes: the pair is 4-7% faster on the K-major products; on the
-  // MN-major dX products (one-CTA 168 us against 174 us for the pair at 8192 x 4096 x 4096) and
-  // the fused W8A8 output path the one-CTA kernel is as fast or faster
+  // MN-major dX products (one-CTA 168 us against 174 us for the pair at 8192 x 4096 x 4096; with
+  // the DoRA K-scaling 0.776 ms against 1.309 ms at 8192 x 11008 x 4096) and the fused W8A8 output
+  // path the one-CTA kernel is as fast or faster
   return mode == TC_FWD || mode == TC_SWIGLU_FWD;
-}
-
-// The K-scaled dX product runs on the CTA pair by default (measured: as fast as the one-CTA
-// kernel on the DoRA workload, 0.776 ms, with a third less L2 traffic for B per SM).
-static bool use_pair_kscale() {
-  const char* e = getenv("LORA_GB300_GEMM_PAIR");
-  return (e && *e) ? atoi(e) != 0 : true;
 }
 
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
