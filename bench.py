@@ -348,7 +348,7 @@ def rank_pass_roofline(L, peaks):
     if n == 0 or ms <= 0:
         return None
     ach = by / (ms * 1e-3) / 1e9
-    return {"kernels": "rowproj_kernel / colreduce_kernel (rank-r passes)", "bound": "hbm",
+    return {"kernels": "rowproj_kernel / rowcol_kernel / colreduce_kernel (rank-r passes)", "bound": "hbm",
             "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(ach / peaks["hbm_gbs"], 4), "launches": n, "avg_launch_ms": round(ms / n, 4),
             "bytes_per_launch": by / n}

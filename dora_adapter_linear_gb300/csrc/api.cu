@@ -98,20 +98,30 @@ struct LinBwdWs {
   float* PB;     // [splitsB, out, r]
   float* PA;     // [splitsA, in, r]
   float* csum;   // [splitsB, out]
+  float* Gp;     // [rc.pn, M, r] row partials of G (one pass over dY for G and the dB partials)
+  RowColPlan rc; // pm == 0: G and the dB partials take a pass over dY each
   int splitsB, splitsA;
 };
+// ranks whose dY side runs as one pass (G and the dB partials together)
+inline bool rowcol_rank(int r) { return r == 8 || r == 16 || r == 24 || r == 32; }
 size_t plan_lin_bwd(const lora_shape& sh, char* base, LinBwdWs* w) {
   Carve c{base};
   const size_t es = sh.dtype == LORA_BF16 ? 2 : 4;
   w->err = c.take<uint32_t>(kErrBytes / 4);
   w->Gs = c.take<char>((size_t)sh.M * sh.r * es);
   w->Zrec = c.take<char>((size_t)sh.M * sh.r * es);
+  w->rc = RowColPlan{};
+  w->Gp = nullptr;
   if (sh.dtype == LORA_BF16) {
-    w->splitsB = colreduce_splits(sh.M, sh.d_out);
+    const char* rc_env = getenv("LORA_GB300_ROWCOL");   // 0: one pass over dY for each of G and dB
+    if (rowcol_rank((int)sh.r) && sh.M > 0 && !(rc_env && atoi(rc_env) == 0))
+      w->rc = rowcol_plan(sh.M, sh.d_out, (int)sh.r);
+    w->splitsB = w->rc.pm > 0 ? w->rc.pm : colreduce_splits(sh.M, sh.d_out);
     w->splitsA = colreduce_splits(sh.M, sh.d_in);
     w->PB = c.take<float>((size_t)w->splitsB * sh.d_out * sh.r);
     w->PA = c.take<float>((size_t)w->splitsA * sh.d_in * sh.r);
     w->csum = c.take<float>((size_t)w->splitsB * sh.d_out);
+    if (w->rc.pm > 0) w->Gp = c.take<float>((size_t)w->rc.pn * sh.M * sh.r);
   } else {
     w->splitsB = w->splitsA = 1;
     w->PB = w->PA = nullptr;
@@ -652,16 +662,38 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       CK(rowproj(d, st));
       Z = w.Zrec;
     }
-    {  // dB partials (dY^T Z) and column sums of dY, one pass over dY
-      ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
+    if (w.rc.pm > 0) {  // one pass over dY: G row partials, dB partials (dY^T Z), column sums of dY
+      RowColDesc d;
+      d.rows = M;
+      d.K = out;
+      d.R = r;
+      d.S = static_cast<const bf16*>(dY);
+      d.lds = out;
+      d.U = static_cast<const bf16*>(B);
+      d.ldu = r;
+      d.T = static_cast<const bf16*>(Z);
+      d.ldt = r;
+      d.gpart = w.Gp;
+      d.part = w.PB;
       d.colsum = dbias ? w.csum : nullptr;
-      CK(colreduce(d, st));
-    }
-    {  // s*G = s * dY B
-      RowProjDesc d = rp_desc(M, out, r, dY, B, true, w.err);
-      d.out_b = static_cast<bf16*>(w.Gs);
-      d.scale_b = s;
-      CK(rowproj(d, st));
+      d.pm = w.rc.pm;
+      d.pn = w.rc.pn;
+      d.nb = w.rc.nb;
+      d.err = w.err;
+      CK(rowcol(d, st));
+      CK(gpart_sum(w.Gp, w.rc.pn, M, r, s, static_cast<bf16*>(w.Gs), st));   // s*G = s * dY B
+    } else {
+      {  // dB partials (dY^T Z) and column sums of dY, one pass over dY
+        ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
+        d.colsum = dbias ? w.csum : nullptr;
+        CK(colreduce(d, st));
+      }
+      {  // s*G = s * dY B
+        RowProjDesc d = rp_desc(M, out, r, dY, B, true, w.err);
+        d.out_b = static_cast<bf16*>(w.Gs);
+        d.scale_b = s;
+        CK(rowproj(d, st));
+      }
     }
     if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, nullptr, w.err), st));
     CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA, w.err), st));

@@ -346,6 +346,15 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
       : "memory");
   return r != 0;
 }
+// A consumer warp hands a ring stage back to its producer: every lane's shared-memory reads of
+// the stage are performed (a CTA-scope fence in each lane) before lane 0's arrival lets the next
+// tensor copy overwrite it.  Without the fence an arrival was seen to overtake the warp's last
+// ldmatrix reads of a stage, which then read the following tile's bytes.
+__device__ __forceinline__ void warp_release(uint64_t* bar, int lane) {
+  __threadfence_block();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

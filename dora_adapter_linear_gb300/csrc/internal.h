@@ -82,7 +82,7 @@ struct TcGemmDesc {
   int32_t* acc_out = nullptr;
   uint32_t* err = nullptr;
   uint64_t timeout_ns = 2000000000ull;
-  int max_ctas = 0;
+  int max_ctas = 0;            // cap on the persistent grid in CTAs (0: one per SM)
   int act = 0;                 // gated MLP activation: 0 SwiGLU, 1 GeGLU
 };
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st);
@@ -141,6 +141,39 @@ struct ColReduceDesc {
 };
 int colreduce_splits(int64_t rows, int64_t K);
 cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st);
+
+// One pass over S [rows, K] for both rank-r products that read it:
+//   gpart[bn][row][j] = sum_{k in column group bn} S[row, k] U[k, j]   (U [K, R], ld ldu; when U is set)
+//   part[(bm K + k) ldp + j0 + j] = sum_{row in row group bm} S[row, k] T[row, j]   (T [rows, R], ld ldt)
+//   colsum[bm][k] = sum_{row in row group bm} S[row, k]                 (when colsum is set)
+// R in {8, 16, 24, 32}.  The grid is pm row groups of nb 128-row blocks x pn column groups of 512
+// columns, from rowcol_plan; gpart is [pn, rows, R] fp32 (summed by gpart_sum), part and colsum
+// have the colreduce layout with splits = pm.
+struct RowColPlan {
+  int pm = 0, pn = 0, nb = 0;
+};
+RowColPlan rowcol_plan(int64_t rows, int64_t K, int R);
+struct RowColDesc {
+  int64_t rows = 0, K = 0;
+  int R = 0;
+  const bf16* S = nullptr;
+  int64_t lds = 0;
+  const bf16* U = nullptr;
+  int64_t ldu = 0;
+  const bf16* T = nullptr;
+  int64_t ldt = 0;
+  float* gpart = nullptr;
+  float* part = nullptr;
+  int ldp = 0;
+  int j0 = 0;
+  float* colsum = nullptr;
+  int pm = 0, pn = 0, nb = 0;
+  uint32_t* err = nullptr;
+  uint64_t timeout_ns = 2000000000ull;
+};
+cudaError_t rowcol(const RowColDesc& d, cudaStream_t st);
+// out [rows, R] = bf16(scale * sum over the pn partials of gpart)
+cudaError_t gpart_sum(const float* gpart, int pn, int64_t rows, int R, float scale, bf16* out, cudaStream_t st);
 
 // ------------------------------------------------------------------ small kernels (templated on T)
 template <typename T>

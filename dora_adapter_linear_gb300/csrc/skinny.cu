@@ -173,8 +173,7 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    warp_release(&empty[s], lane);
   }
 
   // add the other K groups' sums into K group 0, which writes the outputs
@@ -424,8 +423,7 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
         if (HAS_Y) cdot += sv * __bfloat162float(*reinterpret_cast<const bf16*>(tile + C::OFF_Y + o));
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    warp_release(&empty[s], lane);
   }
 
   // ------------------------------------------------------------------ partials of this split
@@ -560,6 +558,362 @@ cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st) {
   }
 #undef CR_CASE
   return cudaErrorInvalidValue;
+}
+
+// ============================================================================ rowcol
+// One pass over S [rows, K] for the two rank-r products that read it (the backward's dY side):
+//   row products    gpart[bn][row][j] = sum over the columns k of column group bn of S[row, k] U[k, j]
+//   column products part[bm][k][j]    = sum over the rows of row group bm of S[row, k] T[row, j]
+//   (+ column sums  colsum[bm][k]     = sum over the same rows of S[row, k])
+// with U [K, R] (row k contiguous) and T [rows, R].  The CTAs form a pm x pn grid of at most one
+// wave: CTA (bm, bn) owns nb row blocks of 128 rows and the 512 columns of column group bn, and
+// streams its 128 x 64 tiles of S (two 64-row TMA boxes), row block by row block, through a TMA
+// ring; each stage also carries the T rows of its tile, and the CTA's U rows stay resident in
+// shared memory.  (One CTA per SM with 8 KB stages streamed at 3 TB/s; 16 KB stages reach the
+// rate of several CTAs per SM.)  Two groups of four consumer warps take alternate column chunks:
+// warp i of a group forms rows 32i.. of the row product and columns 16i.. of the column product
+// of each tile, both with the warp MMA straight from the swizzled tile (and a ones operand for
+// the column sums).  A row block's two group partials meet in shared memory and go out as one
+// fp32 partial; the column partials stay in registers until the CTA is done.  gpart is summed
+// over bn by gpart_sum, part over bm by the gradient finalisation.
+namespace rc {
+constexpr int TR = 128;           // rows per tile (two 64-row boxes)
+constexpr int TC = 64;            // columns per tile (one 128-byte swizzle row)
+constexpr int CN = 512;           // columns per CTA
+constexpr int NCH = CN / TC;      // column chunks per row block
+constexpr int S_BYTES = TR * 128;
+constexpr int NST = 6;            // ring depth (stages)
+
+template <int R>
+struct Cfg {
+  static constexpr int RPAD = R <= 8 ? 8 : (R <= 16 ? 16 : 32);
+  static constexpr int PITCH = RPAD * 2;
+  static constexpr int MASK = RPAD == 8 ? 0 : RPAD == 16 ? 1 : 3;
+  static constexpr int SWZ = RPAD == 8 ? 0 : RPAD * 2;
+  static constexpr int T_BYTES = TR * RPAD * 2;
+  static constexpr int STAGE = S_BYTES + (T_BYTES + 1023) / 1024 * 1024;
+  static constexpr int U_BYTES = CN * RPAD * 2;
+  static constexpr int NTW = R / 8;                          // n-tiles of 8 output columns
+  static constexpr int RED = 2 * 4 * 32 * 2 * NTW * 4 * 4;   // two slots of group 1's row partials
+  static constexpr int OFF_U = NST * STAGE;
+  static constexpr int OFF_RED = OFF_U + U_BYTES;
+  static constexpr int OFF_BAR = OFF_RED + RED;
+  static constexpr int SMEM = OFF_BAR + (2 * NST + 1) * 8 + 16 + 1024;
+  static constexpr int THREADS = 32 * 9;                     // 8 consumer warps + the producer
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+}  // namespace rc
+
+struct RcParams {
+  CUtensorMap tmS;
+  CUtensorMap tmU;
+  CUtensorMap tmT;
+  RowColDesc d;
+};
+
+template <int R, bool ROW, bool SUMS>
+__global__ void __launch_bounds__(rc::Cfg<R>::THREADS, 1) rowcol_kernel(const __grid_constant__ RcParams P) {
+  using namespace rc;
+  using rp::swz;
+  using C = Cfg<R>;
+  constexpr int NTW = C::NTW;
+  const RowColDesc& d = P.d;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sUr = smem + C::OFF_U;
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + NST;
+  uint64_t* ubar = empty + NST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ubar + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bm = blockIdx.x / d.pn, bn = blockIdx.x % d.pn;
+  const int64_t r0 = (int64_t)bm * d.nb * TR;
+  const int64_t nblk_total = (d.rows + TR - 1) / TR;
+  const int nb = (int)min((int64_t)d.nb, nblk_total - (int64_t)bm * d.nb);   // row blocks of this CTA
+  const int c0 = bn * CN;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 4);
+    }
+    mbar_init(ubar, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  pdl_wait();      // S, U and T may come from the previous kernel in the stream
+  if (threadIdx.x == 0) pdl_trigger();
+
+  if (warp == 8) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&P.tmS);
+      tma_prefetch_desc(&P.tmT);
+      if (ROW) {
+        tma_prefetch_desc(&P.tmU);
+        mbar_expect_tx(ubar, C::U_BYTES);
+        tma_load_2d(sUr, &P.tmU, ubar, 0, c0);
+        tma_load_2d(sUr + C::U_BYTES / 2, &P.tmU, ubar, 0, c0 + CN / 2);
+      }
+      const int n = nb * NCH;
+      for (int q = 0; q < n; ++q) {
+        const int s = q % NST;
+        const uint32_t ph = (uint32_t)(q / NST) & 1u;
+        if (q >= NST && !mbar_wait(&empty[s], ph ^ 1u, d.timeout_ns, abort_flag, d.err, 0x321)) break;
+        uint8_t* st = smem + s * C::STAGE;
+        const int y = (int)(r0 + (int64_t)(q / NCH) * TR);
+        const int x = c0 + (q % NCH) * TC;
+        mbar_expect_tx(&full[s], S_BYTES + C::T_BYTES);
+        tma_load_2d(st, &P.tmS, &full[s], x, y);
+        tma_load_2d(st + S_BYTES / 2, &P.tmS, &full[s], x, y + TR / 2);
+        tma_load_2d(st + S_BYTES, &P.tmT, &full[s], 0, y);
+      }
+      if (*abort_flag) spin_ns(100000ull);  // unwind: let copies already issued land
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int grp = warp >> 2;      // chunks grp, grp + 2, ...
+  const int wi = warp & 3;        // rows 32 wi.. of the row product, columns 16 wi.. of the column product
+  const int g = lane >> 2, t = lane & 3;
+  constexpr uint32_t ONES = 0x3F803F80u;   // two bf16 1.0
+  float accP[NCH / 2][NTW][4];
+  float accS[NCH / 2][4];
+#pragma unroll
+  for (int j = 0; j < NCH / 2; ++j) {
+#pragma unroll
+    for (int q = 0; q < NTW; ++q) accP[j][q][0] = accP[j][q][1] = accP[j][q][2] = accP[j][q][3] = 0.f;
+    accS[j][0] = accS[j][1] = accS[j][2] = accS[j][3] = 0.f;
+  }
+  // every lane waits on the barriers itself: the tensor-copy writes are visible to the threads
+  // that observe the phase completion
+  bool ok = true;
+  if (ROW) ok = __all_sync(0xffffffffu, mbar_wait(ubar, 0, d.timeout_ns, abort_flag, d.err, 0x322));
+  const uint32_t sU = smem_u32(sUr);
+  for (int b = 0; b < nb; ++b) {
+    float accG[2][NTW][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int q = 0; q < NTW; ++q) accG[mt][q][0] = accG[mt][q][1] = accG[mt][q][2] = accG[mt][q][3] = 0.f;
+#pragma unroll
+    for (int j = 0; j < NCH / 2; ++j) {
+      const int ch = 2 * j + grp;
+      const int q = b * NCH + ch;
+      const int s = q % NST;
+      const uint32_t ph = (uint32_t)(q / NST) & 1u;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[s], ph, d.timeout_ns, abort_flag, d.err, 0x323));
+      if (!ok) continue;
+      const uint32_t sS = smem_u32(smem + s * C::STAGE);
+      const uint32_t sT = sS + S_BYTES;
+      if (ROW) {   // rows 32 wi.. of the tile times U rows ch*64 ..
+#pragma unroll
+        for (int kk = 0; kk < TC / 16; ++kk) {
+          uint32_t a0[4], a1[4];
+          ldsm_x4(a0[0], a0[1], a0[2], a0[3], sS + swz(wi * 32 + (lane & 15), kk * 2 + (lane >> 4), 128, 7));
+          ldsm_x4(a1[0], a1[1], a1[2], a1[3], sS + swz(wi * 32 + 16 + (lane & 15), kk * 2 + (lane >> 4), 128, 7));
+          const int krow = ch * TC + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+          for (int n = 0; n < NTW; n += 2) {
+            uint32_t b0, b1, b2 = 0, b3 = 0;
+            if (n + 1 < NTW) ldsm_x4_t(b0, b1, b2, b3, sU + swz(krow, n + (lane >> 4), C::PITCH, C::MASK));
+            else ldsm_x2_t(b0, b1, sU + swz(krow, n, C::PITCH, C::MASK));
+            mma_bf16_16816(accG[0][n], a0, b0, b1);
+            mma_bf16_16816(accG[1][n], a1, b0, b1);
+            if (n + 1 < NTW) {
+              mma_bf16_16816(accG[0][n + 1], a0, b2, b3);
+              mma_bf16_16816(accG[1][n + 1], a1, b2, b3);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < TR / 16; ++kk) {   // columns 16 wi.. of the tile (rows of S^T) times its T rows
+        uint32_t a[4];
+        const int row = kk * 16 + (lane & 7) + ((lane >> 4) << 3);
+        ldsm_x4_t(a[0], a[1], a[2], a[3], sS + swz(row, wi * 2 + ((lane >> 3) & 1), 128, 7));
+        const int trow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int n = 0; n < NTW; n += 2) {
+          uint32_t b0, b1, b2 = 0, b3 = 0;
+          if (n + 1 < NTW) ldsm_x4_t(b0, b1, b2, b3, sT + swz(trow, n + (lane >> 4), C::PITCH, C::MASK));
+          else ldsm_x2_t(b0, b1, sT + swz(trow, n, C::PITCH, C::MASK));
+          mma_bf16_16816(accP[j][n], a, b0, b1);
+          if (n + 1 < NTW) mma_bf16_16816(accP[j][n + 1], a, b2, b3);
+        }
+        if (SUMS) mma_bf16_16816(accS[j], a, ONES, ONES);   // every output column = the column sum
+      }
+      warp_release(&empty[s], lane);
+    }
+    if (ROW) {
+      // the two groups' row partials of this block meet in shared memory (slot b & 1; a slot is
+      // written again two blocks later, after group 0 has passed the next barrier)
+      float* slot = red + ((((b & 1) * 4 + wi) * 32 + lane) * 2 * NTW * 4);
+      if (grp == 1) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int n = 0; n < NTW; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) slot[(mt * NTW + n) * 4 + e] = accG[mt][n][e];
+      }
+      named_bar_sync(1, 256);
+      if (grp == 0 && ok) {
+        float* gp = d.gpart + (int64_t)bn * d.rows * R;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+          for (int n = 0; n < NTW; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accG[mt][n][e] += slot[(mt * NTW + n) * 4 + e];
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int64_t grow = r0 + (int64_t)b * TR + wi * 32 + mt * 16 + g + hr * 8;
+            if (grow >= d.rows) continue;
+#pragma unroll
+            for (int n = 0; n < NTW; ++n)
+              *reinterpret_cast<float2*>(gp + grow * R + n * 8 + 2 * t) =
+                  make_float2(accG[mt][n][2 * hr], accG[mt][n][2 * hr + 1]);
+          }
+        }
+      }
+    }
+  }
+  if (!ok) return;
+
+  // ------------------------------------------------------------------ column partials of this row group
+  const int64_t ldp = d.ldp > 0 ? d.ldp : R;
+  float* part = d.part + ((int64_t)bm * d.K) * ldp + d.j0;
+#pragma unroll
+  for (int j = 0; j < NCH / 2; ++j) {
+    const int64_t kb = (int64_t)c0 + (2 * j + grp) * TC + wi * 16;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int64_t k = kb + g + hr * 8;
+      if (k >= d.K) continue;
+#pragma unroll
+      for (int n = 0; n < NTW; ++n)
+        *reinterpret_cast<float2*>(part + k * ldp + n * 8 + 2 * t) = make_float2(accP[j][n][2 * hr], accP[j][n][2 * hr + 1]);
+      if (SUMS && t == 0 && d.colsum) d.colsum[(int64_t)bm * d.K + k] = accS[j][2 * hr];
+    }
+  }
+}
+
+RowColPlan rowcol_plan(int64_t rows, int64_t K, int R) {
+  RowColPlan p;
+  const int64_t pn = (K + rc::CN - 1) / rc::CN;
+  const int64_t blocks = (rows + rc::TR - 1) / rc::TR;
+  const int64_t sms = num_sms_current();
+  // one CTA per SM; cost in tile times: the waves times the longest CTA's tiles plus a ring fill,
+  // plus the fp32 partials written in both directions (a 128 x 64 bf16 tile is 16 KB)
+  double best = 1e30;
+  p.pn = (int)pn;
+  p.pm = 1;
+  p.nb = (int)(blocks > 0 ? blocks : 1);
+  for (int64_t nb = 1; nb <= (blocks > 0 ? blocks : 1); ++nb) {
+    const int64_t pm = (blocks + nb - 1) / nb;
+    const int64_t waves = (pm * pn + sms - 1) / sms;
+    const double partial = 4.0 * R * (double)(pm * K + pn * rows) / (16384.0 * (double)sms);
+    const double t = (double)waves * (double)(nb * rc::NCH + 4) + partial;
+    if (t < best - 1e-9) {
+      best = t;
+      p.pm = (int)pm;
+      p.nb = (int)nb;
+    }
+  }
+  return p;
+}
+
+template <int R, bool ROW, bool SUMS>
+static cudaError_t rowcol_launch(const RowColDesc& d, cudaStream_t st) {
+  using C = rc::Cfg<R>;
+  auto k = rowcol_kernel<R, ROW, SUMS>;
+  static bool set = false;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  RcParams P;
+  memset(&P, 0, sizeof(P));
+  P.d = d;
+  bool ok = make_tmap_bf16(&P.tmS, d.S, (uint64_t)d.K, (uint64_t)d.rows, (uint64_t)d.lds, rc::TC, rc::TR / 2, 128);
+  ok = ok && make_tmap_bf16(&P.tmT, d.T, R, (uint64_t)d.rows, (uint64_t)d.ldt, C::RPAD, rc::TR, C::SWZ);
+  if (ROW) ok = ok && make_tmap_bf16(&P.tmU, d.U, R, (uint64_t)d.K, (uint64_t)d.ldu, C::RPAD, rc::CN / 2, C::SWZ);
+  else P.tmU = P.tmT;
+  if (!ok) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)(d.pm * d.pn), 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  // algorithmic HBM bytes: S once, U and T once, the fp32 partials (and column sums)
+  const double bytes = 2.0 * d.rows * d.K + 2.0 * R * (d.K + d.rows) +
+                       4.0 * R * ((double)d.pm * d.K + (ROW ? (double)d.pn * d.rows : 0.0)) +
+                       (SUMS ? 4.0 * d.pm * d.K : 0.0);
+  prof_mark(st, true, bytes, 1);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, P);
+  prof_mark(st, false, 0.0, 1);
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t rowcol(const RowColDesc& d, cudaStream_t st) {
+  if (d.rows <= 0 || d.K <= 0) return cudaSuccess;
+  if (d.pm <= 0 || d.pn != (int)((d.K + rc::CN - 1) / rc::CN) || d.nb <= 0 ||
+      (int64_t)d.pm * d.nb * rc::TR < d.rows || (d.U != nullptr) != (d.gpart != nullptr))
+    return cudaErrorInvalidValue;
+  const bool row = d.U != nullptr, sums = d.colsum != nullptr;
+#define RC_CASE(RR)                                                              \
+  case RR:                                                                       \
+    if (row) return sums ? rowcol_launch<RR, true, true>(d, st) : rowcol_launch<RR, true, false>(d, st); \
+    return sums ? rowcol_launch<RR, false, true>(d, st) : rowcol_launch<RR, false, false>(d, st);
+  switch (d.R) {
+    RC_CASE(8)
+    RC_CASE(16)
+    RC_CASE(24)
+    RC_CASE(32)
+  }
+#undef RC_CASE
+  return cudaErrorInvalidValue;
+}
+
+// out[i] = bf16(scale * sum_p gpart[p][i]) over rows * R elements (R a multiple of 8)
+__global__ void gpart_sum_kernel(const float* __restrict__ gp, int pn, int64_t n, float scale, bf16* __restrict__ out) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_trigger();
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i >= n) return;
+  float4 a = *reinterpret_cast<const float4*>(gp + i);
+  for (int p = 1; p < pn; ++p) {
+    const float4 v = *reinterpret_cast<const float4*>(gp + (int64_t)p * n + i);
+    a.x += v.x;
+    a.y += v.y;
+    a.z += v.z;
+    a.w += v.w;
+  }
+  *reinterpret_cast<uint2*>(out + i) = make_uint2(pack_bf16x2(scale * a.x, scale * a.y), pack_bf16x2(scale * a.z, scale * a.w));
+}
+
+cudaError_t gpart_sum(const float* gpart, int pn, int64_t rows, int R, float scale, bf16* out, cudaStream_t st) {
+  const int64_t n = rows * R;
+  if (n <= 0) return cudaSuccess;
+  if (R % 8 || pn <= 0) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)((n / 4 + 255) / 256), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gpart_sum_kernel, gpart, pn, n, scale, out);
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace lg

@@ -1043,7 +1043,7 @@ int pdl_attr(cudaLaunchAttribute* a) {
 }
 
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE = false>
-static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
+static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles, int max_ctas) {
   using L = Layout<EPI, false, KSCALE>;
   auto kern = tc_gemm_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
   cudaLaunchConfig_t cfg = {};
@@ -1064,6 +1064,7 @@ static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
   // test knob: cap the persistent grid so that small problems still run several tiles per CTA
   const int cap = env_int("LORA_GB300_MAX_CTAS", 0);
   if (cap > 0 && cap < units) units = cap;
+  if (max_ctas > 0 && max_ctas < units) units = max_ctas;
   if (units > tiles) units = tiles;
   cfg.gridDim = dim3(units, 1, 1);
   cfg.numAttrs += (unsigned)pdl_attr(&attr[cfg.numAttrs]);
@@ -1073,7 +1074,7 @@ static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles) {
 }
 
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE = false>
-static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
+static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles, int max_ctas) {
   using L = Layout<EPI, true, KSCALE>;
   auto kern = tc_pair_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
   static int max_clusters_dev[64] = {0};   // co-resident clusters, per device
@@ -1109,6 +1110,7 @@ static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
   int clusters = max_clusters;     // persistent: every cluster resident at once
   const int cap = env_int("LORA_GB300_MAX_CTAS", 0) / 2;
   if (cap > 0 && cap < clusters) clusters = cap;
+  if (max_ctas > 1 && max_ctas / 2 < clusters) clusters = max_ctas / 2;
   if (clusters > tiles) clusters = tiles;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.numAttrs += (unsigned)pdl_attr(&attr[cfg.numAttrs]);
@@ -1119,33 +1121,34 @@ static cudaError_t launch_pair(const TcParams& p, cudaStream_t st, int tiles) {
 
 // kind: 0 one CTA, 1 CTA pair
 template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE = false>
-static cudaError_t launch_variant(const TcParams& p, cudaStream_t st, int kind, int tiles) {
-  if (kind == 1) return launch_pair<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles);
-  return launch_one<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles);
+static cudaError_t launch_variant(const TcParams& p, cudaStream_t st, int kind, int tiles, int max_ctas) {
+  if (kind == 1) return launch_pair<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles, max_ctas);
+  return launch_one<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>(p, st, tiles, max_ctas);
 }
 
 static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStream_t st, int kind, int tiles) {
+  const int mc = d.max_ctas;
   switch (d.mode) {
     case TC_FWD:
-      if (d.has_tail) return launch_variant<false, false, true, false, EPI_SCALE_BIAS>(p, st, kind, tiles);
-      return launch_variant<false, false, false, false, EPI_SCALE_BIAS>(p, st, kind, tiles);
+      if (d.has_tail) return launch_variant<false, false, true, false, EPI_SCALE_BIAS>(p, st, kind, tiles, mc);
+      return launch_variant<false, false, false, false, EPI_SCALE_BIAS>(p, st, kind, tiles, mc);
     case TC_BWD_DX:
       if (d.a_kscale) {   // A tiles scaled in shared memory by the scaling warps
-        if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS, true>(p, st, kind, tiles);
-        return launch_variant<true, false, false, true, EPI_SCALE_BIAS, true>(p, st, kind, tiles);
+        if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS, true>(p, st, kind, tiles, mc);
+        return launch_variant<true, false, false, true, EPI_SCALE_BIAS, true>(p, st, kind, tiles, mc);
       }
-      if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS>(p, st, kind, tiles);
-      return launch_variant<true, false, false, true, EPI_SCALE_BIAS>(p, st, kind, tiles);
+      if (d.has_tail) return launch_variant<true, false, true, true, EPI_SCALE_BIAS>(p, st, kind, tiles, mc);
+      return launch_variant<true, false, false, true, EPI_SCALE_BIAS>(p, st, kind, tiles, mc);
     case TC_SWIGLU_FWD:
-      return launch_variant<false, true, true, false, EPI_SWIGLU>(p, st, kind, tiles);
+      return launch_variant<false, true, true, false, EPI_SWIGLU>(p, st, kind, tiles, mc);
     case TC_SWIGLU_BWD:
-      return launch_variant<true, false, true, true, EPI_SWIGLU_BWD>(p, st, kind, tiles);
+      return launch_variant<true, false, true, true, EPI_SWIGLU_BWD>(p, st, kind, tiles, mc);
     case TC_W8A8F:
-      if (d.has_tail) return launch_variant<false, true, true, false, EPI_W8A8F>(p, st, kind, tiles);
-      return launch_variant<false, true, false, false, EPI_W8A8F>(p, st, kind, tiles);
+      if (d.has_tail) return launch_variant<false, true, true, false, EPI_W8A8F>(p, st, kind, tiles, mc);
+      return launch_variant<false, true, false, false, EPI_W8A8F>(p, st, kind, tiles, mc);
     case TC_W8A8:  // one-CTA kernel only (its accumulator layout is per-CTA)
-      if (d.has_tail) return launch_one<false, true, true, false, EPI_W8A8>(p, st, tiles);
-      return launch_one<false, true, false, false, EPI_W8A8>(p, st, tiles);
+      if (d.has_tail) return launch_one<false, true, true, false, EPI_W8A8>(p, st, tiles, mc);
+      return launch_one<false, true, false, false, EPI_W8A8>(p, st, tiles, mc);
   }
   return cudaErrorInvalidValue;
 }

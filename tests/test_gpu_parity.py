@@ -87,6 +87,20 @@ def test_lora_bwd_bf16(ops, r):
     assert_close(dbias, rb[None, :], "bf16", "dbias")
 
 
+@pytest.mark.parametrize("r", [8, 16, 24, 32])
+def test_lora_bwd_one_dy_pass_grid(ops, r):
+    """dY side in one pass at a size whose CTA grid has several 64-row blocks per CTA and
+    several 512-column groups, with a ragged last row block and a ragged last column chunk."""
+    case, t, g = lin_inputs("lora_4096_bf16", M=13000, d_in=136, d_out=1096, r=r)
+    _, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s)
+    dX, dA, dB, dbias = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], Z, g["dY"], case.s, need_dbias=True)
+    rX, rA, rB, rb = O.lora_linear_bwd(*(f64(t[k]) for k in ("X", "W0", "A", "B")), case.s, f64(t["dY"]))
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dB, rB, "bf16", "dB")
+    assert_close(dbias, rb[None, :], "bf16", "dbias")
+
+
 def test_lora_bwd_recomputes_z(ops):
     case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=16)
     dX, dA, dB, _ = ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], None, g["dY"], case.s)
