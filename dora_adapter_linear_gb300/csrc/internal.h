@@ -83,6 +83,14 @@ struct TcGemmDesc {
   uint32_t* err = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int max_ctas = 0;            // cap on the persistent grid in CTAs (0: one per SM)
+  // forward with the down-projection in the GEMM (TC_FWD, has_tail, K1 = dn_r in 8 .. 32): Z =
+  // A0 dn_a^T is formed from the staged A0 tiles (dn_a [dn_r, K0], row stride dn_lda), the tail's
+  // A operand is bf16(dn_s Z) written on chip (A1 unused), and bf16(Z) goes to dn_z [M, dn_r] when set
+  const bf16* dn_a = nullptr;
+  int64_t dn_lda = 0;
+  float dn_s = 0.f;
+  int dn_r = 0;
+  bf16* dn_z = nullptr;
   int act = 0;                 // gated MLP activation: 0 SwiGLU, 1 GeGLU
 };
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st);

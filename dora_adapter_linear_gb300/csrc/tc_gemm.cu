@@ -56,6 +56,13 @@ struct TcParams {
   int write_y;          // W8A8: 0 when only the raw product is wanted
   int pair_leader_arms; // CTA pair: the leader posts the transaction bytes of both CTAs
   int act;              // gated MLP activation: 0 SwiGLU, 1 GeGLU
+  // down-projection in the GEMM (forward): Z = A0 dn_a^T from the staged A0 tiles, the tail's A
+  // operand bf16(dn_s Z) written into the tail stage, bf16(Z) to dn_z (the tiles of N-tile 0)
+  const bf16* dn_a;
+  int64_t dn_lda;
+  float dn_s;
+  int dn_r;
+  bf16* dn_z;
   uint32_t* err;
   uint64_t timeout_ns;
 };
@@ -445,16 +452,18 @@ __device__ __forceinline__ void kscale_tile_inplace(uint8_t* a_tile, const float
 // stages pass through unscaled).  No scaled copy of dY exists anywhere.  The scaling reads and
 // writes every A tile once more in shared memory.  It runs on the one-CTA kernel (the CTA pair
 // with the same scaling warps measured 1.7x slower).
-template <int EPI, bool KSCALE = false>
+template <int EPI, bool KSCALE = false, bool ZF = false>
 struct OneCta {
   static constexpr bool EPI8 = EPI == EPI_SCALE_BIAS && !KSCALE;
-  static constexpr int THREADS = (KSCALE || EPI8) ? 320 : 192;
+  static constexpr int THREADS = ((KSCALE || EPI8) ? 320 : 192) + (ZF ? 128 : 0);
 };
 
-template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE = false>
-__global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE = false, bool ZF = false>
+__global__ void __launch_bounds__(OneCta<EPI, KSCALE, ZF>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   static_assert(!KSCALE || (EPI == EPI_SCALE_BIAS && !STACKED), "K-scaling: plain dX products only");
-  using C = OneCta<EPI, KSCALE>;
+  static_assert(!ZF || (EPI == EPI_SCALE_BIAS && !STACKED && !B0_MN && HAS_TAIL && !B1_MN && !KSCALE),
+                "down-projection in the GEMM: the plain forward only");
+  using C = OneCta<EPI, KSCALE, ZF>;
   using L = Layout<EPI, false, KSCALE>;
   constexpr int STAGES = L::STAGES;
   constexpr int BNB = STACKED ? BN / 2 : BN;          // rows per K-major B box
@@ -487,8 +496,10 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      // down-projection: full = the producer's two arrivals on a main step, or its one plus the
+      // Z warps' on the tail step; empty = the MMA commit plus the four Z warps
+      mbar_init(&full[i], ZF ? 2 : 1);
+      mbar_init(&empty[i], ZF ? 5 : 1);
       mbar_init(&ready[i], 4);    // K-scaling: one arrival per scaling warp
     }
     for (int i = 0; i < 2; ++i) {
@@ -539,8 +550,13 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
           const bool tail = HAS_TAIL && ks >= nk0;
           // the W8A8 tail stages only the rank-r B rows of this tile (no second stacked half); a
           // K-scaled main step also brings the 64 scales of its K range
-          mbar_expect_tx(&full[stage], (EPI == EPI_W8A8 && tail) ? A_STAGE_BYTES + BNB * 128
-                                       : ((KSCALE && !tail) ? L::STAGE_BYTES + L::KSC_BYTES : L::STAGE_BYTES));
+          if constexpr (ZF) {   // the tail's A operand is written by the Z warps, not copied
+            mbar_expect_tx(&full[stage], tail ? L::B_STAGE_BYTES : L::STAGE_BYTES);
+            if (!tail) mbar_arrive(&full[stage]);
+          } else {
+            mbar_expect_tx(&full[stage], (EPI == EPI_W8A8 && tail) ? A_STAGE_BYTES + BNB * 128
+                                         : ((KSCALE && !tail) ? L::STAGE_BYTES + L::KSC_BYTES : L::STAGE_BYTES));
+          }
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           uint8_t* a_dst = sA + stage * A_STAGE_BYTES;
@@ -564,7 +580,7 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
             }
           } else {
             const int kt = (ks - nk0) * BK;   // K offset inside the rank-r tail
-            tma_load_2d(a_dst, &p.tmA1, &full[stage], kt, m0);
+            if (!ZF) tma_load_2d(a_dst, &p.tmA1, &full[stage], kt, m0);
             if (B1_MN) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &p.tmB1, &full[stage], n0 + 64 * j, kt);
@@ -695,6 +711,105 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE>::THREADS, 1) tc_gemm_kerne
           stage = 0;
           phase ^= 1;
         }
+      }
+    }
+  } else if (ZF) {
+    // ---------------------------------------------------------------- down-projection Z = A0 dn_a^T
+    // Z warp zw forms rows 32 zw .. 32 zw + 31 of the tile's Z with the warp MMA straight from each
+    // staged (128B-swizzled) A0 tile; the dn_a fragments come from global memory (L1/L2 resident),
+    // loaded while the next stage is awaited.  On the tail step it writes bf16(dn_s Z) as that step's A operand (zeros past
+    // the rank) once the stage is free, and bf16(Z) to dn_z for the tiles of N-tile 0.
+    const int zw = warp - 10;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int nzt = p.dn_r / 8;              // n-tiles of 8 (rank 8 .. 32)
+    const int64_t K0 = p.K0;
+    auto load_b = [&](int ks, uint32_t (&b)[4][4][2]) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          const int64_t k = (int64_t)ks * BK + kk * 16 + 2 * t4;
+          const bf16* row = p.dn_a + (int64_t)(n * 8 + g) * p.dn_lda;
+          const bool okn = n < nzt;
+          b[kk][n][0] = (okn && k < K0) ? __ldg(reinterpret_cast<const uint32_t*>(row + k)) : 0u;
+          b[kk][n][1] = (okn && k + 8 < K0) ? __ldg(reinterpret_cast<const uint32_t*>(row + k + 8)) : 0u;
+        }
+    };
+    // After a failed wait a warp keeps stepping through its tiles without waiting or working, so
+    // that all four still meet at the named barrier of every tail step.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = t_first; t < t_count; t += t_step) {
+      int mt, nt;
+      coords(t, mt, nt);
+      float acc[2][4][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[i][n][0] = acc[i][n][1] = acc[i][n][2] = acc[i][n][3] = 0.f;
+      uint32_t bcur[4][4][2];
+      if (ok) load_b(0, bcur);
+      for (int ks = 0; ks < nk0; ++ks) {
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.err, 0x106));
+        if (ok) {
+          const uint32_t a_base = smem_u32(sA + stage * A_STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int row = zw * 32 + i * 16 + (lane & 15);
+              const int ch = kk * 2 + (lane >> 4);
+              uint32_t a[4];
+              ldsm_x4(a[0], a[1], a[2], a[3], a_base + row * 128 + ((ch ^ (row & 7)) << 4));
+#pragma unroll
+              for (int n = 0; n < 4; ++n)
+                if (n < nzt) mma_bf16_16816(acc[i][n], a, bcur[kk][n][0], bcur[kk][n][1]);
+            }
+          }
+          warp_release(&empty[stage], lane);
+          // the next K-step's fragments, issued after the release so that its fence does not wait
+          // for them
+          if (ks + 1 < nk0) load_b(ks + 1, bcur);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // the tail step: the stage must be free (its previous MMA done) before it is written
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, p.timeout_ns, abort_flag, p.err, 0x107));
+      uint8_t* a_tile = sA + stage * A_STAGE_BYTES;
+      if (ok) {
+        const bool save = p.dn_z != nullptr && nt == 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int row = zw * 32 + i * 16 + g + 8 * hr;
+            const int64_t grow = (int64_t)mt * BM + row;
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+              if (n >= nzt) continue;
+              const float z0 = acc[i][n][2 * hr], z1 = acc[i][n][2 * hr + 1];
+              const int col = n * 8 + 2 * t4;
+              *reinterpret_cast<uint32_t*>(a_tile + row * 128 + ((n ^ (row & 7)) << 4) + (col & 7) * 2) =
+                  pack_bf16x2(z0 * p.dn_s, z1 * p.dn_s);
+              if (save && grow < p.M)
+                *reinterpret_cast<uint32_t*>(p.dn_z + grow * p.dn_r + col) = pack_bf16x2(z0, z1);
+            }
+          }
+        const int row = zw * 32 + lane;   // 16-byte chunks past the rank read as zeros
+        for (int c = nzt; c < 8; ++c)
+          *reinterpret_cast<uint4*>(a_tile + row * 128 + ((c ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();   // visible to the tensor core before the MMA is released
+      }
+      const bool all_ok = named_bar_or(2, 128, !ok) == false;
+      if (all_ok && zw == 0 && lane == 0) mbar_arrive(&full[stage]);
+      if (ok) warp_release(&empty[stage], lane);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1;
       }
     }
   }
@@ -1042,13 +1157,13 @@ int pdl_attr(cudaLaunchAttribute* a) {
   return 1;
 }
 
-template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE = false>
+template <bool B0_MN, bool STACKED, bool HAS_TAIL, bool B1_MN, int EPI, bool KSCALE = false, bool ZF = false>
 static cudaError_t launch_one(const TcParams& p, cudaStream_t st, int tiles, int max_ctas) {
   using L = Layout<EPI, false, KSCALE>;
-  auto kern = tc_gemm_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE>;
+  auto kern = tc_gemm_kernel<B0_MN, STACKED, HAS_TAIL, B1_MN, EPI, KSCALE, ZF>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(OneCta<EPI, KSCALE>::THREADS, 1, 1);
+  cfg.blockDim = dim3(OneCta<EPI, KSCALE, ZF>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = L::TOTAL;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -1130,6 +1245,7 @@ static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStrea
   const int mc = d.max_ctas;
   switch (d.mode) {
     case TC_FWD:
+      if (d.dn_a) return launch_one<false, false, true, false, EPI_SCALE_BIAS, false, true>(p, st, tiles, mc);
       if (d.has_tail) return launch_variant<false, false, true, false, EPI_SCALE_BIAS>(p, st, kind, tiles, mc);
       return launch_variant<false, false, false, false, EPI_SCALE_BIAS>(p, st, kind, tiles, mc);
     case TC_BWD_DX:
@@ -1167,7 +1283,10 @@ static bool use_pair(int mode) {
 
 cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   if (d.M <= 0 || d.N <= 0) return cudaSuccess;
-  const bool pair = use_pair(d.mode) && d.mode != TC_W8A8;
+  // the down-projection in the GEMM runs on the one-CTA kernel (ranks 8 .. 32, one tail step)
+  if (d.dn_a && (d.mode != TC_FWD || !d.has_tail || d.dn_r < 8 || d.dn_r > 32 || d.dn_r % 8 || d.K1 != d.dn_r))
+    return cudaErrorInvalidValue;
+  const bool pair = use_pair(d.mode) && d.mode != TC_W8A8 && d.dn_a == nullptr;
   TcParams p;
   memset(&p, 0, sizeof(p));
   const bool stacked = d.mode == TC_SWIGLU_FWD || d.mode == TC_W8A8 || d.mode == TC_W8A8F;
@@ -1183,8 +1302,10 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   }
   if (d.has_tail) {
     // the tail's last K-step runs over a whole BK: its columns past K1 must read as TMA zero fill
-    if (d.K1_a != d.K1) return cudaErrorInvalidValue;
-    ok = ok && make_map(&p.tmA1, d.A1, d.K1_a, d.M, d.lda1, BM);
+    if (d.dn_a == nullptr) {   // with the down-projection in the GEMM the tail's A is written on chip
+      if (d.K1_a != d.K1) return cudaErrorInvalidValue;
+      ok = ok && make_map(&p.tmA1, d.A1, d.K1_a, d.M, d.lda1, BM);
+    }
     if (d.b1_mn) ok = ok && make_map(&p.tmB1, d.B1, d.N, d.K1, d.ldb1, 64);
     else {
       ok = ok && make_map(&p.tmB1, d.B1, d.K1_b, d.N, d.ldb1, bnb);
@@ -1206,6 +1327,11 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   p.write_y = d.out[0] != nullptr ? 1 : 0;
   p.pair_leader_arms = env_int("LORA_GB300_PAIR_ARM", 1);
   p.act = d.act;
+  p.dn_a = d.dn_a;
+  p.dn_lda = d.dn_lda;
+  p.dn_s = d.dn_s;
+  p.dn_r = d.dn_r;
+  p.dn_z = d.dn_z;
 
   p.M = d.M;
   p.N = d.N;

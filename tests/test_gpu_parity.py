@@ -65,9 +65,12 @@ def test_base_gemm_mnmajor_strength0(ops):
     assert not dA.any() and not dB.any()
 
 
-@pytest.mark.parametrize("r", [8, 16, 32, 64, 96, 128])
+@pytest.mark.parametrize("r", [8, 16, 24, 32, 64, 96, 128])
 @pytest.mark.parametrize("bias", [False, True])
-def test_lora_fwd_bf16(ops, r, bias):
+@pytest.mark.parametrize("fused_z", ["1", "0"])
+def test_lora_fwd_bf16(ops, r, bias, fused_z, monkeypatch):
+    """fused_z 1: Z formed inside the GEMM (ranks 8-32, opt-in); 0: the separate down-projection pass."""
+    monkeypatch.setenv("LORA_GB300_FUSED_Z", fused_z)
     case, t, g = lin_inputs("lora_4096_bf16", **SMALL, r=r, bias=bias)
     Y, Z = ops.lora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], case.s, g["bias"])
     X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
