@@ -683,13 +683,13 @@ def _w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm):
     Wq = torch.from_numpy(Wq).to(dev)
     sw = torch.from_numpy(sw).to(dev)
 
-    # the frozen weight laid out once (split codes for the forward, dequantised copy for the
+    # the frozen weight laid out once (codes as bf16 for the forward, dequantised copy for the
     # backward), outside the timed steps like loading the model
-    Wh, Wl, Wd = ops.w8a8_prepack_weight(Wq, sw)
+    Wb, Wd = ops.w8a8_prepack_weight(Wq, sw)
 
     def w8_step():   # W-1 (codes written as bf16) + the packed product with the LoRA epilogue
         Xc, sx, Z = ops.w8a8_quantize_rows_bf16(X, A)
-        ops.w8a8_lora_fwd_packed(Xc, sx, Wh, Wl, sw, Z, B, case.s)
+        ops.w8a8_lora_fwd_packed(Xc, sx, Wb, sw, Z, B, case.s)
 
     def w8_step_int8():   # the same through the int8 interface (re-lays out codes and weight per call)
         Xq, sx, Z = ops.w8a8_quantize_rows(X, A)
@@ -707,24 +707,22 @@ def _w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm):
            "lora_tflops": lora_fl / (ms * 1e-3) / 1e12,
            "path": "w8a8_quantize_rows_bf16 + w8a8_lora_fwd_packed (weight prepacked once)",
            "int8_interface_ms_per_step": ms_int8,
-           "note": "exact int8 product as two bf16 tcgen05 products of the split weight codes "
-                   "(w = 16 (w >> 4) + (w & 15)); sm_103a has no tcgen05 int8 kind"}
+           "note": "exact int8 product on the bf16 tcgen05 tensor cores with the codes as bf16 values, "
+                   "summed exactly in fp32 over 1024-wide K chunks and added as int32 (sm_103a has no "
+                   "tcgen05 int8 kind)"}
     if gn:
-        # the method's own work per launch: the int8 product 2 M N K plus the rank-r term 2 M N r;
-        # the kernel does twice the int8 product on the bf16 tensor cores (two split-code halves)
+        # the method's own work per launch: the int8 product 2 M N K plus the rank-r term 2 M N r,
+        # which is also the bf16 tensor work the kernel does
         own = ops_int8 + 2 * case.M * case.d_out * case.r
         ach = own * gn / (gms * 1e-3) / 1e12
-        rec["roofline"] = {"kernel": "tc_gemm_kernel (W8A8 split-code mode)", "bound": "tensor",
+        rec["roofline"] = {"kernel": "tc_gemm_kernel (chunked exact W8A8 mode)", "bound": "tensor",
                            "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "T-ops/s",
                            "frac": round(ach / peaks["bf16_tflops"], 4), "launches": gn,
                            "avg_launch_ms": round(gms / gn, 4), "share_of_step": round(gms / ((steps + 1) * ms_ev), 4),
                            "ops_per_launch": own, "traffic": None,
-                           "split_factor": 2,
                            "tensor_work_per_launch": gfl / gn,
-                           "tensor_frac": round(gfl / (gms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                           "note": "achieved counts the method's own work (2 M N K int8 + 2 M N r bf16); the split "
-                                   "codes w = 16 (w >> 4) + (w & 15) make the bf16 tensor cores do 2x the int8 "
-                                   "product (tensor_frac)",
+                           "note": "achieved counts the method's own work (2 M N K int8 + 2 M N r bf16) against "
+                                   "the bf16 tensor peak, on which it runs",
                            "timing": "CUDA events around each GEMM launch in a second pass of the timed steps"}
     out["w8a8_lora_3072"] = rec
 
@@ -785,12 +783,12 @@ def profile_steps(args, ops):
         t = D.make_w8a8(case)
         Wq, sw = O.quantize_rows(t["W0"].numpy())
         X, A, B = t["X"].to(dev), t["A"].to(dev), t["B"].to(dev)
-        Wh, Wl, Wd = ops.w8a8_prepack_weight(torch.from_numpy(Wq).to(dev), torch.from_numpy(sw).to(dev))
+        Wb, Wd = ops.w8a8_prepack_weight(torch.from_numpy(Wq).to(dev), torch.from_numpy(sw).to(dev))
         swd = torch.from_numpy(sw).to(dev)
 
         def step():
             Xc, sx, Z = ops.w8a8_quantize_rows_bf16(X, A)
-            ops.w8a8_lora_fwd_packed(Xc, sx, Wh, Wl, swd, Z, B, case.s)
+            ops.w8a8_lora_fwd_packed(Xc, sx, Wb, swd, Z, B, case.s)
     for _ in range(args.warmup + args.steps):
         step()
     torch.cuda.synchronize()

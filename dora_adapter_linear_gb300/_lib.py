@@ -86,9 +86,9 @@ _SIGS = {
     "w8a8_lora_fwd": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, c_float, P, P, P, P, c_size_t,
                               P]),
     "w8a8_quantize_rows_bf16": (c_int, [c_int64, c_int64, P, P, P, P, c_int64, P, P]),
-    "w8a8_prepack_weight": (c_int, [c_int64, c_int64, P, P, P, P, P, P]),
+    "w8a8_prepack_weight": (c_int, [c_int64, c_int64, P, P, P, P, P]),
     "w8a8_packed_workspace_bytes": (c_size_t, [c_int64, c_int64]),
-    "w8a8_lora_fwd_packed": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, P, c_float, P, P, P, P,
+    "w8a8_lora_fwd_packed": (c_int, [c_int64, c_int64, c_int64, c_int64, P, P, P, P, P, P, c_float, P, P, P, P,
                                      c_size_t, P]),
     "lora_debug_wait_timeout": (c_int, [P, c_uint32, P]),
     "lora_linear_fwd_noalloc": (c_int, [POINTER(LoraShape), P, P, P, P, P, c_float, P, P, P]),
@@ -373,8 +373,8 @@ def w8a8_quantize_rows_bf16(rows, cols, X, Xcodes, sx, A=None, r=0, Z=None, stre
                                        _stream(stream)), "w8a8_quantize_rows_bf16")
 
 
-def w8a8_prepack_weight(d_out, d_in, Wq, sw, Wh, Wl, Wd, stream=None):
-    _ck(_lib().w8a8_prepack_weight(d_out, d_in, ptr(Wq), ptr(sw), ptr(Wh), ptr(Wl), ptr(Wd), _stream(stream)),
+def w8a8_prepack_weight(d_out, d_in, Wq, sw, Wb, Wd, stream=None):
+    _ck(_lib().w8a8_prepack_weight(d_out, d_in, ptr(Wq), ptr(sw), ptr(Wb), ptr(Wd), _stream(stream)),
         "w8a8_prepack_weight")
 
 
@@ -382,8 +382,8 @@ def w8a8_packed_workspace_bytes(M, d_out) -> int:
     return _lib().w8a8_packed_workspace_bytes(M, d_out)
 
 
-def w8a8_lora_fwd_packed(M, d_in, d_out, r, Xcodes, sx, Wh, Wl, sw, Z, B, s, bias, Y, acc_out, ws, stream=None):
-    _ck(_lib().w8a8_lora_fwd_packed(M, d_in, d_out, r, ptr(Xcodes), ptr(sx), ptr(Wh), ptr(Wl), ptr(sw), ptr(Z),
+def w8a8_lora_fwd_packed(M, d_in, d_out, r, Xcodes, sx, Wb, sw, Z, B, s, bias, Y, acc_out, ws, stream=None):
+    _ck(_lib().w8a8_lora_fwd_packed(M, d_in, d_out, r, ptr(Xcodes), ptr(sx), ptr(Wb), ptr(sw), ptr(Z),
                                     ptr(B), float(s), ptr(bias), ptr(Y), ptr(acc_out), ptr(ws),
                                     0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)),
         "w8a8_lora_fwd_packed")

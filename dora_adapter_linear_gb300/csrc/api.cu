@@ -487,7 +487,7 @@ const char* lora_status_string(int status) {
   return "unknown status";
 }
 
-int lora_abi_version(void) { return 7; }
+int lora_abi_version(void) { return 8; }
 
 size_t lora_workspace_bytes(int op, const lora_shape* sh) {
   if (check_shape(sh) != LORA_OK) return 0;
@@ -1608,77 +1608,46 @@ lora_status w8a8_quantize_rows(int64_t rows, int64_t cols, const void* X, int8_t
   return LORA_OK;
 }
 
-// Largest d_in for which both split partial products keep every fp32 partial sum an integer
-// below 2^24 (|x| <= 127, |w >> 4| <= 8, |w & 15| <= 15: 127 * 15 * 8800 < 2^24).
-constexpr int64_t kW8ExactMaxK = 8800;
 constexpr int64_t kW8MaxR = 128;   // largest rank of the low-rank term
+// K-steps of 64 per exactly summed chunk of the int8 product: every fp32 partial sum of a chunk is
+// an integer of magnitude at most 127 * 127 * 1024 < 2^24, hence exact
+constexpr int kW8ChunkSteps = 16;
 
 size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out) {
   if (M < 0 || d_in <= 0 || d_out <= 0) return 0;
-  // + the rank-r operands of the fused epilogue, pre-divided by the dequant scales (r <= 128)
-  return kErrBytes + al256((size_t)M * d_in * 2) + 2 * al256((size_t)d_out * d_in * 2) +
-         al256((size_t)M * kW8MaxR * 2) + al256((size_t)d_out * kW8MaxR * 2);
+  return kErrBytes + al256((size_t)M * d_in * 2) + al256((size_t)d_out * d_in * 2);
 }
 
 }  // extern "C"
 
 namespace {
-// The split-code tensor-core product and its epilogue on operands already laid out for it:
-// Xb [M, d_in] the activation codes as bf16, Wh / Wl [d_out, d_in] the weight codes' high and
-// low parts as bf16; Zt / Bt (each room for kW8MaxR columns) hold the rank-r operands divided by
-// the dequant scales when the folded output-only epilogue runs.
+// The int8 product on the bf16 tensor cores and its epilogue, on operands already laid out for it:
+// Xb [M, d_in] and Wb [d_out, d_in] the activation and weight codes as bf16 (exact: |code| <= 127).
+// The K range goes in chunks of kW8ChunkSteps K-steps, each summed exactly in its own TMEM
+// accumulator and added as int32; the rank-r term Z B^T is one more accumulator.
 lora_status w8a8_fwd_core(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const bf16* Xb, const float* sx,
-                          const bf16* Wh, const bf16* Wl, const float* sw, const void* Z, const void* B, float s,
-                          const void* bias, void* Y, int32_t* acc_out, uint32_t* err, bf16* Zt, bf16* Bt,
-                          cudaStream_t st) {
+                          const bf16* Wb, const float* sw, const void* Z, const void* B, float s, const void* bias,
+                          void* Y, int32_t* acc_out, uint32_t* err, cudaStream_t st) {
   TcGemmDesc d;
+  d.mode = TC_W8A8K;
   d.M = (int)M;
   d.N = (int)d_out;
   d.K0 = (int)d_in;
   d.A0 = Xb;
   d.lda0 = d_in;
-  d.B0 = Wh;
-  d.B0b = Wl;
+  d.B0 = Wb;
   d.ldb0 = d_in;
   d.out[0] = Y;
   d.ldo = d_out;
   d.bias = static_cast<const bf16*>(bias);
   d.sx = sx;
   d.sw = sw;
+  d.ls = s;
+  d.acc_out = acc_out;
+  d.kc_steps = kW8ChunkSteps;
   d.err = err;
   d.timeout_ns = wait_timeout_ns();
-  if (acc_out == nullptr && !env_flag("LORA_GB300_W8A8_EXACT")) {
-    // Only the dequantised output is wanted: fold the rank-r term into the low half as
-    // (s Z / sx) (B / sw)^T, so the epilogue is y = (16 hi + lo) sx sw + bias and the accumulators
-    // fit twice in TMEM (double-buffered, like every other mode).  The low half then holds the
-    // exact integer partial sum plus that term, rounded once in fp32.
-    d.mode = TC_W8A8F;
-    if (Z && s != 0.f) {
-      CK(scale_rows_recip_bf16(static_cast<const bf16*>(Z), M, (int)r, sx, s, Zt, st));
-      CK(scale_rows_recip_bf16(static_cast<const bf16*>(B), d_out, (int)r, sw, 1.f, Bt, st));
-      d.has_tail = true;
-      d.A1 = Zt;
-      d.lda1 = r;
-      d.K1 = (int)r;
-      d.K1_a = (int)r;
-      d.B1 = Bt;          // first (high) half: read past its r columns, i.e. zeros
-      d.B1b = Bt;         // second (low) half
-      d.ldb1 = r;
-      d.K1_b = (int)r;
-      d.ldb1b = r;
-      d.K1_bb = (int)r;
-      d.b1_x = kW8MaxR;   // at or past r for every tail step
-      d.b1b_x = 0;
-    }
-    CK(tc_gemm(d, st));
-    return LORA_OK;
-  }
-  d.mode = TC_W8A8;
-  d.lz = static_cast<const bf16*>(Z);
-  d.lb = static_cast<const bf16*>(B);
-  d.ls = s;
-  d.lr = Z ? (int)r : 0;
-  if (Z) {  // rank-r term Z B^T as a tail MMA into its own accumulator region
+  if (Z) {  // rank-r term Z B^T as a tail K-step into its own accumulator
     d.has_tail = true;
     d.A1 = Z;
     d.lda1 = r;
@@ -1688,7 +1657,6 @@ lora_status w8a8_fwd_core(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
     d.ldb1 = r;
     d.K1_b = (int)r;
   }
-  d.acc_out = acc_out;
   CK(tc_gemm(d, st));
   return LORA_OK;
 }
@@ -1718,7 +1686,7 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
   if ((e = check_ws(ws, ws_bytes, w8a8_workspace_bytes(M, d_in, d_out))) != LORA_OK) return e;
   if (M == 0) return LORA_OK;
   cudaStream_t st = (cudaStream_t)stream;
-  if (d_in > kW8ExactMaxK || getenv("LORA_GB300_W8A8_IMMA")) {
+  if (getenv("LORA_GB300_W8A8_IMMA")) {   // the integer warp-MMA product (s8 x s8 -> s32)
     CK(w8a8_gemm(M, d_in, d_out, Z ? (int)r : 0, Xq, sx, Wq, sw, static_cast<const bf16*>(Z),
                  static_cast<const bf16*>(B), s, static_cast<const bf16*>(bias), static_cast<bf16*>(Y), acc_out, st));
     return LORA_OK;
@@ -1726,13 +1694,10 @@ lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, con
   Carve c{static_cast<char*>(ws)};
   uint32_t* err = c.take<uint32_t>(kErrBytes / 4);
   bf16* Xb = c.take<bf16>((size_t)M * d_in);
-  bf16* Wh = c.take<bf16>((size_t)d_out * d_in);
-  bf16* Wl = c.take<bf16>((size_t)d_out * d_in);
-  bf16* Zt = c.take<bf16>((size_t)M * kW8MaxR);
-  bf16* Bt = c.take<bf16>((size_t)d_out * kW8MaxR);
+  bf16* Wb = c.take<bf16>((size_t)d_out * d_in);
   CK(i8_to_bf16(Xq, M * d_in, Xb, st));
-  CK(i8_split_bf16(Wq, d_out * d_in, Wh, Wl, st));
-  return w8a8_fwd_core(M, d_in, d_out, r, Xb, sx, Wh, Wl, sw, Z, B, s, bias, Y, acc_out, err, Zt, Bt, st);
+  CK(i8_to_bf16(Wq, d_out * d_in, Wb, st));
+  return w8a8_fwd_core(M, d_in, d_out, r, Xb, sx, Wb, sw, Z, B, s, bias, Y, acc_out, err, st);
 }
 
 lora_status w8a8_quantize_rows_bf16(int64_t rows, int64_t cols, const void* X, void* Xcodes, float* sx,
@@ -1753,42 +1718,38 @@ lora_status w8a8_quantize_rows_bf16(int64_t rows, int64_t cols, const void* X, v
   return LORA_OK;
 }
 
-lora_status w8a8_prepack_weight(int64_t d_out, int64_t d_in, const int8_t* Wq, const float* sw, void* Wh, void* Wl,
-                                void* Wd, void* stream) {
+lora_status w8a8_prepack_weight(int64_t d_out, int64_t d_in, const int8_t* Wq, const float* sw, void* Wb, void* Wd,
+                                void* stream) {
   if (d_out <= 0 || d_in <= 0) return LORA_ERR_INVALID_ARG;
   if (d_in % 32 || d_out % 8) return LORA_ERR_UNSUPPORTED;
   REQ(Wq);
-  if ((Wh == nullptr) != (Wl == nullptr)) return LORA_ERR_INVALID_ARG;
   if (Wd && !sw) return LORA_ERR_INVALID_ARG;
-  ALN(Wq); ALN(sw); ALN(Wh); ALN(Wl); ALN(Wd);
+  ALN(Wq); ALN(sw); ALN(Wb); ALN(Wd);
   cudaStream_t st = (cudaStream_t)stream;
-  if (Wh) CK(i8_split_bf16(Wq, d_out * d_in, static_cast<bf16*>(Wh), static_cast<bf16*>(Wl), st));
+  if (Wb) CK(i8_to_bf16(Wq, d_out * d_in, static_cast<bf16*>(Wb), st));
   if (Wd) CK(i8_dequant_rows_bf16(Wq, sw, d_out, d_in, static_cast<bf16*>(Wd), st));
   return LORA_OK;
 }
 
 size_t w8a8_packed_workspace_bytes(int64_t M, int64_t d_out) {
   if (M < 0 || d_out <= 0) return 0;
-  return kErrBytes + al256((size_t)M * kW8MaxR * 2) + al256((size_t)d_out * kW8MaxR * 2);
+  return kErrBytes;
 }
 
 lora_status w8a8_lora_fwd_packed(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const void* Xcodes,
-                                 const float* sx, const void* Wh, const void* Wl, const float* sw, const void* Z,
-                                 const void* B, float s, const void* bias, void* Y, int32_t* acc_out, void* ws,
-                                 size_t ws_bytes, void* stream) {
+                                 const float* sx, const void* Wb, const float* sw, const void* Z, const void* B,
+                                 float s, const void* bias, void* Y, int32_t* acc_out, void* ws, size_t ws_bytes,
+                                 void* stream) {
   lora_status e = check_w8a8(M, d_in, d_out, r, Z, B, s, Y, acc_out, sx, sw);
   if (e != LORA_OK) return e;
-  if (d_in > kW8ExactMaxK) return LORA_ERR_UNSUPPORTED;   // the split-code product is exact up to here
-  REQM(M, Xcodes); REQ(Wh); REQ(Wl);
-  ALN(Xcodes); ALN(sx); ALN(Wh); ALN(Wl); ALN(sw); ALN(Z); ALN(B); ALN(bias); ALN(Y); ALN(acc_out);
+  REQM(M, Xcodes); REQ(Wb);
+  ALN(Xcodes); ALN(sx); ALN(Wb); ALN(sw); ALN(Z); ALN(B); ALN(bias); ALN(Y); ALN(acc_out);
   if ((e = check_ws(ws, ws_bytes, w8a8_packed_workspace_bytes(M, d_out))) != LORA_OK) return e;
   if (M == 0) return LORA_OK;
   Carve c{static_cast<char*>(ws)};
   uint32_t* err = c.take<uint32_t>(kErrBytes / 4);
-  bf16* Zt = c.take<bf16>((size_t)M * kW8MaxR);
-  bf16* Bt = c.take<bf16>((size_t)d_out * kW8MaxR);
-  return w8a8_fwd_core(M, d_in, d_out, r, static_cast<const bf16*>(Xcodes), sx, static_cast<const bf16*>(Wh),
-                       static_cast<const bf16*>(Wl), sw, Z, B, s, bias, Y, acc_out, err, Zt, Bt, (cudaStream_t)stream);
+  return w8a8_fwd_core(M, d_in, d_out, r, static_cast<const bf16*>(Xcodes), sx, static_cast<const bf16*>(Wb), sw, Z,
+                       B, s, bias, Y, acc_out, err, (cudaStream_t)stream);
 }
 
 size_t w8a8_bwd_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int64_t r) {

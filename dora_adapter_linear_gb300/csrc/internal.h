@@ -31,16 +31,16 @@ void prof_mark(cudaStream_t st, bool start, double work, int kind = 0);
 cudaError_t prof_collect(int kind, double* ms, int64_t* launches, double* work, bool reset);
 
 // ------------------------------------------------------------------ tcgen05 GEMM engine
-enum EpiKind { EPI_SCALE_BIAS = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2, EPI_W8A8 = 3, EPI_W8A8F = 4 };
+enum EpiKind { EPI_SCALE_BIAS = 0, EPI_SWIGLU = 1, EPI_SWIGLU_BWD = 2, EPI_W8A8K = 3 };
 enum TcMode {
   TC_FWD = 0,          // A0 [M,K0] x B0 [N,K0]^T (+ A1 [M,K1] x B1 [N,K1]^T), epilogue scale/bias
   TC_BWD_DX = 1,       // A0 [M,K0] x B0 [K0,N] (MN-major) (+ A1 x B1 [K1,N]), optional A-scale along K
   TC_SWIGLU_FWD = 2,   // stacked gate/up weights, SwiGLU epilogue writing e, u, h
   TC_SWIGLU_BWD = 3,   // MN-major B, epilogue forms de, du from saved e, u
-  TC_W8A8 = 4,         // stacked [wh; wl] weight halves, epilogue forms the exact int32 product,
-                       // dequantises and adds the rank-r term
-  TC_W8A8F = 5         // the same product with the rank-r term pre-divided by the dequant scales
-                       // and accumulated into the low half (double-buffered; no int32 output)
+  TC_W8A8K = 4         // int8 codes held as bf16 (B0 [N,K0] K-major, the full codes): the exact int32
+                       // product from K chunks of kc_steps x 64, each summed exactly in fp32 in its
+                       // own TMEM accumulator (the two alternate) and added as int32 in the epilogue;
+                       // the rank-r term A1 x B1^T (fp32) as one more accumulator; y and/or int32 out
 };
 
 struct TcGemmDesc {
@@ -72,17 +72,16 @@ struct TcGemmDesc {
   const bf16* e_in = nullptr;
   const bf16* u_in = nullptr;
   int64_t ld_eu = 0;
-  // W8A8 epilogue: per-row / per-column dequant scales, rank-r term s * Z B^T, raw int32 output
+  // W8A8 epilogue: per-row / per-column dequant scales, scale of the rank-r term (A1 B1^T), raw
+  // int32 output
   const float* sx = nullptr;
   const float* sw = nullptr;
-  const bf16* lz = nullptr;
-  const bf16* lb = nullptr;
   float ls = 0.f;
-  int lr = 0;
   int32_t* acc_out = nullptr;
   uint32_t* err = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int max_ctas = 0;            // cap on the persistent grid in CTAs (0: one per SM)
+  int kc_steps = 16;           // TC_W8A8K: K-steps of 64 per exactly summed chunk
   // forward with the down-projection in the GEMM (TC_FWD, has_tail, K1 = dn_r in 8 .. 32): Z =
   // A0 dn_a^T is formed from the staged A0 tiles (dn_a [dn_r, K0], row stride dn_lda), the tail's
   // A operand is bf16(dn_s Z) written on chip (A1 unused), and bf16(Z) goes to dn_z [M, dn_r] when set
@@ -284,9 +283,6 @@ cudaError_t apply_mask_bf16(const bf16* X, const uint8_t* mask, float scale, int
                             cudaStream_t st);
 cudaError_t add_masked_rank_bf16(bf16* dX, const bf16* G, const bf16* A, const uint8_t* mask, float scale,
                                  int64_t rows, int64_t cols, int r, cudaStream_t st);
-// out[o, j] = bf16(f * in[o, j] / d[o]) for in [rows, r] (a zero d[o] counts as 1)
-cudaError_t scale_rows_recip_bf16(const bf16* in, int64_t rows, int r, const float* d, float f, bf16* out,
-                                  cudaStream_t st);
 // DoRA column variant (bf16): c0 = colsum(W^2); the closed-form column norm n, c = m / n and
 // A_c = A diag(c); out = A diag(w); K = A diag(w) A^T; and the dA assembly
 //   dA[j, k] = c[k] sum_s PA[s][k][j] + 2 s g[k] U[k, j] + 2 s^2 g[k] (Kb A)[j, k].
@@ -340,9 +336,8 @@ cudaError_t coldot_f32(const float* S, const float* Y, int64_t rows, int64_t K, 
 // per-row absmax quantisation: codes as int8 (Xq) and/or as bf16 values (Xb), either may be null
 cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t* Xq, float* sx, cudaStream_t st,
                                bf16* Xb = nullptr);
-// int8 -> bf16 (exact), and the weight split w = 16 wh + wl (n multiple of 16)
+// int8 -> bf16 (exact; n multiple of 16)
 cudaError_t i8_to_bf16(const int8_t* q, int64_t n, bf16* out, cudaStream_t st);
-cudaError_t i8_split_bf16(const int8_t* q, int64_t n, bf16* hi, bf16* lo, cudaStream_t st);
 // out[o, k] = bf16(sw[o] * q[o, k]) (cols multiple of 16)
 cudaError_t i8_dequant_rows_bf16(const int8_t* q, const float* sw, int64_t rows, int64_t cols, bf16* out,
                                  cudaStream_t st);

@@ -604,21 +604,6 @@ cudaError_t finalize_dA_cols(int r, int64_t in, Partial PA, const float* c, cons
   return cudaGetLastError();
 }
 
-__global__ void scale_rows_recip_kernel(const bf16* in, int64_t rows, int r, const float* d, float f, bf16* out) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= rows * r) return;
-  const float dv = d[i / r];
-  out[i] = __float2bfloat16_rn(f * __bfloat162float(in[i]) / (dv != 0.f ? dv : 1.f));
-}
-cudaError_t scale_rows_recip_bf16(const bf16* in, int64_t rows, int r, const float* d, float f, bf16* out,
-                                  cudaStream_t st) {
-  const int64_t n = rows * r;
-  if (n <= 0) return cudaSuccess;
-  scale_rows_recip_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(in, rows, r, d, f, out);
-  count_launch();
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ input dropout (unfused path)
 // out = bf16(X o mask * scale), 8 elements (one 16-byte chunk) per thread; cols a multiple of 8
 __global__ void apply_mask_kernel(const uint4* X, const uint2* mask, float scale, int64_t n8, uint4* out) {

@@ -48,11 +48,9 @@ struct TcParams {
   int ld_eu;
   const float* sx;      // W8A8: per-row activation scales [M]
   const float* sw;      // W8A8: per-column weight scales [N]
-  const bf16* lz;       // W8A8: rank-r input Z [M, lr] (or null)
-  const bf16* lb;       // W8A8: up-projection B [N, lr]
-  float ls;
-  int lr;
+  float ls;             // W8A8: scale of the rank-r term
   int32_t* acc_out;     // W8A8: raw int32 product [M, N] (or null)
+  int kc_steps;         // W8A8 chunked: K-steps per exactly summed chunk
   int write_y;          // W8A8: 0 when only the raw product is wanted
   int pair_leader_arms; // CTA pair: the leader posts the transaction bytes of both CTAs
   int act;              // gated MLP activation: 0 SwiGLU, 1 GeGLU
@@ -80,10 +78,8 @@ template <> struct EpiCfg<EPI_SWIGLU_BWD, false> { static constexpr int STAGES =
 template <> struct EpiCfg<EPI_SCALE_BIAS, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
 template <> struct EpiCfg<EPI_SWIGLU, true> { static constexpr int STAGES = 5, STG_BUFS = 3; };
 template <> struct EpiCfg<EPI_SWIGLU_BWD, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
-template <> struct EpiCfg<EPI_W8A8, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
-template <> struct EpiCfg<EPI_W8A8, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
-template <> struct EpiCfg<EPI_W8A8F, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
-template <> struct EpiCfg<EPI_W8A8F, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
+template <> struct EpiCfg<EPI_W8A8K, false> { static constexpr int STAGES = 4, STG_BUFS = 2; };
+template <> struct EpiCfg<EPI_W8A8K, true> { static constexpr int STAGES = 6, STG_BUFS = 2; };
 
 template <int EPI, bool PAIR, bool KSCALE = false>
 struct Layout {
@@ -299,117 +295,66 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint32_t t_row,
         tma_store_commit();
       }
     }
-  } else if constexpr (EPI == EPI_W8A8F) {
-    // accumulator columns [0, 128) = X wh^T, [128, 256) = X wl^T + s Z B^T / (sx sw) for outputs
-    // n0 .. n0 + 127: y = (16 hi + lo) sx sw (+ bias), with a zero scale read as 1 (its row or
-    // column of the integer product is zero then, and the rank-r term was divided by 1)
-    const int grow = row0 + lane;
-    float rs = grow < p.M ? p.sx[grow] : 0.f;
-    rs = rs != 0.f ? rs : 1.f;
-#pragma unroll 1
-    for (int c = 0; c < N_OUT / 64; ++c, ++chunk_ctr) {
-      uint8_t* stg = my_stg + (chunk_ctr & 1) * 4096;
-      if (lane == 0) tma_store_wait_read<1>();
-      __syncwarp();
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        uint32_t vh[32], vl[32];
-        tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, vh);
-        tmem_ld_32x32b_x32(t_row + BN / 2 + c * 64 + h * 32, vl);
+  }
+}
+
+// Chunked W8A8 epilogue of one warp's 32 rows x 128 columns once the exact int32 sums S of its row
+// are complete: the raw product to acc_out and/or y = S sx sw (+ s T, the rank-r term read from TMEM
+// at t_cols, when TAIL) (+ bias), bf16 through the warp's 32 x 64 staging buffer.
+template <bool TAIL>
+__device__ __forceinline__ void w8k_final(const TcParams& p, const int (&S)[128], uint32_t t_cols, int row0, int col0,
+                                          int lane, uint8_t* stg) {
+  const int grow = row0 + lane;
+  const bool row_ok = grow < p.M;
+  if (p.acc_out != nullptr && row_ok) {
+#pragma unroll
+    for (int g = 0; g < 32; ++g)
+      if (col0 + 4 * g < p.N)
+        *reinterpret_cast<int4*>(p.acc_out + (size_t)grow * p.N + col0 + 4 * g) =
+            make_int4(S[4 * g], S[4 * g + 1], S[4 * g + 2], S[4 * g + 3]);
+  }
+  if (!p.write_y) return;
+  const float rs = row_ok ? p.sx[grow] : 0.f;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {   // unrolled: S is indexed by constants only and stays in registers
+    if (lane == 0) tma_store_wait_read<0>();   // the previous chunk's store has read the buffer
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {   // 16 columns at a time: two 16-byte chunks of the staged row
+      uint32_t v[16];
+      if (TAIL) {
+        tmem_ld_32x32b_x16(t_cols + c * 64 + h * 16, v);
         tmem_ld_wait();
-        const int col0 = n0 + c * 64 + h * 32;
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float y2[2];
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int col = col0 + j + k;
-            float y = 0.f;
-            if (col < p.N) {
-              float cs = __ldg(p.sw + col);
-              cs = cs != 0.f ? cs : 1.f;
-              y = fmaf(16.f, u2f(vh[j + k]), u2f(vl[j + k])) * rs * cs;
-              if (p.bias != nullptr) y += __bfloat162float(p.bias[col]);
-            }
-            y2[k] = y;
-          }
-          w[j / 2] = pack_bf16x2(y2[0], y2[1]);
-        }
-        stage_row(stg, lane, w, h * 4);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&p.tmOut[0], stg, n0 + c * 64, row0);
-        tma_store_commit();
+      uint32_t w[8];
+#pragma unroll
+      for (int j = 0; j < 16; j += 2) {
+        float y2[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int col = col0 + c * 64 + h * 16 + j + k;
+          float y = 0.f;
+          if (col < p.N) {
+            y = (float)S[c * 64 + h * 16 + j + k] * rs * __ldg(p.sw + col);
+            if (TAIL) y += p.ls * u2f(v[j + k]);
+            if (p.bias != nullptr) y += __bfloat162float(p.bias[col]);
+          }
+          y2[k] = y;
+        }
+        w[j / 2] = pack_bf16x2(y2[0], y2[1]);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int ch = 2 * h + jj;
+        *reinterpret_cast<uint4*>(stg + lane * 128 + ((ch ^ (lane & 7)) << 4)) =
+            make_uint4(w[4 * jj], w[4 * jj + 1], w[4 * jj + 2], w[4 * jj + 3]);
       }
     }
-  } else if constexpr (EPI == EPI_W8A8) {
-    // accumulator columns [0, 128) = X wh^T, [128, 256) = X wl^T for outputs n0 .. n0 + 127;
-    // both are exact integers, so acc = 16 * hi + lo is the exact int32 product.  Columns
-    // [256, 384) hold the rank-r term Z B^T (tail MMA) when a low-rank input is given.
-    const int grow = row0 + lane;
-    const bool row_ok = grow < p.M;
-    const float rs = (row_ok && p.write_y) ? p.sx[grow] : 0.f;
-#pragma unroll 1
-    for (int c = 0; c < N_OUT / 64; ++c, ++chunk_ctr) {
-      uint8_t* stg = my_stg + (chunk_ctr & 1) * 4096;
-      if (lane == 0) tma_store_wait_read<1>();
-      __syncwarp();
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        uint32_t vh[32], vl[32];
-        tmem_ld_32x32b_x32(t_row + c * 64 + h * 32, vh);
-        tmem_ld_32x32b_x32(t_row + BN / 2 + c * 64 + h * 32, vl);
-        tmem_ld_wait();
-        const int col0 = n0 + c * 64 + h * 32;
-        int acc[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[j] = 16 * __float2int_rn(u2f(vh[j])) + __float2int_rn(u2f(vl[j]));
-        if (p.acc_out != nullptr && row_ok) {
-#pragma unroll
-          for (int g = 0; g < 8; ++g)
-            if (col0 + 4 * g < p.N)
-              *reinterpret_cast<int4*>(p.acc_out + (size_t)grow * p.N + col0 + 4 * g) =
-                  make_int4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
-        }
-        if (p.write_y) {
-          uint32_t vr[32];
-          if (p.lz != nullptr) {
-            tmem_ld_32x32b_x32(t_row + BN + c * 64 + h * 32, vr);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) vr[j] = 0u;
-          }
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float y2[2];
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int col = col0 + j + k;
-              float y = 0.f;
-              if (col < p.N) {
-                y = (float)acc[j + k] * rs * __ldg(p.sw + col) + p.ls * u2f(vr[j + k]);
-                if (p.bias != nullptr) y += __bfloat162float(p.bias[col]);
-              }
-              y2[k] = y;
-            }
-            w[j / 2] = pack_bf16x2(y2[0], y2[1]);
-          }
-          stage_row(stg, lane, w, h * 4);
-        }
-      }
-      if (p.write_y) {
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&p.tmOut[0], stg, n0 + c * 64, row0);
-          tma_store_commit();
-        }
-      }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&p.tmOut[0], stg, col0 + c * 64, row0);
+      tma_store_commit();
     }
   }
 }
@@ -454,7 +399,7 @@ __device__ __forceinline__ void kscale_tile_inplace(uint8_t* a_tile, const float
 // with the same scaling warps measured 1.7x slower).
 template <int EPI, bool KSCALE = false, bool ZF = false>
 struct OneCta {
-  static constexpr bool EPI8 = EPI == EPI_SCALE_BIAS && !KSCALE;
+  static constexpr bool EPI8 = (EPI == EPI_SCALE_BIAS || EPI == EPI_W8A8K) && !KSCALE;
   static constexpr int THREADS = ((KSCALE || EPI8) ? 320 : 192) + (ZF ? 128 : 0);
 };
 
@@ -554,8 +499,7 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE, ZF>::THREADS, 1) tc_gemm_k
             mbar_expect_tx(&full[stage], tail ? L::B_STAGE_BYTES : L::STAGE_BYTES);
             if (!tail) mbar_arrive(&full[stage]);
           } else {
-            mbar_expect_tx(&full[stage], (EPI == EPI_W8A8 && tail) ? A_STAGE_BYTES + BNB * 128
-                                         : ((KSCALE && !tail) ? L::STAGE_BYTES + L::KSC_BYTES : L::STAGE_BYTES));
+            mbar_expect_tx(&full[stage], (KSCALE && !tail) ? L::STAGE_BYTES + L::KSC_BYTES : L::STAGE_BYTES);
           }
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -586,7 +530,7 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE, ZF>::THREADS, 1) tc_gemm_k
               for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &p.tmB1, &full[stage], n0 + 64 * j, kt);
             } else if (STACKED) {
               tma_load_2d(b_dst, &p.tmB1, &full[stage], p.tail_b1_x + kt, n0);
-              if (EPI != EPI_W8A8) tma_load_2d(b_dst + BNB * 128, &p.tmB1b, &full[stage], p.tail_b1b_x + kt, n0);
+              tma_load_2d(b_dst + BNB * 128, &p.tmB1b, &full[stage], p.tail_b1b_x + kt, n0);
             } else {
               tma_load_2d(b_dst, &p.tmB1, &full[stage], kt, n0);
             }
@@ -606,19 +550,63 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE, ZF>::THREADS, 1) tc_gemm_k
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      // W8A8: one accumulator set per tile, [0,128) hi, [128,256) lo, [256,384) the rank-r term
-      // (N = 128 tail MMA), so that hi and lo stay exact integers
-      constexpr bool W8 = EPI == EPI_W8A8;
+    if (lane == 0 && EPI == EPI_W8A8K) {
+      // chunked W8A8: each chunk of kc_steps K-steps (and the rank-r tail) in its own accumulator,
+      // the two accumulators alternating across chunks and tiles
+      constexpr uint32_t idesc = umma_idesc_bf16(BM, BN, 0, 0);
+      const int kc = p.kc_steps;
+      const int nch = (nk0 + kc - 1) / kc;
+      const int nchunks = nch + (HAS_TAIL ? 1 : 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      uint32_t u = 0;
+      for (int t = t_first; t < t_count && ok; t += t_step) {
+        for (int c = 0; c < nchunks && ok; ++c, ++u) {
+          const int buf = (int)(u & 1);
+          const uint32_t aph = (u >> 1) & 1;
+          if (!mbar_wait(&acc_empty[buf], aph ^ 1, p.timeout_ns, abort_flag, p.err, 0x102)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          const int k_begin = c < nch ? c * kc : nk0;
+          const int k_end = c < nch ? min(nk0, (c + 1) * kc) : nk;
+          for (int ks = k_begin; ks < k_end; ++ks) {
+            if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag, p.err, 0x103)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sA + stage * A_STAGE_BYTES);
+            const uint32_t b_base = smem_u32(sB + stage * L::B_STAGE_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16(d_tmem, umma_smem_desc(a_base + kk * 32, 16, 1024), umma_smem_desc(b_base + kk * 32, 16, 1024),
+                        idesc, (ks > k_begin || kk > 0) ? 1u : 0u);
+            umma_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&acc_full[buf]);
+        }
+      }
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0, 20000000ull);
+    } else if (lane == 0) {
       constexpr uint32_t idesc0 = umma_idesc_bf16(BM, BN, 0, B0_MN ? 1 : 0);
-      constexpr uint32_t idesc1 = W8 ? umma_idesc_bf16(BM, BN / 2, 0, 0) : umma_idesc_bf16(BM, BN, 0, B1_MN ? 1 : 0);
+      constexpr uint32_t idesc1 = umma_idesc_bf16(BM, BN, 0, B1_MN ? 1 : 0);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
       for (int t = t_first; t < t_count && ok; t += t_step, ++it) {
-        const int buf = W8 ? 0 : (it & 1);
-        const uint32_t acc_phase = W8 ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
+        const int buf = it & 1;
+        const uint32_t acc_phase = (uint32_t)((it >> 1) & 1);
         if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1, p.timeout_ns, abort_flag, p.err, 0x102)) {
           ok = false;
           break;
@@ -643,10 +631,7 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE, ZF>::THREADS, 1) tc_gemm_k
             const uint64_t adesc = umma_smem_desc(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc = bmn ? umma_smem_desc(b_base + kk * 2048, 8192, 1024)
                                        : umma_smem_desc(b_base + kk * 32, 16, 1024);
-            if (W8 && tail)
-              umma_bf16(d_tmem + 2 * (BN / 2), adesc, bdesc, idesc1, (ks > nk0 || kk > 0) ? 1u : 0u);
-            else
-              umma_bf16(d_tmem, adesc, bdesc, tail ? idesc1 : idesc0, (ks > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16(d_tmem, adesc, bdesc, tail ? idesc1 : idesc0, (ks > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -670,9 +655,58 @@ __global__ void __launch_bounds__(OneCta<EPI, KSCALE, ZF>::THREADS, 1) tc_gemm_k
     uint8_t* my_stg = sStg + (warp - 2) * (EPI8 ? 4096 : EpiCfg<EPI, false>::STG_BUFS * 4096);
     int it = 0;
     uint32_t chunk_ctr = 0;
+    if constexpr (EPI == EPI_W8A8K) {
+      // chunked W8A8: every integer chunk is added to the row's int32 sums S, held in registers
+      // (exact: each chunk's fp32 sum is an integer below 2^24); the tail chunk (or, without one, the
+      // last integer chunk) closes the tile.  Warp (q, half): rows 32q.., columns 128 half..
+      const int kc = p.kc_steps;
+      const int nch = (nk0 + kc - 1) / kc;
+      const int nchunks = nch + (HAS_TAIL ? 1 : 0);
+      const uint32_t lanes = tmem_base + ((uint32_t)(32 * q) << 16) + half * (BN / 2);
+      uint32_t u = 0;
+      bool ok = true;
+      for (int t = t_first; t < t_count && ok; t += t_step) {
+        int mt, nt;
+        coords(t, mt, nt);
+        const int row0 = mt * BM + 32 * q;
+        const int col0 = nt * BN + half * (BN / 2);
+        int S[128];
+#pragma unroll
+        for (int j = 0; j < 128; ++j) S[j] = 0;
+        for (int c = 0; c < nchunks; ++c, ++u) {
+          const int buf = (int)(u & 1);
+          const uint32_t aph = (u >> 1) & 1;
+          if (!mbar_wait(&acc_full[buf], aph, p.timeout_ns, abort_flag, p.err, 0x104)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t c_cols = lanes + buf * BN;
+          if (c < nch) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t v[16];
+              tmem_ld_32x32b_x16(c_cols + j * 16, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) S[j * 16 + e] += __float2int_rn(u2f(v[e]));
+            }
+          } else {
+            w8k_final<true>(p, S, c_cols, row0, col0, lane, my_stg);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        if (!ok) break;
+        if (!HAS_TAIL) w8k_final<false>(p, S, 0, row0, col0, lane, my_stg);
+      }
+      if (lane == 0) tma_store_wait_all<0>();
+      __syncwarp();
+    } else
     for (int t = t_first; t < t_count; t += t_step, ++it) {
-      const int buf = (EPI == EPI_W8A8) ? 0 : (it & 1);
-      const uint32_t acc_phase = (EPI == EPI_W8A8) ? (uint32_t)(it & 1) : (uint32_t)((it >> 1) & 1);
+      const int buf = it & 1;
+      const uint32_t acc_phase = (uint32_t)((it >> 1) & 1);
       if (!mbar_wait(&acc_full[buf], acc_phase, p.timeout_ns, abort_flag, p.err, 0x104)) break;
       tc_fence_after();
       int mt, nt;
@@ -1259,18 +1293,15 @@ static cudaError_t launch_mode(const TcGemmDesc& d, const TcParams& p, cudaStrea
       return launch_variant<false, true, true, false, EPI_SWIGLU>(p, st, kind, tiles, mc);
     case TC_SWIGLU_BWD:
       return launch_variant<true, false, true, true, EPI_SWIGLU_BWD>(p, st, kind, tiles, mc);
-    case TC_W8A8F:
-      if (d.has_tail) return launch_variant<false, true, true, false, EPI_W8A8F>(p, st, kind, tiles, mc);
-      return launch_variant<false, true, false, false, EPI_W8A8F>(p, st, kind, tiles, mc);
-    case TC_W8A8:  // one-CTA kernel only (its accumulator layout is per-CTA)
-      if (d.has_tail) return launch_one<false, true, true, false, EPI_W8A8>(p, st, tiles, mc);
-      return launch_one<false, true, false, false, EPI_W8A8>(p, st, tiles, mc);
+    case TC_W8A8K:  // one-CTA kernel only
+      if (d.has_tail) return launch_one<false, false, true, false, EPI_W8A8K>(p, st, tiles, mc);
+      return launch_one<false, false, false, false, EPI_W8A8K>(p, st, tiles, mc);
   }
   return cudaErrorInvalidValue;
 }
 
 // Kernel choice per mode.  LORA_GB300_GEMM_PAIR=0 / 1 forces the one-CTA / pair kernel for every
-// mode (W8A8 with the int32 output always runs one-CTA).
+// mode (the chunked W8A8 product always runs one-CTA).
 static bool use_pair(int mode) {
   const char* e = getenv("LORA_GB300_GEMM_PAIR");
   if (e && *e) return atoi(e) != 0;
@@ -1286,10 +1317,10 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
   // the down-projection in the GEMM runs on the one-CTA kernel (ranks 8 .. 32, one tail step)
   if (d.dn_a && (d.mode != TC_FWD || !d.has_tail || d.dn_r < 8 || d.dn_r > 32 || d.dn_r % 8 || d.K1 != d.dn_r))
     return cudaErrorInvalidValue;
-  const bool pair = use_pair(d.mode) && d.mode != TC_W8A8 && d.dn_a == nullptr;
+  const bool pair = use_pair(d.mode) && d.mode != TC_W8A8K && d.dn_a == nullptr;
   TcParams p;
   memset(&p, 0, sizeof(p));
-  const bool stacked = d.mode == TC_SWIGLU_FWD || d.mode == TC_W8A8 || d.mode == TC_W8A8F;
+  const bool stacked = d.mode == TC_SWIGLU_FWD;
   // rows of a K-major B box: 256 (one CTA), 128 (stacked halves, or one CTA's half of a pair)
   const int bnb = (stacked || pair) ? BN / 2 : BN;
   bool ok = make_map(&p.tmA0, d.A0, d.K0, d.M, d.lda0, BM);
@@ -1309,21 +1340,19 @@ cudaError_t tc_gemm(const TcGemmDesc& d, cudaStream_t st) {
     if (d.b1_mn) ok = ok && make_map(&p.tmB1, d.B1, d.N, d.K1, d.ldb1, 64);
     else {
       ok = ok && make_map(&p.tmB1, d.B1, d.K1_b, d.N, d.ldb1, bnb);
-      if (stacked && d.mode != TC_W8A8)
+      if (stacked)
         ok = ok && make_map(&p.tmB1b, d.B1b, d.K1_bb > 0 ? d.K1_bb : d.K1_b, d.N, d.ldb1b > 0 ? d.ldb1b : d.ldb1, bnb);
     }
   }
   int nouts = d.mode == TC_SWIGLU_FWD ? 3 : (d.mode == TC_SWIGLU_BWD ? 2 : 1);
-  if (d.mode == TC_W8A8 && d.out[0] == nullptr) nouts = 0;   // raw int32 product only
+  if (d.mode == TC_W8A8K && d.out[0] == nullptr) nouts = 0;   // raw int32 product only
   for (int i = 0; i < nouts; ++i) ok = ok && make_map(&p.tmOut[i], d.out[i], d.N, d.M, d.ldo, 32);
   if (!ok) return cudaErrorInvalidValue;
   p.sx = d.sx;
   p.sw = d.sw;
-  p.lz = d.lz;
-  p.lb = d.lb;
   p.ls = d.ls;
-  p.lr = d.lr;
   p.acc_out = d.acc_out;
+  p.kc_steps = d.kc_steps > 0 ? d.kc_steps : 16;
   p.write_y = d.out[0] != nullptr ? 1 : 0;
   p.pair_leader_arms = env_int("LORA_GB300_PAIR_ARM", 1);
   p.act = d.act;

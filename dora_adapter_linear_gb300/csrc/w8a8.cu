@@ -1,8 +1,9 @@
-// W8A8 base layer with a LoRA epilogue.
+// W8A8 base layer with a LoRA epilogue: the quantiser, the int8 re-layouts and the warp-level
+// integer product (an alternative to the chunked bf16 tensor-core product of tc_gemm.cu).
 //
 // The int8 product is exact: int8 x int8 products summed in int32 by the warp-level integer
-// MMA (mma.sync m16n8k32 s8.s8.s32).  sm_103a has no tcgen05 integer kind (the PTX
-// assembler rejects .kind::i8 for this target), so this legacy path is the exact one.
+// MMA (mma.sync m16n8k32 s8.s8.s32).  sm_103a has no tcgen05 integer kind (the PTX assembler
+// rejects .kind::i8 for this target).
 // The epilogue works on registers: acc * sx[i] * sw[o] + s * (Z B^T)[i, o] + bias[o] -> bf16,
 // where the rank-r term is one more small bf16 MMA per 16-row tile; the int32 [M, d_out]
 // product is never written unless the raw-product epilogue (acc_out) is asked for.
@@ -15,7 +16,7 @@ namespace lg {
 
 // ------------------------------------------------------------------ per-row absmax quantisation
 // Writes the codes as int8 (Xq) and/or as bf16 values (Xb: the same integers, exact in bf16, ready
-// to be the A operand of the split-code tensor-core product); either may be null.
+// to be the A operand of the tensor-core product); either may be null.
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const bf16* X, int64_t cols, int8_t* Xq, float* sx,
                                                             bf16* Xb) {
   const int64_t row = blockIdx.x;
@@ -70,11 +71,8 @@ cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t
 }
 
 // ------------------------------------------------------------------ int8 codes as bf16 tensor-core operands
-// Every int8 value is exact in bf16.  The weight codes are split once more, w = 16 * wh + wl
-// with wh = w >> 4 in [-8, 7] (arithmetic shift) and wl = w & 15 in [0, 15], so that the two
-// bf16 GEMMs X wh^T and X wl^T accumulate integers whose every partial sum stays below 2^24
-// for d_in <= 8800: fp32 accumulation is then exact and acc = 16 acc_h + acc_l is the int32
-// product (the epilogue forms it).
+// Every int8 value is exact in bf16, so the codes are the operands of the bf16 tensor-core product,
+// which sums them exactly in 1024-wide K chunks (every partial sum an integer below 2^24).
 __global__ void i8_to_bf16_kernel(const int8_t* __restrict__ q, int64_t n16, bf16* __restrict__ out) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n16) return;
@@ -86,27 +84,6 @@ __global__ void i8_to_bf16_kernel(const int8_t* __restrict__ q, int64_t n16, bf1
   uint4* o = reinterpret_cast<uint4*>(out) + 2 * i;
   o[0] = make_uint4(w[0], w[1], w[2], w[3]);
   o[1] = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
-__global__ void i8_split_bf16_kernel(const int8_t* __restrict__ q, int64_t n16, bf16* __restrict__ hi,
-                                     bf16* __restrict__ lo) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n16) return;
-  const uint4 raw = reinterpret_cast<const uint4*>(q)[i];
-  const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
-  uint32_t wh[8], wl[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int x0 = b[2 * j], x1 = b[2 * j + 1];
-    wh[j] = pack_bf16x2((float)(x0 >> 4), (float)(x1 >> 4));
-    wl[j] = pack_bf16x2((float)(x0 & 15), (float)(x1 & 15));
-  }
-  uint4* oh = reinterpret_cast<uint4*>(hi) + 2 * i;
-  uint4* ol = reinterpret_cast<uint4*>(lo) + 2 * i;
-  oh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-  oh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
-  ol[0] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-  ol[1] = make_uint4(wl[4], wl[5], wl[6], wl[7]);
 }
 
 // W_deq[o, k] = bf16(sw[o] * q[o, k]): the int8 base weight in real units, the B operand of
@@ -143,13 +120,6 @@ cudaError_t i8_to_bf16(const int8_t* q, int64_t n, bf16* out, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t i8_split_bf16(const int8_t* q, int64_t n, bf16* hi, bf16* lo, cudaStream_t st) {
-  const int64_t n16 = n / 16;
-  if (n16 <= 0) return cudaSuccess;
-  i8_split_bf16_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(q, n16, hi, lo);
-  count_launch();
-  return cudaGetLastError();
-}
 
 // ------------------------------------------------------------------ int8 GEMM + epilogue
 namespace w8 {

@@ -369,31 +369,30 @@ def w8a8_quantize_rows_bf16(X, A=None):
     return Xc, sx, Z
 
 
-def w8a8_prepack_weight(Wq, sw, split=True, dequant=True):
-    """The frozen int8 weight laid out once: (Wh, Wl) split codes for the forward, Wd the dequantised
-    weight for the backward (each None when not asked for)."""
+def w8a8_prepack_weight(Wq, sw, codes=True, dequant=True):
+    """The frozen int8 weight laid out once: Wb the codes as bf16 for the forward, Wd the
+    dequantised weight for the backward (each None when not asked for)."""
     if Wq.dtype != torch.int8 or Wq.dim() != 2:
         raise ValueError("Wq must be a 2-D int8 tensor")
     d_out, d_in = Wq.shape
     _check_shapes(Wq, Wq=(Wq, (d_out, d_in), torch.int8), sw=(sw, (d_out,), F32))
     mk = lambda: torch.empty(d_out, d_in, dtype=torch.bfloat16, device=Wq.device)  # noqa: E731
-    Wh, Wl = (mk(), mk()) if split else (None, None)
+    Wb = mk() if codes else None
     Wd = mk() if dequant else None
-    L.w8a8_prepack_weight(d_out, d_in, Wq, sw, Wh, Wl, Wd)
-    return Wh, Wl, Wd
+    L.w8a8_prepack_weight(d_out, d_in, Wq, sw, Wb, Wd)
+    return Wb, Wd
 
 
-def w8a8_lora_fwd_packed(Xc, sx, Wh, Wl, sw, Z, B, s, bias=None, want_acc=False, want_y=True):
-    """w8a8_lora_fwd on prepacked operands (Xc from w8a8_quantize_rows_bf16, Wh / Wl from
+def w8a8_lora_fwd_packed(Xc, sx, Wb, sw, Z, B, s, bias=None, want_acc=False, want_y=True):
+    """w8a8_lora_fwd on prepacked operands (Xc from w8a8_quantize_rows_bf16, Wb from
     w8a8_prepack_weight)."""
     M, d_in = Xc.shape
-    d_out = Wh.shape[0]
+    d_out = Wb.shape[0]
     r = 0 if Z is None else Z.shape[1]
-    _check_shapes(Xc, Xc=(Xc, (M, d_in), BF16), sx=(sx, (M,), F32), Wh=(Wh, (d_out, d_in), BF16),
-                  Wl=(Wl, (d_out, d_in), BF16), sw=(sw, (d_out,), F32), Z=(Z, (M, r), BF16), B=(B, (d_out, r), BF16),
-                  bias=(bias, (d_out,), BF16))
+    _check_shapes(Xc, Xc=(Xc, (M, d_in), BF16), sx=(sx, (M,), F32), Wb=(Wb, (d_out, d_in), BF16),
+                  sw=(sw, (d_out,), F32), Z=(Z, (M, r), BF16), B=(B, (d_out, r), BF16), bias=(bias, (d_out,), BF16))
     Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=Xc.device) if want_y else None
     acc = torch.empty(M, d_out, dtype=torch.int32, device=Xc.device) if want_acc else None
     ws = workspace(L.w8a8_packed_workspace_bytes(M, d_out), Xc.device)
-    L.w8a8_lora_fwd_packed(M, d_in, d_out, r, Xc, sx, Wh, Wl, sw, Z, B, s, bias, Y, acc, ws)
+    L.w8a8_lora_fwd_packed(M, d_in, d_out, r, Xc, sx, Wb, sw, Z, B, s, bias, Y, acc, ws)
     return Y, acc

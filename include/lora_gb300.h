@@ -372,31 +372,28 @@ lora_status w8a8_quantize_rows_bf16(int64_t rows, int64_t cols, const void* X, v
                                     const void* A, int64_t r, void* Z, void* stream);
 
 /* One-time preparation of the frozen int8 weight Wq [d_out, d_in] (sw [d_out] fp32):
- *   Wh, Wl [d_out, d_in] bf16: the code split w = 16 * (w >> 4) + (w & 15) used by the tensor-core
- *   product (both NULL or both set);  Wd [d_out, d_in] bf16 = sw[o] * Wq[o, k], the dequantised
- *   weight of the backward (NULL to skip).  The backward through the int8 base given Wd is
- *   lora_linear_bwd with W0 = Wd (what w8a8_lora_bwd does after dequantising per call).
+ *   Wb [d_out, d_in] bf16: the weight codes as bf16 values (the same integers, exact in bf16), the
+ *   B operand of the tensor-core product (NULL to skip);  Wd [d_out, d_in] bf16 = sw[o] * Wq[o, k],
+ *   the dequantised weight of the backward (NULL to skip).  The backward through the int8 base
+ *   given Wd is lora_linear_bwd with W0 = Wd (what w8a8_lora_bwd does after dequantising per call).
  * "nunchaku-style kernel fusion" (OneTrainer #1680), commit reworking the 8-bit matmuls (the
  * frozen 8-bit weight, re-laid out for the product once).  d_in a multiple of 32. */
-lora_status w8a8_prepack_weight(int64_t d_out, int64_t d_in, const int8_t* Wq, const float* sw, void* Wh,
-                                void* Wl, void* Wd, void* stream);
+lora_status w8a8_prepack_weight(int64_t d_out, int64_t d_in, const int8_t* Wq, const float* sw, void* Wb,
+                                void* Wd, void* stream);
 
-/* Workspace of w8a8_lora_fwd_packed: the error word and the rank-r operands divided by the
- * dequant scales (M x 128 and d_out x 128 bf16).  0 on bad input. */
+/* Workspace of w8a8_lora_fwd_packed: the error word (256 bytes).  0 on bad input. */
 size_t w8a8_packed_workspace_bytes(int64_t M, int64_t d_out);
 
 /* w8a8_lora_fwd on prepacked operands: Xcodes [M, d_in] bf16 from w8a8_quantize_rows_bf16 and
- * Wh, Wl [d_out, d_in] bf16 from w8a8_prepack_weight; every other argument, the result and its
- * exactness as w8a8_lora_fwd.  d_in <= 8800 (the split-code product is exact up to there;
- * LORA_ERR_UNSUPPORTED beyond).  Same pages and passages as w8a8_lora_fwd. */
+ * Wb [d_out, d_in] bf16 from w8a8_prepack_weight; every other argument, the result and its
+ * exactness as w8a8_lora_fwd.  Same pages and passages as w8a8_lora_fwd. */
 lora_status w8a8_lora_fwd_packed(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const void* Xcodes,
-                                 const float* sx, const void* Wh, const void* Wl, const float* sw, const void* Z,
-                                 const void* B, float s, const void* bias, void* Y, int32_t* acc_out, void* ws,
-                                 size_t ws_bytes, void* stream);
+                                 const float* sx, const void* Wb, const float* sw, const void* Z, const void* B,
+                                 float s, const void* bias, void* Y, int32_t* acc_out, void* ws, size_t ws_bytes,
+                                 void* stream);
 
-/* Bytes of workspace w8a8_lora_fwd needs: the error word, the int8 codes re-laid out as bf16
- * tensor-core operands (X: M x d_in; W split into two d_out x d_in halves) and the rank-r
- * operands divided by the dequant scales (M x 128 and d_out x 128 bf16).  0 on bad input. */
+/* Bytes of workspace w8a8_lora_fwd needs: the error word and the int8 codes re-laid out as bf16
+ * tensor-core operands (X: M x d_in, W: d_out x d_in).  0 on bad input. */
 size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out);
 
 /* Y = float(acc) * sx[i] * sw[o] + s * (Z B^T)[i, o] (+ bias), acc = Xq Wq^T exact in int32.
@@ -410,12 +407,11 @@ size_t w8a8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out);
  *   bias [d_out] bf16 or NULL, Y [M, d_out] bf16 (or NULL when only acc_out is wanted),
  *   acc_out [M, d_out] int32 or NULL: the raw-product epilogue.  d_in multiple of 32.
  *   ws: workspace of at least w8a8_workspace_bytes(M, d_in, d_out) bytes (256-byte aligned).
- *   For d_in <= 8800 the product runs on the bf16 tensor cores with every weight code split as
- *   w = 16 * (w >> 4) + (w & 15): both partial products accumulate integers below 2^24, so fp32
- *   accumulation is exact and the int32 result is bit-identical to an integer GEMM.  Larger
- *   d_in uses the warp-level integer MMA (sm_103a has no tcgen05 integer kind).
- *   When acc_out is NULL the low-rank term enters the low partial sum as (s Z / sx)(B / sw)^T and
- *   Y = (16 hi + lo) sx sw (+ bias): the same value up to one fp32 rounding of that sum.
+ *   The product runs on the bf16 tensor cores (sm_103a has no tcgen05 integer kind) with the codes
+ *   as bf16 values, the K range in chunks of 1024: every fp32 partial sum of a chunk is an integer
+ *   of magnitude at most 127 * 127 * 1024 < 2^24, so each chunk is exact, and the chunks are added
+ *   as int32; acc is bit-identical to an integer GEMM for any d_in.  The rank-r term Z B^T is a
+ *   separate fp32 accumulator.  LORA_GB300_W8A8_IMMA=1 runs the warp-level integer MMA instead.
  */
 lora_status w8a8_lora_fwd(int64_t M, int64_t d_in, int64_t d_out, int64_t r, const int8_t* Xq,
                           const float* sx, const int8_t* Wq, const float* sw, const void* Z,

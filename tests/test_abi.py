@@ -38,7 +38,7 @@ def test_status_strings(lib):
     assert L.lora_status_string(0) == "ok"
     assert "workspace" in L.lora_status_string(4)
     assert L.lora_status_string(99) == "unknown status"
-    assert L.lora_abi_version() == 7
+    assert L.lora_abi_version() == 8
 
 
 def test_workspace_bytes_rejects_bad_shapes(lib):
@@ -98,7 +98,7 @@ def test_entry_points_validate_before_launch(lib):
     assert r == 1  # Z without B
     r = lib.w8a8_lora_fwd(64, 128, 64, 16, fake, fake, fake, fake, None, None, 1.0, None, fake, None, fake, 16, None)
     assert r == 4  # workspace too small
-    assert L.w8a8_workspace_bytes(64, 128, 64) >= 256 + 64 * 128 * 2 + 2 * 64 * 128 * 2
+    assert L.w8a8_workspace_bytes(64, 128, 64) >= 256 + 64 * 128 * 2 + 64 * 128 * 2
     r = lib.w8a8_quantize_rows(4, 12, fake, fake, fake, None, 0, None, None)
     assert r == 2  # cols % 8
     mlp = L.mlp_shape(64, 128, 256, 16)

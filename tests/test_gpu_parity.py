@@ -488,10 +488,10 @@ def test_w8a8_acc_bit_exact_and_epilogue(ops, bias):
     assert_close(Y, ry, "bf16", "Y")
 
 
-@pytest.mark.parametrize("path", ["tensor_split", "integer_mma"])
+@pytest.mark.parametrize("path", ["tensor_chunks", "integer_mma"])
 def test_w8a8_both_product_paths(ops, path, monkeypatch):
-    """The bf16 tensor-core path (w = 16 (w >> 4) + (w & 15)) and the integer MMA path give the
-    same exact int32 product and the same epilogue."""
+    """The bf16 tensor-core path (codes as bf16, exact 1024-wide K chunks added as int32) and the
+    integer MMA path give the same exact int32 product and the same epilogue."""
     if path == "integer_mma":
         monkeypatch.setenv("LORA_GB300_W8A8_IMMA", "1")
     case, t, Wq, sw, Xq, sx = w8_inputs(M=260, d_in=320, d_out=136, bias=True)
@@ -504,10 +504,10 @@ def test_w8a8_both_product_paths(ops, path, monkeypatch):
 
 
 @pytest.mark.parametrize("bias,zero_rows", [(False, False), (True, True)])
-def test_w8a8_fused_output_path(ops, bias, zero_rows, monkeypatch):
-    """Output-only calls fold the rank-r term into the low accumulator half (pre-divided by the
-    dequant scales): same result as the exact-integer path and the oracle, including an all-zero
-    input row and an all-zero weight row (scale 0)."""
+def test_w8a8_output_with_and_without_int32(ops, bias, zero_rows):
+    """The dequantised output matches the oracle, including an all-zero input row and an all-zero
+    weight row (scale 0), and has the same bits whether or not the raw int32 product is also
+    written."""
     case, t, Wq, sw, Xq, sx = w8_inputs(M=300, d_in=352, d_out=264, bias=bias)
     if zero_rows:
         Xq[5] = 0
@@ -520,19 +520,26 @@ def test_w8a8_fused_output_path(ops, bias, zero_rows, monkeypatch):
     args = (gpu(torch.from_numpy(Xq)), gpu(torch.from_numpy(sx)), gpu(torch.from_numpy(Wq)),
             gpu(torch.from_numpy(sw)), gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]))
     Y, _ = ops.w8a8_lora_fwd(*args)
-    ry, _ = O.w8a8_lora_fwd(Xq, sx, Wq, sw, f64(Z), f64(t["B"]), case.s, f64(t["bias"]))
+    ry, racc = O.w8a8_lora_fwd(Xq, sx, Wq, sw, f64(Z), f64(t["B"]), case.s, f64(t["bias"]))
     assert_close(Y, ry, "bf16", "Y")
-    monkeypatch.setenv("LORA_GB300_W8A8_EXACT", "1")
-    Ye, _ = ops.w8a8_lora_fwd(*args)
-    assert_close(Y, f64(Ye.cpu()), "bf16", "fused vs exact path")
+    Ye, acc = ops.w8a8_lora_fwd(*args, want_acc=True)
+    assert torch.equal(Y, Ye)
+    np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), racc)
 
 
-def test_w8a8_deep_k_uses_integer_path(ops):
-    """d_in above the exact-split bound (8800) runs the integer MMA; still bit-exact."""
+@pytest.mark.parametrize("path", ["tensor_chunks", "integer_mma"])
+def test_w8a8_deep_k_exact(ops, path, monkeypatch):
+    """d_in of 8832 (nine 1024-wide exact chunks, the last one ragged) with all codes at +-127 in
+    places, on both product paths: bit-exact int32."""
+    if path == "integer_mma":
+        monkeypatch.setenv("LORA_GB300_W8A8_IMMA", "1")
     rng = np.random.default_rng(5)
-    M, K, N = 64, 8832, 72
+    M, K, N = 200, 8832, 264
     Xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
     Wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    Xq[3] = 127
+    Wq[7] = 127
+    Wq[8] = -127
     _, acc = ops.w8a8_lora_fwd(gpu(torch.from_numpy(Xq)), None, gpu(torch.from_numpy(Wq)), None, None, None, 0.0,
                                want_acc=True, want_y=False)
     np.testing.assert_array_equal(acc.cpu().numpy().astype(np.int64), O.int8_accumulate(Xq, Wq))
@@ -540,7 +547,7 @@ def test_w8a8_deep_k_uses_integer_path(ops):
 
 @pytest.mark.parametrize("bias", [False, True])
 def test_w8a8_packed_path(ops, bias):
-    """Prepacked operands: the quantiser's bf16 codes, the weight's split halves and dequantised
+    """Prepacked operands: the quantiser's bf16 codes, the weight's bf16 codes and dequantised
     copy made once; the packed forward gives the same bits as w8a8_lora_fwd and the exact int32
     product; the backward through the dequantised weight matches the oracle."""
     case, t, Wq, sw, Xq, sx = w8_inputs(M=300, d_in=352, d_out=264, bias=bias)
@@ -549,19 +556,19 @@ def test_w8a8_packed_path(ops, bias):
     np.testing.assert_array_equal(Xc.float().cpu().numpy(), Xq.astype(np.float32))    # codes, exactly
     np.testing.assert_array_equal(gsx.cpu().numpy(), sx)
     gWq, gsw = gpu(torch.from_numpy(Wq)), gpu(torch.from_numpy(sw))
-    Wh, Wl, Wd = ops.w8a8_prepack_weight(gWq, gsw)
-    np.testing.assert_array_equal((16 * Wh.float() + Wl.float()).cpu().numpy(), Wq.astype(np.float32))
+    Wb, Wd = ops.w8a8_prepack_weight(gWq, gsw)
+    np.testing.assert_array_equal(Wb.float().cpu().numpy(), Wq.astype(np.float32))
     assert_close(Wd, O.w8a8_dequant_weight(Wq, sw), "bf16", "Wd")
     Z = (t["X"].double() @ t["A"].double().T).to(torch.bfloat16)
     ry, racc = O.w8a8_lora_fwd(Xq, sx, Wq, sw, f64(Z), f64(t["B"]), case.s, f64(t["bias"]))
-    Yp, accp = ops.w8a8_lora_fwd_packed(Xc, gsx, Wh, Wl, gsw, gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]),
+    Yp, accp = ops.w8a8_lora_fwd_packed(Xc, gsx, Wb, gsw, gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]),
                                         want_acc=True)
     np.testing.assert_array_equal(accp.cpu().numpy().astype(np.int64), racc)
-    assert_close(Yp, ry, "bf16", "Y packed (exact epilogue)")
-    Yf, _ = ops.w8a8_lora_fwd_packed(Xc, gsx, Wh, Wl, gsw, gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]))
+    assert_close(Yp, ry, "bf16", "Y packed")
+    Yf, _ = ops.w8a8_lora_fwd_packed(Xc, gsx, Wb, gsw, gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]))
     Yu, _ = ops.w8a8_lora_fwd(gpu(torch.from_numpy(Xq)), gsx, gWq, gsw, gpu(Z), gpu(t["B"]), case.s, gpu(t["bias"]))
     assert torch.equal(Yf, Yu), "the packed forward runs the same product and epilogue"
-    assert_close(Yf, ry, "bf16", "Y packed (folded epilogue)")
+    assert torch.equal(Yf, Yp), "the int32 output changes nothing in Y"
     g = torch.Generator().manual_seed(80)
     dY = torch.randn(case.M, case.d_out, generator=g).to(torch.bfloat16)
     dX, dA, dB, db = ops.lora_linear_bwd(X, Wd, A, gpu(t["B"]), gpu(Z), gpu(dY), case.s, need_dbias=True)
