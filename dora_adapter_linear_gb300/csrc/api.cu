@@ -113,8 +113,14 @@ struct LinBwdWs {
   RowColPlan rc; // pm == 0: G and the dB partials take a pass over dY each
   int splitsB, splitsA;
 };
-// ranks whose dY side runs as one pass (G and the dB partials together)
-inline bool rowcol_rank(int r) { return r == 8 || r == 16 || r == 24 || r == 32; }
+// Plan of the one pass over S [M, K] that gives both rank-r products of a backward's dY side (G and
+// the dB partials), or an empty plan (pm == 0: a pass each) for other ranks, M == 0, or with
+// LORA_GB300_ROWCOL=0.
+RowColPlan dy_plan(int64_t M, int64_t K, int64_t r) {
+  const char* rc_env = getenv("LORA_GB300_ROWCOL");
+  if (!(r == 8 || r == 16 || r == 24 || r == 32) || M <= 0 || (rc_env && atoi(rc_env) == 0)) return RowColPlan{};
+  return rowcol_plan(M, K, (int)r);
+}
 size_t plan_lin_bwd(const lora_shape& sh, char* base, LinBwdWs* w) {
   Carve c{base};
   const size_t es = sh.dtype == LORA_BF16 ? 2 : 4;
@@ -124,9 +130,7 @@ size_t plan_lin_bwd(const lora_shape& sh, char* base, LinBwdWs* w) {
   w->rc = RowColPlan{};
   w->Gp = nullptr;
   if (sh.dtype == LORA_BF16) {
-    const char* rc_env = getenv("LORA_GB300_ROWCOL");   // 0: one pass over dY for each of G and dB
-    if (rowcol_rank((int)sh.r) && sh.M > 0 && !(rc_env && atoi(rc_env) == 0))
-      w->rc = rowcol_plan(sh.M, sh.d_out, (int)sh.r);
+    w->rc = dy_plan(sh.M, sh.d_out, sh.r);
     w->splitsB = w->rc.pm > 0 ? w->rc.pm : colreduce_splits(sh.M, sh.d_out);
     w->splitsA = colreduce_splits(sh.M, sh.d_in);
     w->PB = c.take<float>((size_t)w->splitsB * sh.d_out * sh.r);
@@ -275,7 +279,9 @@ struct MlpBwdWs {
   uint32_t* err;
   bf16 *dedu, *Gds, *Ggus, *Agu;
   float *PBd, *PAd, *PBg, *PBu, *PAgu;
-  int sBd, sAd, sBg, sAgu;
+  float *Gpd, *Gpg, *Gpu;      // row partials of the one-pass dY sides (null: two passes)
+  RowColPlan rcd, rcg, rcu;    // one pass over dY, de, du
+  int sBd, sAd, sBg, sBu, sAgu;
 };
 size_t plan_mlp_bwd(const lora_mlp_shape& sh, char* base, MlpBwdWs* w) {
   Carve c{base};
@@ -286,15 +292,22 @@ size_t plan_mlp_bwd(const lora_mlp_shape& sh, char* base, MlpBwdWs* w) {
   w->Gds = c.take<bf16>(M * rd);
   w->Ggus = c.take<bf16>(M * rgu);
   w->Agu = c.take<bf16>(rgu * H);
-  w->sBd = colreduce_splits(M, H);
+  w->rcd = dy_plan(M, H, rd);
+  w->rcg = dy_plan(M, I, rg);
+  w->rcu = dy_plan(M, I, ru);
+  w->sBd = w->rcd.pm > 0 ? w->rcd.pm : colreduce_splits(M, H);
   w->sAd = colreduce_splits(M, I);
-  w->sBg = w->sAd;
+  w->sBg = w->rcg.pm > 0 ? w->rcg.pm : colreduce_splits(M, I);
+  w->sBu = w->rcu.pm > 0 ? w->rcu.pm : colreduce_splits(M, I);
   w->sAgu = colreduce_splits(M, H);
   w->PBd = c.take<float>(w->sBd * H * rd);
   w->PAd = c.take<float>(w->sAd * I * rd);
   w->PBg = c.take<float>(w->sBg * I * rg);
-  w->PBu = c.take<float>(w->sBg * I * ru);
+  w->PBu = c.take<float>(w->sBu * I * ru);
   w->PAgu = c.take<float>(w->sAgu * H * rgu);
+  w->Gpd = w->rcd.pm > 0 ? c.take<float>((int64_t)w->rcd.pn * M * rd) : nullptr;
+  w->Gpg = w->rcg.pm > 0 ? c.take<float>((int64_t)w->rcg.pn * M * rg) : nullptr;
+  w->Gpu = w->rcu.pm > 0 ? c.take<float>((int64_t)w->rcu.pn * M * ru) : nullptr;
   return c.off;
 }
 
@@ -437,6 +450,46 @@ ColReduceDesc cr_desc(int64_t rows, int64_t K, int R, const void* S, const void*
   d.err = err;
   d.timeout_ns = wait_timeout_ns();
   return d;
+}
+
+// The two rank-r products of one projection's backward that read the same S [M, K] (row stride
+// lds): the dB partials part[split][K][R] = S^T T per row split and gout [M, R] (row stride ldg) =
+// bf16(s S U) with U [K, R].  One rowcol pass (plan pl, row partials in gp) when pl.pm > 0, else a
+// colreduce pass and a rowproj pass.
+cudaError_t dy_side(const RowColPlan& pl, int64_t M, int64_t K, int R, const void* S, int64_t lds, const void* U,
+                    const void* T, int64_t ldt, float* part, int splits, float* gp, float s, bf16* gout, int64_t ldg,
+                    uint32_t* err, cudaStream_t st) {
+  cudaError_t e;
+  if (pl.pm > 0) {
+    RowColDesc d;
+    d.rows = M;
+    d.K = K;
+    d.R = R;
+    d.S = static_cast<const bf16*>(S);
+    d.lds = lds;
+    d.U = static_cast<const bf16*>(U);
+    d.ldu = R;
+    d.T = static_cast<const bf16*>(T);
+    d.ldt = ldt;
+    d.gpart = gp;
+    d.part = part;
+    d.pm = pl.pm;
+    d.pn = pl.pn;
+    d.nb = pl.nb;
+    d.err = err;
+    d.timeout_ns = wait_timeout_ns();
+    if ((e = rowcol(d, st)) != cudaSuccess) return e;
+    return gpart_sum(gp, pl.pn, M, R, s, gout, ldg, st);
+  }
+  ColReduceDesc c = cr_desc(M, K, R, S, T, ldt, part, splits, err);
+  c.lds = lds;
+  if ((e = colreduce(c, st)) != cudaSuccess) return e;
+  RowProjDesc d = rp_desc(M, K, R, S, U, true, err);
+  d.lds = lds;
+  d.out_b = gout;
+  d.scale_b = s;
+  d.ldo = ldg;
+  return rowproj(d, st);
 }
 
 // K = B^T T (fp32 [r, r]) for bf16 B, T [rows, r]: a column reduction of B against T on the warp
@@ -705,7 +758,7 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       d.nb = w.rc.nb;
       d.err = w.err;
       CK(rowcol(d, st));
-      CK(gpart_sum(w.Gp, w.rc.pn, M, r, s, static_cast<bf16*>(w.Gs), st));   // s*G = s * dY B
+      CK(gpart_sum(w.Gp, w.rc.pn, M, r, s, static_cast<bf16*>(w.Gs), r, st));   // s*G = s * dY B
     } else {
       {  // dB partials (dY^T Z) and column sums of dY, one pass over dY
         ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
@@ -1484,14 +1537,8 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     return LORA_OK;
   }
   const bf16* Zgu = static_cast<const bf16*>(Zgu_saved);
-  // down projection: dBd partials (dY^T Zd), sd*Gd = sd dY Bd
-  CK(colreduce(cr_desc(M, H, rd, dY, Zd_saved, rd, w.PBd, w.sBd, w.err), st));
-  {
-    RowProjDesc d = rp_desc(M, H, rd, dY, down->B, true, w.err);
-    d.out_b = w.Gds;
-    d.scale_b = down->s;
-    CK(rowproj(d, st));
-  }
+  // down projection: dBd partials (dY^T Zd) and sd*Gd = sd dY Bd
+  CK(dy_side(w.rcd, M, H, rd, dY, H, down->B, Zd_saved, rd, w.PBd, w.sBd, w.Gpd, down->s, w.Gds, rd, w.err, st));
   if (Ip != I) CK(cudaMemsetAsync(w.dedu, 0, (size_t)M * 2 * Ip * 2, st));
   {  // dh = dY Wd + (sd Gd) Ad, gated backward in the epilogue -> de, du
     TcGemmDesc d;
@@ -1525,28 +1572,11 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
     CK(tc_gemm(d, st));
   }
   CK(colreduce(cr_desc(M, I, rd, h_saved, w.Gds, rd, w.PAd, w.sAd, w.err), st));     // h^T (sd Gd)
-  {  // de^T Zg and du^T Zu
-    ColReduceDesc d = cr_desc(M, I, rg, w.dedu, Zgu, rgu, w.PBg, w.sBg, w.err);
-    d.lds = 2 * Ip;
-    CK(colreduce(d, st));
-    ColReduceDesc d2 = cr_desc(M, I, ru, w.dedu + Ip, Zgu + rg, rgu, w.PBu, w.sBg, w.err);
-    d2.lds = 2 * Ip;
-    CK(colreduce(d2, st));
-  }
-  {  // [sg Gg | su Gu] = [sg de Bg | su du Bu]
-    RowProjDesc d = rp_desc(M, I, rg, w.dedu, gate->B, true, w.err);
-    d.lds = 2 * Ip;
-    d.out_b = w.Ggus;
-    d.scale_b = gate->s;
-    d.ldo = rgu;
-    CK(rowproj(d, st));
-    RowProjDesc d2 = rp_desc(M, I, ru, w.dedu + Ip, up->B, true, w.err);
-    d2.lds = 2 * Ip;
-    d2.out_b = w.Ggus + rg;
-    d2.scale_b = up->s;
-    d2.ldo = rgu;
-    CK(rowproj(d2, st));
-  }
+  // gate and up: the dBg / dBu partials (de^T Zg, du^T Zu) and [sg Gg | su Gu] = [sg de Bg | su du Bu]
+  CK(dy_side(w.rcg, M, I, rg, w.dedu, 2 * Ip, gate->B, Zgu, rgu, w.PBg, w.sBg, w.Gpg, gate->s, w.Ggus, rgu, w.err,
+             st));
+  CK(dy_side(w.rcu, M, I, ru, w.dedu + Ip, 2 * Ip, up->B, Zgu + rg, rgu, w.PBu, w.sBu, w.Gpu, up->s, w.Ggus + rg,
+             rgu, w.err, st));
   CK(concat_rows_bf16(static_cast<const bf16*>(gate->A), rg, static_cast<const bf16*>(up->A), ru, H, w.Agu, st));
   if (dX) {  // dX = [de | du] [Wg ; Wu] + [sg Gg | su Gu] [Ag ; Au]
     TcGemmDesc d;
@@ -1584,7 +1614,7 @@ lora_status lora_mlp_swiglu_bwd(const lora_mlp_shape* sh, const void* X, const l
                          fin_dA(rd, I, Partial{w.PAd, w.sAd, rd, 0}, 1.f, nullptr, dAd),
                          fin_dB(H, rd, Partial{w.PBd, w.sBd, rd, 0}, down->s, nullptr, dBd),
                          fin_dB(I, rg, Partial{w.PBg, w.sBg, rg, 0}, gate->s, nullptr, dBg),
-                         fin_dB(I, ru, Partial{w.PBu, w.sBg, ru, 0}, up->s, nullptr, dBu)};
+                         fin_dB(I, ru, Partial{w.PBu, w.sBu, ru, 0}, up->s, nullptr, dBu)};
   CK(finalize_batch(fin, 6, st));
   return LORA_OK;
 }

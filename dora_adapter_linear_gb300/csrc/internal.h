@@ -179,8 +179,9 @@ struct RowColDesc {
   uint64_t timeout_ns = 2000000000ull;
 };
 cudaError_t rowcol(const RowColDesc& d, cudaStream_t st);
-// out [rows, R] = bf16(scale * sum over the pn partials of gpart)
-cudaError_t gpart_sum(const float* gpart, int pn, int64_t rows, int R, float scale, bf16* out, cudaStream_t st);
+// out [rows, R] (row stride ldo) = bf16(scale * sum over the pn partials of gpart)
+cudaError_t gpart_sum(const float* gpart, int pn, int64_t rows, int R, float scale, bf16* out, int64_t ldo,
+                      cudaStream_t st);
 
 // ------------------------------------------------------------------ small kernels (templated on T)
 template <typename T>

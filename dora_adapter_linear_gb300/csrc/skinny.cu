@@ -883,8 +883,10 @@ cudaError_t rowcol(const RowColDesc& d, cudaStream_t st) {
   return cudaErrorInvalidValue;
 }
 
-// out[i] = bf16(scale * sum_p gpart[p][i]) over rows * R elements (R a multiple of 8)
-__global__ void gpart_sum_kernel(const float* __restrict__ gp, int pn, int64_t n, float scale, bf16* __restrict__ out) {
+// out[row][j] (row stride ldo) = bf16(scale * sum_p gpart[p][row][j]) over rows x R elements (R a
+// multiple of 8, so a group of four never straddles rows)
+__global__ void gpart_sum_kernel(const float* __restrict__ gp, int pn, int64_t n, int R, float scale,
+                                 bf16* __restrict__ out, int64_t ldo) {
   pdl_wait();
   if (threadIdx.x == 0) pdl_trigger();
   const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
@@ -897,13 +899,15 @@ __global__ void gpart_sum_kernel(const float* __restrict__ gp, int pn, int64_t n
     a.z += v.z;
     a.w += v.w;
   }
-  *reinterpret_cast<uint2*>(out + i) = make_uint2(pack_bf16x2(scale * a.x, scale * a.y), pack_bf16x2(scale * a.z, scale * a.w));
+  *reinterpret_cast<uint2*>(out + (i / R) * ldo + i % R) =
+      make_uint2(pack_bf16x2(scale * a.x, scale * a.y), pack_bf16x2(scale * a.z, scale * a.w));
 }
 
-cudaError_t gpart_sum(const float* gpart, int pn, int64_t rows, int R, float scale, bf16* out, cudaStream_t st) {
+cudaError_t gpart_sum(const float* gpart, int pn, int64_t rows, int R, float scale, bf16* out, int64_t ldo,
+                      cudaStream_t st) {
   const int64_t n = rows * R;
   if (n <= 0) return cudaSuccess;
-  if (R % 8 || pn <= 0) return cudaErrorInvalidValue;
+  if (R % 8 || pn <= 0 || ldo < R || ldo % 4) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3((unsigned)((n / 4 + 255) / 256), 1, 1);
@@ -911,7 +915,7 @@ cudaError_t gpart_sum(const float* gpart, int pn, int64_t rows, int R, float sca
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_attr(&attr[0]);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gpart_sum_kernel, gpart, pn, n, scale, out);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gpart_sum_kernel, gpart, pn, n, R, scale, out, ldo);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
