@@ -477,6 +477,28 @@ def test_w8a8_quantize_bit_exact(ops):
     assert_close(Z, f64(X.cpu()) @ f64(t["A"]).T, "bf16", "Z")
 
 
+@pytest.mark.parametrize("cols,r", [(1032, 8), (3072, 32), (6400, 24), (6408, 16), (1024, 40)])
+def test_w8a8_quantize_with_z_shapes(ops, cols, r):
+    """Codes and scales bit-exact and Z within the bf16 bar over column counts with several 64-wide
+    stages and a ragged last one, ranks from 8 to 40 (more than one rank-r column chunk per warp
+    at 40), a zero row and a row with one dominant entry; both code formats."""
+    g = torch.Generator().manual_seed(cols + r)
+    M = 200
+    X = (torch.randn(M, cols, generator=g) * 0.5).to(torch.bfloat16)
+    X[3] = 0
+    X[5, 7] = 40.0                                  # one dominant entry in a row
+    A = (torch.randn(r, cols, generator=g) / cols ** 0.5).to(torch.bfloat16)
+    rq, rs = O.quantize_rows(X.float().numpy())
+    Xq, sx, Z = ops.w8a8_quantize_rows(gpu(X), gpu(A))
+    np.testing.assert_array_equal(Xq.cpu().numpy(), rq)
+    np.testing.assert_array_equal(sx.cpu().numpy(), rs)
+    assert_close(Z, f64(X) @ f64(A).T, "bf16", "Z")
+    Xc, sx2, Z2 = ops.w8a8_quantize_rows_bf16(gpu(X), gpu(A))
+    np.testing.assert_array_equal(Xc.float().cpu().numpy(), rq.astype(np.float32))
+    np.testing.assert_array_equal(sx2.cpu().numpy(), rs)
+    assert torch.equal(Z, Z2)
+
+
 @pytest.mark.parametrize("bias", [False, True])
 def test_w8a8_acc_bit_exact_and_epilogue(ops, bias):
     case, t, Wq, sw, Xq, sx = w8_inputs(M=300, d_in=352, d_out=264, bias=bias)
