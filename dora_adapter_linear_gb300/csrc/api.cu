@@ -77,6 +77,13 @@ lora_status check_shape(const lora_shape* sh) {
 // 0.396 ms against 0.184 ms for the separate pass plus the CTA-pair GEMM: the warps that read every
 // staged X tile a second time and hold its stage until they are done halve the tensor pipe's rate.
 // So the separate pass stays the default.
+// The DoRA-rows dX product scales each staged dY tile by c inside the GEMM instead of reading the
+// slab copy of dY o c (same bits; slower).
+bool kscale_dx() {
+  const char* e = getenv("LORA_GB300_DORA_KSCALE");
+  return e && atoi(e) == 1;
+}
+
 bool fused_down_projection(int r) {
   if (r < 8 || r > 32 || r % 8) return false;
   const char* e = getenv("LORA_GB300_FUSED_Z");
@@ -161,10 +168,52 @@ size_t plan_dora_fwd(const lora_shape& sh, char* base, DoraFwdWs* w) {
   return c.off;
 }
 
+// Row slabs of the DoRA-rows backward (bf16): the column pass writes dY o c for one slab of rows
+// into a buffer of at most kDoraSlabBytes and the dX GEMM of that slab reads it back at once,
+// mostly from L2, before the next slab overwrites it; the buffer's size does not grow with M.  The
+// slab height (a multiple of 128 rows) is the one whose GEMMs finish the whole dX product in the
+// fewest waves of 128 x 256 tiles over the SMs, the tallest among equals.
+constexpr int64_t kDoraSlabBytes = 64ll << 20;
+struct DoraSlabs {
+  int64_t rows = 0, count = 0;
+  int splits = 1, splits_last = 1;   // column-pass row splits of a full slab and of the last one
+};
+DoraSlabs dora_slabs(int64_t M, int64_t in, int64_t out, int64_t r) {
+  DoraSlabs s;
+  if (M <= 0) return s;
+  const int64_t mt = (M + 127) / 128, nt = (in + 255) / 256, sms = num_sms_current();
+  int64_t cap = kDoraSlabBytes / (out * 2) / 128;
+  if (cap < 1) cap = 1;
+  const char* e = getenv("LORA_GB300_DORA_SLAB_ROWS");   // a fixed slab height (rounded up to 128 rows)
+  const int64_t forced = e ? (atoll(e) + 127) / 128 : 0;
+  if (forced > 0) {
+    s.rows = forced >= mt ? M : forced * 128;
+  } else if (cap >= mt) {
+    s.rows = M;
+  } else {
+    int64_t best_h = cap, best_w = (int64_t)1 << 62;
+    for (int64_t h = cap; h >= 1; --h) {
+      const int64_t n = mt / h, rem = mt - n * h;
+      const int64_t w = n * ((h * nt + sms - 1) / sms) + (rem ? (rem * nt + sms - 1) / sms : 0);
+      if (w < best_w) {
+        best_w = w;
+        best_h = h;
+      }
+    }
+    s.rows = best_h * 128;
+  }
+  s.count = (M + s.rows - 1) / s.rows;
+  s.splits = colreduce_splits(s.rows, out, (int)r, true);
+  s.splits_last = colreduce_splits(M - (s.count - 1) * s.rows, out, (int)r, true);
+  return s;
+}
+
 struct DoraBwdWs {
   uint32_t* err;
   float *c, *g, *dot, *csum, *dotp, *csump, *Kr, *Kg, *Gw;
   void *Bc, *gB, *Gs, *Zrec;
+  bf16* slab;        // [slab rows, out] dY o c of one slab (bf16)
+  DoraSlabs sl;
   float *PB, *PA, *PW;
   int splitsB, splitsA, splitsW;
 };
@@ -184,8 +233,11 @@ size_t plan_dora_bwd(const lora_shape& sh, char* base, DoraBwdWs* w) {
   w->gB = c.take<char>(out * r * es);
   w->Gs = c.take<char>(M * r * es);
   w->Zrec = c.take<char>(M * r * es);
+  w->slab = nullptr;
   if (sh.dtype == LORA_BF16) {
-    w->splitsB = colreduce_splits(M, out);
+    w->sl = dora_slabs(M, in, out, r);
+    w->slab = c.take<bf16>(w->sl.rows * out);
+    w->splitsB = w->sl.count > 0 ? (int)((w->sl.count - 1) * w->sl.splits + w->sl.splits_last) : 1;   // the slabs' in turn
     w->splitsA = colreduce_splits(M, in);
     w->splitsW = colreduce_splits(out, in);
     w->PB = c.take<float>(w->splitsB * out * r);
@@ -1206,27 +1258,44 @@ lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       CK(rowproj(d, st));
       Z = w.Zrec;
     }
-    {  // one pass over dY and Y: dY^T Z partials, colsum(dY) and colsum(dY o Y)
-      ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
-      d.Y = static_cast<const bf16*>(Y);
-      d.ldy = out;
-      d.colsum = w.csump;
-      d.coldot = w.dotp;
-      CK(colreduce(d, st));
-    }
-    CK(dora_dc<bf16>(out, w.dotp, w.csump, w.splitsB, static_cast<const bf16*>(bias), w.c, n_saved, mb, eps, w.g,
-                     static_cast<bf16*>(dm), static_cast<bf16*>(dbias), st));
     CK(scale_rows<bf16>(static_cast<const bf16*>(B), out, r, w.c, 1.f, static_cast<bf16*>(w.Bc), st));
-    CK(scale_rows<bf16>(static_cast<const bf16*>(B), out, r, w.g, 1.f, static_cast<bf16*>(w.gB), st));
     {  // s * G = s (dY o c) B  =  s dY (c o B)
       RowProjDesc d = rp_desc(M, out, r, dY, w.Bc, true, w.err);
       d.out_b = static_cast<bf16*>(w.Gs);
       d.scale_b = s;
       CK(rowproj(d, st));
     }
-    // dX = (dY o c) W0 + s G A: dP = dY o c is formed tile by tile inside the GEMM (its A tiles are
-    // scaled by c in shared memory), so no [M, out] copy of it is ever written
-    if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, w.c, w.err), st));
+    // Slab by slab: one pass over dY and Y (dY^T Z partials, colsum(dY), colsum(dY o Y)) that also
+    // writes dP = dY o c for the slab's rows, then dX = dP W0 + s G A for those rows from that copy.
+    // With the in-GEMM scaling (LORA_GB300_DORA_KSCALE=1) the passes write no copy and one dX GEMM
+    // scales each staged dY tile by c in shared memory instead.
+    const bool kscale = kscale_dx();
+    const char* dYb = static_cast<const char*>(dY);
+    const char* Yb = static_cast<const char*>(Y);
+    int soff = 0;
+    for (int64_t i = 0, row0 = 0; i < w.sl.count; ++i, row0 += w.sl.rows) {
+      const int64_t rows = M - row0 < w.sl.rows ? M - row0 : w.sl.rows;
+      const int sp = i + 1 < w.sl.count ? w.sl.splits : w.sl.splits_last;
+      ColReduceDesc d = cr_desc(rows, out, r, dYb + row0 * out * 2, static_cast<const bf16*>(Z) + row0 * r, r,
+                                w.PB + (int64_t)soff * out * r, sp, w.err);
+      d.Y = reinterpret_cast<const bf16*>(Yb + row0 * out * 2);
+      d.ldy = out;
+      d.colsum = w.csump + (int64_t)soff * out;
+      d.coldot = w.dotp + (int64_t)soff * out;
+      if (dX && !kscale) {
+        d.sc = w.c;
+        d.sc_out = w.slab;
+      }
+      CK(colreduce(d, st));
+      if (dX && !kscale)
+        CK(tc_gemm(dx_desc(rows, in, out, w.slab, W0, static_cast<const bf16*>(w.Gs) + row0 * r, A, r,
+                           static_cast<bf16*>(dX) + row0 * in, nullptr, w.err), st));
+      soff += sp;
+    }
+    if (dX && kscale) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, w.c, w.err), st));
+    CK(dora_dc<bf16>(out, w.dotp, w.csump, w.splitsB, static_cast<const bf16*>(bias), w.c, n_saved, mb, eps, w.g,
+                     static_cast<bf16*>(dm), static_cast<bf16*>(dbias), st));
+    CK(scale_rows<bf16>(static_cast<const bf16*>(B), out, r, w.g, 1.f, static_cast<bf16*>(w.gB), st));
     CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA, w.err), st));        // X^T (s G)
     CK(colreduce(cr_desc(out, in, r, W0, w.gB, r, w.PW, w.splitsW, w.err), st));     // W0^T (g o B)
     CK(gram_rows<bf16>(static_cast<const bf16*>(A), r, in, w.Kr, st));

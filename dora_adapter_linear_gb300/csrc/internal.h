@@ -142,11 +142,15 @@ struct ColReduceDesc {
   int j0 = 0;                  // first column of part written
   float* colsum = nullptr;     // [splits, K] or null
   float* coldot = nullptr;     // [splits, K] or null
+  const float* sc = nullptr;   // with sc_out (and Y): column scales [K]
+  bf16* sc_out = nullptr;      // optional column-scaled copy of S: sc_out[row K + k] = bf16(S[row, k] sc[k])
   int splits = 1;
   uint32_t* err = nullptr;     // device error word for bounded waits
   uint64_t timeout_ns = 2000000000ull;
 };
-int colreduce_splits(int64_t rows, int64_t K);
+// Row splits of a colreduce pass over [rows, K] at rank R (with or without the second input Y):
+// the split count whose waves of resident CTAs finish the pass soonest.
+int colreduce_splits(int64_t rows, int64_t K, int R = 16, bool has_y = false);
 cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st);
 
 // One pass over S [rows, K] for both rank-r products that read it:

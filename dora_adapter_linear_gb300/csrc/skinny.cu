@@ -389,6 +389,15 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
   for (int i = 0; i < R / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
   float csum = 0.f, cdot = 0.f;
   const int my_col = tid & 63, my_par = tid >> 6;   // column sums: 2 row phases x 64 columns
+  const int c8 = tid & 7;                            // scaled copy: 16-byte chunk of this thread
+  float sc8[8];
+  const bool copy = HAS_Y && d.sc_out != nullptr && k0 + c8 * 8 < d.K;
+  if (copy) {   // the 8 scales of this thread's chunk (K is a multiple of 8)
+    const float4 lo = __ldg(reinterpret_cast<const float4*>(d.sc + k0 + c8 * 8));
+    const float4 hi = __ldg(reinterpret_cast<const float4*>(d.sc + k0 + c8 * 8 + 4));
+    sc8[0] = lo.x; sc8[1] = lo.y; sc8[2] = lo.z; sc8[3] = lo.w;
+    sc8[4] = hi.x; sc8[5] = hi.y; sc8[6] = hi.z; sc8[7] = hi.w;
+  }
   for (int rc = 0; rc < nrc; ++rc) {
     const int s = rc % NST;
     const uint32_t ph = (uint32_t)(rc / NST) & 1u;
@@ -411,6 +420,23 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
         else ldsm_x2_t(b0, b1, sT + swz(row, nt, C::TPITCH, C::TMASK));
         mma_bf16_16816(acc[nt], a, b0, b1);
         if (nt + 1 < R / 8) mma_bf16_16816(acc[nt + 1], a, b2, b3);
+      }
+    }
+    if (copy) {
+      // column-scaled copy of the S tile: thread tid owns chunk c8 of rows tid / 8 + 16 i
+      const int64_t rb = r_begin + (int64_t)rc * BR;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = (tid >> 3) + 16 * i;
+        if (rb + r >= r_end) break;
+        uint4 v = *reinterpret_cast<const uint4*>(tile + swz(r, c8, 128, 7));
+        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack_bf16x2(w[e]);
+          w[e] = pack_bf16x2(f.x * sc8[2 * e], f.y * sc8[2 * e + 1]);
+        }
+        *reinterpret_cast<uint4*>(d.sc_out + (rb + r) * d.K + k0 + c8 * 8) = v;
       }
     }
     if (SUMS) {
@@ -458,13 +484,25 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
   }
 }
 
-int colreduce_splits(int64_t rows, int64_t K) {
+// CTAs of colreduce_kernel<R, HAS_Y, *> resident per SM, from its shared memory (each CTA also
+// holds 1 KB reserved by the system; 228 KB per SM).
+static int colreduce_ctas_per_sm(int R, bool has_y) {
+  int smem;
+  if (R <= 8) smem = has_y ? cr::Cfg<8, true>::SMEM : cr::Cfg<8, false>::SMEM;
+  else if (R <= 16) smem = has_y ? cr::Cfg<16, true>::SMEM : cr::Cfg<16, false>::SMEM;
+  else if (R <= 32) smem = has_y ? cr::Cfg<32, true>::SMEM : cr::Cfg<32, false>::SMEM;
+  else smem = has_y ? cr::Cfg<64, true>::SMEM : cr::Cfg<64, false>::SMEM;
+  const int n = (228 * 1024) / (smem + 1024);
+  return n < 1 ? 1 : n;
+}
+
+int colreduce_splits(int64_t rows, int64_t K, int R, bool has_y) {
   const int64_t kb = (K + cr::BKC - 1) / cr::BKC;
-  // Row splits per column block: with three CTAs resident per SM, a launch of kb * s CTAs runs
-  // in ceil(kb s / slots) waves of CTAs that each stream ceil(rows / (64 s)) row stages plus a
+  // Row splits per column block: with n CTAs resident per SM, a launch of kb * s CTAs runs in
+  // ceil(kb s / slots) waves of CTAs that each stream ceil(rows / (64 s)) row stages plus a
   // fixed cost of about four stages (ring fill, partial sums); pick the s with the least total,
   // the fewest splits among equals.  A half-empty last wave cost ~1% of a LoRA step.
-  const int64_t slots = 3LL * num_sms_current();
+  const int64_t slots = (int64_t)colreduce_ctas_per_sm(R, has_y) * num_sms_current();
   int64_t maxs = (rows + cr::BR - 1) / cr::BR;
   if (maxs > 64) maxs = 64;
   int64_t best = 1;
@@ -509,8 +547,8 @@ static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_attr(&attr[0]);
-  // algorithmic HBM bytes: S (and Y) once, T, the fp32 partials (and column sums)
-  const double bytes = 2.0 * d.rows * d.K * (HAS_Y ? 2.0 : 1.0) + 2.0 * d.rows * R +
+  // algorithmic HBM bytes: S (and Y, and the scaled copy) once, T, the fp32 partials (and column sums)
+  const double bytes = 2.0 * d.rows * d.K * (HAS_Y ? (d.sc_out ? 3.0 : 2.0) : 1.0) + 2.0 * d.rows * R +
                        4.0 * d.splits * d.K * (R + (SUMS ? 2.0 : 0.0));
   prof_mark(st, true, bytes, 1);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k, P);
@@ -521,6 +559,7 @@ static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
 
 cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st) {
   if (d.K <= 0) return cudaSuccess;
+  if (d.sc_out && (!d.Y || !d.sc || d.K % 8)) return cudaErrorInvalidValue;   // the copy rides on the Y pass
   if (d.R > 64) {   // columns of T in chunks of 64: one pass over S per chunk
     if (d.R > 512 || d.R % 8) return cudaErrorInvalidValue;
     for (int c0 = 0; c0 < d.R; c0 += 64) {
@@ -533,6 +572,7 @@ cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st) {
         c.Y = nullptr;
         c.colsum = nullptr;
         c.coldot = nullptr;
+        c.sc_out = nullptr;   // and so does the scaled copy
       }
       const cudaError_t e = colreduce(c, st);
       if (e != cudaSuccess) return e;

@@ -246,6 +246,10 @@ lora_status dora_linear_fwd(const lora_shape* sh, const void* X, const void* W0,
  * gradients for A, B and the magnitude).
  *   Y, Z_saved (or NULL to recompute), n_saved and V_saved from the forward.
  *   dX [M, d_in] or NULL; dA [r, d_in]; dB [d_out, r]; dm [d_out]; dbias [d_out] or NULL.
+ * bf16: dY o c is formed one slab of rows at a time (at most 64 MiB of the workspace, a multiple
+ * of 128 rows chosen so that the slabs' dX GEMMs fill whole waves); the workspace never holds an
+ * [M, d_out] copy of it.  The environment variable LORA_GB300_DORA_KSCALE=1 forms it inside the
+ * dX GEMM instead (same bits, no copy at all, slower).
  */
 lora_status dora_linear_bwd(const lora_shape* sh, const void* X, const void* W0, const void* A,
                             const void* B, const void* m, const void* bias, const void* Y,

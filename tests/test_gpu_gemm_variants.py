@@ -74,12 +74,26 @@ def test_lora_even_m_tiles(ops, variant, cap, M, monkeypatch):
     _ws_ok(ops)
 
 
+def _dora_bwd(ops, g, case):
+    r0 = ops.dora_rownorm2(g["W0"])
+    Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps, g["bias"])
+    return Y, ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V, g["dY"],
+                                  case.s, case.eps, need_dbias=True)
+
+
 @pytest.mark.parametrize("cap", ["0", "4"])
 @pytest.mark.parametrize("M", [500, 1024])
-def test_dora_kscaled_dx(ops, variant, cap, M, monkeypatch):
-    """dP = dY o c is formed inside the dX GEMM: the scaling warps multiply each staged dY tile by
-    its 64 scales in shared memory (no [M, out] copy); ragged M, N and K, several tiles per CTA."""
+@pytest.mark.parametrize("mode", ["kscale", "slabs"])
+def test_dora_kscaled_dx(ops, variant, cap, M, mode, monkeypatch):
+    """dP = dY o c for the dX product, either formed inside the dX GEMM (the scaling warps multiply
+    each staged dY tile by its 64 scales in shared memory) or written by the column pass one slab of
+    rows at a time (slabs of 256 rows here: two to four slabs, the last one ragged) and read back by
+    one dX GEMM per slab; ragged M, N and K, several tiles per CTA."""
     monkeypatch.setenv("LORA_GB300_MAX_CTAS", cap)
+    if mode == "kscale":
+        monkeypatch.setenv("LORA_GB300_DORA_KSCALE", "1")
+    else:
+        monkeypatch.setenv("LORA_GB300_DORA_SLAB_ROWS", "256")
     case = D.scaled(D.WORKLOADS["dora_4096x11008_bf16"], M=M, d_in=328, d_out=776, r=32)
     t = D.make_linear(case)
     g = {k: v.to(DEV) for k, v in t.items()}
@@ -135,4 +149,28 @@ def test_qkv_multistep_tail(ops, variant, monkeypatch):
     for i in range(3):
         assert_close(dA[i], rA[i], "bf16", f"dA{i}")
         assert_close(dB[i], rB[i], "bf16", f"dB{i}")
+    _ws_ok(ops)
+
+
+@pytest.mark.parametrize("slab_rows", [None, "128", "384"])
+def test_dora_slab_copy_matches_kscale_bits(ops, variant, slab_rows, monkeypatch):
+    """The slab copy of dY o c (bf16 of the fp32 product, as the scaling warps round it) and the
+    in-GEMM scaling give the same dX bits, and with the same slab split of the column pass the same
+    dA, dB, dm and dbias bits."""
+    monkeypatch.setenv("LORA_GB300_MAX_CTAS", "6")
+    if slab_rows:
+        monkeypatch.setenv("LORA_GB300_DORA_SLAB_ROWS", slab_rows)
+    case = D.scaled(D.WORKLOADS["dora_4096x11008_bf16"], M=900, d_in=264, d_out=536, r=16, bias=True)
+    t = D.make_linear(case)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    _, slab = _dora_bwd(ops, g, case)
+    monkeypatch.setenv("LORA_GB300_DORA_KSCALE", "1")
+    _, ks = _dora_bwd(ops, g, case)
+    for a, b, nm in zip(slab, ks, ("dX", "dA", "dB", "dm", "dbias")):
+        assert torch.equal(a, b), nm
+    X, W0, A, B, m, bias, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "m", "bias", "dY"))
+    ref = O.dora_linear_bwd(X, W0, A, B, m, case.s, dY, case.eps)
+    for got, rr, nm in zip(slab, (ref[0], ref[1], ref[2], ref[3][None], ref[4][None]),
+                           ("dX", "dA", "dB", "dm", "dbias")):
+        assert_close(got, rr, "bf16", nm)
     _ws_ok(ops)
