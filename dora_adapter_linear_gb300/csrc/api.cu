@@ -138,8 +138,8 @@ size_t plan_lin_bwd(const lora_shape& sh, char* base, LinBwdWs* w) {
   w->Gp = nullptr;
   if (sh.dtype == LORA_BF16) {
     w->rc = dy_plan(sh.M, sh.d_out, sh.r);
-    w->splitsB = w->rc.pm > 0 ? w->rc.pm : colreduce_splits(sh.M, sh.d_out);
-    w->splitsA = colreduce_splits(sh.M, sh.d_in);
+    w->splitsB = w->rc.pm > 0 ? w->rc.pm : colreduce_splits(sh.M, sh.d_out, (int)sh.r);
+    w->splitsA = colreduce_splits(sh.M, sh.d_in, (int)sh.r);
     w->PB = c.take<float>((size_t)w->splitsB * sh.d_out * sh.r);
     w->PA = c.take<float>((size_t)w->splitsA * sh.d_in * sh.r);
     w->csum = c.take<float>((size_t)w->splitsB * sh.d_out);
@@ -238,8 +238,8 @@ size_t plan_dora_bwd(const lora_shape& sh, char* base, DoraBwdWs* w) {
     w->sl = dora_slabs(M, in, out, r);
     w->slab = c.take<bf16>(w->sl.rows * out);
     w->splitsB = w->sl.count > 0 ? (int)((w->sl.count - 1) * w->sl.splits + w->sl.splits_last) : 1;   // the slabs' in turn
-    w->splitsA = colreduce_splits(M, in);
-    w->splitsW = colreduce_splits(out, in);
+    w->splitsA = colreduce_splits(M, in, (int)r);
+    w->splitsW = colreduce_splits(out, in, (int)r);
     w->PB = c.take<float>(w->splitsB * out * r);
     w->PA = c.take<float>(w->splitsA * in * r);
     w->PW = c.take<float>(w->splitsW * in * r);
@@ -269,7 +269,7 @@ size_t plan_dora_cols_fwd(const lora_shape& sh, char* base, DoraColsFwdWs* w) {
   Carve c{base};
   const int64_t out = sh.d_out, in = sh.d_in, r = sh.r, M = sh.M;
   w->err = c.take<uint32_t>(kErrBytes / 4);
-  w->splitsW = colreduce_splits(out, in);
+  w->splitsW = colreduce_splits(out, in, (int)r);
   w->PU = c.take<float>(w->splitsW * in * r);
   w->Kb = c.take<float>(r * r);
   w->Gw = c.take<float>(gram_work_floats((int)r));
@@ -290,8 +290,8 @@ size_t plan_dora_cols_bwd(const lora_shape& sh, char* base, DoraColsBwdWs* w) {
   Carve c{base};
   const int64_t out = sh.d_out, in = sh.d_in, r = sh.r, M = sh.M;
   w->err = c.take<uint32_t>(kErrBytes / 4);
-  w->splitsA = colreduce_splits(M, in);
-  w->splitsB = colreduce_splits(M, out);
+  w->splitsA = colreduce_splits(M, in, (int)r, true);   // with dX as the second input
+  w->splitsB = colreduce_splits(M, out, (int)r);
   w->c = c.take<float>(in);
   w->g = c.take<float>(in);
   w->dot = c.take<float>(in);
@@ -347,11 +347,11 @@ size_t plan_mlp_bwd(const lora_mlp_shape& sh, char* base, MlpBwdWs* w) {
   w->rcd = dy_plan(M, H, rd);
   w->rcg = dy_plan(M, I, rg);
   w->rcu = dy_plan(M, I, ru);
-  w->sBd = w->rcd.pm > 0 ? w->rcd.pm : colreduce_splits(M, H);
-  w->sAd = colreduce_splits(M, I);
-  w->sBg = w->rcg.pm > 0 ? w->rcg.pm : colreduce_splits(M, I);
-  w->sBu = w->rcu.pm > 0 ? w->rcu.pm : colreduce_splits(M, I);
-  w->sAgu = colreduce_splits(M, H);
+  w->sBd = w->rcd.pm > 0 ? w->rcd.pm : colreduce_splits(M, H, (int)rd);
+  w->sAd = colreduce_splits(M, I, (int)rd);
+  w->sBg = w->rcg.pm > 0 ? w->rcg.pm : colreduce_splits(M, I, (int)rg);
+  w->sBu = w->rcu.pm > 0 ? w->rcu.pm : colreduce_splits(M, I, (int)ru);
+  w->sAgu = colreduce_splits(M, H, (int)rgu);
   w->PBd = c.take<float>(w->sBd * H * rd);
   w->PAd = c.take<float>(w->sAd * I * rd);
   w->PBg = c.take<float>(w->sBg * I * rg);
@@ -403,11 +403,11 @@ size_t plan_qkv_bwd(const lora_qkv_shape& sh, char* base, QkvBwdWs* w) {
   w->B_blk = c.take<bf16>(qkv_N(sh) * R);
   w->Gs = c.take<bf16>(sh.M * R);
   w->Zrec = c.take<bf16>(sh.M * R);
-  w->splitsA = colreduce_splits(sh.M, sh.d_in);
+  w->splitsA = colreduce_splits(sh.M, sh.d_in, (int)R);
   w->PA = c.take<float>((size_t)w->splitsA * sh.d_in * R);
   for (int l = 0; l < kMaxLeaves; ++l) {
     const bool live = l < sh.L;
-    w->splitsB[l] = live ? colreduce_splits(sh.M, sh.n[l]) : 0;
+    w->splitsB[l] = live ? colreduce_splits(sh.M, sh.n[l], sh.r) : 0;
     w->PB[l] = live ? c.take<float>((size_t)w->splitsB[l] * sh.n[l] * sh.r) : nullptr;
     w->csum[l] = live ? c.take<float>((size_t)w->splitsB[l] * sh.n[l]) : nullptr;
   }
@@ -549,7 +549,7 @@ cudaError_t dy_side(const RowColPlan& pl, int64_t M, int64_t K, int R, const voi
 // order.  `work` holds gram_work_floats(r) floats.
 cudaError_t gram_bf16(const void* B, const void* T, int64_t rows, int r, float* K, float* work, uint32_t* err,
                       cudaStream_t st) {
-  const int splits = colreduce_splits(rows, r);
+  const int splits = colreduce_splits(rows, r, r);
   cudaError_t e = colreduce(cr_desc(rows, r, r, B, T, r, work, splits, err), st);
   if (e != cudaSuccess) return e;
   return sum_splits<float>(work, splits, (int64_t)r * r, K, nullptr, st);
