@@ -572,7 +572,8 @@ def _dropout_workload(args, L, ops, peaks, D, dev, steps, warm, p=0.1):
     name = "lora_dropout_4096_bf16"
     out = {name: {"ms_per_step": ms, "tflops": (f + b) / (ms * 1e-3) / 1e12,
                   "frac_of_bf16_peak": (f + b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                  "note": f"keep mask with p = {p}; unfused: the masked input is written once per call",
+                  "note": f"keep mask with p = {p}; unfused call: the Z and dA passes read the mask beside X "
+                          "(no masked copy of X), the adapter's share of dX is a masked rank-r pass",
                   "roofline": gemm_roofline(L, peaks, ms_ev, steps + 1, False, name)}}
     for buf in ops._WS.values():
         if L.lora_check_device_error(buf) != 0:

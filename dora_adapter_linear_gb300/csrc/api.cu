@@ -506,11 +506,11 @@ ColReduceDesc cr_desc(int64_t rows, int64_t K, int R, const void* S, const void*
 
 // The two rank-r products of one projection's backward that read the same S [M, K] (row stride
 // lds): the dB partials part[split][K][R] = S^T T per row split and gout [M, R] (row stride ldg) =
-// bf16(s S U) with U [K, R].  One rowcol pass (plan pl, row partials in gp) when pl.pm > 0, else a
-// colreduce pass and a rowproj pass.
+// bf16(s S U) with U [K, R], and (when colsum is set) the column sums of S per split.  One rowcol
+// pass (plan pl, row partials in gp) when pl.pm > 0, else a colreduce pass and a rowproj pass.
 cudaError_t dy_side(const RowColPlan& pl, int64_t M, int64_t K, int R, const void* S, int64_t lds, const void* U,
                     const void* T, int64_t ldt, float* part, int splits, float* gp, float s, bf16* gout, int64_t ldg,
-                    uint32_t* err, cudaStream_t st) {
+                    uint32_t* err, cudaStream_t st, float* colsum = nullptr) {
   cudaError_t e;
   if (pl.pm > 0) {
     RowColDesc d;
@@ -525,6 +525,7 @@ cudaError_t dy_side(const RowColPlan& pl, int64_t M, int64_t K, int R, const voi
     d.ldt = ldt;
     d.gpart = gp;
     d.part = part;
+    d.colsum = colsum;
     d.pm = pl.pm;
     d.pn = pl.pn;
     d.nb = pl.nb;
@@ -535,6 +536,7 @@ cudaError_t dy_side(const RowColPlan& pl, int64_t M, int64_t K, int R, const voi
   }
   ColReduceDesc c = cr_desc(M, K, R, S, T, ldt, part, splits, err);
   c.lds = lds;
+  c.colsum = colsum;
   if ((e = colreduce(c, st)) != cudaSuccess) return e;
   RowProjDesc d = rp_desc(M, K, R, S, U, true, err);
   d.lds = lds;
@@ -594,6 +596,17 @@ const char* lora_status_string(int status) {
 
 int lora_abi_version(void) { return 8; }
 
+// Input dropout: with rows of d_in bytes a multiple of 16 the mask is read by TMA next to X in the
+// rank-r passes (Z = Xd A^T, the dA partials Xd^T (s G)), which form Xd = X o mask k in registers;
+// otherwise Xd [M, d_in] is written once into the workspace and those passes read it.
+static bool dropout_fused(const lora_shape& sh) {
+  const char* e = getenv("LORA_GB300_DROPOUT_XD");   // =1: write Xd even when the mask could be fused
+  return sh.d_in % 16 == 0 && !(e && atoi(e) == 1);
+}
+static size_t dropout_xd_bytes(const lora_shape& sh) {
+  return dropout_fused(sh) ? 0 : al256((size_t)sh.M * sh.d_in * 2);
+}
+
 size_t lora_workspace_bytes(int op, const lora_shape* sh) {
   if (check_shape(sh) != LORA_OK) return 0;
   switch (op) {
@@ -603,10 +616,10 @@ size_t lora_workspace_bytes(int op, const lora_shape* sh) {
     case LORA_OP_DORA_BWD: { DoraBwdWs w; return plan_dora_bwd(*sh, nullptr, &w); }
     case LORA_OP_DROPOUT_FWD:
       if (sh->dtype != LORA_BF16) return 0;
-      { LinFwdWs w; return plan_lin_fwd(*sh, nullptr, &w) + al256((size_t)sh->M * sh->d_in * 2); }
+      { LinFwdWs w; return plan_lin_fwd(*sh, nullptr, &w) + dropout_xd_bytes(*sh); }
     case LORA_OP_DROPOUT_BWD:
       if (sh->dtype != LORA_BF16) return 0;
-      { LinBwdWs w; return plan_lin_bwd(*sh, nullptr, &w) + al256((size_t)sh->M * sh->d_in * 2); }
+      { LinBwdWs w; return plan_lin_bwd(*sh, nullptr, &w) + dropout_xd_bytes(*sh); }
     case LORA_OP_DORA_COLS_FWD:
       if (sh->dtype != LORA_BF16) return 0;
       { DoraColsFwdWs w; return plan_dora_cols_fwd(*sh, nullptr, &w); }
@@ -791,39 +804,9 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
       CK(rowproj(d, st));
       Z = w.Zrec;
     }
-    if (w.rc.pm > 0) {  // one pass over dY: G row partials, dB partials (dY^T Z), column sums of dY
-      RowColDesc d;
-      d.rows = M;
-      d.K = out;
-      d.R = r;
-      d.S = static_cast<const bf16*>(dY);
-      d.lds = out;
-      d.U = static_cast<const bf16*>(B);
-      d.ldu = r;
-      d.T = static_cast<const bf16*>(Z);
-      d.ldt = r;
-      d.gpart = w.Gp;
-      d.part = w.PB;
-      d.colsum = dbias ? w.csum : nullptr;
-      d.pm = w.rc.pm;
-      d.pn = w.rc.pn;
-      d.nb = w.rc.nb;
-      d.err = w.err;
-      CK(rowcol(d, st));
-      CK(gpart_sum(w.Gp, w.rc.pn, M, r, s, static_cast<bf16*>(w.Gs), r, st));   // s*G = s * dY B
-    } else {
-      {  // dB partials (dY^T Z) and column sums of dY, one pass over dY
-        ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
-        d.colsum = dbias ? w.csum : nullptr;
-        CK(colreduce(d, st));
-      }
-      {  // s*G = s * dY B
-        RowProjDesc d = rp_desc(M, out, r, dY, B, true, w.err);
-        d.out_b = static_cast<bf16*>(w.Gs);
-        d.scale_b = s;
-        CK(rowproj(d, st));
-      }
-    }
+    // s G = s dY B, the dB partials dY^T Z and the column sums of dY: one rowcol pass over dY
+    CK(dy_side(w.rc, M, out, r, dY, out, B, Z, r, w.PB, w.splitsB, w.Gp, s, static_cast<bf16*>(w.Gs), r, w.err, st,
+               dbias ? w.csum : nullptr));
     if (dX) CK(tc_gemm(dx_desc(M, in, out, dY, W0, w.Gs, A, r, dX, nullptr, w.err), st));
     CK(colreduce(cr_desc(M, in, r, X, w.Gs, r, w.PA, w.splitsA, w.err), st));
     const FinJob fin[2] = {fin_dA(r, in, Partial{w.PA, w.splitsA, r, 0}, 1.f, A, dA),
@@ -863,7 +846,7 @@ lora_status lora_linear_dropout_fwd(const lora_shape* sh, const void* X, const u
   if (!isfinite(keep_scale) || keep_scale < 0.f) return LORA_ERR_INVALID_ARG;
   LinFwdWs w;
   const size_t lin = plan_lin_fwd(*sh, nullptr, &w);
-  if ((e = check_ws(ws, ws_bytes, lin + al256((size_t)sh->M * sh->d_in * 2))) != LORA_OK) return e;
+  if ((e = check_ws(ws, ws_bytes, lin + dropout_xd_bytes(*sh))) != LORA_OK) return e;
   if (s == 0.f && Z_save == nullptr)  // nothing of the adapter branch reaches Y: the plain layer
     return lora_linear_fwd(sh, X, W0, A, B, bias, s, Y, nullptr, ws, lin, stream);
   REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQM(sh->M, Y);
@@ -874,10 +857,19 @@ lora_status lora_linear_dropout_fwd(const lora_shape* sh, const void* X, const u
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
   const int r = (int)sh->r;
-  bf16* Xd = reinterpret_cast<bf16*>(static_cast<char*>(ws) + lin);
-  CK(apply_mask_bf16(static_cast<const bf16*>(X), mask, keep_scale, M, in, Xd, st));
+  const bool fused = dropout_fused(*sh);
+  const bf16* Xa = static_cast<const bf16*>(X);
+  if (!fused) {
+    bf16* Xd = reinterpret_cast<bf16*>(static_cast<char*>(ws) + lin);
+    CK(apply_mask_bf16(static_cast<const bf16*>(X), mask, keep_scale, M, in, Xd, st));
+    Xa = Xd;
+  }
   {  // Z = Xd A^T (saved unscaled) and s Z for the GEMM tail
-    RowProjDesc d = rp_desc(M, in, r, Xd, A, false, w.err);
+    RowProjDesc d = rp_desc(M, in, r, Xa, A, false, w.err);
+    if (fused) {
+      d.mask = mask;
+      d.mask_scale = keep_scale;
+    }
     d.out_a = static_cast<bf16*>(Z_save);
     d.out_b = s != 0.f ? static_cast<bf16*>(w.Zs) : nullptr;
     d.scale_b = s;
@@ -902,7 +894,7 @@ lora_status lora_linear_dropout_bwd(const lora_shape* sh, const void* X, const u
   if (!isfinite(keep_scale) || keep_scale < 0.f) return LORA_ERR_INVALID_ARG;
   LinBwdWs w;
   const size_t lin = plan_lin_bwd(*sh, nullptr, &w);
-  if ((e = check_ws(ws, ws_bytes, lin + al256((size_t)sh->M * sh->d_in * 2))) != LORA_OK) return e;
+  if ((e = check_ws(ws, ws_bytes, lin + dropout_xd_bytes(*sh))) != LORA_OK) return e;
   if (sh->M == 0 || s == 0.f)  // no adapter gradient flows: exactly the plain layer's backward
     return lora_linear_bwd(sh, X, W0, A, B, Z_saved, dY, s, dX, dA, dB, dbias, ws, lin, stream);
   REQM(sh->M, X); REQ(W0); REQ(A); REQ(B); REQM(sh->M, dY); REQ(dA); REQ(dB);
@@ -912,32 +904,40 @@ lora_status lora_linear_dropout_bwd(const lora_shape* sh, const void* X, const u
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t M = sh->M, in = sh->d_in, out = sh->d_out;
   const int r = (int)sh->r;
-  bf16* Xd = reinterpret_cast<bf16*>(static_cast<char*>(ws) + lin);
-  CK(apply_mask_bf16(static_cast<const bf16*>(X), mask, keep_scale, M, in, Xd, st));
+  const bool fused = dropout_fused(*sh);
+  const bf16* Xa = static_cast<const bf16*>(X);
+  if (!fused) {
+    bf16* Xd = reinterpret_cast<bf16*>(static_cast<char*>(ws) + lin);
+    CK(apply_mask_bf16(static_cast<const bf16*>(X), mask, keep_scale, M, in, Xd, st));
+    Xa = Xd;
+  }
   const void* Z = Z_saved;
   if (!Z) {
-    RowProjDesc d = rp_desc(M, in, r, Xd, A, false, w.err);
+    RowProjDesc d = rp_desc(M, in, r, Xa, A, false, w.err);
+    if (fused) {
+      d.mask = mask;
+      d.mask_scale = keep_scale;
+    }
     d.out_a = static_cast<bf16*>(w.Zrec);
     CK(rowproj(d, st));
     Z = w.Zrec;
   }
-  {  // dB partials (dY^T Z) and column sums of dY, one pass over dY
-    ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
-    d.colsum = dbias ? w.csum : nullptr;
-    CK(colreduce(d, st));
-  }
-  {  // s G = s dY B
-    RowProjDesc d = rp_desc(M, out, r, dY, B, true, w.err);
-    d.out_b = static_cast<bf16*>(w.Gs);
-    d.scale_b = s;
-    CK(rowproj(d, st));
-  }
+  // s G = s dY B, the dB partials dY^T Z and the column sums of dY
+  CK(dy_side(w.rc, M, out, r, dY, out, B, Z, r, w.PB, w.splitsB, w.Gp, s, static_cast<bf16*>(w.Gs), r, w.err, st,
+             dbias ? w.csum : nullptr));
   if (dX) {  // dY W0 on the tensor cores, then the masked adapter share in its own pass
     CK(tc_gemm(dx_desc(M, in, out, dY, W0, nullptr, A, r, dX, nullptr, w.err), st));
     CK(add_masked_rank_bf16(static_cast<bf16*>(dX), static_cast<const bf16*>(w.Gs), static_cast<const bf16*>(A),
                             mask, keep_scale, M, in, r, st));
   }
-  CK(colreduce(cr_desc(M, in, r, Xd, w.Gs, r, w.PA, w.splitsA, w.err), st));   // Xd^T (s G)
+  {  // Xd^T (s G)
+    ColReduceDesc d = cr_desc(M, in, r, Xa, w.Gs, r, w.PA, w.splitsA, w.err);
+    if (fused) {
+      d.mask = mask;
+      d.mask_scale = keep_scale;
+    }
+    CK(colreduce(d, st));
+  }
   const FinJob fin[2] = {fin_dA(r, in, Partial{w.PA, w.splitsA, r, 0}, 1.f, A, dA),
                          fin_dB(out, r, Partial{w.PB, w.splitsB, r, 0}, s, B, dB)};
   CK(finalize_batch(fin, 2, st));

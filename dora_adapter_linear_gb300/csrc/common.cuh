@@ -424,6 +424,13 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
   return __bfloat1622float2(b);
 }
 
+// Input dropout on one bf16x2 operand register: each half becomes bf16(x k) where its mask byte
+// is nonzero and 0 where it is zero (k = 1 / (1 - p)); m0 belongs to the low half.
+__device__ __forceinline__ uint32_t mask_bf16x2(uint32_t v, uint32_t m0, uint32_t m1, float k) {
+  const float2 f = unpack_bf16x2(v);
+  return pack_bf16x2(m0 ? f.x * k : 0.f, m1 ? f.y * k : 0.f);
+}
+
 template <typename T>
 __device__ __forceinline__ float to_f(T v);
 template <>

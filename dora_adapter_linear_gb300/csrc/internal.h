@@ -19,6 +19,9 @@ int pdl_attr(cudaLaunchAttribute* a);
 // box {box_inner, box_outer}, swizzle of 0 / 32 / 64 / 128 bytes; out-of-bounds elements read as zero.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                     uint32_t box_inner, uint32_t box_outer, int swizzle_bytes);
+// A 2-D uint8 tensor map (no swizzle; ld in bytes, a multiple of 16) for the dropout masks.
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+                  uint32_t box_outer);
 
 // tracing (prof.cu)
 void count_launch(int n = 1);
@@ -118,6 +121,10 @@ struct RowProjDesc {
   // optional column-scaled copy of S written on the way: s_out[row, k] = bf16(S[row, k] * s_scale[k])
   const float* s_scale = nullptr;
   bf16* s_out = nullptr;        // [rows, K], leading dimension K
+  // optional keep mask on S (uint8 [rows, K], row stride K bytes, a multiple of 16): the pass reads
+  // S[row, k] as bf16(S[row, k] mask_scale) where mask[row, k] != 0 and as 0 elsewhere
+  const uint8_t* mask = nullptr;
+  float mask_scale = 1.f;
   uint32_t* err = nullptr;      // device error word for bounded waits
   uint64_t timeout_ns = 2000000000ull;
 };
@@ -144,13 +151,17 @@ struct ColReduceDesc {
   float* coldot = nullptr;     // [splits, K] or null
   const float* sc = nullptr;   // with sc_out (and Y): column scales [K]
   bf16* sc_out = nullptr;      // optional column-scaled copy of S: sc_out[row K + k] = bf16(S[row, k] sc[k])
+  // optional keep mask on S (as RowProjDesc::mask; no Y, no column sums, no copy with it)
+  const uint8_t* mask = nullptr;
+  float mask_scale = 1.f;
   int splits = 1;
   uint32_t* err = nullptr;     // device error word for bounded waits
   uint64_t timeout_ns = 2000000000ull;
 };
-// Row splits of a colreduce pass over [rows, K] at rank R (with or without the second input Y):
+// Row splits of a colreduce pass over [rows, K] at rank R (with or without the second input Y, or
+// the keep mask):
 // the split count whose waves of resident CTAs finish the pass soonest.
-int colreduce_splits(int64_t rows, int64_t K, int R = 16, bool has_y = false);
+int colreduce_splits(int64_t rows, int64_t K, int R = 16, bool has_y = false, bool mask = false);
 cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st);
 
 // One pass over S [rows, K] for both rank-r products that read it:

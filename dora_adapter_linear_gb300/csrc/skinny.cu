@@ -31,7 +31,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk, uint32_t p
   return row * pitch + ((chunk ^ (((row * pitch) >> 7) & mask)) << 4);
 }
 
-template <int R, bool U_KR>
+template <int R, bool U_KR, bool MASK = false>
 struct Cfg {
   // U [K, R]: the TMA box spans RPAD >= R columns (power of two, zero-filled past R)
   static constexpr int RPAD = R <= 8 ? 8 : (R <= 16 ? 16 : (R <= 32 ? 32 : 64));
@@ -41,7 +41,9 @@ struct Cfg {
   static constexpr int UROWS = (R + 15) / 16 * 16;              // U [R, K]: rows reserved (even n-tiles)
   static constexpr int U_BYTES = U_KR ? BK * RPAD * 2 : UROWS * 128;
   static constexpr int U_TX = U_KR ? BK * RPAD * 2 : R * 128;   // bytes the U box delivers
-  static constexpr int STAGE = (S_BYTES + U_BYTES + 1023) / 1024 * 1024;
+  static constexpr int OFF_M = S_BYTES + U_BYTES;                // keep-mask tile (32 x 64 bytes)
+  static constexpr int M_BYTES = MASK ? BMR * BK : 0;
+  static constexpr int STAGE = (S_BYTES + U_BYTES + M_BYTES + 1023) / 1024 * 1024;
   // stages in flight: about 96 KB per CTA (two CTAs per SM); 8 stages of the small ranks left
   // the pass latency-bound
   static constexpr int NST = (96 * 1024 / STAGE) > 16 ? 16 : ((96 * 1024 / STAGE) < 8 ? 8 : 96 * 1024 / STAGE);
@@ -60,13 +62,14 @@ struct Cfg {
 struct RpParams {
   CUtensorMap tmS;
   CUtensorMap tmU;
+  CUtensorMap tmM;   // keep mask (MASK)
   RowProjDesc d;
 };
 
-template <int R, bool U_KR>
-__global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(const __grid_constant__ RpParams P) {
+template <int R, bool U_KR, bool MASK>
+__global__ void __launch_bounds__(rp::Cfg<R, U_KR, MASK>::THREADS) rowproj_kernel(const __grid_constant__ RpParams P) {
   using namespace rp;
-  using C = Cfg<R, U_KR>;
+  using C = Cfg<R, U_KR, MASK>;
   const RowProjDesc& d = P.d;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -94,6 +97,7 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
     if (lane == 0) {
       tma_prefetch_desc(&P.tmS);
       tma_prefetch_desc(&P.tmU);
+      if (MASK) tma_prefetch_desc(&P.tmM);
       bool ok = true;
       for (int kc = 0; kc < nkc; ++kc) {
         const int s = kc % C::NST;
@@ -103,8 +107,9 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
           break;
         }
         uint8_t* st = smem + s * C::STAGE;
-        mbar_expect_tx(&full[s], S_BYTES + C::U_TX);
+        mbar_expect_tx(&full[s], S_BYTES + C::U_TX + C::M_BYTES);
         tma_load_2d(st, &P.tmS, &full[s], kc * BK, (int)row0);
+        if (MASK) tma_load_2d(st + C::OFF_M, &P.tmM, &full[s], kc * BK, (int)row0);
         if (U_KR) tma_load_2d(st + S_BYTES, &P.tmU, &full[s], 0, kc * BK);
         else tma_load_2d(st + S_BYTES, &P.tmU, &full[s], kc * BK, 0);
       }
@@ -133,6 +138,16 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
     for (int kk = 0; kk < BK / 16; ++kk) {
       uint32_t a[4];
       ldsm_x4(a[0], a[1], a[2], a[3], sS + swz(rg * 16 + (lane & 15), kk * 2 + (lane >> 4), 128, 7));
+      if constexpr (MASK) {
+        // a[i] holds S[16 rg + g + 8 (i & 1)][16 kk + 2t + 8 (i >> 1) + {0, 1}] (g = lane / 4,
+        // t = lane % 4): the matching two mask bytes are adjacent in the 64-byte mask row
+        const uint8_t* mrow = tile + C::OFF_M + (rg * 16 + (lane >> 2)) * BK + kk * 16 + 2 * (lane & 3);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t m2 = *reinterpret_cast<const uint16_t*>(mrow + (i & 1) * 8 * BK + (i >> 1) * 8);
+          a[i] = mask_bf16x2(a[i], m2 & 0xffu, m2 >> 8, d.mask_scale);
+        }
+      }
 #pragma unroll
       for (int q = 0; q < NTW; q += 2) {
         const int nt = nh * NTW + q;
@@ -219,10 +234,10 @@ __global__ void __launch_bounds__(rp::Cfg<R, U_KR>::THREADS) rowproj_kernel(cons
   }
 }
 
-template <int R, bool KR>
+template <int R, bool KR, bool MASK = false>
 static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
-  using C = rp::Cfg<R, KR>;
-  auto k = rowproj_kernel<R, KR>;
+  using C = rp::Cfg<R, KR, MASK>;
+  auto k = rowproj_kernel<R, KR, MASK>;
   static bool set = false;
   if (!set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -235,6 +250,7 @@ static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
   bool ok = make_tmap_bf16(&P.tmS, d.S, (uint64_t)d.K, (uint64_t)d.rows, (uint64_t)d.lds, rp::BK, rp::BMR, 128);
   if (KR) ok = ok && make_tmap_bf16(&P.tmU, d.U, R, (uint64_t)d.K, (uint64_t)d.ldu, C::RPAD, rp::BK, C::USWZ);
   else ok = ok && make_tmap_bf16(&P.tmU, d.U, (uint64_t)d.K, R, (uint64_t)d.ldu, rp::BK, R, 128);
+  if (MASK) ok = ok && make_tmap_u8(&P.tmM, d.mask, (uint64_t)d.K, (uint64_t)d.rows, (uint64_t)d.K, rp::BK, rp::BMR);
   if (!ok) return cudaErrorInvalidValue;
   const int64_t grid = (d.rows + rp::BMR - 1) / rp::BMR;
   cudaLaunchConfig_t cfg = {};
@@ -247,7 +263,8 @@ static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
   cfg.numAttrs = pdl_attr(&attr[0]);
   // algorithmic HBM bytes: S once, U, the outputs (and the scaled copy of S)
   const double outs = (d.out_a ? 2.0 : 0.0) + (d.out_b ? 2.0 : 0.0) + (d.out_f ? 4.0 : 0.0);
-  const double bytes = 2.0 * d.rows * d.K * (d.s_out ? 2.0 : 1.0) + 2.0 * R * d.K + outs * d.rows * R;
+  const double bytes = 2.0 * d.rows * d.K * (d.s_out ? 2.0 : 1.0) + (MASK ? 1.0 * d.rows * d.K : 0.0) +
+                       2.0 * R * d.K + outs * d.rows * R;
   prof_mark(st, true, bytes, 1);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k, P);
   prof_mark(st, false, 0.0, 1);
@@ -257,6 +274,7 @@ static cudaError_t rowproj_launch(const RowProjDesc& d, cudaStream_t st) {
 
 cudaError_t rowproj(const RowProjDesc& d, cudaStream_t st) {
   if (d.rows <= 0) return cudaSuccess;
+  if (d.mask && (d.u_kr || d.s_out || d.K % 16)) return cudaErrorInvalidValue;   // masked S: X A^T only
   if (d.R > 64) {   // columns in chunks of 64: one pass over S per chunk
     if (d.R > 512 || d.R % 8) return cudaErrorInvalidValue;
     const int64_t ldo = d.ldo > 0 ? d.ldo : d.R;
@@ -280,6 +298,7 @@ cudaError_t rowproj(const RowProjDesc& d, cudaStream_t st) {
   }
 #define RP_CASE(RR)                                                                   \
   case RR:                                                                            \
+    if (d.mask) return rowproj_launch<RR, false, true>(d, st);                        \
     return d.u_kr ? rowproj_launch<RR, true>(d, st) : rowproj_launch<RR, false>(d, st);
   switch (d.R) {
     RP_CASE(8)
@@ -304,17 +323,19 @@ constexpr int BKC = 64;       // columns (K) per CTA
 constexpr int BR = 64;        // rows per stage
 constexpr int S_BYTES = BR * 128;
 
-template <int R, bool HAS_Y>
+template <int R, bool HAS_Y, bool MASK = false>
 struct Cfg {
   static constexpr int RPAD = R <= 8 ? 8 : (R <= 16 ? 16 : (R <= 32 ? 32 : 64));
   static constexpr int TPITCH = RPAD * 2;
   static constexpr int TMASK = RPAD == 8 ? 0 : RPAD == 16 ? 1 : RPAD == 32 ? 3 : 7;
   static constexpr int TSWZ = RPAD == 8 ? 0 : RPAD * 2;
   static constexpr int T_BYTES = BR * RPAD * 2;
-  static constexpr int OFF_Y = S_BYTES + ((T_BYTES + 1023) / 1024) * 1024;
-  static constexpr int STAGE = OFF_Y + (HAS_Y ? S_BYTES : 0);
-  static constexpr int TX = S_BYTES + T_BYTES + (HAS_Y ? S_BYTES : 0);
-  static constexpr int NST = HAS_Y ? 4 : 6;
+  static constexpr int OFF_Y = S_BYTES + ((T_BYTES + 1023) / 1024) * 1024;   // Y tile, or the keep mask
+  static constexpr int M_BYTES = MASK ? BR * BKC : 0;                          // 64 x 64 mask bytes
+  static constexpr int STAGE = OFF_Y + (HAS_Y ? S_BYTES : 0) + M_BYTES;
+  static constexpr int TX = S_BYTES + T_BYTES + (HAS_Y ? S_BYTES : 0) + M_BYTES;
+  // stages: as many as keep the CTAs per SM of the pass without the mask (three up to rank 32)
+  static constexpr int NST = HAS_Y ? 4 : (MASK ? 5 : 6);
   static constexpr int SMEM = NST * STAGE + 1024 + 2 * NST * 8 + 16;
 };
 }  // namespace cr
@@ -322,16 +343,17 @@ struct Cfg {
 struct CrParams {
   CUtensorMap tmS;
   CUtensorMap tmT;
-  CUtensorMap tmY;
+  CUtensorMap tmY;   // Y, or the keep mask (MASK)
   ColReduceDesc d;
   int64_t rows_per_split;
 };
 
-template <int R, bool HAS_Y, bool SUMS>
+template <int R, bool HAS_Y, bool SUMS, bool MASK = false>
 __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ CrParams P) {
   using namespace cr;
   using rp::swz;
-  using C = Cfg<R, HAS_Y>;
+  static_assert(!MASK || (!HAS_Y && !SUMS), "masked S: no second input, no column sums");
+  using C = Cfg<R, HAS_Y, MASK>;
   constexpr int NST = C::NST;
   const ColReduceDesc& d = P.d;
   extern __shared__ uint8_t smem_raw[];
@@ -376,7 +398,7 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
         mbar_expect_tx(&full[s], C::TX);
         tma_load_2d(st, &P.tmS, &full[s], (int)k0, y);
         tma_load_2d(st + S_BYTES, &P.tmT, &full[s], 0, y);
-        if (HAS_Y) tma_load_2d(st + C::OFF_Y, &P.tmY, &full[s], (int)k0, y);
+        if (HAS_Y || MASK) tma_load_2d(st + C::OFF_Y, &P.tmY, &full[s], (int)k0, y);
       }
       if (!ok) spin_ns(100000ull);  // unwind: let copies already issued land
     }
@@ -411,6 +433,16 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
       {  // A = S^T: 16 columns of this warp x 16 rows, transposed out of the row-major tile
         const int row = kk * 16 + (lane & 7) + ((lane >> 4) << 3);
         ldsm_x4_t(a[0], a[1], a[2], a[3], sS + swz(row, warp * 2 + ((lane >> 3) & 1), 128, 7));
+      }
+      if constexpr (MASK) {
+        // a[i] holds S[16 kk + 8 (i >> 1) + 2t + {0, 1}][16 warp + 8 (i & 1) + g] (transposed
+        // fragments; g = lane / 4, t = lane % 4): two mask bytes one 64-byte mask row apart
+        const uint8_t* mcol = tile + C::OFF_Y + (kk * 16 + 2 * (lane & 3)) * BKC + warp * 16 + (lane >> 2);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint8_t* mp = mcol + (i >> 1) * 8 * BKC + (i & 1) * 8;
+          a[i] = mask_bf16x2(a[i], mp[0], mp[BKC], d.mask_scale);
+        }
       }
 #pragma unroll
       for (int nt = 0; nt < R / 8; nt += 2) {
@@ -486,23 +518,25 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
 
 // CTAs of colreduce_kernel<R, HAS_Y, *> resident per SM, from its shared memory (each CTA also
 // holds 1 KB reserved by the system; 228 KB per SM).
-static int colreduce_ctas_per_sm(int R, bool has_y) {
+static int colreduce_ctas_per_sm(int R, bool has_y, bool mask) {
   int smem;
-  if (R <= 8) smem = has_y ? cr::Cfg<8, true>::SMEM : cr::Cfg<8, false>::SMEM;
-  else if (R <= 16) smem = has_y ? cr::Cfg<16, true>::SMEM : cr::Cfg<16, false>::SMEM;
-  else if (R <= 32) smem = has_y ? cr::Cfg<32, true>::SMEM : cr::Cfg<32, false>::SMEM;
-  else smem = has_y ? cr::Cfg<64, true>::SMEM : cr::Cfg<64, false>::SMEM;
+  if (R <= 8) smem = mask ? cr::Cfg<8, false, true>::SMEM : has_y ? cr::Cfg<8, true>::SMEM : cr::Cfg<8, false>::SMEM;
+  else if (R <= 16)
+    smem = mask ? cr::Cfg<16, false, true>::SMEM : has_y ? cr::Cfg<16, true>::SMEM : cr::Cfg<16, false>::SMEM;
+  else if (R <= 32)
+    smem = mask ? cr::Cfg<32, false, true>::SMEM : has_y ? cr::Cfg<32, true>::SMEM : cr::Cfg<32, false>::SMEM;
+  else smem = mask ? cr::Cfg<64, false, true>::SMEM : has_y ? cr::Cfg<64, true>::SMEM : cr::Cfg<64, false>::SMEM;
   const int n = (228 * 1024) / (smem + 1024);
   return n < 1 ? 1 : n;
 }
 
-int colreduce_splits(int64_t rows, int64_t K, int R, bool has_y) {
+int colreduce_splits(int64_t rows, int64_t K, int R, bool has_y, bool mask) {
   const int64_t kb = (K + cr::BKC - 1) / cr::BKC;
   // Row splits per column block: with n CTAs resident per SM, a launch of kb * s CTAs runs in
   // ceil(kb s / slots) waves of CTAs that each stream ceil(rows / (64 s)) row stages plus a
   // fixed cost of about four stages (ring fill, partial sums); pick the s with the least total,
   // the fewest splits among equals.  A half-empty last wave cost ~1% of a LoRA step.
-  const int64_t slots = (int64_t)colreduce_ctas_per_sm(R, has_y) * num_sms_current();
+  const int64_t slots = (int64_t)colreduce_ctas_per_sm(R, has_y, mask) * num_sms_current();
   int64_t maxs = (rows + cr::BR - 1) / cr::BR;
   if (maxs > 64) maxs = 64;
   int64_t best = 1;
@@ -518,10 +552,10 @@ int colreduce_splits(int64_t rows, int64_t K, int R, bool has_y) {
   return (int)best;
 }
 
-template <int R, bool HAS_Y, bool SUMS>
+template <int R, bool HAS_Y, bool SUMS, bool MASK = false>
 static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
-  using C = cr::Cfg<R, HAS_Y>;
-  auto k = colreduce_kernel<R, HAS_Y, SUMS>;
+  using C = cr::Cfg<R, HAS_Y, MASK>;
+  auto k = colreduce_kernel<R, HAS_Y, SUMS, MASK>;
   static bool set = false;
   if (!set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -537,6 +571,7 @@ static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
   ok = ok && make_tmap_bf16(&P.tmT, d.T, R, (uint64_t)d.rows, (uint64_t)d.ldt, C::RPAD, cr::BR, C::TSWZ);
   if (HAS_Y)
     ok = ok && make_tmap_bf16(&P.tmY, d.Y, (uint64_t)d.K, (uint64_t)d.rows, (uint64_t)d.ldy, cr::BKC, cr::BR, 128);
+  if (MASK) ok = ok && make_tmap_u8(&P.tmY, d.mask, (uint64_t)d.K, (uint64_t)d.rows, (uint64_t)d.K, cr::BKC, cr::BR);
   if (!ok) return cudaErrorInvalidValue;
   dim3 grid((unsigned)((d.K + cr::BKC - 1) / cr::BKC), (unsigned)d.splits);
   cudaLaunchConfig_t cfg = {};
@@ -548,7 +583,7 @@ static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = pdl_attr(&attr[0]);
   // algorithmic HBM bytes: S (and Y, and the scaled copy) once, T, the fp32 partials (and column sums)
-  const double bytes = 2.0 * d.rows * d.K * (HAS_Y ? (d.sc_out ? 3.0 : 2.0) : 1.0) + 2.0 * d.rows * R +
+  const double bytes = 2.0 * d.rows * d.K * (HAS_Y ? (d.sc_out ? 3.0 : 2.0) : (MASK ? 1.5 : 1.0)) + 2.0 * d.rows * R +
                        4.0 * d.splits * d.K * (R + (SUMS ? 2.0 : 0.0));
   prof_mark(st, true, bytes, 1);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k, P);
@@ -560,6 +595,7 @@ static cudaError_t colreduce_launch(const ColReduceDesc& d, cudaStream_t st) {
 cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st) {
   if (d.K <= 0) return cudaSuccess;
   if (d.sc_out && (!d.Y || !d.sc || d.K % 8)) return cudaErrorInvalidValue;   // the copy rides on the Y pass
+  if (d.mask && (d.Y || d.colsum || d.coldot || d.sc_out || d.K % 16)) return cudaErrorInvalidValue;
   if (d.R > 64) {   // columns of T in chunks of 64: one pass over S per chunk
     if (d.R > 512 || d.R % 8) return cudaErrorInvalidValue;
     for (int c0 = 0; c0 < d.R; c0 += 64) {
@@ -583,6 +619,7 @@ cudaError_t colreduce(const ColReduceDesc& d, cudaStream_t st) {
   const bool sums = d.colsum != nullptr || d.coldot != nullptr;
 #define CR_CASE(RR)                                                          \
   case RR:                                                                   \
+    if (d.mask) return colreduce_launch<RR, false, false, true>(d, st);      \
     if (has_y) return colreduce_launch<RR, true, true>(d, st);               \
     if (sums) return colreduce_launch<RR, false, true>(d, st);               \
     return colreduce_launch<RR, false, false>(d, st);

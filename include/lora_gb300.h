@@ -195,14 +195,16 @@ lora_status lora_linear_bwd(const lora_shape* sh, const void* X, const void* W0,
  *   Xd = X o mask * keep_scale,  Y = X W0^T + s (Xd A^T) B^T (+ bias),
  * mask [M, d_in] uint8 (0 = dropped, 1 = kept; drawn by the caller, the same bytes for the
  * forward and the backward), keep_scale = 1 / (1 - p).  The mask sits between X and A, so this
- * call takes the unfused path: Xd is written once (workspace) and, in the backward, the adapter's
- * share of dX is a separate masked rank-r pass instead of the dX GEMM's tail.
+ * call takes the unfused path: in the backward, the adapter's share of dX is a separate masked
+ * rank-r pass instead of the dX GEMM's tail.
  * "Fused Kernels (experimental)" (LyCORIS docs), the note that a call whose mask sits between
  * two factors takes the unfused path; "How Unsloth's FastLoRA Kernel Differs ...", Optimized
  * Dropout and Scaling.  LORA_BF16 only (else LORA_ERR_UNSUPPORTED); other arguments as
  * lora_linear_fwd / _bwd.  mask must be 16-byte aligned and non-NULL when M > 0, keep_scale finite
- * and >= 0 (else LORA_ERR_INVALID_ARG); the workspace is the plain layer's plus M * d_in * 2 bytes
- * (lora_workspace_bytes with LORA_OP_DROPOUT_FWD / _BWD).
+ * and >= 0 (else LORA_ERR_INVALID_ARG).  With d_in a multiple of 16 no Xd is written: the rank-r
+ * passes over X read the mask beside it and form Xd in registers, and the workspace is the plain
+ * layer's; otherwise Xd is written once and the workspace adds M * d_in * 2 bytes
+ * (lora_workspace_bytes with LORA_OP_DROPOUT_FWD / _BWD gives either).
  *   Backward: G = s dY B;  dX = dY W0 + (G A) o mask * keep_scale;  dA = G^T Xd;
  *             dB = s dY^T Z (Z = Xd A^T, saved by the forward or NULL to recompute);
  *             dbias = colsum(dY).

@@ -110,11 +110,19 @@ def test_entry_points_validate_before_launch(lib):
 
 def test_dropout_entry_points_validate_before_launch(lib):
     """The input-dropout calls: bf16 only, a mask for M > 0, a finite non-negative keep scale and
-    a workspace that also holds the masked input; nothing is launched on any of these errors."""
+    the workspace they ask for (the plain layer's when d_in is a multiple of 16, which lets the
+    rank-r passes read the mask beside X; else one that also holds the masked input); nothing is
+    launched on any of these errors."""
     sh = L.shape(64, 256, 256, 8, L.LORA_BF16)
     fake = ctypes.c_void_p(1 << 20)
     ws_need = L.lora_workspace_bytes(L.OP_DROPOUT_FWD, sh)
-    assert ws_need >= L.lora_workspace_bytes(L.OP_LINEAR_FWD, sh) + 64 * 256 * 2
+    assert ws_need == L.lora_workspace_bytes(L.OP_LINEAR_FWD, sh)
+    assert L.lora_workspace_bytes(L.OP_DROPOUT_BWD, sh) == L.lora_workspace_bytes(L.OP_LINEAR_BWD, sh)
+    odd = L.shape(64, 264, 256, 8, L.LORA_BF16)   # 264-byte mask rows: Xd is written
+    assert (L.lora_workspace_bytes(L.OP_DROPOUT_FWD, odd)
+            >= L.lora_workspace_bytes(L.OP_LINEAR_FWD, odd) + 64 * 264 * 2)
+    assert (L.lora_workspace_bytes(L.OP_DROPOUT_BWD, odd)
+            >= L.lora_workspace_bytes(L.OP_LINEAR_BWD, odd) + 64 * 264 * 2)
     f32 = L.shape(64, 256, 256, 8, L.LORA_F32)
     r = lib.lora_linear_dropout_fwd(ctypes.byref(f32), fake, fake, 2.0, fake, fake, fake, None, 1.0, fake, None,
                                     fake, 1 << 30, None)
@@ -128,7 +136,7 @@ def test_dropout_entry_points_validate_before_launch(lib):
         assert r == 1
     r = lib.lora_linear_dropout_fwd(ctypes.byref(sh), fake, fake, 2.0, fake, fake, fake, None, 1.0, fake, None,
                                     fake, ws_need - 256, None)
-    assert r == 4  # workspace too small for the masked input
+    assert r == 4  # workspace too small
     wb = L.lora_workspace_bytes(L.OP_DROPOUT_BWD, sh)
     r = lib.lora_linear_dropout_bwd(ctypes.byref(sh), fake, None, 2.0, fake, fake, fake, None, fake, 1.0, fake, fake,
                                     fake, None, fake, wb, None)

@@ -174,3 +174,26 @@ def test_dora_slab_copy_matches_kscale_bits(ops, variant, slab_rows, monkeypatch
                            ("dX", "dA", "dB", "dm", "dbias")):
         assert_close(got, rr, "bf16", nm)
     _ws_ok(ops)
+
+
+@pytest.mark.parametrize("cap", ["0", "4"])
+@pytest.mark.parametrize("r", [8, 24, 32])
+def test_dropout_masked_passes(ops, variant, cap, r, monkeypatch):
+    """Input dropout with 16-byte mask rows: the Z pass and the dA pass read the mask beside X and
+    form Xd in registers; ragged M, ranks 8-32, a capped grid."""
+    monkeypatch.setenv("LORA_GB300_MAX_CTAS", cap)
+    case = D.scaled(D.WORKLOADS["lora_4096_bf16"], M=410, d_in=400, d_out=264, r=r, bias=True)
+    t = D.make_linear(case)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    mk = D.make_dropout_mask(410, 400, 0.2)
+    keep = 1 / 0.8
+    Y, Z = ops.lora_linear_dropout_fwd(g["X"], mk.to(DEV), keep, g["W0"], g["A"], g["B"], case.s, g["bias"])
+    X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
+    assert_close(Y, O.lora_dropout_fwd(X, mk.numpy(), keep, W0, A, B, case.s, f64(t["bias"])), "bf16", "Y")
+    dX, dA, dB, _ = ops.lora_linear_dropout_bwd(g["X"], mk.to(DEV), keep, g["W0"], g["A"], g["B"], None, g["dY"],
+                                                case.s)
+    rX, rA, rB, _ = O.lora_dropout_bwd(X, mk.numpy(), keep, W0, A, B, case.s, f64(t["dY"]))
+    assert_close(dX, rX, "bf16", "dX")
+    assert_close(dA, rA, "bf16", "dA")
+    assert_close(dB, rB, "bf16", "dB")
+    _ws_ok(ops)

@@ -142,9 +142,12 @@ def test_m_zero_is_noop(ops):
 
 
 # ---------------------------------------------------------------------------- LoRA with input dropout
-@pytest.mark.parametrize("M,p", [(300, 0.1), (129, 0.5)])
-def test_lora_dropout_fwd_bwd(ops, M, p):
-    case, t, g = lin_inputs("lora_4096_bf16", M=M, d_in=328, d_out=264, r=16, bias=True)
+@pytest.mark.parametrize("M,p,d_in,r", [(300, 0.1, 328, 16), (129, 0.5, 328, 16), (300, 0.1, 336, 16),
+                                         (200, 0.5, 336, 32), (130, 0.3, 528, 8)])
+def test_lora_dropout_fwd_bwd(ops, M, p, d_in, r):
+    """d_in 328: Xd is written once and read by the rank-r passes; d_in 336 / 528 (16-byte mask
+    rows): those passes read the mask beside X and form Xd in registers."""
+    case, t, g = lin_inputs("lora_4096_bf16", M=M, d_in=d_in, d_out=264, r=r, bias=True)
     mask = D.make_dropout_mask(M, case.d_in, p)
     keep = 1.0 / (1.0 - p)
     Y, Z = ops.lora_linear_dropout_fwd(g["X"], gpu(mask), keep, g["W0"], g["A"], g["B"], case.s, g["bias"])
@@ -160,6 +163,28 @@ def test_lora_dropout_fwd_bwd(ops, M, p):
         assert_close(dA, rA, "bf16", "dA")
         assert_close(dB, rB, "bf16", "dB")
         assert_close(dbias, rb[None, :], "bf16", "dbias")
+
+
+@pytest.mark.parametrize("r", [16, 32])
+def test_lora_dropout_mask_in_passes_matches_written_xd_bits(ops, r, monkeypatch):
+    """The mask applied in registers inside the rank-r passes gives the same bits as those passes
+    over an explicitly written Xd (the same bf16(x k) values in the same order): Z, Y, dX, dA, dB;
+    dX is also checked against the oracle."""
+    case, t, g = lin_inputs("lora_4096_bf16", M=333, d_in=400, d_out=264, r=r, bias=True)
+    mk = D.make_dropout_mask(333, 400, 0.25)
+    mask = gpu(mk)
+    args = (g["X"], mask, 1 / 0.75, g["W0"], g["A"], g["B"])
+    out = {}
+    for xd in ("0", "1"):
+        monkeypatch.setenv("LORA_GB300_DROPOUT_XD", xd)
+        Y, Z = ops.lora_linear_dropout_fwd(*args, case.s, g["bias"])
+        out[xd] = (Y, Z) + tuple(ops.lora_linear_dropout_bwd(*args, None, g["dY"], case.s)[:3])
+    for a, b, nm in zip(out["0"], out["1"], ("Y", "Z", "dX", "dA", "dB")):
+        assert torch.equal(a, b), nm
+    X, W0, A, B = (f64(t[k]) for k in ("X", "W0", "A", "B"))
+    rX = O.lora_dropout_bwd(X, mk.numpy(), 1 / 0.75, W0, A, B, case.s, f64(t["dY"]))[0]
+    for xd in ("0", "1"):
+        assert_close(out[xd][2], rX, "bf16", "dX")
 
 
 def test_lora_dropout_all_kept_matches_plain_layer(ops):
