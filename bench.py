@@ -536,7 +536,6 @@ def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8", "qkv", "d
     import torch
 
     import datagen as D
-    import oracle as O
     dev = torch.device("cuda", torch.cuda.current_device())
     out = {}
     steps, warm = max(3, min(args.steps, 20)), 3
@@ -545,7 +544,7 @@ def extra_workloads(args, L, ops, peaks, which=("dora", "mlp", "w8a8", "qkv", "d
     if "mlp" in which:
         out.update(_mlp_workload(args, L, ops, peaks, D, dev, steps, warm))
     if "w8a8" in which:
-        out.update(_w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm))
+        out.update(_w8a8_workload(args, L, ops, peaks, D, dev, steps, warm))
     if "qkv" in which:
         out.update(_qkv_workload(args, L, ops, peaks, D, dev, steps, warm))
     if "dropout" in which:
@@ -671,18 +670,17 @@ def _mlp_workload(args, L, ops, peaks, D, dev, steps, warm):
     return out
 
 
-def _w8a8_workload(args, L, ops, peaks, D, O, dev, steps, warm):
+def _w8a8_workload(args, L, ops, peaks, D, dev, steps, warm):
     """W8A8 + LoRA forward: quantise X (W-1), exact int8 product with the LoRA epilogue."""
     import torch
     out = {}
     case = D.WORKLOADS["w8a8_lora_3072"]
     t = D.make_w8a8(case)
-    Wq, sw = O.quantize_rows(t["W0"].numpy())
     X = t["X"].to(dev)
     A = t["A"].to(dev)
     B = t["B"].to(dev)
-    Wq = torch.from_numpy(Wq).to(dev)
-    sw = torch.from_numpy(sw).to(dev)
+    # the frozen int8 weight with its per-row scales, from the library's own per-row quantiser
+    Wq, sw, _ = ops.w8a8_quantize_rows(t["W0"].to(torch.bfloat16).to(dev))
 
     # the frozen weight laid out once (codes as bf16 for the forward, dequantised copy for the
     # backward), outside the timed steps like loading the model
@@ -745,7 +743,6 @@ def profile_steps(args, ops):
     import torch
 
     import datagen as D
-    import oracle as O
     dev = torch.device("cuda", torch.cuda.current_device())
     kw = {"M": args.profile_m} if args.profile_m > 0 else {}
     if args.profile in ("lora", "dora"):
@@ -771,6 +768,15 @@ def profile_steps(args, ops):
         def step():
             Y, saved = ops.lora_mlp_swiglu_fwd(g["X"], P["g"], P["u"], P["d"])
             ops.lora_mlp_swiglu_bwd(g["X"], P["g"], P["u"], P["d"], saved, g["dY"])
+    elif args.profile == "dropout":
+        case = D.scaled(D.WORKLOADS[HEADLINE], **kw)
+        g = {k: v.to(dev) for k, v in D.make_linear(case).items() if v is not None}
+        mask = D.make_dropout_mask(case.M, case.d_in, 0.1).to(dev)
+        keep = 1.0 / 0.9
+
+        def step():
+            Y, Z = ops.lora_linear_dropout_fwd(g["X"], mask, keep, g["W0"], g["A"], g["B"], case.s)
+            ops.lora_linear_dropout_bwd(g["X"], mask, keep, g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
     elif args.profile == "qkv":
         case = D.scaled(D.WORKLOADS["qkv_lora_4096_gqa_bf16"], **kw)
         g = {k: v.to(dev) for k, v in D.make_qkv(case).items() if v is not None}
@@ -782,10 +788,9 @@ def profile_steps(args, ops):
     else:
         case = D.scaled(D.WORKLOADS["w8a8_lora_3072"], **kw)
         t = D.make_w8a8(case)
-        Wq, sw = O.quantize_rows(t["W0"].numpy())
         X, A, B = t["X"].to(dev), t["A"].to(dev), t["B"].to(dev)
-        Wb, Wd = ops.w8a8_prepack_weight(torch.from_numpy(Wq).to(dev), torch.from_numpy(sw).to(dev))
-        swd = torch.from_numpy(sw).to(dev)
+        Wq, swd, _ = ops.w8a8_quantize_rows(t["W0"].to(torch.bfloat16).to(dev))
+        Wb, Wd = ops.w8a8_prepack_weight(Wq, swd)
 
         def step():
             Xc, sx, Z = ops.w8a8_quantize_rows_bf16(X, A)
@@ -806,7 +811,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--min-timed-s", type=float, default=1.0,
                     help="repeat the timed region of K steps until the regions cover this many seconds")
-    ap.add_argument("--profile", default=None, choices=["lora", "dora", "mlp", "qkv", "w8a8"],
+    ap.add_argument("--profile", default=None, choices=["lora", "dora", "mlp", "qkv", "w8a8", "dropout"],
                     help="profiling aid: run only W + K steps of this workload (no timing, no context) so that a "
                          "profiler's launch list holds just those kernels")
     ap.add_argument("--profile-m", type=int, default=0, help="token rows of the --profile workload (0: its own)")
