@@ -143,7 +143,8 @@ def test_m_zero_is_noop(ops):
 
 # ---------------------------------------------------------------------------- LoRA with input dropout
 @pytest.mark.parametrize("M,p,d_in,r", [(300, 0.1, 328, 16), (129, 0.5, 328, 16), (300, 0.1, 336, 16),
-                                         (200, 0.5, 336, 32), (130, 0.3, 528, 8)])
+                                         (200, 0.5, 336, 32), (130, 0.3, 528, 8), (150, 0.3, 336, 128),
+                                         (97, 0.2, 328, 96)])
 def test_lora_dropout_fwd_bwd(ops, M, p, d_in, r):
     """d_in 328: Xd is written once and read by the rank-r passes; d_in 336 / 528 (16-byte mask
     rows): those passes read the mask beside X and form Xd in registers."""
