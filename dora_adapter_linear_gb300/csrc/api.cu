@@ -387,12 +387,13 @@ size_t plan_qkv_fwd(const lora_qkv_shape& sh, char* base, QkvFwdWs* w) {
 struct QkvBwdWs {
   uint32_t* err;
   bf16* A_stack;
-  bf16* B_blk;
   bf16* Gs;      // [M, L r] = [s_l dY_l B_l]
   bf16* Zrec;    // [M, L r] when no Z_saved
   float* PA;     // [splitsA, in, L r]
   float* PB[kMaxLeaves];    // [splitsB[l], n_l, r]
   float* csum[kMaxLeaves];  // [splitsB[l], n_l]
+  RowColPlan rc[kMaxLeaves];  // one pass over each leaf's columns of dY (pm 0: two passes)
+  float* Gp;                  // row partials of that pass, reused leaf after leaf
   int splitsA, splitsB[kMaxLeaves];
 };
 size_t plan_qkv_bwd(const lora_qkv_shape& sh, char* base, QkvBwdWs* w) {
@@ -400,17 +401,20 @@ size_t plan_qkv_bwd(const lora_qkv_shape& sh, char* base, QkvBwdWs* w) {
   const int64_t R = (int64_t)sh.L * sh.r;
   w->err = c.take<uint32_t>(kErrBytes / 4);
   w->A_stack = c.take<bf16>(R * sh.d_in);
-  w->B_blk = c.take<bf16>(qkv_N(sh) * R);
   w->Gs = c.take<bf16>(sh.M * R);
   w->Zrec = c.take<bf16>(sh.M * R);
   w->splitsA = colreduce_splits(sh.M, sh.d_in, (int)R);
   w->PA = c.take<float>((size_t)w->splitsA * sh.d_in * R);
+  size_t gp = 0;
   for (int l = 0; l < kMaxLeaves; ++l) {
     const bool live = l < sh.L;
-    w->splitsB[l] = live ? colreduce_splits(sh.M, sh.n[l], sh.r) : 0;
+    w->rc[l] = live ? dy_plan(sh.M, sh.n[l], sh.r) : RowColPlan{};
+    w->splitsB[l] = !live ? 0 : w->rc[l].pm > 0 ? w->rc[l].pm : colreduce_splits(sh.M, sh.n[l], sh.r);
     w->PB[l] = live ? c.take<float>((size_t)w->splitsB[l] * sh.n[l] * sh.r) : nullptr;
     w->csum[l] = live ? c.take<float>((size_t)w->splitsB[l] * sh.n[l]) : nullptr;
+    if (w->rc[l].pm > 0 && (size_t)w->rc[l].pn * sh.M * sh.r > gp) gp = (size_t)w->rc[l].pn * sh.M * sh.r;
   }
+  w->Gp = gp ? c.take<float>(gp) : nullptr;
   return c.off;
 }
 
@@ -1080,33 +1084,17 @@ lora_status lora_qkv_bwd(const lora_qkv_shape* sh, const void* X, const void* W0
     }
     return LORA_OK;
   }
-  CK(pack_leaves(leaf_pack(*sh, leaves, w.A_stack, w.B_blk), st));
+  CK(pack_leaves(leaf_pack(*sh, leaves, w.A_stack, nullptr), st));   // A_stack only
   const bf16* Z = static_cast<const bf16*>(Z_saved);
   if (!Z) {
     if ((e = qkv_down(*sh, X, w.A_stack, w.Zrec, w.err, st)) != LORA_OK) return e;
     Z = w.Zrec;
   }
-  // dB partials of each leaf (its columns of dY against its block of Z) and dY column sums
-  for (int l = 0; l < sh->L; ++l) {
-    ColReduceDesc d = cr_desc(M, sh->n[l], r, dYb + row0[l], Z + l * r, R, w.PB[l], w.splitsB[l], w.err);
-    d.lds = N;
-    d.colsum = dbias ? w.csum[l] : nullptr;
-    CK(colreduce(d, st));
-  }
-  if (R <= 64) {  // [s_l dY_l B_l] for all leaves in one pass over dY (B_blk is block-diagonal)
-    RowProjDesc d = rp_desc(M, N, R, dY, w.B_blk, true, w.err);
-    d.out_a = w.Gs;
-    CK(rowproj(d, st));
-  } else {  // leaf by leaf over its own columns of dY: still one pass over dY in all
-    for (int l = 0; l < sh->L; ++l) {
-      RowProjDesc d = rp_desc(M, sh->n[l], r, dYb + row0[l], leaves[l].B, true, w.err);
-      d.lds = N;
-      d.out_b = w.Gs + l * r;
-      d.scale_b = leaves[l].s;
-      d.ldo = R;
-      CK(rowproj(d, st));
-    }
-  }
+  // leaf by leaf, one pass over its columns of dY: G_l = s_l dY_l B_l into its block of G, the dB
+  // partials of the leaf (dY_l^T Z_l) and the column sums of dY_l
+  for (int l = 0; l < sh->L; ++l)
+    CK(dy_side(w.rc[l], M, sh->n[l], r, dYb + row0[l], N, leaves[l].B, Z + l * r, R, w.PB[l], w.splitsB[l], w.Gp,
+               leaves[l].s, w.Gs + l * r, R, w.err, st, dbias ? w.csum[l] : nullptr));
   if (dX) CK(tc_gemm(dx_desc(M, in, N, dY, W0, w.Gs, w.A_stack, R, dX, nullptr, w.err), st));
   // X^T G partials per leaf group: group i's array [splitsA, in, R_i] starts at column offset c0
   const LeafGroups grp = leaf_groups(*sh);

@@ -436,7 +436,7 @@ cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int6
 __global__ void pack_leaves_kernel(LeafPack p) {
   const int R = p.L * p.r;
   const int64_t nA = (int64_t)R * p.in / 8;   // 16-byte chunks of A_stack
-  const int64_t nB = p.N * R;
+  const int64_t nB = p.B_blk ? p.N * R : 0;   // no B_blk: A_stack only
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nA + nB; i += stride) {
     if (i < nA) {
@@ -459,7 +459,7 @@ __global__ void pack_leaves_kernel(LeafPack p) {
   }
 }
 cudaError_t pack_leaves(const LeafPack& p, cudaStream_t st) {
-  const int64_t n = (int64_t)p.L * p.r * p.in / 8 + p.N * p.L * p.r;
+  const int64_t n = (int64_t)p.L * p.r * p.in / 8 + (p.B_blk ? p.N * p.L * p.r : 0);
   if (n <= 0) return cudaSuccess;
   const int64_t blocks = (n + 255) / 256;
   pack_leaves_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(p);
