@@ -25,6 +25,24 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
 
 // tracing (prof.cu)
 void count_launch(int n = 1);
+// Launch with programmatic stream serialization (when enabled) and count it: the kernel may be
+// scheduled while its predecessor in the stream finishes, so it must call pdl_wait() before it
+// touches global memory (every kernel launched this way does so first).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_attr(&attr[0]);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 uint64_t launch_count();
 bool prof_enabled();
 void prof_set(bool on);

@@ -36,6 +36,8 @@ __device__ __forceinline__ float block_sum(float v) {
 // ------------------------------------------------------------------ rowsum(W^2), one warp per row
 template <typename T>
 __global__ void rownorm2_kernel(const T* W, int64_t rows, int64_t cols, float* r0) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -58,14 +60,14 @@ __global__ void rownorm2_kernel(const T* W, int64_t rows, int64_t cols, float* r
 template <typename T>
 cudaError_t rownorm2(const T* W, int64_t rows, int64_t cols, float* r0, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  rownorm2_kernel<T><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(W, rows, cols, r0);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(rownorm2_kernel<T>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, W, rows, cols, r0);
 }
 
 // ------------------------------------------------------------------ K = A A^T, one block per (i, j)
 template <typename T>
 __global__ void gram_rows_kernel(const T* A, int r, int64_t cols, float* K) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int i = blockIdx.x / r, j = blockIdx.x % r;
   if (j < i) return;
   float acc = 0.f;
@@ -78,9 +80,7 @@ __global__ void gram_rows_kernel(const T* A, int r, int64_t cols, float* K) {
 }
 template <typename T>
 cudaError_t gram_rows(const T* A, int r, int64_t cols, float* K, cudaStream_t st) {
-  gram_rows_kernel<T><<<r * r, 256, 0, st>>>(A, r, cols, K);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(gram_rows_kernel<T>, dim3(r * r), dim3(256), 0, st, A, r, cols, K);
 }
 
 // ------------------------------------------------------------------ Kg = B^T diag(g) B
@@ -92,6 +92,8 @@ constexpr int kGramMaxR = 128;
 template <typename T>
 __global__ void __launch_bounds__(256) gram_partial_kernel(const T* B, int64_t out, int r, const float* g,
                                                            int64_t rows_per, float* part) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   constexpr int NQ = kGramMaxR * kGramMaxR / 256;   // entries (i, j) per thread
   __shared__ float tile[32][kGramMaxR + 1];
   __shared__ float gw[32];
@@ -138,9 +140,7 @@ cudaError_t gram_weighted(const T* B, int64_t out, int r, const float* g, float*
   int nch = (int)((out + 31) / 32);
   if (nch > kGramChunks) nch = kGramChunks;
   const int64_t rows_per = (out + nch - 1) / nch;
-  gram_partial_kernel<T><<<nch, 256, 0, st>>>(B, out, r, g, rows_per, work);
-  count_launch();
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(gram_partial_kernel<T>, dim3(nch), dim3(256), 0, st, B, out, r, g, rows_per, work);
   if (e != cudaSuccess) return e;
   return sum_splits<float>(work, nch, (int64_t)r * r, Kg, nullptr, st);
 }
@@ -152,6 +152,8 @@ constexpr int kNormMaxR = 128;
 template <typename T>
 __global__ void dora_norm_kernel(int64_t out, int r, const float* r0, const float* V, const T* B, const float* Kr,
                                  const T* m, float s, float eps, float* n_out, float* c) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   extern __shared__ float sKr[];
   for (int i = threadIdx.x; i < r * r; i += blockDim.x) sKr[i] = Kr[i];
   __syncthreads();
@@ -197,15 +199,15 @@ cudaError_t dora_norm(int64_t out, int r, const float* r0, const float* V, const
   if (r > kNormMaxR) return cudaErrorInvalidValue;
   const cudaError_t ea = allow_rr_smem(dora_norm_kernel<T>);
   if (ea != cudaSuccess) return ea;
-  dora_norm_kernel<T><<<(unsigned)((out + 7) / 8), 256, r * r * sizeof(float), st>>>(out, r, r0, V, B, Kr, m, s, eps,
-                                                                                    n_out, c);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(dora_norm_kernel<T>, dim3((unsigned)((out + 7) / 8)), dim3(256), r * r * sizeof(float), st,
+                    out, r, r0, V, B, Kr, m, s, eps, n_out, c);
 }
 
 // ------------------------------------------------------------------ c = m / n
 template <typename T>
 __global__ void dora_c_kernel(int64_t out, int64_t padded, const T* m, const float* n, float* c) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (o < out) c[o] = ldf(m, o) / n[o];
   else if (o < padded) c[o] = 0.f;
@@ -214,14 +216,14 @@ template <typename T>
 cudaError_t dora_c(int64_t out, const T* m, const float* n, float* c, cudaStream_t st, int64_t padded) {
   if (out <= 0) return cudaSuccess;
   if (padded < out) padded = out;
-  dora_c_kernel<T><<<(unsigned)((padded + 255) / 256), 256, 0, st>>>(out, padded, m, n, c);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(dora_c_kernel<T>, dim3((unsigned)((padded + 255) / 256)), dim3(256), 0, st, out, padded, m, n, c);
 }
 
 // ------------------------------------------------------------------ sum of split partials
 template <typename T>
 __global__ void sum_splits_kernel(const float* src, int splits, int64_t n, float* dst_f, T* dst_t) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (k >= n) return;
   float a = 0.f;
@@ -232,9 +234,8 @@ __global__ void sum_splits_kernel(const float* src, int splits, int64_t n, float
 template <typename T>
 cudaError_t sum_splits(const float* src, int splits, int64_t n, float* dst_f, T* dst_t, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  sum_splits_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, splits, n, dst_f, dst_t);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(sum_splits_kernel<T>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st,
+                    src, splits, n, dst_f, dst_t);
 }
 
 // ------------------------------------------------------------------ DoRA dc -> dm, g, dbias
@@ -242,6 +243,8 @@ cudaError_t sum_splits(const float* src, int splits, int64_t n, float* dst_f, T*
 template <typename T>
 __global__ void dora_dc_kernel(int64_t out, const float* dot, const float* csum, int splits, const T* bias,
                                const float* c, const float* n, const T* m, float eps, float* g, T* dm, T* dbias) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (o >= out) return;
   float dt = 0.f, cs = 0.f;
@@ -261,15 +264,15 @@ cudaError_t dora_dc(int64_t out, const float* dot, const float* csum, int splits
                     const float* n, const T* m, float eps, float* g, T* dm, T* dbias, cudaStream_t st) {
   if (out <= 0) return cudaSuccess;
   if ((bias || dbias) && !csum) return cudaErrorInvalidValue;
-  dora_dc_kernel<T><<<(unsigned)((out + 255) / 256), 256, 0, st>>>(out, dot, csum, splits, bias, c, n, m, eps, g,
-                                                                     dm, dbias);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(dora_dc_kernel<T>, dim3((unsigned)((out + 255) / 256)), dim3(256), 0, st,
+                    out, dot, csum, splits, bias, c, n, m, eps, g, dm, dbias);
 }
 
 // ------------------------------------------------------------------ out = f * scale[o] * B[o, :]
 template <typename T>
 __global__ void scale_rows_kernel(const T* B, int64_t rows, int r, const float* scale, float f, T* out) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= rows * r) return;
   const int64_t o = i / r;
@@ -280,9 +283,8 @@ template <typename T>
 cudaError_t scale_rows(const T* B, int64_t rows, int r, const float* scale, float f, T* out, cudaStream_t st) {
   const int64_t n = rows * r;
   if (n <= 0) return cudaSuccess;
-  scale_rows_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(B, rows, r, scale, f, out);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(scale_rows_kernel<T>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st,
+                    B, rows, r, scale, f, out);
 }
 
 // ------------------------------------------------------------------ gradient assembly
@@ -333,6 +335,8 @@ __device__ __forceinline__ void finalize_dB_elem(int64_t i, int64_t out, int r, 
 template <typename T>
 __global__ void finalize_dA_kernel(int r, int64_t in, Partial PA, float sA, Partial PW, float sW, const float* Kg,
                                    float s2, const T* A, T* dA) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // index into dA [r, in]
   if (i >= (int64_t)r * in) return;
   const int j = (int)(i / in);
@@ -344,14 +348,15 @@ cudaError_t finalize_dA(int r, int64_t in, Partial PA, float sA, Partial PW, flo
                         const T* A, T* dA, cudaStream_t st) {
   const int64_t n = (int64_t)r * in;
   if (n <= 0) return cudaSuccess;
-  finalize_dA_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(r, in, PA, sA, PW, sW, Kg, s2, A, dA);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(finalize_dA_kernel<T>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st,
+                    r, in, PA, sA, PW, sW, Kg, s2, A, dA);
 }
 
 template <typename T>
 __global__ void finalize_dB_kernel(int64_t out, int r, Partial PB, float sB, const float* rs, const float* g,
                                    const float* V, const T* B, const float* Kr, float s, bool accumulate, T* dB) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // index into dB [out, r]
   if (i < out * r) finalize_dB_elem<T>(i, out, r, PB, sB, rs, g, V, B, Kr, s, accumulate, dB);
 }
@@ -360,10 +365,8 @@ cudaError_t finalize_dB(int64_t out, int r, Partial PB, float sB, const float* r
                         const T* B, const float* Kr, float s, bool accumulate, T* dB, cudaStream_t st) {
   const int64_t n = out * r;
   if (n <= 0) return cudaSuccess;
-  finalize_dB_kernel<T><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(out, r, PB, sB, rs, g, V, B, Kr, s, accumulate,
-                                                                      dB);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(finalize_dB_kernel<T>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st,
+                    out, r, PB, sB, rs, g, V, B, Kr, s, accumulate, dB);
 }
 
 // Several dA / dB assemblies in one launch: job j owns blocks [first[j], first[j + 1]).
@@ -418,6 +421,8 @@ cudaError_t finalize_batch(const FinJob* jobs, int n, cudaStream_t st) {
 
 // ------------------------------------------------------------------ concat / zero
 __global__ void concat_rows_kernel(const uint4* X1, int64_t n1, const uint4* X2, int64_t n2, uint4* dst) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n1) dst[i] = X1[i];
   else if (i < n1 + n2) dst[i] = X2[i - n1];
@@ -426,14 +431,15 @@ cudaError_t concat_rows_bf16(const bf16* X1, int64_t rows1, const bf16* X2, int6
                              cudaStream_t st) {
   const int64_t n1 = rows1 * cols / 8, n2 = rows2 * cols / 8;
   if (n1 + n2 <= 0) return cudaSuccess;
-  concat_rows_kernel<<<(unsigned)((n1 + n2 + 255) / 256), 256, 0, st>>>(
-      reinterpret_cast<const uint4*>(X1), n1, reinterpret_cast<const uint4*>(X2), n2, reinterpret_cast<uint4*>(dst));
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(concat_rows_kernel, dim3((unsigned)((n1 + n2 + 255) / 256)), dim3(256), 0, st,
+                    reinterpret_cast<const uint4*>(X1), n1, reinterpret_cast<const uint4*>(X2), n2,
+                    reinterpret_cast<uint4*>(dst));
 }
 // Fused-leaf operands: A_stack = [A_0; A_1; ...] ([L r, in]) and the block-diagonal
 // B_blk [N, L r] whose rows of leaf l hold s_l B_l in columns l r .. l r + r - 1, zeros elsewhere.
 __global__ void pack_leaves_kernel(LeafPack p) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int R = p.L * p.r;
   const int64_t nA = (int64_t)R * p.in / 8;   // 16-byte chunks of A_stack
   const int64_t nB = p.B_blk ? p.N * R : 0;   // no B_blk: A_stack only
@@ -462,14 +468,14 @@ cudaError_t pack_leaves(const LeafPack& p, cudaStream_t st) {
   const int64_t n = (int64_t)p.L * p.r * p.in / 8 + (p.B_blk ? p.N * p.L * p.r : 0);
   if (n <= 0) return cudaSuccess;
   const int64_t blocks = (n + 255) / 256;
-  pack_leaves_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(p);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(pack_leaves_kernel, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(256), 0, st, p);
 }
 
 // ------------------------------------------------------------------ DoRA column variant (bf16)
 // c0[k] = sum_o W[o, k]^2: 32 columns per block, 8 row phases reduced through shared memory
 __global__ void colnorm2_kernel(const bf16* W, int64_t rows, int64_t cols, float* c0) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   __shared__ float red[8][33];
   const int64_t k = (int64_t)blockIdx.x * 32 + threadIdx.x;
   float acc = 0.f;
@@ -488,9 +494,7 @@ __global__ void colnorm2_kernel(const bf16* W, int64_t rows, int64_t cols, float
 }
 cudaError_t colnorm2_bf16(const bf16* W, int64_t rows, int64_t cols, float* c0, cudaStream_t st) {
   if (cols <= 0) return cudaSuccess;
-  colnorm2_kernel<<<(unsigned)((cols + 31) / 32), dim3(32, 8), 0, st>>>(W, rows, cols, c0);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(colnorm2_kernel, dim3((unsigned)((cols + 31) / 32)), dim3(32, 8), 0, st, W, rows, cols, c0);
 }
 
 // closed-form column norm, one warp per input column k (lane j holds A[j + 32 h, k], h < 4):
@@ -499,6 +503,8 @@ cudaError_t colnorm2_bf16(const bf16* W, int64_t rows, int64_t cols, float* c0, 
 __global__ void dora_colnorm_kernel(int64_t in, int r, const float* c0, const float* U, const bf16* A,
                                     const float* Kb, const bf16* m, float s, float eps, float* n_out, float* c,
                                     bf16* A_c) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   extern __shared__ float sK[];
   for (int i = threadIdx.x; i < r * r; i += blockDim.x) sK[i] = Kb[i];
   __syncthreads();
@@ -543,14 +549,14 @@ cudaError_t dora_colnorm(int64_t in, int r, const float* c0, const float* U, con
   if (r > kNormMaxR) return cudaErrorInvalidValue;
   const cudaError_t ea = allow_rr_smem(dora_colnorm_kernel);
   if (ea != cudaSuccess) return ea;
-  dora_colnorm_kernel<<<(unsigned)((in + 7) / 8), 256, r * r * sizeof(float), st>>>(in, r, c0, U, A, Kb, m, s, eps,
-                                                                                    n_out, c, A_c);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(dora_colnorm_kernel, dim3((unsigned)((in + 7) / 8)), dim3(256), r * r * sizeof(float), st,
+                    in, r, c0, U, A, Kb, m, s, eps, n_out, c, A_c);
 }
 
 // out[j, k] = bf16(A[j, k] * w[k])  (A [r, in])
 __global__ void scale_cols_kernel(const bf16* A, int r, int64_t in, const float* w, bf16* out) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)r * in) return;
   out[i] = __float2bfloat16_rn(__bfloat162float(A[i]) * w[i % in]);
@@ -558,13 +564,13 @@ __global__ void scale_cols_kernel(const bf16* A, int r, int64_t in, const float*
 cudaError_t scale_cols_bf16(const bf16* A, int r, int64_t in, const float* w, bf16* out, cudaStream_t st) {
   const int64_t n = (int64_t)r * in;
   if (n <= 0) return cudaSuccess;
-  scale_cols_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(A, r, in, w, out);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(scale_cols_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, A, r, in, w, out);
 }
 
 // K = A diag(w) A^T (fp32 [r, r]), one block per (i, j >= i)
 __global__ void gram_rows_weighted_kernel(const bf16* A, int r, int64_t cols, const float* w, float* K) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int i = blockIdx.x / r, j = blockIdx.x % r;
   if (j < i) return;
   float acc = 0.f;
@@ -577,14 +583,14 @@ __global__ void gram_rows_weighted_kernel(const bf16* A, int r, int64_t cols, co
   }
 }
 cudaError_t gram_rows_weighted(const bf16* A, int r, int64_t cols, const float* w, float* K, cudaStream_t st) {
-  gram_rows_weighted_kernel<<<r * r, 256, 0, st>>>(A, r, cols, w, K);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(gram_rows_weighted_kernel, dim3(r * r), dim3(256), 0, st, A, r, cols, w, K);
 }
 
 // dA[j, k] = c[k] sum_s PA[s][k][j] + 2 s g[k] U[k, j] + 2 s^2 g[k] (Kb A)[j, k]
 __global__ void finalize_dA_cols_kernel(int r, int64_t in, Partial PA, const float* c, const float* g,
                                         const float* U, const float* Kb, const bf16* A, float s, bf16* dA) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)r * in) return;
   const int j = (int)(i / in);
@@ -599,14 +605,15 @@ cudaError_t finalize_dA_cols(int r, int64_t in, Partial PA, const float* c, cons
                              const float* Kb, const bf16* A, float s, bf16* dA, cudaStream_t st) {
   const int64_t n = (int64_t)r * in;
   if (n <= 0) return cudaSuccess;
-  finalize_dA_cols_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(r, in, PA, c, g, U, Kb, A, s, dA);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(finalize_dA_cols_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st,
+                    r, in, PA, c, g, U, Kb, A, s, dA);
 }
 
 // ------------------------------------------------------------------ input dropout (unfused path)
 // out = bf16(X o mask * scale), 8 elements (one 16-byte chunk) per thread; cols a multiple of 8
 __global__ void apply_mask_kernel(const uint4* X, const uint2* mask, float scale, int64_t n8, uint4* out) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n8) return;
   uint4 v = X[i];
@@ -624,10 +631,9 @@ cudaError_t apply_mask_bf16(const bf16* X, const uint8_t* mask, float scale, int
                             cudaStream_t st) {
   const int64_t n8 = rows * cols / 8;
   if (n8 <= 0) return cudaSuccess;
-  apply_mask_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
-      reinterpret_cast<const uint4*>(X), reinterpret_cast<const uint2*>(mask), scale, n8, reinterpret_cast<uint4*>(out));
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(apply_mask_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, st,
+                    reinterpret_cast<const uint4*>(X), reinterpret_cast<const uint2*>(mask), scale, n8,
+                    reinterpret_cast<uint4*>(out));
 }
 
 // dX[i, k] += scale * mask[i, k] * sum_j G[i, j] A[j, k]  (the adapter's share of dX when a mask
@@ -642,6 +648,8 @@ constexpr int kAmrRows = 32, kAmrCols = 256;
 __global__ void __launch_bounds__(256) add_masked_rank_kernel(bf16* dX, const bf16* G, const bf16* A,
                                                               const uint8_t* mask, float scale, int64_t rows,
                                                               int64_t cols, int r) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   extern __shared__ uint4 amr_smem[];
   bf16* As = reinterpret_cast<bf16*>(amr_smem);                  // [r][256]
   float* Gs = reinterpret_cast<float*>(As + (size_t)r * kAmrCols);  // [32][r]
@@ -723,9 +731,7 @@ cudaError_t add_masked_rank_bf16(bf16* dX, const bf16* G, const bf16* A, const u
     opted = smem;
   }
   const dim3 grid((unsigned)((rows + kAmrRows - 1) / kAmrRows), (unsigned)((cols + kAmrCols - 1) / kAmrCols));
-  add_masked_rank_kernel<<<grid, 256, smem, st>>>(dX, G, A, mask, scale, rows, cols, r);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(add_masked_rank_kernel, dim3(grid), dim3(256), smem, st, dX, G, A, mask, scale, rows, cols, r);
 }
 
 cudaError_t fill_zero(void* p, size_t bytes, cudaStream_t st) {

@@ -19,6 +19,8 @@ namespace lg {
 // to be the A operand of the tensor-core product); either may be null.
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const bf16* X, int64_t cols, int8_t* Xq, float* sx,
                                                             bf16* Xb) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t row = blockIdx.x;
   const bf16* x = X + row * cols;
   float amax = 0.f;
@@ -65,15 +67,15 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const bf16* X, int64
 cudaError_t quantize_rows_bf16(const bf16* X, int64_t rows, int64_t cols, int8_t* Xq, float* sx, cudaStream_t st,
                                bf16* Xb) {
   if (rows <= 0) return cudaSuccess;
-  quantize_rows_kernel<<<(unsigned)rows, 256, 0, st>>>(X, cols, Xq, sx, Xb);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(quantize_rows_kernel, dim3((unsigned)rows), dim3(256), 0, st, X, cols, Xq, sx, Xb);
 }
 
 // ------------------------------------------------------------------ int8 codes as bf16 tensor-core operands
 // Every int8 value is exact in bf16, so the codes are the operands of the bf16 tensor-core product,
 // which sums them exactly in 1024-wide K chunks (every partial sum an integer below 2^24).
 __global__ void i8_to_bf16_kernel(const int8_t* __restrict__ q, int64_t n16, bf16* __restrict__ out) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n16) return;
   const uint4 raw = reinterpret_cast<const uint4*>(q)[i];
@@ -90,6 +92,8 @@ __global__ void i8_to_bf16_kernel(const int8_t* __restrict__ q, int64_t n16, bf1
 // the backward's dX product (the frozen weight, re-laid out once per call like a k-major copy).
 __global__ void i8_dequant_rows_kernel(const int8_t* __restrict__ q, const float* __restrict__ sw, int64_t cols,
                                        int64_t n16, bf16* __restrict__ out) {
+  pdl_wait();   // inputs may come from the previous kernel in the stream
+  if (threadIdx.x == 0 && threadIdx.y == 0) pdl_trigger();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n16) return;
   const float sc = sw[(i * 16) / cols];
@@ -107,17 +111,14 @@ cudaError_t i8_dequant_rows_bf16(const int8_t* q, const float* sw, int64_t rows,
                                  cudaStream_t st) {
   const int64_t n16 = rows * cols / 16;  // cols is a multiple of 16: a group never straddles rows
   if (n16 <= 0) return cudaSuccess;
-  i8_dequant_rows_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(q, sw, cols, n16, out);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(i8_dequant_rows_kernel, dim3((unsigned)((n16 + 255) / 256)), dim3(256), 0, st,
+                    q, sw, cols, n16, out);
 }
 
 cudaError_t i8_to_bf16(const int8_t* q, int64_t n, bf16* out, cudaStream_t st) {
   const int64_t n16 = n / 16;
   if (n16 <= 0) return cudaSuccess;
-  i8_to_bf16_kernel<<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(q, n16, out);
-  count_launch();
-  return cudaGetLastError();
+  return launch_pdl(i8_to_bf16_kernel, dim3((unsigned)((n16 + 255) / 256)), dim3(256), 0, st, q, n16, out);
 }
 
 
