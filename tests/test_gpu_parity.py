@@ -525,6 +525,46 @@ def test_w8a8_quantize_with_z_shapes(ops, cols, r):
     assert torch.equal(Z, Z2)
 
 
+def _near_tie_rows(cols=512, rows=48, seed=77):
+    """bf16 rows whose quotients x / s sit on or next to half-integers: rows with a power-of-two
+    scale (amax = 127 * 2^e) holding exact k + 0.5 multiples of it (ties, rounded to even), and rows
+    with an arbitrary scale filled with values whose float32 quotient lies within 2^-14 of a
+    half-integer (found by search), all beside their row maximum."""
+    rng = np.random.default_rng(seed)
+    out = np.zeros((rows, cols), np.float32)
+    for i in range(rows):
+        if i % 2 == 0:   # exact ties
+            e = int(rng.integers(-6, 6))
+            amax = np.float32(127.0 * 2.0 ** e)
+            k = rng.integers(0, 127, size=cols).astype(np.float32)
+            row = (k + np.float32(0.5)) * np.float32(2.0 ** e) * rng.choice([-1, 1], size=cols).astype(np.float32)
+        else:            # near ties under an arbitrary scale
+            amax = torch.tensor(float(rng.uniform(0.5, 40.0))).to(torch.bfloat16).float().item()
+            sc = np.float32(amax) / np.float32(127.0)
+            cand = torch.from_numpy(rng.uniform(-amax, amax, size=400000).astype(np.float32))
+            cand = cand.to(torch.bfloat16).float().numpy()
+            q = cand / sc                                       # float32 quotients (IEEE)
+            near = np.abs(np.abs(q) - np.floor(np.abs(q)) - np.float32(0.5)) <= 2.0 ** -14
+            pick = cand[near]
+            assert pick.size > 0
+            row = rng.choice(pick, size=cols)
+        row[int(rng.integers(0, cols))] = amax
+        out[i] = row
+    return torch.from_numpy(out).to(torch.bfloat16)
+
+
+def test_w8a8_quantize_near_ties_bit_exact(ops):
+    """The quantiser's codes where the quotient is a tie or within 2^-14 of one (the values whose
+    code depends on the last bits of the correctly rounded quotient) match the oracle's bit for bit."""
+    X = _near_tie_rows()
+    rq, rs = O.quantize_rows(X.float().numpy())
+    Xq, sx, _ = ops.w8a8_quantize_rows(gpu(X))
+    np.testing.assert_array_equal(sx.cpu().numpy(), rs)
+    np.testing.assert_array_equal(Xq.cpu().numpy(), rq)
+    Xc, _, _ = ops.w8a8_quantize_rows_bf16(gpu(X))
+    np.testing.assert_array_equal(Xc.float().cpu().numpy(), rq.astype(np.float32))
+
+
 @pytest.mark.parametrize("bias", [False, True])
 def test_w8a8_acc_bit_exact_and_epilogue(ops, bias):
     case, t, Wq, sw, Xq, sx = w8_inputs(M=300, d_in=352, d_out=264, bias=bias)
