@@ -115,6 +115,32 @@ def test_full_lora_4096(ops):
     assert_close(dB[orows], sB, "bf16", "dB rows")
 
 
+def test_full_lora_dropout_4096(ops):
+    """The headline layer with input dropout (p = 0.1) at full size, the masked rank-r passes on the
+    16-byte mask rows: rows of Y and dX (rows are independent), columns of dA (G does not depend
+    on X, so the oracle on those columns of X, the mask, W0 and A gives them) and rows of dB (the
+    oracle on those columns of dY and rows of W0 and B)."""
+    case = D.WORKLOADS["lora_4096_bf16"]
+    t = D.make_linear(case)
+    g = {k: gpu(v) for k, v in t.items()}
+    mk = D.make_dropout_mask(case.M, case.d_in, 0.1)
+    keep = 1.0 / 0.9
+    Y, Z = ops.lora_linear_dropout_fwd(g["X"], gpu(mk), keep, g["W0"], g["A"], g["B"], case.s)
+    dX, dA, dB, _ = ops.lora_linear_dropout_bwd(g["X"], gpu(mk), keep, g["W0"], g["A"], g["B"], Z, g["dY"], case.s)
+    torch.cuda.synchronize()
+    ws_clear(ops)
+    X, W0, A, B, dY = (f64(t[k]) for k in ("X", "W0", "A", "B", "dY"))
+    m = mk.numpy()
+    assert_close(Y[ROWS], O.lora_dropout_fwd(X[ROWS], m[ROWS], keep, W0, A, B, case.s), "bf16", "Y rows")
+    rX = O.lora_dropout_bwd(X[ROWS], m[ROWS], keep, W0, A, B, case.s, dY[ROWS])[0]
+    assert_close(dX[ROWS], rX, "bf16", "dX rows")
+    cols, orows = [0, 63, 64, 2047, 4095], [0, 255, 256, 3000, 4095]
+    rA = O.lora_dropout_bwd(X[:, cols], m[:, cols], keep, W0[:, cols], A[:, cols], B, case.s, dY)[1]
+    assert_close(dA[:, cols].T, rA.T, "bf16", "dA columns")
+    rB = O.lora_dropout_bwd(X, m, keep, W0[orows], A, B[orows], case.s, dY[:, orows])[2]
+    assert_close(dB[orows], rB, "bf16", "dB rows")
+
+
 def test_full_dora_4096x11008(ops):
     case = D.WORKLOADS["dora_4096x11008_bf16"]
     t = D.make_linear(case)
