@@ -72,18 +72,18 @@ lora_status check_shape(const lora_shape* sh) {
   return LORA_OK;
 }
 
-// LORA_GB300_FUSED_Z=1 makes the bf16 LoRA forward form Z inside the GEMM (ranks 8 .. 32; the one-CTA
-// kernel with four down-projection warps).  Measured on the 8192 x 4096 x 4096 forward it takes
-// 0.396 ms against 0.184 ms for the separate pass plus the CTA-pair GEMM: the warps that read every
-// staged X tile a second time and hold its stage until they are done halve the tensor pipe's rate.
-// So the separate pass stays the default.
-// The DoRA-rows dX product scales each staged dY tile by c inside the GEMM instead of reading the
-// slab copy of dY o c (same bits; slower).
+// LORA_GB300_DORA_KSCALE=1 makes the DoRA-rows dX product scale each staged dY tile by c inside the
+// GEMM instead of reading the slab copy of dY o c (same bits; 1.46 against 1.22 ms per DoRA step).
 bool kscale_dx() {
   const char* e = getenv("LORA_GB300_DORA_KSCALE");
   return e && atoi(e) == 1;
 }
 
+// LORA_GB300_FUSED_Z=1 makes the bf16 LoRA forward form Z inside the GEMM (ranks 8 .. 32; the one-CTA
+// kernel with four down-projection warps).  Measured on the 8192 x 4096 x 4096 forward it takes
+// 0.396 ms against 0.184 ms for the separate pass plus the CTA-pair GEMM: the warps that read every
+// staged X tile a second time and hold its stage until they are done halve the tensor pipe's rate.
+// So the separate pass stays the default.
 bool fused_down_projection(int r) {
   if (r < 8 || r > 32 || r % 8) return false;
   const char* e = getenv("LORA_GB300_FUSED_Z");
@@ -169,10 +169,10 @@ size_t plan_dora_fwd(const lora_shape& sh, char* base, DoraFwdWs* w) {
 }
 
 // Row slabs of the DoRA-rows backward (bf16): the column pass writes dY o c for one slab of rows
-// into a buffer of at most kDoraSlabBytes and the dX GEMM of that slab reads it back at once,
-// mostly from L2, before the next slab overwrites it; the buffer's size does not grow with M.  The
-// slab height (a multiple of 128 rows) is the one whose GEMMs finish the whole dX product in the
-// fewest waves of 128 x 256 tiles over the SMs, the tallest among equals.
+// into a buffer of at most kDoraSlabBytes and the dX GEMM of that slab reads it back right away
+// (part of it still in L2), before the next slab overwrites it; the buffer's size does not grow
+// with M.  The slab height (a multiple of 128 rows) is the one whose GEMMs finish the whole dX
+// product in the fewest waves of 128 x 256 tiles over the SMs, the tallest among equals.
 constexpr int64_t kDoraSlabBytes = 64ll << 20;
 struct DoraSlabs {
   int64_t rows = 0, count = 0;
