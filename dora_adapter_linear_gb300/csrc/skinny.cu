@@ -516,8 +516,8 @@ __global__ void __launch_bounds__(160) colreduce_kernel(const __grid_constant__ 
   }
 }
 
-// CTAs of colreduce_kernel<R, HAS_Y, *> resident per SM, from its shared memory (each CTA also
-// holds 1 KB reserved by the system; 228 KB per SM).
+// CTAs of colreduce_kernel<R, HAS_Y, *, MASK> resident per SM, from its shared memory (each CTA
+// also holds 1 KB reserved by the system; 228 KB per SM).
 static int colreduce_ctas_per_sm(int R, bool has_y, bool mask) {
   int smem;
   if (R <= 8) smem = mask ? cr::Cfg<8, false, true>::SMEM : has_y ? cr::Cfg<8, true>::SMEM : cr::Cfg<8, false>::SMEM;
