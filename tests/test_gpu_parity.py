@@ -259,6 +259,27 @@ def test_dora_strength0_is_frozen_base_bits(ops):
     assert torch.equal(Yd, Yl)
 
 
+def test_dora_m_zero_and_strength0_backward(ops):
+    """No tokens: empty outputs and zero gradients.  Strength 0: the frozen base's backward, dX the
+    bits of the plain layer's s = 0 dX, dbias the column sums of dY, no adapter or magnitude
+    gradient."""
+    case, t, g = lin_inputs("dora_4096x11008_bf16", M=200, d_in=136, d_out=264, r=16)
+    r0 = ops.dora_rownorm2(g["W0"])
+    e = g["X"][:0]
+    Y, Z, n, V = ops.dora_linear_fwd(e, g["W0"], g["A"], g["B"], g["m"], r0, case.s, case.eps, g["bias"])
+    assert Y.shape == (0, 264)
+    dX, dA, dB, dm, dbias = ops.dora_linear_bwd(e, g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V,
+                                                g["dY"][:0], case.s, case.eps, need_dbias=True)
+    assert dX.shape == (0, 136)
+    assert not dA.any() and not dB.any() and not dm.any() and not dbias.any()
+    Y, Z, n, V = ops.dora_linear_fwd(g["X"], g["W0"], g["A"], g["B"], g["m"], r0, 0.0, case.eps, g["bias"])
+    dX, dA, dB, dm, dbias = ops.dora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], g["m"], g["bias"], Y, Z, n, V,
+                                                g["dY"], 0.0, case.eps, need_dbias=True)
+    assert torch.equal(dX, ops.lora_linear_bwd(g["X"], g["W0"], g["A"], g["B"], None, g["dY"], 0.0)[0])
+    assert not dA.any() and not dB.any() and not dm.any()
+    assert_close(dbias, f64(t["dY"]).sum(axis=0)[None, :], "bf16", "dbias")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_dora_eps_floor_rows(ops, dtype):
     """eps above some rows' adapted norm: those rows take the floor n = eps and pass no gradient
