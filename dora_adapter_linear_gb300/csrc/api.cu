@@ -283,6 +283,8 @@ size_t plan_dora_cols_fwd(const lora_shape& sh, char* base, DoraColsFwdWs* w) {
 struct DoraColsBwdWs {
   uint32_t* err;
   float *c, *g, *dot, *dotp, *Kb, *Kga, *Vg, *PA, *PB, *csump, *Gw;
+  float* Gp;       // row partials of the one pass over dY (rowcol)
+  RowColPlan rc;   // pm 0: two passes over dY
   bf16 *Ac, *Ag, *Gs, *Zrec, *dXt;
   int splitsA, splitsB;
 };
@@ -291,7 +293,9 @@ size_t plan_dora_cols_bwd(const lora_shape& sh, char* base, DoraColsBwdWs* w) {
   const int64_t out = sh.d_out, in = sh.d_in, r = sh.r, M = sh.M;
   w->err = c.take<uint32_t>(kErrBytes / 4);
   w->splitsA = colreduce_splits(M, in, (int)r, true);   // with dX as the second input
-  w->splitsB = colreduce_splits(M, out, (int)r);
+  w->rc = dy_plan(M, out, r);
+  w->splitsB = w->rc.pm > 0 ? w->rc.pm : colreduce_splits(M, out, (int)r);
+  w->Gp = w->rc.pm > 0 ? c.take<float>((size_t)w->rc.pn * M * r) : nullptr;
   w->c = c.take<float>(in);
   w->g = c.take<float>(in);
   w->dot = c.take<float>(in);
@@ -1441,17 +1445,9 @@ lora_status dora_cols_bwd(const lora_shape* sh, const void* X, const void* W0, c
     CK(rowproj(d, st));
     Z = w.Zrec;
   }
-  {  // dY^T Z partials and colsum(dY), one pass over dY
-    ColReduceDesc d = cr_desc(M, out, r, dY, Z, r, w.PB, w.splitsB, w.err);
-    d.colsum = dbias ? w.csump : nullptr;
-    CK(colreduce(d, st));
-  }
-  {  // G = s dY B
-    RowProjDesc d = rp_desc(M, out, r, dY, B, true, w.err);
-    d.out_b = w.Gs;
-    d.scale_b = s;
-    CK(rowproj(d, st));
-  }
+  // s G = s dY B, the dB partials dY^T Z and the column sums of dY: one rowcol pass over dY
+  CK(dy_side(w.rc, M, out, r, dY, out, B, Z, r, w.PB, w.splitsB, w.Gp, s, w.Gs, r, w.err, st,
+             dbias ? w.csump : nullptr));
   // dX = (dY W0 + G A) diag(c): the column scale is the GEMM epilogue's
   bf16* dXo = dX ? static_cast<bf16*>(dX) : w.dXt;
   {
